@@ -1,0 +1,511 @@
+// api.cu -- the C ABI of libsmoe.so (declared in include/smoe.h): argument
+// validation, workspace layout and the launch sequence of one MoE layer.
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/smoe.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace smoe {
+
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices] = {0};
+int g_major[kMaxDevices] = {0};
+int g_minor[kMaxDevices] = {0};
+int *g_status_ptr[kMaxDevices] = {nullptr};
+
+int cur_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return 0;
+    return dev;
+}
+
+void ensure_device_info()
+{
+    const int dev = cur_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[dev] == 0) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
+            g_sms[dev] = prop.multiProcessorCount;
+            g_major[dev] = prop.major;
+            g_minor[dev] = prop.minor;
+        } else {
+            g_sms[dev] = 1;
+        }
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess)
+            g_status_ptr[dev] = static_cast<int *>(p);
+    }
+}
+
+}  // namespace
+
+int device_sm_count()
+{
+    ensure_device_info();
+    return g_sms[cur_device()];
+}
+
+int device_cc_major()
+{
+    ensure_device_info();
+    return g_major[cur_device()];
+}
+
+static int device_cc_minor()
+{
+    ensure_device_info();
+    return g_minor[cur_device()];
+}
+
+int *device_status_word()
+{
+    ensure_device_info();
+    return g_status_ptr[cur_device()];
+}
+
+}  // namespace smoe
+
+using namespace smoe;
+
+namespace {
+
+inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool device_supported()
+{
+    // The library is compiled for sm_103a only.
+    return device_cc_major() == 10 && device_cc_minor() == 3;
+}
+
+smoe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE_ERR_CUDA; }
+
+int64_t expert_bytes(int d, int f, int bits)
+{
+    return 3ll * d * f / 1024 * tile_bytes(bits);
+}
+
+int64_t gateup_bytes(int d, int f, int bits) { return 2ll * d * f / 1024 * tile_bytes(bits); }
+
+bool valid_layer(const smoe_layer_desc *L)
+{
+    if (!L)
+        return false;
+    if (L->bits != 2 && L->bits != 4)
+        return false;
+    if (L->group_size != SMOE_GROUP_SIZE)
+        return false;
+    if (L->d_model <= 0 || L->d_model % 128 || L->d_model > 8192)
+        return false;
+    if (L->ffn_dim <= 0 || L->ffn_dim % 64 || L->ffn_dim > 4096)
+        return false;
+    if (L->num_experts < 1 || L->num_experts > kMaxExperts)
+        return false;
+    if (L->top_k < 1 || L->top_k > SMOE_MAX_TOP_K || L->top_k > L->num_experts)
+        return false;
+    if (!L->router_w || !L->expert_tiles || !aligned(L->expert_tiles, 16) ||
+        !aligned(L->router_w, 16))
+        return false;
+    if (L->shared_ffn_dim < 0 || L->shared_ffn_dim % 64 || L->shared_ffn_dim > 4096)
+        return false;
+    if ((L->shared_ffn_dim > 0) != (L->shared_tiles != nullptr))
+        return false;
+    if (L->shared_tiles && !aligned(L->shared_tiles, 16))
+        return false;
+    if (L->shared_gate_w && (!L->shared_tiles || !aligned(L->shared_gate_w, 4)))
+        return false;
+    return true;
+}
+
+struct Plan {
+    int64_t T;
+    int ntiles, ksplit, Epad, max_pairs, fmax, warps;
+    size_t off_ctr_tile, off_ctr_done, off_ctr_blk0, off_ctr_blk1, off_ctr_comb, off_meta,
+        off_plog, off_xsum, off_ids, off_w, off_sw, off_pairs, off_rmap, off_h, off_hsum, off_o,
+        off_part, total;
+};
+
+Plan make_plan(const smoe_layer_desc *L, int64_t T)
+{
+    Plan p;
+    p.T = T;
+    const int d = L->d_model, E = L->num_experts, k = L->top_k;
+    p.ntiles = static_cast<int>((T + kPairCols - 1) / kPairCols);
+    const int G = d / 64;
+    const int target = 2 * device_sm_count();
+    int ks = 1;
+    while (ks * 2 <= G && G % (ks * 2) == 0 && (int64_t)p.ntiles * ks * 2 <= target)
+        ks *= 2;
+    p.ksplit = ks;
+    const int Erows = E + (L->shared_gate_w ? 1 : 0);
+    p.Epad = (Erows + 15) / 16 * 16;
+    const int64_t tk = T * k;
+    const int64_t active = tk < E ? tk : E;
+    int64_t mp = (tk + 7 * active + kPairCols - 1) / kPairCols;
+    if (L->shared_ffn_dim > 0)
+        mp += p.ntiles;
+    if (mp < 1)
+        mp = 1;
+    p.max_pairs = static_cast<int>(mp);
+    p.fmax = L->ffn_dim > L->shared_ffn_dim ? L->ffn_dim : L->shared_ffn_dim;
+    p.warps = expert_grid_warps();
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    p.off_ctr_tile = take(sizeof(unsigned) * p.ntiles);
+    p.off_ctr_done = take(sizeof(unsigned));
+    p.off_ctr_blk0 = take(sizeof(unsigned) * p.max_pairs * kMaxBlocksPerPair);
+    p.off_ctr_blk1 = take(sizeof(unsigned) * p.max_pairs * kMaxBlocksPerPair);
+    p.off_ctr_comb = take(sizeof(unsigned) * kMaxBlocksPerPair);
+    p.off_meta = take(sizeof(int32_t) * 2);
+    p.off_plog = take(sizeof(float) * p.ksplit * T * p.Epad);
+    p.off_xsum = take(sizeof(float) * T * G * 2);
+    p.off_ids = take(sizeof(int32_t) * tk);
+    p.off_w = take(sizeof(float) * tk);
+    p.off_sw = take(sizeof(float) * T);
+    p.off_pairs = take(sizeof(int32_t) * kPairInts * p.max_pairs);
+    p.off_rmap = take(sizeof(int32_t) * T * (k + 1));
+    p.off_h = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * p.fmax);
+    p.off_hsum = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 64) * 2);
+    p.off_o = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
+    p.off_part = take(sizeof(float) * (size_t)p.warps * 2 * 32 * 32);
+    p.total = o;
+    return p;
+}
+
+template <typename T_>
+T_ *at(void *base, size_t off)
+{
+    return reinterpret_cast<T_ *>(static_cast<uint8_t *>(base) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *smoe_status_string(smoe_status s)
+{
+    switch (s) {
+    case SMOE_OK:
+        return "ok";
+    case SMOE_ERR_INVALID_ARG:
+        return "invalid argument";
+    case SMOE_ERR_UNSUPPORTED:
+        return "unsupported (device or configuration)";
+    case SMOE_ERR_WORKSPACE:
+        return "workspace or output buffer too small";
+    case SMOE_ERR_CUDA:
+        return "CUDA error";
+    case SMOE_ERR_DEVICE_FAULT:
+        return "device-side fault recorded";
+    case SMOE_ERR_TIMEOUT:
+        return "device-side bounded wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t smoe_stream_bytes(int64_t rows, int64_t cols, int bits)
+{
+    if (rows < 0 || cols < 0 || (bits != 2 && bits != 4))
+        return 0;
+    return static_cast<size_t>((rows * cols * bits + 7) / 8);
+}
+
+size_t smoe_scales_bytes(int64_t rows, int64_t cols, int group_size)
+{
+    if (rows < 0 || cols < 0 || group_size <= 0)
+        return 0;
+    return static_cast<size_t>((rows * cols + group_size - 1) / group_size) * 2;
+}
+
+size_t smoe_expert_tiles_bytes(int32_t d_model, int32_t ffn_dim, int bits, int group_size)
+{
+    if ((bits != 2 && bits != 4) || group_size != SMOE_GROUP_SIZE || d_model <= 0 ||
+        d_model % 128 || ffn_dim <= 0 || ffn_dim % 64)
+        return 0;
+    return static_cast<size_t>(expert_bytes(d_model, ffn_dim, bits));
+}
+
+size_t smoe_repacked_bytes(int32_t d_model, int32_t ffn_dim, int32_t n_experts, int bits,
+                           int group_size)
+{
+    if (n_experts < 0)
+        return 0;
+    return smoe_expert_tiles_bytes(d_model, ffn_dim, bits, group_size) * (size_t)n_experts;
+}
+
+smoe_status smoe_quantize(const void *w_bf16, int64_t rows, int64_t cols, int bits, int group_size,
+                          uint8_t *codes_lsb, uint16_t *scales_f16, void *cuda_stream)
+{
+    if ((bits != 2 && bits != 4) || group_size != SMOE_GROUP_SIZE || rows < 0 || cols <= 0 ||
+        cols % SMOE_GROUP_SIZE)
+        return SMOE_ERR_INVALID_ARG;
+    if (rows == 0)
+        return SMOE_OK;
+    if (!w_bf16 || !codes_lsb || !scales_f16 || !aligned(w_bf16, 4) || !aligned(scales_f16, 2))
+        return SMOE_ERR_INVALID_ARG;
+    if (!device_supported())
+        return SMOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_quantize(static_cast<const uint16_t *>(w_bf16), rows, cols, bits,
+                                       codes_lsb, scales_f16,
+                                       static_cast<cudaStream_t>(cuda_stream)));
+}
+
+static smoe_status check_repack_args(int32_t d, int32_t f, int32_t n, int bits, int group_size)
+{
+    if ((bits != 2 && bits != 4) || group_size != SMOE_GROUP_SIZE || d <= 0 || d % 128 ||
+        f <= 0 || f % 64 || n < 0)
+        return SMOE_ERR_INVALID_ARG;
+    return SMOE_OK;
+}
+
+smoe_status smoe_repack(const uint8_t *const *codes_lsb, const uint16_t *const *scales_f16,
+                        int32_t d_model, int32_t ffn_dim, int32_t n_experts, int bits,
+                        int group_size, void *tiles_out, size_t tiles_bytes, void *cuda_stream)
+{
+    smoe_status st = check_repack_args(d_model, ffn_dim, n_experts, bits, group_size);
+    if (st)
+        return st;
+    if (n_experts == 0)
+        return SMOE_OK;
+    if (!codes_lsb || !scales_f16 || !tiles_out || !aligned(tiles_out, 16))
+        return SMOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 3 * n_experts; ++i) {
+        const int64_t cols = (i % 3 == 2) ? ffn_dim : d_model;
+        if (!codes_lsb[i] || !scales_f16[i] || !aligned(scales_f16[i], 2) ||
+            !aligned(codes_lsb[i], bits == 4 ? 8 : 4) || cols % 64)
+            return SMOE_ERR_INVALID_ARG;
+    }
+    if (tiles_bytes < smoe_repacked_bytes(d_model, ffn_dim, n_experts, bits, group_size))
+        return SMOE_ERR_WORKSPACE;
+    if (!device_supported())
+        return SMOE_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int64_t eb = expert_bytes(d_model, ffn_dim, bits), gu = gateup_bytes(d_model, ffn_dim, bits);
+    for (int e = 0; e < n_experts; ++e) {
+        uint8_t *base = static_cast<uint8_t *>(tiles_out) + e * eb;
+        for (int kind = 0; kind < 3; ++kind) {
+            const int R = kind < 2 ? ffn_dim : d_model, K = kind < 2 ? d_model : ffn_dim;
+            cudaError_t ce = launch_repack(codes_lsb[3 * e + kind], scales_f16[3 * e + kind], kind,
+                                           R, K, bits, base, gu, s);
+            if (ce != cudaSuccess)
+                return SMOE_ERR_CUDA;
+        }
+    }
+    return SMOE_OK;
+}
+
+smoe_status smoe_unpack(const void *tiles, int32_t d_model, int32_t ffn_dim, int32_t n_experts,
+                        int bits, int group_size, uint8_t *const *codes_lsb,
+                        uint16_t *const *scales_f16, void *cuda_stream)
+{
+    smoe_status st = check_repack_args(d_model, ffn_dim, n_experts, bits, group_size);
+    if (st)
+        return st;
+    if (n_experts == 0)
+        return SMOE_OK;
+    if (!codes_lsb || !scales_f16 || !tiles || !aligned(tiles, 16))
+        return SMOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 3 * n_experts; ++i)
+        if (!codes_lsb[i] || !scales_f16[i] || !aligned(scales_f16[i], 2) ||
+            !aligned(codes_lsb[i], bits == 4 ? 8 : 4))
+            return SMOE_ERR_INVALID_ARG;
+    if (!device_supported())
+        return SMOE_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int64_t eb = expert_bytes(d_model, ffn_dim, bits), gu = gateup_bytes(d_model, ffn_dim, bits);
+    for (int e = 0; e < n_experts; ++e) {
+        const uint8_t *base = static_cast<const uint8_t *>(tiles) + e * eb;
+        for (int kind = 0; kind < 3; ++kind) {
+            const int R = kind < 2 ? ffn_dim : d_model, K = kind < 2 ? d_model : ffn_dim;
+            cudaError_t ce = launch_unpack(base, kind, R, K, bits, gu, codes_lsb[3 * e + kind],
+                                           scales_f16[3 * e + kind], s);
+            if (ce != cudaSuccess)
+                return SMOE_ERR_CUDA;
+        }
+    }
+    return SMOE_OK;
+}
+
+smoe_status smoe_route_from_logits(const float *logits, int64_t T, int32_t E, int32_t k,
+                                   int norm_topk_prob, const float *expert_bias, int32_t *ids,
+                                   float *weights, void *cuda_stream)
+{
+    if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > SMOE_MAX_TOP_K || k > E)
+        return SMOE_ERR_INVALID_ARG;
+    if (T == 0)
+        return SMOE_OK;
+    if (!logits || !ids || !weights)
+        return SMOE_ERR_INVALID_ARG;
+    if (!device_supported())
+        return SMOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_route_logits(logits, T, E, k, norm_topk_prob ? 1 : 0, expert_bias,
+                                           ids, weights, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+size_t smoe_moe_workspace_bytes(const smoe_layer_desc *layer, int64_t num_tokens)
+{
+    if (!valid_layer(layer) || num_tokens < 0)
+        return 0;
+    return make_plan(layer, num_tokens).total;
+}
+
+smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, void *cuda_stream)
+{
+    if (!workspace && workspace_bytes)
+        return SMOE_ERR_INVALID_ARG;
+    if (!workspace_bytes)
+        return SMOE_OK;
+    return cuda_status(cudaMemsetAsync(workspace, 0, workspace_bytes,
+                                       static_cast<cudaStream_t>(cuda_stream)));
+}
+
+static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
+                                  int64_t num_tokens, float *y, void *workspace,
+                                  size_t workspace_bytes, int32_t *ids_out, float *w_out,
+                                  int stage_mask, void *cuda_stream)
+{
+    if (!valid_layer(layer) || num_tokens < 0 || (x_dtype != SMOE_F32 && x_dtype != SMOE_BF16))
+        return SMOE_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return SMOE_OK;
+    if (!x || !y || !workspace || !aligned(x, 16) || !aligned(y, 16) || !aligned(workspace, 256))
+        return SMOE_ERR_INVALID_ARG;
+    if (!device_supported())
+        return SMOE_ERR_UNSUPPORTED;
+    const Plan P = make_plan(layer, num_tokens);
+    if (workspace_bytes < P.total)
+        return SMOE_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const smoe_layer_desc &L = *layer;
+    int *status = device_status_word();
+
+    RouteArgs ra;
+    memset(&ra, 0, sizeof ra);
+    ra.router_w = static_cast<const uint16_t *>(L.router_w);
+    ra.shared_gate = static_cast<const uint16_t *>(L.shared_gate_w);
+    ra.expert_bias = L.expert_bias;
+    ra.x = x;
+    ra.x_bf16 = x_dtype == SMOE_BF16;
+    ra.T = num_tokens;
+    ra.d = L.d_model;
+    ra.E = L.num_experts;
+    ra.k = L.top_k;
+    ra.norm = L.norm_topk_prob ? 1 : 0;
+    ra.bits = L.bits;
+    ra.has_shared = L.shared_ffn_dim > 0;
+    ra.ksplit = P.ksplit;
+    ra.partial = at<float>(workspace, P.off_plog);
+    ra.xsum = at<float>(workspace, P.off_xsum);
+    ra.ids = at<int32_t>(workspace, P.off_ids);
+    ra.weights = at<float>(workspace, P.off_w);
+    ra.shared_w = at<float>(workspace, P.off_sw);
+    ra.ids_out = ids_out;
+    ra.w_out = w_out;
+    ra.pairs = at<int32_t>(workspace, P.off_pairs);
+    ra.route_map = at<int32_t>(workspace, P.off_rmap);
+    ra.meta = at<int32_t>(workspace, P.off_meta);
+    ra.tile_ctr = at<unsigned>(workspace, P.off_ctr_tile);
+    ra.done_ctr = at<unsigned>(workspace, P.off_ctr_done);
+    ra.status = status;
+    ra.max_pairs = P.max_pairs;
+
+    ExpertArgs ea;
+    memset(&ea, 0, sizeof ea);
+    ea.tiles_routed = static_cast<const uint8_t *>(L.expert_tiles);
+    ea.tiles_shared = static_cast<const uint8_t *>(L.shared_tiles);
+    ea.expert_bytes_routed = expert_bytes(L.d_model, L.ffn_dim, L.bits);
+    ea.down_off_routed = gateup_bytes(L.d_model, L.ffn_dim, L.bits);
+    ea.down_off_shared = L.shared_ffn_dim > 0 ? gateup_bytes(L.d_model, L.shared_ffn_dim, L.bits) : 0;
+    ea.x = x;
+    ea.x_bf16 = x_dtype == SMOE_BF16;
+    ea.d = L.d_model;
+    ea.f = L.ffn_dim;
+    ea.fs = L.shared_ffn_dim;
+    ea.E = L.num_experts;
+    ea.k = L.top_k;
+    ea.bits = L.bits;
+    ea.T = num_tokens;
+    ea.pairs = ra.pairs;
+    ea.meta = ra.meta;
+    ea.xsum = ra.xsum;
+    ea.h = at<float>(workspace, P.off_h);
+    ea.hsum = at<float>(workspace, P.off_hsum);
+    ea.o = at<float>(workspace, P.off_o);
+    ea.partial = at<float>(workspace, P.off_part);
+    ea.comb_ctr = at<unsigned>(workspace, P.off_ctr_comb);
+    ea.route_map = ra.route_map;
+    ea.weights = ra.weights;
+    ea.shared_w = ra.shared_w;
+    ea.y = y;
+    ea.status = status;
+    ea.max_pairs = P.max_pairs;
+    ea.fused_combine = num_tokens <= kFusedCombineMaxT;
+
+    if ((stage_mask & 1) && launch_router(ra, s, true) != cudaSuccess)
+        return SMOE_ERR_CUDA;
+    if (stage_mask & 2) {
+        ea.blk_ctr = at<unsigned>(workspace, P.off_ctr_blk0);
+        if (launch_expert(ea, 0, s, true) != cudaSuccess)
+            return SMOE_ERR_CUDA;
+    }
+    if (stage_mask & 4) {
+        ea.blk_ctr = at<unsigned>(workspace, P.off_ctr_blk1);
+        if (launch_expert(ea, 1, s, true) != cudaSuccess)
+            return SMOE_ERR_CUDA;
+        if (!ea.fused_combine && launch_combine(ea, s, true) != cudaSuccess)
+            return SMOE_ERR_CUDA;
+    }
+    return SMOE_OK;
+}
+
+smoe_status smoe_moe_forward(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
+                             int64_t num_tokens, float *y, void *workspace,
+                             size_t workspace_bytes, int32_t *ids_out, float *w_out,
+                             void *cuda_stream)
+{
+    return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
+                          w_out, 7, cuda_stream);
+}
+
+smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
+                                   smoe_dtype x_dtype, int64_t num_tokens, float *y,
+                                   void *workspace, size_t workspace_bytes, int32_t *ids_out,
+                                   float *w_out, int stage, void *cuda_stream)
+{
+    if (stage < 0 || stage > 2)
+        return SMOE_ERR_INVALID_ARG;
+    return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
+                          w_out, 1 << stage, cuda_stream);
+}
+
+smoe_status smoe_get_device_status(void *cuda_stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+        return SMOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess)
+        return SMOE_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+        return SMOE_ERR_CUDA;
+    if (v == 0)
+        return SMOE_OK;
+    return v == kStatusTimeout ? SMOE_ERR_TIMEOUT : SMOE_ERR_DEVICE_FAULT;
+}
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// internal.h -- launchers and host helpers shared by the libsmoe translation
+// units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace smoe {
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+// Compute capability major of the current device (cached per device).
+int device_cc_major();
+// Pointer to the device status word of the current device.
+int *device_status_word();
+
+void grid_fractions(float out[64]);
+
+cudaError_t launch_quantize(const uint16_t *w, int64_t rows, int64_t cols, int bits,
+                            uint8_t *codes, uint16_t *scales, cudaStream_t stream);
+
+// kind: 0 gate, 1 up, 2 down.  R x K is the matrix shape ([f,d] or [d,f]).
+cudaError_t launch_repack(const uint8_t *codes, const uint16_t *scales, int kind, int R, int K,
+                          int bits, uint8_t *expert_base, int64_t gateup_bytes,
+                          cudaStream_t stream);
+cudaError_t launch_unpack(const uint8_t *expert_base, int kind, int R, int K, int bits,
+                          int64_t gateup_bytes, uint8_t *codes, uint16_t *scales,
+                          cudaStream_t stream);
+
+// ------------------------------------------------------------------ forward
+
+// Pair = one expert applied to up to 8 tokens (the n columns of one mma).
+constexpr int kPairCols = 8;
+constexpr int kPairInts = 16;          // pair record: [expert, ncols, tok0..tok7, pad]
+constexpr int kMaxBlocksPerPair = 64;  // counters per pair: f/64 and d/128 blocks
+constexpr int kMaxExperts = 256;       // router / dispatch shared-memory bound
+#define SMOE_MAX_TOPK_DEV 16
+// Token counts up to this many combine inside the down kernel (last pair to
+// finish a block); larger batches use a separate combine kernel.
+constexpr int kFusedCombineMaxT = 8;
+
+struct RouteArgs {
+    const uint16_t *router_w;   // bf16 [E, d]
+    const uint16_t *shared_gate; // nullable bf16 [d]
+    const float *expert_bias;   // nullable [E]
+    const void *x;              // [T, d]
+    int x_bf16;
+    int64_t T;
+    int d, E, k, norm, bits;
+    int has_shared;             // shared expert present
+    int ksplit;                 // K split of the router GEMV
+    int gateup_tiles_routed, gateup_tiles_shared;  // per pair
+    // workspace
+    float *partial;             // [ksplit][T][Epad]
+    float *xsum;                // [T][d/64][2]
+    int32_t *ids;               // [T][k]
+    float *weights;             // [T][k]
+    float *shared_w;            // [T]
+    int32_t *ids_out;           // nullable
+    float *w_out;               // nullable
+    int32_t *pairs;             // pair table (see router.cu)
+    int32_t *route_map;         // [T][k+1] -> pair*8 + col
+    int32_t *meta;              // [0] pairs_routed, [1] pairs_total
+    unsigned *tile_ctr;         // [ceil(T/8)]
+    unsigned *done_ctr;         // [1]
+    int *status;
+    int max_pairs;
+};
+
+cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
+                                const float *bias, int32_t *ids, float *w, cudaStream_t stream);
+cudaError_t launch_router(const RouteArgs &a, cudaStream_t stream, bool pdl);
+
+struct ExpertArgs {
+    const uint8_t *tiles_routed;   // bank base
+    const uint8_t *tiles_shared;   // nullable
+    int64_t expert_bytes_routed;   // stride between experts
+    int64_t down_off_routed, down_off_shared;  // byte offset of the down tiles
+    const void *x;                 // activations [T, d] (gate/up)
+    int x_bf16;
+    int d, f, fs, E, k, bits;
+    int64_t T;
+    const int32_t *pairs;
+    const int32_t *meta;
+    const float *xsum;             // [T][d/64][2] (gate/up)
+    float *h;                      // [maxpairs][8][fmax]
+    float *hsum;                   // [maxpairs][8][fmax/64][2]
+    float *o;                      // [maxpairs][8][d]
+    float *partial;                // [warps][2][32][32]
+    unsigned *blk_ctr;             // gate/up or down block counters
+    unsigned *comb_ctr;            // [d/128]
+    const int32_t *route_map;      // [T][k+1]
+    const float *weights;          // [T][k]
+    const float *shared_w;         // [T]
+    float *y;                      // [T, d]
+    int *status;
+    int max_pairs;
+    int fused_combine;
+};
+
+cudaError_t launch_expert(const ExpertArgs &a, int phase, cudaStream_t stream, bool pdl);
+cudaError_t launch_combine(const ExpertArgs &a, cudaStream_t stream, bool pdl);
+// Warps of the expert kernels' grid on the current device (workspace sizing).
+int expert_grid_warps();
+
+}  // namespace smoe

@@ -1,0 +1,224 @@
+/*
+ * smoe.h -- C ABI of libsmoe.so: the SMOE group-quantised routed-expert MoE
+ * layer forward on one NVIDIA GB300 (sm_103a).
+ *
+ * The method (page title, section):
+ *   "SMOE Quantisation", Quantisation Levels / L2-MSE Scale Optimiser / Bit
+ *     Packing / Decoding: Metal Kernel -- symmetric group-of-64 quantisation,
+ *     Q4 w = (code - 7.5) / 7.5 * scale, Q2 w = (code - 1.5) / 1.5 * scale,
+ *     codes packed LSB-first, one fp16 scale per group chosen by a 64-point
+ *     MSE grid over linspace(0.1, 1.0, 64) * absmax.
+ *   ".smoe Binary Format", File Header / Expert Blob Architecture -- the
+ *     code stream and scale array of each sub-tensor (gate, up, down), and
+ *     the header fields group_size, bits, d_model, ffn_dim.
+ *   "Model Agnosticism", SmoeModelConfig -- d_model, ffn_dim,
+ *     shared_expert_ffn_dim, max_experts_per_layer (router rows),
+ *     norm_topk_prob, moe_top_k; routing width capped at 16; SiLU only.
+ *   "CMF v2 -- Format Specification", 2.2 MoE -- softmax over all router
+ *     logits, top-k with ties to the lower index, selection-only
+ *     expert_bias, optional renormalisation, y = sum_e w_e FFN_e(x), shared
+ *     expert weighted by sigmoid(shared_expert_gate . x) (else 1).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is DEVICE memory owned by the caller unless the
+ *     comment says "host".  The library allocates no device memory and never
+ *     synchronises the stream, except smoe_get_device_status.
+ *   - `cuda_stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - Arguments are validated synchronously on the host; on any error the
+ *     call returns a negative smoe_status and launches nothing.
+ *   - A launch failure returns SMOE_ERR_CUDA.  Faults detected on the device
+ *     (an out-of-range expert id, a bounded wait that ran out) never trap:
+ *     the kernel records a code in a device status word and skips the work;
+ *     smoe_get_device_status reports and clears it.
+ *   - Weights follow the HF orientation [out, in]: gate and up are
+ *     [ffn_dim, d_model], down is [d_model, ffn_dim], the router is
+ *     [num_experts, d_model]; all row-major.  Groups of 64 run along the
+ *     input dimension (the row), so no group straddles two rows.
+ */
+#ifndef SMOE_H
+#define SMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SMOE_OK = 0,
+    SMOE_ERR_INVALID_ARG = -1,  /* a size, pointer or parameter is invalid   */
+    SMOE_ERR_UNSUPPORTED = -2,  /* valid per the pages, not built (e.g. GPU)  */
+    SMOE_ERR_WORKSPACE = -3,    /* workspace or output buffer too small       */
+    SMOE_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed       */
+    SMOE_ERR_DEVICE_FAULT = -5, /* a kernel recorded a device-side fault      */
+    SMOE_ERR_TIMEOUT = -6       /* a kernel's bounded wait ran out            */
+} smoe_status;
+
+typedef enum { SMOE_F32 = 0, SMOE_BF16 = 1 } smoe_dtype;
+
+/* Largest routing width ("Model Agnosticism", Expanding the Frontier: the
+ * kernels cap routing at 16 experts per token). */
+#define SMOE_MAX_TOP_K 16
+/* The only group size the pages use (".smoe Binary Format", File Header:
+ * group_size is always 64). */
+#define SMOE_GROUP_SIZE 64
+
+/* One MoE layer.  Every pointer is device memory owned by the caller. */
+typedef struct {
+    int32_t d_model;        /* hidden size d; multiple of 128                 */
+    int32_t ffn_dim;        /* routed-expert intermediate size f; mult. of 64 */
+    int32_t num_experts;    /* E = router rows (max_experts_per_layer)        */
+    int32_t top_k;          /* k, 1..16 and <= E                              */
+    int32_t norm_topk_prob; /* nonzero: renormalise the k selected weights    */
+    int32_t bits;           /* 4 (SMOE-Q4) or 2 (SMOE-Q2)                     */
+    int32_t group_size;     /* must be 64                                     */
+    const void *router_w;   /* bf16 [E, d]                                    */
+    const float *expert_bias; /* nullable fp32 [E]: added to the logits for
+                                 top-k selection only, never to the weights */
+    const void *expert_tiles; /* the bank of E experts written by smoe_repack */
+    const void *shared_tiles; /* nullable: the shared expert, written by
+                                 smoe_repack with n_experts = 1 and
+                                 ffn_dim = shared_ffn_dim                     */
+    int32_t shared_ffn_dim;   /* 0 = no shared expert; else multiple of 64    */
+    const void *shared_gate_w; /* nullable bf16 [d]: shared-expert weight is
+                                  sigmoid(shared_gate_w . x), else 1          */
+} smoe_layer_desc;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *smoe_status_string(smoe_status s);
+
+/* ---------------------------------------------------------------- sizes */
+
+/* Code bytes of one rows x cols sub-tensor: ceil(rows*cols*bits/8)
+ * (".smoe Binary Format", Expert Blob Architecture).  0 on bad arguments. */
+size_t smoe_stream_bytes(int64_t rows, int64_t cols, int bits);
+
+/* fp16 scale bytes of one sub-tensor: ceil(rows*cols/group_size)*2.  0 on
+ * bad arguments. */
+size_t smoe_scales_bytes(int64_t rows, int64_t cols, int group_size);
+
+/* Bytes of one expert in the device tile layout (gate+up tiles then down
+ * tiles).  The layout keeps each 16-row x 64-column tile's codes and its 16
+ * fp16 scales together (544 B for Q4, 288 B for Q2), so the per-expert size
+ * equals the code+scale bytes of the pages' blob exactly.  0 on bad args. */
+size_t smoe_expert_tiles_bytes(int32_t d_model, int32_t ffn_dim, int bits, int group_size);
+
+/* Bytes of a bank of n_experts experts = n_experts * smoe_expert_tiles_bytes. */
+size_t smoe_repacked_bytes(int32_t d_model, int32_t ffn_dim, int32_t n_experts, int bits,
+                           int group_size);
+
+/* ----------------------------------------------------------- quantiser */
+
+/* L2-MSE grid-search quantisation of a bf16 [rows, cols] tensor
+ * ("SMOE Quantisation", L2-MSE Scale Optimiser and Bit Packing).
+ * Per group of 64 consecutive elements of the row-major tensor: absmax a;
+ * candidates s_j = fl32(fl32(linspace(0.1,1,64)[j]) * a); codes
+ * clamp(rint(((w / s) * L) + L), 0, 2L) in fp32 (L = 7.5 or 1.5); the
+ * candidate with the least reconstruction MSE wins (the first on exact
+ * ties); an all-zero group gets scale 0 and code round(L).
+ *   w_bf16      device, bf16 [rows, cols], finite values
+ *   cols        multiple of 64
+ *   codes_lsb   device, out: smoe_stream_bytes(rows, cols, bits) bytes,
+ *               LSB-first (Q4: 2 codes/byte, Q2: 4 codes/byte)
+ *   scales_f16  device, out: rows*cols/64 fp16 scales (RNE of the fp32
+ *               winning candidate)
+ * Errors: SMOE_ERR_INVALID_ARG (bits not 2/4, group_size != 64, cols % 64,
+ * rows < 0, null pointer), SMOE_ERR_CUDA. */
+smoe_status smoe_quantize(const void *w_bf16, int64_t rows, int64_t cols, int bits,
+                          int group_size, uint8_t *codes_lsb, uint16_t *scales_f16,
+                          void *cuda_stream);
+
+/* -------------------------------------------------------- repack/unpack */
+
+/* Repack E experts from the pages' LSB-first code streams and fp16 scale
+ * arrays (".smoe Binary Format", Expert Blob Architecture) into the device
+ * tile layout read by smoe_moe_forward.
+ *   codes_lsb   HOST array of 3*n_experts DEVICE pointers, order
+ *               (gate, up, down) per expert; gate/up are [ffn_dim, d_model]
+ *               streams, down is [d_model, ffn_dim]
+ *   scales_f16  HOST array of 3*n_experts DEVICE pointers, same order
+ *   tiles_out   device, smoe_repacked_bytes(...) bytes, 16-byte aligned
+ * The result is a byte permutation: smoe_unpack restores every byte.
+ * Errors: SMOE_ERR_INVALID_ARG (shape not d % 128 == 0 and f % 64 == 0,
+ * bits, group_size, null or misaligned pointer), SMOE_ERR_WORKSPACE
+ * (tiles_bytes too small), SMOE_ERR_CUDA. */
+smoe_status smoe_repack(const uint8_t *const *codes_lsb, const uint16_t *const *scales_f16,
+                        int32_t d_model, int32_t ffn_dim, int32_t n_experts, int bits,
+                        int group_size, void *tiles_out, size_t tiles_bytes, void *cuda_stream);
+
+/* Exact inverse of smoe_repack: writes the LSB-first streams and fp16 scale
+ * arrays back.  Same argument conventions (host arrays of device pointers). */
+smoe_status smoe_unpack(const void *tiles, int32_t d_model, int32_t ffn_dim, int32_t n_experts,
+                        int bits, int group_size, uint8_t *const *codes_lsb,
+                        uint16_t *const *scales_f16, void *cuda_stream);
+
+/* ---------------------------------------------------------------- route */
+
+/* Top-k routing from given fp32 logits ("CMF v2", 2.2 MoE).
+ *   logits       device fp32 [T, E]
+ *   expert_bias  nullable device fp32 [E]; the selection key is
+ *                fl32(logit + bias), the weights never see the bias
+ *   ids          device out int32 [T, k], rank order (largest key first,
+ *                equal keys: lower expert index first)
+ *   weights      device out fp32 [T, k]: softmax over all E logits at the
+ *                selected experts, divided by their sum if norm_topk_prob
+ * Errors: SMOE_ERR_INVALID_ARG (T < 0, E < 1, k < 1, k > 16, k > E, null
+ * pointer), SMOE_ERR_CUDA. */
+smoe_status smoe_route_from_logits(const float *logits, int64_t T, int32_t E, int32_t k,
+                                   int norm_topk_prob, const float *expert_bias, int32_t *ids,
+                                   float *weights, void *cuda_stream);
+
+/* ------------------------------------------------------------- forward */
+
+/* Workspace bytes smoe_moe_forward needs for this layer and token count
+ * (0 on invalid arguments). */
+size_t smoe_moe_workspace_bytes(const smoe_layer_desc *layer, int64_t num_tokens);
+
+/* Zero a workspace.  Required once after allocation, and again after a call
+ * that returned an error; the forward leaves its counters at zero itself. */
+smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/* MoE layer forward for T tokens:
+ *   logits = x Wr^T;  top-k routing (see smoe_route_from_logits);
+ *   per selected expert: h = SiLU(W_gate x) * (W_up x), o = W_down h, with
+ *   W decoded as (code - L) / L * scale in registers (never materialised);
+ *   y = sum_j w_j o_j (rank order, deterministic) + shared expert.
+ *   x           device [T, d_model], fp32 or bf16 (x_dtype)
+ *   y           device out fp32 [T, d_model]
+ *   workspace   device, >= smoe_moe_workspace_bytes, 256-byte aligned,
+ *               zeroed once by smoe_moe_workspace_init
+ *   ids_out     nullable device out int32 [T, k]
+ *   w_out       nullable device out fp32 [T, k]
+ * The whole layer is enqueued on cuda_stream; nothing is synchronised.
+ * Errors: SMOE_ERR_INVALID_ARG (layer fields, T < 0, null pointer),
+ * SMOE_ERR_UNSUPPORTED (device is not a Blackwell sm_10x part),
+ * SMOE_ERR_WORKSPACE, SMOE_ERR_CUDA. */
+smoe_status smoe_moe_forward(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
+                             int64_t num_tokens, float *y, void *workspace,
+                             size_t workspace_bytes, int32_t *ids_out, float *w_out,
+                             void *cuda_stream);
+
+/* The same forward as smoe_moe_forward, one launch stage at a time, so that
+ * a caller can put its own work or timing events between the stages:
+ *   stage 0  router GEMV, softmax, top-k, renormalisation, dispatch
+ *   stage 1  fused dequant gate/up GEMV + SiLU(gate) * up
+ *   stage 2  fused dequant down GEMV + routing-weighted combine into y
+ * Calling stages 0, 1, 2 in order on one stream with the same arguments and
+ * workspace is exactly smoe_moe_forward.  Same arguments and errors, plus
+ * SMOE_ERR_INVALID_ARG for a stage outside 0..2. */
+smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
+                                   smoe_dtype x_dtype, int64_t num_tokens, float *y,
+                                   void *workspace, size_t workspace_bytes, int32_t *ids_out,
+                                   float *w_out, int stage, void *cuda_stream);
+
+/* Synchronise cuda_stream, then read and clear the device status word of the
+ * current device.  Returns SMOE_OK, SMOE_ERR_DEVICE_FAULT, SMOE_ERR_TIMEOUT
+ * or SMOE_ERR_CUDA. */
+smoe_status smoe_get_device_status(void *cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMOE_H */

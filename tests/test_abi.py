@@ -1,0 +1,134 @@
+"""The C-ABI library loads, exports every symbol the headers declare, and its
+host-side validation rejects bad arguments without launching anything (these
+run without a GPU: validation happens before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libs():
+    from bit_expert_weight_gb300 import build
+    paths = build.build()
+    import bit_expert_weight_gb300.smoe as S
+    return S, paths
+
+
+def declared(header):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(smoe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(libs):
+    S, paths = libs
+    for header, lib in (("smoe.h", "libsmoe.so"), ("smoe_synth.h", "libsmoe_synth.so")):
+        names = declared(header)
+        assert names, header
+        so = ctypes.CDLL(paths[lib])
+        for n in names:
+            assert hasattr(so, n), f"{lib} does not export {n}"
+    assert sorted(S.EXPORTED) == declared("smoe.h")
+
+
+def test_size_queries_match_the_pages_blob_layout(libs):
+    S, _ = libs
+    assert S.stream_bytes(4096, 1536, 4) == 3_145_728
+    assert S.stream_bytes(4096, 1536, 2) == 1_572_864
+    assert S.scales_bytes(4096, 1536) == 196_608
+    # one Qwen3-235B-like expert: the tile layout is exactly as large as the blob
+    assert S.expert_tiles_bytes(4096, 1536, 4) == 10_027_008
+    assert S.expert_tiles_bytes(4096, 1536, 2) == 5_308_416
+    assert S.repacked_bytes(2048, 1408, 64, 4) == 64 * 4_595_712
+    assert S.expert_tiles_bytes(4096, 1500, 4) == 0   # f % 64
+    assert S.expert_tiles_bytes(4000, 1536, 4) == 0   # d % 128
+    assert S.expert_tiles_bytes(4096, 1536, 3) == 0   # bits
+    assert S.stream_bytes(4, 64, 8) == 0
+
+
+def test_status_strings(libs):
+    S, _ = libs
+    L = S.load()
+    for code in range(-6, 1):
+        assert L.smoe_status_string(code)
+
+
+def _desc(S, **kw):
+    base = dict(d_model=256, ffn_dim=128, num_experts=8, top_k=2, norm_topk_prob=1, bits=4,
+                group_size=64, router_w=256, expert_bias=None, expert_tiles=512,
+                shared_tiles=None, shared_ffn_dim=0, shared_gate_w=None)
+    base.update(kw)
+    return S.LayerDesc(**base)
+
+
+BAD = [
+    dict(bits=3), dict(bits=8), dict(group_size=32), dict(group_size=128),
+    dict(top_k=0), dict(top_k=17), dict(top_k=9), dict(num_experts=0), dict(num_experts=300),
+    dict(d_model=192), dict(ffn_dim=100), dict(d_model=0), dict(router_w=None),
+    dict(expert_tiles=None), dict(expert_tiles=520), dict(shared_ffn_dim=64),
+    dict(shared_tiles=1024), dict(shared_ffn_dim=-64, shared_tiles=1024),
+]
+
+
+@pytest.mark.parametrize("kw", BAD, ids=[",".join(f"{k}={v}" for k, v in b.items()) for b in BAD])
+def test_forward_rejects_bad_layer(libs, kw):
+    S, _ = libs
+    L = S.load()
+    desc = _desc(S, **kw)
+    rc = L.smoe_moe_forward(ctypes.byref(desc), ctypes.c_void_p(4096), 0, 4,
+                            ctypes.c_void_p(8192), ctypes.c_void_p(1 << 20), 1 << 30, None, None,
+                            None)
+    assert rc == -1
+    assert L.smoe_moe_workspace_bytes(ctypes.byref(desc), 4) == 0
+
+
+def test_forward_rejects_bad_call_args(libs):
+    S, _ = libs
+    L = S.load()
+    desc = _desc(S)
+    P = ctypes.c_void_p
+    # negative T, bad dtype, null x / y / workspace, misaligned workspace
+    assert L.smoe_moe_forward(ctypes.byref(desc), P(4096), 0, -1, P(8192), P(1 << 20), 1 << 30,
+                              None, None, None) == -1
+    assert L.smoe_moe_forward(ctypes.byref(desc), P(4096), 7, 4, P(8192), P(1 << 20), 1 << 30,
+                              None, None, None) == -1
+    assert L.smoe_moe_forward(ctypes.byref(desc), None, 0, 4, P(8192), P(1 << 20), 1 << 30,
+                              None, None, None) == -1
+    assert L.smoe_moe_forward(ctypes.byref(desc), P(4096), 0, 4, None, P(1 << 20), 1 << 30,
+                              None, None, None) == -1
+    assert L.smoe_moe_forward(ctypes.byref(desc), P(4096), 0, 4, P(8192), None, 1 << 30,
+                              None, None, None) == -1
+    assert L.smoe_moe_forward(ctypes.byref(desc), P(4096), 0, 4, P(8192), P((1 << 20) + 16),
+                              1 << 30, None, None, None) == -1
+    assert L.smoe_moe_forward(None, P(4096), 0, 4, P(8192), P(1 << 20), 1 << 30,
+                              None, None, None) == -1
+    # zero tokens is a no-op
+    assert L.smoe_moe_forward(ctypes.byref(desc), None, 0, 0, None, None, 0, None, None,
+                              None) == 0
+
+
+def test_other_entry_points_reject_bad_args(libs):
+    S, _ = libs
+    L = S.load()
+    P = ctypes.c_void_p
+    assert L.smoe_quantize(P(4096), 4, 96, 4, 64, P(8192), P(16384), None) == -1   # cols % 64
+    assert L.smoe_quantize(P(4096), 4, 64, 3, 64, P(8192), P(16384), None) == -1   # bits
+    assert L.smoe_quantize(P(4096), 4, 64, 4, 32, P(8192), P(16384), None) == -1   # group
+    assert L.smoe_quantize(None, 4, 64, 4, 64, P(8192), P(16384), None) == -1
+    assert L.smoe_quantize(P(4096), -1, 64, 4, 64, P(8192), P(16384), None) == -1
+    assert L.smoe_quantize(P(4096), 0, 64, 4, 64, None, None, None) == 0          # empty
+    for k, E in ((0, 8), (17, 32), (9, 8)):
+        assert L.smoe_route_from_logits(P(4096), 4, E, k, 1, None, P(8192), P(16384),
+                                        None) == -1
+    assert L.smoe_route_from_logits(None, 4, 8, 2, 1, None, P(8192), P(16384), None) == -1
+    assert L.smoe_route_from_logits(P(4096), 0, 8, 2, 1, None, None, None, None) == 0
+    arr = (P * 3)(4096, 4096, 4096)
+    assert L.smoe_repack(arr, arr, 192, 128, 1, 4, 64, P(4096), 1 << 20, None) == -1
+    assert L.smoe_repack(arr, arr, 256, 100, 1, 4, 64, P(4096), 1 << 20, None) == -1
+    assert L.smoe_repack(arr, arr, 256, 128, 1, 4, 64, P(4096), 16, None) == -3   # too small
+    assert L.smoe_repack(arr, arr, 256, 128, 1, 4, 64, P(4100), 1 << 20, None) == -1  # align
+    assert L.smoe_unpack(P(4096), 256, 128, 1, 5, 64, arr, arr, None) == -1
