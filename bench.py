@@ -71,7 +71,7 @@ def peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("expert.cu", "common.cuh"):
+    for f in ("layer.cu", "common.cuh"):
         with open(os.path.join(ROOT, "bit_expert_weight_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -208,31 +208,14 @@ class DeviceModel:
         for lay, x, y, ids in zip(self.layers, self.x, self.y, self.ids):
             S.forward(lay, x, self.ws, y=y, ids=ids)
 
-    def step_timed_gateup(self, evs):
-        """The same step, stage by stage, with events around every gate/up launch."""
+    def step_timed(self, evs):
+        """The same step with events around every layer's launch(es): for
+        T <= 8 a layer is one fused kernel (router, experts, combine)."""
         import bit_expert_weight_gb300.smoe as S
         for i, (lay, x, y, ids) in enumerate(zip(self.layers, self.x, self.y, self.ids)):
-            S.forward_stage(lay, 0, x, self.ws, y, ids=ids)
             evs[i][0].record()
-            S.forward_stage(lay, 1, x, self.ws, y)
+            S.forward(lay, x, self.ws, y=y, ids=ids)
             evs[i][1].record()
-            S.forward_stage(lay, 2, x, self.ws, y)
-
-
-def gateup_algorithmic_bytes(model):
-    """Bytes the gate/up stage must read per launch, averaged over layers:
-    gate+up codes and scales of the distinct experts the tokens selected
-    (plus the shared expert), plus the activations."""
-    wl, bits = model.wl, model.bits
-    per_expert = 2 * (wl.f * wl.d * bits // 8 + wl.f * wl.d // 64 * 2)
-    tot = 0
-    for ids in model.ids:
-        distinct = len(np.unique(ids.cpu().numpy()))
-        b = distinct * per_expert + model.T * wl.d * model.x[0].element_size()
-        if wl.shared_f:
-            b += 2 * (wl.shared_f * wl.d * bits // 8 + wl.shared_f * wl.d // 64 * 2)
-        tot += b
-    return tot / len(model.ids)
 
 
 def layer_algorithmic_bytes(model):
@@ -302,7 +285,7 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
     ms_per_step = ms / args.steps
     tok_s = world * T * args.steps / (ms / 1e3)
 
-    # dominant kernel (fused dequant gate/up + SiLU): events around each launch
+    # dominant kernel (the fused layer kernel): events around each launch
     reps = max(3, min(50, args.steps))
     evs = [(torch.cuda.Event(enable_timing=True, external=True),
             torch.cuda.Event(enable_timing=True, external=True)) for _ in model.layers]
@@ -310,18 +293,17 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
     if use_graph:
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=stream):
-            model.step_timed_gateup(evs)
+            model.step_timed(evs)
     durs = []
     with torch.cuda.stream(stream):
         for _ in range(reps):
             if g2 is not None:
                 g2.replay()
             else:
-                model.step_timed_gateup(evs)
+                model.step_timed(evs)
             stream.synchronize()
             durs.extend(a.elapsed_time(b) for a, b in evs)
-    gu_ms = float(np.mean(durs))
-    gu_bytes = gateup_algorithmic_bytes(model)
+    kern_ms = float(np.mean(durs))
     layer_bytes = layer_algorithmic_bytes(model)
 
     # end to end: pinned host x -> device, forward, device y -> host, per step
@@ -369,12 +351,12 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
         "layer_us": ms_per_step * 1e3 / n_layers,
         "layer_alg_bytes": layer_bytes,
         "layer_alg_GBps": layer_bytes / (ms_per_step * 1e-3 / n_layers) / 1e9,
-        "gateup_alg_bytes": gu_bytes, "gateup_us": gu_ms * 1e3,
-        "gateup_alg_GBps": gu_bytes / (gu_ms * 1e-3) / 1e9,
+        "kernel_us": kern_ms * 1e3,
+        "kernel_alg_GBps": layer_bytes / (kern_ms * 1e-3) / 1e9,
         "e2e_tokens_per_s": world * T * args.steps / (e2e_ms / 1e3),
         "h2d": h2d, "d2h": d2h, "clocks": clocks, "setup_s": model.setup_s,
         "resident_GB": model.resident_bytes / 1e9, "device_status": status,
-        "launches_per_step": 3 * n_layers if T <= 8 else 4 * n_layers,
+        "launches_per_step": n_layers if T <= 8 else 3 * n_layers,
     }
     del model, graph, g2, g3
     torch.cuda.empty_cache()
@@ -510,11 +492,12 @@ def main():
                    "l2": "inputs larger than L2 (per-step weight footprint "
                          f"{r['layer_alg_bytes'] * n_layers / 1e6:.0f} MB > 129 MB); no flush",
                    "graph": not args.no_graph, "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": r["gateup_alg_GBps"], "peak": hbm,
-                     "unit": "GB/s", "frac": r["gateup_alg_GBps"] / hbm, "traffic": traffic,
-                     "kernel": "expert gate/up (fused dequant GEMV + SiLU)",
-                     "bytes_per_launch": r["gateup_alg_bytes"],
-                     "launch_us": r["gateup_us"], "peak_kind": peak_kind},
+        "roofline": {"bound": "hbm", "achieved": r["kernel_alg_GBps"], "peak": hbm,
+                     "unit": "GB/s", "frac": r["kernel_alg_GBps"] / hbm, "traffic": traffic,
+                     "kernel": "moe_layer_kernel (router, top-k, dispatch, fused dequant "
+                               "gate/up + SiLU, fused dequant down, combine)",
+                     "bytes_per_launch": r["layer_alg_bytes"],
+                     "launch_us": r["kernel_us"], "peak_kind": peak_kind},
         "layer": {"us": r["layer_us"], "alg_GBps": r["layer_alg_GBps"],
                   "frac": r["layer_alg_GBps"] / hbm, "tokens_per_s": r["layer_tokens_per_s"]},
         "e2e": {"value": r["e2e_tokens_per_s"], "unit": "tokens/s",
@@ -530,8 +513,8 @@ def main():
         line[f"q{b}"] = {"value": q["tokens_per_s"], "unit": "tokens/s",
                          "ms_per_step": q["ms_per_step"], "layer_us": q["layer_us"],
                          "layer_alg_GBps": q["layer_alg_GBps"],
-                         "gateup_alg_GBps": q["gateup_alg_GBps"],
-                         "gateup_frac": q["gateup_alg_GBps"] / hbm,
+                         "kernel_alg_GBps": q["kernel_alg_GBps"],
+                         "kernel_frac": q["kernel_alg_GBps"] / hbm,
                          "e2e": q["e2e_tokens_per_s"], "clocks": q["clocks"]}
     print(json.dumps(line), flush=True)
     if world > 1:

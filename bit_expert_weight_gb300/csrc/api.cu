@@ -130,9 +130,10 @@ bool valid_layer(const smoe_layer_desc *L)
 
 struct Plan {
     int64_t T;
-    int ntiles, ksplit, Epad, max_pairs, fmax, warps;
-    size_t off_ctr_tile, off_ctr_done, off_ctr_blk0, off_ctr_blk1, off_ctr_comb, off_meta,
-        off_plog, off_xsum, off_ids, off_w, off_sw, off_pairs, off_rmap, off_h, off_hsum, off_o,
+    int ntiles, ksplit, Epad, max_pairs, fmax, warps, max_strips;
+    size_t off_ctr_tile, off_ctr_done, off_ctr_sg, off_ctr_sd, off_ctr_comb, off_pair_done,
+        off_pair_ready, off_flags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w,
+        off_sw, off_pairs, off_rmap, off_scratch, off_hhi, off_hlo, off_hspart, off_hsum, off_o,
         off_part, total;
 };
 
@@ -159,30 +160,39 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
         mp = 1;
     p.max_pairs = static_cast<int>(mp);
     p.fmax = L->ffn_dim > L->shared_ffn_dim ? L->ffn_dim : L->shared_ffn_dim;
-    p.warps = expert_grid_warps();
+    p.max_strips = (p.fmax > d ? p.fmax : d) / 16;
+    p.warps = layer_grid_warps_max();
     size_t o = 0;
     auto take = [&](size_t bytes) {
         size_t at = o;
         o = align256(o + bytes);
         return at;
     };
+    // counters and flags first (zeroed once, kept at zero by the kernels)
     p.off_ctr_tile = take(sizeof(unsigned) * p.ntiles);
     p.off_ctr_done = take(sizeof(unsigned));
-    p.off_ctr_blk0 = take(sizeof(unsigned) * p.max_pairs * kMaxBlocksPerPair);
-    p.off_ctr_blk1 = take(sizeof(unsigned) * p.max_pairs * kMaxBlocksPerPair);
-    p.off_ctr_comb = take(sizeof(unsigned) * kMaxBlocksPerPair);
+    p.off_ctr_sg = take(sizeof(unsigned) * (size_t)p.max_pairs * p.max_strips);
+    p.off_ctr_sd = take(sizeof(unsigned) * (size_t)p.max_pairs * p.max_strips);
+    p.off_ctr_comb = take(sizeof(unsigned) * (d / 16));
+    p.off_pair_done = take(sizeof(unsigned) * p.max_pairs);
+    p.off_pair_ready = take(sizeof(unsigned) * p.max_pairs);
+    p.off_flags = take(sizeof(unsigned) * 4);
     p.off_meta = take(sizeof(int32_t) * 2);
     p.off_plog = take(sizeof(float) * p.ksplit * T * p.Epad);
+    p.off_logits = take(sizeof(float) * T * p.Epad);
     p.off_xsum = take(sizeof(float) * T * G * 2);
     p.off_ids = take(sizeof(int32_t) * tk);
     p.off_w = take(sizeof(float) * tk);
     p.off_sw = take(sizeof(float) * T);
     p.off_pairs = take(sizeof(int32_t) * kPairInts * p.max_pairs);
     p.off_rmap = take(sizeof(int32_t) * T * (k + 1));
-    p.off_h = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * p.fmax);
+    p.off_scratch = take(sizeof(int32_t) * E);
+    p.off_hhi = take(sizeof(uint16_t) * (size_t)p.max_pairs * kPairCols * p.fmax);
+    p.off_hlo = take(sizeof(uint16_t) * (size_t)p.max_pairs * kPairCols * p.fmax);
+    p.off_hspart = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 16) * 2);
     p.off_hsum = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 64) * 2);
     p.off_o = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
-    p.off_part = take(sizeof(float) * (size_t)p.warps * 2 * 32 * 32);
+    p.off_part = take(sizeof(float) * 4 * (size_t)p.warps * 2 * 2 * 32);
     p.total = o;
     return p;
 }
@@ -393,6 +403,8 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const smoe_layer_desc &L = *layer;
     int *status = device_status_word();
+    // T <= 8 with all stages: one fused launch (routing inside the kernel)
+    const bool fused = num_tokens <= kFusedCombineMaxT && stage_mask == 7;
 
     RouteArgs ra;
     memset(&ra, 0, sizeof ra);
@@ -424,52 +436,70 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     ra.status = status;
     ra.max_pairs = P.max_pairs;
 
-    ExpertArgs ea;
-    memset(&ea, 0, sizeof ea);
-    ea.tiles_routed = static_cast<const uint8_t *>(L.expert_tiles);
-    ea.tiles_shared = static_cast<const uint8_t *>(L.shared_tiles);
-    ea.expert_bytes_routed = expert_bytes(L.d_model, L.ffn_dim, L.bits);
-    ea.down_off_routed = gateup_bytes(L.d_model, L.ffn_dim, L.bits);
-    ea.down_off_shared = L.shared_ffn_dim > 0 ? gateup_bytes(L.d_model, L.shared_ffn_dim, L.bits) : 0;
-    ea.x = x;
-    ea.x_bf16 = x_dtype == SMOE_BF16;
-    ea.d = L.d_model;
-    ea.f = L.ffn_dim;
-    ea.fs = L.shared_ffn_dim;
-    ea.E = L.num_experts;
-    ea.k = L.top_k;
-    ea.bits = L.bits;
-    ea.T = num_tokens;
-    ea.pairs = ra.pairs;
-    ea.meta = ra.meta;
-    ea.xsum = ra.xsum;
-    ea.h = at<float>(workspace, P.off_h);
-    ea.hsum = at<float>(workspace, P.off_hsum);
-    ea.o = at<float>(workspace, P.off_o);
-    ea.partial = at<float>(workspace, P.off_part);
-    ea.comb_ctr = at<unsigned>(workspace, P.off_ctr_comb);
-    ea.route_map = ra.route_map;
-    ea.weights = ra.weights;
-    ea.shared_w = ra.shared_w;
-    ea.y = y;
-    ea.status = status;
-    ea.max_pairs = P.max_pairs;
-    ea.fused_combine = num_tokens <= kFusedCombineMaxT;
+    LayerArgs la;
+    memset(&la, 0, sizeof la);
+    la.router_w = ra.router_w;
+    la.shared_gate = ra.shared_gate;
+    la.expert_bias = L.expert_bias;
+    la.tiles_routed = static_cast<const uint8_t *>(L.expert_tiles);
+    la.tiles_shared = static_cast<const uint8_t *>(L.shared_tiles);
+    la.expert_bytes_routed = expert_bytes(L.d_model, L.ffn_dim, L.bits);
+    la.down_off_routed = gateup_bytes(L.d_model, L.ffn_dim, L.bits);
+    la.down_off_shared =
+        L.shared_ffn_dim > 0 ? gateup_bytes(L.d_model, L.shared_ffn_dim, L.bits) : 0;
+    la.x = x;
+    la.x_bf16 = x_dtype == SMOE_BF16;
+    la.T = num_tokens;
+    la.d = L.d_model;
+    la.f = L.ffn_dim;
+    la.fs = L.shared_ffn_dim;
+    la.E = L.num_experts;
+    la.k = L.top_k;
+    la.norm = ra.norm;
+    la.bits = L.bits;
+    la.Epad = P.Epad;
+    la.has_shared = ra.has_shared;
+    la.do_route = fused ? 1 : 0;
+    la.fused_combine = num_tokens <= kFusedCombineMaxT ? 1 : 0;
+    la.max_pairs = P.max_pairs;
+    la.max_strips = P.max_strips;
+    la.logits = at<float>(workspace, P.off_logits);
+    la.xsum = ra.xsum;
+    la.ids = ra.ids;
+    la.weights = ra.weights;
+    la.shared_w = ra.shared_w;
+    la.ids_out = ids_out;
+    la.w_out = w_out;
+    la.pairs = ra.pairs;
+    la.route_map = ra.route_map;
+    la.meta = ra.meta;
+    la.scratch = at<int32_t>(workspace, P.off_scratch);
+    la.h_hi = at<uint16_t>(workspace, P.off_hhi);
+    la.h_lo = at<uint16_t>(workspace, P.off_hlo);
+    la.hs_part = at<float>(workspace, P.off_hspart);
+    la.hsum = at<float>(workspace, P.off_hsum);
+    la.o = at<float>(workspace, P.off_o);
+    la.partial = at<float>(workspace, P.off_part);
+    la.strip_ctr_g = at<unsigned>(workspace, P.off_ctr_sg);
+    la.strip_ctr_d = at<unsigned>(workspace, P.off_ctr_sd);
+    la.comb_ctr = at<unsigned>(workspace, P.off_ctr_comb);
+    la.pair_done = at<unsigned>(workspace, P.off_pair_done);
+    la.pair_ready = at<unsigned>(workspace, P.off_pair_ready);
+    unsigned *flags = at<unsigned>(workspace, P.off_flags);
+    la.route_ctr = flags + 0;
+    la.route_flag = flags + 1;
+    la.exit_ctr = flags + 2;
+    la.y = y;
+    la.status = status;
 
-    if ((stage_mask & 1) && launch_router(ra, s, true) != cudaSuccess)
+    if (fused)
+        return launch_layer(la, s) == cudaSuccess ? SMOE_OK : SMOE_ERR_CUDA;
+    if ((stage_mask & 1) && launch_router(ra, s, false) != cudaSuccess)
         return SMOE_ERR_CUDA;
-    if (stage_mask & 2) {
-        ea.blk_ctr = at<unsigned>(workspace, P.off_ctr_blk0);
-        if (launch_expert(ea, 0, s, true) != cudaSuccess)
-            return SMOE_ERR_CUDA;
-    }
-    if (stage_mask & 4) {
-        ea.blk_ctr = at<unsigned>(workspace, P.off_ctr_blk1);
-        if (launch_expert(ea, 1, s, true) != cudaSuccess)
-            return SMOE_ERR_CUDA;
-        if (!ea.fused_combine && launch_combine(ea, s, true) != cudaSuccess)
-            return SMOE_ERR_CUDA;
-    }
+    if ((stage_mask & 2) && launch_layer(la, s) != cudaSuccess)
+        return SMOE_ERR_CUDA;
+    if ((stage_mask & 4) && !la.fused_combine && launch_combine(la, s) != cudaSuccess)
+        return SMOE_ERR_CUDA;
     return SMOE_OK;
 }
 

@@ -5,11 +5,10 @@
 //   codes    = 512 B (Q4) or 256 B (Q2) in the register order of the
 //              mma.sync m16n8k16 A fragment (see tile_code_bit below)
 //   scales   = 16 fp16 right after the codes, row r at halfword 2*(r&7)+(r>>3)
-//   block    = 8 tiles stacked along rows: 128 output rows x 64 columns
-//              gate/up: tiles (gate r0-15, up r0-15, gate r16-31, up r16-31,
-//                       ..., up r48-63) of a 64-row slice; down: 128 rows
-//   order    = block-major, then group g, then the 8 tiles:
-//              tile(b, g, s) at ((b * K/64 + g) * 8 + s) * TILE_BYTES
+//   strip    = the tiles of 16 output rows over all of K, in group order;
+//              gate/up strips interleave the gate and up tile of each group
+//   expert   = gate/up strips (f/16 of them, 2*d/64 tiles each), then down
+//              strips (d/16 of them, f/64 tiles each)
 // so each matrix is one contiguous tile stream and every tile is 16-byte
 // aligned.  Within a group the 64 input columns are permuted so that lane
 // (gq, tig) of an mma fragment owns columns 16*tig .. 16*tig + 15; the
@@ -25,7 +24,6 @@ namespace smoe {
 
 constexpr int kGroup = 64;
 constexpr int kTileRows = 16;
-constexpr int kBlockTiles = 8;
 
 __host__ __device__ constexpr int tile_code_bytes(int bits) { return bits * 128; }
 __host__ __device__ constexpr int tile_bytes(int bits) { return bits * 128 + 32; }

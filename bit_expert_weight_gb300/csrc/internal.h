@@ -71,36 +71,52 @@ cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, in
                                 const float *bias, int32_t *ids, float *w, cudaStream_t stream);
 cudaError_t launch_router(const RouteArgs &a, cudaStream_t stream, bool pdl);
 
-struct ExpertArgs {
+// The fused layer kernel (layer.cu).
+constexpr int kMaxLayerCtasPerSm = 3;
+
+struct LayerArgs {
+    // layer
+    const uint16_t *router_w;      // bf16 [E, d]
+    const uint16_t *shared_gate;   // nullable bf16 [d]
+    const float *expert_bias;      // nullable [E]
     const uint8_t *tiles_routed;   // bank base
     const uint8_t *tiles_shared;   // nullable
     int64_t expert_bytes_routed;   // stride between experts
-    int64_t down_off_routed, down_off_shared;  // byte offset of the down tiles
-    const void *x;                 // activations [T, d] (gate/up)
+    int64_t down_off_routed, down_off_shared;
+    const void *x;                 // [T, d]
     int x_bf16;
-    int d, f, fs, E, k, bits;
     int64_t T;
-    const int32_t *pairs;
-    const int32_t *meta;
-    const float *xsum;             // [T][d/64][2] (gate/up)
-    float *h;                      // [maxpairs][8][fmax]
-    float *hsum;                   // [maxpairs][8][fmax/64][2]
-    float *o;                      // [maxpairs][8][d]
-    float *partial;                // [warps][2][32][32]
-    unsigned *blk_ctr;             // gate/up or down block counters
-    unsigned *comb_ctr;            // [d/128]
-    const int32_t *route_map;      // [T][k+1]
-    const float *weights;          // [T][k]
-    const float *shared_w;         // [T]
+    int d, f, fs, E, k, norm, bits, Epad, has_shared;
+    int do_route;                  // 1: phase R inside the kernel (T <= 8)
+    int fused_combine;             // 1: combine inside the kernel (T <= 8)
+    int max_pairs, max_strips;     // counter strides
+    // workspace
+    float *logits;                 // [T][Epad]
+    float *xsum;                   // [T][d/64][2]
+    int32_t *ids;                  // [T][k]
+    float *weights;                // [T][k]
+    float *shared_w;               // [T]
+    int32_t *ids_out;              // nullable
+    float *w_out;                  // nullable
+    int32_t *pairs;                // [max_pairs][kPairInts]
+    int32_t *route_map;            // [T][k+1]
+    int32_t *meta;                 // [0] routed pairs, [1] all pairs
+    int32_t *scratch;              // [E]
+    uint16_t *h_hi, *h_lo;         // bf16 [max_pairs][8][fmax]
+    float *hs_part;                // [max_pairs][8][fmax/16][2]
+    float *hsum;                   // [max_pairs][8][fmax/64][2]
+    float *o;                      // [max_pairs][8][d]
+    float *partial;                // [warps][2][2][32] float4
+    unsigned *strip_ctr_g, *strip_ctr_d;  // [max_pairs][max_strips]
+    unsigned *comb_ctr;            // [d/16]
+    unsigned *pair_done, *pair_ready;     // [max_pairs]
+    unsigned *route_ctr, *route_flag, *exit_ctr;
     float *y;                      // [T, d]
     int *status;
-    int max_pairs;
-    int fused_combine;
 };
 
-cudaError_t launch_expert(const ExpertArgs &a, int phase, cudaStream_t stream, bool pdl);
-cudaError_t launch_combine(const ExpertArgs &a, cudaStream_t stream, bool pdl);
-// Warps of the expert kernels' grid on the current device (workspace sizing).
-int expert_grid_warps();
+int layer_grid_warps_max();
+cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream);
+cudaError_t launch_combine(const LayerArgs &a, cudaStream_t stream);
 
 }  // namespace smoe

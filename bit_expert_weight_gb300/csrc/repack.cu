@@ -14,21 +14,14 @@ namespace smoe {
 
 namespace {
 
-// Destination of tile (rb, g) of matrix `kind` (0 gate, 1 up, 2 down).
+// Destination of tile (rb, g) of matrix `kind` (0 gate, 1 up, 2 down):
+// strip-major, gate and up interleaved per group.
 __device__ __forceinline__ int64_t tile_offset(int kind, int rb, int g, int G, int bits,
                                                int64_t gateup_bytes)
 {
-    int b, slot;
-    int64_t base = 0;
-    if (kind < 2) {
-        b = rb >> 2;
-        slot = 2 * (rb & 3) + kind;
-    } else {
-        b = rb >> 3;
-        slot = rb & 7;
-        base = gateup_bytes;
-    }
-    return base + ((int64_t)(b * G + g) * kBlockTiles + slot) * tile_bytes(bits);
+    if (kind < 2)
+        return (((int64_t)rb * G + g) * 2 + kind) * tile_bytes(bits);
+    return gateup_bytes + ((int64_t)rb * G + g) * tile_bytes(bits);
 }
 
 __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ codes,
