@@ -69,10 +69,6 @@ __device__ __forceinline__ void st_release(unsigned *p, unsigned v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async()
-{
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 
 // Lane 0 polls until *p >= target (bounded); the result is broadcast.
 __device__ bool warp_wait_geq(const unsigned *p, unsigned target, int *status)
@@ -165,7 +161,12 @@ __device__ void route_one_token(const float *lg, int E, int k, int norm, const f
         }
         if ((bi & 31) == lane)
             taken |= 1u << (bi >> 5);
-        const float p = expf(__ldcg(lg + bi) - m) / z;
+        float mine = lv[0];
+#pragma unroll
+        for (int i = 1; i < kPerLane; ++i)
+            if ((bi >> 5) == i)
+                mine = lv[i];
+        const float p = expf(__shfl_sync(0xffffffffu, mine, bi & 31) - m) / z;
         psel += p;
         if (lane == j) {
             pj_mine = p;
@@ -245,20 +246,32 @@ __device__ void router_unit(const LayerArgs &a, int unit)
         const int t = unit - rows;
         for (int g = lane; g < d / kGroup; g += 32) {
             float s0 = 0.f, s1 = 0.f;
-            for (int c = 0; c < kGroup; c += 4) {
-                float v[4];
-                if (XBF16) {
-                    const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(
-                        reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + g * kGroup + c));
-                    v[0] = bf16lo_to_f32(xv.x), v[1] = bf16hi_to_f32(xv.x);
-                    v[2] = bf16lo_to_f32(xv.y), v[3] = bf16hi_to_f32(xv.y);
-                } else {
-                    const float4 xv = __ldg(reinterpret_cast<const float4 *>(
-                        reinterpret_cast<const float *>(a.x) + (int64_t)t * d + g * kGroup + c));
-                    v[0] = xv.x, v[1] = xv.y, v[2] = xv.z, v[3] = xv.w;
+            if (XBF16) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + g * kGroup);
+                uint4 v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = __ldg(src + i);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    s0 += bf16lo_to_f32(v[i].x) + bf16hi_to_f32(v[i].x);
+                    s1 += bf16lo_to_f32(v[i].y) + bf16hi_to_f32(v[i].y);
+                    s0 += bf16lo_to_f32(v[i].z) + bf16hi_to_f32(v[i].z);
+                    s1 += bf16lo_to_f32(v[i].w) + bf16hi_to_f32(v[i].w);
                 }
-                s0 += v[0] + v[1];
-                s1 += v[2] + v[3];
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    reinterpret_cast<const float *>(a.x) + (int64_t)t * d + g * kGroup);
+                float4 v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = __ldg(src + i);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    s0 += v[i].x + v[i].y;
+                    s1 += v[i].z + v[i].w;
+                }
             }
             reinterpret_cast<float2 *>(a.xsum)[(int64_t)t * (d / kGroup) + g] = make_float2(s0, s1);
         }
@@ -420,33 +433,37 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
 
     // activations of (pair, group): this lane's 16 columns of its token
     // row, and the group sums of the two output columns it accumulates
-    auto load_b = [&](int p, int g, BRaw<NV> &r) {
+    // the segment's pair record, read once: its column count, this lane's
+    // token row (gq) and the tokens of the lane's two output columns
+    int pi_ncols = 0, pi_tok = 0, pi_t0 = -1, pi_t1 = -1;
+    auto read_pair = [&](int p) {
         const int32_t *pr = a.pairs + p * kPairInts;
-        const int ncols = __ldcg(pr + 1);
-        const bool valid = gq < ncols;
+        pi_ncols = __ldcg(pr + 1);
+        pi_tok = gq < pi_ncols ? __ldcg(pr + 2 + gq) : 0;
+        pi_t0 = 2 * tig < pi_ncols ? __ldcg(pr + 2 + 2 * tig) : -1;
+        pi_t1 = 2 * tig + 1 < pi_ncols ? __ldcg(pr + 2 + 2 * tig + 1) : -1;
+    };
+    auto load_b = [&](int p, int g, BRaw<NV> &r) {
+        const bool valid = gq < pi_ncols;
         const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
         const float2 z2 = make_float2(0.f, 0.f);
         if (phase == 0) {
-            const int tok = valid ? __ldcg(pr + 2 + gq) : 0;
+            const int tok = pi_tok;
             if (XBF16) {
                 const uint4 *row = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const uint16_t *>(a.x) + (int64_t)tok * d + g * kGroup +
-                    16 * tig);
+                    reinterpret_cast<const uint16_t *>(a.x) + (int64_t)tok * d + g * kGroup + 16 * tig);
                 r.v[0] = valid ? __ldg(row) : z4;
                 r.v[1] = valid ? __ldg(row + 1) : z4;
             } else {
                 const uint4 *row = reinterpret_cast<const uint4 *>(
                     reinterpret_cast<const float *>(a.x) + (int64_t)tok * d + g * kGroup + 16 * tig);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < NV; ++i)
                     r.v[i] = valid ? __ldg(row + i) : z4;
             }
-            const int c0 = 2 * tig, c1 = c0 + 1;
-            const int t0 = c0 < ncols ? __ldcg(pr + 2 + c0) : -1;
-            const int t1 = c1 < ncols ? __ldcg(pr + 2 + c1) : -1;
             const float2 *xs = reinterpret_cast<const float2 *>(a.xsum);
-            r.xs0 = t0 >= 0 ? __ldcg(xs + (int64_t)t0 * (d / kGroup) + g) : z2;
-            r.xs1 = t1 >= 0 ? __ldcg(xs + (int64_t)t1 * (d / kGroup) + g) : z2;
+            r.xs0 = pi_t0 >= 0 ? __ldcg(xs + (int64_t)pi_t0 * (d / kGroup) + g) : z2;
+            r.xs1 = pi_t1 >= 0 ? __ldcg(xs + (int64_t)pi_t1 * (d / kGroup) + g) : z2;
         } else {
             const int64_t off = ((int64_t)p * kPairCols + gq) * fmax + g * kGroup + 16 * tig;
             const uint4 *hi = reinterpret_cast<const uint4 *>(a.h_hi + off);
@@ -458,8 +475,8 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
             const int c0 = 2 * tig, c1 = c0 + 1;
             const float2 *hs = reinterpret_cast<const float2 *>(a.hsum);
             const int64_t base = (int64_t)p * kPairCols * (fmax / kGroup);
-            r.xs0 = c0 < ncols ? __ldcg(hs + base + (int64_t)c0 * (fmax / kGroup) + g) : z2;
-            r.xs1 = c1 < ncols ? __ldcg(hs + base + (int64_t)c1 * (fmax / kGroup) + g) : z2;
+            r.xs0 = c0 < pi_ncols ? __ldcg(hs + base + (int64_t)c0 * (fmax / kGroup) + g) : z2;
+            r.xs1 = c1 < pi_ncols ? __ldcg(hs + base + (int64_t)c1 * (fmax / kGroup) + g) : z2;
         }
     };
     // B fragments for the mma from a BRaw
@@ -727,6 +744,7 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
             }
             waited_p = p;
         }
+        read_pair(p);
         // groups of this segment: phase 0 has 2 tiles (gate, up) per group
         const int tpg = phase == 0 ? 2 : 1;
         const int g0 = pos0 / tpg, g1 = (pos1 - 1) / tpg + 1;
@@ -801,12 +819,8 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
 template <int BITS, bool XBF16>
 __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs a)
 {
-    constexpr int TB = tile_bytes(BITS);
-    constexpr int CB = tile_code_bytes(BITS);
-    constexpr float L = BITS == 4 ? 7.5f : 1.5f;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, tig = lane & 3;
     uint8_t *ring = smem + warp * ring_bytes(BITS);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * ring_bytes(BITS)) + warp * kNS;
     if (lane == 0) {
@@ -818,15 +832,16 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs 
 
     const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
     const int64_t Wall = (int64_t)gridDim.x * kWarps;
-    const int d = a.d;
     bool ok = true;
 
     // ------------------------------------------------------------ phase R
     if (a.do_route) {
         const int rows = a.E + (a.shared_gate ? 1 : 0);
         const int units = rows + static_cast<int>(a.T);
-        if (w < units) {
-            router_unit<XBF16>(a, static_cast<int>(w));
+        // unit i runs on warp i / gridDim.x of CTA i % gridDim.x: one per SM first
+        const int64_t unit = (int64_t)warp * gridDim.x + blockIdx.x;
+        if (unit < units) {
+            router_unit<XBF16>(a, static_cast<int>(unit));
             __threadfence();
             __syncwarp();
             unsigned old = 0;
