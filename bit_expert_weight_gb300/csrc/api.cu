@@ -4,7 +4,7 @@
 
 #include <mutex>
 
-#include "../../include/smoe.h"
+#include "smoe.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -132,9 +132,8 @@ struct Plan {
     int64_t T;
     int ntiles, ksplit, Epad, max_pairs, fmax, warps, max_strips;
     size_t off_ctr_tile, off_ctr_done, off_ctr_sg, off_ctr_sd, off_ctr_comb, off_pair_done,
-        off_pair_ready, off_flags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w,
-        off_sw, off_pairs, off_rmap, off_scratch, off_hhi, off_hlo, off_hspart, off_hsum, off_o,
-        off_part, total;
+        off_flags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w, off_sw, off_pairs,
+        off_rmap, off_hhi, off_hlo, off_hspart, off_o, off_part, total;
 };
 
 Plan make_plan(const smoe_layer_desc *L, int64_t T)
@@ -175,7 +174,6 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_ctr_sd = take(sizeof(unsigned) * (size_t)p.max_pairs * p.max_strips);
     p.off_ctr_comb = take(sizeof(unsigned) * (d / 16));
     p.off_pair_done = take(sizeof(unsigned) * p.max_pairs);
-    p.off_pair_ready = take(sizeof(unsigned) * p.max_pairs);
     p.off_flags = take(sizeof(unsigned) * 4);
     p.off_meta = take(sizeof(int32_t) * 2);
     p.off_plog = take(sizeof(float) * p.ksplit * T * p.Epad);
@@ -186,11 +184,9 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_sw = take(sizeof(float) * T);
     p.off_pairs = take(sizeof(int32_t) * kPairInts * p.max_pairs);
     p.off_rmap = take(sizeof(int32_t) * T * (k + 1));
-    p.off_scratch = take(sizeof(int32_t) * E);
     p.off_hhi = take(sizeof(uint16_t) * (size_t)p.max_pairs * kPairCols * p.fmax);
     p.off_hlo = take(sizeof(uint16_t) * (size_t)p.max_pairs * kPairCols * p.fmax);
     p.off_hspart = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 16) * 2);
-    p.off_hsum = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 64) * 2);
     p.off_o = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
     p.off_part = take(sizeof(float) * 4 * (size_t)p.warps * 2 * 2 * 32);
     p.total = o;
@@ -473,22 +469,18 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     la.pairs = ra.pairs;
     la.route_map = ra.route_map;
     la.meta = ra.meta;
-    la.scratch = at<int32_t>(workspace, P.off_scratch);
     la.h_hi = at<uint16_t>(workspace, P.off_hhi);
     la.h_lo = at<uint16_t>(workspace, P.off_hlo);
     la.hs_part = at<float>(workspace, P.off_hspart);
-    la.hsum = at<float>(workspace, P.off_hsum);
     la.o = at<float>(workspace, P.off_o);
     la.partial = at<float>(workspace, P.off_part);
     la.strip_ctr_g = at<unsigned>(workspace, P.off_ctr_sg);
     la.strip_ctr_d = at<unsigned>(workspace, P.off_ctr_sd);
     la.comb_ctr = at<unsigned>(workspace, P.off_ctr_comb);
     la.pair_done = at<unsigned>(workspace, P.off_pair_done);
-    la.pair_ready = at<unsigned>(workspace, P.off_pair_ready);
     unsigned *flags = at<unsigned>(workspace, P.off_flags);
     la.route_ctr = flags + 0;
-    la.route_flag = flags + 1;
-    la.exit_ctr = flags + 2;
+    la.exit_ctr = flags + 1;
     la.y = y;
     la.status = status;
 

@@ -49,10 +49,9 @@ __host__ __device__ inline int tile_scale_half(int r) { return 2 * (r & 7) + (r 
 // Device status word codes (one per device, cleared by the host query).
 enum : int { kStatusOk = 0, kStatusBadExpert = 1, kStatusTimeout = 2, kStatusBadArg = 3 };
 
-// Bounded waits give up after this many polls (each poll may suspend the
-// thread briefly inside mbarrier.try_wait); in practice a wait ends in
-// microseconds, so reaching the bound means a broken pipeline.
-constexpr unsigned kWaitPolls = 1u << 22;
+// Bounded waits give up after this many SM cycles (~2 s); in practice a wait
+// ends in microseconds, so reaching the bound means a broken pipeline.
+constexpr long long kWaitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -78,26 +77,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned by
                  : "memory");
 }
 
-// Returns true once the phase with the given parity has completed.
+// Returns true once the phase with the given parity has completed.  The
+// waiting thread is suspended by the hardware (up to the hint, 0.5 ms) and
+// woken when the phase completes, so a waiting warp takes no issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(500000u)
                  : "memory");
     return ok != 0;
 }
 
-// Bounded wait; returns false if it gave up.
+// Bounded wait (about kWaitCycles SM cycles); returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity)
 {
-    for (unsigned i = 0; i < kWaitPolls; ++i)
-        if (mbar_try_wait(bar, parity))
-            return true;
-    return false;
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles)
+            return false;
+    return true;
 }
 
 // 1-D bulk copy global -> shared through the TMA engine, completing on an

@@ -101,16 +101,14 @@ struct LayerArgs {
     int32_t *pairs;                // [max_pairs][kPairInts]
     int32_t *route_map;            // [T][k+1]
     int32_t *meta;                 // [0] routed pairs, [1] all pairs
-    int32_t *scratch;              // [E]
     uint16_t *h_hi, *h_lo;         // bf16 [max_pairs][8][fmax]
     float *hs_part;                // [max_pairs][8][fmax/16][2]
-    float *hsum;                   // [max_pairs][8][fmax/64][2]
     float *o;                      // [max_pairs][8][d]
     float *partial;                // [warps][2][2][32] float4
     unsigned *strip_ctr_g, *strip_ctr_d;  // [max_pairs][max_strips]
     unsigned *comb_ctr;            // [d/16]
-    unsigned *pair_done, *pair_ready;     // [max_pairs]
-    unsigned *route_ctr, *route_flag, *exit_ctr;
+    unsigned *pair_done;           // [max_pairs] finished gate/up strips
+    unsigned *route_ctr, *exit_ctr;
     float *y;                      // [T, d]
     int *status;
 };

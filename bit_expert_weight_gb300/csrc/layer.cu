@@ -14,10 +14,12 @@
 // is resident):
 //  R  (T <= 8 only) one warp per router row computes that expert's logits
 //     for all tokens over the full d (no K split, no partials); T more warps
-//     compute the per-group activation sums.  The last warp to finish (an
-//     arrival counter) routes every token and builds the pair table, then
-//     releases the route flag.  For T > 8 a separate router kernel has done
-//     this before the launch.
+//     compute the per-group activation sums; each bumps an arrival counter.
+//     Every CTA then routes the tokens itself (one warp per token) and builds
+//     the pair table in its own shared memory -- the same deterministic code
+//     on the same logits gives the same table in every CTA, so nothing is
+//     written back and re-read.  For T > 8 a separate router kernel has
+//     built the tables in global memory before the launch.
 //  G  gate/up: the tiles of all pairs (pair = one expert x <= 8 tokens) form
 //     one stream of 16-row strips; each warp takes an equal contiguous range
 //     (stream-K), streams it through a private ring of shared-memory stages
@@ -25,12 +27,12 @@
 //     with mma.sync.  A strip (16 rows x all of d, gate and up interleaved)
 //     finished by one warp is finalised in registers; one shared by several
 //     warps is finalised by the last to arrive, summing the partials in warp
-//     order.  Finalising writes h = SiLU(g) * u as bf16 hi + lo and
-//     per-strip class sums; the strip that completes a pair sums those into
-//     per-group sums and releases the pair's ready flag.
+//     order.  Finalising writes h = SiLU(g) * u as bf16 hi + lo and the
+//     strip's per-class sums of h, then bumps the pair's strip count.
 //  D  down: the same streaming over 16-row strips of W_down.  A warp issues
-//     its first weight copies before waiting for its pair's ready flag, so
-//     the weights are in flight while gate/up finishes.  The last pair to
+//     its first weight copies before its CTA waits for the strip counts of
+//     the pairs it reads, so the weights are in flight while gate/up
+//     finishes.  The last pair to
 //     finish an output strip (T <= 8) sums sum_j w_j o_j (+ shared) in rank
 //     order into y.
 // Deterministic throughout: no float atomics.
@@ -43,11 +45,11 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kST = 4;  // tiles per stage
-constexpr int kNS = 4;  // stages per warp ring
+constexpr int kNS = 8;  // stages per warp ring (one group each)
 constexpr long long kSpinCycles = 4000000000ll;  // ~2 s at 2 GHz
 
-__host__ __device__ constexpr int ring_bytes(int bits) { return kNS * kST * tile_bytes(bits); }
+__host__ __device__ constexpr int kStageBytes(int bits) { return 2 * tile_bytes(bits); }
+__host__ __device__ constexpr int ring_bytes(int bits) { return kNS * kStageBytes(bits); }
 __host__ __device__ constexpr int smem_bytes(int bits)
 {
     return kWarps * ring_bytes(bits) + kWarps * kNS * 8;
@@ -64,10 +66,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Lane 0 polls until *p >= target (bounded); the result is broadcast.
@@ -94,6 +92,12 @@ __device__ bool warp_wait_geq(const unsigned *p, unsigned target, int *status)
     return ok != 0;
 }
 
+// CTA-wide named barrier 1 (all kThreads threads).
+__device__ __forceinline__ void cta_barrier()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+
 __device__ __forceinline__ int64_t warp_of(int64_t u, int64_t W, int64_t U)
 {
     return ((u + 1) * W - 1) / U;
@@ -104,7 +108,8 @@ __device__ __forceinline__ int64_t warp_of(int64_t u, int64_t W, int64_t U)
 constexpr int kPerLane = kMaxExperts / 32;
 
 __device__ void route_one_token(const float *lg, int E, int k, int norm, const float *bias,
-                                int32_t *ids, float *w, int32_t *ids2, float *w2, int *status)
+                                int16_t *ids_s, float *w_s, int32_t *ids_g, float *w_g,
+                                int *status)
 {
     const int lane = threadIdx.x & 31;
     float key[kPerLane], lv[kPerLane];
@@ -175,12 +180,12 @@ __device__ void route_one_token(const float *lg, int E, int k, int norm, const f
     }
     if (lane < k) {
         const float wv = norm ? pj_mine / psel : pj_mine;
-        ids[lane] = ej_mine;
-        w[lane] = wv;
-        if (ids2)
-            ids2[lane] = ej_mine;
-        if (w2)
-            w2[lane] = wv;
+        ids_s[lane] = static_cast<int16_t>(ej_mine);
+        w_s[lane] = wv;
+        if (ids_g)
+            ids_g[lane] = ej_mine;
+        if (w_g)
+            w_g[lane] = wv;
     }
 }
 
@@ -198,39 +203,46 @@ __device__ void router_unit(const LayerArgs &a, int unit)
 #pragma unroll
         for (int t = 0; t < kPairCols; ++t)
             acc[t] = 0.f;
-        for (int c = lane * 8; c < d; c += 256) {
-            const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(wr + c));
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-            float wf[8];
+        // four 256-column slices per batch: all loads of a batch in flight
+        for (int c0 = lane * 8; c0 < d; c0 += 1024) {
+            uint4 wv[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                wf[2 * i] = bf16lo_to_f32(ww[i]);
-                wf[2 * i + 1] = bf16hi_to_f32(ww[i]);
-            }
+            for (int i = 0; i < 4; ++i)
+                wv[i] = c0 + 256 * i < d ? __ldg(reinterpret_cast<const uint4 *>(wr + c0 + 256 * i))
+                                         : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int t = 0; t < kPairCols; ++t) {
                 if (t >= T)
                     break;
-                float xf[8];
-                if (XBF16) {
-                    const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
-                        reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + c));
-                    const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        xf[2 * i] = bf16lo_to_f32(xx[i]);
-                        xf[2 * i + 1] = bf16hi_to_f32(xx[i]);
+                for (int i = 0; i < 4; ++i) {
+                    const int c = c0 + 256 * i;
+                    if (c >= d)
+                        break;
+                    const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+                    float xf[8];
+                    if (XBF16) {
+                        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
+                            reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + c));
+                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            xf[2 * q] = bf16lo_to_f32(xx[q]);
+                            xf[2 * q + 1] = bf16hi_to_f32(xx[q]);
+                        }
+                    } else {
+                        const float *xr = reinterpret_cast<const float *>(a.x) + (int64_t)t * d + c;
+                        const float4 x0 = __ldg(reinterpret_cast<const float4 *>(xr));
+                        const float4 x1 = __ldg(reinterpret_cast<const float4 *>(xr) + 1);
+                        xf[0] = x0.x, xf[1] = x0.y, xf[2] = x0.z, xf[3] = x0.w;
+                        xf[4] = x1.x, xf[5] = x1.y, xf[6] = x1.z, xf[7] = x1.w;
                     }
-                } else {
-                    const float *xr = reinterpret_cast<const float *>(a.x) + (int64_t)t * d + c;
-                    const float4 x0 = __ldg(reinterpret_cast<const float4 *>(xr));
-                    const float4 x1 = __ldg(reinterpret_cast<const float4 *>(xr) + 1);
-                    xf[0] = x0.x, xf[1] = x0.y, xf[2] = x0.z, xf[3] = x0.w;
-                    xf[4] = x1.x, xf[5] = x1.y, xf[6] = x1.z, xf[7] = x1.w;
-                }
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[t] = fmaf(wf[i], xf[i], acc[t]);
+                    for (int q = 0; q < 4; ++q) {
+                        acc[t] = fmaf(bf16lo_to_f32(ww[q]), xf[2 * q], acc[t]);
+                        acc[t] = fmaf(bf16hi_to_f32(ww[q]), xf[2 * q + 1], acc[t]);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -278,73 +290,79 @@ __device__ void router_unit(const LayerArgs &a, int unit)
     }
 }
 
-// Route every token and build the pair table (T <= 8): pair = one selected
-// expert with the (ascending) tokens that chose it; then the shared pair.
-__device__ void route_and_dispatch(const LayerArgs &a)
+// Routing tables of a CTA.  On the fused path (T <= 8) every CTA builds its
+// own copy in shared memory from the published logits (the same
+// deterministic code on the same logits gives the same tables everywhere);
+// otherwise they point to the tables the router kernel left in global memory.
+constexpr int kFusedPairs = kPairCols * SMOE_MAX_TOPK_DEV + 1;
+// route_map, weights and ids are [T][k+1], [T][k], [T][k] with the runtime k
+// as the row stride, exactly like the global tables.
+struct RouteSmem {
+    int32_t pairs[kFusedPairs][kPairInts];
+    int32_t route_map[kPairCols * (SMOE_MAX_TOPK_DEV + 1)];
+    float weights[kPairCols * SMOE_MAX_TOPK_DEV];
+    float shared_w[kPairCols];
+    int16_t ids[kPairCols * SMOE_MAX_TOPK_DEV];
+    int16_t pair_of[kMaxExperts];
+    int meta[2];
+};
+struct RouteView {
+    const int32_t *pairs;      // [P][kPairInts]
+    const int32_t *route_map;  // [T][k+1]
+    const float *weights;      // [T][k]
+    const float *shared_w;     // [T]
+};
+
+// Warp 0 of the CTA: pair table from the routed ids (T <= 8).  Pair = one
+// selected expert with the ascending tokens that chose it, pairs in order of
+// first appearance; then the shared expert's pair.
+__device__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
 {
     const int lane = threadIdx.x & 31;
     const int T = static_cast<int>(a.T), k = a.k, E = a.E;
-    for (int t = 0; t < T; ++t) {
-        route_one_token(a.logits + (int64_t)t * a.Epad, E, k, a.norm, a.expert_bias,
-                        a.ids + t * k, a.weights + t * k, a.ids_out ? a.ids_out + t * k : nullptr,
-                        a.w_out ? a.w_out + t * k : nullptr, a.status);
-        if (lane == 0)
-            a.shared_w[t] =
-                a.shared_gate ? 1.0f / (1.0f + expf(-__ldcg(a.logits + (int64_t)t * a.Epad + E)))
-                              : 1.0f;
-    }
-    __syncwarp();
-    __threadfence_block();
-    // pair_of[e] lives in the pair table's scratch area (E ints, zeroed = -1 + 1)
-    int32_t *pair_of = a.scratch;
     for (int e = lane; e < E; e += 32)
-        pair_of[e] = -1;
+        r.pair_of[e] = -1;
     __syncwarp();
     int npairs = 0;
     for (int t = 0; t < T; ++t) {
         int e = -1, p = -1;
         if (lane < k) {
-            e = a.ids[t * k + lane];
-            p = pair_of[e];
+            e = r.ids[t * k + lane];
+            p = r.pair_of[e];
         }
         const unsigned newm = __ballot_sync(0xffffffffu, lane < k && p < 0);
         if (lane < k && p < 0) {
             p = npairs + __popc(newm & ((1u << lane) - 1u));
-            pair_of[e] = p;
-            int32_t *pr = a.pairs + p * kPairInts;
-            pr[0] = e;
-            pr[1] = 0;
+            r.pair_of[e] = static_cast<int16_t>(p);
+            r.pairs[p][0] = e;
+            r.pairs[p][1] = 0;
         }
         npairs += __popc(newm);
         __syncwarp();
         if (lane < k) {
-            int32_t *pr = a.pairs + p * kPairInts;
-            const int col = pr[1];
-            pr[2 + col] = t;
-            pr[1] = col + 1;
-            a.route_map[t * (k + 1) + lane] = p * kPairCols + col;
+            const int col = r.pairs[p][1];
+            r.pairs[p][2 + col] = t;
+            r.pairs[p][1] = col + 1;
+            r.route_map[t * (k + 1) + lane] = p * kPairCols + col;
         }
         __syncwarp();
     }
     if (a.has_shared) {
         if (lane == 0) {
-            int32_t *pr = a.pairs + npairs * kPairInts;
-            pr[0] = -1;
-            pr[1] = T;
-            for (int t = 0; t < kPairCols; ++t)
-                pr[2 + t] = t < T ? t : 0;
+            r.pairs[npairs][0] = -1;
+            r.pairs[npairs][1] = T;
         }
+        if (lane < kPairCols)
+            r.pairs[npairs][2 + lane] = lane < T ? lane : 0;
         if (lane < T)
-            a.route_map[lane * (k + 1) + k] = npairs * kPairCols + lane;
+            r.route_map[lane * (k + 1) + k] = npairs * kPairCols + lane;
     }
     if (lane == 0) {
-        a.meta[0] = npairs;
-        a.meta[1] = npairs + (a.has_shared ? 1 : 0);
+        r.meta[0] = npairs;
+        r.meta[1] = npairs + (a.has_shared ? 1 : 0);
     }
     __syncwarp();
 }
-
-// --------------------------------------------------------------- the kernel
 
 // This lane's 16 activations of one group (bf16 x: 2 vectors; fp32 x: 4;
 // h of the down phase: hi in v[0..1], lo in v[2..3]) and the group sums
@@ -356,107 +374,141 @@ struct BRaw {
 };
 
 // One streaming phase (0: gate/up + SiLU, 1: down + combine) of one warp.
+// The unit of work is a group: 64 input columns of 16 output rows (phase 0:
+// the gate tile and the up tile of those rows, phase 1: one down tile).  A
+// pair's groups are contiguous in memory (strip-major), so a warp's range is
+// a few contiguous runs; each stage of the warp's ring holds one group.
 // Returns false if a bounded wait ran out (the status word is set).
 template <int BITS, bool XBF16, int PHASE>
 __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uint64_t *bars,
-                                          int64_t &seq_base, int P_r, int P_t, int fmax,
-                                          int64_t w, int64_t Wall)
+                                          uint32_t &ring_seq, int P_r, int P_t, int fmax,
+                                          int64_t w, int64_t Wall, bool enabled, int *s_ok,
+                                          const RouteView &rv)
 {
     constexpr int TB = tile_bytes(BITS);
     constexpr int CB = tile_code_bytes(BITS);
     constexpr float L = BITS == 4 ? 7.5f : 1.5f;
-    constexpr int phase = PHASE;
+    constexpr int TPG = PHASE == 0 ? 2 : 1;  // tiles per group
+    constexpr int GB = TPG * TB;             // bytes per group
     constexpr int NV = (PHASE == 1 || !XBF16) ? 4 : 2;
+    constexpr bool kSplit = PHASE == 1 || !XBF16;
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tig = lane & 3;
     const int d = a.d;
     bool ok = true;
-    const int Kr = phase == 0 ? d : a.f;    // K of routed pairs
-    const int Ks = phase == 0 ? d : a.fs;   // K of the shared pair
-    const int Rr = phase == 0 ? a.f : d;    // output rows of routed pairs
-    const int Rs = phase == 0 ? a.fs : d;
-    const int tps_r = phase == 0 ? 2 * (Kr / kGroup) : Kr / kGroup;  // tiles per strip
-    const int tps_s = phase == 0 ? 2 * (Ks / kGroup) : Ks / kGroup;
-    const int64_t U_r = (int64_t)(Rr / kTileRows) * tps_r;
-    const int64_t U_s = P_t > P_r ? (int64_t)(Rs / kTileRows) * tps_s : 0;
-    const int64_t U = (int64_t)P_r * U_r + (int64_t)(P_t - P_r) * U_s;
-    const int64_t W = U < Wall ? U : Wall;
+    const int Kr = PHASE == 0 ? d : a.f, Ks = PHASE == 0 ? d : a.fs;
+    const int Rr = PHASE == 0 ? a.f : d, Rs = PHASE == 0 ? a.fs : d;
+    const int gps_r = Kr / kGroup, gps_s = Ks / kGroup;  // groups per strip
+    // 32-bit group indices: a layer's stream is far below 2^31 groups
+    const int U_r = (Rr / kTileRows) * gps_r;             // groups per routed pair
+    const int U_s = P_t > P_r ? (Rs / kTileRows) * gps_s : 0;
+    const int UR = P_r * U_r;
+    const int U = enabled ? UR + (P_t - P_r) * U_s : 0;
+    const int W = U < Wall ? U : static_cast<int>(Wall);
     const bool active = w < W;
-    const int64_t u0 = active ? w * U / W : 0, u1 = active ? (w + 1) * U / W : 0;
-    const int64_t nst = (u1 - u0 + kST - 1) / kST;
-
-    auto locate = [&](int64_t u, int &p, int64_t &lt) {
-        if (u < (int64_t)P_r * U_r) {
-            p = static_cast<int>(u / U_r);
-            lt = u - (int64_t)p * U_r;
-        } else {
-            const int64_t v = u - (int64_t)P_r * U_r;
-            const int q = static_cast<int>(v / U_s);
-            p = P_r + q;
-            lt = v - (int64_t)q * U_s;
-        }
+    const int u0 = active ? static_cast<int>(w * U / W) : 0;
+    const int u1 = active ? static_cast<int>((w + 1) * U / W) : 0;
+    const int n = u1 - u0;
+    auto pair_of = [&](int u) { return u < UR ? u / U_r : P_r + (u - UR) / U_s; };
+    auto pair_start = [&](int p) { return p < P_r ? p * U_r : UR + (p - P_r) * U_s; };
+    auto pair_units = [&](int p) { return p < P_r ? U_r : U_s; };
+    auto pair_base = [&](int p) -> const uint8_t * {
+        const int e = rv.pairs[p * kPairInts];
+        return e >= 0 ? a.tiles_routed + (int64_t)e * a.expert_bytes_routed +
+                            (PHASE == 0 ? 0 : a.down_off_routed)
+                      : a.tiles_shared + (PHASE == 0 ? 0 : a.down_off_shared);
     };
-    auto tile_src = [&](int p, int64_t lt) -> const uint8_t * {
-        const int e = __ldcg(a.pairs + p * kPairInts);
-        const uint8_t *base = e >= 0 ? a.tiles_routed + (int64_t)e * a.expert_bytes_routed +
-                                           (phase == 0 ? 0 : a.down_off_routed)
-                                     : a.tiles_shared + (phase == 0 ? 0 : a.down_off_shared);
-        return base + lt * TB;
-    };
-    // lane 0 issues stage i of this phase (tiles u0 + i*ST ..); the two
-    // marks let a failing warp drain exactly the copies still in flight
-    int64_t issued_upto = 0, waited_upto = 0;
-    auto issue = [&](int64_t i) {
-        if (i >= nst)
+    // Issue state, lane 0 only: the pair being copied and the next pair's
+    // base, looked up one pair ahead.
+    int is_ps = 0, is_end = 0, is_p = 0;
+    const uint8_t *is_base = nullptr, *nx_base = nullptr;
+    int issued = 0, waited = 0;  // stages issued / consumed, for a bounded drain
+    if (lane == 0 && active) {
+        is_p = pair_of(u0);
+        is_ps = pair_start(is_p);
+        is_end = is_ps + pair_units(is_p);
+        is_base = pair_base(is_p);
+        nx_base = is_end < u1 ? pair_base(is_p + 1) : nullptr;
+    }
+    auto issue = [&](int i) {  // lane 0: the stage of group u0 + i
+        if (i >= n)
             return;
-        issued_upto = i + 1 > issued_upto ? i + 1 : issued_upto;
-        const int64_t seq = seq_base + i;
-        const int slot = static_cast<int>(seq % kNS);
-        int64_t ua = u0 + i * kST;
-        const int64_t ub = ua + kST < u1 ? ua + kST : u1;
-        mbar_arrive_expect_tx(&bars[slot], static_cast<unsigned>((ub - ua) * TB));
-        uint8_t *dst = ring + slot * (kST * TB);
-        while (ua < ub) {
-            int p;
-            int64_t lt;
-            locate(ua, p, lt);
-            const int64_t pe = ua + ((p < P_r ? U_r : U_s) - lt);
-            const int64_t ue = pe < ub ? pe : ub;
-            bulk_g2s(dst, tile_src(p, lt), static_cast<unsigned>((ue - ua) * TB), &bars[slot]);
-            dst += (ue - ua) * TB;
-            ua = ue;
+        issued = i + 1;
+        const int u = u0 + i;
+        if (u == is_end) {
+            is_p += 1;
+            is_ps = is_end;
+            is_end += pair_units(is_p);
+            is_base = nx_base;
+            nx_base = is_end < u1 ? pair_base(is_p + 1) : nullptr;
         }
+        const int slot = static_cast<int>((ring_seq + i) % kNS);
+        mbar_arrive_expect_tx(&bars[slot], GB);
+        bulk_g2s(ring + slot * kStageBytes(BITS), is_base + (int64_t)(u - is_ps) * GB, GB,
+                 &bars[slot]);
     };
     if (lane == 0)
         for (int i = 0; i < kNS; ++i)
             issue(i);
 
-    // activations of (pair, group): this lane's 16 columns of its token
-    // row, and the group sums of the two output columns it accumulates
-    // the segment's pair record, read once: its column count, this lane's
-    // token row (gq) and the tokens of the lane's two output columns
+    if (PHASE == 1) {
+        // Down needs h of its pairs.  The first weight copies are already in
+        // flight; warp 0 waits until every pair the CTA's warps will read has
+        // all its gate/up strips done while the other warps sleep at a
+        // barrier (one poller per CTA).  Every warp passes both barriers
+        // whatever its state, so a timeout cannot strand a warp.
+        cta_barrier();
+        if ((threadIdx.x >> 5) == 0) {
+            int good = enabled ? 1 : 0;
+            const int64_t wa = (int64_t)blockIdx.x * kWarps;
+            int64_t wb = wa + kWarps - 1;
+            if (wb > W - 1)
+                wb = W - 1;
+            if (good && wa < W) {
+                const int pa = pair_of(static_cast<int>(wa * U / W));
+                const int pb = pair_of(static_cast<int>((wb + 1) * U / W) - 1);
+                for (int p = pa; p <= pb && good; ++p) {
+                    const int fp = p < P_r ? a.f : a.fs;
+                    good = warp_wait_geq(a.pair_done + p, static_cast<unsigned>(fp / kTileRows),
+                                         a.status)
+                               ? 1
+                               : 0;
+                }
+            }
+            if (lane == 0)
+                *s_ok = good;
+        }
+        cta_barrier();
+        ok = *s_ok != 0;
+        if (!enabled)
+            return false;
+    }
+
+    // ---- activations of (pair, group) -------------------------------------
+    // the pair record, read once per pair: column count, this lane's token
+    // row (gq) and the tokens of the lane's two output columns
     int pi_ncols = 0, pi_tok = 0, pi_t0 = -1, pi_t1 = -1;
     auto read_pair = [&](int p) {
-        const int32_t *pr = a.pairs + p * kPairInts;
-        pi_ncols = __ldcg(pr + 1);
-        pi_tok = gq < pi_ncols ? __ldcg(pr + 2 + gq) : 0;
-        pi_t0 = 2 * tig < pi_ncols ? __ldcg(pr + 2 + 2 * tig) : -1;
-        pi_t1 = 2 * tig + 1 < pi_ncols ? __ldcg(pr + 2 + 2 * tig + 1) : -1;
+        const int32_t *pr = rv.pairs + p * kPairInts;
+        pi_ncols = pr[1];
+        pi_tok = gq < pi_ncols ? pr[2 + gq] : 0;
+        pi_t0 = 2 * tig < pi_ncols ? pr[2 + 2 * tig] : -1;
+        pi_t1 = 2 * tig + 1 < pi_ncols ? pr[2 + 2 * tig + 1] : -1;
     };
+    const int nstrip = fmax / kTileRows;
     auto load_b = [&](int p, int g, BRaw<NV> &r) {
         const bool valid = gq < pi_ncols;
         const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
         const float2 z2 = make_float2(0.f, 0.f);
-        if (phase == 0) {
-            const int tok = pi_tok;
+        if (PHASE == 0) {
             if (XBF16) {
                 const uint4 *row = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const uint16_t *>(a.x) + (int64_t)tok * d + g * kGroup + 16 * tig);
+                    reinterpret_cast<const uint16_t *>(a.x) + (int64_t)pi_tok * d + g * kGroup + 16 * tig);
                 r.v[0] = valid ? __ldg(row) : z4;
                 r.v[1] = valid ? __ldg(row + 1) : z4;
             } else {
                 const uint4 *row = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const float *>(a.x) + (int64_t)tok * d + g * kGroup + 16 * tig);
+                    reinterpret_cast<const float *>(a.x) + (int64_t)pi_tok * d + g * kGroup + 16 * tig);
 #pragma unroll
                 for (int i = 0; i < NV; ++i)
                     r.v[i] = valid ? __ldg(row + i) : z4;
@@ -472,19 +524,21 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
             r.v[1] = valid ? __ldcg(hi + 1) : z4;
             r.v[2] = valid ? __ldcg(lo) : z4;
             r.v[3] = valid ? __ldcg(lo + 1) : z4;
+            // group sums of h: lane (gq, tig) loads strip 4g + (gq & 3) of its
+            // two columns; cook_b adds the four strips with shuffles
             const int c0 = 2 * tig, c1 = c0 + 1;
-            const float2 *hs = reinterpret_cast<const float2 *>(a.hsum);
-            const int64_t base = (int64_t)p * kPairCols * (fmax / kGroup);
-            r.xs0 = c0 < pi_ncols ? __ldcg(hs + base + (int64_t)c0 * (fmax / kGroup) + g) : z2;
-            r.xs1 = c1 < pi_ncols ? __ldcg(hs + base + (int64_t)c1 * (fmax / kGroup) + g) : z2;
+            const float2 *hp = reinterpret_cast<const float2 *>(a.hs_part);
+            const int st = 4 * g + (gq & 3);
+            r.xs0 = c0 < pi_ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c0) * nstrip + st) : z2;
+            r.xs1 = c1 < pi_ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c1) * nstrip + st) : z2;
         }
     };
     // B fragments for the mma from a BRaw
     uint32_t b0[4], b1[4], b0l[4], b1l[4];
     float bias0 = 0.f, bias1 = 0.f;
-    const bool split = phase == 1 || !XBF16;
     auto cook_b = [&](const BRaw<NV> &r) {
-        if (phase == 1) {
+        float2 x0 = r.xs0, x1 = r.xs1;
+        if (PHASE == 1) {
             const uint32_t *hv = reinterpret_cast<const uint32_t *>(r.v);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -492,6 +546,13 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
                 b1[j] = hv[2 * j + 1];
                 b0l[j] = hv[8 + 2 * j];
                 b1l[j] = hv[8 + 2 * j + 1];
+            }
+#pragma unroll
+            for (int o = 4; o <= 8; o <<= 1) {
+                x0.x += __shfl_xor_sync(0xffffffffu, x0.x, o);
+                x0.y += __shfl_xor_sync(0xffffffffu, x0.y, o);
+                x1.x += __shfl_xor_sync(0xffffffffu, x1.x, o);
+                x1.y += __shfl_xor_sync(0xffffffffu, x1.y, o);
             }
         } else if (!XBF16) {
             const float *xv = reinterpret_cast<const float *>(r.v);
@@ -513,13 +574,14 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 b1[j] = bf16x2_quarter(b1[j]);
-                b1l[j] = bf16x2_quarter(b1l[j]);
+                if (kSplit)
+                    b1l[j] = bf16x2_quarter(b1l[j]);
             }
-            bias0 = 129.5f * r.xs0.x + 33.5f * r.xs0.y;
-            bias1 = 129.5f * r.xs1.x + 33.5f * r.xs1.y;
+            bias0 = 129.5f * x0.x + 33.5f * x0.y;
+            bias1 = 129.5f * x1.x + 33.5f * x1.y;
         } else {
-            bias0 = 135.5f * (r.xs0.x + r.xs0.y);
-            bias1 = 135.5f * (r.xs1.x + r.xs1.y);
+            bias0 = 135.5f * (x0.x + x0.y);
+            bias1 = 135.5f * (x1.x + x1.y);
         }
     };
 
@@ -527,7 +589,9 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
     auto mac_tile = [&](const uint8_t *tile, float (&acc)[4]) {
         const uint32_t sc = *reinterpret_cast<const uint32_t *>(tile + CB + 4 * gq);
         const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
+        // two independent accumulation chains (k-subtiles 0,2 and 1,3)
         float dv[4] = {-bias0, -bias1, -bias0, -bias1};
+        float dw[4] = {0.f, 0.f, 0.f, 0.f};
         if (BITS == 4) {
             const uint4 cw = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
             const uint32_t q4[4] = {cw.x, cw.y, cw.z, cw.w};
@@ -539,9 +603,10 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
                 A[1] = ((q >> 4) & 0x000F000Fu) | 0x43004300u;
                 A[2] = ((q >> 8) & 0x000F000Fu) | 0x43004300u;
                 A[3] = ((q >> 12) & 0x000F000Fu) | 0x43004300u;
-                mma_bf16(dv, A, b0[j], b1[j]);
-                if (split)
-                    mma_bf16(dv, A, b0l[j], b1l[j]);
+                float(&dd)[4] = (j & 1) ? dw : dv;
+                mma_bf16(dd, A, b0[j], b1[j]);
+                if (kSplit)
+                    mma_bf16(dd, A, b0l[j], b1l[j]);
             }
         } else {
             const uint2 cw = *reinterpret_cast<const uint2 *>(tile + 8 * lane);
@@ -555,11 +620,15 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
                 A[1] = ((q >> v1) & 0x00030003u) | 0x43004300u;
                 A[2] = ((q >> v0) & 0x000C000Cu) | 0x43004300u;
                 A[3] = ((q >> v1) & 0x000C000Cu) | 0x43004300u;
-                mma_bf16(dv, A, b0[j], b1[j]);
-                if (split)
-                    mma_bf16(dv, A, b0l[j], b1l[j]);
+                float(&dd)[4] = (j & 1) ? dw : dv;
+                mma_bf16(dd, A, b0[j], b1[j]);
+                if (kSplit)
+                    mma_bf16(dd, A, b0l[j], b1l[j]);
             }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            dv[e] += dw[e];
         acc[0] = fmaf(s01.x, dv[0], acc[0]);
         acc[1] = fmaf(s01.x, dv[1], acc[1]);
         acc[2] = fmaf(s01.y, dv[2], acc[2]);
@@ -568,12 +637,10 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
 
     // ---- strip finalisation -------------------------------------------
     auto finalize = [&](int p, int s, const float (&ag)[4], const float (&au)[4]) {
-        const int32_t *pr = a.pairs + p * kPairInts;
-        const int ncols = __ldcg(pr + 1);
+        const int ncols = rv.pairs[p * kPairInts + 1];
         const float invL = 1.0f / L;
         const int c0 = 2 * tig;
-        if (phase == 0) {
-            const int fp = p < P_r ? a.f : a.fs;
+        if (PHASE == 0) {
             float hs[2] = {0.f, 0.f};  // per output column, this lane's rows
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -599,40 +666,16 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
             }
             if ((gq & 5) == 0) {
                 const int cls = (gq >> 1) & 1;
-                const int nstrip = fmax / kTileRows;
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
                     if (c0 + c < ncols)
                         a.hs_part[(((int64_t)p * kPairCols + c0 + c) * nstrip + s) * 2 + cls] = hs[c];
             }
+            // the down phase polls this count until all strips of the pair are in
             __threadfence();
             __syncwarp();
-            unsigned old = 0;
             if (lane == 0)
-                old = atom_add_acqrel(a.pair_done + p, 1u);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == static_cast<unsigned>(fp / kTileRows - 1)) {
-                // this strip completes the pair: group sums for the down phase
-                __threadfence();
-                const int ng = fp / kGroup, nstrip = fmax / kTileRows;
-                for (int i = lane; i < ncols * ng; i += 32) {
-                    const int col = i / ng, g = i % ng;
-                    const float *src =
-                        a.hs_part + (((int64_t)p * kPairCols + col) * nstrip + 4 * g) * 2;
-                    float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        x0 += __ldcg(src + 2 * q);
-                        x1 += __ldcg(src + 2 * q + 1);
-                    }
-                    reinterpret_cast<float2 *>(a.hsum)[((int64_t)p * kPairCols + col) * (fmax / kGroup) + g] =
-                        make_float2(x0, x1);
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    st_release(a.pair_ready + p, 1u);
-            }
+                atom_add_acqrel(a.pair_done + p, 1u);
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -657,12 +700,12 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
                     const int t = i / kTileRows, row = 16 * s + i % kTileRows;
                     float yv = 0.f;
                     for (int j = 0; j < kk; ++j) {
-                        const int rm = __ldcg(a.route_map + t * (kk + 1) + j);
-                        yv = fmaf(__ldcg(a.weights + t * kk + j), __ldcg(a.o + (int64_t)rm * d + row), yv);
+                        const int rm = rv.route_map[t * (kk + 1) + j];
+                        yv = fmaf(rv.weights[t * kk + j], __ldcg(a.o + (int64_t)rm * d + row), yv);
                     }
                     if (has_sh) {
-                        const int rm = __ldcg(a.route_map + t * (kk + 1) + kk);
-                        yv = fmaf(__ldcg(a.shared_w + t), __ldcg(a.o + (int64_t)rm * d + row), yv);
+                        const int rm = rv.route_map[t * (kk + 1) + kk];
+                        yv = fmaf(rv.shared_w[t], __ldcg(a.o + (int64_t)rm * d + row), yv);
                     }
                     a.y[(int64_t)t * d + row] = yv;
                 }
@@ -673,9 +716,8 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
         }
     };
 
-    // flush strip (p, s) covering global tiles [ss, se)
-    auto flush = [&](int p, int s, int64_t ss, int64_t se, const float (&ag)[4],
-                     const float (&au)[4]) {
+    // flush strip (p, s) covering groups [ss, se)
+    auto flush = [&](int p, int s, int ss, int se, const float (&ag)[4], const float (&au)[4]) {
         const int64_t wf = warp_of(ss, W, U), wl = warp_of(se - 1, W, U);
         if (wf == wl) {
             finalize(p, s, ag, au);
@@ -684,11 +726,11 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
         const int myslot = u0 >= ss ? 0 : 1;
         float4 *mine = reinterpret_cast<float4 *>(a.partial) + ((w * 2 + myslot) * 2) * 32;
         mine[lane] = make_float4(ag[0], ag[1], ag[2], ag[3]);
-        mine[32 + lane] = make_float4(au[0], au[1], au[2], au[3]);
+        if (PHASE == 0)
+            mine[32 + lane] = make_float4(au[0], au[1], au[2], au[3]);
         __threadfence();
         __syncwarp();
-        unsigned *ctr = (phase == 0 ? a.strip_ctr_g : a.strip_ctr_d) +
-                        (int64_t)p * a.max_strips + s;
+        unsigned *ctr = (PHASE == 0 ? a.strip_ctr_g : a.strip_ctr_d) + (int64_t)p * a.max_strips + s;
         unsigned old = 0;
         if (lane == 0)
             old = atom_add_acqrel(ctr, 1u);
@@ -702,19 +744,19 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int64_t ww = w0 + q;
+                vg[q] = vu[q] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (ww <= wl) {
                     const int sl = ww * U / W >= ss ? 0 : 1;
                     const float4 *src = reinterpret_cast<const float4 *>(a.partial) + ((ww * 2 + sl) * 2) * 32;
                     vg[q] = __ldcg(src + lane);
-                    vu[q] = phase == 0 ? __ldcg(src + 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (PHASE == 0)
+                        vu[q] = __ldcg(src + 32 + lane);
                 }
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                if (w0 + q <= wl) {
-                    tg[0] += vg[q].x, tg[1] += vg[q].y, tg[2] += vg[q].z, tg[3] += vg[q].w;
-                    tu[0] += vu[q].x, tu[1] += vu[q].y, tu[2] += vu[q].z, tu[3] += vu[q].w;
-                }
+                tg[0] += vg[q].x, tg[1] += vg[q].y, tg[2] += vg[q].z, tg[3] += vg[q].w;
+                tu[0] += vu[q].x, tu[1] += vu[q].y, tu[2] += vu[q].z, tu[3] += vu[q].w;
             }
         }
         if (lane == 0)
@@ -723,66 +765,51 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
     };
 
     // ---- main loop over (pair, strip) segments ------------------------
-    int waited_p = -1;
-    int64_t u = u0;
+    int cp = active ? pair_of(u0) : 0;
+    int cps = pair_start(cp), cpe = cps + pair_units(cp);
+    int pair_read = -1;
+    int u = u0;
+    int i = 0;  // stage (group) index within this phase
     BRaw<NV> rA, rB, rC;
 #pragma unroll 1
-    while (u < u1) {
-        int p;
-        int64_t lt;
-        locate(u, p, lt);
-        const int tps = p < P_r ? tps_r : tps_s;
-        const int s = static_cast<int>(lt / tps);
-        const int pos0 = static_cast<int>(lt - (int64_t)s * tps);
-        const int64_t ss = u - pos0, se = ss + tps;
-        const int64_t ue = se < u1 ? se : u1;
-        const int pos1 = static_cast<int>(pos0 + (ue - u));
-        if (phase == 1 && p != waited_p) {
-            if (!warp_wait_geq(a.pair_ready + p, 1u, a.status)) {
-                ok = false;
-                break;
-            }
-            waited_p = p;
+    while (u < u1 && ok) {
+        if (u >= cpe) {
+            cp += 1;
+            cps = cpe;
+            cpe += pair_units(cp);
         }
-        read_pair(p);
-        // groups of this segment: phase 0 has 2 tiles (gate, up) per group
-        const int tpg = phase == 0 ? 2 : 1;
-        const int g0 = pos0 / tpg, g1 = (pos1 - 1) / tpg + 1;
+        const int p = cp;
+        const int lt = u - cps;
+        const int gps = p < P_r ? gps_r : gps_s;
+        const int s = lt / gps;
+        const int g0 = lt - s * gps;
+        const int ss = u - g0, se = ss + gps;
+        const int ue = se < u1 ? se : u1;
+        const int g1 = g0 + (ue - u);
+        if (p != pair_read) {
+            read_pair(p);
+            pair_read = p;
+        }
         float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
         auto do_group = [&](const BRaw<NV> &cur, BRaw<NV> &fill, int g) {
             if (g + 2 < g1)
                 load_b(p, g + 2, fill);
             cook_b(cur);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (h >= tpg)
-                    break;
-                const int pos = g * tpg + h;
-                if (pos < pos0 || pos >= pos1)
-                    continue;
-                const int64_t uu = ss + pos;
-                const int64_t i = (uu - u0) / kST;
-                const int within = static_cast<int>((uu - u0) - i * kST);
-                const int64_t seq = seq_base + i;
-                const int slot = static_cast<int>(seq % kNS);
-                if (within == 0) {
-                    if (!mbar_wait_bounded(&bars[slot], static_cast<unsigned>((seq / kNS) & 1))) {
-                        ok = false;
-                        return;
-                    }
-                    waited_upto = i + 1;
-                }
-                const uint8_t *tile = ring + slot * (kST * TB) + within * TB;
-                if (h == 0)
-                    mac_tile(tile, ag);
-                else
-                    mac_tile(tile, au);
-                if (within == kST - 1 || uu == u1 - 1) {
-                    __syncwarp();
-                    if (lane == 0)
-                        issue(i + kNS);
-                }
+            const uint32_t seq = ring_seq + static_cast<uint32_t>(i);
+            const int slot = static_cast<int>(seq % kNS);
+            if (!mbar_wait_bounded(&bars[slot], (seq / kNS) & 1u)) {
+                ok = false;
+                return;
             }
+            waited = i + 1;
+            const uint8_t *st = ring + slot * kStageBytes(BITS);
+            mac_tile(st, ag);
+            if (PHASE == 0)
+                mac_tile(st + TB, au);
+            __syncwarp();
+            if (lane == 0)
+                issue(i + kNS);
+            ++i;
         };
         load_b(p, g0, rA);
         if (g0 + 1 < g1)
@@ -804,15 +831,15 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
         if (lane == 0) {
             set_status(a.status, kStatusTimeout);
             // drain this warp's copies still in flight (bounded)
-            for (int64_t i = waited_upto; i < issued_upto; ++i) {
-                const int64_t seq = seq_base + i;
-                (void)mbar_wait_bounded(&bars[seq % kNS], static_cast<unsigned>((seq / kNS) & 1));
+            for (int j = waited; j < issued; ++j) {
+                const uint32_t seq = ring_seq + static_cast<uint32_t>(j);
+                (void)mbar_wait_bounded(&bars[seq % kNS], (seq / kNS) & 1u);
             }
         }
         __syncwarp();
         return false;
     }
-    seq_base += nst;
+    ring_seq += static_cast<uint32_t>(n);
     return true;
 }
 
@@ -830,11 +857,15 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs 
     }
     __syncwarp();
 
+    __shared__ int s_ok;
     const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
     const int64_t Wall = (int64_t)gridDim.x * kWarps;
     bool ok = true;
 
     // ------------------------------------------------------------ phase R
+    __shared__ RouteSmem rs;
+    RouteView rv;
+    int P_r = 0, P_t = 0;
     if (a.do_route) {
         const int rows = a.E + (a.shared_gate ? 1 : 0);
         const int units = rows + static_cast<int>(a.T);
@@ -844,32 +875,68 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs 
             router_unit<XBF16>(a, static_cast<int>(unit));
             __threadfence();
             __syncwarp();
-            unsigned old = 0;
             if (lane == 0)
-                old = atom_add_acqrel(a.route_ctr, 1u);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == static_cast<unsigned>(units - 1)) {
-                __threadfence();
-                route_and_dispatch(a);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    st_release(a.route_flag, 1u);
-            }
+                atom_add_acqrel(a.route_ctr, 1u);
         }
-        ok = warp_wait_geq(a.route_flag, 1u, a.status);
+        // one poller per CTA waits for every router unit; the others sleep
+        cta_barrier();
+        if (warp == 0) {
+            const int good = warp_wait_geq(a.route_ctr, static_cast<unsigned>(units), a.status) ? 1 : 0;
+            if (lane == 0)
+                s_ok = good;
+        }
+        cta_barrier();
+        ok = s_ok != 0;
+        // route the tokens (one warp each), then warp 0 builds the pair table
+        if (ok && warp < a.T) {
+            const bool out = blockIdx.x == 0;
+            const int t = warp;
+            route_one_token(a.logits + (int64_t)t * a.Epad, a.E, a.k, a.norm, a.expert_bias,
+                            rs.ids + t * a.k, rs.weights + t * a.k, out ? a.ids + t * a.k : nullptr,
+                            out ? a.weights + t * a.k : nullptr, a.status);
+            __syncwarp();
+            if (out) {
+                if (a.ids_out && lane < a.k)
+                    a.ids_out[t * a.k + lane] = rs.ids[t * a.k + lane];
+                if (a.w_out && lane < a.k)
+                    a.w_out[t * a.k + lane] = rs.weights[t * a.k + lane];
+            }
+            if (lane == 0)
+                rs.shared_w[t] =
+                    a.shared_gate ? 1.0f / (1.0f + expf(-__ldcg(a.logits + (int64_t)t * a.Epad + a.E)))
+                                  : 1.0f;
+        }
+        cta_barrier();
+        if (ok && warp == 0)
+            cta_dispatch(a, rs);
+        cta_barrier();
+        rv.pairs = &rs.pairs[0][0];
+        rv.route_map = rs.route_map;
+        rv.weights = rs.weights;
+        rv.shared_w = rs.shared_w;
+        if (ok) {
+            P_r = rs.meta[0];
+            P_t = rs.meta[1];
+        }
+    } else {
+        rv.pairs = a.pairs;
+        rv.route_map = a.route_map;
+        rv.weights = a.weights;
+        rv.shared_w = a.shared_w;
+        P_r = __ldcg(a.meta + 0);
+        P_t = __ldcg(a.meta + 1);
     }
-
-    const int P_r = ok ? __ldcg(a.meta + 0) : 0;
-    const int P_t = ok ? __ldcg(a.meta + 1) : 0;
     const int fmax = a.f > a.fs ? a.f : a.fs;
 
     // ------------------------------------------------------------ phases G, D
-    int64_t seq_base = 0;  // ring stages issued (and consumed) by earlier phases
+    // Phase D runs in every warp (it holds CTA barriers); a warp that failed
+    // earlier passes it with no work.
+    uint32_t ring_seq = 0;  // ring stages issued (and consumed) by earlier phases
     if (ok)
-        ok = run_phase<BITS, XBF16, 0>(a, ring, bars, seq_base, P_r, P_t, fmax, w, Wall);
-    if (ok)
-        ok = run_phase<BITS, XBF16, 1>(a, ring, bars, seq_base, P_r, P_t, fmax, w, Wall);
+        ok = run_phase<BITS, XBF16, 0>(a, ring, bars, ring_seq, P_r, P_t, fmax, w, Wall, true,
+                                       &s_ok, rv);
+    ok = run_phase<BITS, XBF16, 1>(a, ring, bars, ring_seq, P_r, P_t, fmax, w, Wall, ok, &s_ok,
+                                   rv);
 
     // ------------------------------------------------------------ exit: the
     // last warp out resets the flags (counters of strips reset themselves)
@@ -880,13 +947,10 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs 
         old = atom_add_acqrel(a.exit_ctr, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
     if (old == static_cast<unsigned>(Wall - 1)) {
-        for (int p = lane; p < a.max_pairs; p += 32) {
+        for (int p = lane; p < a.max_pairs; p += 32)
             a.pair_done[p] = 0u;
-            a.pair_ready[p] = 0u;
-        }
         if (lane == 0) {
             *a.route_ctr = 0u;
-            *a.route_flag = 0u;
             __threadfence();
             *a.exit_ctr = 0u;
         }

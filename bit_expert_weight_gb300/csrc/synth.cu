@@ -9,7 +9,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/smoe_synth.h"
+#include "smoe_synth.h"
 
 namespace {
 
