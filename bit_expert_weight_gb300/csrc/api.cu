@@ -132,7 +132,7 @@ struct Plan {
     int64_t T;
     int ntiles, ksplit, Epad, max_pairs, fmax, warps, max_strips;
     size_t off_ctr_tile, off_ctr_done, off_ctr_sg, off_ctr_sd, off_ctr_comb, off_pair_done,
-        off_flags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w, off_sw, off_pairs,
+        off_flags, off_ctaflags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w, off_sw, off_pairs,
         off_rmap, off_hhi, off_hlo, off_hspart, off_o, off_part, total;
 };
 
@@ -175,6 +175,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_ctr_comb = take(sizeof(unsigned) * (d / 16));
     p.off_pair_done = take(sizeof(unsigned) * p.max_pairs);
     p.off_flags = take(sizeof(unsigned) * 4);
+    p.off_ctaflags = take(sizeof(unsigned) * 32 * (size_t)device_sm_count() * kMaxLayerCtasPerSm);
     p.off_meta = take(sizeof(int32_t) * 2);
     p.off_plog = take(sizeof(float) * p.ksplit * T * p.Epad);
     p.off_logits = take(sizeof(float) * T * p.Epad);
@@ -481,6 +482,7 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     unsigned *flags = at<unsigned>(workspace, P.off_flags);
     la.route_ctr = flags + 0;
     la.exit_ctr = flags + 1;
+    la.cta_flags = at<unsigned>(workspace, P.off_ctaflags);
     la.y = y;
     la.status = status;
 

@@ -109,6 +109,7 @@ struct LayerArgs {
     unsigned *comb_ctr;            // [d/16]
     unsigned *pair_done;           // [max_pairs] finished gate/up strips
     unsigned *route_ctr, *exit_ctr;
+    unsigned *cta_flags;           // [max CTAs][32]: word 0 route go, word 1 pairs ready
     float *y;                      // [T, d]
     int *status;
 };

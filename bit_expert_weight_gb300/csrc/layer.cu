@@ -61,6 +61,23 @@ __device__ __forceinline__ unsigned atom_add_acqrel(unsigned *p, unsigned v)
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+// Release/acquire fence at GPU scope: orders this thread's (and, through the
+// preceding __syncwarp, its warp's) writes before a following signal, or a
+// signal observed before the following reads.
+__device__ __forceinline__ void fence_acq_rel()
+{
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+// Relaxed fire-and-forget add / store: after one release fence these
+// pipeline, where a chain of acq_rel atomics would serialise.
+__device__ __forceinline__ void red_add_relaxed(unsigned *p, unsigned v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed(unsigned *p, unsigned v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 {
     unsigned v;
@@ -98,16 +115,39 @@ __device__ __forceinline__ void cta_barrier()
     asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
-__device__ __forceinline__ int64_t warp_of(int64_t u, int64_t W, int64_t U)
+// Stream-K split of U units over W warps: warp w owns [start(w), start(w+1))
+// with start(w) = floor(w * U / W), evaluated exactly in 32 bits as
+// w*q + (w*r)/W with q = U / W, r = U % W (W < 2^13 keeps w*r < 2^26).
+struct Split {
+    int U, W, q, r;
+};
+__device__ __forceinline__ Split make_split(int U, int W)
 {
-    return ((u + 1) * W - 1) / U;
+    Split sp;
+    sp.U = U;
+    sp.W = W;
+    sp.q = W > 0 ? U / W : 0;
+    sp.r = W > 0 ? U - sp.q * W : 0;
+    return sp;
+}
+__device__ __forceinline__ int split_start(const Split &sp, int w) { return w * sp.q + (w * sp.r) / sp.W; }
+// The warp whose range holds unit u: a float estimate corrected to exact.
+__device__ __forceinline__ int split_owner(const Split &sp, int u)
+{
+    int w = static_cast<int>((static_cast<float>(u) + 0.5f) * (static_cast<float>(sp.W) / static_cast<float>(sp.U)));
+    w = w < 0 ? 0 : (w >= sp.W ? sp.W - 1 : w);
+    while (w > 0 && split_start(sp, w) > u)
+        --w;
+    while (w + 1 < sp.W && split_start(sp, w + 1) <= u)
+        ++w;
+    return w;
 }
 
 // --------------------------------------------------------------- routing
 
 constexpr int kPerLane = kMaxExperts / 32;
 
-__device__ void route_one_token(const float *lg, int E, int k, int norm, const float *bias,
+__device__ __noinline__ void route_one_token(const float *lg, int E, int k, int norm, const float *bias,
                                 int16_t *ids_s, float *w_s, int32_t *ids_g, float *w_g,
                                 int *status)
 {
@@ -192,66 +232,64 @@ __device__ void route_one_token(const float *lg, int E, int k, int norm, const f
 // Phase R work of one warp: unit < E (+1 shared gate row) -> logits of that
 // row for all tokens; unit >= rows -> group sums of token (unit - rows).
 template <bool XBF16>
-__device__ void router_unit(const LayerArgs &a, int unit)
+__device__ __noinline__ void router_unit(const LayerArgs &a, int unit)
 {
     const int lane = threadIdx.x & 31;
     const int d = a.d, T = static_cast<int>(a.T);
     const int rows = a.E + (a.shared_gate ? 1 : 0);
     if (unit < rows) {
         const uint16_t *wr = unit < a.E ? a.router_w + (int64_t)unit * d : a.shared_gate;
-        float acc[kPairCols];
-#pragma unroll
-        for (int t = 0; t < kPairCols; ++t)
-            acc[t] = 0.f;
-        // four 256-column slices per batch: all loads of a batch in flight
-        for (int c0 = lane * 8; c0 < d; c0 += 1024) {
-            uint4 wv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                wv[i] = c0 + 256 * i < d ? __ldg(reinterpret_cast<const uint4 *>(wr + c0 + 256 * i))
-                                         : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int t = 0; t < kPairCols; ++t) {
-                if (t >= T)
-                    break;
+        // per token: four 256-column slices per batch, all loads in flight
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            float acc = 0.f;
+#pragma unroll 1
+            for (int c0 = lane * 8; c0 < d; c0 += 1024) {
+                uint4 wv[4], xv[4], xw[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int c = c0 + 256 * i;
-                    if (c >= d)
-                        break;
+                    const bool in = c < d;
+                    wv[i] = in ? __ldg(reinterpret_cast<const uint4 *>(wr + c)) : make_uint4(0u, 0u, 0u, 0u);
+                    if (XBF16) {
+                        xv[i] = in ? __ldg(reinterpret_cast<const uint4 *>(
+                                         reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + c))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+                        const uint4 *xr = reinterpret_cast<const uint4 *>(
+                            reinterpret_cast<const float *>(a.x) + (int64_t)t * d + c);
+                        xv[i] = in ? __ldg(xr) : make_uint4(0u, 0u, 0u, 0u);
+                        xw[i] = in ? __ldg(xr + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
                     const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
                     float xf[8];
                     if (XBF16) {
-                        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(
-                            reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + c));
-                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+                        const uint32_t xx[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             xf[2 * q] = bf16lo_to_f32(xx[q]);
                             xf[2 * q + 1] = bf16hi_to_f32(xx[q]);
                         }
                     } else {
-                        const float *xr = reinterpret_cast<const float *>(a.x) + (int64_t)t * d + c;
-                        const float4 x0 = __ldg(reinterpret_cast<const float4 *>(xr));
-                        const float4 x1 = __ldg(reinterpret_cast<const float4 *>(xr) + 1);
-                        xf[0] = x0.x, xf[1] = x0.y, xf[2] = x0.z, xf[3] = x0.w;
-                        xf[4] = x1.x, xf[5] = x1.y, xf[6] = x1.z, xf[7] = x1.w;
+                        xf[0] = __uint_as_float(xv[i].x), xf[1] = __uint_as_float(xv[i].y);
+                        xf[2] = __uint_as_float(xv[i].z), xf[3] = __uint_as_float(xv[i].w);
+                        xf[4] = __uint_as_float(xw[i].x), xf[5] = __uint_as_float(xw[i].y);
+                        xf[6] = __uint_as_float(xw[i].z), xf[7] = __uint_as_float(xw[i].w);
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        acc[t] = fmaf(bf16lo_to_f32(ww[q]), xf[2 * q], acc[t]);
-                        acc[t] = fmaf(bf16hi_to_f32(ww[q]), xf[2 * q + 1], acc[t]);
+                        acc = fmaf(bf16lo_to_f32(ww[q]), xf[2 * q], acc);
+                        acc = fmaf(bf16hi_to_f32(ww[q]), xf[2 * q + 1], acc);
                     }
                 }
             }
-        }
-#pragma unroll
-        for (int t = 0; t < kPairCols; ++t) {
-            float v = acc[t];
             for (int o = 16; o; o >>= 1)
-                v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0 && t < T)
-                a.logits[(int64_t)t * a.Epad + unit] = v;
+                acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0)
+                a.logits[(int64_t)t * a.Epad + unit] = acc;
         }
     } else {
         // group sums of token t: X0 over columns c % 4 in {0,1}, X1 over {2,3}
@@ -316,7 +354,7 @@ struct RouteView {
 // Warp 0 of the CTA: pair table from the routed ids (T <= 8).  Pair = one
 // selected expert with the ascending tokens that chose it, pairs in order of
 // first appearance; then the shared expert's pair.
-__device__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
+__device__ __noinline__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
 {
     const int lane = threadIdx.x & 31;
     const int T = static_cast<int>(a.T), k = a.k, E = a.E;
@@ -364,6 +402,18 @@ __device__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
     __syncwarp();
 }
 
+// ------------------------------------------------------------ streaming
+
+// Per-warp constants of one phase (passed by value to the cold helpers).
+struct Phase {
+    int P_r, P_t, fmax, nstrip;  // pairs, widest f, strips of fmax
+    int U_r, U_s, UR, U, W;      // groups per routed / shared pair, totals, warps
+    Split sp;                    // the stream-K split of U over W
+    int u0, u1;                  // this warp's group range
+    int gps_r, gps_s;            // groups per strip
+    long long w;                 // global warp index
+};
+
 // This lane's 16 activations of one group (bf16 x: 2 vectors; fp32 x: 4;
 // h of the down phase: hi in v[0..1], lo in v[2..3]) and the group sums
 // (X0, X1) of the two output columns the lane accumulates.
@@ -372,6 +422,353 @@ struct BRaw {
     uint4 v[NV];
     float2 xs0, xs1;
 };
+
+// The lane's view of a pair record: column count, its token row (gq) and
+// the tokens of its two output columns.
+struct PairInfo {
+    int ncols, tok, t0, t1;
+};
+
+__device__ __forceinline__ PairInfo read_pair(const RouteView &rv, int p)
+{
+    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const int32_t *pr = rv.pairs + p * kPairInts;
+    PairInfo pi;
+    pi.ncols = pr[1];
+    pi.tok = gq < pi.ncols ? pr[2 + gq] : 0;
+    pi.t0 = 2 * tig < pi.ncols ? pr[2 + 2 * tig] : -1;
+    pi.t1 = 2 * tig + 1 < pi.ncols ? pr[2 + 2 * tig + 1] : -1;
+    return pi;
+}
+
+template <int PHASE, bool XBF16, int NV>
+__device__ __forceinline__ void load_b(const LayerArgs &a, const PairInfo &pi, int p, int g,
+                                       int fmax, int nstrip, BRaw<NV> &r)
+{
+    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const int d = a.d;
+    const bool valid = gq < pi.ncols;
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    const float2 z2 = make_float2(0.f, 0.f);
+    if (PHASE == 0) {
+        if (XBF16) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const uint16_t *>(a.x) + (int64_t)pi.tok * d + g * kGroup + 16 * tig);
+            r.v[0] = valid ? __ldg(row) : z4;
+            r.v[1] = valid ? __ldg(row + 1) : z4;
+        } else {
+            const uint4 *row = reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const float *>(a.x) + (int64_t)pi.tok * d + g * kGroup + 16 * tig);
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                r.v[i] = valid ? __ldg(row + i) : z4;
+        }
+        const float2 *xs = reinterpret_cast<const float2 *>(a.xsum);
+        r.xs0 = pi.t0 >= 0 ? __ldcg(xs + (int64_t)pi.t0 * (d / kGroup) + g) : z2;
+        r.xs1 = pi.t1 >= 0 ? __ldcg(xs + (int64_t)pi.t1 * (d / kGroup) + g) : z2;
+    } else {
+        const int64_t off = ((int64_t)p * kPairCols + gq) * fmax + g * kGroup + 16 * tig;
+        const uint4 *hi = reinterpret_cast<const uint4 *>(a.h_hi + off);
+        const uint4 *lo = reinterpret_cast<const uint4 *>(a.h_lo + off);
+        r.v[0] = valid ? __ldcg(hi) : z4;
+        r.v[1] = valid ? __ldcg(hi + 1) : z4;
+        r.v[2] = valid ? __ldcg(lo) : z4;
+        r.v[3] = valid ? __ldcg(lo + 1) : z4;
+        // group sums of h: lane (gq, tig) loads strip 4g + (gq & 3) of its two
+        // columns; cook_b adds the four strips with shuffles
+        const int c0 = 2 * tig, c1 = c0 + 1;
+        const float2 *hp = reinterpret_cast<const float2 *>(a.hs_part);
+        const int st = 4 * g + (gq & 3);
+        r.xs0 = c0 < pi.ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c0) * nstrip + st) : z2;
+        r.xs1 = c1 < pi.ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c1) * nstrip + st) : z2;
+    }
+}
+
+// mma B fragments (hi and, for fp32 / h activations, lo) and the two column
+// biases -(128 + L) X (Q2: -(129.5 X0 + 33.5 X1)) from a BRaw
+struct BFrag {
+    uint32_t b0[4], b1[4], b0l[4], b1l[4];
+    float bias0, bias1;
+};
+
+template <int BITS, int PHASE, bool XBF16, int NV>
+__device__ __forceinline__ void cook_b(const BRaw<NV> &r, BFrag &f)
+{
+    float2 x0 = r.xs0, x1 = r.xs1;
+    if (PHASE == 1) {
+        const uint32_t *hv = reinterpret_cast<const uint32_t *>(r.v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f.b0[j] = hv[2 * j];
+            f.b1[j] = hv[2 * j + 1];
+            f.b0l[j] = hv[8 + 2 * j];
+            f.b1l[j] = hv[8 + 2 * j + 1];
+        }
+#pragma unroll
+        for (int o = 4; o <= 8; o <<= 1) {
+            x0.x += __shfl_xor_sync(0xffffffffu, x0.x, o);
+            x0.y += __shfl_xor_sync(0xffffffffu, x0.y, o);
+            x1.x += __shfl_xor_sync(0xffffffffu, x1.x, o);
+            x1.y += __shfl_xor_sync(0xffffffffu, x1.y, o);
+        }
+    } else if (!XBF16) {
+        const float *xv = reinterpret_cast<const float *>(r.v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            split_bf16x2(xv[4 * j + 0], xv[4 * j + 1], f.b0[j], f.b0l[j]);
+            split_bf16x2(xv[4 * j + 2], xv[4 * j + 3], f.b1[j], f.b1l[j]);
+        }
+    } else {
+        const uint32_t *xv = reinterpret_cast<const uint32_t *>(r.v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f.b0[j] = xv[2 * j];
+            f.b1[j] = xv[2 * j + 1];
+            f.b0l[j] = f.b1l[j] = 0u;
+        }
+    }
+    if (BITS == 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f.b1[j] = bf16x2_quarter(f.b1[j]);
+            f.b1l[j] = bf16x2_quarter(f.b1l[j]);
+        }
+        f.bias0 = 129.5f * x0.x + 33.5f * x0.y;
+        f.bias1 = 129.5f * x1.x + 33.5f * x1.y;
+    } else {
+        f.bias0 = 135.5f * (x0.x + x0.y);
+        f.bias1 = 135.5f * (x1.x + x1.y);
+    }
+}
+
+// Decode + multiply one tile from shared memory into acc (two independent
+// mma chains: k-subtiles 0,2 and 1,3).
+template <int BITS, bool SPLIT>
+__device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, float (&acc)[4])
+{
+    constexpr int CB = tile_code_bytes(BITS);
+    const int lane = threadIdx.x & 31, gq = lane >> 2;
+    const uint32_t sc = *reinterpret_cast<const uint32_t *>(tile + CB + 4 * gq);
+    const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
+    float dv[4] = {-f.bias0, -f.bias1, -f.bias0, -f.bias1};
+    float dw[4] = {0.f, 0.f, 0.f, 0.f};
+    if (BITS == 4) {
+        const uint4 cw = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
+        const uint32_t q4[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t q = q4[j];
+            uint32_t A[4];
+            A[0] = (q & 0x000F000Fu) | 0x43004300u;
+            A[1] = ((q >> 4) & 0x000F000Fu) | 0x43004300u;
+            A[2] = ((q >> 8) & 0x000F000Fu) | 0x43004300u;
+            A[3] = ((q >> 12) & 0x000F000Fu) | 0x43004300u;
+            float(&dd)[4] = (j & 1) ? dw : dv;
+            mma_bf16(dd, A, f.b0[j], f.b1[j]);
+            if (SPLIT)
+                mma_bf16(dd, A, f.b0l[j], f.b1l[j]);
+        }
+    } else {
+        const uint2 cw = *reinterpret_cast<const uint2 *>(tile + 8 * lane);
+        const uint32_t q2[2] = {cw.x, cw.y};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t q = q2[j >> 1];
+            const int v0 = 8 * (j & 1), v1 = v0 + 4;
+            uint32_t A[4];
+            A[0] = ((q >> v0) & 0x00030003u) | 0x43004300u;
+            A[1] = ((q >> v1) & 0x00030003u) | 0x43004300u;
+            A[2] = ((q >> v0) & 0x000C000Cu) | 0x43004300u;
+            A[3] = ((q >> v1) & 0x000C000Cu) | 0x43004300u;
+            float(&dd)[4] = (j & 1) ? dw : dv;
+            mma_bf16(dd, A, f.b0[j], f.b1[j]);
+            if (SPLIT)
+                mma_bf16(dd, A, f.b0l[j], f.b1l[j]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        dv[e] += dw[e];
+    acc[0] = fmaf(s01.x, dv[0], acc[0]);
+    acc[1] = fmaf(s01.x, dv[1], acc[1]);
+    acc[2] = fmaf(s01.y, dv[2], acc[2]);
+    acc[3] = fmaf(s01.y, dv[3], acc[3]);
+}
+
+__device__ __forceinline__ int pair_of(const Phase &ph, int u)
+{
+    return u < ph.UR ? u / ph.U_r : ph.P_r + (u - ph.UR) / ph.U_s;
+}
+__device__ __forceinline__ int pair_start(const Phase &ph, int p)
+{
+    return p < ph.P_r ? p * ph.U_r : ph.UR + (p - ph.P_r) * ph.U_s;
+}
+__device__ __forceinline__ int pair_units(const Phase &ph, int p) { return p < ph.P_r ? ph.U_r : ph.U_s; }
+
+// Finalise strip s of pair p from its full-K accumulators (cold path).
+// Phase 0: h = SiLU(g) * u stored as bf16 hi + lo, the strip's per-class
+// sums of h, the pair's strip count (the strip completing the pair wakes the
+// CTAs whose down ranges read it).  Phase 1: o, then (T <= 8) the combine of
+// output strip s by the last pair to finish it, in rank order.
+template <int BITS, int PHASE>
+__device__ __noinline__ void finalize_strip(const LayerArgs &a, const RouteView rv, const Phase ph,
+                                            int p, int s, float4 ag, float4 au)
+{
+    constexpr float L = BITS == 4 ? 7.5f : 1.5f;
+    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const int d = a.d;
+    const int ncols = rv.pairs[p * kPairInts + 1];
+    const float invL = 1.0f / L;
+    const int c0 = 2 * tig;
+    const float gv[4] = {ag.x, ag.y, ag.z, ag.w}, uv[4] = {au.x, au.y, au.z, au.w};
+    if (PHASE == 0) {
+        float hs[2] = {0.f, 0.f};  // per output column, this lane's rows
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float g = gv[e] * invL, u = uv[e] * invL;
+            const float hv = g / (1.0f + expf(-g)) * u;
+            const int col = c0 + (e & 1);
+            const int row = 16 * s + gq + 8 * (e >> 1);
+            if (col < ncols) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
+                const int64_t off = ((int64_t)p * kPairCols + col) * ph.fmax + row;
+                a.h_hi[off] = *reinterpret_cast<const uint16_t *>(&hi);
+                a.h_lo[off] = *reinterpret_cast<const uint16_t *>(&lo);
+            }
+            hs[e & 1] += hv;
+        }
+        // class of these rows within their 64-row group: (gq >> 1) & 1; sum
+        // over lanes with equal tig and class (lane bits 2 and 4)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            hs[c] += __shfl_xor_sync(0xffffffffu, hs[c], 4);
+            hs[c] += __shfl_xor_sync(0xffffffffu, hs[c], 16);
+        }
+        if ((gq & 5) == 0) {
+            const int cls = (gq >> 1) & 1;
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                if (c0 + c < ncols)
+                    a.hs_part[(((int64_t)p * kPairCols + c0 + c) * ph.nstrip + s) * 2 + cls] = hs[c];
+        }
+        fence_acq_rel();
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0)
+            old = atom_add_acqrel(a.pair_done + p, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        const int fp = p < ph.P_r ? a.f : a.fs;
+        if (old == static_cast<unsigned>(fp / kTileRows - 1)) {
+            // down-phase geometry (groups of 16 rows x 64 columns of W_down)
+            const int DU_r = (d / kTileRows) * (a.f / kGroup);
+            const int DU_s = ph.P_t > ph.P_r ? (d / kTileRows) * (a.fs / kGroup) : 0;
+            const int DUR = ph.P_r * DU_r;
+            const int DU = DUR + (ph.P_t - ph.P_r) * DU_s;
+            const int64_t Wall = (int64_t)gridDim.x * kWarps;
+            const int DW = DU < Wall ? DU : static_cast<int>(Wall);
+            const int ps = p < ph.P_r ? p * DU_r : DUR + (p - ph.P_r) * DU_s;
+            const int pe = ps + (p < ph.P_r ? DU_r : DU_s);
+            const Split dsp = make_split(DU, DW);
+            const int ca = split_owner(dsp, ps) / kWarps;
+            const int cb = split_owner(dsp, pe - 1) / kWarps;
+            fence_acq_rel();
+            for (int c = ca + lane; c <= cb; c += 32)
+                red_add_relaxed(a.cta_flags + 32 * c + 1, 1u);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int col = c0 + (e & 1);
+            const int row = 16 * s + gq + 8 * (e >> 1);
+            if (col < ncols)
+                a.o[((int64_t)p * kPairCols + col) * d + row] = gv[e] * invL;
+        }
+        if (!a.fused_combine)
+            return;
+        fence_acq_rel();
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0)
+            old = atom_add_acqrel(a.comb_ctr + s, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == static_cast<unsigned>(ph.P_t - 1)) {
+            fence_acq_rel();
+            const int T = static_cast<int>(a.T), kk = a.k;
+            const bool has_sh = ph.P_t > ph.P_r;
+            for (int i = lane; i < kTileRows * T; i += 32) {
+                const int t = i / kTileRows, row = 16 * s + i % kTileRows;
+                float yv = 0.f;
+                for (int j = 0; j < kk; ++j) {
+                    const int rm = rv.route_map[t * (kk + 1) + j];
+                    yv = fmaf(rv.weights[t * kk + j], __ldcg(a.o + (int64_t)rm * d + row), yv);
+                }
+                if (has_sh) {
+                    const int rm = rv.route_map[t * (kk + 1) + kk];
+                    yv = fmaf(rv.shared_w[t], __ldcg(a.o + (int64_t)rm * d + row), yv);
+                }
+                a.y[(int64_t)t * d + row] = yv;
+            }
+            __syncwarp();
+            if (lane == 0)
+                a.comb_ctr[s] = 0u;
+        }
+    }
+}
+
+// Flush strip (p, s) = groups [ss, se) (cold path): finalise it if this warp
+// covered all of it, else store the partial and let the last contributor
+// (arrival counter) sum the partials in warp order and finalise.
+template <int BITS, int PHASE>
+__device__ __noinline__ void flush_strip(const LayerArgs &a, const RouteView rv, const Phase ph,
+                                         int p, int s, int ss, int se, float4 ag, float4 au)
+{
+    const int lane = threadIdx.x & 31;
+    const int wf = split_owner(ph.sp, ss), wl = split_owner(ph.sp, se - 1);
+    if (wf == wl) {
+        finalize_strip<BITS, PHASE>(a, rv, ph, p, s, ag, au);
+        return;
+    }
+    const int myslot = ph.u0 >= ss ? 0 : 1;
+    float4 *mine = reinterpret_cast<float4 *>(a.partial) + ((ph.w * 2 + myslot) * 2) * 32;
+    mine[lane] = ag;
+    if (PHASE == 0)
+        mine[32 + lane] = au;
+    fence_acq_rel();
+    __syncwarp();
+    unsigned *ctr = (PHASE == 0 ? a.strip_ctr_g : a.strip_ctr_d) + (int64_t)p * a.max_strips + s;
+    unsigned old = 0;
+    if (lane == 0)
+        old = atom_add_acqrel(ctr, 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != static_cast<unsigned>(wl - wf))
+        return;
+    fence_acq_rel();
+    float4 tg = make_float4(0.f, 0.f, 0.f, 0.f), tu = tg;
+    for (int w0 = wf; w0 <= wl; w0 += 4) {
+        float4 vg[4], vu[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int ww = w0 + q;
+            vg[q] = vu[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ww <= wl) {
+                const int sl = split_start(ph.sp, ww) >= ss ? 0 : 1;
+                const float4 *src = reinterpret_cast<const float4 *>(a.partial) + ((ww * 2 + sl) * 2) * 32;
+                vg[q] = __ldcg(src + lane);
+                if (PHASE == 0)
+                    vu[q] = __ldcg(src + 32 + lane);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            tg.x += vg[q].x, tg.y += vg[q].y, tg.z += vg[q].z, tg.w += vg[q].w;
+            tu.x += vu[q].x, tu.y += vu[q].y, tu.z += vu[q].z, tu.w += vu[q].w;
+        }
+    }
+    if (lane == 0)
+        *ctr = 0u;
+    finalize_strip<BITS, PHASE>(a, rv, ph, p, s, tg, tu);
+}
 
 // One streaming phase (0: gate/up + SiLU, 1: down + combine) of one warp.
 // The unit of work is a group: 64 input columns of 16 output rows (phase 0:
@@ -386,32 +783,35 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
                                           const RouteView &rv)
 {
     constexpr int TB = tile_bytes(BITS);
-    constexpr int CB = tile_code_bytes(BITS);
-    constexpr float L = BITS == 4 ? 7.5f : 1.5f;
     constexpr int TPG = PHASE == 0 ? 2 : 1;  // tiles per group
     constexpr int GB = TPG * TB;             // bytes per group
     constexpr int NV = (PHASE == 1 || !XBF16) ? 4 : 2;
     constexpr bool kSplit = PHASE == 1 || !XBF16;
     const int lane = threadIdx.x & 31;
-    const int gq = lane >> 2, tig = lane & 3;
     const int d = a.d;
     bool ok = true;
-    const int Kr = PHASE == 0 ? d : a.f, Ks = PHASE == 0 ? d : a.fs;
-    const int Rr = PHASE == 0 ? a.f : d, Rs = PHASE == 0 ? a.fs : d;
-    const int gps_r = Kr / kGroup, gps_s = Ks / kGroup;  // groups per strip
-    // 32-bit group indices: a layer's stream is far below 2^31 groups
-    const int U_r = (Rr / kTileRows) * gps_r;             // groups per routed pair
-    const int U_s = P_t > P_r ? (Rs / kTileRows) * gps_s : 0;
-    const int UR = P_r * U_r;
-    const int U = enabled ? UR + (P_t - P_r) * U_s : 0;
-    const int W = U < Wall ? U : static_cast<int>(Wall);
-    const bool active = w < W;
-    const int u0 = active ? static_cast<int>(w * U / W) : 0;
-    const int u1 = active ? static_cast<int>((w + 1) * U / W) : 0;
-    const int n = u1 - u0;
-    auto pair_of = [&](int u) { return u < UR ? u / U_r : P_r + (u - UR) / U_s; };
-    auto pair_start = [&](int p) { return p < P_r ? p * U_r : UR + (p - P_r) * U_s; };
-    auto pair_units = [&](int p) { return p < P_r ? U_r : U_s; };
+    Phase ph;
+    ph.P_r = P_r;
+    ph.P_t = P_t;
+    ph.fmax = fmax;
+    ph.nstrip = fmax / kTileRows;
+    {
+        const int Kr = PHASE == 0 ? d : a.f, Ks = PHASE == 0 ? d : a.fs;
+        const int Rr = PHASE == 0 ? a.f : d, Rs = PHASE == 0 ? a.fs : d;
+        ph.gps_r = Kr / kGroup;
+        ph.gps_s = Ks / kGroup;
+        ph.U_r = (Rr / kTileRows) * ph.gps_r;
+        ph.U_s = P_t > P_r ? (Rs / kTileRows) * ph.gps_s : 0;
+        ph.UR = P_r * ph.U_r;
+        ph.U = enabled ? ph.UR + (P_t - P_r) * ph.U_s : 0;
+        ph.W = ph.U < Wall ? ph.U : static_cast<int>(Wall);
+        ph.w = w;
+        const bool act = w < ph.W;
+        ph.sp = make_split(ph.U, ph.W);
+        ph.u0 = act ? split_start(ph.sp, static_cast<int>(w)) : 0;
+        ph.u1 = act ? split_start(ph.sp, static_cast<int>(w) + 1) : 0;
+    }
+    const int u0 = ph.u0, u1 = ph.u1, n = u1 - u0;
     auto pair_base = [&](int p) -> const uint8_t * {
         const int e = rv.pairs[p * kPairInts];
         return e >= 0 ? a.tiles_routed + (int64_t)e * a.expert_bytes_routed +
@@ -423,10 +823,10 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
     int is_ps = 0, is_end = 0, is_p = 0;
     const uint8_t *is_base = nullptr, *nx_base = nullptr;
     int issued = 0, waited = 0;  // stages issued / consumed, for a bounded drain
-    if (lane == 0 && active) {
-        is_p = pair_of(u0);
-        is_ps = pair_start(is_p);
-        is_end = is_ps + pair_units(is_p);
+    if (lane == 0 && n > 0) {
+        is_p = pair_of(ph, u0);
+        is_ps = pair_start(ph, is_p);
+        is_end = is_ps + pair_units(ph, is_p);
         is_base = pair_base(is_p);
         nx_base = is_end < u1 ? pair_base(is_p + 1) : nullptr;
     }
@@ -438,7 +838,7 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
         if (u == is_end) {
             is_p += 1;
             is_ps = is_end;
-            is_end += pair_units(is_p);
+            is_end += pair_units(ph, is_p);
             is_base = nx_base;
             nx_base = is_end < u1 ? pair_base(is_p + 1) : nullptr;
         }
@@ -453,30 +853,29 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
 
     if (PHASE == 1) {
         // Down needs h of its pairs.  The first weight copies are already in
-        // flight; warp 0 waits until every pair the CTA's warps will read has
-        // all its gate/up strips done while the other warps sleep at a
-        // barrier (one poller per CTA).  Every warp passes both barriers
-        // whatever its state, so a timeout cannot strand a warp.
+        // flight; warp 0 waits until the strip-completing gate/up warps have
+        // woken this CTA for every pair its warps read, while the other warps
+        // sleep at a barrier.  Every warp passes both barriers whatever its
+        // state, so a timeout cannot strand a warp.
         cta_barrier();
         if ((threadIdx.x >> 5) == 0) {
             int good = enabled ? 1 : 0;
             const int64_t wa = (int64_t)blockIdx.x * kWarps;
             int64_t wb = wa + kWarps - 1;
-            if (wb > W - 1)
-                wb = W - 1;
-            if (good && wa < W) {
-                const int pa = pair_of(static_cast<int>(wa * U / W));
-                const int pb = pair_of(static_cast<int>((wb + 1) * U / W) - 1);
-                for (int p = pa; p <= pb && good; ++p) {
-                    const int fp = p < P_r ? a.f : a.fs;
-                    good = warp_wait_geq(a.pair_done + p, static_cast<unsigned>(fp / kTileRows),
-                                         a.status)
-                               ? 1
-                               : 0;
-                }
+            if (wb > ph.W - 1)
+                wb = ph.W - 1;
+            if (good && wa < ph.W) {
+                const int pa = pair_of(ph, split_start(ph.sp, static_cast<int>(wa)));
+                const int pb = pair_of(ph, split_start(ph.sp, static_cast<int>(wb) + 1) - 1);
+                good = warp_wait_geq(a.cta_flags + 32 * blockIdx.x + 1,
+                                     static_cast<unsigned>(pb - pa + 1), a.status)
+                           ? 1
+                           : 0;
             }
-            if (lane == 0)
+            if (lane == 0) {
                 *s_ok = good;
+                a.cta_flags[32 * blockIdx.x + 1] = 0u;
+            }
         }
         cta_barrier();
         ok = *s_ok != 0;
@@ -484,347 +883,63 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
             return false;
     }
 
-    // ---- activations of (pair, group) -------------------------------------
-    // the pair record, read once per pair: column count, this lane's token
-    // row (gq) and the tokens of the lane's two output columns
-    int pi_ncols = 0, pi_tok = 0, pi_t0 = -1, pi_t1 = -1;
-    auto read_pair = [&](int p) {
-        const int32_t *pr = rv.pairs + p * kPairInts;
-        pi_ncols = pr[1];
-        pi_tok = gq < pi_ncols ? pr[2 + gq] : 0;
-        pi_t0 = 2 * tig < pi_ncols ? pr[2 + 2 * tig] : -1;
-        pi_t1 = 2 * tig + 1 < pi_ncols ? pr[2 + 2 * tig + 1] : -1;
-    };
-    const int nstrip = fmax / kTileRows;
-    auto load_b = [&](int p, int g, BRaw<NV> &r) {
-        const bool valid = gq < pi_ncols;
-        const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-        const float2 z2 = make_float2(0.f, 0.f);
-        if (PHASE == 0) {
-            if (XBF16) {
-                const uint4 *row = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const uint16_t *>(a.x) + (int64_t)pi_tok * d + g * kGroup + 16 * tig);
-                r.v[0] = valid ? __ldg(row) : z4;
-                r.v[1] = valid ? __ldg(row + 1) : z4;
-            } else {
-                const uint4 *row = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const float *>(a.x) + (int64_t)pi_tok * d + g * kGroup + 16 * tig);
-#pragma unroll
-                for (int i = 0; i < NV; ++i)
-                    r.v[i] = valid ? __ldg(row + i) : z4;
-            }
-            const float2 *xs = reinterpret_cast<const float2 *>(a.xsum);
-            r.xs0 = pi_t0 >= 0 ? __ldcg(xs + (int64_t)pi_t0 * (d / kGroup) + g) : z2;
-            r.xs1 = pi_t1 >= 0 ? __ldcg(xs + (int64_t)pi_t1 * (d / kGroup) + g) : z2;
-        } else {
-            const int64_t off = ((int64_t)p * kPairCols + gq) * fmax + g * kGroup + 16 * tig;
-            const uint4 *hi = reinterpret_cast<const uint4 *>(a.h_hi + off);
-            const uint4 *lo = reinterpret_cast<const uint4 *>(a.h_lo + off);
-            r.v[0] = valid ? __ldcg(hi) : z4;
-            r.v[1] = valid ? __ldcg(hi + 1) : z4;
-            r.v[2] = valid ? __ldcg(lo) : z4;
-            r.v[3] = valid ? __ldcg(lo + 1) : z4;
-            // group sums of h: lane (gq, tig) loads strip 4g + (gq & 3) of its
-            // two columns; cook_b adds the four strips with shuffles
-            const int c0 = 2 * tig, c1 = c0 + 1;
-            const float2 *hp = reinterpret_cast<const float2 *>(a.hs_part);
-            const int st = 4 * g + (gq & 3);
-            r.xs0 = c0 < pi_ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c0) * nstrip + st) : z2;
-            r.xs1 = c1 < pi_ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c1) * nstrip + st) : z2;
-        }
-    };
-    // B fragments for the mma from a BRaw
-    uint32_t b0[4], b1[4], b0l[4], b1l[4];
-    float bias0 = 0.f, bias1 = 0.f;
-    auto cook_b = [&](const BRaw<NV> &r) {
-        float2 x0 = r.xs0, x1 = r.xs1;
-        if (PHASE == 1) {
-            const uint32_t *hv = reinterpret_cast<const uint32_t *>(r.v);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                b0[j] = hv[2 * j];
-                b1[j] = hv[2 * j + 1];
-                b0l[j] = hv[8 + 2 * j];
-                b1l[j] = hv[8 + 2 * j + 1];
-            }
-#pragma unroll
-            for (int o = 4; o <= 8; o <<= 1) {
-                x0.x += __shfl_xor_sync(0xffffffffu, x0.x, o);
-                x0.y += __shfl_xor_sync(0xffffffffu, x0.y, o);
-                x1.x += __shfl_xor_sync(0xffffffffu, x1.x, o);
-                x1.y += __shfl_xor_sync(0xffffffffu, x1.y, o);
-            }
-        } else if (!XBF16) {
-            const float *xv = reinterpret_cast<const float *>(r.v);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                split_bf16x2(xv[4 * j + 0], xv[4 * j + 1], b0[j], b0l[j]);
-                split_bf16x2(xv[4 * j + 2], xv[4 * j + 3], b1[j], b1l[j]);
-            }
-        } else {
-            const uint32_t *xv = reinterpret_cast<const uint32_t *>(r.v);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                b0[j] = xv[2 * j];
-                b1[j] = xv[2 * j + 1];
-                b0l[j] = b1l[j] = 0u;
-            }
-        }
-        if (BITS == 2) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                b1[j] = bf16x2_quarter(b1[j]);
-                if (kSplit)
-                    b1l[j] = bf16x2_quarter(b1l[j]);
-            }
-            bias0 = 129.5f * x0.x + 33.5f * x0.y;
-            bias1 = 129.5f * x1.x + 33.5f * x1.y;
-        } else {
-            bias0 = 135.5f * (x0.x + x0.y);
-            bias1 = 135.5f * (x1.x + x1.y);
-        }
-    };
-
-    // decode + multiply one tile from shared memory into acc
-    auto mac_tile = [&](const uint8_t *tile, float (&acc)[4]) {
-        const uint32_t sc = *reinterpret_cast<const uint32_t *>(tile + CB + 4 * gq);
-        const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
-        // two independent accumulation chains (k-subtiles 0,2 and 1,3)
-        float dv[4] = {-bias0, -bias1, -bias0, -bias1};
-        float dw[4] = {0.f, 0.f, 0.f, 0.f};
-        if (BITS == 4) {
-            const uint4 cw = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
-            const uint32_t q4[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t q = q4[j];
-                uint32_t A[4];
-                A[0] = (q & 0x000F000Fu) | 0x43004300u;
-                A[1] = ((q >> 4) & 0x000F000Fu) | 0x43004300u;
-                A[2] = ((q >> 8) & 0x000F000Fu) | 0x43004300u;
-                A[3] = ((q >> 12) & 0x000F000Fu) | 0x43004300u;
-                float(&dd)[4] = (j & 1) ? dw : dv;
-                mma_bf16(dd, A, b0[j], b1[j]);
-                if (kSplit)
-                    mma_bf16(dd, A, b0l[j], b1l[j]);
-            }
-        } else {
-            const uint2 cw = *reinterpret_cast<const uint2 *>(tile + 8 * lane);
-            const uint32_t q2[2] = {cw.x, cw.y};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t q = q2[j >> 1];
-                const int v0 = 8 * (j & 1), v1 = v0 + 4;
-                uint32_t A[4];
-                A[0] = ((q >> v0) & 0x00030003u) | 0x43004300u;
-                A[1] = ((q >> v1) & 0x00030003u) | 0x43004300u;
-                A[2] = ((q >> v0) & 0x000C000Cu) | 0x43004300u;
-                A[3] = ((q >> v1) & 0x000C000Cu) | 0x43004300u;
-                float(&dd)[4] = (j & 1) ? dw : dv;
-                mma_bf16(dd, A, b0[j], b1[j]);
-                if (kSplit)
-                    mma_bf16(dd, A, b0l[j], b1l[j]);
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            dv[e] += dw[e];
-        acc[0] = fmaf(s01.x, dv[0], acc[0]);
-        acc[1] = fmaf(s01.x, dv[1], acc[1]);
-        acc[2] = fmaf(s01.y, dv[2], acc[2]);
-        acc[3] = fmaf(s01.y, dv[3], acc[3]);
-    };
-
-    // ---- strip finalisation -------------------------------------------
-    auto finalize = [&](int p, int s, const float (&ag)[4], const float (&au)[4]) {
-        const int ncols = rv.pairs[p * kPairInts + 1];
-        const float invL = 1.0f / L;
-        const int c0 = 2 * tig;
-        if (PHASE == 0) {
-            float hs[2] = {0.f, 0.f};  // per output column, this lane's rows
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float g = ag[e] * invL, u = au[e] * invL;
-                const float hv = g / (1.0f + expf(-g)) * u;
-                const int col = c0 + (e & 1);
-                const int row = 16 * s + gq + 8 * (e >> 1);
-                if (col < ncols) {
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
-                    const int64_t off = ((int64_t)p * kPairCols + col) * fmax + row;
-                    a.h_hi[off] = *reinterpret_cast<const uint16_t *>(&hi);
-                    a.h_lo[off] = *reinterpret_cast<const uint16_t *>(&lo);
-                }
-                hs[e & 1] += hv;
-            }
-            // class of these rows within their 64-row group: (gq >> 1) & 1;
-            // sum over lanes with equal tig and class (lane bits 2 and 4)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                hs[c] += __shfl_xor_sync(0xffffffffu, hs[c], 4);
-                hs[c] += __shfl_xor_sync(0xffffffffu, hs[c], 16);
-            }
-            if ((gq & 5) == 0) {
-                const int cls = (gq >> 1) & 1;
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    if (c0 + c < ncols)
-                        a.hs_part[(((int64_t)p * kPairCols + c0 + c) * nstrip + s) * 2 + cls] = hs[c];
-            }
-            // the down phase polls this count until all strips of the pair are in
-            __threadfence();
-            __syncwarp();
-            if (lane == 0)
-                atom_add_acqrel(a.pair_done + p, 1u);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = c0 + (e & 1);
-                const int row = 16 * s + gq + 8 * (e >> 1);
-                if (col < ncols)
-                    a.o[((int64_t)p * kPairCols + col) * d + row] = ag[e] * invL;
-            }
-            if (!a.fused_combine)
-                return;
-            __threadfence();
-            __syncwarp();
-            unsigned old = 0;
-            if (lane == 0)
-                old = atom_add_acqrel(a.comb_ctr + s, 1u);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == static_cast<unsigned>(P_t - 1)) {
-                __threadfence();
-                const int T = static_cast<int>(a.T), kk = a.k;
-                const bool has_sh = P_t > P_r;
-                for (int i = lane; i < kTileRows * T; i += 32) {
-                    const int t = i / kTileRows, row = 16 * s + i % kTileRows;
-                    float yv = 0.f;
-                    for (int j = 0; j < kk; ++j) {
-                        const int rm = rv.route_map[t * (kk + 1) + j];
-                        yv = fmaf(rv.weights[t * kk + j], __ldcg(a.o + (int64_t)rm * d + row), yv);
-                    }
-                    if (has_sh) {
-                        const int rm = rv.route_map[t * (kk + 1) + kk];
-                        yv = fmaf(rv.shared_w[t], __ldcg(a.o + (int64_t)rm * d + row), yv);
-                    }
-                    a.y[(int64_t)t * d + row] = yv;
-                }
-                __syncwarp();
-                if (lane == 0)
-                    a.comb_ctr[s] = 0u;
-            }
-        }
-    };
-
-    // flush strip (p, s) covering groups [ss, se)
-    auto flush = [&](int p, int s, int ss, int se, const float (&ag)[4], const float (&au)[4]) {
-        const int64_t wf = warp_of(ss, W, U), wl = warp_of(se - 1, W, U);
-        if (wf == wl) {
-            finalize(p, s, ag, au);
-            return;
-        }
-        const int myslot = u0 >= ss ? 0 : 1;
-        float4 *mine = reinterpret_cast<float4 *>(a.partial) + ((w * 2 + myslot) * 2) * 32;
-        mine[lane] = make_float4(ag[0], ag[1], ag[2], ag[3]);
-        if (PHASE == 0)
-            mine[32 + lane] = make_float4(au[0], au[1], au[2], au[3]);
-        __threadfence();
-        __syncwarp();
-        unsigned *ctr = (PHASE == 0 ? a.strip_ctr_g : a.strip_ctr_d) + (int64_t)p * a.max_strips + s;
-        unsigned old = 0;
-        if (lane == 0)
-            old = atom_add_acqrel(ctr, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != static_cast<unsigned>(wl - wf))
-            return;
-        __threadfence();
-        float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int64_t w0 = wf; w0 <= wl; w0 += 4) {
-            float4 vg[4], vu[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int64_t ww = w0 + q;
-                vg[q] = vu[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (ww <= wl) {
-                    const int sl = ww * U / W >= ss ? 0 : 1;
-                    const float4 *src = reinterpret_cast<const float4 *>(a.partial) + ((ww * 2 + sl) * 2) * 32;
-                    vg[q] = __ldcg(src + lane);
-                    if (PHASE == 0)
-                        vu[q] = __ldcg(src + 32 + lane);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                tg[0] += vg[q].x, tg[1] += vg[q].y, tg[2] += vg[q].z, tg[3] += vg[q].w;
-                tu[0] += vu[q].x, tu[1] += vu[q].y, tu[2] += vu[q].z, tu[3] += vu[q].w;
-            }
-        }
-        if (lane == 0)
-            *ctr = 0u;
-        finalize(p, s, tg, tu);
-    };
-
-    // ---- main loop over (pair, strip) segments ------------------------
-    int cp = active ? pair_of(u0) : 0;
-    int cps = pair_start(cp), cpe = cps + pair_units(cp);
+    // ---- main loop over (pair, strip) segments -------------------------
+    int cp = n > 0 ? pair_of(ph, u0) : 0;
+    int cps = pair_start(ph, cp), cpe = cps + pair_units(ph, cp);
     int pair_read = -1;
+    PairInfo pi = {0, 0, -1, -1};
+    uint32_t seq = ring_seq;  // ring sequence number of the next stage to consume
+    int i = 0;                // stage index within this phase
     int u = u0;
-    int i = 0;  // stage (group) index within this phase
-    BRaw<NV> rA, rB, rC;
 #pragma unroll 1
     while (u < u1 && ok) {
         if (u >= cpe) {
             cp += 1;
             cps = cpe;
-            cpe += pair_units(cp);
+            cpe += pair_units(ph, cp);
         }
         const int p = cp;
         const int lt = u - cps;
-        const int gps = p < P_r ? gps_r : gps_s;
+        const int gps = p < P_r ? ph.gps_r : ph.gps_s;
         const int s = lt / gps;
         const int g0 = lt - s * gps;
         const int ss = u - g0, se = ss + gps;
         const int ue = se < u1 ? se : u1;
         const int g1 = g0 + (ue - u);
         if (p != pair_read) {
-            read_pair(p);
+            pi = read_pair(rv, p);
             pair_read = p;
         }
         float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-        auto do_group = [&](const BRaw<NV> &cur, BRaw<NV> &fill, int g) {
-            if (g + 2 < g1)
-                load_b(p, g + 2, fill);
-            cook_b(cur);
-            const uint32_t seq = ring_seq + static_cast<uint32_t>(i);
+        BRaw<NV> cur, nxt;
+        load_b<PHASE, XBF16, NV>(a, pi, p, g0, fmax, ph.nstrip, cur);
+#pragma unroll 1
+        for (int g = g0; g < g1; ++g) {
+            if (g + 1 < g1)
+                load_b<PHASE, XBF16, NV>(a, pi, p, g + 1, fmax, ph.nstrip, nxt);
+            BFrag f;
+            cook_b<BITS, PHASE, XBF16, NV>(cur, f);
             const int slot = static_cast<int>(seq % kNS);
             if (!mbar_wait_bounded(&bars[slot], (seq / kNS) & 1u)) {
                 ok = false;
-                return;
+                break;
             }
             waited = i + 1;
             const uint8_t *st = ring + slot * kStageBytes(BITS);
-            mac_tile(st, ag);
+            mac_tile<BITS, kSplit>(st, f, ag);
             if (PHASE == 0)
-                mac_tile(st + TB, au);
+                mac_tile<BITS, kSplit>(st + TB, f, au);
             __syncwarp();
             if (lane == 0)
                 issue(i + kNS);
             ++i;
-        };
-        load_b(p, g0, rA);
-        if (g0 + 1 < g1)
-            load_b(p, g0 + 1, rB);
-#pragma unroll 1
-        for (int g = g0; g < g1 && ok; g += 3) {
-            do_group(rA, rC, g);
-            if (g + 1 < g1 && ok)
-                do_group(rB, rA, g + 1);
-            if (g + 2 < g1 && ok)
-                do_group(rC, rB, g + 2);
+            ++seq;
+            cur = nxt;
         }
         if (!ok)
             break;
-        flush(p, s, ss, se, ag, au);
+        flush_strip<BITS, PHASE>(a, rv, ph, p, s, ss, se, make_float4(ag[0], ag[1], ag[2], ag[3]),
+                                 make_float4(au[0], au[1], au[2], au[3]));
         u = ue;
     }
     if (!ok) {
@@ -832,8 +947,8 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
             set_status(a.status, kStatusTimeout);
             // drain this warp's copies still in flight (bounded)
             for (int j = waited; j < issued; ++j) {
-                const uint32_t seq = ring_seq + static_cast<uint32_t>(j);
-                (void)mbar_wait_bounded(&bars[seq % kNS], (seq / kNS) & 1u);
+                const uint32_t sq = ring_seq + static_cast<uint32_t>(j);
+                (void)mbar_wait_bounded(&bars[sq % kNS], (sq / kNS) & 1u);
             }
         }
         __syncwarp();
@@ -844,7 +959,7 @@ __device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uin
 }
 
 template <int BITS, bool XBF16>
-__global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs a)
+__global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const __grid_constant__ LayerArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -873,17 +988,27 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs 
         const int64_t unit = (int64_t)warp * gridDim.x + blockIdx.x;
         if (unit < units) {
             router_unit<XBF16>(a, static_cast<int>(unit));
-            __threadfence();
+            fence_acq_rel();
             __syncwarp();
+            unsigned old = 0;
             if (lane == 0)
-                atom_add_acqrel(a.route_ctr, 1u);
+                old = atom_add_acqrel(a.route_ctr, 1u);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == static_cast<unsigned>(units - 1)) {
+                // the last router unit wakes every CTA through its own flag line
+                fence_acq_rel();
+                for (unsigned c = lane; c < gridDim.x; c += 32)
+                    st_relaxed(a.cta_flags + 32 * c, 1u);
+            }
         }
-        // one poller per CTA waits for every router unit; the others sleep
+        // one poller per CTA, on the CTA's own flag; the others sleep
         cta_barrier();
         if (warp == 0) {
-            const int good = warp_wait_geq(a.route_ctr, static_cast<unsigned>(units), a.status) ? 1 : 0;
-            if (lane == 0)
+            const int good = warp_wait_geq(a.cta_flags + 32 * blockIdx.x, 1u, a.status) ? 1 : 0;
+            if (lane == 0) {
                 s_ok = good;
+                a.cta_flags[32 * blockIdx.x] = 0u;  // only this CTA reads it
+            }
         }
         cta_barrier();
         ok = s_ok != 0;
@@ -940,7 +1065,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs 
 
     // ------------------------------------------------------------ exit: the
     // last warp out resets the flags (counters of strips reset themselves)
-    __threadfence();
+    fence_acq_rel();
     __syncwarp();
     unsigned old = 0;
     if (lane == 0)
@@ -951,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const LayerArgs 
             a.pair_done[p] = 0u;
         if (lane == 0) {
             *a.route_ctr = 0u;
-            __threadfence();
+            fence_acq_rel();
             *a.exit_ctr = 0u;
         }
     }
