@@ -202,6 +202,17 @@ T_ *at(void *base, size_t off)
 
 }  // namespace
 
+namespace smoe {
+
+size_t moe_workspace_zero_bytes(const smoe_layer_desc *layer, int64_t num_tokens)
+{
+    if (!valid_layer(layer) || num_tokens < 0)
+        return 0;
+    return make_plan(layer, num_tokens).off_meta;
+}
+
+}  // namespace smoe
+
 extern "C" {
 
 const char *smoe_status_string(smoe_status s)

@@ -5,7 +5,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "smoe.h"
+
 namespace smoe {
+
+// Leading bytes of the forward workspace that must hold zero when a forward
+// starts (its counters and flags; 0 on invalid arguments).  Everything after
+// them is written before it is read.
+size_t moe_workspace_zero_bytes(const smoe_layer_desc *layer, int64_t num_tokens);
 
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();

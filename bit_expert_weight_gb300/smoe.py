@@ -22,11 +22,16 @@ STATUS_NAMES = {0: "SMOE_OK", -1: "SMOE_ERR_INVALID_ARG", -2: "SMOE_ERR_UNSUPPOR
                 -6: "SMOE_ERR_TIMEOUT"}
 SMOE_F32, SMOE_BF16 = 0, 1
 
+# Bytes of the built-in workspace of smoe_moe_forward_noalloc
+# (SMOE_NOALLOC_SCRATCH_BYTES in include/smoe.h).
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
 EXPORTED = [
     "smoe_status_string", "smoe_stream_bytes", "smoe_scales_bytes", "smoe_expert_tiles_bytes",
     "smoe_repacked_bytes", "smoe_quantize", "smoe_repack", "smoe_unpack",
     "smoe_route_from_logits", "smoe_moe_workspace_bytes", "smoe_moe_workspace_init",
     "smoe_moe_forward", "smoe_moe_forward_stage", "smoe_get_device_status",
+    "smoe_moe_forward_noalloc",
 ]
 
 
@@ -91,6 +96,8 @@ def load(path: str | None = None):
     L.smoe_moe_forward_stage.argtypes = [ctypes.POINTER(LayerDesc), P, I, I64, P, P, S, P, P,
                                           I, P]
     L.smoe_moe_forward_stage.restype = I
+    L.smoe_moe_forward_noalloc.argtypes = [ctypes.POINTER(LayerDesc), P, I, I64, P, P, P, P]
+    L.smoe_moe_forward_noalloc.restype = I
     L.smoe_get_device_status.argtypes = [P]
     L.smoe_get_device_status.restype = I
     _lib = L
@@ -247,6 +254,21 @@ def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None
     _check(load().smoe_moe_forward(ctypes.byref(layer.desc), _ptr(x), dt, T, _ptr(y), _ptr(ws),
                                    ws.numel(), _ptr(ids), _ptr(w), _stream(stream)),
            "smoe_moe_forward")
+    return y
+
+
+def forward_noalloc(layer: MoELayer, x: torch.Tensor, y=None, ids=None, w=None, stream=None):
+    """smoe_moe_forward_noalloc: the forward with the library's built-in
+    workspace (no workspace argument; calls on one device must not overlap)."""
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty((T, layer.d), dtype=torch.float32, device=x.device)
+    dt = SMOE_BF16 if x.dtype == torch.bfloat16 else SMOE_F32
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be fp32 or bf16")
+    _check(load().smoe_moe_forward_noalloc(ctypes.byref(layer.desc), _ptr(x), dt, T, _ptr(y),
+                                           _ptr(ids), _ptr(w), _stream(stream)),
+           "smoe_moe_forward_noalloc")
     return y
 
 

@@ -212,6 +212,52 @@ smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
                                    void *workspace, size_t workspace_bytes, int32_t *ids_out,
                                    float *w_out, int stage, void *cuda_stream);
 
+/* ------------------------------------------------- forward, no allocation */
+
+/* Bytes of the device array that smoe_moe_forward_noalloc uses as its
+ * workspace: 32 MiB, a fixed part of the library image on each device.  It
+ * holds the workspace of a decode batch of up to 8 tokens for layers up to
+ * d_model 4096, ffn_dim 1536, 256 experts and top_k 8;
+ * smoe_moe_workspace_bytes(layer, T) <= SMOE_NOALLOC_SCRATCH_BYTES tells
+ * whether another shape or batch fits. */
+#define SMOE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* smoe_moe_forward without a caller-supplied workspace.  The pages describe
+ * no counterpart of this entry point: it exists for library users only.
+ *
+ * Who needs it: smoe_moe_forward wants a device workspace that the caller
+ * allocates.  Some callers cannot do that on the path where they run the
+ * layer: a plug-in handed device pointers by a host framework that owns all
+ * device memory through its own pool and offers it no allocator, or a
+ * serving loop that must not call cudaMalloc or cudaFree, since those can
+ * block on or synchronise the whole device.  This entry point allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.  Its
+ * workspace is a file-scope device array of SMOE_NOALLOC_SCRATCH_BYTES
+ * bytes that the CUDA driver reserves when libsmoe.so's module is loaded
+ * on a device.
+ *
+ * Arguments, outputs and results are those of smoe_moe_forward (bit for bit
+ * the same y, ids_out and w_out for the same inputs).  Each call first
+ * clears the workspace counters that must start at zero (a
+ * cudaMemsetAsync on cuda_stream), then enqueues the forward.
+ *
+ * Restrictions:
+ *   - All calls on one device share the one array.  Calls whose work can
+ *     overlap on the device (different streams without an ordering between
+ *     them, or several host threads) race on it and give wrong results.
+ *     Issue them on one stream, or order them with events.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it.  Make
+ *     that first call before any stream capture begins.
+ *
+ * Errors: those of smoe_moe_forward, and SMOE_ERR_WORKSPACE when
+ * smoe_moe_workspace_bytes(layer, num_tokens) exceeds
+ * SMOE_NOALLOC_SCRATCH_BYTES (the call then enqueues nothing; use
+ * smoe_moe_forward with a workspace of your own, or fewer tokens). */
+smoe_status smoe_moe_forward_noalloc(const smoe_layer_desc *layer, const void *x,
+                                     smoe_dtype x_dtype, int64_t num_tokens, float *y,
+                                     int32_t *ids_out, float *w_out, void *cuda_stream);
+
 /* Synchronise cuda_stream, then read and clear the device status word of the
  * current device.  Returns SMOE_OK, SMOE_ERR_DEVICE_FAULT, SMOE_ERR_TIMEOUT
  * or SMOE_ERR_CUDA. */
