@@ -106,9 +106,9 @@ bool valid_layer(const smoe_layer_desc *L)
         return false;
     if (L->group_size != SMOE_GROUP_SIZE)
         return false;
-    if (L->d_model <= 0 || L->d_model % 128 || L->d_model > 8192)
+    if (L->d_model <= 0 || L->d_model % 128 || L->d_model > 4096)
         return false;
-    if (L->ffn_dim <= 0 || L->ffn_dim % 64 || L->ffn_dim > 4096)
+    if (L->ffn_dim <= 0 || L->ffn_dim % 64 || L->ffn_dim > 2048)
         return false;
     if (L->num_experts < 1 || L->num_experts > kMaxExperts)
         return false;
@@ -117,7 +117,7 @@ bool valid_layer(const smoe_layer_desc *L)
     if (!L->router_w || !L->expert_tiles || !aligned(L->expert_tiles, 16) ||
         !aligned(L->router_w, 16))
         return false;
-    if (L->shared_ffn_dim < 0 || L->shared_ffn_dim % 64 || L->shared_ffn_dim > 4096)
+    if (L->shared_ffn_dim < 0 || L->shared_ffn_dim % 64 || L->shared_ffn_dim > 2048)
         return false;
     if ((L->shared_ffn_dim > 0) != (L->shared_tiles != nullptr))
         return false;
@@ -130,7 +130,7 @@ bool valid_layer(const smoe_layer_desc *L)
 
 struct Plan {
     int64_t T;
-    int ntiles, ksplit, Epad, max_pairs, fmax, warps, max_strips;
+    int ntiles, ksplit, Epad, max_pairs, fmax, ctas, max_strips;
     size_t off_ctr_tile, off_ctr_done, off_ctr_sg, off_ctr_sd, off_ctr_comb, off_pair_done,
         off_flags, off_ctaflags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w, off_sw, off_pairs,
         off_rmap, off_hhi, off_hlo, off_hspart, off_o, off_part, total;
@@ -160,7 +160,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.max_pairs = static_cast<int>(mp);
     p.fmax = L->ffn_dim > L->shared_ffn_dim ? L->ffn_dim : L->shared_ffn_dim;
     p.max_strips = (p.fmax > d ? p.fmax : d) / 16;
-    p.warps = layer_grid_warps_max();
+    p.ctas = layer_grid_ctas_max();
     size_t o = 0;
     auto take = [&](size_t bytes) {
         size_t at = o;
@@ -175,7 +175,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_ctr_comb = take(sizeof(unsigned) * (d / 16));
     p.off_pair_done = take(sizeof(unsigned) * p.max_pairs);
     p.off_flags = take(sizeof(unsigned) * 4);
-    p.off_ctaflags = take(sizeof(unsigned) * 32 * (size_t)device_sm_count() * kMaxLayerCtasPerSm);
+    p.off_ctaflags = take(sizeof(unsigned) * 32 * (size_t)p.ctas);
     p.off_meta = take(sizeof(int32_t) * 2);
     p.off_plog = take(sizeof(float) * p.ksplit * T * p.Epad);
     p.off_logits = take(sizeof(float) * T * p.Epad);
@@ -189,7 +189,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_hlo = take(sizeof(uint16_t) * (size_t)p.max_pairs * kPairCols * p.fmax);
     p.off_hspart = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 16) * 2);
     p.off_o = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
-    p.off_part = take(sizeof(float) * 4 * (size_t)p.warps * 2 * 2 * 32);
+    p.off_part = take(sizeof(float) * 4 * 2 * (size_t)p.ctas * 2 * 2 * 32);
     p.total = o;
     return p;
 }

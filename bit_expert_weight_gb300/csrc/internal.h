@@ -78,8 +78,8 @@ cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, in
                                 const float *bias, int32_t *ids, float *w, cudaStream_t stream);
 cudaError_t launch_router(const RouteArgs &a, cudaStream_t stream, bool pdl);
 
-// The fused layer kernel (layer.cu).
-constexpr int kMaxLayerCtasPerSm = 3;
+// The fused layer kernel (layer.cu): one CTA of 16 warps per SM.
+constexpr int kMaxLayerCtasPerSm = 1;
 
 struct LayerArgs {
     // layer
@@ -111,17 +111,17 @@ struct LayerArgs {
     uint16_t *h_hi, *h_lo;         // bf16 [max_pairs][8][fmax]
     float *hs_part;                // [max_pairs][8][fmax/16][2]
     float *o;                      // [max_pairs][8][d]
-    float *partial;                // [warps][2][2][32] float4
+    float *partial;                // [phase][CTAs][2 slots][2][32] float4
     unsigned *strip_ctr_g, *strip_ctr_d;  // [max_pairs][max_strips]
     unsigned *comb_ctr;            // [d/16]
     unsigned *pair_done;           // [max_pairs] finished gate/up strips
     unsigned *route_ctr, *exit_ctr;
-    unsigned *cta_flags;           // [max CTAs][32]: word 0 route go, word 1 pairs ready
+    unsigned *cta_flags;           // [max CTAs][32]: word 0 route go
     float *y;                      // [T, d]
     int *status;
 };
 
-int layer_grid_warps_max();
+int layer_grid_ctas_max();
 cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream);
 cudaError_t launch_combine(const LayerArgs &a, cudaStream_t stream);
 

@@ -43,17 +43,17 @@ namespace smoe {
 
 namespace {
 
-constexpr int kWarps = 8;
+// 16 streaming warps (decode, mma), 2 epilogue warps (unit sums, SiLU,
+// stores, cross-CTA fixups) and one producer warp (the TMA ring): global-
+// memory round trips and fences are slow while an SM streams, so the
+// streaming warps make none.
+constexpr int kStreamWarps = 16;
+constexpr int kEpiWarps = 2;
+constexpr int kProducerWarp = kStreamWarps + kEpiWarps;
+constexpr int kWarps = kStreamWarps + kEpiWarps + 1;
 constexpr int kThreads = kWarps * 32;
-constexpr int kNS = 8;  // stages per warp ring (one group each)
+constexpr int kMaxStripsD = 4096 / 16;  // output strips (d <= 4096)
 constexpr long long kSpinCycles = 4000000000ll;  // ~2 s at 2 GHz
-
-__host__ __device__ constexpr int kStageBytes(int bits) { return 2 * tile_bytes(bits); }
-__host__ __device__ constexpr int ring_bytes(int bits) { return kNS * kStageBytes(bits); }
-__host__ __device__ constexpr int smem_bytes(int bits)
-{
-    return kWarps * ring_bytes(bits) + kWarps * kNS * 8;
-}
 
 __device__ __forceinline__ unsigned atom_add_acqrel(unsigned *p, unsigned v)
 {
@@ -109,10 +109,19 @@ __device__ bool warp_wait_geq(const unsigned *p, unsigned target, int *status)
     return ok != 0;
 }
 
-// CTA-wide named barrier 1 (all kThreads threads).
+// CTA-wide named barrier 1 (all kThreads threads); 2: the streaming warps;
+// 3: the epilogue warps.
 __device__ __forceinline__ void cta_barrier()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+__device__ __forceinline__ void stream_barrier()
+{
+    asm volatile("bar.sync 2, %0;" ::"n"(kStreamWarps * 32) : "memory");
+}
+__device__ __forceinline__ void epi_barrier()
+{
+    asm volatile("bar.sync 3, %0;" ::"n"(kEpiWarps * 32) : "memory");
 }
 
 // Stream-K split of U units over W warps: warp w owns [start(w), start(w+1))
@@ -404,24 +413,209 @@ __device__ __noinline__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
 
 // ------------------------------------------------------------ streaming
 
-// Per-warp constants of one phase (passed by value to the cold helpers).
-struct Phase {
-    int P_r, P_t, fmax, nstrip;  // pairs, widest f, strips of fmax
-    int U_r, U_s, UR, U, W;      // groups per routed / shared pair, totals, warps
-    Split sp;                    // the stream-K split of U over W
-    int u0, u1;                  // this warp's group range
-    int gps_r, gps_s;            // groups per strip
-    long long w;                 // global warp index
+// A chunk is a run of consecutive groups of one strip; one stage of the
+// CTA's ring holds one chunk.  Gate/up: up to kChunkGroups groups (one per
+// streaming warp, gate and up tile each); down: the whole strip, up to
+// 2 * kChunkGroups groups (two per warp, one tile each) -- the same bytes.
+constexpr int kChunkGroups = kStreamWarps;
+constexpr int kDownGroupsMax = 2 * kChunkGroups;  // ffn_dim <= 2048
+
+__host__ __device__ constexpr int stage_bytes(int bits) { return kChunkGroups * 2 * tile_bytes(bits); }
+// About 64 KB in flight per SM: enough for the full HBM rate, and no deeper,
+// since every other memory access of the SM queues behind the ring.
+__host__ __device__ constexpr int num_stages(int bits) { return bits == 4 ? 4 : 7; }
+// kRedSlots slots of per-warp unit sums (gate and up float4 per lane)
+constexpr int kRedSlots = 4;
+__host__ __device__ constexpr int red_bytes() { return kRedSlots * kStreamWarps * 2 * 32 * 16; }
+__host__ __device__ constexpr int smem_bytes(int bits)
+{
+    return num_stages(bits) * stage_bytes(bits) + red_bytes() + (2 * num_stages(bits) + 2 * kRedSlots) * 8;
+}
+// Pairs whose finished gate/up strips a CTA counts in shared memory and
+// publishes once, at the end of its gate/up range.
+constexpr int kMaxSpan = 64;
+
+// Step geometry of one phase.  Units are (pair, strip) in pair order; a
+// unit's K groups are cut into ch chunks of gc groups (the last may be
+// shorter); the steps (chunks) of all units are split evenly over the CTAs.
+// Index [0]: routed pairs, [1]: the shared expert's pair.
+// (Scalar fields with select accessors: a runtime-indexed array would live
+// in local memory.)
+struct Geo {
+    int P_r, P_t;
+    int nstr0, gk0, ch0, gc0, spp0;  // routed: strips, groups per strip, chunks, groups per chunk, steps
+    int nstr1, gk1, ch1, gc1, spp1;  // shared
+    int SR, S;                       // steps of the routed pairs, of all pairs
+    Split sp;                        // steps over CTAs
+    int a0, a1;                      // this CTA's steps
+    int ts;                          // the CTA runs [ts, a1) first, then [a0, ts)
 };
 
-// This lane's 16 activations of one group (bf16 x: 2 vectors; fp32 x: 4;
-// h of the down phase: hi in v[0..1], lo in v[2..3]) and the group sums
-// (X0, X1) of the two output columns the lane accumulates.
-template <int NV>
-struct BRaw {
-    uint4 v[NV];
-    float2 xs0, xs1;
+struct UnitGeo {
+    int nstr, gk, ch, gc;
 };
+
+__device__ __forceinline__ UnitGeo unit_geo(const Geo &g, int p)
+{
+    const bool r = p < g.P_r;
+    UnitGeo u;
+    u.nstr = r ? g.nstr0 : g.nstr1;
+    u.gk = r ? g.gk0 : g.gk1;
+    u.ch = r ? g.ch0 : g.ch1;
+    u.gc = r ? g.gc0 : g.gc1;
+    return u;
+}
+
+__device__ __forceinline__ Geo make_geo(const LayerArgs &a, int phase, int P_r, int P_t)
+{
+    Geo g;
+    g.P_r = P_r;
+    g.P_t = P_t;
+    {
+        const int rows = phase == 0 ? a.f : a.d, K = phase == 0 ? a.d : a.f;
+        g.nstr0 = rows / kTileRows;
+        g.gk0 = K / kGroup;
+        g.ch0 = phase == 0 ? (g.gk0 + kChunkGroups - 1) / kChunkGroups : 1;
+        g.gc0 = g.ch0 > 0 ? (g.gk0 + g.ch0 - 1) / g.ch0 : 0;
+        g.spp0 = g.nstr0 * g.ch0;
+    }
+    {
+        const int rows = phase == 0 ? a.fs : a.d, K = phase == 0 ? a.d : a.fs;
+        g.nstr1 = rows / kTileRows;
+        g.gk1 = K / kGroup;
+        g.ch1 = phase == 0 ? (g.gk1 + kChunkGroups - 1) / kChunkGroups : (g.gk1 > 0 ? 1 : 0);
+        g.gc1 = g.ch1 > 0 ? (g.gk1 + g.ch1 - 1) / g.ch1 : 0;
+        g.spp1 = g.nstr1 * g.ch1;
+    }
+    g.SR = P_r * g.spp0;
+    g.S = g.SR + (P_t - P_r) * g.spp1;
+    g.sp = make_split(g.S, static_cast<int>(gridDim.x));
+    g.a0 = split_start(g.sp, static_cast<int>(blockIdx.x));
+    g.a1 = split_start(g.sp, static_cast<int>(blockIdx.x) + 1);
+    g.ts = g.a1;
+    return g;
+}
+
+struct Pos {
+    int p, s, c;  // pair, strip, chunk
+};
+
+__device__ __forceinline__ Pos decode(const Geo &g, int i)
+{
+    Pos q;
+    int r, ch;
+    if (i < g.SR) {
+        q.p = i / g.spp0;
+        r = i - q.p * g.spp0;
+        ch = g.ch0;
+    } else {
+        const int j = i - g.SR, pp = j / g.spp1;
+        q.p = g.P_r + pp;
+        r = j - pp * g.spp1;
+        ch = g.ch1;
+    }
+    q.s = r / ch;
+    q.c = r - q.s * ch;
+    return q;
+}
+
+__device__ __forceinline__ void advance(const UnitGeo &u, Pos &q)
+{
+    if (++q.c == u.ch) {
+        q.c = 0;
+        if (++q.s == u.nstr) {
+            q.s = 0;
+            ++q.p;
+        }
+    }
+}
+
+// The ring's producer (lane 0 of warp 0): the next stage to issue, as a
+// phase and a step of that phase.
+// Order of a CTA's steps: a unit cut by the end of the range is run first,
+// then the range from its start (whose first unit may be cut by the start).
+// Both contributors of a shared unit then reach it early, so the fixup that
+// joins their sums is off the critical path.
+__device__ __forceinline__ void set_order(Geo &g)
+{
+    g.ts = g.a1;
+    if (g.a1 <= g.a0)
+        return;
+    const Pos ql = decode(g, g.a1 - 1);
+    const int ch = ql.p < g.P_r ? g.ch0 : g.ch1;
+    const int ustart = (g.a1 - 1) - ql.c;
+    if (ql.c != ch - 1 && ustart > g.a0)
+        g.ts = ustart;
+}
+// Step index of position k in that order.
+__device__ __forceinline__ int step_at(const Geo &g, int k)
+{
+    const int nt = g.a1 - g.ts;
+    return k < nt ? g.ts + k : g.a0 + (k - nt);
+}
+
+// Kept in shared memory, like the geometry of both phases (CTA-uniform).
+struct Producer {
+    int phase;      // 0 gate/up, 1 down, 2 nothing left
+    int k;          // position in the phase's step order
+    Pos q;
+    uint32_t next;  // stages issued so far
+};
+
+__device__ __forceinline__ void producer_seek(const Geo *geo, Producer &pr)
+{
+    while (pr.phase <= 1 && geo[pr.phase].a0 >= geo[pr.phase].a1)
+        ++pr.phase;
+    if (pr.phase <= 1) {
+        pr.k = 0;
+        pr.q = decode(geo[pr.phase], step_at(geo[pr.phase], 0));
+    }
+}
+
+// Issue the next stage: 1 issued, 0 not now (slot still in use and
+// !block, or nothing left), -1 the bounded wait for the slot ran out.
+template <int BITS>
+__device__ __forceinline__ int produce(const LayerArgs &a, const RouteView &rv, const Geo *geo,
+                                       Producer &pr, uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                       bool block)
+{
+    constexpr int NS = num_stages(BITS), SB = stage_bytes(BITS), TB = tile_bytes(BITS);
+    if (pr.phase > 1)
+        return 0;
+    const uint32_t j = pr.next;
+    const int slot = static_cast<int>(j % NS);
+    if (j >= static_cast<uint32_t>(NS)) {
+        const unsigned par = ((j / NS) - 1u) & 1u;
+        if (block) {
+            if (!mbar_wait_bounded(&empty[slot], par))
+                return -1;
+        } else if (!mbar_test_wait(&empty[slot], par)) {
+            return 0;
+        }
+    }
+    const Geo &g = geo[pr.phase];
+    const UnitGeo u = unit_geo(g, pr.q.p);
+    const int GB = pr.phase == 0 ? 2 * TB : TB;
+    const int g0 = pr.q.c * u.gc;
+    const int ng = min(u.gk - g0, u.gc);
+    const int e = rv.pairs[pr.q.p * kPairInts];
+    const uint8_t *base =
+        e >= 0 ? a.tiles_routed + (int64_t)e * a.expert_bytes_routed + (pr.phase ? a.down_off_routed : 0)
+               : a.tiles_shared + (pr.phase ? a.down_off_shared : 0);
+    const uint8_t *src = base + ((int64_t)pr.q.s * u.gk + g0) * GB;
+    mbar_arrive_expect_tx(&full[slot], static_cast<unsigned>(ng * GB));
+    bulk_g2s(ring + slot * SB, src, static_cast<unsigned>(ng * GB), &full[slot]);
+    pr.next = j + 1;
+    if (++pr.k == g.a1 - g.a0) {
+        ++pr.phase;
+        producer_seek(geo, pr);
+    } else if (pr.k == g.a1 - g.ts) {
+        pr.q = decode(g, g.a0);
+    } else {
+        advance(u, pr.q);
+    }
+    return 1;
+}
 
 // The lane's view of a pair record: column count, its token row (gq) and
 // the tokens of its two output columns.
@@ -441,9 +635,45 @@ __device__ __forceinline__ PairInfo read_pair(const RouteView &rv, int p)
     return pi;
 }
 
+// mma B fragments of one group (hi and, for fp32 / h activations, lo) and
+// the two column biases -(128 + L) X (Q2: -(129.5 X0 + 33.5 X1)).
+struct BFrag {
+    uint32_t b0[4], b1[4], b0l[4], b1l[4];
+    float bias0, bias1;
+};
+
+template <int BITS>
+__device__ __forceinline__ void finish_bias(BFrag &f, float2 x0, float2 x1)
+{
+    if (BITS == 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f.b1[j] = bf16x2_quarter(f.b1[j]);
+            f.b1l[j] = bf16x2_quarter(f.b1l[j]);
+        }
+        f.bias0 = 129.5f * x0.x + 33.5f * x0.y;
+        f.bias1 = 129.5f * x1.x + 33.5f * x1.y;
+    } else {
+        f.bias0 = 135.5f * (x0.x + x0.y);
+        f.bias1 = 135.5f * (x1.x + x1.y);
+    }
+}
+
+// Raw B operand of one group as loaded: gate/up -- this lane's 16
+// activations (columns 64 gi + 16 tig .. +15 of its token; bf16 x: 2
+// vectors, fp32 x: 4) and the group sums of its two output columns; down --
+// h hi (v[0..1]) and lo (v[2..3]) and the lane's strip of the group sums.
+// All through L1: x is read-only, and h, the group sums and xsum were
+// published (release / acquire) before the first read of each.
+template <int NV>
+struct BRaw {
+    uint4 v[NV];
+    float2 xs0, xs1;
+};
+
 template <int PHASE, bool XBF16, int NV>
-__device__ __forceinline__ void load_b(const LayerArgs &a, const PairInfo &pi, int p, int g,
-                                       int fmax, int nstrip, BRaw<NV> &r)
+__device__ __forceinline__ void load_raw(const LayerArgs &a, const PairInfo &pi, int p, int gi, int fmax,
+                                         BRaw<NV> &r)
 {
     const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
     const int d = a.d;
@@ -453,44 +683,39 @@ __device__ __forceinline__ void load_b(const LayerArgs &a, const PairInfo &pi, i
     if (PHASE == 0) {
         if (XBF16) {
             const uint4 *row = reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const uint16_t *>(a.x) + (int64_t)pi.tok * d + g * kGroup + 16 * tig);
+                reinterpret_cast<const uint16_t *>(a.x) + (int64_t)pi.tok * d + gi * kGroup + 16 * tig);
             r.v[0] = valid ? __ldg(row) : z4;
             r.v[1] = valid ? __ldg(row + 1) : z4;
         } else {
             const uint4 *row = reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const float *>(a.x) + (int64_t)pi.tok * d + g * kGroup + 16 * tig);
+                reinterpret_cast<const float *>(a.x) + (int64_t)pi.tok * d + gi * kGroup + 16 * tig);
 #pragma unroll
             for (int i = 0; i < NV; ++i)
                 r.v[i] = valid ? __ldg(row + i) : z4;
         }
         const float2 *xs = reinterpret_cast<const float2 *>(a.xsum);
-        r.xs0 = pi.t0 >= 0 ? __ldcg(xs + (int64_t)pi.t0 * (d / kGroup) + g) : z2;
-        r.xs1 = pi.t1 >= 0 ? __ldcg(xs + (int64_t)pi.t1 * (d / kGroup) + g) : z2;
+        r.xs0 = pi.t0 >= 0 ? __ldca(xs + (int64_t)pi.t0 * (d / kGroup) + gi) : z2;
+        r.xs1 = pi.t1 >= 0 ? __ldca(xs + (int64_t)pi.t1 * (d / kGroup) + gi) : z2;
     } else {
-        const int64_t off = ((int64_t)p * kPairCols + gq) * fmax + g * kGroup + 16 * tig;
+        const int64_t off = ((int64_t)p * kPairCols + gq) * fmax + gi * kGroup + 16 * tig;
         const uint4 *hi = reinterpret_cast<const uint4 *>(a.h_hi + off);
         const uint4 *lo = reinterpret_cast<const uint4 *>(a.h_lo + off);
-        r.v[0] = valid ? __ldcg(hi) : z4;
-        r.v[1] = valid ? __ldcg(hi + 1) : z4;
-        r.v[2] = valid ? __ldcg(lo) : z4;
-        r.v[3] = valid ? __ldcg(lo + 1) : z4;
-        // group sums of h: lane (gq, tig) loads strip 4g + (gq & 3) of its two
-        // columns; cook_b adds the four strips with shuffles
+        r.v[0] = valid ? __ldca(hi) : z4;
+        r.v[1] = valid ? __ldca(hi + 1) : z4;
+        r.v[2] = valid ? __ldca(lo) : z4;
+        r.v[3] = valid ? __ldca(lo + 1) : z4;
+        // group sums of h: lane (gq, tig) loads strip 4 gi + (gq & 3) of its
+        // two columns; cook_b adds the four strips with shuffles
+        const int nstrip = fmax / kTileRows;
         const int c0 = 2 * tig, c1 = c0 + 1;
         const float2 *hp = reinterpret_cast<const float2 *>(a.hs_part);
-        const int st = 4 * g + (gq & 3);
-        r.xs0 = c0 < pi.ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c0) * nstrip + st) : z2;
-        r.xs1 = c1 < pi.ncols ? __ldcg(hp + ((int64_t)p * kPairCols + c1) * nstrip + st) : z2;
+        const int st = 4 * gi + (gq & 3);
+        r.xs0 = c0 < pi.ncols ? __ldca(hp + ((int64_t)p * kPairCols + c0) * nstrip + st) : z2;
+        r.xs1 = c1 < pi.ncols ? __ldca(hp + ((int64_t)p * kPairCols + c1) * nstrip + st) : z2;
     }
 }
 
-// mma B fragments (hi and, for fp32 / h activations, lo) and the two column
-// biases -(128 + L) X (Q2: -(129.5 X0 + 33.5 X1)) from a BRaw
-struct BFrag {
-    uint32_t b0[4], b1[4], b0l[4], b1l[4];
-    float bias0, bias1;
-};
-
+// mma fragments and biases from a BRaw (every lane of the warp calls it).
 template <int BITS, int PHASE, bool XBF16, int NV>
 __device__ __forceinline__ void cook_b(const BRaw<NV> &r, BFrag &f)
 {
@@ -527,18 +752,7 @@ __device__ __forceinline__ void cook_b(const BRaw<NV> &r, BFrag &f)
             f.b0l[j] = f.b1l[j] = 0u;
         }
     }
-    if (BITS == 2) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f.b1[j] = bf16x2_quarter(f.b1[j]);
-            f.b1l[j] = bf16x2_quarter(f.b1l[j]);
-        }
-        f.bias0 = 129.5f * x0.x + 33.5f * x0.y;
-        f.bias1 = 129.5f * x1.x + 33.5f * x1.y;
-    } else {
-        f.bias0 = 135.5f * (x0.x + x0.y);
-        f.bias1 = 135.5f * (x1.x + x1.y);
-    }
+    finish_bias<BITS>(f, x0, x1);
 }
 
 // Decode + multiply one tile from shared memory into acc (two independent
@@ -595,33 +809,23 @@ __device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, fl
     acc[3] = fmaf(s01.y, dv[3], acc[3]);
 }
 
-__device__ __forceinline__ int pair_of(const Phase &ph, int u)
-{
-    return u < ph.UR ? u / ph.U_r : ph.P_r + (u - ph.UR) / ph.U_s;
-}
-__device__ __forceinline__ int pair_start(const Phase &ph, int p)
-{
-    return p < ph.P_r ? p * ph.U_r : ph.UR + (p - ph.P_r) * ph.U_s;
-}
-__device__ __forceinline__ int pair_units(const Phase &ph, int p) { return p < ph.P_r ? ph.U_r : ph.U_s; }
-
-// Finalise strip s of pair p from its full-K accumulators (cold path).
-// Phase 0: h = SiLU(g) * u stored as bf16 hi + lo, the strip's per-class
-// sums of h, the pair's strip count (the strip completing the pair wakes the
-// CTAs whose down ranges read it).  Phase 1: o, then (T <= 8) the combine of
-// output strip s by the last pair to finish it, in rank order.
+// Finalise unit (p, s) from its full-K sums, one warp (cold path).
+// Phase 0: h = SiLU(g) * u as bf16 hi + lo and the strip's per-class sums of
+// h.  Phase 1: o.  The caller counts the finished unit.
 template <int BITS, int PHASE>
-__device__ __noinline__ void finalize_strip(const LayerArgs &a, const RouteView rv, const Phase ph,
-                                            int p, int s, float4 ag, float4 au)
+__device__ __noinline__ void finalize_unit(const LayerArgs &a, const RouteView rv, int p, int s,
+                                           float4 ag, float4 au)
 {
     constexpr float L = BITS == 4 ? 7.5f : 1.5f;
     const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
     const int d = a.d;
+    const int fmax = a.f > a.fs ? a.f : a.fs;
     const int ncols = rv.pairs[p * kPairInts + 1];
     const float invL = 1.0f / L;
     const int c0 = 2 * tig;
     const float gv[4] = {ag.x, ag.y, ag.z, ag.w}, uv[4] = {au.x, au.y, au.z, au.w};
     if (PHASE == 0) {
+        const int nstrip = fmax / kTileRows;
         float hs[2] = {0.f, 0.f};  // per output column, this lane's rows
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -632,7 +836,7 @@ __device__ __noinline__ void finalize_strip(const LayerArgs &a, const RouteView 
             if (col < ncols) {
                 const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
                 const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
-                const int64_t off = ((int64_t)p * kPairCols + col) * ph.fmax + row;
+                const int64_t off = ((int64_t)p * kPairCols + col) * fmax + row;
                 a.h_hi[off] = *reinterpret_cast<const uint16_t *>(&hi);
                 a.h_lo[off] = *reinterpret_cast<const uint16_t *>(&lo);
             }
@@ -650,32 +854,9 @@ __device__ __noinline__ void finalize_strip(const LayerArgs &a, const RouteView 
 #pragma unroll
             for (int c = 0; c < 2; ++c)
                 if (c0 + c < ncols)
-                    a.hs_part[(((int64_t)p * kPairCols + c0 + c) * ph.nstrip + s) * 2 + cls] = hs[c];
+                    a.hs_part[(((int64_t)p * kPairCols + c0 + c) * nstrip + s) * 2 + cls] = hs[c];
         }
-        fence_acq_rel();
-        __syncwarp();
-        unsigned old = 0;
-        if (lane == 0)
-            old = atom_add_acqrel(a.pair_done + p, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        const int fp = p < ph.P_r ? a.f : a.fs;
-        if (old == static_cast<unsigned>(fp / kTileRows - 1)) {
-            // down-phase geometry (groups of 16 rows x 64 columns of W_down)
-            const int DU_r = (d / kTileRows) * (a.f / kGroup);
-            const int DU_s = ph.P_t > ph.P_r ? (d / kTileRows) * (a.fs / kGroup) : 0;
-            const int DUR = ph.P_r * DU_r;
-            const int DU = DUR + (ph.P_t - ph.P_r) * DU_s;
-            const int64_t Wall = (int64_t)gridDim.x * kWarps;
-            const int DW = DU < Wall ? DU : static_cast<int>(Wall);
-            const int ps = p < ph.P_r ? p * DU_r : DUR + (p - ph.P_r) * DU_s;
-            const int pe = ps + (p < ph.P_r ? DU_r : DU_s);
-            const Split dsp = make_split(DU, DW);
-            const int ca = split_owner(dsp, ps) / kWarps;
-            const int cb = split_owner(dsp, pe - 1) / kWarps;
-            fence_acq_rel();
-            for (int c = ca + lane; c <= cb; c += 32)
-                red_add_relaxed(a.cta_flags + 32 * c + 1, 1u);
-        }
+        __syncwarp();  // the caller counts the strip (see count_strip)
     } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -684,76 +865,74 @@ __device__ __noinline__ void finalize_strip(const LayerArgs &a, const RouteView 
             if (col < ncols)
                 a.o[((int64_t)p * kPairCols + col) * d + row] = gv[e] * invL;
         }
-        if (!a.fused_combine)
-            return;
-        fence_acq_rel();
-        __syncwarp();
-        unsigned old = 0;
-        if (lane == 0)
-            old = atom_add_acqrel(a.comb_ctr + s, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == static_cast<unsigned>(ph.P_t - 1)) {
-            fence_acq_rel();
-            const int T = static_cast<int>(a.T), kk = a.k;
-            const bool has_sh = ph.P_t > ph.P_r;
-            for (int i = lane; i < kTileRows * T; i += 32) {
-                const int t = i / kTileRows, row = 16 * s + i % kTileRows;
-                float yv = 0.f;
-                for (int j = 0; j < kk; ++j) {
-                    const int rm = rv.route_map[t * (kk + 1) + j];
-                    yv = fmaf(rv.weights[t * kk + j], __ldcg(a.o + (int64_t)rm * d + row), yv);
-                }
-                if (has_sh) {
-                    const int rm = rv.route_map[t * (kk + 1) + kk];
-                    yv = fmaf(rv.shared_w[t], __ldcg(a.o + (int64_t)rm * d + row), yv);
-                }
-                a.y[(int64_t)t * d + row] = yv;
-            }
-            __syncwarp();
-            if (lane == 0)
-                a.comb_ctr[s] = 0u;
-        }
+        __syncwarp();  // the caller counts the output strip
     }
 }
 
-// Flush strip (p, s) = groups [ss, se) (cold path): finalise it if this warp
-// covered all of it, else store the partial and let the last contributor
-// (arrival counter) sum the partials in warp order and finalise.
+// One more finished gate/up strip of pair p: counted in shared memory and
+// published at the end of the CTA's gate/up range, or published at once
+// (release) when the CTA's range spans too many pairs.
+__device__ __forceinline__ void count_strip(const LayerArgs &a, const int *pspan, unsigned *pcnt, int p)
+{
+    if ((threadIdx.x & 31) != 0)
+        return;
+    const int j = p - pspan[0];
+    if (pspan[1] > 0 && j >= 0 && j < pspan[1]) {
+        atomicAdd(pcnt + j, 1u);
+    } else {
+        fence_acq_rel();
+        red_add_relaxed(a.pair_done + p, 1u);
+    }
+}
+
+// A finished unit: a gate/up strip of pair p, or a down unit of output
+// strip s (counted per CTA, published after the down phase).
+template <int PHASE>
+__device__ __forceinline__ void count_unit(const LayerArgs &a, const int *pspan, unsigned *pcnt,
+                                           unsigned *ccnt, int p, int s)
+{
+    if (PHASE == 0)
+        count_strip(a, pspan, pcnt, p);
+    else if ((threadIdx.x & 31) == 0)
+        atomicAdd(ccnt + s, 1u);
+}
+
+// Unit (p, s) shared with other CTAs (cold path): store this CTA's sums,
+// count the contributors; the last one adds all sums in CTA order and
+// finalises.  Slot 0 of a CTA holds the unit straddling its first step,
+// slot 1 the one straddling its last; each phase has its own slots.
 template <int BITS, int PHASE>
-__device__ __noinline__ void flush_strip(const LayerArgs &a, const RouteView rv, const Phase ph,
-                                         int p, int s, int ss, int se, float4 ag, float4 au)
+__device__ __noinline__ void fixup_unit(const LayerArgs &a, const RouteView rv, const Geo &g, int p,
+                                        int s, int ustart, int uend, float4 tg, float4 tu,
+                                        unsigned *pcnt, const int *pspan, unsigned *ccnt)
 {
     const int lane = threadIdx.x & 31;
-    const int wf = split_owner(ph.sp, ss), wl = split_owner(ph.sp, se - 1);
-    if (wf == wl) {
-        finalize_strip<BITS, PHASE>(a, rv, ph, p, s, ag, au);
-        return;
-    }
-    const int myslot = ph.u0 >= ss ? 0 : 1;
-    float4 *mine = reinterpret_cast<float4 *>(a.partial) + ((ph.w * 2 + myslot) * 2) * 32;
-    mine[lane] = ag;
+    float4 *part = reinterpret_cast<float4 *>(a.partial) + (size_t)PHASE * gridDim.x * 2 * 64;
+    const int my = ustart < g.a0 ? 0 : 1;
+    float4 *mine = part + ((size_t)blockIdx.x * 2 + my) * 64;
+    mine[lane] = tg;
     if (PHASE == 0)
-        mine[32 + lane] = au;
-    fence_acq_rel();
+        mine[32 + lane] = tu;
     __syncwarp();
+    const int cf = split_owner(g.sp, ustart), cl = split_owner(g.sp, uend - 1);
     unsigned *ctr = (PHASE == 0 ? a.strip_ctr_g : a.strip_ctr_d) + (int64_t)p * a.max_strips + s;
     unsigned old = 0;
     if (lane == 0)
         old = atom_add_acqrel(ctr, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != static_cast<unsigned>(wl - wf))
+    if (old != static_cast<unsigned>(cl - cf))
         return;
-    fence_acq_rel();
-    float4 tg = make_float4(0.f, 0.f, 0.f, 0.f), tu = tg;
-    for (int w0 = wf; w0 <= wl; w0 += 4) {
+    __syncwarp();
+    float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg;
+    for (int c0 = cf; c0 <= cl; c0 += 4) {
         float4 vg[4], vu[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int ww = w0 + q;
+            const int c = c0 + q;
             vg[q] = vu[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (ww <= wl) {
-                const int sl = split_start(ph.sp, ww) >= ss ? 0 : 1;
-                const float4 *src = reinterpret_cast<const float4 *>(a.partial) + ((ww * 2 + sl) * 2) * 32;
+            if (c <= cl) {
+                const int sl = split_start(g.sp, c) > ustart ? 0 : 1;
+                const float4 *src = part + ((size_t)c * 2 + sl) * 64;
                 vg[q] = __ldcg(src + lane);
                 if (PHASE == 0)
                     vu[q] = __ldcg(src + 32 + lane);
@@ -761,220 +940,275 @@ __device__ __noinline__ void flush_strip(const LayerArgs &a, const RouteView rv,
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            tg.x += vg[q].x, tg.y += vg[q].y, tg.z += vg[q].z, tg.w += vg[q].w;
-            tu.x += vu[q].x, tu.y += vu[q].y, tu.z += vu[q].z, tu.w += vu[q].w;
+            sg.x += vg[q].x, sg.y += vg[q].y, sg.z += vg[q].z, sg.w += vg[q].w;
+            su.x += vu[q].x, su.y += vu[q].y, su.z += vu[q].z, su.w += vu[q].w;
         }
     }
     if (lane == 0)
         *ctr = 0u;
-    finalize_strip<BITS, PHASE>(a, rv, ph, p, s, tg, tu);
+    finalize_unit<BITS, PHASE>(a, rv, p, s, sg, su);
+    count_unit<PHASE>(a, pspan, pcnt, ccnt, p, s);
 }
 
-// One streaming phase (0: gate/up + SiLU, 1: down + combine) of one warp.
-// The unit of work is a group: 64 input columns of 16 output rows (phase 0:
-// the gate tile and the up tile of those rows, phase 1: one down tile).  A
-// pair's groups are contiguous in memory (strip-major), so a warp's range is
-// a few contiguous runs; each stage of the warp's ring holds one group.
-// Returns false if a bounded wait ran out (the status word is set).
-template <int BITS, bool XBF16, int PHASE>
-__device__ __forceinline__ bool run_phase(const LayerArgs &a, uint8_t *ring, uint64_t *bars,
-                                          uint32_t &ring_seq, int P_r, int P_t, int fmax,
-                                          int64_t w, int64_t Wall, bool enabled, int *s_ok,
-                                          const RouteView &rv)
+// Shared state of the streaming phases, one per CTA.
+struct Stream {
+    uint8_t *ring;
+    uint64_t *full, *empty;          // [NS]: 1 arrival + bytes / kStreamWarps arrivals
+    uint64_t *red_full, *red_empty;  // [kRedSlots]: kStreamWarps arrivals / 1 arrival
+    unsigned *pcnt;                  // [kMaxSpan] finished gate/up strips per pair
+    const int *pspan;                // [0] first pair, [1] span (0: publish each at once)
+    unsigned *ccnt;                  // [d/16] finished down units per output strip
+    float4 *red;                     // [kRedSlots][kStreamWarps][2][32]
+    volatile int *fail;              // a bounded wait ran out somewhere in the CTA
+    Producer *pr;                    // shared; used by lane 0 of warp 0 only
+    const Geo *geo;                  // shared, [2]
+    uint32_t seq;                    // stages consumed by this (streaming) warp
+    int uc;                          // units ended so far
+};
+
+__device__ __forceinline__ bool unit_ends(const Geo &g, const UnitGeo &u, const Pos &q, int i)
 {
-    constexpr int TB = tile_bytes(BITS);
-    constexpr int TPG = PHASE == 0 ? 2 : 1;  // tiles per group
-    constexpr int GB = TPG * TB;             // bytes per group
+    return q.c == u.ch - 1 || i == g.a1 - 1 || (g.ts < g.a1 && i == g.ts - 1);
+}
+
+// One phase (0: gate/up, 1: down) of a streaming warp.  The warp holds the
+// B fragments of its groups of the current pair: gate/up -- group
+// c * gc + w of each chunk c (at most KG chunks); down -- groups w and
+// w + 16 of the single chunk (the whole strip).  At a unit's end it leaves
+// its sums in a slot for the epilogue warps.
+template <int BITS, bool XBF16, int KG, int PHASE>
+__device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView &rv, Stream &st)
+{
+    constexpr int NS = num_stages(BITS), SB = stage_bytes(BITS), TB = tile_bytes(BITS);
+    constexpr int GB = PHASE == 0 ? 2 * TB : TB;
     constexpr int NV = (PHASE == 1 || !XBF16) ? 4 : 2;
     constexpr bool kSplit = PHASE == 1 || !XBF16;
-    const int lane = threadIdx.x & 31;
-    const int d = a.d;
-    bool ok = true;
-    Phase ph;
-    ph.P_r = P_r;
-    ph.P_t = P_t;
-    ph.fmax = fmax;
-    ph.nstrip = fmax / kTileRows;
-    {
-        const int Kr = PHASE == 0 ? d : a.f, Ks = PHASE == 0 ? d : a.fs;
-        const int Rr = PHASE == 0 ? a.f : d, Rs = PHASE == 0 ? a.fs : d;
-        ph.gps_r = Kr / kGroup;
-        ph.gps_s = Ks / kGroup;
-        ph.U_r = (Rr / kTileRows) * ph.gps_r;
-        ph.U_s = P_t > P_r ? (Rs / kTileRows) * ph.gps_s : 0;
-        ph.UR = P_r * ph.U_r;
-        ph.U = enabled ? ph.UR + (P_t - P_r) * ph.U_s : 0;
-        ph.W = ph.U < Wall ? ph.U : static_cast<int>(Wall);
-        ph.w = w;
-        const bool act = w < ph.W;
-        ph.sp = make_split(ph.U, ph.W);
-        ph.u0 = act ? split_start(ph.sp, static_cast<int>(w)) : 0;
-        ph.u1 = act ? split_start(ph.sp, static_cast<int>(w) + 1) : 0;
-    }
-    const int u0 = ph.u0, u1 = ph.u1, n = u1 - u0;
-    auto pair_base = [&](int p) -> const uint8_t * {
-        const int e = rv.pairs[p * kPairInts];
-        return e >= 0 ? a.tiles_routed + (int64_t)e * a.expert_bytes_routed +
-                            (PHASE == 0 ? 0 : a.down_off_routed)
-                      : a.tiles_shared + (PHASE == 0 ? 0 : a.down_off_shared);
-    };
-    // Issue state, lane 0 only: the pair being copied and the next pair's
-    // base, looked up one pair ahead.
-    int is_ps = 0, is_end = 0, is_p = 0;
-    const uint8_t *is_base = nullptr, *nx_base = nullptr;
-    int issued = 0, waited = 0;  // stages issued / consumed, for a bounded drain
-    if (lane == 0 && n > 0) {
-        is_p = pair_of(ph, u0);
-        is_ps = pair_start(ph, is_p);
-        is_end = is_ps + pair_units(ph, is_p);
-        is_base = pair_base(is_p);
-        nx_base = is_end < u1 ? pair_base(is_p + 1) : nullptr;
-    }
-    auto issue = [&](int i) {  // lane 0: the stage of group u0 + i
-        if (i >= n)
-            return;
-        issued = i + 1;
-        const int u = u0 + i;
-        if (u == is_end) {
-            is_p += 1;
-            is_ps = is_end;
-            is_end += pair_units(ph, is_p);
-            is_base = nx_base;
-            nx_base = is_end < u1 ? pair_base(is_p + 1) : nullptr;
-        }
-        const int slot = static_cast<int>((ring_seq + i) % kNS);
-        mbar_arrive_expect_tx(&bars[slot], GB);
-        bulk_g2s(ring + slot * kStageBytes(BITS), is_base + (int64_t)(u - is_ps) * GB, GB,
-                 &bars[slot]);
-    };
-    if (lane == 0)
-        for (int i = 0; i < kNS; ++i)
-            issue(i);
-
-    if (PHASE == 1) {
-        // Down needs h of its pairs.  The first weight copies are already in
-        // flight; warp 0 waits until the strip-completing gate/up warps have
-        // woken this CTA for every pair its warps read, while the other warps
-        // sleep at a barrier.  Every warp passes both barriers whatever its
-        // state, so a timeout cannot strand a warp.
-        cta_barrier();
-        if ((threadIdx.x >> 5) == 0) {
-            int good = enabled ? 1 : 0;
-            const int64_t wa = (int64_t)blockIdx.x * kWarps;
-            int64_t wb = wa + kWarps - 1;
-            if (wb > ph.W - 1)
-                wb = ph.W - 1;
-            if (good && wa < ph.W) {
-                const int pa = pair_of(ph, split_start(ph.sp, static_cast<int>(wa)));
-                const int pb = pair_of(ph, split_start(ph.sp, static_cast<int>(wb) + 1) - 1);
-                good = warp_wait_geq(a.cta_flags + 32 * blockIdx.x + 1,
-                                     static_cast<unsigned>(pb - pa + 1), a.status)
-                           ? 1
-                           : 0;
+    constexpr int NB = PHASE == 0 ? KG : 2;  // B fragments held
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = st.geo[PHASE];
+    const int a0 = g.a0, a1 = g.a1, n = a1 - a0, ts = g.ts, nt = a1 - ts;
+    if (n <= 0)
+        return;
+    const int fmax = a.f > a.fs ? a.f : a.fs;
+    Pos q = decode(g, nt > 0 ? ts : a0);
+    UnitGeo u = unit_geo(g, q.p);
+    int loaded = -1;
+    BFrag bf[NB];
+    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int kk = 0; kk < n; ++kk) {
+        const int i = kk < nt ? ts + kk : a0 + (kk - nt);
+        if (kk == nt && kk > 0)
+            q = decode(g, a0);
+        if (q.p != loaded) {
+            u = unit_geo(g, q.p);
+            if (PHASE == 1) {
+                // h of pair q.p is complete once all its gate/up strips are
+                // published; one warp polls, the others sleep at the barrier
+                stream_barrier();
+                if (warp == kStreamWarps - 1 && !*st.fail) {
+                    const int fp = q.p < g.P_r ? a.f : a.fs;
+                    if (!warp_wait_geq(a.pair_done + q.p, static_cast<unsigned>(fp / kTileRows), a.status) &&
+                        lane == 0)
+                        *st.fail = 1;
+                }
+                stream_barrier();
             }
+            const PairInfo pi = read_pair(rv, q.p);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const int gi = PHASE == 0 ? b * u.gc + warp : warp + b * kChunkGroups;
+                if ((PHASE == 1 || b < u.ch) && gi < u.gk && (PHASE == 1 || warp < u.gc)) {
+                    BRaw<NV> raw;
+                    load_raw<PHASE, XBF16, NV>(a, pi, q.p, gi, fmax, raw);
+                    cook_b<BITS, PHASE, XBF16, NV>(raw, bf[b]);
+                }
+            }
+            loaded = q.p;
+        }
+        const int slot = static_cast<int>(st.seq % NS);
+        bool ok = !*st.fail;
+        if (ok && !mbar_wait_bounded(&st.full[slot], (st.seq / NS) & 1u)) {
+            ok = false;
             if (lane == 0) {
-                *s_ok = good;
-                a.cta_flags[32 * blockIdx.x + 1] = 0u;
+                set_status(a.status, kStatusTimeout);
+                *st.fail = 1;
             }
         }
-        cta_barrier();
-        ok = *s_ok != 0;
-        if (!enabled)
-            return false;
-    }
-
-    // ---- main loop over (pair, strip) segments -------------------------
-    int cp = n > 0 ? pair_of(ph, u0) : 0;
-    int cps = pair_start(ph, cp), cpe = cps + pair_units(ph, cp);
-    int pair_read = -1;
-    PairInfo pi = {0, 0, -1, -1};
-    uint32_t seq = ring_seq;  // ring sequence number of the next stage to consume
-    int i = 0;                // stage index within this phase
-    int u = u0;
-#pragma unroll 1
-    while (u < u1 && ok) {
-        if (u >= cpe) {
-            cp += 1;
-            cps = cpe;
-            cpe += pair_units(ph, cp);
-        }
-        const int p = cp;
-        const int lt = u - cps;
-        const int gps = p < P_r ? ph.gps_r : ph.gps_s;
-        const int s = lt / gps;
-        const int g0 = lt - s * gps;
-        const int ss = u - g0, se = ss + gps;
-        const int ue = se < u1 ? se : u1;
-        const int g1 = g0 + (ue - u);
-        if (p != pair_read) {
-            pi = read_pair(rv, p);
-            pair_read = p;
-        }
-        float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-        BRaw<NV> cur, nxt;
-        load_b<PHASE, XBF16, NV>(a, pi, p, g0, fmax, ph.nstrip, cur);
-#pragma unroll 1
-        for (int g = g0; g < g1; ++g) {
-            if (g + 1 < g1)
-                load_b<PHASE, XBF16, NV>(a, pi, p, g + 1, fmax, ph.nstrip, nxt);
-            BFrag f;
-            cook_b<BITS, PHASE, XBF16, NV>(cur, f);
-            const int slot = static_cast<int>(seq % kNS);
-            if (!mbar_wait_bounded(&bars[slot], (seq / kNS) & 1u)) {
-                ok = false;
-                break;
-            }
-            waited = i + 1;
-            const uint8_t *st = ring + slot * kStageBytes(BITS);
-            mac_tile<BITS, kSplit>(st, f, ag);
-            if (PHASE == 0)
-                mac_tile<BITS, kSplit>(st + TB, f, au);
-            __syncwarp();
-            if (lane == 0)
-                issue(i + kNS);
-            ++i;
-            ++seq;
-            cur = nxt;
-        }
-        if (!ok)
-            break;
-        flush_strip<BITS, PHASE>(a, rv, ph, p, s, ss, se, make_float4(ag[0], ag[1], ag[2], ag[3]),
-                                 make_float4(au[0], au[1], au[2], au[3]));
-        u = ue;
-    }
-    if (!ok) {
-        if (lane == 0) {
-            set_status(a.status, kStatusTimeout);
-            // drain this warp's copies still in flight (bounded)
-            for (int j = waited; j < issued; ++j) {
-                const uint32_t sq = ring_seq + static_cast<uint32_t>(j);
-                (void)mbar_wait_bounded(&bars[sq % kNS], (sq / kNS) & 1u);
+        if (ok) {
+            const uint8_t *stage = st.ring + slot * SB;
+            if (PHASE == 0) {
+                const int gi = q.c * u.gc + warp;
+                if (warp < u.gc && gi < u.gk) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        if (b == q.c) {
+                            mac_tile<BITS, kSplit>(stage + warp * GB, bf[b], accg);
+                            mac_tile<BITS, kSplit>(stage + warp * GB + TB, bf[b], accu);
+                        }
+                    }
+                }
+            } else {
+                if (warp < u.gk)
+                    mac_tile<BITS, kSplit>(stage + warp * GB, bf[0], accg);
+                if (warp + kChunkGroups < u.gk)
+                    mac_tile<BITS, kSplit>(stage + (warp + kChunkGroups) * GB, bf[1], accu);
             }
         }
         __syncwarp();
-        return false;
+        if (ok && lane == 0)
+            mbar_arrive(&st.empty[slot]);
+        ++st.seq;
+        if (q.c == u.ch - 1 || i == a1 - 1 || (nt > 0 && i == ts - 1)) {
+            const int rs = st.uc % kRedSlots;
+            const unsigned rph = static_cast<unsigned>(st.uc / kRedSlots);
+            if (st.uc >= kRedSlots && !*st.fail &&
+                !mbar_wait_bounded(&st.red_empty[rs], (rph - 1u) & 1u) && lane == 0) {
+                set_status(a.status, kStatusTimeout);
+                *st.fail = 1;
+            }
+            if (PHASE == 1) {
+                // the two groups' partial sums of the same output rows
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    accg[e] += accu[e];
+            }
+            float4 *rw = st.red + ((rs * kStreamWarps + warp) * 2) * 32;
+            rw[lane] = make_float4(accg[0], accg[1], accg[2], accg[3]);
+            if (PHASE == 0)
+                rw[32 + lane] = make_float4(accu[0], accu[1], accu[2], accu[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                accg[e] = accu[e] = 0.f;
+            __syncwarp();
+            if (lane == 0 && !*st.fail)
+                mbar_arrive(&st.red_full[rs]);
+            ++st.uc;
+        }
+        advance(u, q);
     }
-    ring_seq += static_cast<uint32_t>(n);
-    return true;
 }
 
-template <int BITS, bool XBF16>
-__global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const __grid_constant__ LayerArgs a)
+// The ring's producer (lane 0 of the producer warp): every stage of both
+// phases in the CTA's step order, each as soon as its slot is free.
+template <int BITS>
+__device__ __forceinline__ void produce_all(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
+    Producer &pr = *st.pr;
+    while (pr.phase <= 1 && !*st.fail) {
+        const int r = produce<BITS>(a, rv, st.geo, pr, st.ring, st.full, st.empty, true);
+        if (r < 0) {
+            set_status(a.status, kStatusTimeout);
+            *st.fail = 1;
+        }
+        if (r <= 0)
+            break;
+    }
+}
+
+// One phase of an epilogue warp: the same walk over the CTA's steps; at
+// each unit end it owns (units alternate between the epilogue warps) it adds
+// the 16 streaming warps' sums in warp order, frees the slot, and finalises
+// the unit or, for a unit shared with another CTA, runs the fixup.
+template <int BITS, int PHASE>
+__device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &rv, Stream &st)
+{
+    const int e = (threadIdx.x >> 5) - kStreamWarps, lane = threadIdx.x & 31;
+    const Geo &g = st.geo[PHASE];
+    const int a0 = g.a0, a1 = g.a1, nt = g.a1 - g.ts;
+    if (a0 >= a1)
+        return;
+    Pos q = decode(g, step_at(g, 0));
+    UnitGeo u = unit_geo(g, q.p);
+    int curp = q.p;
+#pragma unroll 1
+    for (int kk = 0; kk < a1 - a0; ++kk) {
+        const int i = step_at(g, kk);
+        if (kk == nt && kk > 0)
+            q = decode(g, a0);
+        if (q.p != curp) {
+            u = unit_geo(g, q.p);
+            curp = q.p;
+        }
+        if (unit_ends(g, u, q, i)) {
+            if (st.uc % kEpiWarps == e && !*st.fail) {
+                const int rs = st.uc % kRedSlots;
+                const unsigned rph = static_cast<unsigned>(st.uc / kRedSlots);
+                if (!mbar_wait_bounded(&st.red_full[rs], rph & 1u)) {
+                    if (lane == 0) {
+                        set_status(a.status, kStatusTimeout);
+                        *st.fail = 1;
+                    }
+                } else {
+                    float4 tg = make_float4(0.f, 0.f, 0.f, 0.f), tu = tg;
+#pragma unroll 4
+                    for (int w2 = 0; w2 < kStreamWarps; ++w2) {
+                        const float4 *rr = st.red + ((rs * kStreamWarps + w2) * 2) * 32;
+                        const float4 vg = rr[lane];
+                        tg.x += vg.x, tg.y += vg.y, tg.z += vg.z, tg.w += vg.w;
+                        if (PHASE == 0) {
+                            const float4 vu = rr[32 + lane];
+                            tu.x += vu.x, tu.y += vu.y, tu.z += vu.z, tu.w += vu.w;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&st.red_empty[rs]);
+                    const int ustart = i - q.c, uend = ustart + u.ch;
+                    if (ustart >= a0 && uend <= a1) {
+                        finalize_unit<BITS, PHASE>(a, rv, q.p, q.s, tg, tu);
+                        count_unit<PHASE>(a, st.pspan, st.pcnt, st.ccnt, q.p, q.s);
+                    } else {
+                        fixup_unit<BITS, PHASE>(a, rv, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
+                                                st.pspan, st.ccnt);
+                    }
+                }
+            }
+            ++st.uc;
+        }
+        advance(u, q);
+    }
+}
+
+template <int BITS, bool XBF16, int KG>
+__global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_constant__ LayerArgs a)
+{
+    constexpr int NS = num_stages(BITS);
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *ring = smem + warp * ring_bytes(BITS);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * ring_bytes(BITS)) + warp * kNS;
-    if (lane == 0) {
-        for (int s = 0; s < kNS; ++s)
-            mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
     __shared__ int s_ok;
-    const int64_t w = (int64_t)blockIdx.x * kWarps + warp;
-    const int64_t Wall = (int64_t)gridDim.x * kWarps;
+    __shared__ int s_fail;
+    __shared__ unsigned s_pcnt[kMaxSpan];
+    __shared__ int s_pspan[2];
+    __shared__ unsigned s_ccnt[kMaxStripsD];
+    Stream st;
+    st.ring = smem;
+    st.red = reinterpret_cast<float4 *>(smem + NS * stage_bytes(BITS));
+    st.full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes(BITS) + red_bytes());
+    st.empty = st.full + NS;
+    st.red_full = st.empty + NS;
+    st.red_empty = st.red_full + kRedSlots;
+    st.pcnt = s_pcnt;
+    st.pspan = s_pspan;
+    st.ccnt = s_ccnt;
+    st.fail = &s_fail;
+    st.seq = 0;
+    st.uc = 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&st.full[s], 1);
+            mbar_init(&st.empty[s], kStreamWarps);
+        }
+        for (int s = 0; s < kRedSlots; ++s) {
+            mbar_init(&st.red_full[s], kStreamWarps);
+            mbar_init(&st.red_empty[s], 1);
+        }
+        fence_mbar_init();
+        s_fail = 0;
+    }
+    for (int j = threadIdx.x; j < kMaxStripsD; j += kThreads)
+        s_ccnt[j] = 0u;
+    cta_barrier();
     bool ok = true;
 
     // ------------------------------------------------------------ phase R
@@ -1051,41 +1285,151 @@ __global__ void __launch_bounds__(kThreads, 2) moe_layer_kernel(const __grid_con
         P_r = __ldcg(a.meta + 0);
         P_t = __ldcg(a.meta + 1);
     }
-    const int fmax = a.f > a.fs ? a.f : a.fs;
+    if (!ok && threadIdx.x == 0)
+        s_fail = 1;
 
     // ------------------------------------------------------------ phases G, D
-    // Phase D runs in every warp (it holds CTA barriers); a warp that failed
-    // earlier passes it with no work.
-    uint32_t ring_seq = 0;  // ring stages issued (and consumed) by earlier phases
-    if (ok)
-        ok = run_phase<BITS, XBF16, 0>(a, ring, bars, ring_seq, P_r, P_t, fmax, w, Wall, true,
-                                       &s_ok, rv);
-    ok = run_phase<BITS, XBF16, 1>(a, ring, bars, ring_seq, P_r, P_t, fmax, w, Wall, ok, &s_ok,
-                                   rv);
+    __shared__ Geo s_geo[2];
+    __shared__ Producer s_pr;
+    if (threadIdx.x == 0) {
+        s_geo[0] = make_geo(a, 0, P_r, P_t);
+        s_geo[1] = make_geo(a, 1, P_r, P_t);
+        set_order(s_geo[0]);
+        set_order(s_geo[1]);
+        s_pr.phase = 0;
+        s_pr.next = 0;
+        producer_seek(s_geo, s_pr);
+        if (s_geo[0].ch0 > KG || (P_t > P_r && s_geo[0].ch1 > KG) || s_geo[1].gk0 > kDownGroupsMax ||
+            (P_t > P_r && s_geo[1].gk1 > kDownGroupsMax)) {
+            // the host checks both limits; never reached
+            set_status(a.status, kStatusBadArg);
+            s_fail = 1;
+        }
+        // the pairs of this CTA's gate/up range, for batched strip counts
+        s_pspan[0] = 0;
+        s_pspan[1] = 0;
+        if (s_geo[0].a0 < s_geo[0].a1) {
+            const int pf = decode(s_geo[0], s_geo[0].a0).p, pl = decode(s_geo[0], s_geo[0].a1 - 1).p;
+            if (pl - pf + 1 <= kMaxSpan) {
+                s_pspan[0] = pf;
+                s_pspan[1] = pl - pf + 1;
+            }
+        }
+        for (int j = 0; j < kMaxSpan; ++j)
+            s_pcnt[j] = 0u;
+    }
+    cta_barrier();
+    st.geo = s_geo;
+    st.pr = &s_pr;
+    if (warp < kStreamWarps) {
+        stream_phase<BITS, XBF16, KG, 0>(a, rv, st);
+        stream_phase<BITS, XBF16, KG, 1>(a, rv, st);
+    } else if (warp == kProducerWarp) {
+        if (lane == 0)
+            produce_all<BITS>(a, rv, st);
+        __syncwarp();
+    } else {
+        epi_phase<BITS, 0>(a, rv, st);
+        // publish this CTA's finished gate/up strips: the barrier orders the
+        // other epilogue warp's h stores before the release fence
+        epi_barrier();
+        if (warp == kStreamWarps && lane == 0 && !s_fail) {
+            bool any = false;
+            for (int j = 0; j < s_pspan[1]; ++j)
+                any |= s_pcnt[j] != 0u;
+            if (any) {
+                fence_acq_rel();
+                for (int j = 0; j < s_pspan[1]; ++j)
+                    if (s_pcnt[j])
+                        red_add_relaxed(a.pair_done + s_pspan[0] + j, s_pcnt[j]);
+            }
+        }
+        epi_phase<BITS, 1>(a, rv, st);
+        epi_barrier();
+        if (a.fused_combine && warp == kStreamWarps && lane == 0 && !s_fail) {
+            // publish the finished down units per output strip
+            const int ns = a.d / kTileRows;
+            bool any = false;
+            for (int j = 0; j < ns; ++j)
+                any |= s_ccnt[j] != 0u;
+            if (any) {
+                fence_acq_rel();
+                for (int j = 0; j < ns; ++j)
+                    if (s_ccnt[j])
+                        red_add_relaxed(a.comb_ctr + j, s_ccnt[j]);
+            }
+        }
+    }
+    cta_barrier();
 
-    // ------------------------------------------------------------ exit: the
-    // last warp out resets the flags (counters of strips reset themselves)
-    fence_acq_rel();
-    __syncwarp();
-    unsigned old = 0;
-    if (lane == 0)
-        old = atom_add_acqrel(a.exit_ctr, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == static_cast<unsigned>(Wall - 1)) {
-        for (int p = lane; p < a.max_pairs; p += 32)
-            a.pair_done[p] = 0u;
+    // ------------------------------------------------------------ combine
+    // (T <= 8) CTA c owns output strips c, c + grid, ...: once all P_t pairs
+    // have published their down unit of a strip, y rows = sum_j w_j o_j
+    // (+ shared) in rank order.
+    if (a.fused_combine) {
+        const int ns = a.d / kTileRows;
+        if (warp == 0 && !s_fail) {
+            for (int s = blockIdx.x; s < ns; s += gridDim.x)
+                if (!warp_wait_geq(a.comb_ctr + s, static_cast<unsigned>(P_t), a.status)) {
+                    if (lane == 0)
+                        s_fail = 1;
+                    break;
+                }
+        }
+        cta_barrier();
+        if (!s_fail) {
+            const int T = static_cast<int>(a.T), kk = a.k, d = a.d;
+            const bool has_sh = P_t > P_r;
+            for (int s = blockIdx.x; s < ns; s += gridDim.x) {
+                for (int i = threadIdx.x; i < kTileRows * T; i += kThreads) {
+                    const int t = i / kTileRows, row = 16 * s + i % kTileRows;
+                    float yv = 0.f;
+                    for (int j = 0; j < kk; ++j) {
+                        const int rm = rv.route_map[t * (kk + 1) + j];
+                        yv = fmaf(rv.weights[t * kk + j], __ldcg(a.o + (int64_t)rm * d + row), yv);
+                    }
+                    if (has_sh) {
+                        const int rm = rv.route_map[t * (kk + 1) + kk];
+                        yv = fmaf(rv.shared_w[t], __ldcg(a.o + (int64_t)rm * d + row), yv);
+                    }
+                    a.y[(int64_t)t * d + row] = yv;
+                }
+                if (threadIdx.x == 0)
+                    a.comb_ctr[s] = 0u;
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ exit
+    if (warp == 0) {
         if (lane == 0) {
-            *a.route_ctr = 0u;
-            fence_acq_rel();
-            *a.exit_ctr = 0u;
+            // every stage issued has been consumed unless a wait ran out;
+            // then wait (bounded) for the copies still in flight
+            const uint32_t n = s_pr.next;
+            for (uint32_t j = n > static_cast<uint32_t>(NS) ? n - NS : 0u; j < n; ++j)
+                (void)mbar_wait_bounded(&st.full[j % NS], (j / NS) & 1u);
+        }
+        // the last CTA out resets the per-launch counters
+        unsigned old = 0;
+        if (lane == 0)
+            old = atom_add_acqrel(a.exit_ctr, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == gridDim.x - 1) {
+            for (int p = lane; p < a.max_pairs; p += 32)
+                a.pair_done[p] = 0u;
+            if (lane == 0) {
+                *a.route_ctr = 0u;
+                fence_acq_rel();
+                *a.exit_ctr = 0u;
+            }
         }
     }
 }
 
-template <int BITS, bool XBF16>
+template <int BITS, bool XBF16, int KG>
 cudaError_t launch_t(const LayerArgs &a, cudaStream_t stream)
 {
-    auto kern = moe_layer_kernel<BITS, XBF16>;
+    auto kern = moe_layer_kernel<BITS, XBF16, KG>;
     const int smem = smem_bytes(BITS);
     static int attr_done[64] = {0};
     int dev = 0;
@@ -1102,10 +1446,8 @@ cudaError_t launch_t(const LayerArgs &a, cudaStream_t stream)
         return e;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
-    if (per_sm > kMaxLayerCtasPerSm)
-        per_sm = kMaxLayerCtasPerSm;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(device_sm_count() * per_sm));
+    cfg.gridDim = dim3(static_cast<unsigned>(device_sm_count() * kMaxLayerCtasPerSm));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1154,13 +1496,23 @@ cudaError_t launch_combine(const LayerArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-int layer_grid_warps_max() { return device_sm_count() * kMaxLayerCtasPerSm * kWarps; }
+int layer_grid_ctas_max() { return device_sm_count() * kMaxLayerCtasPerSm; }
 
 cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream)
 {
+    // gate/up chunks per strip (d / 1024, rounded up) decide how many B
+    // fragments a streaming warp holds
+    const int kg = (a.d / kGroup + kChunkGroups - 1) / kChunkGroups;
+    if (kg > 4 || a.f / kGroup > kDownGroupsMax || a.fs / kGroup > kDownGroupsMax)
+        return cudaErrorInvalidValue;
+    if (kg <= 2) {
+        if (a.bits == 4)
+            return a.x_bf16 ? launch_t<4, true, 2>(a, stream) : launch_t<4, false, 2>(a, stream);
+        return a.x_bf16 ? launch_t<2, true, 2>(a, stream) : launch_t<2, false, 2>(a, stream);
+    }
     if (a.bits == 4)
-        return a.x_bf16 ? launch_t<4, true>(a, stream) : launch_t<4, false>(a, stream);
-    return a.x_bf16 ? launch_t<2, true>(a, stream) : launch_t<2, false>(a, stream);
+        return a.x_bf16 ? launch_t<4, true, 4>(a, stream) : launch_t<4, false, 4>(a, stream);
+    return a.x_bf16 ? launch_t<2, true, 4>(a, stream) : launch_t<2, false, 4>(a, stream);
 }
 
 }  // namespace smoe

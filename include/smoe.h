@@ -66,8 +66,9 @@ typedef enum { SMOE_F32 = 0, SMOE_BF16 = 1 } smoe_dtype;
 
 /* One MoE layer.  Every pointer is device memory owned by the caller. */
 typedef struct {
-    int32_t d_model;        /* hidden size d; multiple of 128                 */
-    int32_t ffn_dim;        /* routed-expert intermediate size f; mult. of 64 */
+    int32_t d_model;        /* hidden size d; multiple of 128, <= 4096        */
+    int32_t ffn_dim;        /* routed-expert intermediate size f; multiple of
+                               64, <= 2048 (one down strip per ring stage)    */
     int32_t num_experts;    /* E = router rows (max_experts_per_layer)        */
     int32_t top_k;          /* k, 1..16 and <= E                              */
     int32_t norm_topk_prob; /* nonzero: renormalise the k selected weights    */
@@ -80,7 +81,8 @@ typedef struct {
     const void *shared_tiles; /* nullable: the shared expert, written by
                                  smoe_repack with n_experts = 1 and
                                  ffn_dim = shared_ffn_dim                     */
-    int32_t shared_ffn_dim;   /* 0 = no shared expert; else multiple of 64    */
+    int32_t shared_ffn_dim;   /* 0 = no shared expert; else multiple of 64,
+                                 <= 2048                                      */
     const void *shared_gate_w; /* nullable bf16 [d]: shared-expert weight is
                                   sigmoid(shared_gate_w . x), else 1          */
 } smoe_layer_desc;

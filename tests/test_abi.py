@@ -69,6 +69,7 @@ BAD = [
     dict(bits=3), dict(bits=8), dict(group_size=32), dict(group_size=128),
     dict(top_k=0), dict(top_k=17), dict(top_k=9), dict(num_experts=0), dict(num_experts=300),
     dict(d_model=192), dict(ffn_dim=100), dict(d_model=0), dict(router_w=None),
+    dict(d_model=4224), dict(ffn_dim=2112), dict(shared_ffn_dim=2112, shared_tiles=1024),
     dict(expert_tiles=None), dict(expert_tiles=520), dict(shared_ffn_dim=64),
     dict(shared_tiles=1024), dict(shared_ffn_dim=-64, shared_tiles=1024),
 ]
