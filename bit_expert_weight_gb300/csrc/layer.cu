@@ -154,94 +154,65 @@ __device__ __forceinline__ int split_owner(const Split &sp, int u)
 
 // --------------------------------------------------------------- routing
 
-constexpr int kPerLane = kMaxExperts / 32;
+// 1 / (1 + e^-x) with the hardware exp and divide; the exponent is capped
+// so that the divisor stays finite (the result is then 0 to fp32).
+__device__ __forceinline__ float sigmoid_fast(float x)
+{
+    return __fdividef(1.0f, 1.0f + __expf(fminf(-x, 80.0f)));
+}
 
-__device__ __noinline__ void route_one_token(const float *lg, int E, int k, int norm, const float *bias,
-                                int16_t *ids_s, float *w_s, int32_t *ids_g, float *w_g,
-                                int *status)
+// Routing from the logits of one CTA's copy in shared memory.  Every CTA
+// runs the same code on the same values, so every CTA derives the same
+// tables.  Task (token t, chunk c) on one warp: lane L takes expert
+// e = 32 c + L, whose rank is the number of experts before it in the order
+// (key descending, index ascending) -- ties go to the lower index; ranks
+// below k are the selection, stored at their rank.  The softmax maximum and
+// sum run over all E logits in a fixed order (lane-strided, then a shuffle
+// tree), the same in every task; exp and divide are the hardware
+// approximations (a few ulp), well inside the weights' tolerance.
+__device__ __noinline__ void route_chunk(const float *lg, const float *key, int E, int k, int c,
+                                         int16_t *ids_s, float *p_s)
 {
     const int lane = threadIdx.x & 31;
-    float key[kPerLane], lv[kPerLane];
     float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        const int e = lane + 32 * i;
-        float l = -INFINITY, kk = -INFINITY;
-        if (e < E) {
-            l = __ldcg(lg + e);
-            if (l != l) {
-                set_status(status, kStatusBadArg);
-                l = -INFINITY;
-            }
-            kk = bias ? __fadd_rn(l, __ldg(bias + e)) : l;
-            if (kk != kk)
-                kk = -INFINITY;
-        }
-        key[i] = kk;
-        lv[i] = l;
-        m = fmaxf(m, l);
-    }
+    for (int i = lane; i < E; i += 32)
+        m = fmaxf(m, lg[i]);
     for (int o = 16; o; o >>= 1)
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i)
-        if (lane + 32 * i < E)
-            z += expf(lv[i] - m);
+    for (int i = lane; i < E; i += 32)
+        z += __expf(lg[i] - m);
     for (int o = 16; o; o >>= 1)
         z += __shfl_xor_sync(0xffffffffu, z, o);
-    unsigned taken = 0u;
-    float psel = 0.f, pj_mine = 0.f;
-    int ej_mine = 0;
-    for (int j = 0; j < k; ++j) {
-        float bk = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u))
-                if (bi == 0x7fffffff || key[i] > bk || (key[i] == bk && e < bi)) {
-                    bk = key[i];
-                    bi = e;
-                }
-        }
-        for (int o = 16; o; o >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ok > bk || (ok == bk && oi < bi))) {
-                bk = ok;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane)
-            taken |= 1u << (bi >> 5);
-        float mine = lv[0];
-#pragma unroll
-        for (int i = 1; i < kPerLane; ++i)
-            if ((bi >> 5) == i)
-                mine = lv[i];
-        const float p = expf(__shfl_sync(0xffffffffu, mine, bi & 31) - m) / z;
-        psel += p;
-        if (lane == j) {
-            pj_mine = p;
-            ej_mine = bi;
-        }
+    const int e = 32 * c + lane;
+    if (e >= E)
+        return;
+    const float ke = key[e];
+    int r = 0;
+    const float4 *k4 = reinterpret_cast<const float4 *>(key);
+#pragma unroll 2
+    for (int j = 0; j < E / 4; ++j) {
+        const float4 v = k4[j];
+        const int e0 = 4 * j;
+        r += (v.x > ke || (v.x == ke && e0 < e)) ? 1 : 0;
+        r += (v.y > ke || (v.y == ke && e0 + 1 < e)) ? 1 : 0;
+        r += (v.z > ke || (v.z == ke && e0 + 2 < e)) ? 1 : 0;
+        r += (v.w > ke || (v.w == ke && e0 + 3 < e)) ? 1 : 0;
     }
-    if (lane < k) {
-        const float wv = norm ? pj_mine / psel : pj_mine;
-        ids_s[lane] = static_cast<int16_t>(ej_mine);
-        w_s[lane] = wv;
-        if (ids_g)
-            ids_g[lane] = ej_mine;
-        if (w_g)
-            w_g[lane] = wv;
+    for (int e2 = E & ~3; e2 < E; ++e2) {
+        const float v = key[e2];
+        r += (v > ke || (v == ke && e2 < e)) ? 1 : 0;
+    }
+    if (r < k) {
+        ids_s[r] = static_cast<int16_t>(e);
+        p_s[r] = __fdividef(__expf(lg[e] - m), z);  // z in [1, E]
     }
 }
 
 // Phase R work of one warp: unit < E (+1 shared gate row) -> logits of that
 // row for all tokens; unit >= rows -> group sums of token (unit - rows).
 template <bool XBF16>
-__device__ __noinline__ void router_unit(const LayerArgs &a, int unit)
+__device__ __forceinline__ void router_unit(const LayerArgs &a, int unit)
 {
     const int lane = threadIdx.x & 31;
     const int d = a.d, T = static_cast<int>(a.T);
@@ -344,7 +315,10 @@ __device__ __noinline__ void router_unit(const LayerArgs &a, int unit)
 constexpr int kFusedPairs = kPairCols * SMOE_MAX_TOPK_DEV + 1;
 // route_map, weights and ids are [T][k+1], [T][k], [T][k] with the runtime k
 // as the row stride, exactly like the global tables.
-struct RouteSmem {
+struct __align__(16) RouteSmem {
+    float lg[kPairCols * kMaxExperts];   // [T][E4] logits, row stride E4 = E rounded up to 4
+    float key[kPairCols * kMaxExperts];  // [T][E4] selection keys fl32(logit + bias)
+    float prob[kPairCols * SMOE_MAX_TOPK_DEV];  // [T][k] softmax of the rank-j expert
     int32_t pairs[kFusedPairs][kPairInts];
     int32_t route_map[kPairCols * (SMOE_MAX_TOPK_DEV + 1)];
     float weights[kPairCols * SMOE_MAX_TOPK_DEV];
@@ -360,10 +334,10 @@ struct RouteView {
     const float *shared_w;     // [T]
 };
 
-// Warp 0 of the CTA: pair table from the routed ids (T <= 8).  Pair = one
+// One warp of the CTA: pair table from the routed ids (T <= 8).  Pair = one
 // selected expert with the ascending tokens that chose it, pairs in order of
 // first appearance; then the shared expert's pair.
-__device__ __noinline__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
+__device__ __forceinline__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
 {
     const int lane = threadIdx.x & 31;
     const int T = static_cast<int>(a.T), k = a.k, E = a.E;
@@ -489,9 +463,23 @@ __device__ __forceinline__ Geo make_geo(const LayerArgs &a, int phase, int P_r, 
     }
     g.SR = P_r * g.spp0;
     g.S = g.SR + (P_t - P_r) * g.spp1;
-    g.sp = make_split(g.S, static_cast<int>(gridDim.x));
-    g.a0 = split_start(g.sp, static_cast<int>(blockIdx.x));
-    g.a1 = split_start(g.sp, static_cast<int>(blockIdx.x) + 1);
+    const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    g.sp = make_split(g.S, C);
+    g.a0 = split_start(g.sp, c);
+    g.a1 = split_start(g.sp, c + 1);
+    // Whole units per CTA when every unit has the same chunk count and the
+    // extra unit a CTA may get costs under ~48 KB (about a microsecond of
+    // one SM's share of HBM): no unit is then shared between CTAs.
+    if (g.ch0 > 1 && (P_t == P_r || g.ch1 == g.ch0)) {
+        const int U = g.S / g.ch0;
+        const int unit_bytes = g.gk0 * (phase == 0 ? 2 : 1) * (a.bits * 128 + 32);
+        const int64_t extra = (int64_t)((U + C - 1) / C) * C - U;  // C x (max - mean) units
+        if (extra * unit_bytes < (int64_t)C * 48 * 1024) {
+            const Split su = make_split(U, C);
+            g.a0 = split_start(su, c) * g.ch0;
+            g.a1 = split_start(su, c + 1) * g.ch0;
+        }
+    }
     g.ts = g.a1;
     return g;
 }
@@ -812,15 +800,21 @@ __device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, fl
 // Finalise unit (p, s) from its full-K sums, one warp (cold path).
 // Phase 0: h = SiLU(g) * u as bf16 hi + lo and the strip's per-class sums of
 // h.  Phase 1: o.  The caller counts the finished unit.
+// What the epilogue writes, passed by value (registers) to its cold helpers.
+struct EpiOut {
+    uint16_t *h_hi, *h_lo;
+    float *hs_part, *o, *partial;
+    unsigned *strip_ctr_g, *strip_ctr_d, *pair_done;
+    int d, fmax, max_strips;
+};
+
 template <int BITS, int PHASE>
-__device__ __noinline__ void finalize_unit(const LayerArgs &a, const RouteView rv, int p, int s,
-                                           float4 ag, float4 au)
+__device__ __noinline__ void finalize_unit(const EpiOut a, int ncols, int p, int s, float4 ag, float4 au)
 {
     constexpr float L = BITS == 4 ? 7.5f : 1.5f;
     const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
     const int d = a.d;
-    const int fmax = a.f > a.fs ? a.f : a.fs;
-    const int ncols = rv.pairs[p * kPairInts + 1];
+    const int fmax = a.fmax;
     const float invL = 1.0f / L;
     const int c0 = 2 * tig;
     const float gv[4] = {ag.x, ag.y, ag.z, ag.w}, uv[4] = {au.x, au.y, au.z, au.w};
@@ -830,7 +824,7 @@ __device__ __noinline__ void finalize_unit(const LayerArgs &a, const RouteView r
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float g = gv[e] * invL, u = uv[e] * invL;
-            const float hv = g / (1.0f + expf(-g)) * u;
+            const float hv = __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;  // SiLU(g) * u
             const int col = c0 + (e & 1);
             const int row = 16 * s + gq + 8 * (e >> 1);
             if (col < ncols) {
@@ -872,7 +866,7 @@ __device__ __noinline__ void finalize_unit(const LayerArgs &a, const RouteView r
 // One more finished gate/up strip of pair p: counted in shared memory and
 // published at the end of the CTA's gate/up range, or published at once
 // (release) when the CTA's range spans too many pairs.
-__device__ __forceinline__ void count_strip(const LayerArgs &a, const int *pspan, unsigned *pcnt, int p)
+__device__ __forceinline__ void count_strip(const EpiOut &a, const int *pspan, unsigned *pcnt, int p)
 {
     if ((threadIdx.x & 31) != 0)
         return;
@@ -888,7 +882,7 @@ __device__ __forceinline__ void count_strip(const LayerArgs &a, const int *pspan
 // A finished unit: a gate/up strip of pair p, or a down unit of output
 // strip s (counted per CTA, published after the down phase).
 template <int PHASE>
-__device__ __forceinline__ void count_unit(const LayerArgs &a, const int *pspan, unsigned *pcnt,
+__device__ __forceinline__ void count_unit(const EpiOut &a, const int *pspan, unsigned *pcnt,
                                            unsigned *ccnt, int p, int s)
 {
     if (PHASE == 0)
@@ -902,9 +896,9 @@ __device__ __forceinline__ void count_unit(const LayerArgs &a, const int *pspan,
 // finalises.  Slot 0 of a CTA holds the unit straddling its first step,
 // slot 1 the one straddling its last; each phase has its own slots.
 template <int BITS, int PHASE>
-__device__ __noinline__ void fixup_unit(const LayerArgs &a, const RouteView rv, const Geo &g, int p,
-                                        int s, int ustart, int uend, float4 tg, float4 tu,
-                                        unsigned *pcnt, const int *pspan, unsigned *ccnt)
+__device__ __noinline__ void fixup_unit(const EpiOut a, int ncols, const Geo &g, int p, int s, int ustart,
+                                        int uend, float4 tg, float4 tu, unsigned *pcnt, const int *pspan,
+                                        unsigned *ccnt)
 {
     const int lane = threadIdx.x & 31;
     float4 *part = reinterpret_cast<float4 *>(a.partial) + (size_t)PHASE * gridDim.x * 2 * 64;
@@ -946,7 +940,7 @@ __device__ __noinline__ void fixup_unit(const LayerArgs &a, const RouteView rv, 
     }
     if (lane == 0)
         *ctr = 0u;
-    finalize_unit<BITS, PHASE>(a, rv, p, s, sg, su);
+    finalize_unit<BITS, PHASE>(a, ncols, p, s, sg, su);
     count_unit<PHASE>(a, pspan, pcnt, ccnt, p, s);
 }
 
@@ -1114,6 +1108,18 @@ template <int BITS, int PHASE>
 __device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
     const int e = (threadIdx.x >> 5) - kStreamWarps, lane = threadIdx.x & 31;
+    EpiOut eo;
+    eo.h_hi = a.h_hi;
+    eo.h_lo = a.h_lo;
+    eo.hs_part = a.hs_part;
+    eo.o = a.o;
+    eo.partial = a.partial;
+    eo.strip_ctr_g = a.strip_ctr_g;
+    eo.strip_ctr_d = a.strip_ctr_d;
+    eo.pair_done = a.pair_done;
+    eo.d = a.d;
+    eo.fmax = a.f > a.fs ? a.f : a.fs;
+    eo.max_strips = a.max_strips;
     const Geo &g = st.geo[PHASE];
     const int a0 = g.a0, a1 = g.a1, nt = g.a1 - g.ts;
     if (a0 >= a1)
@@ -1155,11 +1161,12 @@ __device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &r
                     if (lane == 0)
                         mbar_arrive(&st.red_empty[rs]);
                     const int ustart = i - q.c, uend = ustart + u.ch;
+                    const int ncols = rv.pairs[q.p * kPairInts + 1];
                     if (ustart >= a0 && uend <= a1) {
-                        finalize_unit<BITS, PHASE>(a, rv, q.p, q.s, tg, tu);
-                        count_unit<PHASE>(a, st.pspan, st.pcnt, st.ccnt, q.p, q.s);
+                        finalize_unit<BITS, PHASE>(eo, ncols, q.p, q.s, tg, tu);
+                        count_unit<PHASE>(eo, st.pspan, st.pcnt, st.ccnt, q.p, q.s);
                     } else {
-                        fixup_unit<BITS, PHASE>(a, rv, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
+                        fixup_unit<BITS, PHASE>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
                                                 st.pspan, st.ccnt);
                     }
                 }
@@ -1246,27 +1253,58 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
         cta_barrier();
         ok = s_ok != 0;
-        // route the tokens (one warp each), then warp 0 builds the pair table
-        if (ok && warp < a.T) {
-            const bool out = blockIdx.x == 0;
+        // route: stage logits and keys, rank every expert, then warp t
+        // turns token t's selection into weights; the last warp builds the pairs
+        const int T = static_cast<int>(a.T), E = a.E, kk = a.k, E4 = (a.E + 3) & ~3;
+        if (ok) {
+            for (int idx = threadIdx.x; idx < T * E; idx += kThreads) {
+                const int t = idx / E, e = idx - t * E;
+                float l = __ldcg(a.logits + (int64_t)t * a.Epad + e);
+                if (l != l) {
+                    set_status(a.status, kStatusBadArg);
+                    l = -INFINITY;
+                }
+                float key = a.expert_bias ? __fadd_rn(l, __ldg(a.expert_bias + e)) : l;
+                if (key != key)
+                    key = -INFINITY;
+                rs.lg[t * E4 + e] = l;
+                rs.key[t * E4 + e] = key;
+            }
+        }
+        cta_barrier();
+        if (ok) {
+            const int nc = (E + 31) / 32;
+            for (int task = warp; task < T * nc; task += kWarps) {
+                const int t = task / nc, c = task - t * nc;
+                route_chunk(rs.lg + t * E4, rs.key + t * E4, E, kk, c, rs.ids + t * kk, rs.prob + t * kk);
+            }
+        }
+        cta_barrier();
+        if (ok && warp < T) {
             const int t = warp;
-            route_one_token(a.logits + (int64_t)t * a.Epad, a.E, a.k, a.norm, a.expert_bias,
-                            rs.ids + t * a.k, rs.weights + t * a.k, out ? a.ids + t * a.k : nullptr,
-                            out ? a.weights + t * a.k : nullptr, a.status);
-            __syncwarp();
-            if (out) {
-                if (a.ids_out && lane < a.k)
-                    a.ids_out[t * a.k + lane] = rs.ids[t * a.k + lane];
-                if (a.w_out && lane < a.k)
-                    a.w_out[t * a.k + lane] = rs.weights[t * a.k + lane];
+            float psel = 0.f;
+            for (int j = 0; j < kk; ++j)
+                psel += rs.prob[t * kk + j];
+            if (lane < kk) {
+                const float pj = rs.prob[t * kk + lane];
+                const float wv = a.norm ? __fdividef(pj, psel) : pj;
+                rs.weights[t * kk + lane] = wv;
+                if (blockIdx.x == 0) {
+                    const int id = rs.ids[t * kk + lane];
+                    a.ids[t * kk + lane] = id;
+                    a.weights[t * kk + lane] = wv;
+                    if (a.ids_out)
+                        a.ids_out[t * kk + lane] = id;
+                    if (a.w_out)
+                        a.w_out[t * kk + lane] = wv;
+                }
             }
             if (lane == 0)
                 rs.shared_w[t] =
-                    a.shared_gate ? 1.0f / (1.0f + expf(-__ldcg(a.logits + (int64_t)t * a.Epad + a.E)))
-                                  : 1.0f;
+                    a.shared_gate ? sigmoid_fast(__ldcg(a.logits + (int64_t)t * a.Epad + a.E)) : 1.0f;
         }
-        cta_barrier();
-        if (ok && warp == 0)
+        // the pair table needs only the ids: built while the weights are
+        if (ok && warp == kWarps - 1)
             cta_dispatch(a, rs);
         cta_barrier();
         rv.pairs = &rs.pairs[0][0];
@@ -1291,32 +1329,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     // ------------------------------------------------------------ phases G, D
     __shared__ Geo s_geo[2];
     __shared__ Producer s_pr;
+    if (lane == 0 && warp < 2) {
+        Geo gg = make_geo(a, warp, P_r, P_t);
+        set_order(gg);
+        s_geo[warp] = gg;
+    }
+    cta_barrier();
     if (threadIdx.x == 0) {
-        s_geo[0] = make_geo(a, 0, P_r, P_t);
-        s_geo[1] = make_geo(a, 1, P_r, P_t);
-        set_order(s_geo[0]);
-        set_order(s_geo[1]);
-        s_pr.phase = 0;
-        s_pr.next = 0;
-        producer_seek(s_geo, s_pr);
         if (s_geo[0].ch0 > KG || (P_t > P_r && s_geo[0].ch1 > KG) || s_geo[1].gk0 > kDownGroupsMax ||
             (P_t > P_r && s_geo[1].gk1 > kDownGroupsMax)) {
             // the host checks both limits; never reached
             set_status(a.status, kStatusBadArg);
             s_fail = 1;
         }
-        // the pairs of this CTA's gate/up range, for batched strip counts
-        s_pspan[0] = 0;
-        s_pspan[1] = 0;
-        if (s_geo[0].a0 < s_geo[0].a1) {
-            const int pf = decode(s_geo[0], s_geo[0].a0).p, pl = decode(s_geo[0], s_geo[0].a1 - 1).p;
-            if (pl - pf + 1 <= kMaxSpan) {
-                s_pspan[0] = pf;
-                s_pspan[1] = pl - pf + 1;
-            }
-        }
-        for (int j = 0; j < kMaxSpan; ++j)
-            s_pcnt[j] = 0u;
     }
     cta_barrier();
     st.geo = s_geo;
@@ -1325,10 +1350,32 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         stream_phase<BITS, XBF16, KG, 0>(a, rv, st);
         stream_phase<BITS, XBF16, KG, 1>(a, rv, st);
     } else if (warp == kProducerWarp) {
-        if (lane == 0)
-            produce_all<BITS>(a, rv, st);
+        if (lane == 0) {
+            s_pr.phase = 0;
+            s_pr.next = 0;
+            producer_seek(s_geo, s_pr);
+            if (!s_fail)
+                produce_all<BITS>(a, rv, st);
+        }
         __syncwarp();
     } else {
+        if (warp == kStreamWarps) {
+            // the pairs of this CTA's gate/up range, for batched strip counts
+            if (lane == 0) {
+                s_pspan[0] = 0;
+                s_pspan[1] = 0;
+                if (s_geo[0].a0 < s_geo[0].a1) {
+                    const int pf = decode(s_geo[0], s_geo[0].a0).p, pl = decode(s_geo[0], s_geo[0].a1 - 1).p;
+                    if (pl - pf + 1 <= kMaxSpan) {
+                        s_pspan[0] = pf;
+                        s_pspan[1] = pl - pf + 1;
+                    }
+                }
+            }
+            for (int j = lane; j < kMaxSpan; j += 32)
+                s_pcnt[j] = 0u;
+        }
+        epi_barrier();
         epi_phase<BITS, 0>(a, rv, st);
         // publish this CTA's finished gate/up strips: the barrier orders the
         // other epilogue warp's h stores before the release fence
