@@ -387,17 +387,17 @@ __device__ __forceinline__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
 
 // ------------------------------------------------------------ streaming
 
-// A chunk is a run of consecutive groups of one strip; one stage of the
-// CTA's ring holds one chunk.  Gate/up: up to kChunkGroups groups (one per
-// streaming warp, gate and up tile each); down: the whole strip, up to
-// 2 * kChunkGroups groups (two per warp, one tile each) -- the same bytes.
-constexpr int kChunkGroups = kStreamWarps;
-constexpr int kDownGroupsMax = 2 * kChunkGroups;  // ffn_dim <= 2048
+// A chunk is a run of up to kChunkGroups consecutive groups of one strip,
+// two per streaming warp (groups w and w + 16 of the chunk); one stage of
+// the CTA's ring holds one chunk.  Gate/up: a strip of d/64 groups in 1 or
+// 2 chunks (gate and up tile per group); down: the whole strip in one chunk.
+constexpr int kChunkGroups = 2 * kStreamWarps;
+constexpr int kDownGroupsMax = kChunkGroups;  // ffn_dim <= 2048
 
 __host__ __device__ constexpr int stage_bytes(int bits) { return kChunkGroups * 2 * tile_bytes(bits); }
-// About 64 KB in flight per SM: enough for the full HBM rate, and no deeper,
-// since every other memory access of the SM queues behind the ring.
-__host__ __device__ constexpr int num_stages(int bits) { return bits == 4 ? 4 : 7; }
+// About 100 KB in flight per SM: the full HBM rate needs ~64 KB; deeper
+// rings delay every other memory access of the SM, which queues behind them.
+__host__ __device__ constexpr int num_stages(int bits) { return bits == 4 ? 3 : 5; }
 // kRedSlots slots of per-warp unit sums (gate and up float4 per lane)
 constexpr int kRedSlots = 4;
 __host__ __device__ constexpr int red_bytes() { return kRedSlots * kStreamWarps * 2 * 32 * 16; }
@@ -966,10 +966,9 @@ __device__ __forceinline__ bool unit_ends(const Geo &g, const UnitGeo &u, const 
 }
 
 // One phase (0: gate/up, 1: down) of a streaming warp.  The warp holds the
-// B fragments of its groups of the current pair: gate/up -- group
-// c * gc + w of each chunk c (at most KG chunks); down -- groups w and
-// w + 16 of the single chunk (the whole strip).  At a unit's end it leaves
-// its sums in a slot for the epilogue warps.
+// B fragments of its groups of the current pair: groups c * gc + w and
+// c * gc + w + 16 of each chunk c (gate/up: at most KG chunks; down: one).
+// At a unit's end it leaves its sums in a slot for the epilogue warps.
 template <int BITS, bool XBF16, int KG, int PHASE>
 __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
@@ -977,7 +976,7 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
     constexpr int GB = PHASE == 0 ? 2 * TB : TB;
     constexpr int NV = (PHASE == 1 || !XBF16) ? 4 : 2;
     constexpr bool kSplit = PHASE == 1 || !XBF16;
-    constexpr int NB = PHASE == 0 ? KG : 2;  // B fragments held
+    constexpr int NB = PHASE == 0 ? 2 * KG : 2;  // B fragments held
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geo &g = st.geo[PHASE];
     const int a0 = g.a0, a1 = g.a1, n = a1 - a0, ts = g.ts, nt = a1 - ts;
@@ -989,6 +988,7 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
     int loaded = -1;
     BFrag bf[NB];
     float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+    float accg2[4] = {0.f, 0.f, 0.f, 0.f}, accu2[4] = {0.f, 0.f, 0.f, 0.f};  // gate/up: second group
 #pragma unroll 1
     for (int kk = 0; kk < n; ++kk) {
         const int i = kk < nt ? ts + kk : a0 + (kk - nt);
@@ -1011,8 +1011,9 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
             const PairInfo pi = read_pair(rv, q.p);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const int gi = PHASE == 0 ? b * u.gc + warp : warp + b * kChunkGroups;
-                if ((PHASE == 1 || b < u.ch) && gi < u.gk && (PHASE == 1 || warp < u.gc)) {
+                const int c = b >> 1, lg = warp + (b & 1) * kStreamWarps;  // chunk, group in chunk
+                const int gi = c * u.gc + lg;
+                if (c < u.ch && lg < u.gc && gi < u.gk) {
                     BRaw<NV> raw;
                     load_raw<PHASE, XBF16, NV>(a, pi, q.p, gi, fmax, raw);
                     cook_b<BITS, PHASE, XBF16, NV>(raw, bf[b]);
@@ -1031,22 +1032,28 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
         }
         if (ok) {
             const uint8_t *stage = st.ring + slot * SB;
+            const int ng = min(u.gc, u.gk - q.c * u.gc);  // groups in this chunk
+            const bool g0 = warp < ng, g1 = warp + kStreamWarps < ng;
             if (PHASE == 0) {
-                const int gi = q.c * u.gc + warp;
-                if (warp < u.gc && gi < u.gk) {
+                // two groups, gate and up tile each: four independent chains
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        if (b == q.c) {
-                            mac_tile<BITS, kSplit>(stage + warp * GB, bf[b], accg);
-                            mac_tile<BITS, kSplit>(stage + warp * GB + TB, bf[b], accu);
+                for (int c = 0; c < KG; ++c) {
+                    if (c == q.c) {
+                        if (g0) {
+                            mac_tile<BITS, kSplit>(stage + warp * GB, bf[2 * c], accg);
+                            mac_tile<BITS, kSplit>(stage + warp * GB + TB, bf[2 * c], accu);
+                        }
+                        if (g1) {
+                            mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[2 * c + 1], accg2);
+                            mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB + TB, bf[2 * c + 1], accu2);
                         }
                     }
                 }
             } else {
-                if (warp < u.gk)
+                if (g0)
                     mac_tile<BITS, kSplit>(stage + warp * GB, bf[0], accg);
-                if (warp + kChunkGroups < u.gk)
-                    mac_tile<BITS, kSplit>(stage + (warp + kChunkGroups) * GB, bf[1], accu);
+                if (g1)
+                    mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[1], accu);
             }
         }
         __syncwarp();
@@ -1061,11 +1068,15 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
                 set_status(a.status, kStatusTimeout);
                 *st.fail = 1;
             }
-            if (PHASE == 1) {
-                // the two groups' partial sums of the same output rows
+            // the two groups' partial sums of the same output rows
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
+            for (int e = 0; e < 4; ++e) {
+                if (PHASE == 1) {
                     accg[e] += accu[e];
+                } else {
+                    accg[e] += accg2[e];
+                    accu[e] += accu2[e];
+                }
             }
             float4 *rw = st.red + ((rs * kStreamWarps + warp) * 2) * 32;
             rw[lane] = make_float4(accg[0], accg[1], accg[2], accg[3]);
@@ -1073,7 +1084,7 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
                 rw[32 + lane] = make_float4(accu[0], accu[1], accu[2], accu[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                accg[e] = accu[e] = 0.f;
+                accg[e] = accu[e] = accg2[e] = accu2[e] = 0.f;
             __syncwarp();
             if (lane == 0 && !*st.fail)
                 mbar_arrive(&st.red_full[rs]);
@@ -1547,19 +1558,19 @@ int layer_grid_ctas_max() { return device_sm_count() * kMaxLayerCtasPerSm; }
 
 cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream)
 {
-    // gate/up chunks per strip (d / 1024, rounded up) decide how many B
+    // gate/up chunks per strip (d / 2048, rounded up) decide how many B
     // fragments a streaming warp holds
     const int kg = (a.d / kGroup + kChunkGroups - 1) / kChunkGroups;
-    if (kg > 4 || a.f / kGroup > kDownGroupsMax || a.fs / kGroup > kDownGroupsMax)
+    if (kg > 2 || a.f / kGroup > kDownGroupsMax || a.fs / kGroup > kDownGroupsMax)
         return cudaErrorInvalidValue;
-    if (kg <= 2) {
+    if (kg <= 1) {
         if (a.bits == 4)
-            return a.x_bf16 ? launch_t<4, true, 2>(a, stream) : launch_t<4, false, 2>(a, stream);
-        return a.x_bf16 ? launch_t<2, true, 2>(a, stream) : launch_t<2, false, 2>(a, stream);
+            return a.x_bf16 ? launch_t<4, true, 1>(a, stream) : launch_t<4, false, 1>(a, stream);
+        return a.x_bf16 ? launch_t<2, true, 1>(a, stream) : launch_t<2, false, 1>(a, stream);
     }
     if (a.bits == 4)
-        return a.x_bf16 ? launch_t<4, true, 4>(a, stream) : launch_t<4, false, 4>(a, stream);
-    return a.x_bf16 ? launch_t<2, true, 4>(a, stream) : launch_t<2, false, 4>(a, stream);
+        return a.x_bf16 ? launch_t<4, true, 2>(a, stream) : launch_t<4, false, 2>(a, stream);
+    return a.x_bf16 ? launch_t<2, true, 2>(a, stream) : launch_t<2, false, 2>(a, stream);
 }
 
 }  // namespace smoe
