@@ -127,13 +127,14 @@ class Workload:
 
     def __init__(self, name, d, f, E, k, norm, bits_list, T_list, layers, seed,
                  x_dtype="bf16", p_out=0.01, p_zero=0.0, router_p_out=None,
-                 router_p_zero=None, shared_f=0, shared_gate=False, zipf_s=None):
+                 router_p_zero=None, shared_f=0, shared_gate=False, zipf_s=None, zipf_tau=None):
         self.name, self.d, self.f, self.E, self.k, self.norm = name, d, f, E, k, norm
         self.bits_list, self.T_list, self.layers, self.seed = bits_list, T_list, layers, seed
         self.x_dtype, self.p_out, self.p_zero = x_dtype, p_out, p_zero
         self.router_p_out = p_out if router_p_out is None else router_p_out
         self.router_p_zero = p_zero if router_p_zero is None else router_p_zero
         self.shared_f, self.shared_gate, self.zipf_s = shared_f, shared_gate, zipf_s
+        self.zipf_tau = zipf_tau
 
     sigma = 0.02
 
@@ -153,6 +154,61 @@ class Workload:
     def shared_gate_weight(self, layer):
         key = stream_key(self.seed, layer, SHARED_EXPERT, ROLE_SHARED_GATE)
         return values_bf16(key, self.d, self.sigma).reshape(self.d)
+
+    # ---------------------------------------------------------- Zipf routing
+    # Workload construction for the batched Qwen-like config: expert
+    # popularity p_e proportional to rank^-s over a seeded permutation, turned
+    # into the selection-only expert_bias tau * ln p_e; tau is calibrated so
+    # that the share of tokens whose top-k contains the most popular expert
+    # matches p_1 within 10 %.  The same bias array is an input to both the
+    # GPU path and the oracle.
+
+    def zipf_ranks(self):
+        """rank[e] in 1..E (1 = most popular), a seeded permutation."""
+        key = stream_key(self.seed, 0, 0, ROLE_BIAS)
+        order = np.argsort(words(key, 0, self.E), kind="stable")
+        rank = np.empty(self.E, dtype=np.int64)
+        rank[order] = np.arange(1, self.E + 1)
+        return rank
+
+    def zipf_p(self):
+        r = self.zipf_ranks().astype(np.float64) ** (-self.zipf_s)
+        return r / r.sum()
+
+    def zipf_bias(self, tau=None):
+        """fp32 [E] selection-only bias tau * ln p_e."""
+        tau = self.zipf_tau if tau is None else tau
+        return (tau * np.log(self.zipf_p())).astype(np.float32)
+
+    def zipf_logits(self, layer, n_tokens):
+        x, _ = self.activations(layer, n_tokens)
+        r = bf16_to_f32(self.router_weight(layer)).astype(np.float64)
+        return x.astype(np.float64) @ r.T
+
+    def zipf_share(self, layer, tau, n_tokens, logits=None):
+        """Share of the first n_tokens tokens whose top-k (by logit plus bias,
+        numpy argpartition) contains the most popular expert."""
+        lg = self.zipf_logits(layer, n_tokens) if logits is None else logits
+        key = lg + self.zipf_bias(tau).astype(np.float64)
+        top = np.argpartition(-key, self.k - 1, axis=1)[:, :self.k]
+        hot = int(np.argmin(self.zipf_ranks()))
+        return float(np.mean(np.any(top == hot, axis=1)))
+
+    def calibrate_zipf_tau(self, layer=0, n_tokens=4096, iters=30):
+        """Bisection on tau in [0, 8] for share(tau) = p_1 (within 10 %)."""
+        target = float(self.zipf_p().max())
+        lg = self.zipf_logits(layer, n_tokens)
+        lo, hi = 0.0, 8.0
+        for _ in range(iters):
+            mid = 0.5 * (lo + hi)
+            sh = self.zipf_share(layer, mid, n_tokens, lg)
+            if abs(sh - target) <= 0.1 * target:
+                return mid, sh, target
+            if sh < target:
+                lo = mid
+            else:
+                hi = mid
+        return mid, sh, target
 
     def activations(self, layer, T, start_token=0):
         """x [T, d]: fp32 values (bf16-rounded when x_dtype == 'bf16').
@@ -175,7 +231,9 @@ WORKLOADS = {
     "qwen235b": Workload("Qwen3-235B-like decode d4096 f1536 E128 k8 renorm Q4", 4096, 1536, 128,
                          8, True, [4], [1], 94, 2),
     "qwen235b_batched": Workload("Qwen3-235B-like layer batched (Zipf 1.1)", 4096, 1536, 128, 8,
-                                 True, [4], [1, 8, 64, 512, 4096], 1, 3, zipf_s=1.1),
+                                 True, [4], [1, 8, 64, 512, 4096], 1, 3, zipf_s=1.1,
+                                 # calibrate_zipf_tau(layer 0, 4096 tokens): share 0.2424 vs p_1 0.2257
+                                 zipf_tau=0.375),
     "a3b35b": Workload("35B-A3B-like fine-grained layer d2048 f512 E256 k8 + shared", 2048, 512,
                        256, 8, True, [4, 2], [1, 256], 40, 4, shared_f=512, shared_gate=True),
 }

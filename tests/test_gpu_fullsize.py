@@ -1,0 +1,184 @@
+"""GPU parity at the full layer geometries of the benchmark workloads, in the
+launch configuration bench.py times (one layer per forward call).
+
+The oracle cannot run a whole full-size layer in seconds, so each test
+samples a few tokens: the oracle routes them from fixed host logits and
+quantises only the experts they select; every other expert is generated and
+quantised on the device (it does not affect the sampled tokens).  The GPU
+forward runs over all T tokens; the sampled rows of y, their expert ids
+(bit-exact except near ties) and weights are compared with the oracle.
+"""
+import multiprocessing as mp
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as O  # noqa: E402
+from bit_expert_weight_gb300 import synth as Y  # noqa: E402
+
+from helpers import near_tie_tokens, to_dev, to_dev_bf16  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+ROLES = (Y.ROLE_GATE, Y.ROLE_UP, Y.ROLE_DOWN)
+
+
+def _oracle_expert(args):
+    """Pool worker: host weights of one expert, quantised by the oracle."""
+    wl_name, layer, e, bits = args
+    wl = Y.WORKLOADS[wl_name]
+    qs = [O.quantize(wl.expert_weight(layer, e, r), bits) for r in ROLES]
+    return e, [(q["codes_lsb"], q["scales_f16"]) for q in qs]
+
+
+@pytest.fixture(scope="module")
+def pool():
+    # spawn: the workers never inherit a CUDA context
+    p = mp.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 1)))
+    yield p
+    p.close()
+    p.join()
+
+
+@pytest.fixture(scope="module")
+def S():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_expert_weight_gb300 import build
+    build.build()
+    import bit_expert_weight_gb300.smoe as S
+    S.load()
+    return S
+
+
+class FullLayer:
+    """One full-geometry layer: oracle-quantised experts for the sampled
+    tokens' selections, device-quantised experts elsewhere."""
+
+    def __init__(self, S, pool, wl_name, layer, bits, sample, bias=None):
+        wl = Y.WORKLOADS[wl_name]
+        self.wl, self.layer, self.bits, self.sample, self.bias = wl, layer, bits, list(sample), bias
+        self.router = wl.router_weight(layer)
+        xs = np.stack([wl.activations(layer, 1, start_token=t)[0][0] for t in self.sample])
+        self.x_sample = xs
+        lg = O.router_logits(self.router, xs)
+        ids, _ = O.route(lg, wl.k, wl.norm, bias)
+        self.logits = lg
+        chosen = sorted(set(int(e) for e in np.asarray(ids).ravel()))
+        jobs = [(wl_name, layer, e, bits) for e in chosen]
+        if wl.shared_f:
+            jobs.append((wl_name, layer, Y.SHARED_EXPERT, bits))
+        got = dict(pool.map(_oracle_expert, jobs))
+        self.blob = {e: O.make_blob(*[{"codes_lsb": c, "scales_f16": s} for c, s in got[e]])
+                     for e in chosen}
+        self.shared_blob = None
+        if wl.shared_f:
+            self.shared_blob = O.make_blob(*[{"codes_lsb": c, "scales_f16": s}
+                                             for c, s in got[Y.SHARED_EXPERT]])
+        # device bank
+        codes, scales = [], []
+        for e in range(wl.E):
+            for r_i, r in enumerate(ROLES):
+                if e in got:
+                    c, s = got[e][r_i]
+                    codes.append(to_dev(c, DEV))
+                    scales.append(to_dev(s.view(np.int16), DEV))
+                else:
+                    c, s = self._device_quantised(S, e, r)
+                    codes.append(c)
+                    scales.append(s)
+        tiles = S.repack(codes, scales, wl.d, wl.f, wl.E, bits)
+        sh_tiles, sh_gate = None, None
+        if wl.shared_f:
+            sc = [to_dev(c, DEV) for c, _ in got[Y.SHARED_EXPERT]]
+            ss = [to_dev(s.view(np.int16), DEV) for _, s in got[Y.SHARED_EXPERT]]
+            sh_tiles = S.repack(sc, ss, wl.d, wl.shared_f, 1, bits)
+            if wl.shared_gate:
+                self.shared_gate = wl.shared_gate_weight(layer)
+                sh_gate = to_dev_bf16(self.shared_gate, DEV)
+        if not wl.shared_gate:
+            self.shared_gate = None
+        bias_t = None if bias is None else to_dev(bias.astype(np.float32), DEV)
+        self.lay = S.MoELayer(wl.d, wl.f, wl.E, wl.k, wl.norm, bits, to_dev_bf16(self.router, DEV),
+                              tiles, expert_bias=bias_t, shared_tiles=sh_tiles, shared_f=wl.shared_f,
+                              shared_gate_w=sh_gate)
+        del codes, scales
+
+    def _device_quantised(self, S, e, role):
+        wl = self.wl
+        rows, cols = (wl.f, wl.d) if role in (Y.ROLE_GATE, Y.ROLE_UP) else (wl.d, wl.f)
+        w = torch.empty(rows * cols, dtype=torch.int16, device=DEV)
+        S.synth_bf16(w, Y.stream_key(wl.seed, self.layer, e, role), wl.sigma, p_out=wl.p_out,
+                     p_zero=wl.p_zero)
+        return S.quantize(w.view(torch.bfloat16).view(rows, cols), self.bits)
+
+    def device_x(self, S, T):
+        """x [T, d] bf16 on the device: the generator's device twin."""
+        wl = self.wl
+        x = torch.empty(T * wl.d, dtype=torch.int16, device=DEV)
+        S.synth_bf16(x, Y.stream_key(wl.seed, self.layer, 0, Y.ROLE_X), 1.0)
+        return x.view(torch.bfloat16).view(T, wl.d)
+
+    def check(self, S, T, tol=1e-3):
+        wl = self.wl
+        assert max(self.sample) < T
+        xt = self.device_x(S, T)
+        ws = S.workspace(self.lay, T)
+        ids = torch.empty((T, wl.k), dtype=torch.int32, device=DEV)
+        w = torch.empty((T, wl.k), dtype=torch.float32, device=DEV)
+        y = S.forward(self.lay, xt, ws, ids=ids, w=w)
+        torch.cuda.synchronize()
+        assert S.device_status() == 0
+        # the device x rows are the host generator's rows, bit for bit
+        xs = xt[self.sample].float().cpu().numpy()
+        assert np.array_equal(xs, self.x_sample)
+        yg = y[self.sample].cpu().numpy()
+        idg = ids[self.sample].cpu().numpy()
+        wg = w[self.sample].cpu().numpy()
+        y_ref, ids_ref, w_ref, lg = O.moe_forward(wl.d, wl.f, wl.E, wl.k, wl.norm, self.bits,
+                                                  self.router, self.blob, self.x_sample,
+                                                  expert_bias=self.bias,
+                                                  shared_blob=self.shared_blob, fs=wl.shared_f,
+                                                  shared_gate=self.shared_gate)
+        ties = set(near_tie_tokens(lg, wl.k, self.bias))
+        mism = [i for i in range(len(self.sample)) if not np.array_equal(idg[i], ids_ref[i])]
+        assert set(mism) <= ties, f"routing differs on non-tie sampled tokens {mism}"
+        ok = [i for i in range(len(self.sample)) if i not in mism]
+        assert np.allclose(wg[ok], w_ref[ok], rtol=1e-5, atol=1e-6)
+        err = float(np.abs(yg[ok] - y_ref[ok]).max()) if ok else 0.0
+        bound = tol * float(np.abs(y_ref[ok]).max()) if ok else 1.0
+        assert err <= bound, f"T={T}: max abs err {err:.3e} > {bound:.3e}"
+        return err, bound
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_deepseek16b_layer_full_size(S, pool, bits):
+    fl = FullLayer(S, pool, "deepseek16b", 0, bits, sample=[0])
+    fl.check(S, 1)
+
+
+def test_qwen235b_decode_layer_full_size(S, pool):
+    fl = FullLayer(S, pool, "qwen235b", 0, 4, sample=[0])
+    fl.check(S, 1)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_a3b35b_layer_full_size(S, pool, bits):
+    """Shared expert with a sigmoid gate; T = 1 and T = 256 (sampled)."""
+    fl = FullLayer(S, pool, "a3b35b", 0, bits, sample=[0, 3, 255])
+    fl.check(S, 256)
+    fl1 = FullLayer(S, pool, "a3b35b", 1, bits, sample=[0])
+    fl1.check(S, 1)
+
+
+def test_qwen235b_batched_zipf_full_size(S, pool):
+    """Zipf(1.1)-skewed selection bias; T = 8, 64, 512, 4096 with the same
+    sampled tokens (token i is the same vector whatever T)."""
+    wl = Y.WORKLOADS["qwen235b_batched"]
+    bias = wl.zipf_bias()
+    fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=[0, 5], bias=bias)
+    for T in (8, 64, 512, 4096):
+        fl.check(S, T)

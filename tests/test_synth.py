@@ -42,3 +42,23 @@ def test_bf16_rounding_is_nearest_even():
     assert S.bf16_to_f32(bits)[2] == np.float32(1.015625)
     ref = v.astype(np.float32)
     assert np.all(np.abs(S.bf16_to_f32(bits) - ref) <= np.abs(ref) * 2.0 ** -8)
+
+
+def test_zipf_bias_construction():
+    """The batched Qwen-like workload's selection-only bias: a seeded
+    permutation of Zipf(1.1) popularities, tau calibrated so the most popular
+    expert is in the top-k of ~p_1 of the tokens (checked on a 1024-token
+    sample, with the margin widened for the smaller sample)."""
+    wl = S.WORKLOADS["qwen235b_batched"]
+    rank = wl.zipf_ranks()
+    assert sorted(rank.tolist()) == list(range(1, wl.E + 1))
+    p = wl.zipf_p()
+    assert abs(p.sum() - 1.0) < 1e-12
+    assert np.allclose(p * (rank.astype(float) ** 1.1), p[np.argmin(rank)])
+    b = wl.zipf_bias()
+    assert b.dtype == np.float32 and np.array_equal(b, wl.zipf_bias())
+    target = float(p.max())
+    lg = wl.zipf_logits(0, 1024)
+    s_lo, s_mid, s_hi = (wl.zipf_share(0, t, 1024, lg) for t in (0.25, wl.zipf_tau, 0.5))
+    assert s_lo < s_mid < s_hi
+    assert abs(s_mid - target) <= 0.2 * target
