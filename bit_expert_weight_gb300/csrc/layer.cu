@@ -319,6 +319,8 @@ struct __align__(16) RouteSmem {
     float lg[kPairCols * kMaxExperts];   // [T][E4] logits, row stride E4 = E rounded up to 4
     float key[kPairCols * kMaxExperts];  // [T][E4] selection keys fl32(logit + bias)
     float prob[kPairCols * SMOE_MAX_TOPK_DEV];  // [T][k] softmax of the rank-j expert
+    float warm_p[SMOE_MAX_TOPK_DEV];     // scratch of the instruction-cache warm-up
+    int16_t warm_id[SMOE_MAX_TOPK_DEV];
     int32_t pairs[kFusedPairs][kPairInts];
     int32_t route_map[kPairCols * (SMOE_MAX_TOPK_DEV + 1)];
     float weights[kPairCols * SMOE_MAX_TOPK_DEV];
@@ -624,7 +626,8 @@ __device__ __forceinline__ PairInfo read_pair(const RouteView &rv, int p)
 }
 
 // mma B fragments of one group (hi and, for fp32 / h activations, lo) and
-// the two column biases -(128 + L) X (Q2: -(129.5 X0 + 33.5 X1)).
+// the two column biases -(128 + L) X (Q2: -(129.5 X0 + 33.5 X1)), stored
+// negated: they are the C operand of a tile's first mma.
 struct BFrag {
     uint32_t b0[4], b1[4], b0l[4], b1l[4];
     float bias0, bias1;
@@ -639,11 +642,11 @@ __device__ __forceinline__ void finish_bias(BFrag &f, float2 x0, float2 x1)
             f.b1[j] = bf16x2_quarter(f.b1[j]);
             f.b1l[j] = bf16x2_quarter(f.b1l[j]);
         }
-        f.bias0 = 129.5f * x0.x + 33.5f * x0.y;
-        f.bias1 = 129.5f * x1.x + 33.5f * x1.y;
+        f.bias0 = -(129.5f * x0.x + 33.5f * x0.y);
+        f.bias1 = -(129.5f * x1.x + 33.5f * x1.y);
     } else {
-        f.bias0 = 135.5f * (x0.x + x0.y);
-        f.bias1 = 135.5f * (x1.x + x1.y);
+        f.bias0 = -(135.5f * (x0.x + x0.y));
+        f.bias1 = -(135.5f * (x1.x + x1.y));
     }
 }
 
@@ -743,17 +746,23 @@ __device__ __forceinline__ void cook_b(const BRaw<NV> &r, BFrag &f)
     finish_bias<BITS>(f, x0, x1);
 }
 
-// Decode + multiply one tile from shared memory into acc (two independent
-// mma chains: k-subtiles 0,2 and 1,3).
+// Decode + multiply one tile from shared memory into acc: one mma chain
+// over the four k-subtiles (hi then lo fragments when split), started from
+// the column biases; the warp's other tiles of the step supply the ILP.
+// Codes decode to finite values (128 + c) whatever the bytes, so a disabled
+// tile (on == false) is computed branch-free and dropped by a zero scale.
 template <int BITS, bool SPLIT>
-__device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, float (&acc)[4])
+__device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, float (&acc)[4], bool on)
 {
     constexpr int CB = tile_code_bytes(BITS);
     const int lane = threadIdx.x & 31, gq = lane >> 2;
     const uint32_t sc = *reinterpret_cast<const uint32_t *>(tile + CB + 4 * gq);
-    const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
-    float dv[4] = {-f.bias0, -f.bias1, -f.bias0, -f.bias1};
-    float dw[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
+    // a tile of an absent group (in-bounds stage bytes, zero B fragment)
+    // contributes exactly nothing: its scale is replaced, not multiplied
+    s01.x = on ? s01.x : 0.f;
+    s01.y = on ? s01.y : 0.f;
+    float dv[4];
     if (BITS == 4) {
         const uint4 cw = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
         const uint32_t q4[4] = {cw.x, cw.y, cw.z, cw.w};
@@ -765,10 +774,12 @@ __device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, fl
             A[1] = ((q >> 4) & 0x000F000Fu) | 0x43004300u;
             A[2] = ((q >> 8) & 0x000F000Fu) | 0x43004300u;
             A[3] = ((q >> 12) & 0x000F000Fu) | 0x43004300u;
-            float(&dd)[4] = (j & 1) ? dw : dv;
-            mma_bf16(dd, A, f.b0[j], f.b1[j]);
+            if (j == 0)
+                mma_bf16_c(dv, A, f.b0[0], f.b1[0], f.bias0, f.bias1, f.bias0, f.bias1);
+            else
+                mma_bf16(dv, A, f.b0[j], f.b1[j]);
             if (SPLIT)
-                mma_bf16(dd, A, f.b0l[j], f.b1l[j]);
+                mma_bf16(dv, A, f.b0l[j], f.b1l[j]);
         }
     } else {
         const uint2 cw = *reinterpret_cast<const uint2 *>(tile + 8 * lane);
@@ -782,15 +793,14 @@ __device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, fl
             A[1] = ((q >> v1) & 0x00030003u) | 0x43004300u;
             A[2] = ((q >> v0) & 0x000C000Cu) | 0x43004300u;
             A[3] = ((q >> v1) & 0x000C000Cu) | 0x43004300u;
-            float(&dd)[4] = (j & 1) ? dw : dv;
-            mma_bf16(dd, A, f.b0[j], f.b1[j]);
+            if (j == 0)
+                mma_bf16_c(dv, A, f.b0[0], f.b1[0], f.bias0, f.bias1, f.bias0, f.bias1);
+            else
+                mma_bf16(dv, A, f.b0[j], f.b1[j]);
             if (SPLIT)
-                mma_bf16(dd, A, f.b0l[j], f.b1l[j]);
+                mma_bf16(dv, A, f.b0l[j], f.b1l[j]);
         }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-        dv[e] += dw[e];
     acc[0] = fmaf(s01.x, dv[0], acc[0]);
     acc[1] = fmaf(s01.x, dv[1], acc[1]);
     acc[2] = fmaf(s01.y, dv[2], acc[2]);
@@ -1013,6 +1023,10 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
             for (int b = 0; b < NB; ++b) {
                 const int c = b >> 1, lg = warp + (b & 1) * kStreamWarps;  // chunk, group in chunk
                 const int gi = c * u.gc + lg;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    bf[b].b0[j] = bf[b].b1[j] = bf[b].b0l[j] = bf[b].b1l[j] = 0u;
+                bf[b].bias0 = bf[b].bias1 = 0.f;
                 if (c < u.ch && lg < u.gc && gi < u.gk) {
                     BRaw<NV> raw;
                     load_raw<PHASE, XBF16, NV>(a, pi, q.p, gi, fmax, raw);
@@ -1031,29 +1045,25 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
             }
         }
         if (ok) {
+            // branch-free over the warp's two groups (tiles of absent groups
+            // read in-bounds stage bytes and are dropped), so the four (down:
+            // two) mma chains of the step schedule together
             const uint8_t *stage = st.ring + slot * SB;
             const int ng = min(u.gc, u.gk - q.c * u.gc);  // groups in this chunk
             const bool g0 = warp < ng, g1 = warp + kStreamWarps < ng;
             if (PHASE == 0) {
-                // two groups, gate and up tile each: four independent chains
 #pragma unroll
                 for (int c = 0; c < KG; ++c) {
                     if (c == q.c) {
-                        if (g0) {
-                            mac_tile<BITS, kSplit>(stage + warp * GB, bf[2 * c], accg);
-                            mac_tile<BITS, kSplit>(stage + warp * GB + TB, bf[2 * c], accu);
-                        }
-                        if (g1) {
-                            mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[2 * c + 1], accg2);
-                            mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB + TB, bf[2 * c + 1], accu2);
-                        }
+                        mac_tile<BITS, kSplit>(stage + warp * GB, bf[2 * c], accg, g0);
+                        mac_tile<BITS, kSplit>(stage + warp * GB + TB, bf[2 * c], accu, g0);
+                        mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[2 * c + 1], accg2, g1);
+                        mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB + TB, bf[2 * c + 1], accu2, g1);
                     }
                 }
             } else {
-                if (g0)
-                    mac_tile<BITS, kSplit>(stage + warp * GB, bf[0], accg);
-                if (g1)
-                    mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[1], accu);
+                mac_tile<BITS, kSplit>(stage + warp * GB, bf[0], accg, g0);
+                mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[1], accu, g1);
             }
         }
         __syncwarp();
@@ -1253,7 +1263,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                     st_relaxed(a.cta_flags + 32 * c, 1u);
             }
         }
-        // one poller per CTA, on the CTA's own flag; the others sleep
+        // one poller per CTA, on the CTA's own flag; meanwhile other warps run
+        // the routing code once on scratch (in-bounds, results unused) so its
+        // instructions are fetched while the logits are still being made
         cta_barrier();
         if (warp == 0) {
             const int good = warp_wait_geq(a.cta_flags + 32 * blockIdx.x, 1u, a.status) ? 1 : 0;
@@ -1261,6 +1273,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                 s_ok = good;
                 a.cta_flags[32 * blockIdx.x] = 0u;  // only this CTA reads it
             }
+        } else if (warp <= (a.E + 31) / 32) {
+            route_chunk(rs.lg, rs.key, a.E, a.k, warp - 1, rs.warm_id, rs.warm_p);
         }
         cta_barrier();
         ok = s_ok != 0;
