@@ -134,7 +134,18 @@ struct Plan {
     size_t off_ctr_tile, off_ctr_done, off_ctr_sg, off_ctr_sd, off_ctr_comb, off_pair_done,
         off_flags, off_ctaflags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w, off_sw, off_pairs,
         off_rmap, off_hhi, off_hlo, off_hspart, off_o, off_part, total;
+    // grouped path (T >= kGroupedMinT only)
+    bool grouped;
+    int64_t grows;
+    size_t off_grow, off_gseg, off_gxs, off_gh, off_go;
 };
+
+// Whether the forward takes the expert-sorted tensor-core path: a token
+// batch large enough that an average expert sees a dense block of rows.
+bool auto_grouped(const smoe_layer_desc *L, int64_t T)
+{
+    return T >= kGroupedMinT && T * L->top_k >= 16ll * L->num_experts;
+}
 
 Plan make_plan(const smoe_layer_desc *L, int64_t T)
 {
@@ -190,6 +201,18 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_hspart = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 16) * 2);
     p.off_o = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
     p.off_part = take(sizeof(float) * 4 * 2 * (size_t)p.ctas * 2 * 2 * 32);
+    p.grouped = T >= kGroupedMinT;
+    p.grows = 0;
+    p.off_grow = p.off_gseg = p.off_gxs = p.off_gh = p.off_go = 0;
+    if (p.grouped) {
+        const int has_sh = L->shared_ffn_dim > 0 ? 1 : 0;
+        p.grows = grouped_max_rows(T, E, k, has_sh);
+        p.off_grow = take(sizeof(int32_t) * T * (k + 1));
+        p.off_gseg = take(sizeof(int32_t) * (2 * (kMaxExperts + 1) + 1));
+        p.off_gxs = take(sizeof(uint16_t) * (size_t)p.grows * d);
+        p.off_gh = take(sizeof(uint16_t) * (size_t)p.grows * p.fmax);
+        p.off_go = take(sizeof(float) * (size_t)p.grows * d);
+    }
     p.total = o;
     return p;
 }
@@ -395,7 +418,7 @@ smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, voi
 static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
                                   int64_t num_tokens, float *y, void *workspace,
                                   size_t workspace_bytes, int32_t *ids_out, float *w_out,
-                                  int stage_mask, void *cuda_stream)
+                                  int stage_mask, int path, void *cuda_stream)
 {
     if (!valid_layer(layer) || num_tokens < 0 || (x_dtype != SMOE_F32 && x_dtype != SMOE_BF16))
         return SMOE_ERR_INVALID_ARG;
@@ -411,6 +434,10 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const smoe_layer_desc &L = *layer;
     int *status = device_status_word();
+    const bool grouped = path == SMOE_PATH_GROUPED ||
+                         (path == SMOE_PATH_AUTO && auto_grouped(layer, num_tokens));
+    if (grouped && (!P.grouped || stage_mask != 7))
+        return SMOE_ERR_UNSUPPORTED;
     // T <= 8 with all stages: one fused launch (routing inside the kernel)
     const bool fused = num_tokens <= kFusedCombineMaxT && stage_mask == 7;
 
@@ -438,6 +465,9 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     ra.w_out = w_out;
     ra.pairs = at<int32_t>(workspace, P.off_pairs);
     ra.route_map = at<int32_t>(workspace, P.off_rmap);
+    ra.grp_row = grouped ? at<int32_t>(workspace, P.off_grow) : nullptr;
+    ra.grp_seg = grouped ? at<int32_t>(workspace, P.off_gseg) : nullptr;
+    ra.grp_rows = P.grows;
     ra.meta = at<int32_t>(workspace, P.off_meta);
     ra.tile_ctr = at<unsigned>(workspace, P.off_ctr_tile);
     ra.done_ctr = at<unsigned>(workspace, P.off_ctr_done);
@@ -497,6 +527,36 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     la.y = y;
     la.status = status;
 
+    if (grouped) {
+        GroupedArgs ga;
+        memset(&ga, 0, sizeof ga);
+        ga.tiles_routed = la.tiles_routed;
+        ga.tiles_shared = la.tiles_shared;
+        ga.expert_bytes_routed = la.expert_bytes_routed;
+        ga.down_off_routed = la.down_off_routed;
+        ga.down_off_shared = la.down_off_shared;
+        ga.T = num_tokens;
+        ga.d = L.d_model;
+        ga.f = L.ffn_dim;
+        ga.fs = L.shared_ffn_dim;
+        ga.E = L.num_experts;
+        ga.k = L.top_k;
+        ga.bits = L.bits;
+        ga.has_shared = ra.has_shared;
+        ga.seg = ra.grp_seg;
+        ga.rows_of = ra.grp_row;
+        ga.rows = P.grows;
+        ga.xs = at<uint16_t>(workspace, P.off_gxs);
+        ga.h = at<uint16_t>(workspace, P.off_gh);
+        ga.hstride = P.fmax;
+        ga.o = at<float>(workspace, P.off_go);
+        ga.status = status;
+        if (launch_router(ra, s, false) != cudaSuccess)
+            return SMOE_ERR_CUDA;
+        return launch_grouped(ga, x, ra.x_bf16, ra.weights, ra.shared_w, y, s) == cudaSuccess
+                   ? SMOE_OK
+                   : SMOE_ERR_CUDA;
+    }
     if (fused)
         return launch_layer(la, s) == cudaSuccess ? SMOE_OK : SMOE_ERR_CUDA;
     if ((stage_mask & 1) && launch_router(ra, s, false) != cudaSuccess)
@@ -514,7 +574,25 @@ smoe_status smoe_moe_forward(const smoe_layer_desc *layer, const void *x, smoe_d
                              void *cuda_stream)
 {
     return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
-                          w_out, 7, cuda_stream);
+                          w_out, 7, SMOE_PATH_AUTO, cuda_stream);
+}
+
+smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
+                                  int64_t num_tokens, float *y, void *workspace,
+                                  size_t workspace_bytes, int32_t *ids_out, float *w_out, int path,
+                                  void *cuda_stream)
+{
+    if (path != SMOE_PATH_AUTO && path != SMOE_PATH_STREAM && path != SMOE_PATH_GROUPED)
+        return SMOE_ERR_INVALID_ARG;
+    return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
+                          w_out, 7, path, cuda_stream);
+}
+
+int smoe_moe_path(const smoe_layer_desc *layer, int64_t num_tokens)
+{
+    if (!valid_layer(layer) || num_tokens < 0)
+        return -1;
+    return auto_grouped(layer, num_tokens) ? SMOE_PATH_GROUPED : SMOE_PATH_STREAM;
 }
 
 smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
@@ -525,7 +603,7 @@ smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
     if (stage < 0 || stage > 2)
         return SMOE_ERR_INVALID_ARG;
     return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
-                          w_out, 1 << stage, cuda_stream);
+                          w_out, 1 << stage, SMOE_PATH_STREAM, cuda_stream);
 }
 
 smoe_status smoe_get_device_status(void *cuda_stream)

@@ -72,6 +72,10 @@ struct RouteArgs {
     unsigned *done_ctr;         // [1]
     int *status;
     int max_pairs;
+    // expert-sorted rows of the grouped path (null: not built)
+    int32_t *grp_row;           // [T][k+1] sorted row of (token, slot); slot k: shared
+    int32_t *grp_seg;           // [nseg+1] first row per segment, then [nseg] rows used
+    int64_t grp_rows;           // rows available in the sorted matrices
 };
 
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
@@ -120,6 +124,32 @@ struct LayerArgs {
     float *y;                      // [T, d]
     int *status;
 };
+
+// The expert-sorted grouped path (grouped.cu): segments = the routed experts,
+// then the shared expert (all tokens); rows padded to 128 per segment.
+struct GroupedArgs {
+    const uint8_t *tiles_routed;   // bank base
+    const uint8_t *tiles_shared;   // nullable
+    int64_t expert_bytes_routed;
+    int64_t down_off_routed, down_off_shared;
+    int64_t T;
+    int d, f, fs, E, k, bits, has_shared;
+    const int32_t *seg;            // [nseg+1] first rows, then [nseg] counts
+    const int32_t *rows_of;        // [T][k+1]
+    int64_t rows;                  // rows of xs, h and o
+    uint16_t *xs;                  // bf16 [rows][d]
+    uint16_t *h;                   // bf16 [rows][hstride]
+    int hstride;                   // max(f, fs)
+    float *o;                      // [rows][d]
+    int *status;
+};
+
+// Token batches from this size on may take the grouped path (the workspace
+// holds its buffers).
+constexpr int64_t kGroupedMinT = 16;
+int64_t grouped_max_rows(int64_t T, int E, int k, int has_shared);
+cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, const float *w,
+                           const float *sw, float *y, cudaStream_t stream);
 
 int layer_grid_ctas_max();
 cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream);

@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kRThreads) route_logits_kernel(const float *lo
 struct DispatchSmem {
     int cnt[kMaxExperts];
     int pbase[kMaxExperts + 1];
+    int goff[kMaxExperts + 1];  // grouped path: first sorted row per segment
     int run[kMaxExperts];
     unsigned mask[kRWarps][kMaxExperts];
     int wbase[kRWarps][kMaxExperts];
@@ -154,6 +155,27 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
     __syncthreads();
     __shared__ int s_ok, s_pr, s_pt;
     if (tid == 0) {
+        if (a.grp_row) {
+            // segments: the experts, then the shared expert; rows padded to 128
+            const int nseg = E + (a.has_shared ? 1 : 0);
+            int64_t G = 0;
+            for (int e = 0; e < E; ++e) {
+                s.goff[e] = static_cast<int>(G);
+                G += (s.cnt[e] + 127) / 128 * 128;
+            }
+            s.goff[E] = static_cast<int>(G);
+            if (a.has_shared)
+                G += (T + 127) / 128 * 128;
+            const bool fits = G <= a.grp_rows;
+            if (!fits)
+                set_status(a.status, kStatusBadArg);
+            for (int sg = 0; sg < nseg; ++sg) {
+                a.grp_seg[sg] = fits ? (sg < E ? s.goff[sg] : s.goff[E]) : 0;
+                a.grp_seg[nseg + 1 + sg] =
+                    fits ? (sg < E ? s.cnt[sg] : static_cast<int>(T)) : 0;
+            }
+            a.grp_seg[nseg] = fits ? static_cast<int>(G) : 0;
+        }
         int P = 0;
         for (int e = 0; e < E; ++e) {
             s.pbase[e] = P;
@@ -172,6 +194,11 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
         if (tid == 0) {
             a.meta[0] = 0;
             a.meta[1] = 0;
+            if (a.grp_row) {
+                const int nseg = E + (a.has_shared ? 1 : 0);
+                for (int sg = 0; sg <= 2 * nseg; ++sg)
+                    a.grp_seg[sg] = 0;
+            }
         }
         return;
     }
@@ -205,9 +232,13 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
                 const int e = ev[j];
                 if (e < 0) {
                     a.route_map[t * (k + 1) + j] = 0;
+                    if (a.grp_row)
+                        a.grp_row[t * (k + 1) + j] = -1;
                     continue;
                 }
                 const int pos = s.wbase[warp][e] + __popc(s.mask[warp][e] & lt_mask);
+                if (a.grp_row)
+                    a.grp_row[t * (k + 1) + j] = s.goff[e] + pos;
                 const int pair = s.pbase[e] + pos / kPairCols, col = pos % kPairCols;
                 int32_t *pr = a.pairs + pair * kPairInts;
                 pr[2 + col] = static_cast<int32_t>(t);
@@ -231,8 +262,11 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
             pr[2 + i] = static_cast<int32_t>((int64_t)c * kPairCols + i < T ? c * kPairCols + i : 0);
     }
     if (a.has_shared)
-        for (int64_t t = tid; t < T; t += kRThreads)
+        for (int64_t t = tid; t < T; t += kRThreads) {
             a.route_map[t * (k + 1) + k] = static_cast<int32_t>((P_r + t / kPairCols) * kPairCols + t % kPairCols);
+            if (a.grp_row)
+                a.grp_row[t * (k + 1) + k] = s.goff[E] + static_cast<int32_t>(t);
+        }
     if (tid == 0) {
         a.meta[0] = P_r;
         a.meta[1] = P_t;

@@ -31,8 +31,11 @@ EXPORTED = [
     "smoe_repacked_bytes", "smoe_quantize", "smoe_repack", "smoe_unpack",
     "smoe_route_from_logits", "smoe_moe_workspace_bytes", "smoe_moe_workspace_init",
     "smoe_moe_forward", "smoe_moe_forward_stage", "smoe_get_device_status",
-    "smoe_moe_forward_noalloc",
+    "smoe_moe_forward_noalloc", "smoe_moe_forward_path", "smoe_moe_path",
 ]
+
+# Execution paths (SMOE_PATH_* in include/smoe.h).
+PATH_AUTO, PATH_STREAM, PATH_GROUPED = 0, 1, 2
 
 
 class SmoeError(RuntimeError):
@@ -98,6 +101,11 @@ def load(path: str | None = None):
     L.smoe_moe_forward_stage.restype = I
     L.smoe_moe_forward_noalloc.argtypes = [ctypes.POINTER(LayerDesc), P, I, I64, P, P, P, P]
     L.smoe_moe_forward_noalloc.restype = I
+    L.smoe_moe_forward_path.argtypes = [ctypes.POINTER(LayerDesc), P, I, I64, P, P, S, P, P, I,
+                                         P]
+    L.smoe_moe_forward_path.restype = I
+    L.smoe_moe_path.argtypes = [ctypes.POINTER(LayerDesc), I64]
+    L.smoe_moe_path.restype = I
     L.smoe_get_device_status.argtypes = [P]
     L.smoe_get_device_status.restype = I
     _lib = L
@@ -243,18 +251,29 @@ def workspace(layer: MoELayer, T: int, device=None, stream=None):
 
 
 def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None, w=None,
-            stream=None):
-    """smoe_moe_forward; x is [T, d] fp32 or bf16; returns y fp32 [T, d]."""
+            stream=None, path=None):
+    """smoe_moe_forward (or smoe_moe_forward_path when `path` is given); x is
+    [T, d] fp32 or bf16; returns y fp32 [T, d]."""
     T = x.shape[0]
     if y is None:
         y = torch.empty((T, layer.d), dtype=torch.float32, device=x.device)
     dt = SMOE_BF16 if x.dtype == torch.bfloat16 else SMOE_F32
     if x.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("x must be fp32 or bf16")
-    _check(load().smoe_moe_forward(ctypes.byref(layer.desc), _ptr(x), dt, T, _ptr(y), _ptr(ws),
-                                   ws.numel(), _ptr(ids), _ptr(w), _stream(stream)),
-           "smoe_moe_forward")
+    if path is None:
+        _check(load().smoe_moe_forward(ctypes.byref(layer.desc), _ptr(x), dt, T, _ptr(y), _ptr(ws),
+                                       ws.numel(), _ptr(ids), _ptr(w), _stream(stream)),
+               "smoe_moe_forward")
+    else:
+        _check(load().smoe_moe_forward_path(ctypes.byref(layer.desc), _ptr(x), dt, T, _ptr(y),
+                                            _ptr(ws), ws.numel(), _ptr(ids), _ptr(w), int(path),
+                                            _stream(stream)), "smoe_moe_forward_path")
     return y
+
+
+def path_for(layer: MoELayer, T: int) -> int:
+    """smoe_moe_path: the execution path smoe_moe_forward takes at T tokens."""
+    return int(load().smoe_moe_path(ctypes.byref(layer.desc), T))
 
 
 def forward_noalloc(layer: MoELayer, x: torch.Tensor, y=None, ids=None, w=None, stream=None):

@@ -184,8 +184,17 @@ smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, voi
 /* MoE layer forward for T tokens:
  *   logits = x Wr^T;  top-k routing (see smoe_route_from_logits);
  *   per selected expert: h = SiLU(W_gate x) * (W_up x), o = W_down h, with
- *   W decoded as (code - L) / L * scale in registers (never materialised);
+ *   W decoded as (code - L) / L * scale (never written to global memory);
  *   y = sum_j w_j o_j (rank order, deterministic) + shared expert.
+ * Two execution paths compute this ("Model Agnosticism"; "CMF v2", 2.2 MoE):
+ *   streaming  codes decoded in registers, fp32 accumulation with the
+ *              activations split into bf16 hi + lo (fp32-accurate); taken
+ *              for small batches
+ *   grouped    tokens sorted by expert, weights decoded to bf16 in shared
+ *              memory, tensor-core GEMMs (tcgen05) with bf16 activations and
+ *              bf16 h, fp32 accumulation; taken when T >= 16 and
+ *              T * top_k >= 16 * num_experts (smoe_moe_path tells which)
+ * Both are deterministic: the same inputs give the same bits on every call.
  *   x           device [T, d_model], fp32 or bf16 (x_dtype)
  *   y           device out fp32 [T, d_model]
  *   workspace   device, >= smoe_moe_workspace_bytes, 256-byte aligned,
@@ -201,13 +210,32 @@ smoe_status smoe_moe_forward(const smoe_layer_desc *layer, const void *x, smoe_d
                              size_t workspace_bytes, int32_t *ids_out, float *w_out,
                              void *cuda_stream);
 
+/* Execution paths of the forward. */
+#define SMOE_PATH_AUTO 0
+#define SMOE_PATH_STREAM 1
+#define SMOE_PATH_GROUPED 2
+
+/* smoe_moe_forward with the execution path chosen by the caller (path
+ * SMOE_PATH_AUTO is smoe_moe_forward itself).  The grouped path needs
+ * num_tokens >= 16 (the workspace of smaller batches has no room for it):
+ * otherwise SMOE_ERR_UNSUPPORTED, nothing enqueued.  Same arguments and
+ * errors as smoe_moe_forward, plus SMOE_ERR_INVALID_ARG for an unknown path. */
+smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
+                                  int64_t num_tokens, float *y, void *workspace,
+                                  size_t workspace_bytes, int32_t *ids_out, float *w_out, int path,
+                                  void *cuda_stream);
+
+/* The path smoe_moe_forward takes for this layer and token count
+ * (SMOE_PATH_STREAM or SMOE_PATH_GROUPED), or -1 on invalid arguments. */
+int smoe_moe_path(const smoe_layer_desc *layer, int64_t num_tokens);
+
 /* The same forward as smoe_moe_forward, one launch stage at a time, so that
  * a caller can put its own work or timing events between the stages:
  *   stage 0  router GEMV, softmax, top-k, renormalisation, dispatch
  *   stage 1  fused dequant gate/up GEMV + SiLU(gate) * up
  *   stage 2  fused dequant down GEMV + routing-weighted combine into y
  * Calling stages 0, 1, 2 in order on one stream with the same arguments and
- * workspace is exactly smoe_moe_forward.  Same arguments and errors, plus
+ * workspace is exactly smoe_moe_forward on the streaming path.  Same arguments and errors, plus
  * SMOE_ERR_INVALID_ARG for a stage outside 0..2. */
 smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
                                    smoe_dtype x_dtype, int64_t num_tokens, float *y,

@@ -133,3 +133,27 @@ def test_other_entry_points_reject_bad_args(libs):
     assert L.smoe_repack(arr, arr, 256, 128, 1, 4, 64, P(4096), 16, None) == -3   # too small
     assert L.smoe_repack(arr, arr, 256, 128, 1, 4, 64, P(4100), 1 << 20, None) == -1  # align
     assert L.smoe_unpack(P(4096), 256, 128, 1, 5, 64, arr, arr, None) == -1
+
+
+def test_path_selection_and_path_argument(libs):
+    """smoe_moe_path: the streaming path below 16 tokens or below 16 routed
+    rows per expert on average, the grouped path from there on; an unknown
+    path is refused before anything else."""
+    S, _ = libs
+    L = S.load()
+    P = ctypes.c_void_p
+    desc = _desc(S)  # E = 8, k = 2
+    assert L.smoe_moe_path(ctypes.byref(desc), 1) == S.PATH_STREAM
+    assert L.smoe_moe_path(ctypes.byref(desc), 15) == S.PATH_STREAM
+    assert L.smoe_moe_path(ctypes.byref(desc), 63) == S.PATH_STREAM     # 126 < 128 rows
+    assert L.smoe_moe_path(ctypes.byref(desc), 64) == S.PATH_GROUPED    # 128 rows
+    assert L.smoe_moe_path(ctypes.byref(desc), -1) == -1
+    assert L.smoe_moe_path(ctypes.byref(_desc(S, bits=3)), 64) == -1
+    for bad_path in (-1, 3, 7):
+        assert L.smoe_moe_forward_path(ctypes.byref(desc), P(4096), 0, 64, P(8192), P(1 << 20),
+                                       1 << 30, None, None, bad_path, None) == -1
+    # the workspace makes room for the sorted rows from 16 tokens on
+    w15 = L.smoe_moe_workspace_bytes(ctypes.byref(desc), 15)
+    w16 = L.smoe_moe_workspace_bytes(ctypes.byref(desc), 16)
+    rows16 = 16 * 2 + 8 * 127
+    assert w16 - w15 >= rows16 * (256 * 2 + 128 * 2 + 256 * 4)
