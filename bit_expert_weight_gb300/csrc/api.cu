@@ -137,7 +137,7 @@ struct Plan {
     // grouped path (T >= kGroupedMinT only)
     bool grouped;
     int64_t grows;
-    size_t off_grow, off_gseg, off_gxs, off_gh, off_go;
+    size_t off_grow, off_gseg, off_gtile, off_gxs, off_gh, off_go;
 };
 
 // Whether the forward takes the expert-sorted tensor-core path: a token
@@ -203,12 +203,13 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_part = take(sizeof(float) * 4 * 2 * (size_t)p.ctas * 2 * 2 * 32);
     p.grouped = T >= kGroupedMinT;
     p.grows = 0;
-    p.off_grow = p.off_gseg = p.off_gxs = p.off_gh = p.off_go = 0;
+    p.off_grow = p.off_gseg = p.off_gtile = p.off_gxs = p.off_gh = p.off_go = 0;
     if (p.grouped) {
         const int has_sh = L->shared_ffn_dim > 0 ? 1 : 0;
         p.grows = grouped_max_rows(T, E, k, has_sh);
         p.off_grow = take(sizeof(int32_t) * T * (k + 1));
         p.off_gseg = take(sizeof(int32_t) * (2 * (kMaxExperts + 1) + 1));
+        p.off_gtile = take(sizeof(int32_t) * (size_t)p.ntiles * E);
         p.off_gxs = take(sizeof(uint16_t) * (size_t)p.grows * d);
         p.off_gh = take(sizeof(uint16_t) * (size_t)p.grows * p.fmax);
         p.off_go = take(sizeof(float) * (size_t)p.grows * d);
@@ -465,9 +466,7 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     ra.w_out = w_out;
     ra.pairs = at<int32_t>(workspace, P.off_pairs);
     ra.route_map = at<int32_t>(workspace, P.off_rmap);
-    ra.grp_row = grouped ? at<int32_t>(workspace, P.off_grow) : nullptr;
-    ra.grp_seg = grouped ? at<int32_t>(workspace, P.off_gseg) : nullptr;
-    ra.grp_rows = P.grows;
+    ra.grp_tilecnt = grouped ? at<int32_t>(workspace, P.off_gtile) : nullptr;
     ra.meta = at<int32_t>(workspace, P.off_meta);
     ra.tile_ctr = at<unsigned>(workspace, P.off_ctr_tile);
     ra.done_ctr = at<unsigned>(workspace, P.off_ctr_done);
@@ -543,9 +542,13 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
         ga.k = L.top_k;
         ga.bits = L.bits;
         ga.has_shared = ra.has_shared;
-        ga.seg = ra.grp_seg;
-        ga.rows_of = ra.grp_row;
+        ga.seg = at<int32_t>(workspace, P.off_gseg);
+        ga.rows_of = at<int32_t>(workspace, P.off_grow);
         ga.rows = P.grows;
+        ga.ids = ra.ids;
+        ga.tilecnt = ra.grp_tilecnt;
+        ga.ntiles = P.ntiles;
+        ga.scan_ctr = flags + 2;
         ga.xs = at<uint16_t>(workspace, P.off_gxs);
         ga.h = at<uint16_t>(workspace, P.off_gh);
         ga.hstride = P.fmax;

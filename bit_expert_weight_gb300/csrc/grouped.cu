@@ -16,19 +16,25 @@
 // rows padded to a multiple of 128 in the sorted activation matrix; the
 // router's dispatch writes each (token, slot)'s row.  A work item is one
 // (segment, n-tile, m-tile): 128 rows times 256 output columns over the
-// whole K.  Items are ordered so that the m-tiles of one (segment, n-tile)
-// are adjacent: CTAs working at the same time read the same weight tiles.
+// whole K, for one or two m-tiles (one decoded weight stage then feeds two
+// MMA groups).  Items are ordered so that the m-tiles of one (segment,
+// n-tile) are adjacent: CTAs working at the same time read the same weights.
 //
-// One persistent CTA per SM, 14 warps:
-//   warp 0       producer: TMA of the 128 x 64 bf16 activation tile
-//                (128-byte swizzle) and bulk copies of the 16 code tiles of
-//                the K block into a 5-stage load ring
-//   warp 1       tensor memory allocation; lane 0 issues the MMAs
-//   warps 2..9   decoders: code tiles -> bf16 weights in the 128-byte
-//                swizzled K-major layout the MMA reads (2-stage ring)
-//   warps 10..13 epilogue: tensor memory -> registers -> h (bf16) or o (fp32)
-// Two accumulators of 256 columns let the epilogue of one item overlap the
-// MMAs of the next.  Every wait is bounded; a timeout records
+// One persistent CTA per SM, 28 warps (warp w issues on sub-partition w % 4):
+//   warp 0        code producer: bulk copies of the 16 code tiles of every
+//                 K block (3-stage ring, freed once decoded)
+//   warp 1        tensor memory allocation; lane 0 issues the MMAs, one
+//                 commit per K block frees that block's stage
+//   warp 2        activation producer: TMA of the item's one or two 128 x 64
+//                 bf16 activation tiles of every K block, 128-byte swizzle
+//   warps 3..6    epilogue: tensor memory -> registers -> h (bf16) or o (fp32)
+//   16 warps      decoders (warps 7..27 off sub-partition 1; the others
+//                 exit), one code tile each per K block: bf16 weights in the
+//                 128-byte-swizzled K-major layout the MMA reads
+// A stage (3 of them) holds a K block's activations and decoded weights.
+// Two accumulators of 256 columns: an item of two m-tiles uses both, an item
+// of one m-tile alternates between them so that its epilogue overlaps the
+// next item's MMAs.  Every wait is bounded; a timeout records
 // SMOE_ERR_TIMEOUT, sets the CTA's fail flag, and the CTA drains its copies
 // and MMAs in flight before it frees tensor memory and exits.
 #include <cuda.h>
@@ -46,15 +52,28 @@ namespace {
 constexpr int kGM = 128;             // rows per item (MMA M)
 constexpr int kGN = 256;             // output columns per item (MMA N)
 constexpr int kGK = 64;              // K per stage (one quantisation group)
-constexpr int kLoadStages = 5;
-constexpr int kBStages = 2;
-constexpr int kDecWarps = 8;
+constexpr int kCodeStages = 3;       // code tiles of one K block each
+constexpr int kStages = 3;           // activations (up to 2 m-tiles) + decoded weights of one K block
+constexpr int kDecWarps = 16;
 constexpr int kEpiWarpsG = 4;
-constexpr int kGWarps = 2 + kDecWarps + kEpiWarpsG;
+constexpr int kEpiWarp0 = 3;         // warps 0 codes, 1 MMA, 2 activations, 3..6 epilogue
+constexpr int kGWarps = 28;          // decoders: warps 7..27 off sub-partition 1
+
+// Warp w issues on sub-partition w % 4.  The MMA warp (1) keeps its
+// sub-partition to itself and the idle epilogue quarter: the decoders take
+// warps 7..27 except those of sub-partition 1, which exit at once, so the
+// single MMA-issuing thread never queues behind decoder instructions.
+__device__ __forceinline__ int decoder_index(int w)
+{
+    if (w < 7 || (w & 3) == 1)
+        return -1;
+    return (w - 7) - (w > 9 ? (w - 6) / 4 : 0);
+}
 constexpr int kGThreads = kGWarps * 32;
 constexpr int kTilesPerStage = 16;
 constexpr uint32_t kATileBytes = kGM * kGK * 2;   // 16 KB
 constexpr uint32_t kBTileBytes = kGN * kGK * 2;   // 32 KB
+constexpr uint32_t kAStageBytes = 2 * kATileBytes; // two m-tiles
 constexpr int kMaxSeg = kMaxExperts + 1;
 
 __host__ __device__ constexpr uint32_t code_stage_bytes(int bits)
@@ -63,20 +82,22 @@ __host__ __device__ constexpr uint32_t code_stage_bytes(int bits)
 }
 __host__ __device__ constexpr uint32_t grouped_smem_bytes(int bits)
 {
-    return kLoadStages * kATileBytes + kBStages * kBTileBytes + kLoadStages * code_stage_bytes(bits) +
+    return kStages * (kAStageBytes + kBTileBytes) + kCodeStages * code_stage_bytes(bits) +
            1024;  // slack for the manual 1024-byte alignment
 }
 
 struct GSmem {
-    uint64_t load_full[kLoadStages];   // producer: 1 arrival + bytes
-    uint64_t load_empty[kLoadStages];  // decoder warps + 1 MMA commit
-    uint64_t b_full[kBStages];         // decoder warps
-    uint64_t b_empty[kBStages];        // 1 MMA commit
+    uint64_t code_full[kCodeStages];   // code producer: 1 arrival + bytes
+    uint64_t code_empty[kCodeStages];  // decoder warps
+    uint64_t a_full[kStages];          // activation producer: 1 arrival + bytes
+    uint64_t b_full[kStages];          // decoder warps
+    uint64_t stage_empty[kStages];     // 1 MMA commit: activations and weights free
     uint64_t acc_full[2];              // 1 MMA commit
     uint64_t acc_empty[2];             // epilogue warps
     uint64_t drain;                    // final MMA commit
     uint32_t tmem_base;
-    uint32_t last_it[kLoadStages];     // producer: 1 + last iteration filled per stage
+    uint32_t last_code[kCodeStages];   // 1 + last use filled, per stage (drain
+    uint32_t last_a[kStages];          // after a failure)
     int fail;
     int nseg, total_items;
     int ipre[kMaxSeg + 1];             // item prefix per segment
@@ -174,8 +195,10 @@ __device__ __forceinline__ bool gwait(GSmem &sm, uint64_t *bar, unsigned parity,
 
 // ------------------------------------------------------------ work items
 
+// One item: one (segment, n-tile) and one or two consecutive m-tiles of the
+// segment, so that each decoded weight stage feeds up to two MMA groups.
 struct Item {
-    int seg, nt, mt, row0, nvalid;
+    int seg, nt, nm, row0, nvalid0, nvalid1;
 };
 
 template <int PHASE>
@@ -184,6 +207,8 @@ __device__ __forceinline__ int seg_ntiles(const GroupedArgs &a, int s)
     const int fsg = s < a.E ? a.f : a.fs;
     return PHASE == 0 ? (fsg + 127) / 128 : (a.d + kGN - 1) / kGN;
 }
+
+__device__ __forceinline__ int seg_mpairs(int cnt) { return ((cnt + kGM - 1) / kGM + 1) / 2; }
 
 __device__ __forceinline__ Item item_at(const GSmem &sm, int i)
 {
@@ -198,20 +223,24 @@ __device__ __forceinline__ Item item_at(const GSmem &sm, int i)
     Item it;
     it.seg = lo;
     const int local = i - sm.ipre[lo];
-    const int mtc = (sm.cnt[lo] + kGM - 1) / kGM;
-    it.nt = local / mtc;
-    it.mt = local % mtc;
-    it.row0 = sm.off[lo] + kGM * it.mt;
-    const int left = sm.cnt[lo] - kGM * it.mt;
-    it.nvalid = left < kGM ? left : kGM;
+    const int c = sm.cnt[lo];
+    const int mtc = (c + kGM - 1) / kGM;
+    const int pairs = (mtc + 1) / 2;
+    it.nt = local / pairs;
+    const int mt0 = 2 * (local % pairs);
+    it.nm = mtc - mt0 < 2 ? 1 : 2;
+    it.row0 = sm.off[lo] + kGM * mt0;
+    const int left = c - kGM * mt0;
+    it.nvalid0 = left < kGM ? left : kGM;
+    it.nvalid1 = left - kGM < kGM ? left - kGM : kGM;
     return it;
 }
 
 // ------------------------------------------------------------ roles
 
+// Code tiles of every K block, in item order (warp 0).
 template <int BITS, int PHASE>
-__device__ void producer(const GroupedArgs &a, const CUtensorMap *amap, GSmem &sm, uint8_t *sA,
-                         uint8_t *sC)
+__device__ void code_producer(const GroupedArgs &a, GSmem &sm, uint8_t *sC)
 {
     const int lane = threadIdx.x & 31;
     constexpr uint32_t TB = tile_bytes(BITS);
@@ -231,53 +260,104 @@ __device__ void producer(const GroupedArgs &a, const CUtensorMap *amap, GSmem &s
         int nvalid_copy = nstrips - r0;
         nvalid_copy = nvalid_copy < ncopy ? nvalid_copy : ncopy;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = static_cast<int>(it % kLoadStages);
-            const unsigned par = ((it / kLoadStages) & 1u) ^ 1u;
-            if (!__all_sync(0xffffffffu, gwait(sm, &sm.load_empty[s], par, a.status)))
+            const int s = static_cast<int>(it % kCodeStages);
+            const unsigned par = ((it / kCodeStages) & 1u) ^ 1u;
+            if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_empty[s], par, a.status)))
                 return;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&sm.load_full[s], kATileBytes + nvalid_copy * csize);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&sm.code_full[s], nvalid_copy * csize);
+                sm.last_code[s] = it + 1;
+            }
             __syncwarp();
-            if (lane == 0)
-                tma_load_2d(sA + s * kATileBytes, amap, kb * kGK, w.row0, &sm.load_full[s]);
-            if (lane == 0)
-                sm.last_it[s] = it + 1;
             if (lane < nvalid_copy) {
                 const int r = r0 + lane;
                 const uint8_t *src =
                     PHASE == 0 ? wb + (((int64_t)r * (a.d / kGK) + kb) * 2) * TB
                                : wb + down_off + ((int64_t)r * (fsg / kGK) + kb) * TB;
                 bulk_g2s(sC + s * code_stage_bytes(BITS) + lane * csize, src, csize,
-                         &sm.load_full[s]);
+                         &sm.code_full[s]);
             }
         }
     }
 }
 
-// Decode one 16 x 64 code tile into rows rowbase .. rowbase + 15 of a
-// 128-byte-swizzled K-major bf16 tile: w = (c - L) * (s / L) with
-// c - (L + 1/2) exact in bf16 and one rounding in the fused multiply-add.
-template <int BITS>
-__device__ __forceinline__ void decode_tile(const uint8_t *tile, uint8_t *sB, int rowbase, int lane)
+// Activation tiles: for every K block, one 128 x 64 tile per m-tile of the
+// item, into the K block's stage (warp 2, lane 0).
+template <int PHASE>
+__device__ void act_producer(const GroupedArgs &a, const CUtensorMap *amap, GSmem &sm, uint8_t *sA)
 {
-    const int gq = lane >> 2, tig = lane & 3;
+    uint32_t it = 0;
+    for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
+        const Item w = item_at(sm, i);
+        const int fsg = w.seg < a.E ? a.f : a.fs;
+        const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const int s = static_cast<int>(it % kStages);
+            if (!gwait(sm, &sm.stage_empty[s], ((it / kStages) & 1u) ^ 1u, a.status))
+                return;
+            mbar_arrive_expect_tx(&sm.a_full[s], w.nm * kATileBytes);
+            sm.last_a[s] = it + 1;
+            for (int j = 0; j < w.nm; ++j)
+                tma_load_2d(sA + s * kAStageBytes + j * kATileBytes, amap, kb * kGK,
+                            w.row0 + kGM * j, &sm.a_full[s]);
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Decode one 16 x 64 code tile (shared address `tile`) into rows rowbase ..
+// rowbase + 15 of a 128-byte-swizzled K-major bf16 tile at `sb`:
+// w = (c - L) * (s / L), with c - (L + 1/2) exact in bf16 and one rounding
+// in the fused multiply-add.  off[rh][h] = the lane's byte offsets of its
+// two 16-byte chunks in rows gq and gq + 8 (swizzle included).
+template <int BITS>
+__device__ __forceinline__ void decode_tile(uint32_t tile, uint32_t sb, const uint32_t (&off)[2][2],
+                                            int lane)
+{
+    const int gq = lane >> 2;
     constexpr float kInvL = BITS == 4 ? (1.0f / 7.5f) : (1.0f / 1.5f);
     // bf16 128 + c minus 128 + L + 1/2 (136 for Q4, 130 for Q2), both halves
     constexpr uint32_t kSub = BITS == 4 ? 0x43084308u : 0x43024302u;
-    const uint32_t sc = *reinterpret_cast<const uint32_t *>(tile + tile_code_bytes(BITS) + 4 * gq);
-    const __half2 sh = *reinterpret_cast<const __half2 *>(&sc);
+    const uint32_t sc = lds32(tile + tile_code_bytes(BITS) + 4 * gq);
     uint32_t smul[2], sadd[2];
     {
-        const float s0 = __low2float(sh) * kInvL, s1 = __high2float(sh) * kInvL;
+        const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sc));
+        const float s0 = sf.x * kInvL, s1 = sf.y * kInvL;
         smul[0] = pack_bf16x2(s0, s0);
         smul[1] = pack_bf16x2(s1, s1);
         // half of the rounded scale: exact
-        sadd[0] = bf16x2_fma(smul[0], 0x3F003F00u, 0u);
-        sadd[1] = bf16x2_fma(smul[1], 0x3F003F00u, 0u);
+        sadd[0] = bf16x2_fma(smul[0], 0x3F003F00u, 0x80008000u);
+        sadd[1] = bf16x2_fma(smul[1], 0x3F003F00u, 0x80008000u);
     }
-    uint32_t v[2][8];  // [rh][4*pair-in-row ...]: cols 16 tig + 2 m, +1 for m = 0..7
+    uint32_t v[2][8];  // [rh][m]: columns 16 tig + 2 m, + 1
     if (BITS == 4) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(tile + 16 * lane);
+        const uint4 q = lds128(tile + 16 * lane);
         const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -289,7 +369,7 @@ __device__ __forceinline__ void decode_tile(const uint8_t *tile, uint8_t *sB, in
                 v[rh][2 * j + 1] = bf16x2_fma(bf16x2_sub(hi, kSub), smul[rh], sadd[rh]);
             }
     } else {
-        const uint2 q = *reinterpret_cast<const uint2 *>(tile + 8 * lane);
+        const uint2 q = lds64(tile + 8 * lane);
         const uint32_t wds[2] = {q.x, q.y};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -304,23 +384,26 @@ __device__ __forceinline__ void decode_tile(const uint8_t *tile, uint8_t *sB, in
             }
     }
 #pragma unroll
-    for (int rh = 0; rh < 2; ++rh) {
-        const int n = rowbase + gq + 8 * rh;  // n & 7 == gq
-        uint8_t *row = sB + n * 128;
+    for (int rh = 0; rh < 2; ++rh)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int chunk = (2 * tig + h) ^ gq;
-            *reinterpret_cast<uint4 *>(row + chunk * 16) =
-                make_uint4(v[rh][4 * h], v[rh][4 * h + 1], v[rh][4 * h + 2], v[rh][4 * h + 3]);
-        }
-    }
+        for (int h = 0; h < 2; ++h)
+            sts128(sb + off[rh][h], v[rh][4 * h], v[rh][4 * h + 1], v[rh][4 * h + 2],
+                   v[rh][4 * h + 3]);
 }
 
 template <int BITS, int PHASE>
 __device__ void decoders(const GroupedArgs &a, GSmem &sm, uint8_t *sB, const uint8_t *sC, int dw)
 {
     const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tig = lane & 3;
     constexpr uint32_t TB = tile_bytes(BITS);
+    uint32_t off[2][2];
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            off[rh][h] = (gq + 8 * rh) * 128 + ((((2 * tig + h) ^ gq) & 7) << 4);
+    const uint32_t sB0 = smem_u32(sB), sC0 = smem_u32(sC);
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
         const Item w = item_at(sm, i);
@@ -329,14 +412,14 @@ __device__ void decoders(const GroupedArgs &a, GSmem &sm, uint8_t *sB, const uin
         const int r0 = (PHASE == 0 ? 128 * w.nt : kGN * w.nt) / 16;
         const int nstrips = PHASE == 0 ? fsg / 16 : a.d / 16;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = static_cast<int>(it % kLoadStages);
-            const int b = static_cast<int>(it % kBStages);
-            if (!__all_sync(0xffffffffu, gwait(sm, &sm.load_full[s], (it / kLoadStages) & 1u, a.status)))
+            const int s = static_cast<int>(it % kCodeStages);
+            const int b = static_cast<int>(it % kStages);
+            if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_full[s], (it / kCodeStages) & 1u, a.status)))
                 return;
-            if (!__all_sync(0xffffffffu, gwait(sm, &sm.b_empty[b], ((it / kBStages) & 1u) ^ 1u, a.status)))
+            if (!__all_sync(0xffffffffu, gwait(sm, &sm.stage_empty[b], ((it / kStages) & 1u) ^ 1u, a.status)))
                 return;
-            const uint8_t *cs = sC + s * code_stage_bytes(BITS);
-            uint8_t *bs = sB + b * kBTileBytes;
+            const uint32_t cs = sC0 + s * code_stage_bytes(BITS);
+            const uint32_t bs = sB0 + b * kBTileBytes;
 #pragma unroll
             for (int qq = 0; qq < kTilesPerStage / kDecWarps; ++qq) {
                 const int q = dw + kDecWarps * qq;
@@ -344,50 +427,94 @@ __device__ void decoders(const GroupedArgs &a, GSmem &sm, uint8_t *sB, const uin
                 const int strip = PHASE == 0 ? q >> 1 : q;
                 const int rowbase = PHASE == 0 ? (q & 1) * 128 + 16 * (q >> 1) : 16 * q;
                 if (r0 + strip < nstrips)
-                    decode_tile<BITS>(cs + q * TB, bs, rowbase, lane);
+                    decode_tile<BITS>(cs + q * TB, bs + rowbase * 128, off, lane);
             }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.b_full[b]);
-                mbar_arrive(&sm.load_empty[s]);
+                mbar_arrive(&sm.code_empty[s]);
             }
         }
     }
 }
 
+// Accumulator slots: an item of two m-tiles takes both 256-column slots; an
+// item of one m-tile takes the slot after the last single one, so that its
+// epilogue overlaps the next item's MMAs.  The MMA issuer and the epilogue
+// walk the same item sequence, so they agree on every slot and phase.
+struct SlotState {
+    uint32_t use0, use1;  // completed uses of slot 0 and 1
+    int next;
+    __device__ void init()
+    {
+        use0 = use1 = 0u;
+        next = 0;
+    }
+    __device__ int slot(const Item &w, int j) const { return w.nm == 2 ? j : next; }
+    __device__ uint32_t uses(int sl) const { return sl == 0 ? use0 : use1; }
+    __device__ void done(const Item &w)
+    {
+        if (w.nm == 2) {
+            ++use0;
+            ++use1;
+        } else {
+            if (next == 0)
+                ++use0;
+            else
+                ++use1;
+            next ^= 1;
+        }
+    }
+};
+
 template <int PHASE>
 __device__ void mma_issuer(const GroupedArgs &a, GSmem &sm, const uint8_t *sA, const uint8_t *sB)
 {
-    uint32_t it = 0, ic = 0;
+    uint32_t it = 0;
+    SlotState st;
+    st.init();
     const uint32_t tbase = sm.tmem_base;
-    for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x, ++ic) {
+    const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
+    for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
         const Item w = item_at(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
         const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
-        const int ab = static_cast<int>(ic & 1u);
-        if (!gwait(sm, &sm.acc_empty[ab], ((ic >> 1) & 1u) ^ 1u, a.status))
+        const int slot0 = st.slot(w, 0), slot1 = st.slot(w, 1);
+        if (!gwait(sm, &sm.acc_empty[slot0], (st.uses(slot0) & 1u) ^ 1u, a.status))
             return;
-        tc_fence_after();
-        const uint32_t dcol = tbase + static_cast<uint32_t>(ab * kGN);
+        if (w.nm == 2 && !gwait(sm, &sm.acc_empty[slot1], (st.uses(slot1) & 1u) ^ 1u, a.status))
+            return;
+        const uint32_t d0 = tbase + static_cast<uint32_t>(slot0 * kGN);
+        const uint32_t d1 = tbase + static_cast<uint32_t>(slot1 * kGN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = static_cast<int>(it % kLoadStages);
-            const int b = static_cast<int>(it % kBStages);
-            if (!gwait(sm, &sm.b_full[b], (it / kBStages) & 1u, a.status))
+            const int s = static_cast<int>(it % kStages);
+            const unsigned par = (it / kStages) & 1u;
+            if (!gwait(sm, &sm.b_full[s], par, a.status))
                 return;
-            if (!gwait(sm, &sm.load_full[s], (it / kLoadStages) & 1u, a.status))
+            if (!gwait(sm, &sm.a_full[s], par, a.status))
                 return;
             tc_fence_after();
-            const uint32_t aaddr = smem_u32(sA + s * kATileBytes);
-            const uint32_t baddr = smem_u32(sB + b * kBTileBytes);
+            // descriptor start addresses are in 16-byte units: one K step of
+            // 16 bf16 is +2, one stage +size/16
+            const uint64_t ad = adesc0 + (uint64_t)(s * (kAStageBytes >> 4));
+            const uint64_t bd = bdesc0 + (uint64_t)(s * (kBTileBytes >> 4));
 #pragma unroll
             for (int ks = 0; ks < kGK / 16; ++ks)
-                umma_bf16(dcol, sw128_desc(aaddr + 32 * ks), sw128_desc(baddr + 32 * ks),
-                          (kb | ks) != 0 ? 1u : 0u);
-            umma_commit(&sm.b_empty[b]);
-            umma_commit(&sm.load_empty[s]);
+                umma_bf16(d0, ad + 2 * ks, bd + 2 * ks, (kb | ks) != 0 ? 1u : 0u);
+            if (kb == nkb - 1)
+                umma_commit(&sm.acc_full[slot0]);  // its epilogue may start now
+            if (w.nm == 2) {
+#pragma unroll
+                for (int ks = 0; ks < kGK / 16; ++ks)
+                    umma_bf16(d1, ad + (kATileBytes >> 4) + 2 * ks, bd + 2 * ks,
+                              (kb | ks) != 0 ? 1u : 0u);
+                if (kb == nkb - 1)
+                    umma_commit(&sm.acc_full[slot1]);
+            }
+            umma_commit(&sm.stage_empty[s]);
         }
-        umma_commit(&sm.acc_full[ab]);
+        st.done(w);
     }
 }
 
@@ -403,55 +530,60 @@ __device__ void epilogue(const GroupedArgs &a, GSmem &sm)
     const int quarter = (threadIdx.x >> 5) & 3;  // tensor-memory lanes 32 q .. 32 q + 31
     const int r = 32 * quarter + lane;
     const uint32_t tbase = sm.tmem_base;
-    uint32_t ic = 0;
-    for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x, ++ic) {
+    SlotState st;
+    st.init();
+    for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
         const Item w = item_at(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
-        const int ab = static_cast<int>(ic & 1u);
-        if (!__all_sync(0xffffffffu, gwait(sm, &sm.acc_full[ab], (ic >> 1) & 1u, a.status)))
-            return;
-        tc_fence_after();
-        const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * quarter) << 16) +
-                               static_cast<uint32_t>(ab * kGN);
-        const bool valid = r < w.nvalid;
-        const int64_t row = w.row0 + r;
-        if (PHASE == 0) {
-            const int n0 = 128 * w.nt;
-            for (int c = 0; c < 128 && n0 + c < fsg; c += 16) {
-                uint32_t g[16], u[16];
-                tmem_ld16(taddr + c, g);
-                tmem_ld16(taddr + 128 + c, u);
-                tmem_wait_ld();
-                uint32_t hv[8];
+        for (int j = 0; j < w.nm; ++j) {
+            const int sl = st.slot(w, j);
+            if (!__all_sync(0xffffffffu, gwait(sm, &sm.acc_full[sl], st.uses(sl) & 1u, a.status)))
+                return;
+            tc_fence_after();
+            const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * quarter) << 16) +
+                                   static_cast<uint32_t>(sl * kGN);
+            const bool valid = r < (j == 0 ? w.nvalid0 : w.nvalid1);
+            const int64_t row = w.row0 + kGM * j + r;
+            if (PHASE == 0) {
+                const int n0 = 128 * w.nt;
+                for (int c = 0; c < 128 && n0 + c < fsg; c += 16) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(taddr + c, g);
+                    tmem_ld16(taddr + 128 + c, u);
+                    tmem_wait_ld();
+                    uint32_t hv[8];
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    hv[m] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * m]), __uint_as_float(u[2 * m])),
-                                        silu_mul(__uint_as_float(g[2 * m + 1]), __uint_as_float(u[2 * m + 1])));
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.h + row * a.hstride + n0 + c);
-                    dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                    dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                    for (int m = 0; m < 8; ++m)
+                        hv[m] = pack_bf16x2(
+                            silu_mul(__uint_as_float(g[2 * m]), __uint_as_float(u[2 * m])),
+                            silu_mul(__uint_as_float(g[2 * m + 1]), __uint_as_float(u[2 * m + 1])));
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(a.h + row * a.hstride + n0 + c);
+                        dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                        dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                    }
+                }
+            } else {
+                const int n0 = kGN * w.nt;
+                for (int c = 0; c < kGN && n0 + c < a.d; c += 16) {
+                    uint32_t o[16];
+                    tmem_ld16(taddr + c, o);
+                    tmem_wait_ld();
+                    if (valid) {
+                        float4 *dst = reinterpret_cast<float4 *>(a.o + row * a.d + n0 + c);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m)
+                            dst[m] = make_float4(__uint_as_float(o[4 * m]), __uint_as_float(o[4 * m + 1]),
+                                                 __uint_as_float(o[4 * m + 2]), __uint_as_float(o[4 * m + 3]));
+                    }
                 }
             }
-        } else {
-            const int n0 = kGN * w.nt;
-            for (int c = 0; c < kGN && n0 + c < a.d; c += 16) {
-                uint32_t o[16];
-                tmem_ld16(taddr + c, o);
-                tmem_wait_ld();
-                if (valid) {
-                    float4 *dst = reinterpret_cast<float4 *>(a.o + row * a.d + n0 + c);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        dst[m] = make_float4(__uint_as_float(o[4 * m]), __uint_as_float(o[4 * m + 1]),
-                                             __uint_as_float(o[4 * m + 2]), __uint_as_float(o[4 * m + 3]));
-                }
-            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.acc_empty[sl]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&sm.acc_empty[ab]);
+        st.done(w);
     }
 }
 
@@ -462,9 +594,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     extern __shared__ uint8_t g_smem_raw[];
     __shared__ GSmem sm;
     uint8_t *base = g_smem_raw + ((1024u - (smem_u32(g_smem_raw) & 1023u)) & 1023u);
-    uint8_t *sA = base;                                   // kLoadStages x 16 KB
-    uint8_t *sB = sA + kLoadStages * kATileBytes;          // kBStages x 32 KB
-    uint8_t *sC = sB + kBStages * kBTileBytes;             // kLoadStages code stages
+    uint8_t *sA = base;                                   // kStages x 2 x 16 KB
+    uint8_t *sB = sA + kStages * kAStageBytes;             // kStages x 32 KB
+    uint8_t *sC = sB + kStages * kBTileBytes;              // kCodeStages code stages
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // segment table -> item prefix (one warp; at most 257 segments)
@@ -484,7 +616,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 }
                 sm.cnt[s] = c;
                 sm.off[s] = o;
-                items = ((c + kGM - 1) / kGM) * seg_ntiles<PHASE>(a, s);
+                items = seg_mpairs(c) * seg_ntiles<PHASE>(a, s);
             }
             int incl = items;
 #pragma unroll
@@ -502,14 +634,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
             sm.nseg = nseg;
             sm.total_items = run;
             sm.fail = 0;
-            for (int s = 0; s < kLoadStages; ++s) {
-                sm.last_it[s] = 0;
-                mbar_init(&sm.load_full[s], 1);
-                mbar_init(&sm.load_empty[s], kDecWarps + 1);
+            for (int s = 0; s < kCodeStages; ++s) {
+                sm.last_code[s] = 0;
+                mbar_init(&sm.code_full[s], 1);
+                mbar_init(&sm.code_empty[s], kDecWarps);
             }
-            for (int b = 0; b < kBStages; ++b) {
-                mbar_init(&sm.b_full[b], kDecWarps);
-                mbar_init(&sm.b_empty[b], 1);
+            for (int s = 0; s < kStages; ++s) {
+                sm.last_a[s] = 0;
+                mbar_init(&sm.a_full[s], 1);
+                mbar_init(&sm.b_full[s], kDecWarps);
+                mbar_init(&sm.stage_empty[s], 1);
             }
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&sm.acc_full[b], 1);
@@ -534,7 +668,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc_fence_after();
 
     if (warp == 0) {
-        producer<BITS, PHASE>(a, &amap, sm, sA, sC);
+        code_producer<BITS, PHASE>(a, sm, sC);
+    } else if (warp == 2) {
+        if (lane == 0)
+            act_producer<PHASE>(a, &amap, sm, sA);
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             mma_issuer<PHASE>(a, sm, sA, sB);
@@ -546,19 +684,26 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 2 + kDecWarps) {
-        decoders<BITS, PHASE>(a, sm, sB, sC, warp - 2);
-    } else {
+    } else if (warp < kEpiWarp0 + kEpiWarpsG) {
         epilogue<PHASE>(a, sm);
+    } else if (decoder_index(warp) >= 0) {
+        decoders<BITS, PHASE>(a, sm, sB, sC, decoder_index(warp));
     }
     __syncwarp();
     // After a failure the consumers may have left copies unwaited: the
-    // producer waits (bounded) for the last phase it filled on every stage,
+    // producers wait (bounded) for the last phase they filled on every stage,
     // so no copy is in flight when the CTA exits.
-    if (warp == 0 && *reinterpret_cast<volatile int *>(&sm.fail) && lane < kLoadStages) {
-        const uint32_t last = sm.last_it[lane];
-        if (last > 0 && !mbar_wait_bounded(&sm.load_full[lane], ((last - 1) / kLoadStages) & 1u))
-            set_status(a.status, kStatusTimeout);
+    if (*reinterpret_cast<volatile int *>(&sm.fail)) {
+        if (warp == 0 && lane < kCodeStages) {
+            const uint32_t last = sm.last_code[lane];
+            if (last > 0 && !mbar_wait_bounded(&sm.code_full[lane], ((last - 1) / kCodeStages) & 1u))
+                set_status(a.status, kStatusTimeout);
+        }
+        if (warp == 2 && lane < kStages) {
+            const uint32_t last = sm.last_a[lane];
+            if (last > 0 && !mbar_wait_bounded(&sm.a_full[lane], ((last - 1) / kStages) & 1u))
+                set_status(a.status, kStatusTimeout);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -572,14 +717,130 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
 // ------------------------------------------------------------ gather, combine
 
-// x_sorted[row(t, j)] = bf16(x[t]) for every slot j (and the shared segment).
-template <bool XBF16>
-__global__ void __launch_bounds__(256) gather_kernel(const void *x, int64_t T, int d, int k,
-                                                     int has_shared, const int32_t *rows,
-                                                     int64_t nrows, uint16_t *xs)
+// Inclusive scan of v over a 256-thread block; *total gets the block sum.
+// s_w holds 8 ints; the caller syncs before reusing it.
+__device__ __forceinline__ int block_scan_incl(int v, int *s_w, int &total)
 {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += u;
+    }
+    if (lane == 31)
+        s_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = lane < 8 ? s_w[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, wv, o);
+            if (lane >= o)
+                wv += u;
+        }
+        if (lane < 8)
+            s_w[lane] = wv;
+    }
+    __syncthreads();
+    total = s_w[7];
+    return incl + (warp > 0 ? s_w[warp - 1] : 0);
+}
+
+// The counting sort of the (token, slot) selections by expert, stable in
+// token order.  The router leaves each 8-token tile's count per expert; one
+// CTA per expert turns its column into exclusive bases in tile order (in
+// place) and its total; the last CTA to finish writes the segment table:
+// first row of every segment (rows padded to 128; the shared expert, all T
+// tokens, last) and its row count.
+__global__ void __launch_bounds__(256) grp_scan_kernel(const GroupedArgs a)
+{
+    __shared__ int s_w[8];
+    __shared__ int s_last;
+    const int e = blockIdx.x, tid = threadIdx.x;
+    const int E = a.E, nseg = E + (a.has_shared ? 1 : 0);
+    int carry = 0;
+    for (int b0 = 0; b0 < a.ntiles; b0 += 256) {
+        const int tl = b0 + tid;
+        int32_t *p = a.tilecnt + (int64_t)tl * E + e;
+        const int c = tl < a.ntiles ? __ldcg(p) : 0;
+        int tot;
+        const int incl = block_scan_incl(c, s_w, tot);
+        if (tl < a.ntiles)
+            *p = carry + incl - c;
+        carry += tot;
+        __syncthreads();
+    }
+    if (tid == 0)
+        a.seg[nseg + 1 + e] = carry;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+        s_last = atomicAdd(a.scan_ctr, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    int run = 0;
+    for (int s0 = 0; s0 < nseg; s0 += 256) {
+        const int sg = s0 + tid;
+        const int c = sg < nseg ? (sg < E ? __ldcg(a.seg + nseg + 1 + sg) : static_cast<int>(a.T)) : 0;
+        const int padc = (c + kGM - 1) / kGM * kGM;
+        int tot;
+        const int incl = block_scan_incl(padc, s_w, tot);
+        if (sg < nseg) {
+            a.seg[sg] = run + incl - padc;
+            if (sg == E)
+                a.seg[nseg + 1 + E] = static_cast<int>(a.T);
+        }
+        run += tot;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        a.seg[nseg] = run;
+        if (run > a.rows) {  // cannot happen with the planned row count
+            set_status(a.status, kStatusBadArg);
+            for (int sg = 0; sg < nseg; ++sg)
+                a.seg[nseg + 1 + sg] = 0;
+        }
+        *a.scan_ctr = 0u;
+    }
+}
+
+// Row of every (token, slot): its segment's first row + its tile's base
+// inside the expert + its rank among the tile's earlier tokens that chose
+// the same expert (a token chooses an expert once).  Then x_sorted[row] =
+// bf16(x[t]) for every slot (and the shared segment).
+template <bool XBF16>
+__global__ void __launch_bounds__(256) gather_kernel(const GroupedArgs a, const void *x)
+{
+    __shared__ int32_t s_rows[SMOE_MAX_TOPK_DEV + 1];
     const int64_t t = blockIdx.x;
-    const int nslot = k + (has_shared ? 1 : 0);
+    const int d = a.d, k = a.k, E = a.E;
+    const int nslot = k + (a.has_shared ? 1 : 0);
+    if (static_cast<int>(threadIdx.x) < nslot) {
+        const int j = threadIdx.x;
+        int64_t row = -1;
+        if (j < k) {
+            const int e = __ldg(a.ids + t * k + j);
+            if (e >= 0 && e < E) {
+                const int64_t tile = t / kPairCols;
+                int local = 0;
+                for (int64_t t2 = tile * kPairCols; t2 < t; ++t2)
+                    for (int j2 = 0; j2 < k; ++j2)
+                        local += __ldg(a.ids + t2 * k + j2) == e ? 1 : 0;
+                row = (int64_t)__ldg(a.seg + e) + __ldg(a.tilecnt + tile * E + e) + local;
+            }
+        } else {
+            row = (int64_t)__ldg(a.seg + E) + t;
+        }
+        if (row < 0 || row >= a.rows)
+            row = -1;
+        s_rows[j] = static_cast<int32_t>(row);
+        a.rows_of[t * (k + 1) + j] = static_cast<int32_t>(row);
+    }
+    __syncthreads();
     for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
         uint4 v;
         if (XBF16) {
@@ -591,9 +852,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *x, int64_t T, i
                            pack_bf16x2(a1.z, a1.w));
         }
         for (int j = 0; j < nslot; ++j) {
-            const int32_t r = __ldg(rows + t * (k + 1) + (j < k ? j : k));
-            if (r >= 0 && r < nrows)
-                *reinterpret_cast<uint4 *>(xs + (int64_t)r * d + c) = v;
+            const int32_t r = s_rows[j];
+            if (r >= 0)
+                *reinterpret_cast<uint4 *>(a.xs + (int64_t)r * d + c) = v;
         }
     }
 }
@@ -716,10 +977,11 @@ cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, cons
     if (!make_map(&mx, a.xs, a.rows, a.d) || !make_map(&mh, a.h, a.rows, a.hstride))
         return cudaErrorInvalidValue;
     const unsigned nt = static_cast<unsigned>(a.T);
+    grp_scan_kernel<<<a.E, 256, 0, s>>>(a);
     if (x_bf16)
-        gather_kernel<true><<<nt, 256, 0, s>>>(x, a.T, a.d, a.k, a.has_shared, a.rows_of, a.rows, a.xs);
+        gather_kernel<true><<<nt, 256, 0, s>>>(a, x);
     else
-        gather_kernel<false><<<nt, 256, 0, s>>>(x, a.T, a.d, a.k, a.has_shared, a.rows_of, a.rows, a.xs);
+        gather_kernel<false><<<nt, 256, 0, s>>>(a, x);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;

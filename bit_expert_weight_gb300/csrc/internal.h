@@ -72,10 +72,8 @@ struct RouteArgs {
     unsigned *done_ctr;         // [1]
     int *status;
     int max_pairs;
-    // expert-sorted rows of the grouped path (null: not built)
-    int32_t *grp_row;           // [T][k+1] sorted row of (token, slot); slot k: shared
-    int32_t *grp_seg;           // [nseg+1] first row per segment, then [nseg] rows used
-    int64_t grp_rows;           // rows available in the sorted matrices
+    // grouped path (null: the streaming path's pair table is built instead)
+    int32_t *grp_tilecnt;       // [T/8 tiles][E] selections per (token tile, expert)
 };
 
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
@@ -134,9 +132,13 @@ struct GroupedArgs {
     int64_t down_off_routed, down_off_shared;
     int64_t T;
     int d, f, fs, E, k, bits, has_shared;
-    const int32_t *seg;            // [nseg+1] first rows, then [nseg] counts
-    const int32_t *rows_of;        // [T][k+1]
+    int32_t *seg;                  // [nseg+1] first rows, then [nseg] counts
+    int32_t *rows_of;              // [T][k+1] sorted row of (token, slot); slot k: shared
     int64_t rows;                  // rows of xs, h and o
+    const int32_t *ids;            // [T][k] routing
+    int32_t *tilecnt;              // [ntiles][E] from the router; scanned in place
+    int ntiles;                    // token tiles of the router (8 tokens each)
+    unsigned *scan_ctr;            // zero-initialised arrival counter
     uint16_t *xs;                  // bf16 [rows][d]
     uint16_t *h;                   // bf16 [rows][hstride]
     int hstride;                   // max(f, fs)

@@ -122,7 +122,6 @@ __global__ void __launch_bounds__(kRThreads) route_logits_kernel(const float *lo
 struct DispatchSmem {
     int cnt[kMaxExperts];
     int pbase[kMaxExperts + 1];
-    int goff[kMaxExperts + 1];  // grouped path: first sorted row per segment
     int run[kMaxExperts];
     unsigned mask[kRWarps][kMaxExperts];
     int wbase[kRWarps][kMaxExperts];
@@ -155,27 +154,6 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
     __syncthreads();
     __shared__ int s_ok, s_pr, s_pt;
     if (tid == 0) {
-        if (a.grp_row) {
-            // segments: the experts, then the shared expert; rows padded to 128
-            const int nseg = E + (a.has_shared ? 1 : 0);
-            int64_t G = 0;
-            for (int e = 0; e < E; ++e) {
-                s.goff[e] = static_cast<int>(G);
-                G += (s.cnt[e] + 127) / 128 * 128;
-            }
-            s.goff[E] = static_cast<int>(G);
-            if (a.has_shared)
-                G += (T + 127) / 128 * 128;
-            const bool fits = G <= a.grp_rows;
-            if (!fits)
-                set_status(a.status, kStatusBadArg);
-            for (int sg = 0; sg < nseg; ++sg) {
-                a.grp_seg[sg] = fits ? (sg < E ? s.goff[sg] : s.goff[E]) : 0;
-                a.grp_seg[nseg + 1 + sg] =
-                    fits ? (sg < E ? s.cnt[sg] : static_cast<int>(T)) : 0;
-            }
-            a.grp_seg[nseg] = fits ? static_cast<int>(G) : 0;
-        }
         int P = 0;
         for (int e = 0; e < E; ++e) {
             s.pbase[e] = P;
@@ -194,11 +172,6 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
         if (tid == 0) {
             a.meta[0] = 0;
             a.meta[1] = 0;
-            if (a.grp_row) {
-                const int nseg = E + (a.has_shared ? 1 : 0);
-                for (int sg = 0; sg <= 2 * nseg; ++sg)
-                    a.grp_seg[sg] = 0;
-            }
         }
         return;
     }
@@ -232,13 +205,9 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
                 const int e = ev[j];
                 if (e < 0) {
                     a.route_map[t * (k + 1) + j] = 0;
-                    if (a.grp_row)
-                        a.grp_row[t * (k + 1) + j] = -1;
                     continue;
                 }
                 const int pos = s.wbase[warp][e] + __popc(s.mask[warp][e] & lt_mask);
-                if (a.grp_row)
-                    a.grp_row[t * (k + 1) + j] = s.goff[e] + pos;
                 const int pair = s.pbase[e] + pos / kPairCols, col = pos % kPairCols;
                 int32_t *pr = a.pairs + pair * kPairInts;
                 pr[2 + col] = static_cast<int32_t>(t);
@@ -262,11 +231,8 @@ __device__ void dispatch(const RouteArgs &a, DispatchSmem &s)
             pr[2 + i] = static_cast<int32_t>((int64_t)c * kPairCols + i < T ? c * kPairCols + i : 0);
     }
     if (a.has_shared)
-        for (int64_t t = tid; t < T; t += kRThreads) {
+        for (int64_t t = tid; t < T; t += kRThreads)
             a.route_map[t * (k + 1) + k] = static_cast<int32_t>((P_r + t / kPairCols) * kPairCols + t % kPairCols);
-            if (a.grp_row)
-                a.grp_row[t * (k + 1) + k] = s.goff[E] + static_cast<int32_t>(t);
-        }
     if (tid == 0) {
         a.meta[0] = P_r;
         a.meta[1] = P_t;
@@ -310,41 +276,63 @@ __global__ void __launch_bounds__(kRThreads) router_kernel(const RouteArgs a)
                                : (r == E && a.shared_gate ? a.shared_gate : nullptr);
         }
     float xs = 0.f;  // per-lane activation sum of the current group (class tig & 1)
-    for (int k = kb; k < kb + Kc; k += 16) {
-        uint32_t b0, b1, b0l = 0u, b1l = 0u;
-        if (XBF16) {
-            const uint16_t *xr = reinterpret_cast<const uint16_t *>(a.x) + tok * d + k + 2 * tig;
-            b0 = tvalid ? __ldg(reinterpret_cast<const uint32_t *>(xr)) : 0u;
-            b1 = tvalid ? __ldg(reinterpret_cast<const uint32_t *>(xr + 8)) : 0u;
-            if (warp == 0)
-                xs += bf16lo_to_f32(b0) + bf16hi_to_f32(b0) + bf16lo_to_f32(b1) + bf16hi_to_f32(b1);
-        } else {
-            const float *xr = reinterpret_cast<const float *>(a.x) + tok * d + k + 2 * tig;
-            const float2 v0 = tvalid ? __ldg(reinterpret_cast<const float2 *>(xr)) : make_float2(0.f, 0.f);
-            const float2 v1 = tvalid ? __ldg(reinterpret_cast<const float2 *>(xr + 8)) : make_float2(0.f, 0.f);
-            split_bf16x2(v0.x, v0.y, b0, b0l);
-            split_bf16x2(v1.x, v1.y, b1, b1l);
-            if (warp == 0)
-                xs += (v0.x + v0.y) + (v1.x + v1.y);
-        }
+    // one quantisation group (4 k-steps of 16) per iteration: every load of
+    // the group is issued before its MMAs, so the L2 round trips overlap
+    for (int k0 = kb; k0 < kb + Kc; k0 += kGroup) {
+        uint32_t b0[4], b1[4], b0l[4], b1l[4];
+        float xs4[4];
 #pragma unroll
-        for (int i = 0; i < kMtPerWarp; ++i) {
-            if (warp + kRWarps * i >= mtiles)
-                continue;
-            uint32_t A[4];
-            A[0] = rowp[i][0] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][0] + k + 2 * tig)) : 0u;
-            A[1] = rowp[i][1] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][1] + k + 2 * tig)) : 0u;
-            A[2] = rowp[i][0] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][0] + k + 2 * tig + 8)) : 0u;
-            A[3] = rowp[i][1] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][1] + k + 2 * tig + 8)) : 0u;
-            mma_bf16(acc[i], A, b0, b1);
-            if (!XBF16)
-                mma_bf16(acc[i], A, b0l, b1l);
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + 16 * j;
+            b0l[j] = b1l[j] = 0u;
+            if (XBF16) {
+                const uint16_t *xr = reinterpret_cast<const uint16_t *>(a.x) + tok * d + k + 2 * tig;
+                b0[j] = tvalid ? __ldg(reinterpret_cast<const uint32_t *>(xr)) : 0u;
+                b1[j] = tvalid ? __ldg(reinterpret_cast<const uint32_t *>(xr + 8)) : 0u;
+            } else {
+                const float *xr = reinterpret_cast<const float *>(a.x) + tok * d + k + 2 * tig;
+                const float2 v0 = tvalid ? __ldg(reinterpret_cast<const float2 *>(xr)) : make_float2(0.f, 0.f);
+                const float2 v1 = tvalid ? __ldg(reinterpret_cast<const float2 *>(xr + 8)) : make_float2(0.f, 0.f);
+                split_bf16x2(v0.x, v0.y, b0[j], b0l[j]);
+                split_bf16x2(v1.x, v1.y, b1[j], b1l[j]);
+                xs4[j] = (v0.x + v0.y) + (v1.x + v1.y);
+            }
         }
-        if (warp == 0 && ((k + 16) & 63) == 0) {
+        uint32_t A[kMtPerWarp][4][4];
+#pragma unroll
+        for (int i = 0; i < kMtPerWarp; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = k0 + 16 * j;
+                const bool on = warp + kRWarps * i < mtiles;
+                A[i][j][0] = on && rowp[i][0] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][0] + k + 2 * tig)) : 0u;
+                A[i][j][1] = on && rowp[i][1] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][1] + k + 2 * tig)) : 0u;
+                A[i][j][2] = on && rowp[i][0] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][0] + k + 2 * tig + 8)) : 0u;
+                A[i][j][3] = on && rowp[i][1] ? __ldg(reinterpret_cast<const uint32_t *>(rowp[i][1] + k + 2 * tig + 8)) : 0u;
+            }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (warp == 0) {
+                if (XBF16)
+                    xs += bf16lo_to_f32(b0[j]) + bf16hi_to_f32(b0[j]) + bf16lo_to_f32(b1[j]) +
+                          bf16hi_to_f32(b1[j]);
+                else
+                    xs += xs4[j];
+            }
+#pragma unroll
+            for (int i = 0; i < kMtPerWarp; ++i) {
+                if (warp + kRWarps * i >= mtiles)
+                    continue;
+                mma_bf16(acc[i], A[i][j], b0[j], b1[j]);
+                if (!XBF16)
+                    mma_bf16(acc[i], A[i][j], b0l[j], b1l[j]);
+            }
+        }
+        if (warp == 0) {
             // group complete: lanes tig and tig ^ 2 hold the same class
             const float tot = xs + __shfl_xor_sync(0xffffffffu, xs, 2);
             if (tig < 2 && tvalid)
-                a.xsum[(tok * (d / kGroup) + k / kGroup) * 2 + tig] = tot;
+                a.xsum[(tok * (d / kGroup) + k0 / kGroup) * 2 + tig] = tot;
             xs = 0.f;
         }
     }
@@ -394,6 +382,26 @@ __global__ void __launch_bounds__(kRThreads) router_kernel(const RouteArgs a)
     }
     if (tid == 0)
         a.tile_ctr[nt] = 0u;
+    if (a.grp_tilecnt) {
+        // grouped path: this tile's selections per expert; the sort's scan
+        // and row assignment run in their own kernels
+        __syncthreads();  // routing done: the logit buffer is free, ids written
+        for (int e = tid; e < E; e += kRThreads)
+            sm.dsp.cnt[e] = 0;
+        __syncthreads();
+        for (int i = tid; i < kPairCols * a.k; i += kRThreads) {
+            const int64_t t = t0 + i / a.k;
+            if (t < a.T) {
+                const int e = __ldcg(a.ids + t * a.k + i % a.k);
+                if (e >= 0 && e < E)
+                    atomicAdd(&sm.dsp.cnt[e], 1);
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += kRThreads)
+            a.grp_tilecnt[(int64_t)nt * E + e] = sm.dsp.cnt[e];
+        return;
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) {
