@@ -554,8 +554,15 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
         ga.hstride = P.fmax;
         ga.o = at<float>(workspace, P.off_go);
         ga.status = status;
-        if (launch_router(ra, s, false) != cudaSuccess)
+        if (ra.x_bf16) {
+            if (launch_tc_logits(static_cast<const uint16_t *>(x), ra.router_w, num_tokens,
+                                 L.d_model, L.num_experts, P.Epad, la.logits, status,
+                                 s) != cudaSuccess ||
+                launch_route_tiles(ra, la.logits, P.Epad, s) != cudaSuccess)
+                return SMOE_ERR_CUDA;
+        } else if (launch_router(ra, s, false) != cudaSuccess) {
             return SMOE_ERR_CUDA;
+        }
         return launch_grouped(ga, x, ra.x_bf16, ra.weights, ra.shared_w, y, s) == cudaSuccess
                    ? SMOE_OK
                    : SMOE_ERR_CUDA;

@@ -894,6 +894,127 @@ __global__ void __launch_bounds__(256) grouped_combine_kernel(const float *o, in
     }
 }
 
+// ------------------------------------------------------------ router logits
+
+// logits[t, e] = sum_i x[t, i] * Wr[e, i] for a batch of bf16 tokens, on the
+// tensor cores: one CTA per 128 tokens x 128 experts, both operands by TMA
+// (128-byte swizzle, 4 stages), fp32 accumulation in tensor memory ("Model
+// Agnosticism": the gate has max_experts_per_layer rows).  Warp 0 lane 0
+// loads, warp 1 lane 0 issues the MMAs, all four warps write the logits.
+constexpr int kRStages = 4;
+constexpr uint32_t kRIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                             ((128u >> 4) << 24);
+
+struct RSmem {
+    uint64_t full[kRStages], empty[kRStages], done;
+    uint32_t tmem_base;
+    uint32_t last[kRStages];
+    int fail;
+};
+
+__global__ void __launch_bounds__(128, 1)
+    tc_logits_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw,
+                     int64_t T, int d, int E, int Epad, uint32_t stage_tx, float *logits, int *status)
+{
+    extern __shared__ uint8_t r_smem_raw[];
+    __shared__ RSmem sm;
+    uint8_t *base = r_smem_raw + ((1024u - (smem_u32(r_smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = base, *sB = base + kRStages * kATileBytes;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t m0 = (int64_t)blockIdx.x * 128;
+    const int n0 = blockIdx.y * 128;
+    const int nkb = d / kGK;
+    if (tid == 0) {
+        for (int s = 0; s < kRStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+            sm.last[s] = 0;
+        }
+        mbar_init(&sm.done, 1);
+        sm.fail = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sm.tmem_base)),
+                     "r"(128)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sm.tmem_base;
+    volatile int *fail = &sm.fail;
+    if (tid == 0) {
+        for (int kb = 0; kb < nkb && !*fail; ++kb) {
+            const int s = kb % kRStages;
+            if (!mbar_wait_bounded(&sm.empty[s], ((kb / kRStages) & 1) ^ 1)) {
+                set_status(status, kStatusTimeout);
+                *fail = 1;
+                break;
+            }
+            mbar_arrive_expect_tx(&sm.full[s], stage_tx);
+            sm.last[s] = kb + 1;
+            tma_load_2d(sA + s * kATileBytes, &mx, kb * kGK, static_cast<int>(m0), &sm.full[s]);
+            tma_load_2d(sB + s * kATileBytes, &mw, kb * kGK, n0, &sm.full[s]);
+        }
+    } else if (tid == 32) {
+        const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
+        for (int kb = 0; kb < nkb && !*fail; ++kb) {
+            const int s = kb % kRStages;
+            if (!mbar_wait_bounded(&sm.full[s], (kb / kRStages) & 1)) {
+                set_status(status, kStatusTimeout);
+                *fail = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t off = (uint64_t)(s * (kATileBytes >> 4));
+#pragma unroll
+            for (int ks = 0; ks < kGK / 16; ++ks)
+                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tbase),
+                             "l"(ad0 + off + 2 * ks), "l"(bd0 + off + 2 * ks), "r"(kRIdesc),
+                             "r"((kb | ks) != 0 ? 1u : 0u)
+                             : "memory");
+            umma_commit(&sm.empty[s]);
+        }
+        umma_commit(&sm.done);
+    }
+    __syncwarp();
+    // every warp: its 32 rows of the accumulator
+    const bool ok = mbar_wait_bounded(&sm.done, 0);
+    if (!ok && lane == 0) {
+        set_status(status, kStatusTimeout);
+        *fail = 1;
+    }
+    tc_fence_after();
+    if (__all_sync(0xffffffffu, ok) && !*fail) {
+        const int64_t row = m0 + 32 * warp + lane;
+        for (int c = 0; c < 128 && n0 + c < E; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(tbase + (static_cast<uint32_t>(32 * warp) << 16) + c, v);
+            tmem_wait_ld();
+            if (row < T)
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    if (n0 + c + q < E)
+                        logits[row * Epad + n0 + c + q] = __uint_as_float(v[q]);
+        }
+    }
+    // after a failure: no copy of this CTA may still be in flight
+    if (*fail && tid < kRStages && sm.last[tid] > 0 &&
+        !mbar_wait_bounded(&sm.full[tid], ((sm.last[tid] - 1) / kRStages) & 1))
+        set_status(status, kStatusTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(128)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -917,16 +1038,16 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Tensor map of a row-major bf16 matrix [rows, cols] read in 128 x 64 boxes
-// with the 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols)
+// Tensor map of a row-major bf16 matrix [rows, cols] read in box_rows x 64
+// boxes with the 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int box_rows = kGM)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGK), static_cast<cuuint32_t>(kGM)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGK), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -957,6 +1078,40 @@ cudaError_t launch_gemm_t(const GroupedArgs &a, const CUtensorMap &map, cudaStre
 }
 
 }  // namespace
+
+cudaError_t launch_tc_logits(const uint16_t *x, const uint16_t *router_w, int64_t T, int d, int E,
+                             int Epad, float *logits, int *status, cudaStream_t s)
+{
+    if (T == 0)
+        return cudaSuccess;
+    // boxes never taller than the matrices: rows past the end of a box are
+    // left over from earlier stages and only reach accumulator rows/columns
+    // that are not written out
+    const int bx = T < kGM ? static_cast<int>(T) : kGM;
+    const int bw = E < 128 ? E : 128;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, T, d, bx) || !make_map(&mw, router_w, E, d, bw))
+        return cudaErrorInvalidValue;
+    const int smem = 2 * kRStages * kATileBytes + 1024;
+    static std::mutex mu;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(tc_logits_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess)
+                return e;
+            attr_set[dev] = true;
+        }
+    }
+    const dim3 grid(static_cast<unsigned>((T + 127) / 128), static_cast<unsigned>((E + 127) / 128));
+    const uint32_t tx = static_cast<uint32_t>(kGK * 2 * (bx + bw));
+    tc_logits_kernel<<<grid, 128, smem, s>>>(mx, mw, T, d, E, Epad, tx, logits, status);
+    return cudaGetLastError();
+}
 
 int64_t grouped_max_rows(int64_t T, int E, int k, int has_shared)
 {

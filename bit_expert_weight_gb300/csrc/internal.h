@@ -79,6 +79,10 @@ struct RouteArgs {
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
                                 const float *bias, int32_t *ids, float *w, cudaStream_t stream);
 cudaError_t launch_router(const RouteArgs &a, cudaStream_t stream, bool pdl);
+// Grouped path, bf16 tokens: routing of tiles of 8 tokens from logits
+// [T][Epad] (plus the shared gate and the per-tile expert counts).
+cudaError_t launch_route_tiles(const RouteArgs &a, const float *logits, int Epad,
+                               cudaStream_t stream);
 
 // The fused layer kernel (layer.cu): one CTA of 16 warps per SM.
 constexpr int kMaxLayerCtasPerSm = 1;
@@ -150,6 +154,9 @@ struct GroupedArgs {
 // holds its buffers).
 constexpr int64_t kGroupedMinT = 16;
 int64_t grouped_max_rows(int64_t T, int E, int k, int has_shared);
+// logits[T][Epad] = x Wr^T on the tensor cores (bf16 x, 16-byte aligned rows).
+cudaError_t launch_tc_logits(const uint16_t *x, const uint16_t *router_w, int64_t T, int d, int E,
+                             int Epad, float *logits, int *status, cudaStream_t stream);
 cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, const float *w,
                            const float *sw, float *y, cudaStream_t stream);
 

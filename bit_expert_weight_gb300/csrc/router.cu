@@ -417,7 +417,66 @@ __global__ void __launch_bounds__(kRThreads) router_kernel(const RouteArgs a)
         *a.done_ctr = 0u;
 }
 
+// Grouped path with bf16 tokens: the logits come from the tensor-core GEMM.
+// One CTA per 8-token tile, one warp per token: the shared expert's gate
+// logit (sum_i gate[i] * x[t, i], fp32), the routing, then the tile's
+// selections per expert for the sort.
+__global__ void __launch_bounds__(kRThreads) route_tiles_kernel(const RouteArgs a, const float *logits,
+                                                                int Epad)
+{
+    __shared__ int cnt[kMaxExperts];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = a.E, k = a.k;
+    const int64_t t0 = (int64_t)blockIdx.x * kPairCols;
+    for (int e = tid; e < E; e += kRThreads)
+        cnt[e] = 0;
+    const int64_t t = t0 + warp;
+    if (warp < kPairCols && t < a.T) {
+        route_token_warp(logits + t * Epad, E, k, a.norm, a.expert_bias, a.ids + t * k,
+                         a.weights + t * k, a.ids_out ? a.ids_out + t * k : nullptr,
+                         a.w_out ? a.w_out + t * k : nullptr, a.status);
+        float sw = 1.0f;
+        if (a.shared_gate) {
+            const uint16_t *xr = static_cast<const uint16_t *>(a.x) + t * a.d;
+            float acc = 0.f;
+            // the gate vector is 4-byte aligned (API contract): 32-bit loads
+            for (int i = 2 * lane; i < a.d; i += 64) {
+                const uint32_t xv = __ldg(reinterpret_cast<const uint32_t *>(xr + i));
+                const uint32_t gv = __ldg(reinterpret_cast<const uint32_t *>(a.shared_gate + i));
+                acc = fmaf(bf16lo_to_f32(xv), bf16lo_to_f32(gv), acc);
+                acc = fmaf(bf16hi_to_f32(xv), bf16hi_to_f32(gv), acc);
+            }
+            for (int o = 16; o; o >>= 1)
+                acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            sw = 1.0f / (1.0f + expf(-acc));
+        }
+        if (lane == 0)
+            a.shared_w[t] = sw;
+    }
+    __syncthreads();  // the tile's ids are written
+    for (int i = tid; i < kPairCols * k; i += kRThreads) {
+        const int64_t tt = t0 + i / k;
+        if (tt < a.T) {
+            const int e = __ldcg(a.ids + tt * k + i % k);
+            if (e >= 0 && e < E)
+                atomicAdd(&cnt[e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kRThreads)
+        a.grp_tilecnt[(int64_t)blockIdx.x * E + e] = cnt[e];
+}
+
 }  // namespace
+
+cudaError_t launch_route_tiles(const RouteArgs &a, const float *logits, int Epad, cudaStream_t stream)
+{
+    if (a.T == 0)
+        return cudaSuccess;
+    route_tiles_kernel<<<static_cast<unsigned>((a.T + kPairCols - 1) / kPairCols), kRThreads, 0,
+                         stream>>>(a, logits, Epad);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
                                 const float *bias, int32_t *ids, float *w, cudaStream_t stream)

@@ -17,7 +17,8 @@ torch = pytest.importorskip("torch")
 
 from bit_expert_weight_gb300 import synth as Y  # noqa: E402
 
-from helpers import HostLayer, check_forward, to_dev  # noqa: E402
+import oracle as O  # noqa: E402
+from helpers import HostLayer, check_forward, near_tie_tokens, to_dev  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -102,14 +103,19 @@ def test_grouped_with_expert_bias_skew(S):
 
 
 def test_grouped_agrees_with_streaming_path(S):
+    """The two paths make their logits in different summation orders (tensor
+    cores vs the streaming router), so ids may differ only on near-tie tokens
+    and weights only in rounding."""
     wl, hl = host_layer("wide_bf16", 4)
     lay = hl.device_layer(DEV)
     x, _ = wl.activations(0, 96)
     yg, idg, wg = run(S, lay, wl, x, S.PATH_GROUPED)
     ys, ids_, ws_ = run(S, lay, wl, x, S.PATH_STREAM)
-    assert np.array_equal(idg, ids_)
-    assert np.array_equal(wg, ws_)
-    assert float(np.abs(yg - ys).max()) <= TOL * float(np.abs(ys).max())
+    ties = set(near_tie_tokens(O.router_logits(hl.router, x), wl.k))
+    same = [t for t in range(x.shape[0]) if t not in ties]
+    assert np.array_equal(idg[same], ids_[same])
+    assert np.allclose(wg[same], ws_[same], rtol=1e-5, atol=1e-6)
+    assert float(np.abs(yg[same] - ys[same]).max()) <= TOL * float(np.abs(ys).max())
 
 
 def test_grouped_is_deterministic(S):
