@@ -40,6 +40,7 @@ from bit_expert_weight_gb300 import synth as Y  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and fused-dequant HBM GB/s vs GB300 peak (Q4 and Q2)"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -69,9 +70,21 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s: the measured burst figure (a kernel
+    timed by itself), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash(files=("layer.cu", "common.cuh")):
     h = hashlib.sha256()
-    for f in ("layer.cu", "common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "bit_expert_weight_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -200,6 +213,7 @@ class DeviceModel:
         torch.cuda.synchronize()
         self.setup_s = time.time() - t0
         self.ws = S.workspace(self.layers[0], T)
+        self.grouped = S.path_for(self.layers[0], T) == S.PATH_GROUPED
         self.ids = [torch.empty((T, wl.k), dtype=torch.int32, device=dev) for _ in self.layers]
         self.resident_bytes = sum(l.expert_tiles.numel() for l in self.layers)
 
@@ -209,13 +223,24 @@ class DeviceModel:
             S.forward(lay, x, self.ws, y=y, ids=ids)
 
     def step_timed(self, evs):
-        """The same step with events around every layer's launch(es): for
-        T <= 8 a layer is one fused kernel (router, experts, combine)."""
+        """The same step with events around the dominant kernel of every
+        layer: for T <= 8 the fused layer kernel (router, experts, combine);
+        on the grouped path the gate/up grouped GEMM (stage 1), the other
+        stages bracketed by events too (evs[i] = 4 events)."""
         import bit_expert_weight_gb300.smoe as S
         for i, (lay, x, y, ids) in enumerate(zip(self.layers, self.x, self.y, self.ids)):
-            evs[i][0].record()
-            S.forward(lay, x, self.ws, y=y, ids=ids)
-            evs[i][1].record()
+            if self.grouped:
+                evs[i][2].record()
+                S.forward_stage(lay, 0, x, self.ws, y, ids=ids)
+                evs[i][0].record()
+                S.forward_stage(lay, 1, x, self.ws, y, ids=ids)
+                evs[i][1].record()
+                S.forward_stage(lay, 2, x, self.ws, y, ids=ids)
+                evs[i][3].record()
+            else:
+                evs[i][0].record()
+                S.forward(lay, x, self.ws, y=y, ids=ids)
+                evs[i][1].record()
 
 
 def layer_algorithmic_bytes(model):
@@ -231,6 +256,31 @@ def layer_algorithmic_bytes(model):
             b += 3 * (wl.shared_f * wl.d * bits // 8 + wl.shared_f * wl.d // 64 * 2) + wl.d * 2
         tot += b
     return tot / len(model.ids)
+
+
+def gateup_bytes(model):
+    """Algorithmic bytes of the gate/up grouped GEMM per layer: the gate and
+    up codes and scales of the distinct experts the tokens selected (plus the
+    shared expert's), the bf16 token rows in and the bf16 h rows out."""
+    wl, bits = model.wl, model.bits
+    per = 2 * (wl.f * wl.d * bits // 8 + wl.f * wl.d // 64 * 2)
+    distinct = np.mean([len(np.unique(ids.cpu().numpy())) for ids in model.ids])
+    b = distinct * per + model.T * wl.d * 2 + model.T * wl.k * wl.f * 2
+    if wl.shared_f:
+        b += 2 * (wl.shared_f * wl.d * bits // 8 + wl.shared_f * wl.d // 64 * 2)
+        b += model.T * wl.shared_f * 2
+    return float(b)
+
+
+def gateup_flops(model):
+    """Algorithmic flops of the gate/up grouped GEMM per layer: 2 (gate and
+    up) x 2 (multiply-add) x d x f per routed (token, slot), plus the shared
+    expert's over all tokens; padding rows are not counted."""
+    wl = model.wl
+    f = 4.0 * model.T * wl.k * wl.d * wl.f
+    if wl.shared_f:
+        f += 4.0 * model.T * wl.d * wl.shared_f
+    return f
 
 
 def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
@@ -287,14 +337,14 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
 
     # dominant kernel (the fused layer kernel): events around each launch
     reps = max(3, min(50, args.steps))
-    evs = [(torch.cuda.Event(enable_timing=True, external=True),
-            torch.cuda.Event(enable_timing=True, external=True)) for _ in model.layers]
+    evs = [tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(4))
+           for _ in model.layers]
     g2 = None
     if use_graph:
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=stream):
             model.step_timed(evs)
-    durs = []
+    durs, stage_ms = [], []
     with torch.cuda.stream(stream):
         for _ in range(reps):
             if g2 is not None:
@@ -302,7 +352,10 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
             else:
                 model.step_timed(evs)
             stream.synchronize()
-            durs.extend(a.elapsed_time(b) for a, b in evs)
+            durs.extend(e[0].elapsed_time(e[1]) for e in evs)
+            if model.grouped:
+                stage_ms.extend((e[2].elapsed_time(e[0]), e[0].elapsed_time(e[1]),
+                                 e[1].elapsed_time(e[3])) for e in evs)
     kern_ms = float(np.mean(durs))
     layer_bytes = layer_algorithmic_bytes(model)
 
@@ -356,7 +409,13 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
         "e2e_tokens_per_s": world * T * args.steps / (e2e_ms / 1e3),
         "h2d": h2d, "d2h": d2h, "clocks": clocks, "setup_s": model.setup_s,
         "resident_GB": model.resident_bytes / 1e9, "device_status": status,
-        "launches_per_step": n_layers if T <= 8 else 3 * n_layers,
+        "launches_per_step": n_layers * (1 if T <= 8 else
+                                         (7 if model.x[0].dtype == torch.bfloat16 else 6)
+                                         if model.grouped else 3),
+        "grouped": model.grouped,
+        "stage_us": [float(v) * 1e3 for v in np.mean(stage_ms, axis=0)] if stage_ms else None,
+        "gemm1_flops": gateup_flops(model) if model.grouped else None,
+        "gemm1_bytes": gateup_bytes(model) if model.grouped else None,
     }
     del model, graph, g2, g3
     torch.cuda.empty_cache()
@@ -479,6 +538,38 @@ def main():
                          f"{len(times)}x ({dt:.3f} s each), x{n_layers} layers extrapolated"}
     if rank != 0:
         return
+    if r["grouped"]:
+        # the binding roofline of the gate/up GEMM: flops / tensor peak or
+        # weight bytes / HBM bandwidth, whichever ideal time is longer
+        tp, tp_kind = tensor_peak()
+        t_tc = r["gemm1_flops"] / (tp * 1e12)
+        t_hbm = r["gemm1_bytes"] / (hbm * 1e9)
+        sec = r["kernel_us"] * 1e-6
+        if t_tc >= t_hbm:
+            ach = r["gemm1_flops"] / sec / 1e12
+            roofline = {"bound": "tensor", "achieved": ach, "peak": tp, "unit": "TFLOP/s",
+                        "frac": ach / tp, "peak_kind": tp_kind}
+        else:
+            ach = r["gemm1_bytes"] / sec / 1e9
+            roofline = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                        "frac": ach / hbm, "peak_kind": peak_kind}
+        roofline.update({
+            "traffic": None,
+            "kernel": "grouped_gemm_kernel (gate/up: dequant to bf16 in shared memory, "
+                      "tcgen05 MMA, SiLU(g)*u epilogue)",
+            "flops_per_launch": r["gemm1_flops"], "bytes_per_launch": r["gemm1_bytes"],
+            "launch_us": r["kernel_us"],
+            "ideal_us": {"tensor": t_tc * 1e6, "hbm": t_hbm * 1e6},
+            "stage_us": {"route_sort_gather": r["stage_us"][0],
+                         "gateup_gemm": r["stage_us"][1],
+                         "down_gemm_combine": r["stage_us"][2]}})
+    else:
+        roofline = {"bound": "hbm", "achieved": r["kernel_alg_GBps"], "peak": hbm,
+                    "unit": "GB/s", "frac": r["kernel_alg_GBps"] / hbm, "traffic": traffic,
+                    "kernel": "moe_layer_kernel (router, top-k, dispatch, fused dequant "
+                              "gate/up + SiLU, fused dequant down, combine)",
+                    "bytes_per_launch": r["layer_alg_bytes"],
+                    "launch_us": r["kernel_us"], "peak_kind": peak_kind}
     line = {
         "metric": METRIC, "value": r["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
@@ -492,12 +583,7 @@ def main():
                    "l2": "inputs larger than L2 (per-step weight footprint "
                          f"{r['layer_alg_bytes'] * n_layers / 1e6:.0f} MB > 129 MB); no flush",
                    "graph": not args.no_graph, "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": r["kernel_alg_GBps"], "peak": hbm,
-                     "unit": "GB/s", "frac": r["kernel_alg_GBps"] / hbm, "traffic": traffic,
-                     "kernel": "moe_layer_kernel (router, top-k, dispatch, fused dequant "
-                               "gate/up + SiLU, fused dequant down, combine)",
-                     "bytes_per_launch": r["layer_alg_bytes"],
-                     "launch_us": r["kernel_us"], "peak_kind": peak_kind},
+        "roofline": roofline,
         "layer": {"us": r["layer_us"], "alg_GBps": r["layer_alg_GBps"],
                   "frac": r["layer_alg_GBps"] / hbm, "tokens_per_s": r["layer_tokens_per_s"]},
         "e2e": {"value": r["e2e_tokens_per_s"], "unit": "tokens/s",

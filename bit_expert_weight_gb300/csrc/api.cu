@@ -437,7 +437,7 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     int *status = device_status_word();
     const bool grouped = path == SMOE_PATH_GROUPED ||
                          (path == SMOE_PATH_AUTO && auto_grouped(layer, num_tokens));
-    if (grouped && (!P.grouped || stage_mask != 7))
+    if (grouped && !P.grouped)
         return SMOE_ERR_UNSUPPORTED;
     // T <= 8 with all stages: one fused launch (routing inside the kernel)
     const bool fused = num_tokens <= kFusedCombineMaxT && stage_mask == 7;
@@ -554,16 +554,19 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
         ga.hstride = P.fmax;
         ga.o = at<float>(workspace, P.off_go);
         ga.status = status;
-        if (ra.x_bf16) {
-            if (launch_tc_logits(static_cast<const uint16_t *>(x), ra.router_w, num_tokens,
-                                 L.d_model, L.num_experts, P.Epad, la.logits, status,
-                                 s) != cudaSuccess ||
-                launch_route_tiles(ra, la.logits, P.Epad, s) != cudaSuccess)
+        if (stage_mask & 1) {
+            if (ra.x_bf16) {
+                if (launch_tc_logits(static_cast<const uint16_t *>(x), ra.router_w, num_tokens,
+                                     L.d_model, L.num_experts, P.Epad, la.logits, status,
+                                     s) != cudaSuccess ||
+                    launch_route_tiles(ra, la.logits, P.Epad, s) != cudaSuccess)
+                    return SMOE_ERR_CUDA;
+            } else if (launch_router(ra, s, false) != cudaSuccess) {
                 return SMOE_ERR_CUDA;
-        } else if (launch_router(ra, s, false) != cudaSuccess) {
-            return SMOE_ERR_CUDA;
+            }
         }
-        return launch_grouped(ga, x, ra.x_bf16, ra.weights, ra.shared_w, y, s) == cudaSuccess
+        return launch_grouped(ga, x, ra.x_bf16, ra.weights, ra.shared_w, y, stage_mask, s) ==
+                       cudaSuccess
                    ? SMOE_OK
                    : SMOE_ERR_CUDA;
     }
@@ -613,7 +616,7 @@ smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
     if (stage < 0 || stage > 2)
         return SMOE_ERR_INVALID_ARG;
     return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
-                          w_out, 1 << stage, SMOE_PATH_STREAM, cuda_stream);
+                          w_out, 1 << stage, SMOE_PATH_AUTO, cuda_stream);
 }
 
 smoe_status smoe_get_device_status(void *cuda_stream)

@@ -31,7 +31,8 @@
 //   16 warps      decoders (warps 7..27 off sub-partition 1; the others
 //                 exit), one code tile each per K block: bf16 weights in the
 //                 128-byte-swizzled K-major layout the MMA reads
-// A stage (3 of them) holds a K block's activations and decoded weights.
+// A stage holds a K block's activations and decoded weights: 3 stages when
+// items pair two m-tiles (two activation tiles each), 4 otherwise.
 // Two accumulators of 256 columns: an item of two m-tiles uses both, an item
 // of one m-tile alternates between them so that its epilogue overlaps the
 // next item's MMAs.  Every wait is bounded; a timeout records
@@ -53,7 +54,7 @@ constexpr int kGM = 128;             // rows per item (MMA M)
 constexpr int kGN = 256;             // output columns per item (MMA N)
 constexpr int kGK = 64;              // K per stage (one quantisation group)
 constexpr int kCodeStages = 3;       // code tiles of one K block each
-constexpr int kStages = 3;           // activations (up to 2 m-tiles) + decoded weights of one K block
+constexpr int kMaxStages = 4;        // activations + decoded weights of one K block each
 constexpr int kDecWarps = 16;
 constexpr int kEpiWarpsG = 4;
 constexpr int kEpiWarp0 = 3;         // warps 0 codes, 1 MMA, 2 activations, 3..6 epilogue
@@ -73,31 +74,38 @@ constexpr int kGThreads = kGWarps * 32;
 constexpr int kTilesPerStage = 16;
 constexpr uint32_t kATileBytes = kGM * kGK * 2;   // 16 KB
 constexpr uint32_t kBTileBytes = kGN * kGK * 2;   // 32 KB
-constexpr uint32_t kAStageBytes = 2 * kATileBytes; // two m-tiles
+// Items of two m-tiles (one decoded weight stage feeds both) take 3 stages
+// with room for two activation tiles; items of one m-tile take 4 stages.
+__host__ __device__ constexpr int num_stages(bool pair) { return pair ? 3 : 4; }
+__host__ __device__ constexpr uint32_t a_stage_bytes(bool pair)
+{
+    return pair ? 2 * kATileBytes : kATileBytes;
+}
 constexpr int kMaxSeg = kMaxExperts + 1;
 
 __host__ __device__ constexpr uint32_t code_stage_bytes(int bits)
 {
     return kTilesPerStage * tile_bytes(bits);
 }
-__host__ __device__ constexpr uint32_t grouped_smem_bytes(int bits)
+__host__ __device__ constexpr uint32_t grouped_smem_bytes(int bits, bool pair)
 {
-    return kStages * (kAStageBytes + kBTileBytes) + kCodeStages * code_stage_bytes(bits) +
+    return num_stages(pair) * (a_stage_bytes(pair) + kBTileBytes) +
+           kCodeStages * code_stage_bytes(bits) +
            1024;  // slack for the manual 1024-byte alignment
 }
 
 struct GSmem {
     uint64_t code_full[kCodeStages];   // code producer: 1 arrival + bytes
     uint64_t code_empty[kCodeStages];  // decoder warps
-    uint64_t a_full[kStages];          // activation producer: 1 arrival + bytes
-    uint64_t b_full[kStages];          // decoder warps
-    uint64_t stage_empty[kStages];     // 1 MMA commit: activations and weights free
+    uint64_t a_full[kMaxStages];       // activation producer: 1 arrival + bytes
+    uint64_t b_full[kMaxStages];       // decoder warps
+    uint64_t stage_empty[kMaxStages];  // 1 MMA commit: activations and weights free
     uint64_t acc_full[2];              // 1 MMA commit
     uint64_t acc_empty[2];             // epilogue warps
     uint64_t drain;                    // final MMA commit
     uint32_t tmem_base;
     uint32_t last_code[kCodeStages];   // 1 + last use filled, per stage (drain
-    uint32_t last_a[kStages];          // after a failure)
+    uint32_t last_a[kMaxStages];       // after a failure)
     int fail;
     int nseg, total_items;
     int ipre[kMaxSeg + 1];             // item prefix per segment
@@ -208,8 +216,15 @@ __device__ __forceinline__ int seg_ntiles(const GroupedArgs &a, int s)
     return PHASE == 0 ? (fsg + 127) / 128 : (a.d + kGN - 1) / kGN;
 }
 
-__device__ __forceinline__ int seg_mpairs(int cnt) { return ((cnt + kGM - 1) / kGM + 1) / 2; }
+// Items of one segment per n-tile: its m-tiles, in pairs when PAIR.
+template <bool PAIR>
+__device__ __forceinline__ int seg_items(int cnt)
+{
+    const int mtc = (cnt + kGM - 1) / kGM;
+    return PAIR ? (mtc + 1) / 2 : mtc;
+}
 
+template <bool PAIR>
 __device__ __forceinline__ Item item_at(const GSmem &sm, int i)
 {
     int lo = 0, hi = sm.nseg - 1;  // last segment with ipre[s] <= i
@@ -225,10 +240,10 @@ __device__ __forceinline__ Item item_at(const GSmem &sm, int i)
     const int local = i - sm.ipre[lo];
     const int c = sm.cnt[lo];
     const int mtc = (c + kGM - 1) / kGM;
-    const int pairs = (mtc + 1) / 2;
-    it.nt = local / pairs;
-    const int mt0 = 2 * (local % pairs);
-    it.nm = mtc - mt0 < 2 ? 1 : 2;
+    const int per = seg_items<PAIR>(c);
+    it.nt = local / per;
+    const int mt0 = (PAIR ? 2 : 1) * (local % per);
+    it.nm = PAIR && mtc - mt0 >= 2 ? 2 : 1;
     it.row0 = sm.off[lo] + kGM * mt0;
     const int left = c - kGM * mt0;
     it.nvalid0 = left < kGM ? left : kGM;
@@ -238,67 +253,80 @@ __device__ __forceinline__ Item item_at(const GSmem &sm, int i)
 
 // ------------------------------------------------------------ roles
 
-// Code tiles of every K block, in item order (warp 0).
+// Where an item's code tiles come from: K block kb, copy c (one strip: the
+// gate and up tiles of the K block for gate/up, the down tile for down).
 template <int BITS, int PHASE>
+struct CodeSrc {
+    const uint8_t *wb;
+    int64_t down_off;
+    int nkb, r0, ncopy, fsg, d;
+    __device__ CodeSrc(const GroupedArgs &a, const Item &w)
+    {
+        const bool routed = w.seg < a.E;
+        fsg = routed ? a.f : a.fs;
+        d = a.d;
+        wb = routed ? a.tiles_routed + (int64_t)w.seg * a.expert_bytes_routed : a.tiles_shared;
+        down_off = routed ? a.down_off_routed : a.down_off_shared;
+        nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
+        r0 = (PHASE == 0 ? 128 * w.nt : kGN * w.nt) / 16;  // first strip
+        const int nstrips = PHASE == 0 ? fsg / 16 : a.d / 16;
+        const int nc = PHASE == 0 ? 8 : 16;
+        ncopy = nstrips - r0 < nc ? nstrips - r0 : nc;
+    }
+    static constexpr uint32_t csize = PHASE == 0 ? 2 * tile_bytes(BITS) : tile_bytes(BITS);
+    __device__ const uint8_t *chunk(int kb, int c) const
+    {
+        constexpr uint32_t TB = tile_bytes(BITS);
+        const int r = r0 + c;
+        return PHASE == 0 ? wb + (((int64_t)r * (d / kGK) + kb) * 2) * TB
+                          : wb + down_off + ((int64_t)r * (fsg / kGK) + kb) * TB;
+    }
+};
+
+// Code tiles of every K block, in item order (warp 0).
+template <int BITS, int PHASE, bool PAIR>
 __device__ void code_producer(const GroupedArgs &a, GSmem &sm, uint8_t *sC)
 {
     const int lane = threadIdx.x & 31;
-    constexpr uint32_t TB = tile_bytes(BITS);
+    typedef CodeSrc<BITS, PHASE> Src;
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
-        const Item w = item_at(sm, i);
-        const bool routed = w.seg < a.E;
-        const int fsg = routed ? a.f : a.fs;
-        const uint8_t *wb = routed ? a.tiles_routed + (int64_t)w.seg * a.expert_bytes_routed
-                                   : a.tiles_shared;
-        const int64_t down_off = routed ? a.down_off_routed : a.down_off_shared;
-        const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
-        const int r0 = (PHASE == 0 ? 128 * w.nt : kGN * w.nt) / 16;  // first strip
-        const int nstrips = PHASE == 0 ? fsg / 16 : a.d / 16;
-        const int ncopy = PHASE == 0 ? 8 : 16;
-        const uint32_t csize = PHASE == 0 ? 2 * TB : TB;
-        int nvalid_copy = nstrips - r0;
-        nvalid_copy = nvalid_copy < ncopy ? nvalid_copy : ncopy;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const Src cs(a, item_at<PAIR>(sm, i));
+        for (int kb = 0; kb < cs.nkb; ++kb, ++it) {
             const int s = static_cast<int>(it % kCodeStages);
             const unsigned par = ((it / kCodeStages) & 1u) ^ 1u;
             if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_empty[s], par, a.status)))
                 return;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&sm.code_full[s], nvalid_copy * csize);
+                mbar_arrive_expect_tx(&sm.code_full[s], cs.ncopy * Src::csize);
                 sm.last_code[s] = it + 1;
             }
             __syncwarp();
-            if (lane < nvalid_copy) {
-                const int r = r0 + lane;
-                const uint8_t *src =
-                    PHASE == 0 ? wb + (((int64_t)r * (a.d / kGK) + kb) * 2) * TB
-                               : wb + down_off + ((int64_t)r * (fsg / kGK) + kb) * TB;
-                bulk_g2s(sC + s * code_stage_bytes(BITS) + lane * csize, src, csize,
-                         &sm.code_full[s]);
-            }
+            if (lane < cs.ncopy)
+                bulk_g2s(sC + s * code_stage_bytes(BITS) + lane * Src::csize, cs.chunk(kb, lane),
+                         Src::csize, &sm.code_full[s]);
         }
     }
 }
 
 // Activation tiles: for every K block, one 128 x 64 tile per m-tile of the
 // item, into the K block's stage (warp 2, lane 0).
-template <int PHASE>
+template <int PHASE, bool PAIR>
 __device__ void act_producer(const GroupedArgs &a, const CUtensorMap *amap, GSmem &sm, uint8_t *sA)
 {
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
-        const Item w = item_at(sm, i);
+        const Item w = item_at<PAIR>(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
         const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = static_cast<int>(it % kStages);
-            if (!gwait(sm, &sm.stage_empty[s], ((it / kStages) & 1u) ^ 1u, a.status))
+            const int s = static_cast<int>(it % num_stages(PAIR));
+            if (!gwait(sm, &sm.stage_empty[s], ((it / num_stages(PAIR)) & 1u) ^ 1u, a.status))
                 return;
             mbar_arrive_expect_tx(&sm.a_full[s], w.nm * kATileBytes);
             sm.last_a[s] = it + 1;
             for (int j = 0; j < w.nm; ++j)
-                tma_load_2d(sA + s * kAStageBytes + j * kATileBytes, amap, kb * kGK,
+                tma_load_2d(sA + s * a_stage_bytes(PAIR) + j * kATileBytes, amap, kb * kGK,
                             w.row0 + kGM * j, &sm.a_full[s]);
         }
     }
@@ -391,7 +419,7 @@ __device__ __forceinline__ void decode_tile(uint32_t tile, uint32_t sb, const ui
                    v[rh][4 * h + 3]);
 }
 
-template <int BITS, int PHASE>
+template <int BITS, int PHASE, bool PAIR>
 __device__ void decoders(const GroupedArgs &a, GSmem &sm, uint8_t *sB, const uint8_t *sC, int dw)
 {
     const int lane = threadIdx.x & 31;
@@ -406,17 +434,17 @@ __device__ void decoders(const GroupedArgs &a, GSmem &sm, uint8_t *sB, const uin
     const uint32_t sB0 = smem_u32(sB), sC0 = smem_u32(sC);
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
-        const Item w = item_at(sm, i);
+        const Item w = item_at<PAIR>(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
         const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
         const int r0 = (PHASE == 0 ? 128 * w.nt : kGN * w.nt) / 16;
         const int nstrips = PHASE == 0 ? fsg / 16 : a.d / 16;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
             const int s = static_cast<int>(it % kCodeStages);
-            const int b = static_cast<int>(it % kStages);
+            const int b = static_cast<int>(it % num_stages(PAIR));
             if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_full[s], (it / kCodeStages) & 1u, a.status)))
                 return;
-            if (!__all_sync(0xffffffffu, gwait(sm, &sm.stage_empty[b], ((it / kStages) & 1u) ^ 1u, a.status)))
+            if (!__all_sync(0xffffffffu, gwait(sm, &sm.stage_empty[b], ((it / num_stages(PAIR)) & 1u) ^ 1u, a.status)))
                 return;
             const uint32_t cs = sC0 + s * code_stage_bytes(BITS);
             const uint32_t bs = sB0 + b * kBTileBytes;
@@ -468,7 +496,7 @@ struct SlotState {
     }
 };
 
-template <int PHASE>
+template <int PHASE, bool PAIR>
 __device__ void mma_issuer(const GroupedArgs &a, GSmem &sm, const uint8_t *sA, const uint8_t *sB)
 {
     uint32_t it = 0;
@@ -477,7 +505,7 @@ __device__ void mma_issuer(const GroupedArgs &a, GSmem &sm, const uint8_t *sA, c
     const uint32_t tbase = sm.tmem_base;
     const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
-        const Item w = item_at(sm, i);
+        const Item w = item_at<PAIR>(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
         const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
         const int slot0 = st.slot(w, 0), slot1 = st.slot(w, 1);
@@ -488,8 +516,8 @@ __device__ void mma_issuer(const GroupedArgs &a, GSmem &sm, const uint8_t *sA, c
         const uint32_t d0 = tbase + static_cast<uint32_t>(slot0 * kGN);
         const uint32_t d1 = tbase + static_cast<uint32_t>(slot1 * kGN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = static_cast<int>(it % kStages);
-            const unsigned par = (it / kStages) & 1u;
+            const int s = static_cast<int>(it % num_stages(PAIR));
+            const unsigned par = (it / num_stages(PAIR)) & 1u;
             if (!gwait(sm, &sm.b_full[s], par, a.status))
                 return;
             if (!gwait(sm, &sm.a_full[s], par, a.status))
@@ -497,7 +525,7 @@ __device__ void mma_issuer(const GroupedArgs &a, GSmem &sm, const uint8_t *sA, c
             tc_fence_after();
             // descriptor start addresses are in 16-byte units: one K step of
             // 16 bf16 is +2, one stage +size/16
-            const uint64_t ad = adesc0 + (uint64_t)(s * (kAStageBytes >> 4));
+            const uint64_t ad = adesc0 + (uint64_t)(s * (a_stage_bytes(PAIR) >> 4));
             const uint64_t bd = bdesc0 + (uint64_t)(s * (kBTileBytes >> 4));
 #pragma unroll
             for (int ks = 0; ks < kGK / 16; ++ks)
@@ -523,7 +551,7 @@ __device__ __forceinline__ float silu_mul(float g, float u)
     return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;
 }
 
-template <int PHASE>
+template <int PHASE, bool PAIR>
 __device__ void epilogue(const GroupedArgs &a, GSmem &sm)
 {
     const int lane = threadIdx.x & 31;
@@ -533,7 +561,7 @@ __device__ void epilogue(const GroupedArgs &a, GSmem &sm)
     SlotState st;
     st.init();
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
-        const Item w = item_at(sm, i);
+        const Item w = item_at<PAIR>(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
         for (int j = 0; j < w.nm; ++j) {
             const int sl = st.slot(w, j);
@@ -587,16 +615,17 @@ __device__ void epilogue(const GroupedArgs &a, GSmem &sm)
     }
 }
 
-template <int BITS, int PHASE>
+template <int BITS, int PHASE, bool PAIR>
 __global__ void __launch_bounds__(kGThreads, 1)
     grouped_gemm_kernel(const GroupedArgs a, const __grid_constant__ CUtensorMap amap)
 {
     extern __shared__ uint8_t g_smem_raw[];
     __shared__ GSmem sm;
     uint8_t *base = g_smem_raw + ((1024u - (smem_u32(g_smem_raw) & 1023u)) & 1023u);
-    uint8_t *sA = base;                                   // kStages x 2 x 16 KB
-    uint8_t *sB = sA + kStages * kAStageBytes;             // kStages x 32 KB
-    uint8_t *sC = sB + kStages * kBTileBytes;              // kCodeStages code stages
+    constexpr int NS = num_stages(PAIR);
+    uint8_t *sA = base;                                // NS activation stages
+    uint8_t *sB = sA + NS * a_stage_bytes(PAIR);        // NS x 32 KB decoded weights
+    uint8_t *sC = sB + NS * kBTileBytes;                // kCodeStages code stages
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // segment table -> item prefix (one warp; at most 257 segments)
@@ -616,7 +645,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 }
                 sm.cnt[s] = c;
                 sm.off[s] = o;
-                items = seg_mpairs(c) * seg_ntiles<PHASE>(a, s);
+                items = seg_items<PAIR>(c) * seg_ntiles<PHASE>(a, s);
             }
             int incl = items;
 #pragma unroll
@@ -639,7 +668,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 mbar_init(&sm.code_full[s], 1);
                 mbar_init(&sm.code_empty[s], kDecWarps);
             }
-            for (int s = 0; s < kStages; ++s) {
+            for (int s = 0; s < num_stages(PAIR); ++s) {
                 sm.last_a[s] = 0;
                 mbar_init(&sm.a_full[s], 1);
                 mbar_init(&sm.b_full[s], kDecWarps);
@@ -668,14 +697,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc_fence_after();
 
     if (warp == 0) {
-        code_producer<BITS, PHASE>(a, sm, sC);
+        code_producer<BITS, PHASE, PAIR>(a, sm, sC);
     } else if (warp == 2) {
         if (lane == 0)
-            act_producer<PHASE>(a, &amap, sm, sA);
+            act_producer<PHASE, PAIR>(a, &amap, sm, sA);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            mma_issuer<PHASE>(a, sm, sA, sB);
+            mma_issuer<PHASE, PAIR>(a, sm, sA, sB);
             // every MMA issued so far has completed once this commit lands
             umma_commit(&sm.drain);
             if (!mbar_wait_bounded(&sm.drain, 0)) {
@@ -685,9 +714,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else if (warp < kEpiWarp0 + kEpiWarpsG) {
-        epilogue<PHASE>(a, sm);
+        epilogue<PHASE, PAIR>(a, sm);
     } else if (decoder_index(warp) >= 0) {
-        decoders<BITS, PHASE>(a, sm, sB, sC, decoder_index(warp));
+        decoders<BITS, PHASE, PAIR>(a, sm, sB, sC, decoder_index(warp));
     }
     __syncwarp();
     // After a failure the consumers may have left copies unwaited: the
@@ -699,9 +728,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
             if (last > 0 && !mbar_wait_bounded(&sm.code_full[lane], ((last - 1) / kCodeStages) & 1u))
                 set_status(a.status, kStatusTimeout);
         }
-        if (warp == 2 && lane < kStages) {
+        if (warp == 2 && lane < num_stages(PAIR)) {
             const uint32_t last = sm.last_a[lane];
-            if (last > 0 && !mbar_wait_bounded(&sm.a_full[lane], ((last - 1) / kStages) & 1u))
+            if (last > 0 && !mbar_wait_bounded(&sm.a_full[lane], ((last - 1) / num_stages(PAIR)) & 1u))
                 set_status(a.status, kStatusTimeout);
         }
     }
@@ -1054,7 +1083,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int b
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BITS, int PHASE>
+template <int BITS, int PHASE, bool PAIR>
 cudaError_t launch_gemm_t(const GroupedArgs &a, const CUtensorMap &map, cudaStream_t s)
 {
     static std::mutex mu;
@@ -1064,16 +1093,16 @@ cudaError_t launch_gemm_t(const GroupedArgs &a, const CUtensorMap &map, cudaStre
     {
         std::lock_guard<std::mutex> lk(mu);
         if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<BITS, PHASE>,
+            cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<BITS, PHASE, PAIR>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 grouped_smem_bytes(BITS));
+                                                 grouped_smem_bytes(BITS, PAIR));
             if (e != cudaSuccess)
                 return e;
             attr_set[dev] = true;
         }
     }
-    grouped_gemm_kernel<BITS, PHASE>
-        <<<device_sm_count(), kGThreads, grouped_smem_bytes(BITS), s>>>(a, map);
+    grouped_gemm_kernel<BITS, PHASE, PAIR>
+        <<<device_sm_count(), kGThreads, grouped_smem_bytes(BITS, PAIR), s>>>(a, map);
     return cudaGetLastError();
 }
 
@@ -1124,31 +1153,48 @@ int64_t grouped_max_rows(int64_t T, int E, int k, int has_shared)
 }
 
 cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, const float *w,
-                           const float *sw, float *y, cudaStream_t s)
+                           const float *sw, float *y, int stage_mask, cudaStream_t s)
 {
     if (a.T == 0)
         return cudaSuccess;
-    CUtensorMap mx, mh;
-    if (!make_map(&mx, a.xs, a.rows, a.d) || !make_map(&mh, a.h, a.rows, a.hstride))
-        return cudaErrorInvalidValue;
     const unsigned nt = static_cast<unsigned>(a.T);
-    grp_scan_kernel<<<a.E, 256, 0, s>>>(a);
-    if (x_bf16)
-        gather_kernel<true><<<nt, 256, 0, s>>>(a, x);
-    else
-        gather_kernel<false><<<nt, 256, 0, s>>>(a, x);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return e;
-    e = a.bits == 4 ? launch_gemm_t<4, 0>(a, mx, s) : launch_gemm_t<2, 0>(a, mx, s);
-    if (e != cudaSuccess)
-        return e;
-    e = a.bits == 4 ? launch_gemm_t<4, 1>(a, mh, s) : launch_gemm_t<2, 1>(a, mh, s);
-    if (e != cudaSuccess)
-        return e;
-    grouped_combine_kernel<<<nt, 256, 0, s>>>(a.o, a.T, a.d, a.k, a.has_shared, a.rows_of, a.rows, w,
-                                              sw, y);
-    return cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+    if (stage_mask & 1) {  // sort and gather
+        grp_scan_kernel<<<a.E, 256, 0, s>>>(a);
+        if (x_bf16)
+            gather_kernel<true><<<nt, 256, 0, s>>>(a, x);
+        else
+            gather_kernel<false><<<nt, 256, 0, s>>>(a, x);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
+    if (stage_mask & 2) {  // gate/up GEMM + SiLU(g) * u
+        CUtensorMap mx;
+        if (!make_map(&mx, a.xs, a.rows, a.d))
+            return cudaErrorInvalidValue;
+        // pairs of m-tiles once the experts average two or more
+        const bool pair = a.T * a.k >= 2ll * kGM * a.E;
+        if ((e = a.bits == 4 ? (pair ? launch_gemm_t<4, 0, true>(a, mx, s)
+                                     : launch_gemm_t<4, 0, false>(a, mx, s))
+                             : (pair ? launch_gemm_t<2, 0, true>(a, mx, s)
+                                     : launch_gemm_t<2, 0, false>(a, mx, s))) != cudaSuccess)
+            return e;
+    }
+    if (stage_mask & 4) {  // down GEMM + combine
+        CUtensorMap mh;
+        if (!make_map(&mh, a.h, a.rows, a.hstride))
+            return cudaErrorInvalidValue;
+        const bool pair = a.T * a.k >= 2ll * kGM * a.E;
+        if ((e = a.bits == 4 ? (pair ? launch_gemm_t<4, 1, true>(a, mh, s)
+                                     : launch_gemm_t<4, 1, false>(a, mh, s))
+                             : (pair ? launch_gemm_t<2, 1, true>(a, mh, s)
+                                     : launch_gemm_t<2, 1, false>(a, mh, s))) != cudaSuccess)
+            return e;
+        grouped_combine_kernel<<<nt, 256, 0, s>>>(a.o, a.T, a.d, a.k, a.has_shared, a.rows_of,
+                                                  a.rows, w, sw, y);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace smoe

@@ -157,8 +157,9 @@ int64_t grouped_max_rows(int64_t T, int E, int k, int has_shared);
 // logits[T][Epad] = x Wr^T on the tensor cores (bf16 x, 16-byte aligned rows).
 cudaError_t launch_tc_logits(const uint16_t *x, const uint16_t *router_w, int64_t T, int d, int E,
                              int Epad, float *logits, int *status, cudaStream_t stream);
+// stage_mask: 1 sort + gather, 2 gate/up GEMM, 4 down GEMM + combine.
 cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, const float *w,
-                           const float *sw, float *y, cudaStream_t stream);
+                           const float *sw, float *y, int stage_mask, cudaStream_t stream);
 
 int layer_grid_ctas_max();
 cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream);

@@ -230,12 +230,19 @@ smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, s
 int smoe_moe_path(const smoe_layer_desc *layer, int64_t num_tokens);
 
 /* The same forward as smoe_moe_forward, one launch stage at a time, so that
- * a caller can put its own work or timing events between the stages:
- *   stage 0  router GEMV, softmax, top-k, renormalisation, dispatch
- *   stage 1  fused dequant gate/up GEMV + SiLU(gate) * up
- *   stage 2  fused dequant down GEMV + routing-weighted combine into y
+ * a caller can put its own work or timing events between the stages.  The
+ * stages follow the path smoe_moe_forward takes (smoe_moe_path):
+ *   streaming path
+ *     stage 0  router GEMV, softmax, top-k, renormalisation, dispatch
+ *     stage 1  fused dequant gate/up GEMV + SiLU(gate) * up
+ *     stage 2  fused dequant down GEMV + routing-weighted combine into y
+ *   grouped path
+ *     stage 0  router logits, softmax, top-k, renormalisation, sort of the
+ *              selections by expert, gather of the tokens as bf16 rows
+ *     stage 1  gate/up grouped GEMM (tensor cores) + SiLU(gate) * up
+ *     stage 2  down grouped GEMM (tensor cores) + routing-weighted combine
  * Calling stages 0, 1, 2 in order on one stream with the same arguments and
- * workspace is exactly smoe_moe_forward on the streaming path.  Same arguments and errors, plus
+ * workspace is exactly smoe_moe_forward.  Same arguments and errors, plus
  * SMOE_ERR_INVALID_ARG for a stage outside 0..2. */
 smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
                                    smoe_dtype x_dtype, int64_t num_tokens, float *y,

@@ -77,7 +77,10 @@ def run(S, lay, wl, x_host, path):
 @pytest.mark.parametrize("name,T", [("tiny_f32", 16), ("tiny_f32", 200), ("tiny_f32", 700),
                                     ("half_ntile_bf16", 64), ("half_ntile_bf16", 333),
                                     ("wide_bf16", 257), ("shared_bf16", 40),
-                                    ("shared_bf16", 300), ("shared_nogate_f32", 150)])
+                                    ("shared_bf16", 300), ("shared_nogate_f32", 150),
+                                    # >= 256 rows per expert on average: items pair two
+                                    # m-tiles in the gate/up GEMM
+                                    ("tiny_f32", 1100), ("half_ntile_bf16", 1030)])
 def test_grouped_matches_oracle(S, name, T, bits):
     wl, hl = host_layer(name, bits)
     lay = hl.device_layer(DEV)
