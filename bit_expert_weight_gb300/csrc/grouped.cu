@@ -53,7 +53,16 @@ namespace {
 constexpr int kGM = 128;             // rows per item (MMA M)
 constexpr int kGN = 256;             // output columns per item (MMA N)
 constexpr int kGK = 64;              // K per stage (one quantisation group)
-constexpr int kCodeStages = 3;       // code tiles of one K block each
+constexpr int kMaxCodeStages = 3;
+// Code stages: one bulk copy moves a strip's tiles of code_kb consecutive K
+// blocks.  A bulk copy has a fixed cost: copies of one K block's tiles
+// (1088 B for a gate/up strip at Q4) cap the weight stream near 2 TB/s on
+// this part, copies of 4 K blocks reach about 7 TB/s.  Items of one m-tile
+// stream each weight tile once per m-tile and take 2 stages of 4 K blocks;
+// items of two m-tiles need 3 activation stages and keep 3 code stages of
+// one K block (what the shared memory leaves).
+__host__ __device__ constexpr int code_kb(bool pair) { return pair ? 1 : 4; }
+__host__ __device__ constexpr int code_stages(bool pair) { return pair ? 3 : 2; }
 constexpr int kMaxStages = 4;        // activations + decoded weights of one K block each
 constexpr int kDecWarps = 16;
 constexpr int kEpiWarpsG = 4;
@@ -76,27 +85,27 @@ constexpr uint32_t kATileBytes = kGM * kGK * 2;   // 16 KB
 constexpr uint32_t kBTileBytes = kGN * kGK * 2;   // 32 KB
 // Items of two m-tiles (one decoded weight stage feeds both) take 3 stages
 // with room for two activation tiles; items of one m-tile take 4 stages.
-__host__ __device__ constexpr int num_stages(bool pair) { return pair ? 3 : 4; }
+__host__ __device__ constexpr int num_stages(bool pair) { return 3; }
 __host__ __device__ constexpr uint32_t a_stage_bytes(bool pair)
 {
     return pair ? 2 * kATileBytes : kATileBytes;
 }
 constexpr int kMaxSeg = kMaxExperts + 1;
 
-__host__ __device__ constexpr uint32_t code_stage_bytes(int bits)
+__host__ __device__ constexpr uint32_t code_stage_bytes(int bits, bool pair)
 {
-    return kTilesPerStage * tile_bytes(bits);
+    return code_kb(pair) * kTilesPerStage * tile_bytes(bits);
 }
 __host__ __device__ constexpr uint32_t grouped_smem_bytes(int bits, bool pair)
 {
     return num_stages(pair) * (a_stage_bytes(pair) + kBTileBytes) +
-           kCodeStages * code_stage_bytes(bits) +
+           code_stages(pair) * code_stage_bytes(bits, pair) +
            1024;  // slack for the manual 1024-byte alignment
 }
 
 struct GSmem {
-    uint64_t code_full[kCodeStages];   // code producer: 1 arrival + bytes
-    uint64_t code_empty[kCodeStages];  // decoder warps
+    uint64_t code_full[kMaxCodeStages];   // code producer: 1 arrival + bytes
+    uint64_t code_empty[kMaxCodeStages];  // decoder warps
     uint64_t a_full[kMaxStages];       // activation producer: 1 arrival + bytes
     uint64_t b_full[kMaxStages];       // decoder warps
     uint64_t stage_empty[kMaxStages];  // 1 MMA commit: activations and weights free
@@ -104,7 +113,7 @@ struct GSmem {
     uint64_t acc_empty[2];             // epilogue warps
     uint64_t drain;                    // final MMA commit
     uint32_t tmem_base;
-    uint32_t last_code[kCodeStages];   // 1 + last use filled, per stage (drain
+    uint32_t last_code[kMaxCodeStages];   // 1 + last use filled, per stage (drain
     uint32_t last_a[kMaxStages];       // after a failure)
     int fail;
     int nseg, total_items;
@@ -292,19 +301,21 @@ __device__ void code_producer(const GroupedArgs &a, GSmem &sm, uint8_t *sC)
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
         const Src cs(a, item_at<PAIR>(sm, i));
-        for (int kb = 0; kb < cs.nkb; ++kb, ++it) {
-            const int s = static_cast<int>(it % kCodeStages);
-            const unsigned par = ((it / kCodeStages) & 1u) ^ 1u;
+        for (int kb0 = 0; kb0 < cs.nkb; kb0 += code_kb(PAIR), ++it) {
+            const int nb = cs.nkb - kb0 < code_kb(PAIR) ? cs.nkb - kb0 : code_kb(PAIR);
+            const int s = static_cast<int>(it % code_stages(PAIR));
+            const unsigned par = ((it / code_stages(PAIR)) & 1u) ^ 1u;
             if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_empty[s], par, a.status)))
                 return;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&sm.code_full[s], cs.ncopy * Src::csize);
+                mbar_arrive_expect_tx(&sm.code_full[s], cs.ncopy * nb * Src::csize);
                 sm.last_code[s] = it + 1;
             }
             __syncwarp();
+            // copy c: the strip's tiles of K blocks kb0 .. kb0 + nb - 1 (contiguous)
             if (lane < cs.ncopy)
-                bulk_g2s(sC + s * code_stage_bytes(BITS) + lane * Src::csize, cs.chunk(kb, lane),
-                         Src::csize, &sm.code_full[s]);
+                bulk_g2s(sC + s * code_stage_bytes(BITS, PAIR) + lane * code_kb(PAIR) * Src::csize,
+                         cs.chunk(kb0, lane), nb * Src::csize, &sm.code_full[s]);
         }
     }
 }
@@ -432,37 +443,40 @@ __device__ void decoders(const GroupedArgs &a, GSmem &sm, uint8_t *sB, const uin
         for (int h = 0; h < 2; ++h)
             off[rh][h] = (gq + 8 * rh) * 128 + ((((2 * tig + h) ^ gq) & 7) << 4);
     const uint32_t sB0 = smem_u32(sB), sC0 = smem_u32(sC);
-    uint32_t it = 0;
+    uint32_t it = 0, ic = 0;  // K blocks, code stages
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
         const Item w = item_at<PAIR>(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
         const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
         const int r0 = (PHASE == 0 ? 128 * w.nt : kGN * w.nt) / 16;
         const int nstrips = PHASE == 0 ? fsg / 16 : a.d / 16;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const int s = static_cast<int>(it % kCodeStages);
-            const int b = static_cast<int>(it % num_stages(PAIR));
-            if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_full[s], (it / kCodeStages) & 1u, a.status)))
+        // this warp's tile: gate/up copy q/2 holds strip r0 + q/2 (gate tile
+        // then up tile per K block), down copy q holds strip r0 + q
+        const int q = dw;
+        const int strip = PHASE == 0 ? q >> 1 : q;
+        const int rowbase = PHASE == 0 ? (q & 1) * 128 + 16 * (q >> 1) : 16 * q;
+        constexpr uint32_t csize = PHASE == 0 ? 2 * TB : TB;
+        const uint32_t tile_off = strip * code_kb(PAIR) * csize + (PHASE == 0 ? (q & 1) * TB : 0);
+        for (int kb0 = 0; kb0 < nkb; kb0 += code_kb(PAIR), ++ic) {
+            const int nb = nkb - kb0 < code_kb(PAIR) ? nkb - kb0 : code_kb(PAIR);
+            const int s = static_cast<int>(ic % code_stages(PAIR));
+            if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_full[s], (ic / code_stages(PAIR)) & 1u, a.status)))
                 return;
-            if (!__all_sync(0xffffffffu, gwait(sm, &sm.stage_empty[b], ((it / num_stages(PAIR)) & 1u) ^ 1u, a.status)))
-                return;
-            const uint32_t cs = sC0 + s * code_stage_bytes(BITS);
-            const uint32_t bs = sB0 + b * kBTileBytes;
-#pragma unroll
-            for (int qq = 0; qq < kTilesPerStage / kDecWarps; ++qq) {
-                const int q = dw + kDecWarps * qq;
-                // gate/up: copy q/2 holds strip r0 + q/2, gate tile then up tile
-                const int strip = PHASE == 0 ? q >> 1 : q;
-                const int rowbase = PHASE == 0 ? (q & 1) * 128 + 16 * (q >> 1) : 16 * q;
+            const uint32_t cs = sC0 + s * code_stage_bytes(BITS, PAIR) + tile_off;
+            for (int j = 0; j < nb; ++j, ++it) {
+                const int b = static_cast<int>(it % num_stages(PAIR));
+                if (!__all_sync(0xffffffffu, gwait(sm, &sm.stage_empty[b], ((it / num_stages(PAIR)) & 1u) ^ 1u, a.status)))
+                    return;
                 if (r0 + strip < nstrips)
-                    decode_tile<BITS>(cs + q * TB, bs + rowbase * 128, off, lane);
+                    decode_tile<BITS>(cs + j * csize, sB0 + b * kBTileBytes + rowbase * 128, off, lane);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.b_full[b]);
             }
-            fence_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.b_full[b]);
+            if (lane == 0)
                 mbar_arrive(&sm.code_empty[s]);
-            }
         }
     }
 }
@@ -625,7 +639,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     constexpr int NS = num_stages(PAIR);
     uint8_t *sA = base;                                // NS activation stages
     uint8_t *sB = sA + NS * a_stage_bytes(PAIR);        // NS x 32 KB decoded weights
-    uint8_t *sC = sB + NS * kBTileBytes;                // kCodeStages code stages
+    uint8_t *sC = sB + NS * kBTileBytes;                // code_stages(PAIR) code stages
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // segment table -> item prefix (one warp; at most 257 segments)
@@ -663,7 +677,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             sm.nseg = nseg;
             sm.total_items = run;
             sm.fail = 0;
-            for (int s = 0; s < kCodeStages; ++s) {
+            for (int s = 0; s < code_stages(PAIR); ++s) {
                 sm.last_code[s] = 0;
                 mbar_init(&sm.code_full[s], 1);
                 mbar_init(&sm.code_empty[s], kDecWarps);
@@ -723,9 +737,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // producers wait (bounded) for the last phase they filled on every stage,
     // so no copy is in flight when the CTA exits.
     if (*reinterpret_cast<volatile int *>(&sm.fail)) {
-        if (warp == 0 && lane < kCodeStages) {
+        if (warp == 0 && lane < code_stages(PAIR)) {
             const uint32_t last = sm.last_code[lane];
-            if (last > 0 && !mbar_wait_bounded(&sm.code_full[lane], ((last - 1) / kCodeStages) & 1u))
+            if (last > 0 && !mbar_wait_bounded(&sm.code_full[lane], ((last - 1) / code_stages(PAIR)) & 1u))
                 set_status(a.status, kStatusTimeout);
         }
         if (warp == 2 && lane < num_stages(PAIR)) {
