@@ -122,19 +122,21 @@ class FullLayer:
         S.synth_bf16(x, Y.stream_key(wl.seed, self.layer, 0, Y.ROLE_X), 1.0)
         return x.view(torch.bfloat16).view(T, wl.d)
 
-    def check(self, S, T, tol=None):
+    def check(self, S, T, tol=None, path=None):
         """tol defaults to the bar of the path the forward takes: 1e-3 on the
         streaming path (fp32 accumulation), 2e-2 on the grouped tensor-core
-        path (bf16 operands)."""
+        path (bf16 operands).  path forces a path (smoe_moe_forward_path)."""
         wl = self.wl
+        grouped = (path == S.PATH_GROUPED or
+                   (path in (None, S.PATH_AUTO) and S.path_for(self.lay, T) == S.PATH_GROUPED))
         if tol is None:
-            tol = 2e-2 if S.path_for(self.lay, T) == S.PATH_GROUPED else 1e-3
+            tol = 2e-2 if grouped else 1e-3
         assert max(self.sample) < T
         xt = self.device_x(S, T)
         ws = S.workspace(self.lay, T)
         ids = torch.empty((T, wl.k), dtype=torch.int32, device=DEV)
         w = torch.empty((T, wl.k), dtype=torch.float32, device=DEV)
-        y = S.forward(self.lay, xt, ws, ids=ids, w=w)
+        y = S.forward(self.lay, xt, ws, ids=ids, w=w, path=path)
         torch.cuda.synchronize()
         assert S.device_status() == 0
         # the device x rows are the host generator's rows, bit for bit
@@ -177,6 +179,15 @@ def test_a3b35b_layer_full_size(S, pool, bits):
     fl.check(S, 256)
     fl1 = FullLayer(S, pool, "a3b35b", 1, bits, sample=[0])
     fl1.check(S, 1)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_a3b35b_grouped_path_full_size(S, pool, bits):
+    """The 256-token batch forced onto the grouped path: 256 experts (two
+    128-expert tiles of router logits), the gated shared expert as a
+    segment of all 256 tokens, Q4 and Q2."""
+    fl = FullLayer(S, pool, "a3b35b", 2, bits, sample=[0, 100, 255])
+    fl.check(S, 256, path=S.PATH_GROUPED)
 
 
 def test_qwen235b_batched_zipf_full_size(S, pool):
