@@ -1236,6 +1236,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     }
     for (int j = threadIdx.x; j < kMaxStripsD; j += kThreads)
         s_ccnt[j] = 0u;
+    // Launched with programmatic stream serialization: the previous kernel on
+    // the stream may still be finishing.  Wait until it has completed and its
+    // writes are visible before any global access (the workspace, x), then
+    // let the next kernel's launch begin.
+    pdl_wait();
+    pdl_launch_dependents();
     cta_barrier();
     bool ok = true;
 
@@ -1523,12 +1529,25 @@ cudaError_t launch_t(const LayerArgs &a, cudaStream_t stream)
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    // cooperative (every CTA resident: the phases hand off through global
+    // counters) and, where the runtime accepts it, programmatic stream
+    // serialization so that the launch overlaps the previous kernel's tail
+    static int pdl_refused[64] = {0};
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    cfg.numAttrs = pdl_refused[dev & 63] ? 1 : 2;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess && cfg.numAttrs == 2) {
+        (void)cudaGetLastError();
+        pdl_refused[dev & 63] = 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, a);
+    }
+    return e;
 }
 
 // y[t] = sum_j w[t,j] * o[pair(t,j)] (rank order) + shared_w[t] * o[shared]
