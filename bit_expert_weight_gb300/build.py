@@ -24,7 +24,8 @@ NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "
            "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
 LIBS = {
-    "libsmoe.so": ["api.cu", "quant.cu", "repack.cu", "router.cu", "layer.cu", "grouped.cu", "noalloc.cu"],
+    "libsmoe.so": ["api.cu", "quant.cu", "repack.cu", "router.cu", "layer.cu", "grouped.cu", "noalloc.cu",
+                   "vault.cu"],
     "libsmoe_synth.so": ["synth.cu"],
 }
 

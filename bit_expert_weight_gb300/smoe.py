@@ -32,10 +32,42 @@ EXPORTED = [
     "smoe_route_from_logits", "smoe_moe_workspace_bytes", "smoe_moe_workspace_init",
     "smoe_moe_forward", "smoe_moe_forward_stage", "smoe_get_device_status",
     "smoe_moe_forward_noalloc", "smoe_moe_forward_path", "smoe_moe_path",
+    "smoe_vault_parse", "smoe_vault_find_expert", "smoe_vault_repack_layer",
 ]
 
 # Execution paths (SMOE_PATH_* in include/smoe.h).
 PATH_AUTO, PATH_STREAM, PATH_GROUPED = 0, 1, 2
+
+
+class VaultInfo(ctypes.Structure):
+    """smoe_vault_info (include/smoe.h)."""
+    _fields_ = [("version", ctypes.c_uint32), ("num_moe_layers", ctypes.c_uint32),
+                ("max_experts_per_layer", ctypes.c_uint32), ("total_experts", ctypes.c_uint32),
+                ("table_offset", ctypes.c_uint64), ("data_offset", ctypes.c_uint64),
+                ("group_size", ctypes.c_uint32), ("bits", ctypes.c_uint32),
+                ("d_model", ctypes.c_uint32), ("vocab_size", ctypes.c_uint32),
+                ("ffn_dim", ctypes.c_uint32), ("reserved_ext", ctypes.c_uint32),
+                ("has_arch", ctypes.c_int32), ("arch_flags", ctypes.c_uint32),
+                ("rope_theta", ctypes.c_float), ("num_heads", ctypes.c_uint32),
+                ("num_kv_heads", ctypes.c_uint32), ("head_dim", ctypes.c_uint32),
+                ("moe_top_k", ctypes.c_uint32), ("moe_ffn_dim", ctypes.c_uint32),
+                ("dense_ffn_dim", ctypes.c_uint32), ("shared_expert_ffn_dim", ctypes.c_uint32),
+                ("activation", ctypes.c_uint32), ("num_hidden_layers", ctypes.c_uint32),
+                ("rms_norm_eps", ctypes.c_float), ("model_type", ctypes.c_char * 25)]
+
+
+class VaultTensor(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_uint32), ("cols", ctypes.c_uint32),
+                ("packed_offset", ctypes.c_uint64), ("packed_size", ctypes.c_uint64),
+                ("scales_offset", ctypes.c_uint64), ("scales_size", ctypes.c_uint64)]
+
+
+class VaultExpert(ctypes.Structure):
+    """smoe_vault_expert (include/smoe.h)."""
+    _fields_ = [("layer_id", ctypes.c_uint32), ("expert_id", ctypes.c_uint32),
+                ("byte_offset", ctypes.c_uint64), ("raw_size", ctypes.c_uint64),
+                ("padded_size", ctypes.c_uint64), ("num_groups", ctypes.c_uint64),
+                ("tensor", VaultTensor * 3)]
 
 
 class SmoeError(RuntimeError):
@@ -106,6 +138,15 @@ def load(path: str | None = None):
     L.smoe_moe_forward_path.restype = I
     L.smoe_moe_path.argtypes = [ctypes.POINTER(LayerDesc), I64]
     L.smoe_moe_path.restype = I
+    VP = ctypes.POINTER(VaultInfo)
+    L.smoe_vault_parse.argtypes = [P, S, ctypes.c_uint64, VP]
+    L.smoe_vault_parse.restype = I
+    L.smoe_vault_find_expert.argtypes = [P, S, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                                         ctypes.POINTER(VaultExpert)]
+    L.smoe_vault_find_expert.restype = I
+    L.smoe_vault_repack_layer.argtypes = [P, S, P, ctypes.c_uint64, ctypes.c_uint32,
+                                          ctypes.c_uint32, P, S, P]
+    L.smoe_vault_repack_layer.restype = I
     L.smoe_get_device_status.argtypes = [P]
     L.smoe_get_device_status.restype = I
     _lib = L
@@ -299,6 +340,36 @@ def forward_stage(layer: MoELayer, stage: int, x: torch.Tensor, ws: torch.Tensor
                                          _ptr(y), _ptr(ws), ws.numel(), _ptr(ids), _ptr(w), stage,
                                          _stream(stream)), f"smoe_moe_forward_stage({stage})")
     return y
+
+
+def vault_parse(meta: bytes, file_bytes: int) -> "VaultInfo":
+    """smoe_vault_parse on a host byte string (the file's metadata region)."""
+    info = VaultInfo()
+    buf = ctypes.create_string_buffer(bytes(meta), len(meta))
+    _check(load().smoe_vault_parse(buf, len(meta), file_bytes, ctypes.byref(info)),
+           "smoe_vault_parse")
+    return info
+
+
+def vault_find_expert(meta: bytes, file_bytes: int, layer: int, expert: int) -> "VaultExpert":
+    out = VaultExpert()
+    buf = ctypes.create_string_buffer(bytes(meta), len(meta))
+    _check(load().smoe_vault_find_expert(buf, len(meta), file_bytes, layer, expert,
+                                         ctypes.byref(out)), "smoe_vault_find_expert")
+    return out
+
+
+def vault_repack_layer(meta: bytes, vault_dev: torch.Tensor, layer: int, num_experts: int,
+                       d: int, f: int, bits: int, stream=None) -> torch.Tensor:
+    """smoe_vault_repack_layer: the layer's tile bank from a device copy of
+    the vault (uint8 tensor holding the whole file)."""
+    n = load().smoe_repacked_bytes(d, f, num_experts, bits, 64)
+    tiles = torch.empty(n, dtype=torch.uint8, device=vault_dev.device)
+    buf = ctypes.create_string_buffer(bytes(meta), len(meta))
+    _check(load().smoe_vault_repack_layer(buf, len(meta), _ptr(vault_dev), vault_dev.numel(), layer,
+                                          num_experts, _ptr(tiles), n, _stream(stream)),
+           "smoe_vault_repack_layer")
+    return tiles
 
 
 def device_status(stream=None) -> int:

@@ -155,6 +155,84 @@ smoe_status smoe_unpack(const void *tiles, int32_t d_model, int32_t ffn_dim, int
                         int bits, int group_size, uint8_t *const *codes_lsb,
                         uint16_t *const *scales_f16, void *cuda_stream);
 
+/* ------------------------------------------------------------ .smoe vault */
+
+/* The pages' binary vault (".smoe Binary Format"): a 64-byte file header, an
+ * expert table (48-byte entries, sorted by layer then expert), three 44-byte
+ * tensor descriptors per entry (gate, up, down), in version 2 a 128-byte
+ * arch block "SARC" at header.reserved_ext, then 16 KB-aligned expert blobs
+ * [gate codes][gate fp16 scales][up codes][up scales][down codes][down
+ * scales][padding].  All integers little-endian, all offsets from the start
+ * of the file.  Here the vault is the input of smoe_repack: nothing is
+ * streamed from disk.
+ *
+ * The functions below read the metadata from a HOST buffer `meta` holding at
+ * least the file's first header.data_offset bytes (header, table,
+ * descriptors, arch block); `file_bytes` is the size of the whole file, used
+ * to bound the blob extents.  They validate what the page fixes and refuse
+ * the vault otherwise (SMOE_ERR_INVALID_ARG): magic 53 4D 4F 45 DE EA 00 01,
+ * version 1 or 2, table_offset 64, data_offset 16 KB-aligned and past the
+ * descriptors, group_size 64, bits 2 or 4; for version 2 an arch block with
+ * magic "SARC", block_version 1, block_size 128, activation 0 (SiLU),
+ * moe_top_k <= 16, head_dim <= 256, num_heads divisible by num_kv_heads,
+ * zero reserved bytes; table entries in (layer, expert) order, group_size
+ * 64, zero reserved bytes, 16 KB-aligned blobs inside the file, raw_size <=
+ * padded_size; descriptors typed gate, up, down in order, ndim 2, zero
+ * reserved bytes, packed_size = ceil(rows*cols*bits/8), scales_size =
+ * ceil(rows*cols/64)*2, both inside the blob's raw bytes, num_groups = the
+ * three tensors' groups.  Nothing is allocated; no GPU is used. */
+typedef struct {
+    uint32_t version, num_moe_layers, max_experts_per_layer, total_experts;
+    uint64_t table_offset, data_offset;
+    uint32_t group_size, bits, d_model, vocab_size;
+    uint32_t ffn_dim;        /* header field: dense/shared FFN dimension */
+    uint32_t reserved_ext;   /* v2: byte offset of the arch block */
+    int32_t has_arch;        /* 1 for version 2 */
+    uint32_t arch_flags;     /* bit 0 norm_topk_prob, bit 1 has_qk_norm, bit 2 has_dense_layer_0 */
+    float rope_theta;
+    uint32_t num_heads, num_kv_heads, head_dim, moe_top_k, moe_ffn_dim, dense_ffn_dim,
+        shared_expert_ffn_dim, activation, num_hidden_layers;
+    float rms_norm_eps;
+    char model_type[25];     /* NUL-terminated */
+} smoe_vault_info;
+
+typedef struct {
+    uint32_t rows, cols;
+    uint64_t packed_offset, packed_size, scales_offset, scales_size;  /* within the blob */
+} smoe_vault_tensor;
+
+typedef struct {
+    uint32_t layer_id, expert_id;
+    uint64_t byte_offset, raw_size, padded_size, num_groups;
+    smoe_vault_tensor tensor[3];  /* gate, up, down */
+} smoe_vault_expert;
+
+/* Parse and validate the vault metadata; fills *info.  Errors:
+ * SMOE_ERR_INVALID_ARG (null pointer, short buffer, any rule above). */
+smoe_status smoe_vault_parse(const void *meta, size_t meta_bytes, uint64_t file_bytes,
+                             smoe_vault_info *info);
+
+/* Locate expert (layer, expert) through the table and its descriptors.
+ * SMOE_ERR_INVALID_ARG also when the vault has no such entry. */
+smoe_status smoe_vault_find_expert(const void *meta, size_t meta_bytes, uint64_t file_bytes,
+                                   uint32_t layer, uint32_t expert, smoe_vault_expert *out);
+
+/* smoe_repack of one MoE layer straight from a vault: experts 0 ..
+ * num_experts - 1 of `layer`, each found through the table and its
+ * descriptors (never a fixed stride), their codes and scales read from
+ * `vault_dev`, a DEVICE copy of the whole file (file_bytes bytes, 16-byte
+ * aligned).  d_model is the header's; the expert ffn_dim is the descriptors'
+ * gate rows, which must be equal for every expert of the layer (and equal
+ * the arch block's moe_ffn_dim in version 2).  Writes the same tiles as
+ * smoe_repack with the same streams, into tiles_out (device,
+ * smoe_repacked_bytes(d, f, num_experts, bits, 64) bytes).  Errors:
+ * SMOE_ERR_INVALID_ARG (vault rules, missing expert, mismatched shapes, a
+ * stream not aligned for the repack kernel), SMOE_ERR_WORKSPACE (tiles_bytes
+ * too small), SMOE_ERR_UNSUPPORTED (device), SMOE_ERR_CUDA. */
+smoe_status smoe_vault_repack_layer(const void *meta, size_t meta_bytes, const void *vault_dev,
+                                    uint64_t file_bytes, uint32_t layer, uint32_t num_experts,
+                                    void *tiles_out, size_t tiles_bytes, void *cuda_stream);
+
 /* ---------------------------------------------------------------- route */
 
 /* Top-k routing from given fp32 logits ("CMF v2", 2.2 MoE).
