@@ -307,15 +307,22 @@ void oracle_router_logits(const uint16_t *wr_bf16, const float *x, int64_t T, in
         }
 }
 
-/* "CMF v2", 2.2 MoE: softmax over all E logits; top-k chosen by the key
- * (logit + expert_bias in fp32 when a bias is given, else the logit), larger
- * key first, ties to the lower expert index; the bias never enters the
- * weights; with norm_topk_prob the k weights are divided by their sum.
- * Slots are written in rank order.  Returns 0, or -1 on bad arguments. */
-int oracle_route(const float *logits, int64_t T, int32_t E, int32_t k, int32_t norm,
-                 const float *bias, int32_t *ids, float *weights)
+/* "CMF v2", 2.2 MoE: scores are the softmax over all E logits, or with
+ * router_sigmoid each expert's sigmoid(logit) on its own (double, the
+ * selection key rounded to fp32); top-k chosen by the key, larger first,
+ * ties to the lower expert index.  Key: the logit when no bias is given
+ * (selecting on it selects on either score, both being increasing in the
+ * logit); with an expert_bias, logit + bias for softmax scores, fl32(score) +
+ * bias for sigmoid scores, each addition in fp32.  The bias never enters the
+ * weights.  The selected scores are divided by their sum with norm_topk_prob,
+ * then multiplied by routed_scaling_factor.  Slots are written in rank order.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_route_ex(const float *logits, int64_t T, int32_t E, int32_t k, int32_t norm,
+                    const float *bias, int32_t router_sigmoid, float routed_scaling_factor,
+                    int32_t *ids, float *weights)
 {
-    if (E <= 0 || k < 1 || k > 16 || k > E)
+    if (E <= 0 || k < 1 || k > 16 || k > E || !(routed_scaling_factor > 0.0f) ||
+        routed_scaling_factor > 3.0e38f)
         return -1;
     float *key = (float *)malloc(sizeof(float) * (size_t)E);
     uint8_t *taken = (uint8_t *)malloc((size_t)E);
@@ -328,21 +335,31 @@ int oracle_route(const float *logits, int64_t T, int32_t E, int32_t k, int32_t n
     }
     for (int64_t t = 0; t < T; ++t) {
         const float *l = logits + t * E;
+        if (router_sigmoid) {
+            for (int32_t e = 0; e < E; ++e)
+                p[e] = 1.0 / (1.0 + exp(-(double)l[e]));
+        } else {
+            double m = -INFINITY;
+            for (int32_t e = 0; e < E; ++e)
+                if ((double)l[e] > m)
+                    m = (double)l[e];
+            double z = 0.0;
+            for (int32_t e = 0; e < E; ++e) {
+                p[e] = exp((double)l[e] - m);
+                z += p[e];
+            }
+            for (int32_t e = 0; e < E; ++e)
+                p[e] /= z;
+        }
         for (int32_t e = 0; e < E; ++e) {
-            key[e] = bias ? l[e] + bias[e] : l[e];
+            if (!bias)
+                key[e] = l[e];
+            else if (router_sigmoid)
+                key[e] = (float)p[e] + bias[e];
+            else
+                key[e] = l[e] + bias[e];
             taken[e] = 0;
         }
-        double m = -INFINITY;
-        for (int32_t e = 0; e < E; ++e)
-            if ((double)l[e] > m)
-                m = (double)l[e];
-        double z = 0.0;
-        for (int32_t e = 0; e < E; ++e) {
-            p[e] = exp((double)l[e] - m);
-            z += p[e];
-        }
-        for (int32_t e = 0; e < E; ++e)
-            p[e] /= z;
         double sel = 0.0;
         for (int32_t j = 0; j < k; ++j) {
             int32_t best = -1;
@@ -358,13 +375,19 @@ int oracle_route(const float *logits, int64_t T, int32_t E, int32_t k, int32_t n
         }
         for (int32_t j = 0; j < k; ++j) {
             double pj = p[ids[t * k + j]];
-            weights[t * k + j] = (float)(norm ? pj / sel : pj);
+            weights[t * k + j] = (float)((norm ? pj / sel : pj) * (double)routed_scaling_factor);
         }
     }
     free(key);
     free(taken);
     free(p);
     return 0;
+}
+
+int oracle_route(const float *logits, int64_t T, int32_t E, int32_t k, int32_t norm,
+                 const float *bias, int32_t *ids, float *weights)
+{
+    return oracle_route_ex(logits, T, E, k, norm, bias, 0, 1.0f, ids, weights);
 }
 
 /* --------------------------------------------------- expert FFN (a5-a6) */
@@ -501,11 +524,12 @@ done:
  * then oracle_moe_apply.  x is [T, d] fp32 (bf16 activations are widened
  * exactly by the caller); router_w is bf16 [E, d].  Optionally writes the
  * routing (ids/weights [T, k]) and the logits [T, E]. */
-int oracle_moe_forward(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm, int bits,
-                       const uint16_t *router_w, const float *expert_bias,
-                       const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
-                       const uint16_t *shared_gate, const float *x, int64_t T, float *y,
-                       int32_t *ids_out, float *w_out, float *logits_out)
+int oracle_moe_forward_ex(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm, int bits,
+                          const uint16_t *router_w, const float *expert_bias,
+                          int32_t router_sigmoid, float routed_scaling_factor,
+                          const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
+                          const uint16_t *shared_gate, const float *x, int64_t T, float *y,
+                          int32_t *ids_out, float *w_out, float *logits_out)
 {
     if (d <= 0 || f <= 0 || E <= 0 || k < 1 || k > 16 || k > E || (bits != 2 && bits != 4))
         return -1;
@@ -518,7 +542,8 @@ int oracle_moe_forward(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm,
         goto done;
     }
     oracle_router_logits(router_w, x, T, E, d, logits);
-    if (oracle_route(logits, T, E, k, norm, expert_bias, ids, wts)) {
+    if (oracle_route_ex(logits, T, E, k, norm, expert_bias, router_sigmoid, routed_scaling_factor,
+                        ids, wts)) {
         rc = -1;
         goto done;
     }
@@ -536,4 +561,15 @@ done:
     free(ids);
     free(wts);
     return rc;
+}
+
+int oracle_moe_forward(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm, int bits,
+                       const uint16_t *router_w, const float *expert_bias,
+                       const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
+                       const uint16_t *shared_gate, const float *x, int64_t T, float *y,
+                       int32_t *ids_out, float *w_out, float *logits_out)
+{
+    return oracle_moe_forward_ex(d, f, E, k, norm, bits, router_w, expert_bias, 0, 1.0f, blobs,
+                                 shared_blob, fs, shared_gate, x, T, y, ids_out, w_out,
+                                 logits_out);
 }

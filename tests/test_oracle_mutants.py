@@ -29,8 +29,11 @@ MUTANTS = [
     ("MSE not squared", "            acc += e * e;\n", "            acc += fabs(e);\n"),
     ("no SiLU", "double hv = (double)g / (1.0 + exp(-(double)g)) * (double)u;",
      "double hv = (double)g * (double)u;"),
-    ("no renorm", "weights[t * k + j] = (float)(norm ? pj / sel : pj);",
-     "weights[t * k + j] = (float)pj;"),
+    ("no renorm", "weights[t * k + j] = (float)((norm ? pj / sel : pj) * (double)routed_scaling_factor);",
+     "weights[t * k + j] = (float)(pj * (double)routed_scaling_factor);"),
+    ("sigmoid router scores by softmax", "        if (router_sigmoid) {\n",
+     "        if (0) {\n"),
+    ("scaling factor ignored", "* (double)routed_scaling_factor);", ");"),
     ("grid off by one", "double v = (double)j * step + start;",
      "double v = (double)(j + 1) * step + start;"),
     ("shared gate ignored", "                sw = 1.0 / (1.0 + exp(-z));\n",
@@ -52,6 +55,7 @@ def test_pins_reject_mutant(name, old, new, tmp_path):
     env = dict(os.environ, SMOE_ORACLE_SO=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_quant.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_route_forward.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_route_forward.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_router_variants.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins passed a mutant oracle ({name})"
