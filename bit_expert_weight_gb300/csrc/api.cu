@@ -383,6 +383,32 @@ smoe_status smoe_unpack(const void *tiles, int32_t d_model, int32_t ffn_dim, int
     return SMOE_OK;
 }
 
+static bool valid_opts(const smoe_router_opts *o)
+{
+    // a positive, finite scaling factor; NaN fails both comparisons
+    return !o || (o->routed_scaling_factor > 0.0f && o->routed_scaling_factor <= 3.0e38f);
+}
+
+smoe_status smoe_route_from_logits_ex(const float *logits, int64_t T, int32_t E, int32_t k,
+                                      int norm_topk_prob, const float *expert_bias,
+                                      const smoe_router_opts *opts, int32_t *ids,
+                                      float *weights, void *cuda_stream)
+{
+    if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > SMOE_MAX_TOP_K || k > E ||
+        !valid_opts(opts))
+        return SMOE_ERR_INVALID_ARG;
+    if (T == 0)
+        return SMOE_OK;
+    if (!logits || !ids || !weights)
+        return SMOE_ERR_INVALID_ARG;
+    if (!device_supported())
+        return SMOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_route_logits(logits, T, E, k, norm_topk_prob ? 1 : 0, expert_bias,
+                                           opts && opts->router_sigmoid ? 1 : 0,
+                                           opts ? opts->routed_scaling_factor : 1.0f, ids,
+                                           weights, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 smoe_status smoe_route_from_logits(const float *logits, int64_t T, int32_t E, int32_t k,
                                    int norm_topk_prob, const float *expert_bias, int32_t *ids,
                                    float *weights, void *cuda_stream)
@@ -395,8 +421,9 @@ smoe_status smoe_route_from_logits(const float *logits, int64_t T, int32_t E, in
         return SMOE_ERR_INVALID_ARG;
     if (!device_supported())
         return SMOE_ERR_UNSUPPORTED;
-    return cuda_status(launch_route_logits(logits, T, E, k, norm_topk_prob ? 1 : 0, expert_bias,
-                                           ids, weights, static_cast<cudaStream_t>(cuda_stream)));
+    return cuda_status(launch_route_logits(logits, T, E, k, norm_topk_prob ? 1 : 0, expert_bias, 0,
+                                           1.0f, ids, weights,
+                                           static_cast<cudaStream_t>(cuda_stream)));
 }
 
 size_t smoe_moe_workspace_bytes(const smoe_layer_desc *layer, int64_t num_tokens)
@@ -416,12 +443,13 @@ smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, voi
                                        static_cast<cudaStream_t>(cuda_stream)));
 }
 
-static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
-                                  int64_t num_tokens, float *y, void *workspace,
-                                  size_t workspace_bytes, int32_t *ids_out, float *w_out,
-                                  int stage_mask, int path, void *cuda_stream)
+static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_router_opts *opts,
+                                  const void *x, smoe_dtype x_dtype, int64_t num_tokens, float *y,
+                                  void *workspace, size_t workspace_bytes, int32_t *ids_out,
+                                  float *w_out, int stage_mask, int path, void *cuda_stream)
 {
-    if (!valid_layer(layer) || num_tokens < 0 || (x_dtype != SMOE_F32 && x_dtype != SMOE_BF16))
+    if (!valid_layer(layer) || num_tokens < 0 || (x_dtype != SMOE_F32 && x_dtype != SMOE_BF16) ||
+        !valid_opts(opts))
         return SMOE_ERR_INVALID_ARG;
     if (num_tokens == 0)
         return SMOE_OK;
@@ -472,6 +500,8 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     ra.done_ctr = at<unsigned>(workspace, P.off_ctr_done);
     ra.status = status;
     ra.max_pairs = P.max_pairs;
+    ra.router_sigmoid = opts && opts->router_sigmoid ? 1 : 0;
+    ra.rsf = opts ? opts->routed_scaling_factor : 1.0f;
 
     LayerArgs la;
     memset(&la, 0, sizeof la);
@@ -496,6 +526,8 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const void *x, s
     la.bits = L.bits;
     la.Epad = P.Epad;
     la.has_shared = ra.has_shared;
+    la.router_sigmoid = ra.router_sigmoid;
+    la.rsf = ra.rsf;
     la.do_route = fused ? 1 : 0;
     la.fused_combine = num_tokens <= kFusedCombineMaxT ? 1 : 0;
     la.max_pairs = P.max_pairs;
@@ -586,8 +618,19 @@ smoe_status smoe_moe_forward(const smoe_layer_desc *layer, const void *x, smoe_d
                              size_t workspace_bytes, int32_t *ids_out, float *w_out,
                              void *cuda_stream)
 {
-    return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
-                          w_out, 7, SMOE_PATH_AUTO, cuda_stream);
+    return forward_stages(layer, nullptr, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
+                          ids_out, w_out, 7, SMOE_PATH_AUTO, cuda_stream);
+}
+
+smoe_status smoe_moe_forward_ex(const smoe_layer_desc *layer, const smoe_router_opts *opts,
+                                const void *x, smoe_dtype x_dtype, int64_t num_tokens, float *y,
+                                void *workspace, size_t workspace_bytes, int32_t *ids_out,
+                                float *w_out, int path, void *cuda_stream)
+{
+    if (path != SMOE_PATH_AUTO && path != SMOE_PATH_STREAM && path != SMOE_PATH_GROUPED)
+        return SMOE_ERR_INVALID_ARG;
+    return forward_stages(layer, opts, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
+                          ids_out, w_out, 7, path, cuda_stream);
 }
 
 smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
@@ -597,8 +640,8 @@ smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, s
 {
     if (path != SMOE_PATH_AUTO && path != SMOE_PATH_STREAM && path != SMOE_PATH_GROUPED)
         return SMOE_ERR_INVALID_ARG;
-    return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
-                          w_out, 7, path, cuda_stream);
+    return forward_stages(layer, nullptr, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
+                          ids_out, w_out, 7, path, cuda_stream);
 }
 
 int smoe_moe_path(const smoe_layer_desc *layer, int64_t num_tokens)
@@ -615,8 +658,8 @@ smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
 {
     if (stage < 0 || stage > 2)
         return SMOE_ERR_INVALID_ARG;
-    return forward_stages(layer, x, x_dtype, num_tokens, y, workspace, workspace_bytes, ids_out,
-                          w_out, 1 << stage, SMOE_PATH_AUTO, cuda_stream);
+    return forward_stages(layer, nullptr, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
+                          ids_out, w_out, 1 << stage, SMOE_PATH_AUTO, cuda_stream);
 }
 
 smoe_status smoe_get_device_status(void *cuda_stream)

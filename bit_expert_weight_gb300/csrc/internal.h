@@ -72,12 +72,15 @@ struct RouteArgs {
     unsigned *done_ctr;         // [1]
     int *status;
     int max_pairs;
+    int router_sigmoid;         // 1: per-expert sigmoid scores
+    float rsf;                  // routed scaling factor
     // grouped path (null: the streaming path's pair table is built instead)
     int32_t *grp_tilecnt;       // [T/8 tiles][E] selections per (token tile, expert)
 };
 
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
-                                const float *bias, int32_t *ids, float *w, cudaStream_t stream);
+                                const float *bias, int router_sigmoid, float rsf, int32_t *ids,
+                                float *w, cudaStream_t stream);
 cudaError_t launch_router(const RouteArgs &a, cudaStream_t stream, bool pdl);
 // Grouped path, bf16 tokens: routing of tiles of 8 tokens from logits
 // [T][Epad] (plus the shared gate and the per-tile expert counts).
@@ -100,6 +103,8 @@ struct LayerArgs {
     int x_bf16;
     int64_t T;
     int d, f, fs, E, k, norm, bits, Epad, has_shared;
+    int router_sigmoid;            // 1: per-expert sigmoid scores
+    float rsf;                     // routed scaling factor
     int do_route;                  // 1: phase R inside the kernel (T <= 8)
     int fused_combine;             // 1: combine inside the kernel (T <= 8)
     int max_pairs, max_strips;     // counter strides

@@ -166,24 +166,28 @@ __device__ __forceinline__ float sigmoid_fast(float x)
 // tables.  Task (token t, chunk c) on one warp: lane L takes expert
 // e = 32 c + L, whose rank is the number of experts before it in the order
 // (key descending, index ascending) -- ties go to the lower index; ranks
-// below k are the selection, stored at their rank.  The softmax maximum and
-// sum run over all E logits in a fixed order (lane-strided, then a shuffle
-// tree), the same in every task; exp and divide are the hardware
-// approximations (a few ulp), well inside the weights' tolerance.
+// below k are the selection, stored at their rank with its score: the
+// softmax over all E logits, or (sigm) the expert's own sigmoid.  The
+// softmax maximum and sum run over all E logits in a fixed order
+// (lane-strided, then a shuffle tree), the same in every task; exp and divide
+// are the hardware approximations (a few ulp), well inside the weights'
+// tolerance.
 __device__ __noinline__ void route_chunk(const float *lg, const float *key, int E, int k, int c,
-                                         int16_t *ids_s, float *p_s)
+                                         int sigm, int16_t *ids_s, float *p_s)
 {
     const int lane = threadIdx.x & 31;
-    float m = -INFINITY;
-    for (int i = lane; i < E; i += 32)
-        m = fmaxf(m, lg[i]);
-    for (int o = 16; o; o >>= 1)
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float z = 0.f;
-    for (int i = lane; i < E; i += 32)
-        z += __expf(lg[i] - m);
-    for (int o = 16; o; o >>= 1)
-        z += __shfl_xor_sync(0xffffffffu, z, o);
+    float m = -INFINITY, z = 1.f;
+    if (!sigm) {
+        for (int i = lane; i < E; i += 32)
+            m = fmaxf(m, lg[i]);
+        for (int o = 16; o; o >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        z = 0.f;
+        for (int i = lane; i < E; i += 32)
+            z += __expf(lg[i] - m);
+        for (int o = 16; o; o >>= 1)
+            z += __shfl_xor_sync(0xffffffffu, z, o);
+    }
     const int e = 32 * c + lane;
     if (e >= E)
         return;
@@ -205,7 +209,7 @@ __device__ __noinline__ void route_chunk(const float *lg, const float *key, int 
     }
     if (r < k) {
         ids_s[r] = static_cast<int16_t>(e);
-        p_s[r] = __fdividef(__expf(lg[e] - m), z);  // z in [1, E]
+        p_s[r] = sigm ? sigmoid_fast(lg[e]) : __fdividef(__expf(lg[e] - m), z);  // z in [1, E]
     }
 }
 
@@ -1280,7 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                 a.cta_flags[32 * blockIdx.x] = 0u;  // only this CTA reads it
             }
         } else if (warp <= (a.E + 31) / 32) {
-            route_chunk(rs.lg, rs.key, a.E, a.k, warp - 1, rs.warm_id, rs.warm_p);
+            route_chunk(rs.lg, rs.key, a.E, a.k, warp - 1, a.router_sigmoid, rs.warm_id, rs.warm_p);
         }
         cta_barrier();
         ok = s_ok != 0;
@@ -1295,7 +1299,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                     set_status(a.status, kStatusBadArg);
                     l = -INFINITY;
                 }
-                float key = a.expert_bias ? __fadd_rn(l, __ldg(a.expert_bias + e)) : l;
+                // selection key: the logit; with a bias, logit + bias
+                // (softmax) or fl32(sigmoid(logit)) + bias (sigmoid)
+                float key = a.expert_bias ? __fadd_rn(a.router_sigmoid ? sigmoid_fast(l) : l,
+                                                      __ldg(a.expert_bias + e))
+                                          : l;
                 if (key != key)
                     key = -INFINITY;
                 rs.lg[t * E4 + e] = l;
@@ -1307,7 +1315,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             const int nc = (E + 31) / 32;
             for (int task = warp; task < T * nc; task += kWarps) {
                 const int t = task / nc, c = task - t * nc;
-                route_chunk(rs.lg + t * E4, rs.key + t * E4, E, kk, c, rs.ids + t * kk, rs.prob + t * kk);
+                route_chunk(rs.lg + t * E4, rs.key + t * E4, E, kk, c, a.router_sigmoid,
+                            rs.ids + t * kk, rs.prob + t * kk);
             }
         }
         cta_barrier();
@@ -1318,7 +1327,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                 psel += rs.prob[t * kk + j];
             if (lane < kk) {
                 const float pj = rs.prob[t * kk + lane];
-                const float wv = a.norm ? __fdividef(pj, psel) : pj;
+                const float wv = (a.norm ? __fdividef(pj, psel) : pj) * a.rsf;
                 rs.weights[t * kk + lane] = wv;
                 if (blockIdx.x == 0) {
                     const int id = rs.ids[t * kk + lane];

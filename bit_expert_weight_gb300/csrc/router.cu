@@ -28,8 +28,12 @@ constexpr int kMtPerWarp = (kMaxMt + kRWarps - 1) / kRWarps;   // 3 for 256 expe
 constexpr int kPerLane = kMaxExperts / 32;
 
 // Route one token with one warp: lg = its E logits (any address space).
+// Scores: softmax over all E, or (sigm) each expert's sigmoid; key = the
+// logit, or with a bias logit + bias (softmax) / fl32(sigmoid) + bias
+// (sigmoid); weights = selected scores, renormalised if norm, times rsf.
 __device__ void route_token_warp(const float *lg, int E, int k, int norm, const float *bias,
-                                 int32_t *ids, float *w, int32_t *ids2, float *w2, int *status)
+                                 int sigm, float rsf, int32_t *ids, float *w, int32_t *ids2,
+                                 float *w2, int *status)
 {
     const int lane = threadIdx.x & 31;
     float key[kPerLane], lv[kPerLane];
@@ -44,7 +48,10 @@ __device__ void route_token_warp(const float *lg, int E, int k, int norm, const 
                 set_status(status, kStatusBadArg);
                 l = -INFINITY;
             }
-            kk = bias ? __fadd_rn(l, __ldg(bias + e)) : l;
+            if (bias)
+                kk = __fadd_rn(sigm ? 1.0f / (1.0f + expf(-l)) : l, __ldg(bias + e));
+            else
+                kk = l;
             if (kk != kk)
                 kk = -INFINITY;
         }
@@ -89,7 +96,7 @@ __device__ void route_token_warp(const float *lg, int E, int k, int norm, const 
         }
         if ((bi & 31) == lane)
             taken |= 1u << (bi >> 5);
-        const float p = expf(lg[bi] - m) / z;
+        const float p = sigm ? 1.0f / (1.0f + expf(-lg[bi])) : expf(lg[bi] - m) / z;
         psel += p;
         if (lane == j) {
             pj_mine = p;
@@ -97,7 +104,7 @@ __device__ void route_token_warp(const float *lg, int E, int k, int norm, const 
         }
     }
     if (lane < k) {
-        const float wv = norm ? pj_mine / psel : pj_mine;
+        const float wv = (norm ? pj_mine / psel : pj_mine) * rsf;
         ids[lane] = ej_mine;
         w[lane] = wv;
         if (ids2)
@@ -109,14 +116,15 @@ __device__ void route_token_warp(const float *lg, int E, int k, int norm, const 
 
 __global__ void __launch_bounds__(kRThreads) route_logits_kernel(const float *logits, int64_t T,
                                                                  int E, int k, int norm,
-                                                                 const float *bias, int32_t *ids,
+                                                                 const float *bias, int sigm,
+                                                                 float rsf, int32_t *ids,
                                                                  float *w, int *status)
 {
     const int64_t t = (int64_t)blockIdx.x * kRWarps + (threadIdx.x >> 5);
     if (t >= T)
         return;
-    route_token_warp(logits + t * E, E, k, norm, bias, ids + t * k, w + t * k, nullptr, nullptr,
-                     status);
+    route_token_warp(logits + t * E, E, k, norm, bias, sigm, rsf, ids + t * k, w + t * k, nullptr,
+                     nullptr, status);
 }
 
 struct DispatchSmem {
@@ -373,8 +381,9 @@ __global__ void __launch_bounds__(kRThreads) router_kernel(const RouteArgs a)
     {
         const int64_t t = t0 + warp;
         if (warp < kPairCols && t < a.T) {
-            route_token_warp(sm.lgt.lg[warp], E, a.k, a.norm, a.expert_bias, a.ids + t * a.k,
-                             a.weights + t * a.k, a.ids_out ? a.ids_out + t * a.k : nullptr,
+            route_token_warp(sm.lgt.lg[warp], E, a.k, a.norm, a.expert_bias, a.router_sigmoid,
+                             a.rsf, a.ids + t * a.k, a.weights + t * a.k,
+                             a.ids_out ? a.ids_out + t * a.k : nullptr,
                              a.w_out ? a.w_out + t * a.k : nullptr, a.status);
             if (lane == 0)
                 a.shared_w[t] = a.shared_gate ? 1.0f / (1.0f + expf(-sm.lgt.lg[warp][E])) : 1.0f;
@@ -432,8 +441,8 @@ __global__ void __launch_bounds__(kRThreads) route_tiles_kernel(const RouteArgs 
         cnt[e] = 0;
     const int64_t t = t0 + warp;
     if (warp < kPairCols && t < a.T) {
-        route_token_warp(logits + t * Epad, E, k, a.norm, a.expert_bias, a.ids + t * k,
-                         a.weights + t * k, a.ids_out ? a.ids_out + t * k : nullptr,
+        route_token_warp(logits + t * Epad, E, k, a.norm, a.expert_bias, a.router_sigmoid, a.rsf,
+                         a.ids + t * k, a.weights + t * k, a.ids_out ? a.ids_out + t * k : nullptr,
                          a.w_out ? a.w_out + t * k : nullptr, a.status);
         float sw = 1.0f;
         if (a.shared_gate) {
@@ -479,12 +488,13 @@ cudaError_t launch_route_tiles(const RouteArgs &a, const float *logits, int Epad
 }
 
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
-                                const float *bias, int32_t *ids, float *w, cudaStream_t stream)
+                                const float *bias, int router_sigmoid, float rsf, int32_t *ids,
+                                float *w, cudaStream_t stream)
 {
     if (T == 0)
         return cudaSuccess;
     route_logits_kernel<<<static_cast<unsigned>((T + kRWarps - 1) / kRWarps), kRThreads, 0, stream>>>(
-        logits, T, E, k, norm, bias, ids, w, device_status_word());
+        logits, T, E, k, norm, bias, router_sigmoid, rsf, ids, w, device_status_word());
     return cudaGetLastError();
 }
 

@@ -33,10 +33,16 @@ EXPORTED = [
     "smoe_moe_forward", "smoe_moe_forward_stage", "smoe_get_device_status",
     "smoe_moe_forward_noalloc", "smoe_moe_forward_path", "smoe_moe_path",
     "smoe_vault_parse", "smoe_vault_find_expert", "smoe_vault_repack_layer",
+    "smoe_route_from_logits_ex", "smoe_moe_forward_ex",
 ]
 
 # Execution paths (SMOE_PATH_* in include/smoe.h).
 PATH_AUTO, PATH_STREAM, PATH_GROUPED = 0, 1, 2
+
+
+class RouterOpts(ctypes.Structure):
+    """smoe_router_opts (include/smoe.h)."""
+    _fields_ = [("router_sigmoid", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float)]
 
 
 class VaultInfo(ctypes.Structure):
@@ -138,6 +144,12 @@ def load(path: str | None = None):
     L.smoe_moe_forward_path.restype = I
     L.smoe_moe_path.argtypes = [ctypes.POINTER(LayerDesc), I64]
     L.smoe_moe_path.restype = I
+    RP = ctypes.POINTER(RouterOpts)
+    L.smoe_route_from_logits_ex.argtypes = [P, I64, I32, I32, I, P, RP, P, P, P]
+    L.smoe_route_from_logits_ex.restype = I
+    L.smoe_moe_forward_ex.argtypes = [ctypes.POINTER(LayerDesc), RP, P, I, I64, P, P, S, P, P, I,
+                                      P]
+    L.smoe_moe_forward_ex.restype = I
     VP = ctypes.POINTER(VaultInfo)
     L.smoe_vault_parse.argtypes = [P, S, ctypes.c_uint64, VP]
     L.smoe_vault_parse.restype = I
@@ -248,13 +260,27 @@ def unpack(tiles, d: int, f: int, n_experts: int, bits: int, stream=None):
 
 # ------------------------------------------------------------------ route
 
-def route_from_logits(logits: torch.Tensor, k: int, norm: bool, bias=None, stream=None):
+def _opts(router_sigmoid, routed_scaling_factor):
+    if not router_sigmoid and routed_scaling_factor == 1.0:
+        return None
+    return RouterOpts(int(bool(router_sigmoid)), float(routed_scaling_factor))
+
+
+def route_from_logits(logits: torch.Tensor, k: int, norm: bool, bias=None, stream=None,
+                      router_sigmoid=False, routed_scaling_factor=1.0):
+    """smoe_route_from_logits (smoe_route_from_logits_ex with router options)."""
     T, E = logits.shape
     ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
-    _check(load().smoe_route_from_logits(_ptr(logits), T, E, k, int(bool(norm)), _ptr(bias),
-                                         _ptr(ids), _ptr(w), _stream(stream)),
-           "smoe_route_from_logits")
+    o = _opts(router_sigmoid, routed_scaling_factor)
+    if o is None:
+        _check(load().smoe_route_from_logits(_ptr(logits), T, E, k, int(bool(norm)), _ptr(bias),
+                                             _ptr(ids), _ptr(w), _stream(stream)),
+               "smoe_route_from_logits")
+    else:
+        _check(load().smoe_route_from_logits_ex(_ptr(logits), T, E, k, int(bool(norm)),
+                                                _ptr(bias), ctypes.byref(o), _ptr(ids), _ptr(w),
+                                                _stream(stream)), "smoe_route_from_logits_ex")
     return ids, w
 
 
@@ -292,16 +318,23 @@ def workspace(layer: MoELayer, T: int, device=None, stream=None):
 
 
 def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None, w=None,
-            stream=None, path=None):
-    """smoe_moe_forward (or smoe_moe_forward_path when `path` is given); x is
-    [T, d] fp32 or bf16; returns y fp32 [T, d]."""
+            stream=None, path=None, router_sigmoid=False, routed_scaling_factor=1.0):
+    """smoe_moe_forward (smoe_moe_forward_path when `path` is given,
+    smoe_moe_forward_ex with router options); x is [T, d] fp32 or bf16;
+    returns y fp32 [T, d]."""
     T = x.shape[0]
     if y is None:
         y = torch.empty((T, layer.d), dtype=torch.float32, device=x.device)
     dt = SMOE_BF16 if x.dtype == torch.bfloat16 else SMOE_F32
     if x.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("x must be fp32 or bf16")
-    if path is None:
+    o = _opts(router_sigmoid, routed_scaling_factor)
+    if o is not None:
+        _check(load().smoe_moe_forward_ex(ctypes.byref(layer.desc), ctypes.byref(o), _ptr(x), dt,
+                                          T, _ptr(y), _ptr(ws), ws.numel(), _ptr(ids), _ptr(w),
+                                          PATH_AUTO if path is None else int(path),
+                                          _stream(stream)), "smoe_moe_forward_ex")
+    elif path is None:
         _check(load().smoe_moe_forward(ctypes.byref(layer.desc), _ptr(x), dt, T, _ptr(y), _ptr(ws),
                                        ws.numel(), _ptr(ids), _ptr(w), _stream(stream)),
                "smoe_moe_forward")

@@ -249,6 +249,29 @@ smoe_status smoe_route_from_logits(const float *logits, int64_t T, int32_t E, in
                                    int norm_topk_prob, const float *expert_bias, int32_t *ids,
                                    float *weights, void *cuda_stream);
 
+/* Router variants ("CMF v2 -- Format Specification", 2.2 MoE).  Passing
+ * NULL where an entry point takes options means the defaults: softmax,
+ * factor 1 (what smoe_route_from_logits and smoe_moe_forward do).
+ *   router_sigmoid         0: softmax over all E logits; 1: each expert
+ *                          scored by sigmoid(logit) on its own
+ *   routed_scaling_factor  multiplies the selected weights after the
+ *                          optional renormalisation; finite and > 0
+ * Selection key: the logit without a bias; with an expert_bias, logit + bias
+ * (softmax) or fl32(sigmoid(logit)) + bias (sigmoid); ties to the lower
+ * expert index.  The shared expert's weight is not scaled. */
+typedef struct {
+    int32_t router_sigmoid;
+    float routed_scaling_factor;
+} smoe_router_opts;
+
+/* smoe_route_from_logits with router options (opts nullable).  Errors as
+ * smoe_route_from_logits, plus SMOE_ERR_INVALID_ARG for a factor that is not
+ * finite and positive. */
+smoe_status smoe_route_from_logits_ex(const float *logits, int64_t T, int32_t E, int32_t k,
+                                      int norm_topk_prob, const float *expert_bias,
+                                      const smoe_router_opts *opts, int32_t *ids,
+                                      float *weights, void *cuda_stream);
+
 /* ------------------------------------------------------------- forward */
 
 /* Workspace bytes smoe_moe_forward needs for this layer and token count
@@ -302,6 +325,14 @@ smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, s
                                   int64_t num_tokens, float *y, void *workspace,
                                   size_t workspace_bytes, int32_t *ids_out, float *w_out, int path,
                                   void *cuda_stream);
+
+/* smoe_moe_forward_path with router options (opts nullable; see
+ * smoe_router_opts).  Same arguments and errors, plus SMOE_ERR_INVALID_ARG
+ * for a scaling factor that is not finite and positive. */
+smoe_status smoe_moe_forward_ex(const smoe_layer_desc *layer, const smoe_router_opts *opts,
+                                const void *x, smoe_dtype x_dtype, int64_t num_tokens, float *y,
+                                void *workspace, size_t workspace_bytes, int32_t *ids_out,
+                                float *w_out, int path, void *cuda_stream);
 
 /* The path smoe_moe_forward takes for this layer and token count
  * (SMOE_PATH_STREAM or SMOE_PATH_GROUPED), or -1 on invalid arguments. */

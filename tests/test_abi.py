@@ -157,3 +157,23 @@ def test_path_selection_and_path_argument(libs):
     w16 = L.smoe_moe_workspace_bytes(ctypes.byref(desc), 16)
     rows16 = 16 * 2 + 8 * 127
     assert w16 - w15 >= rows16 * (256 * 2 + 128 * 2 + 256 * 4)
+
+
+def test_router_options_are_validated_on_the_host(libs):
+    """smoe_router_opts: the routed scaling factor must be finite and > 0
+    (refused before anything is launched)."""
+    S, _ = libs
+    L = S.load()
+    P = ctypes.c_void_p
+    desc = _desc(S)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        o = S.RouterOpts(0, bad)
+        assert L.smoe_moe_forward_ex(ctypes.byref(desc), ctypes.byref(o), P(4096), 0, 4, P(8192),
+                                     P(1 << 20), 1 << 30, None, None, 0, None) == -1
+        assert L.smoe_route_from_logits_ex(P(4096), 4, 8, 2, 1, None, ctypes.byref(o), P(8192),
+                                           P(16384), None) == -1
+    o = S.RouterOpts(1, 2.5)
+    assert L.smoe_moe_forward_ex(ctypes.byref(desc), ctypes.byref(o), P(4096), 0, 4, P(8192),
+                                 P(1 << 20), 1 << 30, None, None, 9, None) == -1   # bad path
+    assert L.smoe_route_from_logits_ex(P(4096), 0, 8, 2, 1, None, ctypes.byref(o), None, None,
+                                       None) == 0                                  # T = 0
