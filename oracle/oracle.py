@@ -90,7 +90,9 @@ def lib():
             L.oracle_route_ex.argtypes = [P, I64, I32, I32, I32, P, I32, F, P, P]
             L.oracle_route_ex.restype = ctypes.c_int
             L.oracle_moe_forward_ex.argtypes = [I32, I32, I32, I32, I32, ctypes.c_int, P, P, I32,
-                                                F, P, P, I32, P, P, I64, P, P, P, P]
+                                                F, P, P, P, I32, P, P, I64, P, P, P, P]
+            L.oracle_route_ex2.argtypes = [P, I64, I32, I32, I32, P, I32, F, P, P, P]
+            L.oracle_route_ex2.restype = ctypes.c_int
             L.oracle_moe_forward_ex.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -218,17 +220,21 @@ def router_logits(wr_bf16: np.ndarray, x: np.ndarray) -> np.ndarray:
 
 
 def route(logits: np.ndarray, k: int, norm: bool, bias: np.ndarray | None = None,
-          router_sigmoid: bool = False, routed_scaling_factor: float = 1.0):
+          router_sigmoid: bool = False, routed_scaling_factor: float = 1.0,
+          mask: np.ndarray | None = None):
     """Top-k routing ("CMF v2 -- Format Specification", 2.2 MoE): softmax or
     per-expert sigmoid scores, selection-only bias, renormalisation, then
-    the routed scaling factor."""
+    the routed scaling factor; an optional routing mask (§5: uint8
+    bitfield, LSB-first) limits selection and softmax to the routable
+    experts."""
     lg = _c(logits, np.float32)
     T, E = lg.shape
     b = None if bias is None else _c(bias, np.float32)
+    m = None if mask is None else _c(mask, np.uint8)
     ids = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float32)
-    if lib().oracle_route_ex(_p(lg), T, E, k, int(bool(norm)), _p(b), int(bool(router_sigmoid)),
-                             ctypes.c_float(routed_scaling_factor), _p(ids), _p(w)):
+    if lib().oracle_route_ex2(_p(lg), T, E, k, int(bool(norm)), _p(b), int(bool(router_sigmoid)),
+                              ctypes.c_float(routed_scaling_factor), _p(m), _p(ids), _p(w)):
         raise ValueError("oracle_route rejected its arguments")
     return ids, w
 
@@ -281,7 +287,7 @@ def moe_apply(d, f, E, k, bits, blobs, x, ids, weights, shared_blob=None, fs=0,
 
 def moe_forward(d, f, E, k, norm, bits, router_w, blobs, x, expert_bias=None,
                 shared_blob=None, fs=0, shared_gate=None, router_sigmoid=False,
-                routed_scaling_factor=1.0):
+                routed_scaling_factor=1.0, mask=None):
     """Full MoE layer forward; returns (y, ids, weights, logits)."""
     xx = _c(x, np.float32)
     T = xx.shape[0]
@@ -294,9 +300,10 @@ def moe_forward(d, f, E, k, norm, bits, router_w, blobs, x, expert_bias=None,
     ids = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float32)
     lg = np.zeros((T, E), np.float32)
+    mk = None if mask is None else _c(mask, np.uint8)
     rc = lib().oracle_moe_forward_ex(d, f, E, k, int(bool(norm)), bits, _p(wr), _p(eb),
                                      int(bool(router_sigmoid)), ctypes.c_float(routed_scaling_factor),
-                                     ctypes.cast(table, ctypes.c_void_p), _p(sb), fs, _p(sg),
+                                     _p(mk), ctypes.cast(table, ctypes.c_void_p), _p(sb), fs, _p(sg),
                                      _p(xx), T, _p(y), _p(ids), _p(w), _p(lg))
     if rc:
         raise ValueError(f"oracle_moe_forward failed ({rc})")

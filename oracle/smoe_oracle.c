@@ -315,15 +315,34 @@ void oracle_router_logits(const uint16_t *wr_bf16, const float *x, int64_t T, in
  * logit); with an expert_bias, logit + bias for softmax scores, fl32(score) +
  * bias for sigmoid scores, each addition in fp32.  The bias never enters the
  * weights.  The selected scores are divided by their sum with norm_topk_prob,
- * then multiplied by routed_scaling_factor.  Slots are written in rank order.
- * Returns 0, or -1 on bad arguments. */
-int oracle_route_ex(const float *logits, int64_t T, int32_t E, int32_t k, int32_t norm,
-                    const float *bias, int32_t router_sigmoid, float routed_scaling_factor,
-                    int32_t *ids, float *weights)
+ * then multiplied by routed_scaling_factor.  A routing mask ("CMF v2", 5:
+ * expert bitfield, LSB-first, bit e set = expert e routable; nullable) limits
+ * the selection to the routable experts and the softmax to them (its
+ * normalisation runs over the routable set); its tail bits must be zero and
+ * at least k experts routable.  Slots are written in rank order.  Returns 0,
+ * or -1 on bad arguments. */
+static int routable(const uint8_t *mask, int32_t e)
+{
+    return !mask || ((mask[e >> 3] >> (e & 7)) & 1);
+}
+
+int oracle_route_ex2(const float *logits, int64_t T, int32_t E, int32_t k, int32_t norm,
+                     const float *bias, int32_t router_sigmoid, float routed_scaling_factor,
+                     const uint8_t *mask, int32_t *ids, float *weights)
 {
     if (E <= 0 || k < 1 || k > 16 || k > E || !(routed_scaling_factor > 0.0f) ||
         routed_scaling_factor > 3.0e38f)
         return -1;
+    if (mask) {
+        int32_t n = 0;
+        for (int32_t e = 0; e < E; ++e)
+            n += routable(mask, e);
+        for (int32_t e = E; e < (E + 7) / 8 * 8; ++e)
+            if ((mask[e >> 3] >> (e & 7)) & 1)
+                return -1; /* tail bits beyond E must be zero */
+        if (n < k)
+            return -1;
+    }
     float *key = (float *)malloc(sizeof(float) * (size_t)E);
     uint8_t *taken = (uint8_t *)malloc((size_t)E);
     double *p = (double *)malloc(sizeof(double) * (size_t)E);
@@ -341,11 +360,11 @@ int oracle_route_ex(const float *logits, int64_t T, int32_t E, int32_t k, int32_
         } else {
             double m = -INFINITY;
             for (int32_t e = 0; e < E; ++e)
-                if ((double)l[e] > m)
+                if (routable(mask, e) && (double)l[e] > m)
                     m = (double)l[e];
             double z = 0.0;
             for (int32_t e = 0; e < E; ++e) {
-                p[e] = exp((double)l[e] - m);
+                p[e] = routable(mask, e) ? exp((double)l[e] - m) : 0.0;
                 z += p[e];
             }
             for (int32_t e = 0; e < E; ++e)
@@ -364,7 +383,7 @@ int oracle_route_ex(const float *logits, int64_t T, int32_t E, int32_t k, int32_
         for (int32_t j = 0; j < k; ++j) {
             int32_t best = -1;
             for (int32_t e = 0; e < E; ++e) {
-                if (taken[e])
+                if (taken[e] || !routable(mask, e))
                     continue;
                 if (best < 0 || key[e] > key[best]) /* strict: lower index on ties */
                     best = e;
@@ -384,10 +403,18 @@ int oracle_route_ex(const float *logits, int64_t T, int32_t E, int32_t k, int32_
     return 0;
 }
 
+int oracle_route_ex(const float *logits, int64_t T, int32_t E, int32_t k, int32_t norm,
+                    const float *bias, int32_t router_sigmoid, float routed_scaling_factor,
+                    int32_t *ids, float *weights)
+{
+    return oracle_route_ex2(logits, T, E, k, norm, bias, router_sigmoid, routed_scaling_factor,
+                            NULL, ids, weights);
+}
+
 int oracle_route(const float *logits, int64_t T, int32_t E, int32_t k, int32_t norm,
                  const float *bias, int32_t *ids, float *weights)
 {
-    return oracle_route_ex(logits, T, E, k, norm, bias, 0, 1.0f, ids, weights);
+    return oracle_route_ex2(logits, T, E, k, norm, bias, 0, 1.0f, NULL, ids, weights);
 }
 
 /* --------------------------------------------------- expert FFN (a5-a6) */
@@ -527,7 +554,7 @@ done:
 int oracle_moe_forward_ex(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm, int bits,
                           const uint16_t *router_w, const float *expert_bias,
                           int32_t router_sigmoid, float routed_scaling_factor,
-                          const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
+                          const uint8_t *mask, const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
                           const uint16_t *shared_gate, const float *x, int64_t T, float *y,
                           int32_t *ids_out, float *w_out, float *logits_out)
 {
@@ -542,8 +569,8 @@ int oracle_moe_forward_ex(int32_t d, int32_t f, int32_t E, int32_t k, int32_t no
         goto done;
     }
     oracle_router_logits(router_w, x, T, E, d, logits);
-    if (oracle_route_ex(logits, T, E, k, norm, expert_bias, router_sigmoid, routed_scaling_factor,
-                        ids, wts)) {
+    if (oracle_route_ex2(logits, T, E, k, norm, expert_bias, router_sigmoid, routed_scaling_factor,
+                         mask, ids, wts)) {
         rc = -1;
         goto done;
     }
@@ -569,7 +596,7 @@ int oracle_moe_forward(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm,
                        const uint16_t *shared_gate, const float *x, int64_t T, float *y,
                        int32_t *ids_out, float *w_out, float *logits_out)
 {
-    return oracle_moe_forward_ex(d, f, E, k, norm, bits, router_w, expert_bias, 0, 1.0f, blobs,
-                                 shared_blob, fs, shared_gate, x, T, y, ids_out, w_out,
+    return oracle_moe_forward_ex(d, f, E, k, norm, bits, router_w, expert_bias, 0, 1.0f, NULL,
+                                 blobs, shared_blob, fs, shared_gate, x, T, y, ids_out, w_out,
                                  logits_out);
 }

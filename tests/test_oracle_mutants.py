@@ -34,6 +34,9 @@ MUTANTS = [
     ("sigmoid router scores by softmax", "        if (router_sigmoid) {\n",
      "        if (0) {\n"),
     ("scaling factor ignored", "* (double)routed_scaling_factor);", ");"),
+    ("mask ignored by the softmax", "p[e] = routable(mask, e) ? exp((double)l[e] - m) : 0.0;",
+     "p[e] = exp((double)l[e] - m);"),
+    ("mask ignored by the selection", "if (taken[e] || !routable(mask, e))", "if (taken[e])"),
     ("grid off by one", "double v = (double)j * step + start;",
      "double v = (double)(j + 1) * step + start;"),
     ("shared gate ignored", "                sw = 1.0 / (1.0 + exp(-z));\n",

@@ -78,3 +78,43 @@ def test_scaling_factor_is_linear_and_validated():
     for bad in (0.0, -1.0, float("nan"), float("inf")):
         with pytest.raises(ValueError):
             O.route(lg, 4, True, routed_scaling_factor=bad)
+
+
+def _mask_bits(routable, E):
+    m = np.zeros((E + 7) // 8, np.uint8)
+    for e in routable:
+        m[e // 8] |= 1 << (e % 8)
+    return m
+
+
+@pytest.mark.parametrize("sigm", [False, True])
+def test_routing_mask_restricts_selection_and_softmax(sigm):
+    """"CMF v2", 5: bit e of the layer's row set = expert e routable;
+    selection over the routable set only, the softmax renormalising over
+    it."""
+    rng = np.random.default_rng(21)
+    T, E, k = 12, 20, 3
+    lg = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+    allowed = [1, 2, 5, 8, 9, 13, 17, 19]
+    mask = _mask_bits(allowed, E)
+    ids, w = O.route(lg, k, False, router_sigmoid=sigm, mask=mask)
+    for t in range(T):
+        sub = lg[t, allowed].astype(np.float64)
+        s = expit(sub) if sigm else softmax(sub)
+        order = sorted(range(len(allowed)), key=lambda i: (-float(lg[t, allowed[i]]), allowed[i]))[:k]
+        assert list(ids[t]) == [allowed[i] for i in order]
+        assert np.allclose(w[t], s[order], rtol=1e-6)
+    # an all-ones row restricts nothing
+    i1, w1 = O.route(lg, k, True)
+    i2, w2 = O.route(lg, k, True, mask=_mask_bits(range(E), E))
+    assert np.array_equal(i1, i2) and np.array_equal(w1, w2)
+
+
+def test_routing_mask_is_validated():
+    lg = np.zeros((2, 10), np.float32)
+    with pytest.raises(ValueError):  # fewer routable experts than k
+        O.route(lg, 3, True, mask=_mask_bits([1, 2], 10))
+    bad = _mask_bits([1, 2, 3], 10)
+    bad[1] |= 0x80  # a tail bit beyond E
+    with pytest.raises(ValueError):
+        O.route(lg, 2, True, mask=bad)
