@@ -389,13 +389,35 @@ static bool valid_opts(const smoe_router_opts *o)
     return !o || (o->routed_scaling_factor > 0.0f && o->routed_scaling_factor <= 3.0e38f);
 }
 
+// The routing mask of the options as kernel words; false if its tail bits
+// beyond E are set or fewer than k experts are routable.
+static bool make_mask(const smoe_router_opts *o, int E, int k, ExpertMask *m)
+{
+    memset(m, 0, sizeof *m);
+    if (!o || !o->expert_mask)
+        return true;
+    int n = 0;
+    for (int e = 0; e < (E + 7) / 8 * 8; ++e) {
+        const bool bit = (o->expert_mask[e >> 3] >> (e & 7)) & 1;
+        if (bit && e >= E)
+            return false;
+        if (bit) {
+            m->w[e >> 5] |= 1u << (e & 31);
+            ++n;
+        }
+    }
+    m->on = 1;
+    return n >= k;
+}
+
 smoe_status smoe_route_from_logits_ex(const float *logits, int64_t T, int32_t E, int32_t k,
                                       int norm_topk_prob, const float *expert_bias,
                                       const smoe_router_opts *opts, int32_t *ids,
                                       float *weights, void *cuda_stream)
 {
+    ExpertMask mask;
     if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > SMOE_MAX_TOP_K || k > E ||
-        !valid_opts(opts))
+        !valid_opts(opts) || !make_mask(opts, E, k, &mask))
         return SMOE_ERR_INVALID_ARG;
     if (T == 0)
         return SMOE_OK;
@@ -405,7 +427,7 @@ smoe_status smoe_route_from_logits_ex(const float *logits, int64_t T, int32_t E,
         return SMOE_ERR_UNSUPPORTED;
     return cuda_status(launch_route_logits(logits, T, E, k, norm_topk_prob ? 1 : 0, expert_bias,
                                            opts && opts->router_sigmoid ? 1 : 0,
-                                           opts ? opts->routed_scaling_factor : 1.0f, ids,
+                                           opts ? opts->routed_scaling_factor : 1.0f, mask, ids,
                                            weights, static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -421,8 +443,10 @@ smoe_status smoe_route_from_logits(const float *logits, int64_t T, int32_t E, in
         return SMOE_ERR_INVALID_ARG;
     if (!device_supported())
         return SMOE_ERR_UNSUPPORTED;
+    ExpertMask none;
+    memset(&none, 0, sizeof none);
     return cuda_status(launch_route_logits(logits, T, E, k, norm_topk_prob ? 1 : 0, expert_bias, 0,
-                                           1.0f, ids, weights,
+                                           1.0f, none, ids, weights,
                                            static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -448,8 +472,9 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
                                   void *workspace, size_t workspace_bytes, int32_t *ids_out,
                                   float *w_out, int stage_mask, int path, void *cuda_stream)
 {
+    ExpertMask mask;
     if (!valid_layer(layer) || num_tokens < 0 || (x_dtype != SMOE_F32 && x_dtype != SMOE_BF16) ||
-        !valid_opts(opts))
+        !valid_opts(opts) || !make_mask(opts, layer->num_experts, layer->top_k, &mask))
         return SMOE_ERR_INVALID_ARG;
     if (num_tokens == 0)
         return SMOE_OK;
@@ -502,6 +527,7 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
     ra.max_pairs = P.max_pairs;
     ra.router_sigmoid = opts && opts->router_sigmoid ? 1 : 0;
     ra.rsf = opts ? opts->routed_scaling_factor : 1.0f;
+    ra.mask = mask;
 
     LayerArgs la;
     memset(&la, 0, sizeof la);
@@ -528,6 +554,7 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
     la.has_shared = ra.has_shared;
     la.router_sigmoid = ra.router_sigmoid;
     la.rsf = ra.rsf;
+    la.mask = mask;
     la.do_route = fused ? 1 : 0;
     la.fused_combine = num_tokens <= kFusedCombineMaxT ? 1 : 0;
     la.max_pairs = P.max_pairs;

@@ -41,6 +41,12 @@ constexpr int kPairCols = 8;
 constexpr int kPairInts = 16;          // pair record: [expert, ncols, tok0..tok7, pad]
 constexpr int kMaxBlocksPerPair = 64;  // counters per pair: f/64 and d/128 blocks
 constexpr int kMaxExperts = 256;       // router / dispatch shared-memory bound
+
+// Routable experts (a routing mask), bit e of w[e / 32]; all ones = none.
+struct ExpertMask {
+    uint32_t w[kMaxExperts / 32];
+    int on;                            // 0: every expert routable
+};
 #define SMOE_MAX_TOPK_DEV 16
 // Token counts up to this many combine inside the down kernel (last pair to
 // finish a block); larger batches use a separate combine kernel.
@@ -74,13 +80,15 @@ struct RouteArgs {
     int max_pairs;
     int router_sigmoid;         // 1: per-expert sigmoid scores
     float rsf;                  // routed scaling factor
+    ExpertMask mask;            // routable experts
     // grouped path (null: the streaming path's pair table is built instead)
     int32_t *grp_tilecnt;       // [T/8 tiles][E] selections per (token tile, expert)
 };
 
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
-                                const float *bias, int router_sigmoid, float rsf, int32_t *ids,
-                                float *w, cudaStream_t stream);
+                                const float *bias, int router_sigmoid, float rsf,
+                                const ExpertMask &mask, int32_t *ids, float *w,
+                                cudaStream_t stream);
 cudaError_t launch_router(const RouteArgs &a, cudaStream_t stream, bool pdl);
 // Grouped path, bf16 tokens: routing of tiles of 8 tokens from logits
 // [T][Epad] (plus the shared gate and the per-tile expert counts).
@@ -105,6 +113,7 @@ struct LayerArgs {
     int d, f, fs, E, k, norm, bits, Epad, has_shared;
     int router_sigmoid;            // 1: per-expert sigmoid scores
     float rsf;                     // routed scaling factor
+    ExpertMask mask;               // routable experts
     int do_route;                  // 1: phase R inside the kernel (T <= 8)
     int fused_combine;             // 1: combine inside the kernel (T <= 8)
     int max_pairs, max_strips;     // counter strides

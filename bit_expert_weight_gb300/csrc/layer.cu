@@ -1306,6 +1306,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                                           : l;
                 if (key != key)
                     key = -INFINITY;
+                // outside the routing mask: never selected, no softmax term
+                if (a.mask.on && !((a.mask.w[e >> 5] >> (e & 31)) & 1u)) {
+                    key = -INFINITY;
+                    l = -INFINITY;
+                }
                 rs.lg[t * E4 + e] = l;
                 rs.key[t * E4 + e] = key;
             }

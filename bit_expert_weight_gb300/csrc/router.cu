@@ -32,8 +32,8 @@ constexpr int kPerLane = kMaxExperts / 32;
 // logit, or with a bias logit + bias (softmax) / fl32(sigmoid) + bias
 // (sigmoid); weights = selected scores, renormalised if norm, times rsf.
 __device__ void route_token_warp(const float *lg, int E, int k, int norm, const float *bias,
-                                 int sigm, float rsf, int32_t *ids, float *w, int32_t *ids2,
-                                 float *w2, int *status)
+                                 int sigm, float rsf, const ExpertMask &mask, int32_t *ids,
+                                 float *w, int32_t *ids2, float *w2, int *status)
 {
     const int lane = threadIdx.x & 31;
     float key[kPerLane], lv[kPerLane];
@@ -52,6 +52,11 @@ __device__ void route_token_warp(const float *lg, int E, int k, int norm, const 
                 kk = __fadd_rn(sigm ? 1.0f / (1.0f + expf(-l)) : l, __ldg(bias + e));
             else
                 kk = l;
+            // an expert outside the routing mask: no key, no softmax term
+            if (mask.on && !((mask.w[e >> 5] >> (e & 31)) & 1u)) {
+                kk = -INFINITY;
+                l = -INFINITY;
+            }
             if (kk != kk)
                 kk = -INFINITY;
         }
@@ -117,14 +122,15 @@ __device__ void route_token_warp(const float *lg, int E, int k, int norm, const 
 __global__ void __launch_bounds__(kRThreads) route_logits_kernel(const float *logits, int64_t T,
                                                                  int E, int k, int norm,
                                                                  const float *bias, int sigm,
-                                                                 float rsf, int32_t *ids,
-                                                                 float *w, int *status)
+                                                                 float rsf, const ExpertMask mask,
+                                                                 int32_t *ids, float *w,
+                                                                 int *status)
 {
     const int64_t t = (int64_t)blockIdx.x * kRWarps + (threadIdx.x >> 5);
     if (t >= T)
         return;
-    route_token_warp(logits + t * E, E, k, norm, bias, sigm, rsf, ids + t * k, w + t * k, nullptr,
-                     nullptr, status);
+    route_token_warp(logits + t * E, E, k, norm, bias, sigm, rsf, mask, ids + t * k, w + t * k,
+                     nullptr, nullptr, status);
 }
 
 struct DispatchSmem {
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(kRThreads) router_kernel(const RouteArgs a)
         const int64_t t = t0 + warp;
         if (warp < kPairCols && t < a.T) {
             route_token_warp(sm.lgt.lg[warp], E, a.k, a.norm, a.expert_bias, a.router_sigmoid,
-                             a.rsf, a.ids + t * a.k, a.weights + t * a.k,
+                             a.rsf, a.mask, a.ids + t * a.k, a.weights + t * a.k,
                              a.ids_out ? a.ids_out + t * a.k : nullptr,
                              a.w_out ? a.w_out + t * a.k : nullptr, a.status);
             if (lane == 0)
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kRThreads) route_tiles_kernel(const RouteArgs 
     const int64_t t = t0 + warp;
     if (warp < kPairCols && t < a.T) {
         route_token_warp(logits + t * Epad, E, k, a.norm, a.expert_bias, a.router_sigmoid, a.rsf,
-                         a.ids + t * k, a.weights + t * k, a.ids_out ? a.ids_out + t * k : nullptr,
+                         a.mask, a.ids + t * k, a.weights + t * k, a.ids_out ? a.ids_out + t * k : nullptr,
                          a.w_out ? a.w_out + t * k : nullptr, a.status);
         float sw = 1.0f;
         if (a.shared_gate) {
@@ -488,13 +494,14 @@ cudaError_t launch_route_tiles(const RouteArgs &a, const float *logits, int Epad
 }
 
 cudaError_t launch_route_logits(const float *logits, int64_t T, int E, int k, int norm,
-                                const float *bias, int router_sigmoid, float rsf, int32_t *ids,
-                                float *w, cudaStream_t stream)
+                                const float *bias, int router_sigmoid, float rsf,
+                                const ExpertMask &mask, int32_t *ids, float *w,
+                                cudaStream_t stream)
 {
     if (T == 0)
         return cudaSuccess;
     route_logits_kernel<<<static_cast<unsigned>((T + kRWarps - 1) / kRWarps), kRThreads, 0, stream>>>(
-        logits, T, E, k, norm, bias, router_sigmoid, rsf, ids, w, device_status_word());
+        logits, T, E, k, norm, bias, router_sigmoid, rsf, mask, ids, w, device_status_word());
     return cudaGetLastError();
 }
 

@@ -42,7 +42,8 @@ PATH_AUTO, PATH_STREAM, PATH_GROUPED = 0, 1, 2
 
 class RouterOpts(ctypes.Structure):
     """smoe_router_opts (include/smoe.h)."""
-    _fields_ = [("router_sigmoid", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float)]
+    _fields_ = [("router_sigmoid", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
+                ("expert_mask", ctypes.c_void_p)]
 
 
 class VaultInfo(ctypes.Structure):
@@ -260,19 +261,27 @@ def unpack(tiles, d: int, f: int, n_experts: int, bits: int, stream=None):
 
 # ------------------------------------------------------------------ route
 
-def _opts(router_sigmoid, routed_scaling_factor):
-    if not router_sigmoid and routed_scaling_factor == 1.0:
+def _opts(router_sigmoid, routed_scaling_factor, expert_mask=None):
+    """smoe_router_opts, or None for the defaults.  expert_mask: a host
+    uint8 bitfield (numpy array or bytes), LSB-first, bit e = expert e
+    routable; the returned options keep it alive."""
+    if not router_sigmoid and routed_scaling_factor == 1.0 and expert_mask is None:
         return None
-    return RouterOpts(int(bool(router_sigmoid)), float(routed_scaling_factor))
+    o = RouterOpts(int(bool(router_sigmoid)), float(routed_scaling_factor), None)
+    if expert_mask is not None:
+        buf = ctypes.create_string_buffer(bytes(bytearray(expert_mask)), len(bytes(bytearray(expert_mask))))
+        o._mask_buf = buf
+        o.expert_mask = ctypes.cast(buf, ctypes.c_void_p)
+    return o
 
 
 def route_from_logits(logits: torch.Tensor, k: int, norm: bool, bias=None, stream=None,
-                      router_sigmoid=False, routed_scaling_factor=1.0):
+                      router_sigmoid=False, routed_scaling_factor=1.0, expert_mask=None):
     """smoe_route_from_logits (smoe_route_from_logits_ex with router options)."""
     T, E = logits.shape
     ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
-    o = _opts(router_sigmoid, routed_scaling_factor)
+    o = _opts(router_sigmoid, routed_scaling_factor, expert_mask)
     if o is None:
         _check(load().smoe_route_from_logits(_ptr(logits), T, E, k, int(bool(norm)), _ptr(bias),
                                              _ptr(ids), _ptr(w), _stream(stream)),
@@ -318,7 +327,8 @@ def workspace(layer: MoELayer, T: int, device=None, stream=None):
 
 
 def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None, w=None,
-            stream=None, path=None, router_sigmoid=False, routed_scaling_factor=1.0):
+            stream=None, path=None, router_sigmoid=False, routed_scaling_factor=1.0,
+            expert_mask=None):
     """smoe_moe_forward (smoe_moe_forward_path when `path` is given,
     smoe_moe_forward_ex with router options); x is [T, d] fp32 or bf16;
     returns y fp32 [T, d]."""
@@ -328,7 +338,7 @@ def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None
     dt = SMOE_BF16 if x.dtype == torch.bfloat16 else SMOE_F32
     if x.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("x must be fp32 or bf16")
-    o = _opts(router_sigmoid, routed_scaling_factor)
+    o = _opts(router_sigmoid, routed_scaling_factor, expert_mask)
     if o is not None:
         _check(load().smoe_moe_forward_ex(ctypes.byref(layer.desc), ctypes.byref(o), _ptr(x), dt,
                                           T, _ptr(y), _ptr(ws), ws.numel(), _ptr(ids), _ptr(w),

@@ -249,19 +249,28 @@ smoe_status smoe_route_from_logits(const float *logits, int64_t T, int32_t E, in
                                    int norm_topk_prob, const float *expert_bias, int32_t *ids,
                                    float *weights, void *cuda_stream);
 
-/* Router variants ("CMF v2 -- Format Specification", 2.2 MoE).  Passing
- * NULL where an entry point takes options means the defaults: softmax,
- * factor 1 (what smoe_route_from_logits and smoe_moe_forward do).
+/* Router variants ("CMF v2 -- Format Specification", 2.2 MoE) and routing
+ * masks (same page, 5: expert bitfields).  Passing NULL where an entry point
+ * takes options means the defaults: softmax, factor 1, no mask (what
+ * smoe_route_from_logits and smoe_moe_forward do).
  *   router_sigmoid         0: softmax over all E logits; 1: each expert
  *                          scored by sigmoid(logit) on its own
  *   routed_scaling_factor  multiplies the selected weights after the
  *                          optional renormalisation; finite and > 0
+ *   expert_mask            nullable HOST bitfield of ceil(E/8) bytes,
+ *                          LSB-first: bit e set = expert e routable.  The
+ *                          selection runs over the routable experts only
+ *                          and the softmax normalises over them; the tail
+ *                          bits beyond E must be zero and at least top_k
+ *                          experts routable (else SMOE_ERR_INVALID_ARG).
+ *                          Read during the call; not kept.
  * Selection key: the logit without a bias; with an expert_bias, logit + bias
  * (softmax) or fl32(sigmoid(logit)) + bias (sigmoid); ties to the lower
  * expert index.  The shared expert's weight is not scaled. */
 typedef struct {
     int32_t router_sigmoid;
     float routed_scaling_factor;
+    const uint8_t *expert_mask;
 } smoe_router_opts;
 
 /* smoe_route_from_logits with router options (opts nullable).  Errors as

@@ -177,3 +177,24 @@ def test_router_options_are_validated_on_the_host(libs):
                                  P(1 << 20), 1 << 30, None, None, 9, None) == -1   # bad path
     assert L.smoe_route_from_logits_ex(P(4096), 0, 8, 2, 1, None, ctypes.byref(o), None, None,
                                        None) == 0                                  # T = 0
+
+
+def test_routing_mask_is_validated_on_the_host(libs):
+    """An expert mask with a tail bit beyond E, or fewer routable experts
+    than top_k, is refused before anything is launched."""
+    S, _ = libs
+    L = S.load()
+    P = ctypes.c_void_p
+    desc = _desc(S)  # E = 8, k = 2
+    o = S._opts(False, 1.0, bytes([0b00000001]))  # one routable expert, k = 2
+    assert L.smoe_moe_forward_ex(ctypes.byref(desc), ctypes.byref(o), P(4096), 0, 4, P(8192),
+                                 P(1 << 20), 1 << 30, None, None, 0, None) == -1
+    assert L.smoe_route_from_logits_ex(P(4096), 4, 8, 2, 1, None, ctypes.byref(o), P(8192),
+                                       P(16384), None) == -1
+    # E = 10: two bytes, bits 10..15 of the second are tail bits
+    o = S._opts(False, 1.0, bytes([0b00000011, 0b00000100]))
+    assert L.smoe_route_from_logits_ex(P(4096), 4, 10, 2, 1, None, ctypes.byref(o), P(8192),
+                                       P(16384), None) == -1
+    o = S._opts(False, 1.0, bytes([0b00000011, 0b00000010]))  # bit 9: valid (3 routable)
+    assert L.smoe_route_from_logits_ex(P(4096), 0, 10, 2, 1, None, ctypes.byref(o), None, None,
+                                       None) == 0

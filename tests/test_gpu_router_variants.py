@@ -44,7 +44,8 @@ def _near_ties(lg, k, bias, sigm, rel=1e-5):
     out = set()
     for t in range(key.shape[0]):
         s = np.sort(key[t])[::-1]
-        if k < s.size and abs(s[k - 1] - s[k]) < rel * max(np.abs(key[t]).max(), 1e-30):
+        fin = np.abs(key[t][np.isfinite(key[t])])
+        if k < s.size and np.isfinite(s[k]) and abs(s[k - 1] - s[k]) < rel * max(fin.max(), 1e-30):
             out.add(t)
     return out
 
@@ -128,3 +129,69 @@ def test_forward_with_router_variants(S, name, T, path, sigm, rsf, with_bias):
     tol = 2e-2 if (path == 2 or S.path_for(lay, T) == S.PATH_GROUPED) else 1e-3
     err = float(np.abs(y - y_ref).max())
     assert err <= tol * float(np.abs(y_ref).max()), (err, tol)
+
+
+def _mask_bits(routable, E):
+    m = np.zeros((E + 7) // 8, np.uint8)
+    for e in routable:
+        m[e // 8] |= 1 << (e % 8)
+    return m
+
+
+@pytest.mark.parametrize("E,k", [(20, 3), (64, 6), (256, 8)])
+@pytest.mark.parametrize("sigm", [False, True])
+def test_route_from_logits_with_mask(S, E, k, sigm):
+    rng = np.random.default_rng(E + k + sigm)
+    T = 29
+    lg = (rng.standard_normal((T, E)) * 1.5).astype(np.float32)
+    allowed = sorted(rng.choice(E, size=max(k, E // 3), replace=False).tolist())
+    mask = _mask_bits(allowed, E)
+    ids_r, w_r = O.route(lg, k, True, router_sigmoid=sigm, routed_scaling_factor=1.5, mask=mask)
+    ids, w = S.route_from_logits(to_dev(lg, DEV), k, True, router_sigmoid=sigm,
+                                 routed_scaling_factor=1.5, expert_mask=mask)
+    ids, w = ids.cpu().numpy(), w.cpu().numpy()
+    masked = np.full_like(lg, -np.inf)
+    masked[:, allowed] = lg[:, allowed]
+    ties = _near_ties(masked, k, None, sigm)
+    ok = [t for t in range(T) if t not in ties]
+    assert set(ids.ravel().tolist()) <= set(allowed)
+    assert np.array_equal(ids[ok], ids_r[ok])
+    assert np.allclose(w[ok], w_r[ok], rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("name,T,path", [("tiny_f32", 3, None), ("wide_bf16", 13, None),
+                                         ("wide_bf16", 96, 2), ("shared_bf16", 40, 2)])
+def test_forward_with_routing_mask(S, name, T, path):
+    wl, hl = _host(name)
+    allowed = list(range(0, wl.E, 3))[:max(wl.k, wl.E // 2)]
+    if len(allowed) < wl.k:
+        allowed = list(range(wl.k))
+    mask = _mask_bits(allowed, wl.E)
+    lay = hl.device_layer(DEV)
+    x, _ = wl.activations(0, T)
+    xt = to_dev(x, DEV)
+    if wl.x_dtype == "bf16":
+        xt = xt.to(torch.bfloat16)
+    ws = S.workspace(lay, T)
+    ids = torch.empty((T, wl.k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, wl.k), dtype=torch.float32, device=DEV)
+    y = S.forward(lay, xt, ws, ids=ids, w=w, path=path, expert_mask=mask)
+    torch.cuda.synchronize()
+    assert S.device_status() == 0
+    y, ids, w = y.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+    y_ref, ids_ref, w_ref, lg = O.moe_forward(
+        wl.d, wl.f, wl.E, wl.k, wl.norm, 4, hl.router, hl.blob, x, shared_blob=hl.shared_blob,
+        fs=wl.shared_f, shared_gate=hl.shared_gate, mask=mask)
+    assert set(ids.ravel().tolist()) <= set(allowed)
+    masked = np.full_like(lg, -np.inf)
+    masked[:, allowed] = lg[:, allowed]
+    ties = _near_ties(masked, wl.k, None, False)
+    mism = [t for t in range(T) if not np.array_equal(ids[t], ids_ref[t])]
+    assert set(mism) <= ties
+    if mism:
+        y_ref = y_ref.copy()
+        y_ref[mism] = hl.oracle_apply(x[mism], ids[mism], w[mism])
+    ok = [t for t in range(T) if t not in mism]
+    assert np.allclose(w[ok], w_ref[ok], rtol=1e-5, atol=1e-6)
+    tol = 2e-2 if (path == 2 or S.path_for(lay, T) == S.PATH_GROUPED) else 1e-3
+    assert float(np.abs(y - y_ref).max()) <= tol * float(np.abs(y_ref).max())
