@@ -89,8 +89,11 @@ def lib():
             L.oracle_moe_forward.restype = ctypes.c_int
             L.oracle_route_ex.argtypes = [P, I64, I32, I32, I32, P, I32, F, P, P]
             L.oracle_route_ex.restype = ctypes.c_int
-            L.oracle_moe_forward_ex.argtypes = [I32, I32, I32, I32, I32, ctypes.c_int, P, P, I32,
-                                                F, P, P, P, I32, P, P, I64, P, P, P, P]
+            L.oracle_moe_forward_ex.argtypes = [I32, I32, I32, I32, I32, ctypes.c_int, P, P, P,
+                                                I32, F, P, P, P, I32, P, P, I64, P, P, P, P]
+            L.oracle_moe_apply_mixed.argtypes = [I32, I32, I32, I32, ctypes.c_int, P, P, P, I32,
+                                                 P, P, I64, P, P, P]
+            L.oracle_moe_apply_mixed.restype = ctypes.c_int
             L.oracle_route_ex2.argtypes = [P, I64, I32, I32, I32, P, I32, F, P, P, P]
             L.oracle_route_ex2.restype = ctypes.c_int
             L.oracle_moe_forward_ex.restype = ctypes.c_int
@@ -267,8 +270,9 @@ def _blob_table(blobs, E):
 
 
 def moe_apply(d, f, E, k, bits, blobs, x, ids, weights, shared_blob=None, fs=0,
-              shared_gate=None):
-    """Apply a given routing to T tokens (rank-order combine, shared expert)."""
+              shared_gate=None, expert_bits=None):
+    """Apply a given routing to T tokens (rank-order combine, shared expert);
+    expert_bits: each routed expert's own depth (shared expert at bits)."""
     xx = _c(x, np.float32)
     T = xx.shape[0]
     table, keep = _blob_table(blobs, E)
@@ -277,8 +281,9 @@ def moe_apply(d, f, E, k, bits, blobs, x, ids, weights, shared_blob=None, fs=0,
     ii = _c(ids, np.int32)
     ww = _c(weights, np.float32)
     y = np.zeros((T, d), np.float32)
-    rc = lib().oracle_moe_apply(d, f, E, k, bits, ctypes.cast(table, ctypes.c_void_p), _p(sb),
-                                fs, _p(sg), _p(xx), T, _p(ii), _p(ww), _p(y))
+    eb_ = None if expert_bits is None else _c(expert_bits, np.int32)
+    rc = lib().oracle_moe_apply_mixed(d, f, E, k, bits, _p(eb_), ctypes.cast(table, ctypes.c_void_p),
+                                      _p(sb), fs, _p(sg), _p(xx), T, _p(ii), _p(ww), _p(y))
     if rc:
         raise ValueError(f"oracle_moe_apply failed ({rc})")
     del keep
@@ -287,7 +292,7 @@ def moe_apply(d, f, E, k, bits, blobs, x, ids, weights, shared_blob=None, fs=0,
 
 def moe_forward(d, f, E, k, norm, bits, router_w, blobs, x, expert_bias=None,
                 shared_blob=None, fs=0, shared_gate=None, router_sigmoid=False,
-                routed_scaling_factor=1.0, mask=None):
+                routed_scaling_factor=1.0, mask=None, expert_bits=None):
     """Full MoE layer forward; returns (y, ids, weights, logits)."""
     xx = _c(x, np.float32)
     T = xx.shape[0]
@@ -301,7 +306,8 @@ def moe_forward(d, f, E, k, norm, bits, router_w, blobs, x, expert_bias=None,
     w = np.zeros((T, k), np.float32)
     lg = np.zeros((T, E), np.float32)
     mk = None if mask is None else _c(mask, np.uint8)
-    rc = lib().oracle_moe_forward_ex(d, f, E, k, int(bool(norm)), bits, _p(wr), _p(eb),
+    ebits = None if expert_bits is None else _c(expert_bits, np.int32)
+    rc = lib().oracle_moe_forward_ex(d, f, E, k, int(bool(norm)), bits, _p(ebits), _p(wr), _p(eb),
                                      int(bool(router_sigmoid)), ctypes.c_float(routed_scaling_factor),
                                      _p(mk), ctypes.cast(table, ctypes.c_void_p), _p(sb), fs, _p(sg),
                                      _p(xx), T, _p(y), _p(ids), _p(w), _p(lg))

@@ -487,13 +487,21 @@ int oracle_expert_ffn(const uint8_t *blob, int32_t d, int32_t f, int bits, const
  *   shared_blob   nullable; shared expert of intermediate size fs
  *   shared_gate   nullable bf16 [d]
  * Returns 0, -1 on bad arguments, -2 if a selected expert's blob is NULL. */
-int oracle_moe_apply(int32_t d, int32_t f, int32_t E, int32_t k, int bits,
-                     const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
-                     const uint16_t *shared_gate, const float *x, int64_t T,
-                     const int32_t *ids, const float *wts, float *y)
+/* expert_bits (nullable, [E]): each routed expert's own depth, 2 or 4
+ * (mixed bit depth per expert, "CMF v2" 2.2: each expert its own dtype);
+ * NULL = every expert at `bits`.  The shared expert is at `bits`. */
+int oracle_moe_apply_mixed(int32_t d, int32_t f, int32_t E, int32_t k, int bits,
+                           const int32_t *expert_bits, const uint8_t *const *blobs,
+                           const uint8_t *shared_blob, int32_t fs, const uint16_t *shared_gate,
+                           const float *x, int64_t T, const int32_t *ids, const float *wts,
+                           float *y)
 {
     if (d <= 0 || f <= 0 || E <= 0 || k < 1 || (bits != 2 && bits != 4))
         return -1;
+    if (expert_bits)
+        for (int32_t e = 0; e < E; ++e)
+            if (expert_bits[e] != 2 && expert_bits[e] != 4)
+                return -1;
     float *o = (float *)malloc(sizeof(float) * (size_t)d);
     double *acc = (double *)malloc(sizeof(double) * (size_t)d);
     int rc = 0;
@@ -516,7 +524,7 @@ int oracle_moe_apply(int32_t d, int32_t f, int32_t E, int32_t k, int bits,
                 rc = -2;
                 goto done;
             }
-            if (oracle_expert_ffn(b, d, f, bits, xt, o, NULL)) {
+            if (oracle_expert_ffn(b, d, f, expert_bits ? expert_bits[e] : bits, xt, o, NULL)) {
                 rc = -1;
                 goto done;
             }
@@ -547,14 +555,24 @@ done:
     return rc;
 }
 
+int oracle_moe_apply(int32_t d, int32_t f, int32_t E, int32_t k, int bits,
+                     const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
+                     const uint16_t *shared_gate, const float *x, int64_t T,
+                     const int32_t *ids, const float *wts, float *y)
+{
+    return oracle_moe_apply_mixed(d, f, E, k, bits, NULL, blobs, shared_blob, fs, shared_gate, x,
+                                  T, ids, wts, y);
+}
+
 /* Full layer forward for T tokens, each independent: router logits, route,
  * then oracle_moe_apply.  x is [T, d] fp32 (bf16 activations are widened
  * exactly by the caller); router_w is bf16 [E, d].  Optionally writes the
  * routing (ids/weights [T, k]) and the logits [T, E]. */
 int oracle_moe_forward_ex(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm, int bits,
-                          const uint16_t *router_w, const float *expert_bias,
-                          int32_t router_sigmoid, float routed_scaling_factor,
-                          const uint8_t *mask, const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
+                          const int32_t *expert_bits, const uint16_t *router_w,
+                          const float *expert_bias, int32_t router_sigmoid,
+                          float routed_scaling_factor, const uint8_t *mask,
+                          const uint8_t *const *blobs, const uint8_t *shared_blob, int32_t fs,
                           const uint16_t *shared_gate, const float *x, int64_t T, float *y,
                           int32_t *ids_out, float *w_out, float *logits_out)
 {
@@ -574,7 +592,8 @@ int oracle_moe_forward_ex(int32_t d, int32_t f, int32_t E, int32_t k, int32_t no
         rc = -1;
         goto done;
     }
-    rc = oracle_moe_apply(d, f, E, k, bits, blobs, shared_blob, fs, shared_gate, x, T, ids, wts, y);
+    rc = oracle_moe_apply_mixed(d, f, E, k, bits, expert_bits, blobs, shared_blob, fs, shared_gate,
+                                x, T, ids, wts, y);
     if (rc)
         goto done;
     if (ids_out)
@@ -596,7 +615,7 @@ int oracle_moe_forward(int32_t d, int32_t f, int32_t E, int32_t k, int32_t norm,
                        const uint16_t *shared_gate, const float *x, int64_t T, float *y,
                        int32_t *ids_out, float *w_out, float *logits_out)
 {
-    return oracle_moe_forward_ex(d, f, E, k, norm, bits, router_w, expert_bias, 0, 1.0f, NULL,
-                                 blobs, shared_blob, fs, shared_gate, x, T, y, ids_out, w_out,
-                                 logits_out);
+    return oracle_moe_forward_ex(d, f, E, k, norm, bits, NULL, router_w, expert_bias, 0, 1.0f,
+                                 NULL, blobs, shared_blob, fs, shared_gate, x, T, y, ids_out,
+                                 w_out, logits_out);
 }

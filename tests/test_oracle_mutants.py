@@ -41,6 +41,8 @@ MUTANTS = [
      "double v = (double)(j + 1) * step + start;"),
     ("shared gate ignored", "                sw = 1.0 / (1.0 + exp(-z));\n",
      "                sw = 1.0;\n"),
+    ("expert depth ignored", "oracle_expert_ffn(b, d, f, expert_bits ? expert_bits[e] : bits, xt, o, NULL)",
+     "oracle_expert_ffn(b, d, f, bits, xt, o, NULL)"),
     ("f16 truncates", "double m = rint((ldexp(a, -E) - 1.0) * 1024.0);",
      "double m = floor((ldexp(a, -E) - 1.0) * 1024.0);"),
 ]

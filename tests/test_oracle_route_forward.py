@@ -203,3 +203,30 @@ def test_forward_missing_blob_is_an_error():
     blobs = {e: experts[e]["blob"] for e in range(E) if e != ids[0, 0]}
     with pytest.raises(ValueError):
         O.moe_forward(d, f, E, 1, True, 4, router, blobs, x)
+
+
+def test_mixed_bit_depth_forward_matches_dense_brute_force():
+    """Experts at their own depths (Q2 and Q4 in one layer): each expert's
+    FFN decodes its own levels; the shared expert at the layer's depth."""
+    d, f, E, k, T = 128, 64, 6, 3, 5
+    bits_e = [4, 2, 2, 4, 2, 4]
+    layers = {b: make_layer(d, f, E, b, seed=30, shared_f=64) for b in (2, 4)}
+    experts = [layers[bits_e[e]][0][e] for e in range(E)]
+    shared = layers[4][0][E]
+    router = layers[4][1]
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    y, ids, w, lg = O.moe_forward(d, f, E, k, True, 4, router, [e["blob"] for e in experts], x,
+                                  shared_blob=shared["blob"], fs=64, expert_bits=bits_e)
+    for t in range(T):
+        xt = x[t].astype(np.float64)
+        ref = sum(float(w[t, j]) * swiglu(experts[ids[t, j]], xt) for j in range(k))
+        ref = ref + swiglu(shared, xt)
+        assert np.allclose(y[t], ref, rtol=1e-4, atol=1e-5 * np.abs(ref).max())
+    # all experts at one depth: the uniform forward
+    y4, _, _, _ = O.moe_forward(d, f, E, k, True, 4, router,
+                                [layers[4][0][e]["blob"] for e in range(E)], x,
+                                expert_bits=[4] * E)
+    y4u, _, _, _ = O.moe_forward(d, f, E, k, True, 4, router,
+                                 [layers[4][0][e]["blob"] for e in range(E)], x)
+    assert np.array_equal(y4, y4u)
