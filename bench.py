@@ -51,7 +51,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="deepseek16b", choices=sorted(Y.WORKLOADS))
     p.add_argument("--tokens", type=int, default=None)
-    p.add_argument("--bits", default="both", choices=["4", "2", "both"])
+    p.add_argument("--bits", default="both", choices=["4", "2", "both", "mixed"],
+                   help="mixed: the most popular quarter of the experts at Q4, the rest at Q2 "
+                        "(shared expert Q4)")
     p.add_argument("--layers", type=int, default=None, help="override resident layer count")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
@@ -155,6 +157,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ device model
 
+def depths(wl, bits):
+    """(per-expert depths, shared-expert depth) of a run at `bits` (2, 4 or
+    "mixed": the most popular quarter of the experts by Zipf rank at Q4, the
+    others at Q2, the shared expert at Q4)."""
+    if bits == "mixed":
+        return wl.mixed_bits(0.25), 4
+    return [bits] * wl.E, bits
+
+
+def expert_bytes(wl, f, bits, n_mats):
+    """Codes and scales of n_mats [f, d] matrices at one depth."""
+    return n_mats * (f * wl.d * bits // 8 + f * wl.d // 64 * 2)
+
+
 class DeviceModel:
     """All resident layers of one workload at one bit depth, built on device:
     seeded bf16 weights (device twin of the host generator) -> grid-search
@@ -166,6 +182,8 @@ class DeviceModel:
         import bit_expert_weight_gb300.smoe as S
         self.wl, self.bits, self.T, self.dev = wl, bits, T, dev
         d, f, E = wl.d, wl.f, wl.E
+        self.expert_bits, self.shared_bits = depths(wl, bits)
+        mixed = bits == "mixed"
         fmax = max(f, wl.shared_f)
         tmp = torch.empty(d * fmax, dtype=torch.int16, device=dev)
         self.layers, self.x, self.y = [], [], []
@@ -178,10 +196,14 @@ class DeviceModel:
                     w = tmp[: rows * cols]
                     S.synth_bf16(w, Y.stream_key(wl.seed, l, e, role), wl.sigma, wl.p_out, 10.0,
                                  wl.p_zero)
-                    c, s = S.quantize(w.view(torch.bfloat16).view(rows, cols), bits)
+                    c, s = S.quantize(w.view(torch.bfloat16).view(rows, cols),
+                                      self.expert_bits[e])
                     codes.append(c)
                     scales.append(s)
-            bank = S.repack(codes, scales, d, f, E, bits)
+            if mixed:
+                bank = S.repack_mixed(codes, scales, d, f, self.expert_bits)
+            else:
+                bank = S.repack(codes, scales, d, f, E, bits)
             del codes, scales
             sh_tiles, sh_gate = None, None
             if wl.shared_f:
@@ -191,19 +213,24 @@ class DeviceModel:
                     w = tmp[: rows * cols]
                     S.synth_bf16(w, Y.stream_key(wl.seed, l, Y.SHARED_EXPERT, role), wl.sigma,
                                  wl.p_out, 10.0, wl.p_zero)
-                    c, s = S.quantize(w.view(torch.bfloat16).view(rows, cols), bits)
+                    c, s = S.quantize(w.view(torch.bfloat16).view(rows, cols),
+                                      self.shared_bits)
                     sc.append(c)
                     ss.append(s)
-                sh_tiles = S.repack(sc, ss, d, wl.shared_f, 1, bits)
+                sh_tiles = S.repack(sc, ss, d, wl.shared_f, 1, self.shared_bits)
                 if wl.shared_gate:
                     sh_gate = torch.from_numpy(wl.shared_gate_weight(l).view(np.int16)).to(
                         dev).view(torch.bfloat16)
             router = torch.from_numpy(wl.router_weight(l).view(np.int16)).to(dev).view(
                 torch.bfloat16)
+            # the batched workload's Zipf(s) popularity as a selection-only bias
             bias = None
-            self.layers.append(S.MoELayer(d, f, E, wl.k, wl.norm, bits, router, bank,
+            if wl.zipf_s:
+                bias = torch.from_numpy(wl.zipf_bias()).to(dev)
+            self.layers.append(S.MoELayer(d, f, E, wl.k, wl.norm, self.shared_bits, router, bank,
                                           expert_bias=bias, shared_tiles=sh_tiles,
-                                          shared_f=wl.shared_f, shared_gate_w=sh_gate))
+                                          shared_f=wl.shared_f, shared_gate_w=sh_gate,
+                                          expert_bits=self.expert_bits if mixed else None))
             xf, xb = wl.activations(l, T)
             if xb is not None:
                 self.x.append(torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16))
@@ -246,14 +273,13 @@ class DeviceModel:
 def layer_algorithmic_bytes(model):
     """Whole-layer algorithmic bytes (router + distinct experts' gate/up/down
     codes and scales + x + y), averaged over layers."""
-    wl, bits = model.wl, model.bits
-    per_expert = 3 * (wl.f * wl.d * bits // 8 + wl.f * wl.d // 64 * 2)
+    wl = model.wl
     tot = 0
     for ids in model.ids:
-        distinct = len(np.unique(ids.cpu().numpy()))
-        b = distinct * per_expert + wl.E * wl.d * 2 + model.T * wl.d * (model.x[0].element_size() + 4)
+        b = sum(expert_bytes(wl, wl.f, model.expert_bits[e], 3) for e in np.unique(ids.cpu().numpy()))
+        b += wl.E * wl.d * 2 + model.T * wl.d * (model.x[0].element_size() + 4)
         if wl.shared_f:
-            b += 3 * (wl.shared_f * wl.d * bits // 8 + wl.shared_f * wl.d // 64 * 2) + wl.d * 2
+            b += expert_bytes(wl, wl.shared_f, model.shared_bits, 3) + wl.d * 2
         tot += b
     return tot / len(model.ids)
 
@@ -262,12 +288,12 @@ def gateup_bytes(model):
     """Algorithmic bytes of the gate/up grouped GEMM per layer: the gate and
     up codes and scales of the distinct experts the tokens selected (plus the
     shared expert's), the bf16 token rows in and the bf16 h rows out."""
-    wl, bits = model.wl, model.bits
-    per = 2 * (wl.f * wl.d * bits // 8 + wl.f * wl.d // 64 * 2)
-    distinct = np.mean([len(np.unique(ids.cpu().numpy())) for ids in model.ids])
-    b = distinct * per + model.T * wl.d * 2 + model.T * wl.k * wl.f * 2
+    wl = model.wl
+    b = np.mean([sum(expert_bytes(wl, wl.f, model.expert_bits[e], 2)
+                     for e in np.unique(ids.cpu().numpy())) for ids in model.ids])
+    b += model.T * wl.d * 2 + model.T * wl.k * wl.f * 2
     if wl.shared_f:
-        b += 2 * (wl.shared_f * wl.d * bits // 8 + wl.shared_f * wl.d // 64 * 2)
+        b += expert_bytes(wl, wl.shared_f, model.shared_bits, 2)
         b += model.T * wl.shared_f * 2
     return float(b)
 
@@ -281,6 +307,18 @@ def gateup_flops(model):
     if wl.shared_f:
         f += 4.0 * model.T * wl.d * wl.shared_f
     return f
+
+
+def launches_per_layer(model):
+    """Kernels one layer forward launches: the fused layer kernel for T <= 8
+    on the streaming path, else router + layer + combine; on the grouped path
+    router (bf16: logits GEMM + routing), sort, gather, one gate/up and one
+    down GEMM per depth present, combine."""
+    if not model.grouped:
+        return 1 if model.T <= 8 else 3
+    router = 2 if model.x[0].dtype.itemsize == 2 else 1
+    present = set(model.expert_bits) | ({model.shared_bits} if model.wl.shared_f else set())
+    return router + 3 + 2 * len(present)
 
 
 def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
@@ -409,11 +447,10 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
         "e2e_tokens_per_s": world * T * args.steps / (e2e_ms / 1e3),
         "h2d": h2d, "d2h": d2h, "clocks": clocks, "setup_s": model.setup_s,
         "resident_GB": model.resident_bytes / 1e9, "device_status": status,
-        "launches_per_step": n_layers * (1 if T <= 8 else
-                                         (7 if model.x[0].dtype == torch.bfloat16 else 6)
-                                         if model.grouped else 3),
+        "launches_per_step": n_layers * launches_per_layer(model),
         "grouped": model.grouped,
         "stage_us": [float(v) * 1e3 for v in np.mean(stage_ms, axis=0)] if stage_ms else None,
+        "expert_bits": list(model.expert_bits), "shared_bits": model.shared_bits,
         "gemm1_flops": gateup_flops(model) if model.grouped else None,
         "gemm1_bytes": gateup_bytes(model) if model.grouped else None,
     }
@@ -439,27 +476,31 @@ def prepare_oracle(wl, bits, layer, T):
     O.build_oracle()
     xf, _ = wl.activations(layer, T)
     router = wl.router_weight(layer)
-    ids, _ = O.route(O.router_logits(router, xf), wl.k, wl.norm)
+    bias = wl.zipf_bias() if wl.zipf_s else None
+    ids, _ = O.route(O.router_logits(router, xf), wl.k, wl.norm, bias)
     experts = sorted(set(int(e) for e in ids.ravel()))
     roles = (Y.ROLE_GATE, Y.ROLE_UP, Y.ROLE_DOWN)
-    jobs = [(wl.expert_weight(layer, e, r), bits) for e in experts for r in roles]
+    ebits, sbits = depths(wl, bits)
+    jobs = [(wl.expert_weight(layer, e, r), ebits[e]) for e in experts for r in roles]
     if wl.shared_f:
-        jobs += [(wl.expert_weight(layer, Y.SHARED_EXPERT, r), bits) for r in roles]
+        jobs += [(wl.expert_weight(layer, Y.SHARED_EXPERT, r), sbits) for r in roles]
     with mp.get_context("spawn").Pool(min(len(jobs), os.cpu_count() or 1)) as pool:
         qs = pool.map(_quant_job, jobs)
     blobs = {e: O.make_blob(*qs[3 * i:3 * i + 3]) for i, e in enumerate(experts)}
     sb = O.make_blob(*qs[-3:]) if wl.shared_f else None
     sg = wl.shared_gate_weight(layer) if wl.shared_gate else None
-    return (xf, router, blobs, sb, sg)
+    return (xf, router, blobs, sb, sg, bias)
 
 
 def time_oracle(wl, bits, prep):
     """Seconds for one oracle layer forward of the prepared tokens."""
     import oracle as O
-    xf, router, blobs, sb, sg = prep
+    xf, router, blobs, sb, sg, bias = prep
+    ebits, sbits = depths(wl, bits)
     t0 = time.perf_counter()
-    O.moe_forward(wl.d, wl.f, wl.E, wl.k, wl.norm, bits, router, blobs, xf, shared_blob=sb,
-                  fs=wl.shared_f, shared_gate=sg)
+    O.moe_forward(wl.d, wl.f, wl.E, wl.k, wl.norm, sbits, router, blobs, xf, expert_bias=bias,
+                  shared_blob=sb, fs=wl.shared_f, shared_gate=sg,
+                  expert_bits=ebits if bits == "mixed" else None)
     return time.perf_counter() - t0
 
 
@@ -469,7 +510,7 @@ def run_reference(args, wl, T, n_layers, world, rank):
     layer time times the layer count (tokens/s through all layers)."""
     if rank != 0:
         return
-    bits = wl.bits_list[0]
+    bits = "mixed" if args.bits == "mixed" else wl.bits_list[0]
     prep = prepare_oracle(wl, bits, 0, T)
     for _ in range(args.warmup):
         time_oracle(wl, bits, prep)
@@ -519,8 +560,12 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     from bit_expert_weight_gb300 import build
     build.build()
-    bits_list = [4, 2] if args.bits == "both" else [int(args.bits)]
-    bits_list = [b for b in bits_list if b in wl.bits_list] or [wl.bits_list[0]]
+    if args.bits == "mixed":
+        bits_list = ["mixed"]
+    elif args.bits == "both":
+        bits_list = [b for b in (4, 2) if b in wl.bits_list]
+    else:
+        bits_list = [int(args.bits)]  # an explicit depth, whatever the workload lists
     results = {b: run_bits(args, wl, b, n_layers, T, dev, world, rank) for b in bits_list}
     hbm, peak_kind = peaks()
     main_bits = bits_list[0]
@@ -584,6 +629,8 @@ def main():
                          f"{r['layer_alg_bytes'] * n_layers / 1e6:.0f} MB > 129 MB); no flush",
                    "graph": not args.no_graph, "parallelism": f"replicas x{world}"},
         "roofline": roofline,
+        "depths": {"q4_experts": r["expert_bits"].count(4), "q2_experts": r["expert_bits"].count(2),
+                   "shared": r["shared_bits"] if wl.shared_f else None},
         "layer": {"us": r["layer_us"], "alg_GBps": r["layer_alg_GBps"],
                   "frac": r["layer_alg_GBps"] / hbm, "tokens_per_s": r["layer_tokens_per_s"]},
         "e2e": {"value": r["e2e_tokens_per_s"], "unit": "tokens/s",

@@ -147,7 +147,8 @@ bool auto_grouped(const smoe_layer_desc *L, int64_t T)
     return T >= kGroupedMinT && T * L->top_k >= 16ll * L->num_experts;
 }
 
-Plan make_plan(const smoe_layer_desc *L, int64_t T)
+// mixed: a layer with per-expert depths, which always takes the grouped path.
+Plan make_plan(const smoe_layer_desc *L, int64_t T, bool mixed = false)
 {
     Plan p;
     p.T = T;
@@ -201,7 +202,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T)
     p.off_hspart = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 16) * 2);
     p.off_o = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
     p.off_part = take(sizeof(float) * 4 * 2 * (size_t)p.ctas * 2 * 2 * 32);
-    p.grouped = T >= kGroupedMinT;
+    p.grouped = T >= kGroupedMinT || mixed;
     p.grows = 0;
     p.off_grow = p.off_gseg = p.off_gtile = p.off_gxs = p.off_gh = p.off_go = 0;
     if (p.grouped) {
@@ -467,14 +468,36 @@ smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, voi
                                        static_cast<cudaStream_t>(cuda_stream)));
 }
 
+// The Q4 experts of a per-expert depth array as mask words; false unless
+// every entry is 2 or 4.
+static bool make_q4mask(const uint8_t *expert_bits, int E, uint32_t q4[8])
+{
+    memset(q4, 0, 8 * sizeof(uint32_t));
+    if (!expert_bits || E < 1 || E > kMaxExperts)
+        return false;
+    for (int e = 0; e < E; ++e) {
+        if (expert_bits[e] != 2 && expert_bits[e] != 4)
+            return false;
+        if (expert_bits[e] == 4)
+            q4[e >> 5] |= 1u << (e & 31);
+    }
+    return true;
+}
+
+// expert_bits: nullable host [E] per-expert depths (a mixed layer: grouped
+// path only, whatever `path` says).
 static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_router_opts *opts,
                                   const void *x, smoe_dtype x_dtype, int64_t num_tokens, float *y,
                                   void *workspace, size_t workspace_bytes, int32_t *ids_out,
-                                  float *w_out, int stage_mask, int path, void *cuda_stream)
+                                  float *w_out, int stage_mask, int path, void *cuda_stream,
+                                  const uint8_t *expert_bits = nullptr)
 {
     ExpertMask mask;
+    uint32_t q4mask[8];
+    const bool mixed = expert_bits != nullptr;
     if (!valid_layer(layer) || num_tokens < 0 || (x_dtype != SMOE_F32 && x_dtype != SMOE_BF16) ||
-        !valid_opts(opts) || !make_mask(opts, layer->num_experts, layer->top_k, &mask))
+        !valid_opts(opts) || !make_mask(opts, layer->num_experts, layer->top_k, &mask) ||
+        (mixed && !make_q4mask(expert_bits, layer->num_experts, q4mask)))
         return SMOE_ERR_INVALID_ARG;
     if (num_tokens == 0)
         return SMOE_OK;
@@ -482,13 +505,13 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
         return SMOE_ERR_INVALID_ARG;
     if (!device_supported())
         return SMOE_ERR_UNSUPPORTED;
-    const Plan P = make_plan(layer, num_tokens);
+    const Plan P = make_plan(layer, num_tokens, mixed);
     if (workspace_bytes < P.total)
         return SMOE_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const smoe_layer_desc &L = *layer;
     int *status = device_status_word();
-    const bool grouped = path == SMOE_PATH_GROUPED ||
+    const bool grouped = mixed || path == SMOE_PATH_GROUPED ||
                          (path == SMOE_PATH_AUTO && auto_grouped(layer, num_tokens));
     if (grouped && !P.grouped)
         return SMOE_ERR_UNSUPPORTED;
@@ -591,7 +614,6 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
         ga.tiles_routed = la.tiles_routed;
         ga.tiles_shared = la.tiles_shared;
         ga.expert_bytes_routed = la.expert_bytes_routed;
-        ga.down_off_routed = la.down_off_routed;
         ga.down_off_shared = la.down_off_shared;
         ga.T = num_tokens;
         ga.d = L.d_model;
@@ -613,6 +635,10 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
         ga.hstride = P.fmax;
         ga.o = at<float>(workspace, P.off_go);
         ga.status = status;
+        if (mixed) {
+            ga.mixed = 1;
+            memcpy(ga.q4mask, q4mask, sizeof q4mask);
+        }
         if (stage_mask & 1) {
             if (ra.x_bf16) {
                 if (launch_tc_logits(static_cast<const uint16_t *>(x), ra.router_w, num_tokens,
@@ -687,6 +713,115 @@ smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
         return SMOE_ERR_INVALID_ARG;
     return forward_stages(layer, nullptr, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
                           ids_out, w_out, 1 << stage, SMOE_PATH_AUTO, cuda_stream);
+}
+
+size_t smoe_repacked_bytes_mixed(int32_t d_model, int32_t ffn_dim, int32_t n_experts,
+                                 const uint8_t *expert_bits, int group_size)
+{
+    if (n_experts < 0 || (n_experts > 0 && !expert_bits))
+        return 0;
+    size_t total = 0;
+    for (int e = 0; e < n_experts; ++e) {
+        const size_t b = smoe_expert_tiles_bytes(d_model, ffn_dim, expert_bits[e], group_size);
+        if (!b)
+            return 0;
+        total += b;
+    }
+    return total;
+}
+
+// One repack or unpack of experts at their own depths, back to back.
+static smoe_status mixed_pass(bool repack, const uint8_t *const *codes, const uint16_t *const *scales,
+                              int32_t d, int32_t f, int32_t n, const uint8_t *expert_bits,
+                              int group_size, const void *tiles_in, void *tiles_out,
+                              size_t tiles_bytes, void *cuda_stream)
+{
+    if (n < 0 || group_size != SMOE_GROUP_SIZE || d <= 0 || d % 128 || f <= 0 || f % 64)
+        return SMOE_ERR_INVALID_ARG;
+    if (n == 0)
+        return SMOE_OK;
+    if (!expert_bits || !codes || !scales || !(repack ? tiles_out : tiles_in) ||
+        !aligned(repack ? tiles_out : tiles_in, 16))
+        return SMOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 3 * n; ++i) {
+        const int bits = expert_bits[i / 3];
+        if ((bits != 2 && bits != 4) || !codes[i] || !scales[i] || !aligned(scales[i], 2) ||
+            !aligned(codes[i], bits == 4 ? 8 : 4))
+            return SMOE_ERR_INVALID_ARG;
+    }
+    if (repack && tiles_bytes < smoe_repacked_bytes_mixed(d, f, n, expert_bits, group_size))
+        return SMOE_ERR_WORKSPACE;
+    if (!device_supported())
+        return SMOE_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    int64_t off = 0;
+    for (int e = 0; e < n; ++e) {
+        const int bits = expert_bits[e];
+        const int64_t gu = gateup_bytes(d, f, bits);
+        for (int kind = 0; kind < 3; ++kind) {
+            const int R = kind < 2 ? f : d, K = kind < 2 ? d : f;
+            const cudaError_t ce =
+                repack ? launch_repack(codes[3 * e + kind], scales[3 * e + kind], kind, R, K, bits,
+                                       static_cast<uint8_t *>(tiles_out) + off, gu, s)
+                       : launch_unpack(static_cast<const uint8_t *>(tiles_in) + off, kind, R, K,
+                                       bits, gu, const_cast<uint8_t *>(codes[3 * e + kind]),
+                                       const_cast<uint16_t *>(scales[3 * e + kind]), s);
+            if (ce != cudaSuccess)
+                return SMOE_ERR_CUDA;
+        }
+        off += expert_bytes(d, f, bits);
+    }
+    return SMOE_OK;
+}
+
+smoe_status smoe_repack_mixed(const uint8_t *const *codes_lsb, const uint16_t *const *scales_f16,
+                              int32_t d_model, int32_t ffn_dim, int32_t n_experts,
+                              const uint8_t *expert_bits, int group_size, void *tiles_out,
+                              size_t tiles_bytes, void *cuda_stream)
+{
+    return mixed_pass(true, codes_lsb, scales_f16, d_model, ffn_dim, n_experts, expert_bits,
+                      group_size, nullptr, tiles_out, tiles_bytes, cuda_stream);
+}
+
+smoe_status smoe_unpack_mixed(const void *tiles, int32_t d_model, int32_t ffn_dim,
+                              int32_t n_experts, const uint8_t *expert_bits, int group_size,
+                              uint8_t *const *codes_lsb, uint16_t *const *scales_f16,
+                              void *cuda_stream)
+{
+    return mixed_pass(false, const_cast<const uint8_t *const *>(codes_lsb),
+                      const_cast<const uint16_t *const *>(scales_f16), d_model, ffn_dim, n_experts,
+                      expert_bits, group_size, tiles, nullptr, 0, cuda_stream);
+}
+
+size_t smoe_moe_workspace_bytes_mixed(const smoe_layer_desc *layer, int64_t num_tokens)
+{
+    if (!valid_layer(layer) || num_tokens < 0)
+        return 0;
+    return make_plan(layer, num_tokens, true).total;
+}
+
+smoe_status smoe_moe_forward_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
+                                   const smoe_router_opts *opts, const void *x, smoe_dtype x_dtype,
+                                   int64_t num_tokens, float *y, void *workspace,
+                                   size_t workspace_bytes, int32_t *ids_out, float *w_out,
+                                   void *cuda_stream)
+{
+    if (!expert_bits)
+        return SMOE_ERR_INVALID_ARG;
+    return forward_stages(layer, opts, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
+                          ids_out, w_out, 7, SMOE_PATH_GROUPED, cuda_stream, expert_bits);
+}
+
+smoe_status smoe_moe_forward_stage_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
+                                         const void *x, smoe_dtype x_dtype, int64_t num_tokens,
+                                         float *y, void *workspace, size_t workspace_bytes,
+                                         int32_t *ids_out, float *w_out, int stage,
+                                         void *cuda_stream)
+{
+    if (!expert_bits || stage < 0 || stage > 2)
+        return SMOE_ERR_INVALID_ARG;
+    return forward_stages(layer, nullptr, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
+                          ids_out, w_out, 1 << stage, SMOE_PATH_GROUPED, cuda_stream, expert_bits);
 }
 
 smoe_status smoe_get_device_status(void *cuda_stream)

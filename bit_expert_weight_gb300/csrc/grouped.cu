@@ -218,6 +218,44 @@ struct Item {
     int seg, nt, nm, row0, nvalid0, nvalid1;
 };
 
+// Word w of the Q4-expert mask (constant indices only: the arguments stay
+// in parameter space).
+__device__ __forceinline__ uint32_t q4_word(const GroupedArgs &a, int w)
+{
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v = i == w ? a.q4mask[i] : v;
+    return v;
+}
+
+// Bit depth of segment s (the shared expert: the layer's depth).
+__device__ __forceinline__ int seg_bits(const GroupedArgs &a, int s)
+{
+    if (!a.mixed || s >= a.E)
+        return a.bits;
+    return (q4_word(a, s >> 5) >> (s & 31)) & 1u ? 4 : 2;
+}
+
+// Byte offset of routed expert s in the bank: with mixed depths, the Q2
+// size of every expert before s plus the Q4 surplus of the Q4 ones.
+__device__ __forceinline__ int64_t routed_offset(const GroupedArgs &a, int s)
+{
+    if (!a.mixed)
+        return (int64_t)s * a.expert_bytes_routed;
+    int n4 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t m = a.q4mask[i];
+        if (i < (s >> 5))
+            n4 += __popc(m);
+        else if (i == (s >> 5))
+            n4 += __popc(m & ((1u << (s & 31)) - 1u));
+    }
+    const int64_t tiles = 3ll * a.d * a.f / 1024;
+    return tiles * ((int64_t)s * tile_bytes(2) + (int64_t)n4 * (tile_bytes(4) - tile_bytes(2)));
+}
+
 template <int PHASE>
 __device__ __forceinline__ int seg_ntiles(const GroupedArgs &a, int s)
 {
@@ -274,8 +312,9 @@ struct CodeSrc {
         const bool routed = w.seg < a.E;
         fsg = routed ? a.f : a.fs;
         d = a.d;
-        wb = routed ? a.tiles_routed + (int64_t)w.seg * a.expert_bytes_routed : a.tiles_shared;
-        down_off = routed ? a.down_off_routed : a.down_off_shared;
+        // an item only reaches the instance of its segment's depth (BITS)
+        wb = routed ? a.tiles_routed + routed_offset(a, w.seg) : a.tiles_shared;
+        down_off = routed ? 2ll * a.d * a.f / 1024 * tile_bytes(BITS) : a.down_off_shared;
         nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
         r0 = (PHASE == 0 ? 128 * w.nt : kGN * w.nt) / 16;  // first strip
         const int nstrips = PHASE == 0 ? fsg / 16 : a.d / 16;
@@ -659,7 +698,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 }
                 sm.cnt[s] = c;
                 sm.off[s] = o;
-                items = seg_items<PAIR>(c) * seg_ntiles<PHASE>(a, s);
+                // segments of the other depth belong to the other instance
+                if (seg_bits(a, s) == BITS)
+                    items = seg_items<PAIR>(c) * seg_ntiles<PHASE>(a, s);
             }
             int incl = items;
 #pragma unroll
@@ -1182,27 +1223,35 @@ cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, cons
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
+    // pairs of m-tiles once the experts average two or more
+    const bool pair = a.T * a.k >= 2ll * kGM * a.E;
+    // the depths present: one GEMM instance per depth, each taking only the
+    // segments of its own depth
+    const bool layer_depth = !a.mixed || a.has_shared;  // a segment at a.bits
+    bool has4 = layer_depth && a.bits == 4, has2 = layer_depth && a.bits == 2;
+    if (a.mixed)
+        for (int ex = 0; ex < a.E; ++ex)
+            ((a.q4mask[ex >> 5] >> (ex & 31)) & 1u ? has4 : has2) = true;
     if (stage_mask & 2) {  // gate/up GEMM + SiLU(g) * u
         CUtensorMap mx;
         if (!make_map(&mx, a.xs, a.rows, a.d))
             return cudaErrorInvalidValue;
-        // pairs of m-tiles once the experts average two or more
-        const bool pair = a.T * a.k >= 2ll * kGM * a.E;
-        if ((e = a.bits == 4 ? (pair ? launch_gemm_t<4, 0, true>(a, mx, s)
-                                     : launch_gemm_t<4, 0, false>(a, mx, s))
-                             : (pair ? launch_gemm_t<2, 0, true>(a, mx, s)
-                                     : launch_gemm_t<2, 0, false>(a, mx, s))) != cudaSuccess)
+        if (has4 && (e = pair ? launch_gemm_t<4, 0, true>(a, mx, s)
+                              : launch_gemm_t<4, 0, false>(a, mx, s)) != cudaSuccess)
+            return e;
+        if (has2 && (e = pair ? launch_gemm_t<2, 0, true>(a, mx, s)
+                              : launch_gemm_t<2, 0, false>(a, mx, s)) != cudaSuccess)
             return e;
     }
     if (stage_mask & 4) {  // down GEMM + combine
         CUtensorMap mh;
         if (!make_map(&mh, a.h, a.rows, a.hstride))
             return cudaErrorInvalidValue;
-        const bool pair = a.T * a.k >= 2ll * kGM * a.E;
-        if ((e = a.bits == 4 ? (pair ? launch_gemm_t<4, 1, true>(a, mh, s)
-                                     : launch_gemm_t<4, 1, false>(a, mh, s))
-                             : (pair ? launch_gemm_t<2, 1, true>(a, mh, s)
-                                     : launch_gemm_t<2, 1, false>(a, mh, s))) != cudaSuccess)
+        if (has4 && (e = pair ? launch_gemm_t<4, 1, true>(a, mh, s)
+                              : launch_gemm_t<4, 1, false>(a, mh, s)) != cudaSuccess)
+            return e;
+        if (has2 && (e = pair ? launch_gemm_t<2, 1, true>(a, mh, s)
+                              : launch_gemm_t<2, 1, false>(a, mh, s)) != cudaSuccess)
             return e;
         grouped_combine_kernel<<<nt, 256, 0, s>>>(a.o, a.T, a.d, a.k, a.has_shared, a.rows_of,
                                                   a.rows, w, sw, y);

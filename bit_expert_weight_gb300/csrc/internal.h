@@ -147,7 +147,7 @@ struct GroupedArgs {
     const uint8_t *tiles_routed;   // bank base
     const uint8_t *tiles_shared;   // nullable
     int64_t expert_bytes_routed;
-    int64_t down_off_routed, down_off_shared;
+    int64_t down_off_shared;
     int64_t T;
     int d, f, fs, E, k, bits, has_shared;
     int32_t *seg;                  // [nseg+1] first rows, then [nseg] counts
@@ -162,6 +162,12 @@ struct GroupedArgs {
     int hstride;                   // max(f, fs)
     float *o;                      // [rows][d]
     int *status;
+    // mixed bit depth per routed expert: bit e of q4mask set = expert e is
+    // Q4, clear = Q2; the bank holds the experts back to back at their own
+    // sizes.  mixed = 0: every expert at `bits`, expert_bytes_routed apart.
+    // The shared expert is at `bits` in both cases.
+    int mixed;
+    uint32_t q4mask[8];
 };
 
 // Token batches from this size on may take the grouped path (the workspace

@@ -34,6 +34,8 @@ EXPORTED = [
     "smoe_moe_forward_noalloc", "smoe_moe_forward_path", "smoe_moe_path",
     "smoe_vault_parse", "smoe_vault_find_expert", "smoe_vault_repack_layer",
     "smoe_route_from_logits_ex", "smoe_moe_forward_ex",
+    "smoe_repacked_bytes_mixed", "smoe_repack_mixed", "smoe_unpack_mixed",
+    "smoe_moe_workspace_bytes_mixed", "smoe_moe_forward_mixed", "smoe_moe_forward_stage_mixed",
 ]
 
 # Execution paths (SMOE_PATH_* in include/smoe.h).
@@ -160,6 +162,21 @@ def load(path: str | None = None):
     L.smoe_vault_repack_layer.argtypes = [P, S, P, ctypes.c_uint64, ctypes.c_uint32,
                                           ctypes.c_uint32, P, S, P]
     L.smoe_vault_repack_layer.restype = I
+    U8P = ctypes.POINTER(ctypes.c_uint8)
+    L.smoe_repacked_bytes_mixed.argtypes = [I32, I32, I32, U8P, I]
+    L.smoe_repacked_bytes_mixed.restype = S
+    L.smoe_repack_mixed.argtypes = [P, P, I32, I32, I32, U8P, I, P, S, P]
+    L.smoe_repack_mixed.restype = I
+    L.smoe_unpack_mixed.argtypes = [P, I32, I32, I32, U8P, I, P, P, P]
+    L.smoe_unpack_mixed.restype = I
+    L.smoe_moe_workspace_bytes_mixed.argtypes = [ctypes.POINTER(LayerDesc), I64]
+    L.smoe_moe_workspace_bytes_mixed.restype = S
+    L.smoe_moe_forward_mixed.argtypes = [ctypes.POINTER(LayerDesc), U8P, RP, P, I, I64, P, P, S,
+                                         P, P, P]
+    L.smoe_moe_forward_mixed.restype = I
+    L.smoe_moe_forward_stage_mixed.argtypes = [ctypes.POINTER(LayerDesc), U8P, P, I, I64, P, P,
+                                               S, P, P, I, P]
+    L.smoe_moe_forward_stage_mixed.restype = I
     L.smoe_get_device_status.argtypes = [P]
     L.smoe_get_device_status.restype = I
     _lib = L
@@ -212,6 +229,17 @@ def repacked_bytes(d, f, n_experts, bits, group_size=64):
     return int(load().smoe_repacked_bytes(d, f, n_experts, bits, group_size))
 
 
+def _bits_array(expert_bits):
+    """Per-expert depths as a host uint8 array (kept alive by the caller)."""
+    vals = [int(b) for b in expert_bits]
+    return (ctypes.c_uint8 * max(len(vals), 1))(*vals)
+
+
+def repacked_bytes_mixed(d, f, expert_bits, group_size=64):
+    eb = _bits_array(expert_bits)
+    return int(load().smoe_repacked_bytes_mixed(d, f, len(expert_bits), eb, group_size))
+
+
 # ------------------------------------------------------------------ quantise
 
 def quantize(w_bf16: torch.Tensor, bits: int, codes=None, scales=None, stream=None):
@@ -243,6 +271,35 @@ def repack(codes: list, scales: list, d: int, f: int, n_experts: int, bits: int,
                               _ptr(out), out.numel() * out.element_size(), _stream(stream)),
            "smoe_repack")
     return out
+
+
+def repack_mixed(codes: list, scales: list, d: int, f: int, expert_bits, out=None, stream=None):
+    """smoe_repack_mixed: expert e's streams at depth expert_bits[e]."""
+    n = len(expert_bits)
+    eb = _bits_array(expert_bits)
+    nbytes = repacked_bytes_mixed(d, f, expert_bits)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=codes[0].device)
+    _check(load().smoe_repack_mixed(_ptr_array(codes), _ptr_array(scales), d, f, n, eb, 64,
+                                    _ptr(out), out.numel() * out.element_size(), _stream(stream)),
+           "smoe_repack_mixed")
+    return out
+
+
+def unpack_mixed(tiles, d: int, f: int, expert_bits, stream=None):
+    """smoe_unpack_mixed: returns (codes list, scales list) of 3*E tensors."""
+    dev = tiles.device
+    codes, scales = [], []
+    for b in expert_bits:
+        for kind in range(3):
+            R, K = (f, d) if kind < 2 else (d, f)
+            codes.append(torch.empty(stream_bytes(R, K, int(b)), dtype=torch.uint8, device=dev))
+            scales.append(torch.empty(R * K // 64, dtype=torch.int16, device=dev))
+    eb = _bits_array(expert_bits)
+    _check(load().smoe_unpack_mixed(_ptr(tiles), d, f, len(expert_bits), eb, 64,
+                                    _ptr_array(codes), _ptr_array(scales), _stream(stream)),
+           "smoe_unpack_mixed")
+    return codes, scales
 
 
 def unpack(tiles, d: int, f: int, n_experts: int, bits: int, stream=None):
@@ -299,8 +356,12 @@ class MoELayer:
     """Holds one layer's device tensors and its smoe_layer_desc."""
 
     def __init__(self, d, f, E, k, norm, bits, router_w, expert_tiles, expert_bias=None,
-                 shared_tiles=None, shared_f=0, shared_gate_w=None):
+                 shared_tiles=None, shared_f=0, shared_gate_w=None, expert_bits=None):
+        """expert_bits: per-expert depths of a bank written by repack_mixed
+        (then `bits` is the shared expert's depth); None = all at `bits`."""
         self.d, self.f, self.E, self.k, self.norm, self.bits = d, f, E, k, bool(norm), bits
+        self.expert_bits = None if expert_bits is None else [int(b) for b in expert_bits]
+        self._ebits = None if expert_bits is None else _bits_array(expert_bits)
         self.router_w, self.expert_tiles, self.expert_bias = router_w, expert_tiles, expert_bias
         self.shared_tiles, self.shared_f, self.shared_gate_w = shared_tiles, shared_f, shared_gate_w
         self.desc = LayerDesc(
@@ -310,7 +371,10 @@ class MoELayer:
             shared_f, None if shared_gate_w is None else shared_gate_w.data_ptr())
 
     def workspace_bytes(self, T: int) -> int:
-        n = int(load().smoe_moe_workspace_bytes(ctypes.byref(self.desc), T))
+        if self.expert_bits is not None:
+            n = int(load().smoe_moe_workspace_bytes_mixed(ctypes.byref(self.desc), T))
+        else:
+            n = int(load().smoe_moe_workspace_bytes(ctypes.byref(self.desc), T))
         if n == 0 and T >= 0:
             raise SmoeError(-1, "smoe_moe_workspace_bytes")
         return n
@@ -339,7 +403,14 @@ def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None
     if x.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("x must be fp32 or bf16")
     o = _opts(router_sigmoid, routed_scaling_factor, expert_mask)
-    if o is not None:
+    if layer.expert_bits is not None:
+        if path not in (None, PATH_GROUPED, PATH_AUTO):
+            raise ValueError("a layer with per-expert depths runs the grouped path only")
+        _check(load().smoe_moe_forward_mixed(ctypes.byref(layer.desc), layer._ebits,
+                                             None if o is None else ctypes.byref(o), _ptr(x), dt,
+                                             T, _ptr(y), _ptr(ws), ws.numel(), _ptr(ids),
+                                             _ptr(w), _stream(stream)), "smoe_moe_forward_mixed")
+    elif o is not None:
         _check(load().smoe_moe_forward_ex(ctypes.byref(layer.desc), ctypes.byref(o), _ptr(x), dt,
                                           T, _ptr(y), _ptr(ws), ws.numel(), _ptr(ids), _ptr(w),
                                           PATH_AUTO if path is None else int(path),
@@ -356,13 +427,18 @@ def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None
 
 
 def path_for(layer: MoELayer, T: int) -> int:
-    """smoe_moe_path: the execution path smoe_moe_forward takes at T tokens."""
+    """smoe_moe_path: the execution path smoe_moe_forward takes at T tokens
+    (a layer with per-expert depths: always the grouped path)."""
+    if layer.expert_bits is not None:
+        return PATH_GROUPED
     return int(load().smoe_moe_path(ctypes.byref(layer.desc), T))
 
 
 def forward_noalloc(layer: MoELayer, x: torch.Tensor, y=None, ids=None, w=None, stream=None):
     """smoe_moe_forward_noalloc: the forward with the library's built-in
     workspace (no workspace argument; calls on one device must not overlap)."""
+    if layer.expert_bits is not None:
+        raise ValueError("smoe_moe_forward_noalloc takes layers of one depth only")
     T = x.shape[0]
     if y is None:
         y = torch.empty((T, layer.d), dtype=torch.float32, device=x.device)
@@ -377,8 +453,15 @@ def forward_noalloc(layer: MoELayer, x: torch.Tensor, y=None, ids=None, w=None, 
 
 def forward_stage(layer: MoELayer, stage: int, x: torch.Tensor, ws: torch.Tensor, y: torch.Tensor,
                   ids=None, w=None, stream=None):
-    """smoe_moe_forward_stage: one of the forward's three launch stages."""
+    """smoe_moe_forward_stage (smoe_moe_forward_stage_mixed for a layer with
+    per-expert depths): one of the forward's three launch stages."""
     dt = SMOE_BF16 if x.dtype == torch.bfloat16 else SMOE_F32
+    if layer.expert_bits is not None:
+        _check(load().smoe_moe_forward_stage_mixed(ctypes.byref(layer.desc), layer._ebits, _ptr(x),
+                                                   dt, x.shape[0], _ptr(y), _ptr(ws), ws.numel(),
+                                                   _ptr(ids), _ptr(w), stage, _stream(stream)),
+               f"smoe_moe_forward_stage_mixed({stage})")
+        return y
     _check(load().smoe_moe_forward_stage(ctypes.byref(layer.desc), _ptr(x), dt, x.shape[0],
                                          _ptr(y), _ptr(ws), ws.numel(), _ptr(ids), _ptr(w), stage,
                                          _stream(stream)), f"smoe_moe_forward_stage({stage})")

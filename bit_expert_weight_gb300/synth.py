@@ -210,6 +210,13 @@ class Workload:
                 hi = mid
         return mid, sh, target
 
+    def mixed_bits(self, q4_share=0.25):
+        """Per-expert depths of a mixed layer: the round(q4_share * E) most
+        popular experts (zipf_ranks) at Q4, the others at Q2 -- more bits
+        where the router sends more tokens."""
+        n4 = int(round(q4_share * self.E))
+        return [4 if int(r) <= n4 else 2 for r in self.zipf_ranks()]
+
     def activations(self, layer, T, start_token=0):
         """x [T, d]: fp32 values (bf16-rounded when x_dtype == 'bf16').
 

@@ -110,6 +110,13 @@ size_t smoe_expert_tiles_bytes(int32_t d_model, int32_t ffn_dim, int bits, int g
 size_t smoe_repacked_bytes(int32_t d_model, int32_t ffn_dim, int32_t n_experts, int bits,
                            int group_size);
 
+/* Bytes of a bank whose experts each have their own depth ("CMF v2", 2.2
+ * MoE: every expert declares its own dtype): the sum of
+ * smoe_expert_tiles_bytes(d, f, expert_bits[e], 64).  expert_bits is a HOST
+ * array of n_experts entries, each 2 or 4.  0 on bad args. */
+size_t smoe_repacked_bytes_mixed(int32_t d_model, int32_t ffn_dim, int32_t n_experts,
+                                 const uint8_t *expert_bits, int group_size);
+
 /* ----------------------------------------------------------- quantiser */
 
 /* L2-MSE grid-search quantisation of a bf16 [rows, cols] tensor
@@ -154,6 +161,23 @@ smoe_status smoe_repack(const uint8_t *const *codes_lsb, const uint16_t *const *
 smoe_status smoe_unpack(const void *tiles, int32_t d_model, int32_t ffn_dim, int32_t n_experts,
                         int bits, int group_size, uint8_t *const *codes_lsb,
                         uint16_t *const *scales_f16, void *cuda_stream);
+
+/* smoe_repack of a bank whose experts each have their own depth:
+ * expert_bits is a HOST array of n_experts entries (2 = SMOE-Q2, 4 =
+ * SMOE-Q4); expert e's streams are at its depth and its tiles follow
+ * expert e-1's, at offset sum_{j<e} smoe_expert_tiles_bytes(d, f,
+ * expert_bits[j], 64).  tiles_out: smoe_repacked_bytes_mixed(...) bytes.
+ * Errors as smoe_repack (an entry that is not 2 or 4: SMOE_ERR_INVALID_ARG). */
+smoe_status smoe_repack_mixed(const uint8_t *const *codes_lsb, const uint16_t *const *scales_f16,
+                              int32_t d_model, int32_t ffn_dim, int32_t n_experts,
+                              const uint8_t *expert_bits, int group_size, void *tiles_out,
+                              size_t tiles_bytes, void *cuda_stream);
+
+/* Exact inverse of smoe_repack_mixed. */
+smoe_status smoe_unpack_mixed(const void *tiles, int32_t d_model, int32_t ffn_dim,
+                              int32_t n_experts, const uint8_t *expert_bits, int group_size,
+                              uint8_t *const *codes_lsb, uint16_t *const *scales_f16,
+                              void *cuda_stream);
 
 /* ------------------------------------------------------------ .smoe vault */
 
@@ -342,6 +366,35 @@ smoe_status smoe_moe_forward_ex(const smoe_layer_desc *layer, const smoe_router_
                                 const void *x, smoe_dtype x_dtype, int64_t num_tokens, float *y,
                                 void *workspace, size_t workspace_bytes, int32_t *ids_out,
                                 float *w_out, int path, void *cuda_stream);
+
+/* Workspace bytes of smoe_moe_forward_mixed for this layer and token count
+ * (0 on invalid arguments). */
+size_t smoe_moe_workspace_bytes_mixed(const smoe_layer_desc *layer, int64_t num_tokens);
+
+/* The forward of a layer whose routed experts each have their own depth
+ * (some SMOE-Q2, some SMOE-Q4).  layer->expert_tiles is a bank written by
+ * smoe_repack_mixed with the same expert_bits (HOST array of num_experts
+ * entries, each 2 or 4; read during the call, not kept); layer->bits is the
+ * shared expert's depth.  Each expert decodes its own levels (L = 7.5 or
+ * 1.5); otherwise the same computation as smoe_moe_forward_ex.  It always
+ * takes the grouped path, at every token count: one GEMM launch per depth
+ * present for gate/up and again for down, each taking the experts of its
+ * own depth.  workspace: >= smoe_moe_workspace_bytes_mixed.  Errors as
+ * smoe_moe_forward_ex (expert_bits null or an entry not 2 or 4:
+ * SMOE_ERR_INVALID_ARG). */
+smoe_status smoe_moe_forward_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
+                                   const smoe_router_opts *opts, const void *x, smoe_dtype x_dtype,
+                                   int64_t num_tokens, float *y, void *workspace,
+                                   size_t workspace_bytes, int32_t *ids_out, float *w_out,
+                                   void *cuda_stream);
+
+/* smoe_moe_forward_mixed (without router options) one launch stage at a
+ * time, the stages of the grouped path as in smoe_moe_forward_stage. */
+smoe_status smoe_moe_forward_stage_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
+                                         const void *x, smoe_dtype x_dtype, int64_t num_tokens,
+                                         float *y, void *workspace, size_t workspace_bytes,
+                                         int32_t *ids_out, float *w_out, int stage,
+                                         void *cuda_stream);
 
 /* The path smoe_moe_forward takes for this layer and token count
  * (SMOE_PATH_STREAM or SMOE_PATH_GROUPED), or -1 on invalid arguments. */

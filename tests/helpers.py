@@ -25,15 +25,19 @@ def to_dev(a, dev):
 class HostLayer:
     """Seeded weights of one layer, quantised by the oracle."""
 
-    def __init__(self, wl: Y.Workload, layer: int, bits: int, experts=None):
+    def __init__(self, wl: Y.Workload, layer: int, bits: int, experts=None, expert_bits=None):
+        """expert_bits: per-expert depths (a mixed layer; `bits` is then the
+        shared expert's depth)."""
         self.wl, self.layer, self.bits = wl, layer, bits
         self.d, self.f, self.E, self.k = wl.d, wl.f, wl.E, wl.k
         self.router = wl.router_weight(layer)
         self.experts = list(range(wl.E)) if experts is None else list(experts)
+        self.expert_bits = None if expert_bits is None else [int(b) for b in expert_bits]
         self.q = {}      # expert -> [q_gate, q_up, q_down] (oracle quantised)
         self.blob = {}
         for e in self.experts:
-            qs = [O.quantize(wl.expert_weight(layer, e, r), bits) for r in ROLES]
+            be = bits if expert_bits is None else self.expert_bits[e]
+            qs = [O.quantize(wl.expert_weight(layer, e, r), be) for r in ROLES]
             self.q[e] = qs
             self.blob[e] = O.make_blob(*qs)
         self.shared_blob = None
@@ -53,7 +57,10 @@ class HostLayer:
             for q in self.q[e]:
                 codes.append(to_dev(q["codes_lsb"], dev))
                 scales.append(to_dev(q["scales_f16"].view(np.int16), dev))
-        tiles = S.repack(codes, scales, self.d, self.f, self.E, self.bits)
+        if self.expert_bits is None:
+            tiles = S.repack(codes, scales, self.d, self.f, self.E, self.bits)
+        else:
+            tiles = S.repack_mixed(codes, scales, self.d, self.f, self.expert_bits)
         sh_tiles, sh_gate = None, None
         if self.shared_blob is not None:
             sc = [to_dev(q["codes_lsb"], dev) for q in self.q["shared"]]
@@ -64,20 +71,21 @@ class HostLayer:
         bias_t = None if expert_bias is None else to_dev(expert_bias.astype(np.float32), dev)
         lay = S.MoELayer(self.d, self.f, self.E, self.k, self.wl.norm, self.bits,
                          to_dev_bf16(self.router, dev), tiles, expert_bias=bias_t,
-                         shared_tiles=sh_tiles, shared_f=self.wl.shared_f, shared_gate_w=sh_gate)
+                         shared_tiles=sh_tiles, shared_f=self.wl.shared_f, shared_gate_w=sh_gate,
+                         expert_bits=self.expert_bits)
         lay._keep = (codes, scales)
         return lay
 
-    def oracle_forward(self, x, expert_bias=None):
+    def oracle_forward(self, x, expert_bias=None, **router):
         return O.moe_forward(self.d, self.f, self.E, self.k, self.wl.norm, self.bits,
                              self.router, self.blob, x, expert_bias=expert_bias,
                              shared_blob=self.shared_blob, fs=self.wl.shared_f,
-                             shared_gate=self.shared_gate)
+                             shared_gate=self.shared_gate, expert_bits=self.expert_bits, **router)
 
     def oracle_apply(self, x, ids, w):
         return O.moe_apply(self.d, self.f, self.E, self.k, self.bits, self.blob, x, ids, w,
                            shared_blob=self.shared_blob, fs=self.wl.shared_f,
-                           shared_gate=self.shared_gate)
+                           shared_gate=self.shared_gate, expert_bits=self.expert_bits)
 
 
 def near_tie_tokens(logits, k, bias=None, rel=1e-5):

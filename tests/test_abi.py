@@ -198,3 +198,42 @@ def test_routing_mask_is_validated_on_the_host(libs):
     o = S._opts(False, 1.0, bytes([0b00000011, 0b00000010]))  # bit 9: valid (3 routable)
     assert L.smoe_route_from_logits_ex(P(4096), 0, 10, 2, 1, None, ctypes.byref(o), None, None,
                                        None) == 0
+
+
+def test_mixed_depth_entry_points_validate_on_the_host(libs):
+    """Per-expert depths: sizes are the sum of each expert's own size; a
+    depth that is not 2 or 4, or no depth array, is refused before anything
+    is launched; the mixed forward's workspace holds the grouped buffers at
+    every token count."""
+    S, _ = libs
+    L = S.load()
+    P = ctypes.c_void_p
+    q4, q2 = S.expert_tiles_bytes(256, 128, 4), S.expert_tiles_bytes(256, 128, 2)
+    assert S.repacked_bytes_mixed(256, 128, [4, 2, 2, 4, 2]) == 2 * q4 + 3 * q2
+    assert S.repacked_bytes_mixed(256, 128, [4] * 3) == S.repacked_bytes(256, 128, 3, 4)
+    assert S.repacked_bytes_mixed(256, 128, [4, 3]) == 0
+    assert S.repacked_bytes_mixed(192, 128, [4, 2]) == 0
+    assert L.smoe_repacked_bytes_mixed(256, 128, 2, None, 64) == 0
+    desc = _desc(S)  # E = 8, k = 2
+    good = S._bits_array([4, 2] * 4)
+    bad = S._bits_array([4, 2, 2, 4, 8, 2, 4, 4])
+    arr = (P * 24)(*([4096] * 24))
+    assert L.smoe_repack_mixed(arr, arr, 256, 128, 8, bad, 64, P(4096), 1 << 20, None) == -1
+    assert L.smoe_repack_mixed(arr, arr, 256, 128, 8, None, 64, P(4096), 1 << 20, None) == -1
+    assert L.smoe_repack_mixed(arr, arr, 256, 128, 8, good, 64, P(4096), 16, None) == -3
+    assert L.smoe_repack_mixed(arr, arr, 256, 128, 8, good, 64, P(4100), 1 << 20, None) == -1
+    assert L.smoe_unpack_mixed(P(4096), 256, 128, 8, bad, 64, arr, arr, None) == -1
+    for eb in (bad, None):
+        assert L.smoe_moe_forward_mixed(ctypes.byref(desc), eb, None, P(4096), 0, 4, P(8192),
+                                        P(1 << 20), 1 << 30, None, None, None) == -1
+        assert L.smoe_moe_forward_stage_mixed(ctypes.byref(desc), eb, P(4096), 0, 4, P(8192),
+                                              P(1 << 20), 1 << 30, None, None, 0, None) == -1
+    assert L.smoe_moe_forward_stage_mixed(ctypes.byref(desc), good, P(4096), 0, 4, P(8192),
+                                          P(1 << 20), 1 << 30, None, None, 3, None) == -1
+    assert L.smoe_moe_forward_mixed(ctypes.byref(desc), good, None, None, 0, 0, None, None, 0,
+                                    None, None, None) == 0                      # T = 0
+    w1 = L.smoe_moe_workspace_bytes_mixed(ctypes.byref(desc), 1)
+    assert w1 > L.smoe_moe_workspace_bytes(ctypes.byref(desc), 1)
+    assert w1 >= 128 * (256 * 2 + 128 * 2 + 256 * 4)      # one padded 128-row tile per segment
+    assert L.smoe_moe_workspace_bytes_mixed(ctypes.byref(desc), 64) == \
+        L.smoe_moe_workspace_bytes(ctypes.byref(desc), 64)

@@ -58,9 +58,13 @@ class FullLayer:
     """One full-geometry layer: oracle-quantised experts for the sampled
     tokens' selections, device-quantised experts elsewhere."""
 
-    def __init__(self, S, pool, wl_name, layer, bits, sample, bias=None):
+    def __init__(self, S, pool, wl_name, layer, bits, sample, bias=None, expert_bits=None):
+        """expert_bits: per-expert depths (a mixed layer; `bits` is then the
+        shared expert's depth)."""
         wl = Y.WORKLOADS[wl_name]
         self.wl, self.layer, self.bits, self.sample, self.bias = wl, layer, bits, list(sample), bias
+        self.expert_bits = None if expert_bits is None else [int(b) for b in expert_bits]
+        bits_of = (lambda e: bits) if expert_bits is None else (lambda e: self.expert_bits[e])
         self.router = wl.router_weight(layer)
         xs = np.stack([wl.activations(layer, 1, start_token=t)[0][0] for t in self.sample])
         self.x_sample = xs
@@ -68,7 +72,7 @@ class FullLayer:
         ids, _ = O.route(lg, wl.k, wl.norm, bias)
         self.logits = lg
         chosen = sorted(set(int(e) for e in np.asarray(ids).ravel()))
-        jobs = [(wl_name, layer, e, bits) for e in chosen]
+        jobs = [(wl_name, layer, e, bits_of(e)) for e in chosen]
         if wl.shared_f:
             jobs.append((wl_name, layer, Y.SHARED_EXPERT, bits))
         got = dict(pool.map(_oracle_expert, jobs))
@@ -87,10 +91,13 @@ class FullLayer:
                     codes.append(to_dev(c, DEV))
                     scales.append(to_dev(s.view(np.int16), DEV))
                 else:
-                    c, s = self._device_quantised(S, e, r)
+                    c, s = self._device_quantised(S, e, r, bits_of(e))
                     codes.append(c)
                     scales.append(s)
-        tiles = S.repack(codes, scales, wl.d, wl.f, wl.E, bits)
+        if expert_bits is None:
+            tiles = S.repack(codes, scales, wl.d, wl.f, wl.E, bits)
+        else:
+            tiles = S.repack_mixed(codes, scales, wl.d, wl.f, self.expert_bits)
         sh_tiles, sh_gate = None, None
         if wl.shared_f:
             sc = [to_dev(c, DEV) for c, _ in got[Y.SHARED_EXPERT]]
@@ -104,16 +111,16 @@ class FullLayer:
         bias_t = None if bias is None else to_dev(bias.astype(np.float32), DEV)
         self.lay = S.MoELayer(wl.d, wl.f, wl.E, wl.k, wl.norm, bits, to_dev_bf16(self.router, DEV),
                               tiles, expert_bias=bias_t, shared_tiles=sh_tiles, shared_f=wl.shared_f,
-                              shared_gate_w=sh_gate)
+                              shared_gate_w=sh_gate, expert_bits=self.expert_bits)
         del codes, scales
 
-    def _device_quantised(self, S, e, role):
+    def _device_quantised(self, S, e, role, bits):
         wl = self.wl
         rows, cols = (wl.f, wl.d) if role in (Y.ROLE_GATE, Y.ROLE_UP) else (wl.d, wl.f)
         w = torch.empty(rows * cols, dtype=torch.int16, device=DEV)
         S.synth_bf16(w, Y.stream_key(wl.seed, self.layer, e, role), wl.sigma, p_out=wl.p_out,
                      p_zero=wl.p_zero)
-        return S.quantize(w.view(torch.bfloat16).view(rows, cols), self.bits)
+        return S.quantize(w.view(torch.bfloat16).view(rows, cols), bits)
 
     def device_x(self, S, T):
         """x [T, d] bf16 on the device: the generator's device twin."""
@@ -149,7 +156,8 @@ class FullLayer:
                                                   self.router, self.blob, self.x_sample,
                                                   expert_bias=self.bias,
                                                   shared_blob=self.shared_blob, fs=wl.shared_f,
-                                                  shared_gate=self.shared_gate)
+                                                  shared_gate=self.shared_gate,
+                                                  expert_bits=self.expert_bits)
         ties = set(near_tie_tokens(lg, wl.k, self.bias))
         mism = [i for i in range(len(self.sample)) if not np.array_equal(idg[i], ids_ref[i])]
         assert set(mism) <= ties, f"routing differs on non-tie sampled tokens {mism}"
@@ -198,3 +206,21 @@ def test_qwen235b_batched_zipf_full_size(S, pool):
     fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=[0, 5], bias=bias)
     for T in (8, 64, 512, 4096):
         fl.check(S, T)
+
+
+def test_qwen235b_batched_mixed_depth_full_size(S, pool):
+    """Mixed depths at the batched geometry: the 32 most popular experts
+    (Zipf rank) at Q4, the other 96 at Q2, with the Zipf selection bias;
+    T = 8, 64 and 4096 (the benchmark's batch), sampled."""
+    wl = Y.WORKLOADS["qwen235b_batched"]
+    fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=[0, 5], bias=wl.zipf_bias(),
+                   expert_bits=wl.mixed_bits(0.25))
+    for T in (4096, 64, 8):
+        fl.check(S, T)
+
+
+def test_a3b35b_mixed_depth_full_size(S, pool):
+    """256 experts at alternating depths and the gated shared expert at Q2."""
+    fl = FullLayer(S, pool, "a3b35b", 3, 2, sample=[0, 200],
+                   expert_bits=[4 if e % 2 == 0 else 2 for e in range(256)])
+    fl.check(S, 256)
