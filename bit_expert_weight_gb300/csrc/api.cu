@@ -484,8 +484,7 @@ static bool make_q4mask(const uint8_t *expert_bits, int E, uint32_t q4[8])
     return true;
 }
 
-// expert_bits: nullable host [E] per-expert depths (a mixed layer: grouped
-// path only, whatever `path` says).
+// expert_bits: nullable host [E] per-expert depths (a mixed layer).
 static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_router_opts *opts,
                                   const void *x, smoe_dtype x_dtype, int64_t num_tokens, float *y,
                                   void *workspace, size_t workspace_bytes, int32_t *ids_out,
@@ -511,7 +510,7 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const smoe_layer_desc &L = *layer;
     int *status = device_status_word();
-    const bool grouped = mixed || path == SMOE_PATH_GROUPED ||
+    const bool grouped = path == SMOE_PATH_GROUPED ||
                          (path == SMOE_PATH_AUTO && auto_grouped(layer, num_tokens));
     if (grouped && !P.grouped)
         return SMOE_ERR_UNSUPPORTED;
@@ -607,6 +606,10 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
     la.cta_flags = at<unsigned>(workspace, P.off_ctaflags);
     la.y = y;
     la.status = status;
+    if (mixed) {
+        la.mixed = 1;
+        memcpy(la.q4mask, q4mask, sizeof q4mask);
+    }
 
     if (grouped) {
         GroupedArgs ga;
@@ -803,13 +806,14 @@ size_t smoe_moe_workspace_bytes_mixed(const smoe_layer_desc *layer, int64_t num_
 smoe_status smoe_moe_forward_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
                                    const smoe_router_opts *opts, const void *x, smoe_dtype x_dtype,
                                    int64_t num_tokens, float *y, void *workspace,
-                                   size_t workspace_bytes, int32_t *ids_out, float *w_out,
+                                   size_t workspace_bytes, int32_t *ids_out, float *w_out, int path,
                                    void *cuda_stream)
 {
-    if (!expert_bits)
+    if (!expert_bits ||
+        (path != SMOE_PATH_AUTO && path != SMOE_PATH_STREAM && path != SMOE_PATH_GROUPED))
         return SMOE_ERR_INVALID_ARG;
     return forward_stages(layer, opts, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
-                          ids_out, w_out, 7, SMOE_PATH_GROUPED, cuda_stream, expert_bits);
+                          ids_out, w_out, 7, path, cuda_stream, expert_bits);
 }
 
 smoe_status smoe_moe_forward_stage_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
@@ -821,7 +825,7 @@ smoe_status smoe_moe_forward_stage_mixed(const smoe_layer_desc *layer, const uin
     if (!expert_bits || stage < 0 || stage > 2)
         return SMOE_ERR_INVALID_ARG;
     return forward_stages(layer, nullptr, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
-                          ids_out, w_out, 1 << stage, SMOE_PATH_GROUPED, cuda_stream, expert_bits);
+                          ids_out, w_out, 1 << stage, SMOE_PATH_AUTO, cuda_stream, expert_bits);
 }
 
 smoe_status smoe_get_device_status(void *cuda_stream)

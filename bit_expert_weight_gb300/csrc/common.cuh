@@ -28,6 +28,42 @@ constexpr int kTileRows = 16;
 __host__ __device__ constexpr int tile_code_bytes(int bits) { return bits * 128; }
 __host__ __device__ constexpr int tile_bytes(int bits) { return bits * 128 + 32; }
 
+// Banks whose experts each have their own depth: bit e of Args::q4mask
+// (8 words) set = expert e is Q4, clear = Q2; the experts lie back to back
+// at their own sizes (3 d f / 1024 tiles each).  Constant indices only, so
+// the mask stays in kernel parameter space.
+template <class Args>
+__device__ __forceinline__ uint32_t q4_word(const Args &a, int w)
+{
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v = i == w ? a.q4mask[i] : v;
+    return v;
+}
+template <class Args>
+__device__ __forceinline__ int mixed_expert_bits(const Args &a, int e)
+{
+    return (q4_word(a, e >> 5) >> (e & 31)) & 1u ? 4 : 2;
+}
+// Byte offset of expert e: the Q2 size of every expert before it plus the
+// Q4 surplus of the Q4 ones among them.
+template <class Args>
+__device__ __forceinline__ int64_t mixed_expert_offset(const Args &a, int e)
+{
+    int n4 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t m = a.q4mask[i];
+        if (i < (e >> 5))
+            n4 += __popc(m);
+        else if (i == (e >> 5))
+            n4 += __popc(m & ((1u << (e & 31)) - 1u));
+    }
+    const int64_t tiles = 3ll * a.d * a.f / 1024;
+    return tiles * ((int64_t)e * tile_bytes(2) + (int64_t)n4 * (tile_bytes(4) - tile_bytes(2)));
+}
+
 // Bit position, inside lane t's code word(s) of a tile, of the code for
 // W[row gq + 8*rh][column 16*tig + 4*j + e] (j = k-subtile 0..3, e = 0..3).
 // Q4: word j of the lane's four 32-bit words; register a_i (i = rh + 2*(e>>1))

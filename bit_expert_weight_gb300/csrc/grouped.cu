@@ -218,42 +218,16 @@ struct Item {
     int seg, nt, nm, row0, nvalid0, nvalid1;
 };
 
-// Word w of the Q4-expert mask (constant indices only: the arguments stay
-// in parameter space).
-__device__ __forceinline__ uint32_t q4_word(const GroupedArgs &a, int w)
-{
-    uint32_t v = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        v = i == w ? a.q4mask[i] : v;
-    return v;
-}
-
 // Bit depth of segment s (the shared expert: the layer's depth).
 __device__ __forceinline__ int seg_bits(const GroupedArgs &a, int s)
 {
-    if (!a.mixed || s >= a.E)
-        return a.bits;
-    return (q4_word(a, s >> 5) >> (s & 31)) & 1u ? 4 : 2;
+    return a.mixed && s < a.E ? mixed_expert_bits(a, s) : a.bits;
 }
 
-// Byte offset of routed expert s in the bank: with mixed depths, the Q2
-// size of every expert before s plus the Q4 surplus of the Q4 ones.
+// Byte offset of routed expert s in the bank.
 __device__ __forceinline__ int64_t routed_offset(const GroupedArgs &a, int s)
 {
-    if (!a.mixed)
-        return (int64_t)s * a.expert_bytes_routed;
-    int n4 = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t m = a.q4mask[i];
-        if (i < (s >> 5))
-            n4 += __popc(m);
-        else if (i == (s >> 5))
-            n4 += __popc(m & ((1u << (s & 31)) - 1u));
-    }
-    const int64_t tiles = 3ll * a.d * a.f / 1024;
-    return tiles * ((int64_t)s * tile_bytes(2) + (int64_t)n4 * (tile_bytes(4) - tile_bytes(2)));
+    return a.mixed ? mixed_expert_offset(a, s) : (int64_t)s * a.expert_bytes_routed;
 }
 
 template <int PHASE>

@@ -139,6 +139,11 @@ struct LayerArgs {
     unsigned *cta_flags;           // [max CTAs][32]: word 0 route go
     float *y;                      // [T, d]
     int *status;
+    // mixed bit depth per routed expert (as in GroupedArgs): the kernel
+    // instance for mixed banks takes each pair's depth from q4mask and the
+    // expert's place in the bank from the depths before it
+    int mixed;
+    uint32_t q4mask[8];
 };
 
 // The expert-sorted grouped path (grouped.cu): segments = the routed experts,

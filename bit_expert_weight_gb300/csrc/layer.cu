@@ -401,6 +401,9 @@ constexpr int kChunkGroups = 2 * kStreamWarps;
 constexpr int kDownGroupsMax = kChunkGroups;  // ffn_dim <= 2048
 
 __host__ __device__ constexpr int stage_bytes(int bits) { return kChunkGroups * 2 * tile_bytes(bits); }
+// Kernel instances: BITS = 4 or 2 for a bank of one depth, BITS = 0 for a
+// bank of mixed depths, whose ring is sized for Q4 stages.
+__host__ __device__ constexpr int ring_bits(int bits) { return bits == 0 ? 4 : bits; }
 // About 100 KB in flight per SM: the full HBM rate needs ~64 KB; deeper
 // rings delay every other memory access of the SM, which queues behind them.
 __host__ __device__ constexpr int num_stages(int bits) { return bits == 4 ? 3 : 5; }
@@ -566,6 +569,16 @@ __device__ __forceinline__ void producer_seek(const Geo *geo, Producer &pr)
     }
 }
 
+// Depth of the expert of a pair (e < 0: the shared expert, at the layer's
+// depth); a compile-time constant except in the mixed-depth instance.
+template <int BITS>
+__device__ __forceinline__ int pair_bits(const LayerArgs &a, int e)
+{
+    if (BITS != 0)
+        return BITS;
+    return e < 0 ? a.bits : mixed_expert_bits(a, e);
+}
+
 // Issue the next stage: 1 issued, 0 not now (slot still in use and
 // !block, or nothing left), -1 the bounded wait for the slot ran out.
 template <int BITS>
@@ -573,7 +586,7 @@ __device__ __forceinline__ int produce(const LayerArgs &a, const RouteView &rv, 
                                        Producer &pr, uint8_t *ring, uint64_t *full, uint64_t *empty,
                                        bool block)
 {
-    constexpr int NS = num_stages(BITS), SB = stage_bytes(BITS), TB = tile_bytes(BITS);
+    constexpr int NS = num_stages(ring_bits(BITS)), SB = stage_bytes(ring_bits(BITS));
     if (pr.phase > 1)
         return 0;
     const uint32_t j = pr.next;
@@ -589,13 +602,19 @@ __device__ __forceinline__ int produce(const LayerArgs &a, const RouteView &rv, 
     }
     const Geo &g = geo[pr.phase];
     const UnitGeo u = unit_geo(g, pr.q.p);
+    const int e = rv.pairs[pr.q.p * kPairInts];
+    const int TB = tile_bytes(pair_bits<BITS>(a, e));
     const int GB = pr.phase == 0 ? 2 * TB : TB;
     const int g0 = pr.q.c * u.gc;
     const int ng = min(u.gk - g0, u.gc);
-    const int e = rv.pairs[pr.q.p * kPairInts];
-    const uint8_t *base =
-        e >= 0 ? a.tiles_routed + (int64_t)e * a.expert_bytes_routed + (pr.phase ? a.down_off_routed : 0)
-               : a.tiles_shared + (pr.phase ? a.down_off_shared : 0);
+    const uint8_t *base;
+    if (e < 0)
+        base = a.tiles_shared + (pr.phase ? a.down_off_shared : 0);
+    else if (BITS != 0)
+        base = a.tiles_routed + (int64_t)e * a.expert_bytes_routed + (pr.phase ? a.down_off_routed : 0);
+    else  // the expert's own place and down offset in a bank of mixed depths
+        base = a.tiles_routed + mixed_expert_offset(a, e) +
+               (pr.phase ? 2ll * a.d * a.f / 1024 * TB : 0);
     const uint8_t *src = base + ((int64_t)pr.q.s * u.gk + g0) * GB;
     mbar_arrive_expect_tx(&full[slot], static_cast<unsigned>(ng * GB));
     bulk_g2s(ring + slot * SB, src, static_cast<unsigned>(ng * GB), &full[slot]);
@@ -646,8 +665,9 @@ __device__ __forceinline__ void finish_bias(BFrag &f, float2 x0, float2 x1)
             f.b1[j] = bf16x2_quarter(f.b1[j]);
             f.b1l[j] = bf16x2_quarter(f.b1l[j]);
         }
-        f.bias0 = -(129.5f * x0.x + 33.5f * x0.y);
-        f.bias1 = -(129.5f * x1.x + 33.5f * x1.y);
+        // one explicit fma: the same rounding in every kernel instance
+        f.bias0 = -fmaf(129.5f, x0.x, 33.5f * x0.y);
+        f.bias1 = -fmaf(129.5f, x1.x, 33.5f * x1.y);
     } else {
         f.bias0 = -(135.5f * (x0.x + x0.y));
         f.bias1 = -(135.5f * (x1.x + x1.y));
@@ -979,6 +999,33 @@ __device__ __forceinline__ bool unit_ends(const Geo &g, const UnitGeo &u, const 
     return q.c == u.ch - 1 || i == g.a1 - 1 || (g.ts < g.a1 && i == g.ts - 1);
 }
 
+// The warp's tiles of one stage (chunk c of the unit) at depth B:
+// branch-free over the warp's two groups (tiles of absent groups read
+// in-bounds stage bytes and are dropped), so the four (down: two) mma
+// chains of the step schedule together.
+template <int B, int PHASE, int KG, bool kSplit, int NB>
+__device__ __forceinline__ void step_tiles(const uint8_t *stage, const BFrag (&bf)[NB], int qc, bool g0,
+                                           bool g1, float (&accg)[4], float (&accu)[4],
+                                           float (&accg2)[4], float (&accu2)[4])
+{
+    constexpr int TB = tile_bytes(B), GB = PHASE == 0 ? 2 * TB : TB;
+    const int warp = threadIdx.x >> 5;
+    if (PHASE == 0) {
+#pragma unroll
+        for (int c = 0; c < KG; ++c) {
+            if (c == qc) {
+                mac_tile<B, kSplit>(stage + warp * GB, bf[2 * c], accg, g0);
+                mac_tile<B, kSplit>(stage + warp * GB + TB, bf[2 * c], accu, g0);
+                mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * GB, bf[2 * c + 1], accg2, g1);
+                mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * GB + TB, bf[2 * c + 1], accu2, g1);
+            }
+        }
+    } else {
+        mac_tile<B, kSplit>(stage + warp * GB, bf[0], accg, g0);
+        mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * GB, bf[1], accu, g1);
+    }
+}
+
 // One phase (0: gate/up, 1: down) of a streaming warp.  The warp holds the
 // B fragments of its groups of the current pair: groups c * gc + w and
 // c * gc + w + 16 of each chunk c (gate/up: at most KG chunks; down: one).
@@ -986,8 +1033,7 @@ __device__ __forceinline__ bool unit_ends(const Geo &g, const UnitGeo &u, const 
 template <int BITS, bool XBF16, int KG, int PHASE>
 __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
-    constexpr int NS = num_stages(BITS), SB = stage_bytes(BITS), TB = tile_bytes(BITS);
-    constexpr int GB = PHASE == 0 ? 2 * TB : TB;
+    constexpr int NS = num_stages(ring_bits(BITS)), SB = stage_bytes(ring_bits(BITS));
     constexpr int NV = (PHASE == 1 || !XBF16) ? 4 : 2;
     constexpr bool kSplit = PHASE == 1 || !XBF16;
     constexpr int NB = PHASE == 0 ? 2 * KG : 2;  // B fragments held
@@ -1000,6 +1046,7 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
     Pos q = decode(g, nt > 0 ? ts : a0);
     UnitGeo u = unit_geo(g, q.p);
     int loaded = -1;
+    int pb = ring_bits(BITS);  // depth of the loaded pair
     BFrag bf[NB];
     float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
     float accg2[4] = {0.f, 0.f, 0.f, 0.f}, accu2[4] = {0.f, 0.f, 0.f, 0.f};  // gate/up: second group
@@ -1023,6 +1070,7 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
                 stream_barrier();
             }
             const PairInfo pi = read_pair(rv, q.p);
+            pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 const int c = b >> 1, lg = warp + (b & 1) * kStreamWarps;  // chunk, group in chunk
@@ -1034,7 +1082,10 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
                 if (c < u.ch && lg < u.gc && gi < u.gk) {
                     BRaw<NV> raw;
                     load_raw<PHASE, XBF16, NV>(a, pi, q.p, gi, fmax, raw);
-                    cook_b<BITS, PHASE, XBF16, NV>(raw, bf[b]);
+                    if (BITS != 0 || pb == 4)
+                        cook_b<ring_bits(BITS), PHASE, XBF16, NV>(raw, bf[b]);
+                    else
+                        cook_b<2, PHASE, XBF16, NV>(raw, bf[b]);
                 }
             }
             loaded = q.p;
@@ -1055,20 +1106,11 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
             const uint8_t *stage = st.ring + slot * SB;
             const int ng = min(u.gc, u.gk - q.c * u.gc);  // groups in this chunk
             const bool g0 = warp < ng, g1 = warp + kStreamWarps < ng;
-            if (PHASE == 0) {
-#pragma unroll
-                for (int c = 0; c < KG; ++c) {
-                    if (c == q.c) {
-                        mac_tile<BITS, kSplit>(stage + warp * GB, bf[2 * c], accg, g0);
-                        mac_tile<BITS, kSplit>(stage + warp * GB + TB, bf[2 * c], accu, g0);
-                        mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[2 * c + 1], accg2, g1);
-                        mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB + TB, bf[2 * c + 1], accu2, g1);
-                    }
-                }
-            } else {
-                mac_tile<BITS, kSplit>(stage + warp * GB, bf[0], accg, g0);
-                mac_tile<BITS, kSplit>(stage + (warp + kStreamWarps) * GB, bf[1], accu, g1);
-            }
+            if (BITS != 0 || pb == 4)
+                step_tiles<ring_bits(BITS), PHASE, KG, kSplit>(stage, bf, q.c, g0, g1, accg, accu, accg2,
+                                                               accu2);
+            else
+                step_tiles<2, PHASE, KG, kSplit>(stage, bf, q.c, g0, g1, accg, accu, accg2, accu2);
         }
         __syncwarp();
         if (ok && lane == 0)
@@ -1152,6 +1194,7 @@ __device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &r
     Pos q = decode(g, step_at(g, 0));
     UnitGeo u = unit_geo(g, q.p);
     int curp = q.p;
+    int pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
 #pragma unroll 1
     for (int kk = 0; kk < a1 - a0; ++kk) {
         const int i = step_at(g, kk);
@@ -1160,6 +1203,7 @@ __device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &r
         if (q.p != curp) {
             u = unit_geo(g, q.p);
             curp = q.p;
+            pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
         }
         if (unit_ends(g, u, q, i)) {
             if (st.uc % kEpiWarps == e && !*st.fail) {
@@ -1187,12 +1231,19 @@ __device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &r
                         mbar_arrive(&st.red_empty[rs]);
                     const int ustart = i - q.c, uend = ustart + u.ch;
                     const int ncols = rv.pairs[q.p * kPairInts + 1];
+                    constexpr int RB = ring_bits(BITS);
                     if (ustart >= a0 && uend <= a1) {
-                        finalize_unit<BITS, PHASE>(eo, ncols, q.p, q.s, tg, tu);
+                        if (BITS != 0 || pb == 4)
+                            finalize_unit<RB, PHASE>(eo, ncols, q.p, q.s, tg, tu);
+                        else
+                            finalize_unit<2, PHASE>(eo, ncols, q.p, q.s, tg, tu);
                         count_unit<PHASE>(eo, st.pspan, st.pcnt, st.ccnt, q.p, q.s);
+                    } else if (BITS != 0 || pb == 4) {
+                        fixup_unit<RB, PHASE>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
+                                              st.pspan, st.ccnt);
                     } else {
-                        fixup_unit<BITS, PHASE>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
-                                                st.pspan, st.ccnt);
+                        fixup_unit<2, PHASE>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
+                                             st.pspan, st.ccnt);
                     }
                 }
             }
@@ -1205,7 +1256,7 @@ __device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &r
 template <int BITS, bool XBF16, int KG>
 __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_constant__ LayerArgs a)
 {
-    constexpr int NS = num_stages(BITS);
+    constexpr int NS = num_stages(ring_bits(BITS));
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int s_ok;
@@ -1215,8 +1266,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     __shared__ unsigned s_ccnt[kMaxStripsD];
     Stream st;
     st.ring = smem;
-    st.red = reinterpret_cast<float4 *>(smem + NS * stage_bytes(BITS));
-    st.full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes(BITS) + red_bytes());
+    st.red = reinterpret_cast<float4 *>(smem + NS * stage_bytes(ring_bits(BITS)));
+    st.full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes(ring_bits(BITS)) + red_bytes());
     st.empty = st.full + NS;
     st.red_full = st.empty + NS;
     st.red_empty = st.red_full + kRedSlots;
@@ -1522,7 +1573,7 @@ template <int BITS, bool XBF16, int KG>
 cudaError_t launch_t(const LayerArgs &a, cudaStream_t stream)
 {
     auto kern = moe_layer_kernel<BITS, XBF16, KG>;
-    const int smem = smem_bytes(BITS);
+    const int smem = smem_bytes(ring_bits(BITS));
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1610,6 +1661,9 @@ cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream)
     const int kg = (a.d / kGroup + kChunkGroups - 1) / kChunkGroups;
     if (kg > 2 || a.f / kGroup > kDownGroupsMax || a.fs / kGroup > kDownGroupsMax)
         return cudaErrorInvalidValue;
+    if (a.mixed)
+        return kg <= 1 ? (a.x_bf16 ? launch_t<0, true, 1>(a, stream) : launch_t<0, false, 1>(a, stream))
+                       : (a.x_bf16 ? launch_t<0, true, 2>(a, stream) : launch_t<0, false, 2>(a, stream));
     if (kg <= 1) {
         if (a.bits == 4)
             return a.x_bf16 ? launch_t<4, true, 1>(a, stream) : launch_t<4, false, 1>(a, stream);

@@ -172,7 +172,7 @@ def load(path: str | None = None):
     L.smoe_moe_workspace_bytes_mixed.argtypes = [ctypes.POINTER(LayerDesc), I64]
     L.smoe_moe_workspace_bytes_mixed.restype = S
     L.smoe_moe_forward_mixed.argtypes = [ctypes.POINTER(LayerDesc), U8P, RP, P, I, I64, P, P, S,
-                                         P, P, P]
+                                         P, P, I, P]
     L.smoe_moe_forward_mixed.restype = I
     L.smoe_moe_forward_stage_mixed.argtypes = [ctypes.POINTER(LayerDesc), U8P, P, I, I64, P, P,
                                                S, P, P, I, P]
@@ -404,12 +404,11 @@ def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None
         raise TypeError("x must be fp32 or bf16")
     o = _opts(router_sigmoid, routed_scaling_factor, expert_mask)
     if layer.expert_bits is not None:
-        if path not in (None, PATH_GROUPED, PATH_AUTO):
-            raise ValueError("a layer with per-expert depths runs the grouped path only")
         _check(load().smoe_moe_forward_mixed(ctypes.byref(layer.desc), layer._ebits,
                                              None if o is None else ctypes.byref(o), _ptr(x), dt,
                                              T, _ptr(y), _ptr(ws), ws.numel(), _ptr(ids),
-                                             _ptr(w), _stream(stream)), "smoe_moe_forward_mixed")
+                                             _ptr(w), PATH_AUTO if path is None else int(path),
+                                             _stream(stream)), "smoe_moe_forward_mixed")
     elif o is not None:
         _check(load().smoe_moe_forward_ex(ctypes.byref(layer.desc), ctypes.byref(o), _ptr(x), dt,
                                           T, _ptr(y), _ptr(ws), ws.numel(), _ptr(ids), _ptr(w),
@@ -427,10 +426,8 @@ def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None
 
 
 def path_for(layer: MoELayer, T: int) -> int:
-    """smoe_moe_path: the execution path smoe_moe_forward takes at T tokens
-    (a layer with per-expert depths: always the grouped path)."""
-    if layer.expert_bits is not None:
-        return PATH_GROUPED
+    """smoe_moe_path: the execution path smoe_moe_forward (and, for a layer
+    with per-expert depths, smoe_moe_forward_mixed) takes at T tokens."""
     return int(load().smoe_moe_path(ctypes.byref(layer.desc), T))
 
 

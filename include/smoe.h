@@ -376,20 +376,24 @@ size_t smoe_moe_workspace_bytes_mixed(const smoe_layer_desc *layer, int64_t num_
  * smoe_repack_mixed with the same expert_bits (HOST array of num_experts
  * entries, each 2 or 4; read during the call, not kept); layer->bits is the
  * shared expert's depth.  Each expert decodes its own levels (L = 7.5 or
- * 1.5); otherwise the same computation as smoe_moe_forward_ex.  It always
- * takes the grouped path, at every token count: one GEMM launch per depth
- * present for gate/up and again for down, each taking the experts of its
- * own depth.  workspace: >= smoe_moe_workspace_bytes_mixed.  Errors as
+ * 1.5); otherwise the same computation as smoe_moe_forward_ex, on the same
+ * two paths, chosen the same way (path as in smoe_moe_forward_path; the
+ * grouped path also below 16 tokens):
+ *   streaming  one launch; each (expert, token block) unit streams and
+ *              decodes its tiles at its expert's depth
+ *   grouped    one gate/up and one down GEMM launch per depth present, each
+ *              taking the experts of its own depth
+ * workspace: >= smoe_moe_workspace_bytes_mixed.  Errors as
  * smoe_moe_forward_ex (expert_bits null or an entry not 2 or 4:
  * SMOE_ERR_INVALID_ARG). */
 smoe_status smoe_moe_forward_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
                                    const smoe_router_opts *opts, const void *x, smoe_dtype x_dtype,
                                    int64_t num_tokens, float *y, void *workspace,
-                                   size_t workspace_bytes, int32_t *ids_out, float *w_out,
+                                   size_t workspace_bytes, int32_t *ids_out, float *w_out, int path,
                                    void *cuda_stream);
 
-/* smoe_moe_forward_mixed (without router options) one launch stage at a
- * time, the stages of the grouped path as in smoe_moe_forward_stage. */
+/* smoe_moe_forward_mixed (without router options, path SMOE_PATH_AUTO) one
+ * launch stage at a time, as smoe_moe_forward_stage. */
 smoe_status smoe_moe_forward_stage_mixed(const smoe_layer_desc *layer, const uint8_t *expert_bits,
                                          const void *x, smoe_dtype x_dtype, int64_t num_tokens,
                                          float *y, void *workspace, size_t workspace_bytes,

@@ -225,13 +225,15 @@ def test_mixed_depth_entry_points_validate_on_the_host(libs):
     assert L.smoe_unpack_mixed(P(4096), 256, 128, 8, bad, 64, arr, arr, None) == -1
     for eb in (bad, None):
         assert L.smoe_moe_forward_mixed(ctypes.byref(desc), eb, None, P(4096), 0, 4, P(8192),
-                                        P(1 << 20), 1 << 30, None, None, None) == -1
+                                        P(1 << 20), 1 << 30, None, None, 0, None) == -1
         assert L.smoe_moe_forward_stage_mixed(ctypes.byref(desc), eb, P(4096), 0, 4, P(8192),
                                               P(1 << 20), 1 << 30, None, None, 0, None) == -1
     assert L.smoe_moe_forward_stage_mixed(ctypes.byref(desc), good, P(4096), 0, 4, P(8192),
                                           P(1 << 20), 1 << 30, None, None, 3, None) == -1
     assert L.smoe_moe_forward_mixed(ctypes.byref(desc), good, None, None, 0, 0, None, None, 0,
-                                    None, None, None) == 0                      # T = 0
+                                    None, None, 0, None) == 0                   # T = 0
+    assert L.smoe_moe_forward_mixed(ctypes.byref(desc), good, None, P(4096), 0, 4, P(8192),
+                                    P(1 << 20), 1 << 30, None, None, 5, None) == -1  # bad path
     w1 = L.smoe_moe_workspace_bytes_mixed(ctypes.byref(desc), 1)
     assert w1 > L.smoe_moe_workspace_bytes(ctypes.byref(desc), 1)
     assert w1 >= 128 * (256 * 2 + 128 * 2 + 256 * 4)      # one padded 128-row tile per segment

@@ -2,10 +2,13 @@
 (some SMOE-Q2, some SMOE-Q4 in one bank; "CMF v2", 2.2 MoE: every expert
 entry carries its own dtype) against the oracle.
 
-Such a layer always runs the grouped tensor-core path (bar: max-abs-error
-<= 2e-2 * ||y_ref||_inf), one GEMM launch per depth present; the tests
-cover every token count from one token up (small batches included), both
-shared-expert depths, one expert of the minority depth, and m-tile pairing.
+Such a layer runs on both paths: the streaming kernel (bar 1e-3 *
+||y_ref||_inf), whose units each decode at their expert's depth, and the
+grouped tensor-core path (bar 2e-2), one GEMM launch per depth present.
+The tests cover one token (fused routing and combine), small batches on
+either path, both shared-expert depths, one expert of the minority depth,
+m-tile pairing, and bit-equality with the single-depth kernels when every
+expert has the same depth.
 """
 import zlib
 
@@ -83,22 +86,31 @@ def run(S, lay, wl, x_host, **router):
     return y.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
 
 
-@pytest.mark.parametrize("name,pat,T", [
-    ("tiny_f32", "alternate", 1), ("tiny_f32", "alternate", 16), ("tiny_f32", "one_q4", 200),
-    ("tiny_f32", "one_q2", 700),
+STREAM, GROUPED = 1, 2
+
+
+@pytest.mark.parametrize("name,pat,T,path", [
+    # streaming: fused routing + combine (T <= 8), then the separate stages
+    ("tiny_f32", "alternate", 1, None), ("half_ntile_bf16", "alternate", 5, None),
+    ("shared_bf16", "alternate", 3, None), ("shared_f32", "alternate", 9, None),
+    ("shared_bf16", "one_q2", 40, STREAM), ("tiny_f32", "one_q4", 200, STREAM),
+    ("half_ntile_bf16", "popular", 64, STREAM), ("shared_f32", "one_q4", 150, STREAM),
+    # grouped, small batches included
+    ("tiny_f32", "alternate", 1, GROUPED), ("shared_bf16", "popular", 7, GROUPED),
+    ("tiny_f32", "alternate", 16, GROUPED), ("tiny_f32", "one_q4", 200, GROUPED),
+    ("tiny_f32", "one_q2", 700, None), ("half_ntile_bf16", "one_q4", 333, None),
+    ("shared_bf16", "popular", 300, None), ("shared_bf16", "one_q2", 40, GROUPED),
+    ("shared_f32", "one_q4", 150, GROUPED),
     # >= 256 rows per expert on average: items pair two m-tiles
-    ("tiny_f32", "alternate", 1100), ("half_ntile_bf16", "popular", 1030),
-    ("half_ntile_bf16", "alternate", 5), ("half_ntile_bf16", "one_q4", 333),
-    ("shared_bf16", "alternate", 3), ("shared_bf16", "popular", 300),
-    ("shared_bf16", "one_q2", 40), ("shared_f32", "one_q4", 150), ("shared_f32", "alternate", 9),
+    ("tiny_f32", "alternate", 1100, None), ("half_ntile_bf16", "popular", 1030, None),
 ])
-def test_mixed_matches_oracle(S, name, pat, T):
+def test_mixed_matches_oracle(S, name, pat, T, path):
     wl, hl = host_layer(name, pat)
     lay = hl.device_layer(DEV)
-    assert S.path_for(lay, T) == S.PATH_GROUPED
+    grouped = path == GROUPED or (path is None and S.path_for(lay, T) == S.PATH_GROUPED)
     x, _ = wl.activations(0, T)
-    y, ids, w = run(S, lay, wl, x)
-    check_forward(y, ids, w, hl, x, tol=TOL)
+    y, ids, w = run(S, lay, wl, x, path=path)
+    check_forward(y, ids, w, hl, x, tol=TOL if grouped else 1e-3)
 
 
 def test_repack_mixed_is_the_per_expert_repacks_back_to_back(S):
@@ -121,24 +133,28 @@ def test_repack_mixed_is_the_per_expert_repacks_back_to_back(S):
         assert torch.equal(a, b)
 
 
-def test_all_q4_mixed_equals_the_uniform_grouped_path(S):
-    """Every expert at Q4: the mixed forward is the uniform grouped forward,
-    bit for bit."""
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("T,path", [(5, STREAM), (40, STREAM), (96, GROUPED)])
+def test_one_depth_mixed_equals_the_single_depth_kernels(S, bits, T, path):
+    """Every expert at the same depth: the mixed-depth kernels give the
+    single-depth kernels' bits on both paths."""
     d, f, E, k, norm, xd, sf, sg, _ = CFG["shared_bf16"]
-    wl = Y.Workload("shared_bf16", d, f, E, k, norm, [4], [1], 1, 77, x_dtype=xd, shared_f=sf,
-                    shared_gate=sg)
-    hu = HostLayer(wl, 0, 4)
-    hm = HostLayer(wl, 0, 4, expert_bits=[4] * E)
-    x, _ = wl.activations(0, 96)
-    yu, idu, wu = run(S, hu.device_layer(DEV), wl, x, path=S.PATH_GROUPED)
-    ym, idm, wm = run(S, hm.device_layer(DEV), wl, x)
+    wl = Y.Workload("shared_bf16", d, f, E, k, norm, [bits], [1], 1, 77, x_dtype=xd,
+                    shared_f=sf, shared_gate=sg)
+    hu = HostLayer(wl, 0, bits)
+    hm = HostLayer(wl, 0, bits, expert_bits=[bits] * E)
+    x, _ = wl.activations(0, T)
+    yu, idu, wu = run(S, hu.device_layer(DEV), wl, x, path=path)
+    ym, idm, wm = run(S, hm.device_layer(DEV), wl, x, path=path)
     assert np.array_equal(idu, idm) and np.array_equal(wu, wm)
     assert np.array_equal(yu, ym)
 
 
-def test_mixed_with_router_options(S):
+@pytest.mark.parametrize("T", [6, 70])
+def test_mixed_with_router_options(S, T):
     """Sigmoid scores, a routed scaling factor, a selection bias and a
-    routing mask on a mixed layer (the router is independent of depth)."""
+    routing mask on a mixed layer (the router is independent of depth), on
+    the streaming (6 tokens) and the grouped path (70)."""
     wl, hl = host_layer("shared_bf16", "alternate")
     bias = (np.random.default_rng(9).standard_normal(wl.E) * 0.05).astype(np.float32)
     allowed = [e for e in range(wl.E) if e % 3 != 1]
@@ -146,7 +162,6 @@ def test_mixed_with_router_options(S):
     for e in allowed:
         mask[e // 8] |= 1 << (e % 8)
     lay = hl.device_layer(DEV, expert_bias=bias)
-    T = 70
     x, _ = wl.activations(0, T)
     y, ids, w = run(S, lay, wl, x, router_sigmoid=True, routed_scaling_factor=2.5,
                     expert_mask=mask)
@@ -164,7 +179,8 @@ def test_mixed_with_router_options(S):
         y_ref[mism] = hl.oracle_apply(x[mism], ids[mism], w[mism])
     ok = [t for t in range(T) if t not in mism]
     assert np.allclose(w[ok], w_ref[ok], rtol=1e-5, atol=1e-6)
-    assert float(np.abs(y - y_ref).max()) <= TOL * float(np.abs(y_ref).max())
+    tol = TOL if S.path_for(lay, T) == S.PATH_GROUPED else 1e-3
+    assert float(np.abs(y - y_ref).max()) <= tol * float(np.abs(y_ref).max())
 
 
 def test_mixed_is_deterministic(S):
@@ -176,11 +192,12 @@ def test_mixed_is_deterministic(S):
     assert np.array_equal(y1, y2)
 
 
-def test_mixed_stages_compose_to_the_whole_forward(S):
-    """The three launch stages, called one by one, give the forward's bits."""
+@pytest.mark.parametrize("T", [12, 50])
+def test_mixed_stages_compose_to_the_whole_forward(S, T):
+    """The three launch stages, called one by one, give the forward's bits
+    (12 tokens: streaming stages; 50: grouped)."""
     wl, hl = host_layer("shared_bf16", "one_q4")
     lay = hl.device_layer(DEV)
-    T = 50
     x, _ = wl.activations(0, T)
     y_all, _, _ = run(S, lay, wl, x)
     xt = to_dev(x, DEV).to(torch.bfloat16)
