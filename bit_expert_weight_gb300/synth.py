@@ -241,6 +241,9 @@ WORKLOADS = {
                                  True, [4], [1, 8, 64, 512, 4096], 1, 3, zipf_s=1.1,
                                  # calibrate_zipf_tau(layer 0, 4096 tokens): share 0.2424 vs p_1 0.2257
                                  zipf_tau=0.375),
+    # the largest layer the kernels take (d, f, shared f and k at their limits)
+    "edge_max": Workload("maximum-size layer d4096 f2048 E16 k16 + shared 2048", 4096, 2048, 16,
+                         16, True, [4, 2], [1, 9], 1, 5, shared_f=2048, shared_gate=True),
     "a3b35b": Workload("35B-A3B-like fine-grained layer d2048 f512 E256 k8 + shared", 2048, 512,
                        256, 8, True, [4, 2], [1, 256], 40, 4, shared_f=512, shared_gate=True),
 }

@@ -129,17 +129,27 @@ class FullLayer:
         S.synth_bf16(x, Y.stream_key(wl.seed, self.layer, 0, Y.ROLE_X), 1.0)
         return x.view(torch.bfloat16).view(T, wl.d)
 
-    def check(self, S, T, tol=None, path=None):
+    def check(self, S, T, tol=None, path=None, x_f32=False):
         """tol defaults to the bar of the path the forward takes: 1e-3 on the
         streaming path (fp32 accumulation), 2e-2 on the grouped tensor-core
-        path (bf16 operands).  path forces a path (smoe_moe_forward_path)."""
+        path (bf16 operands).  path forces a path (smoe_moe_forward_path).
+        Sampled tokens at or past T are skipped.  x_f32: the tokens as fp32
+        values of the seeded stream (not rounded to bf16)."""
         wl = self.wl
         grouped = (path == S.PATH_GROUPED or
                    (path in (None, S.PATH_AUTO) and S.path_for(self.lay, T) == S.PATH_GROUPED))
         if tol is None:
             tol = 2e-2 if grouped else 1e-3
-        assert max(self.sample) < T
-        xt = self.device_x(S, T)
+        sample = [t for t in self.sample if t < T]
+        assert sample
+        if x_f32:
+            key = Y.stream_key(wl.seed, self.layer, 0, Y.ROLE_X)
+            xh = Y.values_f32(key, T * wl.d, 1.0).reshape(T, wl.d)
+            xt = torch.from_numpy(xh).to(DEV)
+            x_sample = xh[sample]
+        else:
+            xt = self.device_x(S, T)
+            x_sample = self.x_sample[[self.sample.index(t) for t in sample]]
         ws = S.workspace(self.lay, T)
         ids = torch.empty((T, wl.k), dtype=torch.int32, device=DEV)
         w = torch.empty((T, wl.k), dtype=torch.float32, device=DEV)
@@ -147,21 +157,21 @@ class FullLayer:
         torch.cuda.synchronize()
         assert S.device_status() == 0
         # the device x rows are the host generator's rows, bit for bit
-        xs = xt[self.sample].float().cpu().numpy()
-        assert np.array_equal(xs, self.x_sample)
-        yg = y[self.sample].cpu().numpy()
-        idg = ids[self.sample].cpu().numpy()
-        wg = w[self.sample].cpu().numpy()
+        xs = xt[sample].float().cpu().numpy()
+        assert np.array_equal(xs, x_sample)
+        yg = y[sample].cpu().numpy()
+        idg = ids[sample].cpu().numpy()
+        wg = w[sample].cpu().numpy()
         y_ref, ids_ref, w_ref, lg = O.moe_forward(wl.d, wl.f, wl.E, wl.k, wl.norm, self.bits,
-                                                  self.router, self.blob, self.x_sample,
+                                                  self.router, self.blob, x_sample,
                                                   expert_bias=self.bias,
                                                   shared_blob=self.shared_blob, fs=wl.shared_f,
                                                   shared_gate=self.shared_gate,
                                                   expert_bits=self.expert_bits)
         ties = set(near_tie_tokens(lg, wl.k, self.bias))
-        mism = [i for i in range(len(self.sample)) if not np.array_equal(idg[i], ids_ref[i])]
+        mism = [i for i in range(len(sample)) if not np.array_equal(idg[i], ids_ref[i])]
         assert set(mism) <= ties, f"routing differs on non-tie sampled tokens {mism}"
-        ok = [i for i in range(len(self.sample)) if i not in mism]
+        ok = [i for i in range(len(sample)) if i not in mism]
         assert np.allclose(wg[ok], w_ref[ok], rtol=1e-5, atol=1e-6)
         err = float(np.abs(yg[ok] - y_ref[ok]).max()) if ok else 0.0
         bound = tol * float(np.abs(y_ref[ok]).max()) if ok else 1.0
@@ -224,3 +234,18 @@ def test_a3b35b_mixed_depth_full_size(S, pool):
     fl = FullLayer(S, pool, "a3b35b", 3, 2, sample=[0, 200],
                    expert_bits=[4 if e % 2 == 0 else 2 for e in range(256)])
     fl.check(S, 256)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_maximum_size_layer(S, pool, bits):
+    """The largest layer the kernels take: d 4096 (two gate/up chunks per
+    strip), f and shared f 2048 (a down strip fills one ring stage), k = E =
+    16 with a gated shared expert; bf16 and fp32 tokens (hi + lo split); one
+    token (fused routing and combine), 9 tokens (separate stages), 16 tokens
+    on the grouped path."""
+    fl = FullLayer(S, pool, "edge_max", 0, bits, sample=[0, 8])
+    fl.check(S, 1)
+    fl.check(S, 1, x_f32=True)
+    fl.check(S, 9)
+    fl.check(S, 9, x_f32=True)
+    fl.check(S, 16, path=S.PATH_GROUPED)
