@@ -333,25 +333,40 @@ __device__ void code_producer(const GroupedArgs &a, GSmem &sm, uint8_t *sC)
     }
 }
 
-// Activation tiles: for every K block, one 128 x 64 tile per m-tile of the
-// item, into the K block's stage (warp 2, lane 0).
+// Tensor maps of one activation matrix (the sorted token rows, or h) read in
+// boxes of 32, 64 and 128 rows x 64 columns.
+struct AMaps {
+    CUtensorMap box[3];
+};
+
+// Activation tiles of every K block, in item order (warp 2, lane 0).  Each
+// m-tile is loaded in the shortest box that covers its valid rows: the rest
+// of the 128-row tile keeps older rows, which only reach accumulator rows
+// the epilogue never stores.
 template <int PHASE, bool PAIR>
-__device__ void act_producer(const GroupedArgs &a, const CUtensorMap *amap, GSmem &sm, uint8_t *sA)
+__device__ void act_producer(const GroupedArgs &a, const AMaps *am, GSmem &sm, uint8_t *sA)
 {
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
         const Item w = item_at<PAIR>(sm, i);
         const int fsg = w.seg < a.E ? a.f : a.fs;
         const int nkb = PHASE == 0 ? a.d / kGK : fsg / kGK;
+        int bx[2];  // box per m-tile: 0 = 32 rows, 1 = 64, 2 = 128
+        uint32_t bytes = 0;
+        for (int j = 0; j < w.nm; ++j) {
+            const int nv = j == 0 ? w.nvalid0 : w.nvalid1;
+            bx[j] = nv <= 32 ? 0 : (nv <= 64 ? 1 : 2);
+            bytes += (32u << bx[j]) * (kGK * 2);
+        }
         for (int kb = 0; kb < nkb; ++kb, ++it) {
             const int s = static_cast<int>(it % num_stages(PAIR));
             if (!gwait(sm, &sm.stage_empty[s], ((it / num_stages(PAIR)) & 1u) ^ 1u, a.status))
                 return;
-            mbar_arrive_expect_tx(&sm.a_full[s], w.nm * kATileBytes);
+            mbar_arrive_expect_tx(&sm.a_full[s], bytes);
             sm.last_a[s] = it + 1;
             for (int j = 0; j < w.nm; ++j)
-                tma_load_2d(sA + s * a_stage_bytes(PAIR) + j * kATileBytes, amap, kb * kGK,
-                            w.row0 + kGM * j, &sm.a_full[s]);
+                tma_load_2d(sA + s * a_stage_bytes(PAIR) + j * kATileBytes, &am->box[bx[j]],
+                            kb * kGK, w.row0 + kGM * j, &sm.a_full[s]);
         }
     }
 }
@@ -644,7 +659,7 @@ __device__ void epilogue(const GroupedArgs &a, GSmem &sm)
 
 template <int BITS, int PHASE, bool PAIR>
 __global__ void __launch_bounds__(kGThreads, 1)
-    grouped_gemm_kernel(const GroupedArgs a, const __grid_constant__ CUtensorMap amap)
+    grouped_gemm_kernel(const GroupedArgs a, const __grid_constant__ AMaps amaps)
 {
     extern __shared__ uint8_t g_smem_raw[];
     __shared__ GSmem sm;
@@ -729,7 +744,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         code_producer<BITS, PHASE, PAIR>(a, sm, sC);
     } else if (warp == 2) {
         if (lane == 0)
-            act_producer<PHASE, PAIR>(a, &amap, sm, sA);
+            act_producer<PHASE, PAIR>(a, &amaps, sm, sA);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
@@ -1113,7 +1128,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int b
 }
 
 template <int BITS, int PHASE, bool PAIR>
-cudaError_t launch_gemm_t(const GroupedArgs &a, const CUtensorMap &map, cudaStream_t s)
+cudaError_t launch_gemm_t(const GroupedArgs &a, const AMaps &maps, cudaStream_t s)
 {
     static std::mutex mu;
     static bool attr_set[64] = {false};
@@ -1131,7 +1146,7 @@ cudaError_t launch_gemm_t(const GroupedArgs &a, const CUtensorMap &map, cudaStre
         }
     }
     grouped_gemm_kernel<BITS, PHASE, PAIR>
-        <<<device_sm_count(), kGThreads, grouped_smem_bytes(BITS, PAIR), s>>>(a, map);
+        <<<device_sm_count(), kGThreads, grouped_smem_bytes(BITS, PAIR), s>>>(a, maps);
     return cudaGetLastError();
 }
 
@@ -1207,9 +1222,10 @@ cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, cons
         for (int ex = 0; ex < a.E; ++ex)
             ((a.q4mask[ex >> 5] >> (ex & 31)) & 1u ? has4 : has2) = true;
     if (stage_mask & 2) {  // gate/up GEMM + SiLU(g) * u
-        CUtensorMap mx;
-        if (!make_map(&mx, a.xs, a.rows, a.d))
-            return cudaErrorInvalidValue;
+        AMaps mx;
+        for (int b = 0; b < 3; ++b)
+            if (!make_map(&mx.box[b], a.xs, a.rows, a.d, 32 << b))
+                return cudaErrorInvalidValue;
         if (has4 && (e = pair ? launch_gemm_t<4, 0, true>(a, mx, s)
                               : launch_gemm_t<4, 0, false>(a, mx, s)) != cudaSuccess)
             return e;
@@ -1218,9 +1234,10 @@ cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, cons
             return e;
     }
     if (stage_mask & 4) {  // down GEMM + combine
-        CUtensorMap mh;
-        if (!make_map(&mh, a.h, a.rows, a.hstride))
-            return cudaErrorInvalidValue;
+        AMaps mh;
+        for (int b = 0; b < 3; ++b)
+            if (!make_map(&mh.box[b], a.h, a.rows, a.hstride, 32 << b))
+                return cudaErrorInvalidValue;
         if (has4 && (e = pair ? launch_gemm_t<4, 1, true>(a, mh, s)
                               : launch_gemm_t<4, 1, false>(a, mh, s)) != cudaSuccess)
             return e;
