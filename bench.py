@@ -231,12 +231,19 @@ class DeviceModel:
                                           expert_bias=bias, shared_tiles=sh_tiles,
                                           shared_f=wl.shared_f, shared_gate_w=sh_gate,
                                           expert_bits=self.expert_bits if mixed else None))
+        # every layer's tokens and outputs in one contiguous tensor each, so
+        # that a step's inputs and results cross PCIe/C2C in one copy each
+        xdt = torch.bfloat16 if wl.x_dtype == "bf16" else torch.float32
+        self.x_all = torch.empty((n_layers, T, d), dtype=xdt, device=dev)
+        self.y_all = torch.empty((n_layers, T, d), dtype=torch.float32, device=dev)
+        for l in range(n_layers):
             xf, xb = wl.activations(l, T)
             if xb is not None:
-                self.x.append(torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16))
+                self.x_all[l].view(torch.int16).copy_(torch.from_numpy(xb.view(np.int16)))
             else:
-                self.x.append(torch.from_numpy(xf).to(dev))
-            self.y.append(torch.empty((T, d), dtype=torch.float32, device=dev))
+                self.x_all[l].copy_(torch.from_numpy(xf))
+        self.x = [self.x_all[l] for l in range(n_layers)]
+        self.y = [self.y_all[l] for l in range(n_layers)]
         torch.cuda.synchronize()
         self.setup_s = time.time() - t0
         self.ws = S.workspace(self.layers[0], T)
@@ -398,17 +405,16 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
     layer_bytes = layer_algorithmic_bytes(model)
 
     # end to end: pinned host x -> device, forward, device y -> host, per step
-    xs_host = [x.cpu().pin_memory() for x in model.x]
-    ys_host = [torch.empty_like(y, device="cpu").pin_memory() for y in model.y]
-    h2d = sum(x.numel() * x.element_size() for x in xs_host)
-    d2h = sum(y.numel() * y.element_size() for y in ys_host)
+    # (all layers' tokens in one copy, all their outputs in one copy)
+    x_host = model.x_all.cpu().pin_memory()
+    y_host = torch.empty_like(model.y_all, device="cpu").pin_memory()
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = y_host.numel() * y_host.element_size()
 
     def e2e_step():
-        for xh, xd in zip(xs_host, model.x):
-            xd.copy_(xh, non_blocking=True)
+        model.x_all.copy_(x_host, non_blocking=True)
         model.step()
-        for yd, yh in zip(model.y, ys_host):
-            yh.copy_(yd, non_blocking=True)
+        y_host.copy_(model.y_all, non_blocking=True)
 
     g3 = None
     if use_graph:
