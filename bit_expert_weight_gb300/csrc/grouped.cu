@@ -54,13 +54,15 @@ constexpr int kGM = 128;             // rows per item (MMA M)
 constexpr int kGN = 256;             // output columns per item (MMA N)
 constexpr int kGK = 64;              // K per stage (one quantisation group)
 constexpr int kMaxCodeStages = 3;
-// Code stages: one bulk copy moves a strip's tiles of code_kb consecutive K
-// blocks.  A bulk copy has a fixed cost: copies of one K block's tiles
-// (1088 B for a gate/up strip at Q4) cap the weight stream near 2 TB/s on
-// this part, copies of 4 K blocks reach about 7 TB/s.  Items of one m-tile
-// stream each weight tile once per m-tile and take 2 stages of 4 K blocks;
-// items of two m-tiles need 3 activation stages and keep 3 code stages of
-// one K block (what the shared memory leaves).
+// Code stages: the tiles of code_kb consecutive K blocks of the item's
+// strips.  Banks of one depth fill a stage with one tensor copy (a 4-D map:
+// tile bytes x K blocks x strips x experts); banks of mixed depths with one
+// bulk copy per strip.  A bulk copy has a fixed cost: copies of one K
+// block's tiles (1088 B for a gate/up strip at Q4) cap the weight stream
+// near 2 TB/s on this part, copies of 4 K blocks reach about 7 TB/s.  Items
+// of one m-tile stream each weight tile once per m-tile and take 2 stages
+// of 4 K blocks; items of two m-tiles need 3 activation stages and keep 3
+// code stages of one K block (what the shared memory leaves).
 __host__ __device__ constexpr int code_kb(bool pair) { return pair ? 1 : 4; }
 __host__ __device__ constexpr int code_stages(bool pair) { return pair ? 3 : 2; }
 constexpr int kMaxStages = 4;        // activations + decoded weights of one K block each
@@ -123,6 +125,16 @@ struct GSmem {
 };
 
 // ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar)
@@ -305,21 +317,47 @@ struct CodeSrc {
     }
 };
 
+// Tensor maps of one GEMM launch: the activation matrix (the sorted token
+// rows, or h) in boxes of 32, 64 and 128 rows x 64 columns, and the code
+// tiles of the routed bank and of the shared expert as 4-D tensors of
+// 8-byte elements (tile bytes of one K block of a strip, K blocks, strips,
+// experts) read in boxes of one code stage.
+struct GMaps {
+    CUtensorMap act[3];
+    CUtensorMap code[2];  // routed, shared
+    int code_tma;         // 1: code stages by tensor copy
+};
+
 // Code tiles of every K block, in item order (warp 0).
 template <int BITS, int PHASE, bool PAIR>
-__device__ void code_producer(const GroupedArgs &a, GSmem &sm, uint8_t *sC)
+__device__ void code_producer(const GroupedArgs &a, const GMaps *gm, GSmem &sm, uint8_t *sC)
 {
     const int lane = threadIdx.x & 31;
     typedef CodeSrc<BITS, PHASE> Src;
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
-        const Src cs(a, item_at<PAIR>(sm, i));
+        const Item w = item_at<PAIR>(sm, i);
+        const Src cs(a, w);
         for (int kb0 = 0; kb0 < cs.nkb; kb0 += code_kb(PAIR), ++it) {
             const int nb = cs.nkb - kb0 < code_kb(PAIR) ? cs.nkb - kb0 : code_kb(PAIR);
             const int s = static_cast<int>(it % code_stages(PAIR));
             const unsigned par = ((it / code_stages(PAIR)) & 1u) ^ 1u;
             if (!__all_sync(0xffffffffu, gwait(sm, &sm.code_empty[s], par, a.status)))
                 return;
+            if (gm->code_tma) {
+                // one box: K blocks kb0 .. kb0 + code_kb - 1 of the item's
+                // strips; boxes past the last K block or strip are zero-filled
+                // and still count their full size
+                if (lane == 0) {
+                    const bool routed = w.seg < a.E;
+                    mbar_arrive_expect_tx(&sm.code_full[s], code_stage_bytes(BITS, PAIR));
+                    sm.last_code[s] = it + 1;
+                    tma_load_4d(sC + s * code_stage_bytes(BITS, PAIR), &gm->code[routed ? 0 : 1], 0,
+                                kb0, cs.r0, routed ? w.seg : 0, &sm.code_full[s]);
+                }
+                __syncwarp();
+                continue;
+            }
             if (lane == 0) {
                 mbar_arrive_expect_tx(&sm.code_full[s], cs.ncopy * nb * Src::csize);
                 sm.last_code[s] = it + 1;
@@ -333,18 +371,12 @@ __device__ void code_producer(const GroupedArgs &a, GSmem &sm, uint8_t *sC)
     }
 }
 
-// Tensor maps of one activation matrix (the sorted token rows, or h) read in
-// boxes of 32, 64 and 128 rows x 64 columns.
-struct AMaps {
-    CUtensorMap box[3];
-};
-
 // Activation tiles of every K block, in item order (warp 2, lane 0).  Each
 // m-tile is loaded in the shortest box that covers its valid rows: the rest
 // of the 128-row tile keeps older rows, which only reach accumulator rows
 // the epilogue never stores.
 template <int PHASE, bool PAIR>
-__device__ void act_producer(const GroupedArgs &a, const AMaps *am, GSmem &sm, uint8_t *sA)
+__device__ void act_producer(const GroupedArgs &a, const GMaps *gm, GSmem &sm, uint8_t *sA)
 {
     uint32_t it = 0;
     for (int i = blockIdx.x; i < sm.total_items; i += gridDim.x) {
@@ -365,7 +397,7 @@ __device__ void act_producer(const GroupedArgs &a, const AMaps *am, GSmem &sm, u
             mbar_arrive_expect_tx(&sm.a_full[s], bytes);
             sm.last_a[s] = it + 1;
             for (int j = 0; j < w.nm; ++j)
-                tma_load_2d(sA + s * a_stage_bytes(PAIR) + j * kATileBytes, &am->box[bx[j]],
+                tma_load_2d(sA + s * a_stage_bytes(PAIR) + j * kATileBytes, &gm->act[bx[j]],
                             kb * kGK, w.row0 + kGM * j, &sm.a_full[s]);
         }
     }
@@ -659,7 +691,7 @@ __device__ void epilogue(const GroupedArgs &a, GSmem &sm)
 
 template <int BITS, int PHASE, bool PAIR>
 __global__ void __launch_bounds__(kGThreads, 1)
-    grouped_gemm_kernel(const GroupedArgs a, const __grid_constant__ AMaps amaps)
+    grouped_gemm_kernel(const GroupedArgs a, const __grid_constant__ GMaps maps)
 {
     extern __shared__ uint8_t g_smem_raw[];
     __shared__ GSmem sm;
@@ -741,10 +773,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc_fence_after();
 
     if (warp == 0) {
-        code_producer<BITS, PHASE, PAIR>(a, sm, sC);
+        code_producer<BITS, PHASE, PAIR>(a, &maps, sm, sC);
     } else if (warp == 2) {
         if (lane == 0)
-            act_producer<PHASE, PAIR>(a, &amaps, sm, sA);
+            act_producer<PHASE, PAIR>(a, &maps, sm, sA);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
@@ -1127,8 +1159,55 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int b
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Code tiles of a bank region as a 4-D tensor of 8-byte elements: csize
+// bytes (one K block of a strip), G K blocks, nstr strips, nexp experts
+// expert_stride bytes apart; boxes of box_kb K blocks x box_str strips.
+// False where the encoder refuses it or a box would exceed the tensor.
+bool make_code_map(CUtensorMap *m, const uint8_t *base, uint32_t csize, int G, int nstr, int nexp,
+                   int64_t expert_stride, int box_kb, int box_str)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base || box_kb > G || box_str > nstr || csize % 16 || expert_stride % 16)
+        return false;
+    const cuuint64_t dims[4] = {csize / 8, static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(nstr),
+                                static_cast<cuuint64_t>(nexp)};
+    const cuuint64_t strides[3] = {csize, static_cast<cuuint64_t>(G) * csize,
+                                   static_cast<cuuint64_t>(expert_stride)};
+    const cuuint32_t box[4] = {csize / 8, static_cast<cuuint32_t>(box_kb),
+                               static_cast<cuuint32_t>(box_str), 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<uint8_t *>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The maps of one GEMM launch (phase 0: gate/up, 1: down) over activation
+// matrix `act` [rows, cols].
+bool make_gemm_maps(GMaps *g, const GroupedArgs &a, int phase, bool pair, const void *act, int cols)
+{
+    memset(g, 0, sizeof *g);
+    for (int b = 0; b < 3; ++b)
+        if (!make_map(&g->act[b], act, a.rows, cols, 32 << b))
+            return false;
+    if (a.mixed)
+        return true;  // experts of two sizes: per-strip bulk copies
+    const uint32_t TB = tile_bytes(a.bits);
+    const uint32_t csize = phase == 0 ? 2 * TB : TB;
+    const int kbx = pair ? code_kb(true) : code_kb(false), strips = phase == 0 ? 8 : 16;
+    bool ok = make_code_map(&g->code[0],
+                            a.tiles_routed + (phase == 0 ? 0 : 2ll * a.d * a.f / 1024 * TB), csize,
+                            phase == 0 ? a.d / kGK : a.f / kGK, phase == 0 ? a.f / 16 : a.d / 16,
+                            a.E, a.expert_bytes_routed, kbx, strips);
+    if (ok && a.has_shared)
+        ok = make_code_map(&g->code[1], a.tiles_shared + (phase == 0 ? 0 : a.down_off_shared), csize,
+                           phase == 0 ? a.d / kGK : a.fs / kGK, phase == 0 ? a.fs / 16 : a.d / 16, 1,
+                           3ll * a.d * a.fs / 1024 * TB, kbx, strips);
+    g->code_tma = ok ? 1 : 0;
+    return true;
+}
+
 template <int BITS, int PHASE, bool PAIR>
-cudaError_t launch_gemm_t(const GroupedArgs &a, const AMaps &maps, cudaStream_t s)
+cudaError_t launch_gemm_t(const GroupedArgs &a, const GMaps &maps, cudaStream_t s)
 {
     static std::mutex mu;
     static bool attr_set[64] = {false};
@@ -1222,10 +1301,9 @@ cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, cons
         for (int ex = 0; ex < a.E; ++ex)
             ((a.q4mask[ex >> 5] >> (ex & 31)) & 1u ? has4 : has2) = true;
     if (stage_mask & 2) {  // gate/up GEMM + SiLU(g) * u
-        AMaps mx;
-        for (int b = 0; b < 3; ++b)
-            if (!make_map(&mx.box[b], a.xs, a.rows, a.d, 32 << b))
-                return cudaErrorInvalidValue;
+        GMaps mx;
+        if (!make_gemm_maps(&mx, a, 0, pair, a.xs, a.d))
+            return cudaErrorInvalidValue;
         if (has4 && (e = pair ? launch_gemm_t<4, 0, true>(a, mx, s)
                               : launch_gemm_t<4, 0, false>(a, mx, s)) != cudaSuccess)
             return e;
@@ -1234,10 +1312,9 @@ cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, cons
             return e;
     }
     if (stage_mask & 4) {  // down GEMM + combine
-        AMaps mh;
-        for (int b = 0; b < 3; ++b)
-            if (!make_map(&mh.box[b], a.h, a.rows, a.hstride, 32 << b))
-                return cudaErrorInvalidValue;
+        GMaps mh;
+        if (!make_gemm_maps(&mh, a, 1, pair, a.h, a.hstride))
+            return cudaErrorInvalidValue;
         if (has4 && (e = pair ? launch_gemm_t<4, 1, true>(a, mh, s)
                               : launch_gemm_t<4, 1, false>(a, mh, s)) != cudaSuccess)
             return e;
