@@ -85,8 +85,10 @@ constexpr int kGThreads = kGWarps * 32;
 constexpr int kTilesPerStage = 16;
 constexpr uint32_t kATileBytes = kGM * kGK * 2;   // 16 KB
 constexpr uint32_t kBTileBytes = kGN * kGK * 2;   // 32 KB
-// Items of two m-tiles (one decoded weight stage feeds both) take 3 stages
-// with room for two activation tiles; items of one m-tile take 4 stages.
+// Stages of activations + decoded weights: 3 for both item kinds, what the
+// shared memory holds beside the code ring (two activation tiles per stage
+// for items of two m-tiles, code stages of 4 K blocks for items of one).
+// 4 stages with code stages of 1 K block measured slower.
 __host__ __device__ constexpr int num_stages(bool pair) { return 3; }
 __host__ __device__ constexpr uint32_t a_stage_bytes(bool pair)
 {
