@@ -316,6 +316,17 @@ def gateup_flops(model):
     return f
 
 
+def max_over_ranks(value, world, dev):
+    """The largest of every rank's value (all ranks call it; world 1: the
+    value itself).  The timed region ends when the slowest replica does."""
+    import torch
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def launches_per_layer(model):
     """Kernels one layer forward launches: the fused layer kernel for T <= 8
     on the streaming path, else router + layer + combine; on the grouped path
@@ -372,11 +383,7 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks = clk.stop()
-    ms = e0.elapsed_time(e1)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / args.steps
     tok_s = world * T * args.steps / (ms / 1e3)
 
@@ -435,11 +442,7 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
             g3.replay() if g3 is not None else e2e_step()
         f1.record()
     stream.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
-    et = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(et, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = float(et.item())
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     import bit_expert_weight_gb300.smoe as S
     status = S.device_status(stream)
     res = {

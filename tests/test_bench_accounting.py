@@ -1,0 +1,77 @@
+"""bench.py's algorithmic bytes, flops and launch counts (the numerators of
+the roofline it reports), checked on the CPU against sizes the pages print
+and against counts written out by hand."""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from bit_expert_weight_gb300 import synth as Y  # noqa: E402
+
+
+class FakeModel:
+    """The fields of bench.DeviceModel the accounting reads."""
+
+    def __init__(self, wl, bits, ids, T, x_dtype=torch.bfloat16, grouped=False):
+        self.wl, self.bits, self.T, self.grouped = wl, bits, T, grouped
+        self.expert_bits, self.shared_bits = bench.depths(wl, bits)
+        self.ids = [torch.tensor(np.asarray(i, dtype=np.int32)) for i in ids]
+        self.x = [torch.zeros((T, wl.d), dtype=x_dtype) for _ in ids]
+
+
+def test_expert_bytes_match_the_pages_blob_sizes():
+    # ".smoe Binary Format": a Qwen3-235B expert (d 4096, f 1536) is
+    # 10,027,008 B at Q4 and 5,308,416 B at Q2 (codes + fp16 scales)
+    wl = Y.WORKLOADS["qwen235b"]
+    assert bench.expert_bytes(wl, wl.f, 4, 3) == 10_027_008
+    assert bench.expert_bytes(wl, wl.f, 2, 3) == 5_308_416
+
+
+def test_decode_layer_bytes():
+    ds = Y.WORKLOADS["deepseek16b"]  # 6 selected experts of 4,595,712 B + router + x/y
+    m = FakeModel(ds, 4, [[[0, 1, 2, 3, 4, 5]]], 1)
+    assert bench.layer_algorithmic_bytes(m) == 6 * 4_595_712 + 64 * 2048 * 2 + 2048 * (2 + 4)
+    qw = Y.WORKLOADS["qwen235b"]
+    m = FakeModel(qw, 4, [[list(range(8))]], 1)
+    assert bench.layer_algorithmic_bytes(m) == 8 * 10_027_008 + 128 * 4096 * 2 + 4096 * 6
+    # the same expert chosen twice is read once
+    m = FakeModel(ds, 4, [[[0, 1, 2, 3, 4, 5], [5, 4, 3, 2, 1, 0]]], 2)
+    assert bench.layer_algorithmic_bytes(m) == 6 * 4_595_712 + 64 * 2048 * 2 + 2 * 2048 * 6
+
+
+def test_mixed_depth_bytes_follow_each_experts_depth():
+    qw = Y.WORKLOADS["qwen235b_batched"]
+    m = FakeModel(qw, "mixed", [[list(range(8))]], 1)
+    eb = m.expert_bits
+    assert eb.count(4) == 32 and eb.count(2) == 96
+    want = sum(10_027_008 if eb[e] == 4 else 5_308_416 for e in range(8))
+    assert bench.layer_algorithmic_bytes(m) == want + 128 * 4096 * 2 + 4096 * 6
+
+
+def test_gateup_flops_and_bytes():
+    qw = Y.WORKLOADS["qwen235b_batched"]
+    T = 4096
+    ids = np.arange(T * 8, dtype=np.int32).reshape(T, 8) % 128
+    m = FakeModel(qw, 4, [ids], T, grouped=True)
+    assert bench.gateup_flops(m) == 4.0 * T * 8 * 4096 * 1536 == 824_633_720_832.0
+    # every expert's gate and up (2/3 of its blob), token rows in, bf16 h out
+    assert bench.gateup_bytes(m) == 128 * (2 * 10_027_008 // 3) + T * 4096 * 2 + T * 8 * 1536 * 2
+
+
+def test_launches_per_layer():
+    ds = Y.WORKLOADS["deepseek16b"]
+    assert bench.launches_per_layer(FakeModel(ds, 4, [[[0] * 6]], 1)) == 1       # fused
+    assert bench.launches_per_layer(FakeModel(ds, 4, [[[0] * 6] * 9], 9)) == 3   # router, layer, combine
+    # grouped, bf16 tokens: logits GEMM, routing, sort, gather, 2 GEMMs, combine
+    assert bench.launches_per_layer(FakeModel(ds, 4, [[[0] * 6]], 64, grouped=True)) == 7
+    assert bench.launches_per_layer(
+        FakeModel(ds, 4, [[[0] * 6]], 64, x_dtype=torch.float32, grouped=True)) == 6
+    # two depths: one gate/up and one down GEMM per depth
+    assert bench.launches_per_layer(FakeModel(ds, "mixed", [[[0] * 6]], 64, grouped=True)) == 9
