@@ -137,7 +137,7 @@ struct Plan {
     // grouped path (T >= kGroupedMinT only)
     bool grouped;
     int64_t grows;
-    size_t off_grow, off_gseg, off_gtile, off_gxs, off_gh, off_go;
+    size_t off_grow, off_gseg, off_gtile, off_gxs, off_gh, off_go, off_grw;
 };
 
 // Whether the forward takes the expert-sorted tensor-core path: a token
@@ -204,7 +204,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T, bool mixed = false)
     p.off_part = take(sizeof(float) * 4 * 2 * (size_t)p.ctas * 2 * 2 * 32);
     p.grouped = T >= kGroupedMinT || mixed;
     p.grows = 0;
-    p.off_grow = p.off_gseg = p.off_gtile = p.off_gxs = p.off_gh = p.off_go = 0;
+    p.off_grow = p.off_gseg = p.off_gtile = p.off_gxs = p.off_gh = p.off_go = p.off_grw = 0;
     if (p.grouped) {
         const int has_sh = L->shared_ffn_dim > 0 ? 1 : 0;
         p.grows = grouped_max_rows(T, E, k, has_sh);
@@ -213,7 +213,8 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T, bool mixed = false)
         p.off_gtile = take(sizeof(int32_t) * (size_t)p.ntiles * E);
         p.off_gxs = take(sizeof(uint16_t) * (size_t)p.grows * d);
         p.off_gh = take(sizeof(uint16_t) * (size_t)p.grows * p.fmax);
-        p.off_go = take(sizeof(float) * (size_t)p.grows * d);
+        p.off_go = take(sizeof(uint16_t) * (size_t)p.grows * d);
+        p.off_grw = take(sizeof(float) * (size_t)p.grows);
     }
     p.total = o;
     return p;
@@ -636,7 +637,10 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
         ga.xs = at<uint16_t>(workspace, P.off_gxs);
         ga.h = at<uint16_t>(workspace, P.off_gh);
         ga.hstride = P.fmax;
-        ga.o = at<float>(workspace, P.off_go);
+        ga.o = at<uint16_t>(workspace, P.off_go);
+        ga.w = ra.weights;
+        ga.sw = ra.shared_w;
+        ga.roww = at<float>(workspace, P.off_grw);
         ga.status = status;
         if (mixed) {
             ga.mixed = 1;
@@ -653,7 +657,7 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
                 return SMOE_ERR_CUDA;
             }
         }
-        return launch_grouped(ga, x, ra.x_bf16, ra.weights, ra.shared_w, y, stage_mask, s) ==
+        return launch_grouped(ga, x, ra.x_bf16, y, stage_mask, s) ==
                        cudaSuccess
                    ? SMOE_OK
                    : SMOE_ERR_CUDA;

@@ -668,17 +668,23 @@ __device__ void epilogue(const GroupedArgs &a, GSmem &sm)
                     }
                 }
             } else {
+                // the row's routing weight applied here, the product stored
+                // as bf16: the combine only adds the rows of each token
                 const int n0 = kGN * w.nt;
+                const float wr = valid ? __ldg(a.roww + row) : 0.f;
                 for (int c = 0; c < kGN && n0 + c < a.d; c += 16) {
                     uint32_t o[16];
                     tmem_ld16(taddr + c, o);
                     tmem_wait_ld();
                     if (valid) {
-                        float4 *dst = reinterpret_cast<float4 *>(a.o + row * a.d + n0 + c);
+                        uint32_t ov[8];
 #pragma unroll
-                        for (int m = 0; m < 4; ++m)
-                            dst[m] = make_float4(__uint_as_float(o[4 * m]), __uint_as_float(o[4 * m + 1]),
-                                                 __uint_as_float(o[4 * m + 2]), __uint_as_float(o[4 * m + 3]));
+                        for (int m = 0; m < 8; ++m)
+                            ov[m] = pack_bf16x2(wr * __uint_as_float(o[2 * m]),
+                                                wr * __uint_as_float(o[2 * m + 1]));
+                        uint4 *dst = reinterpret_cast<uint4 *>(a.o + row * a.d + n0 + c);
+                        dst[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                        dst[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
                     }
                 }
             }
@@ -946,6 +952,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const GroupedArgs a, const 
             row = -1;
         s_rows[j] = static_cast<int32_t>(row);
         a.rows_of[t * (k + 1) + j] = static_cast<int32_t>(row);
+        if (row >= 0)  // the weight the down GEMM's epilogue applies to this row
+            a.roww[row] = j < k ? __ldg(a.w + t * k + j) : __ldg(a.sw + t);
     }
     __syncthreads();
     for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
@@ -966,38 +974,31 @@ __global__ void __launch_bounds__(256) gather_kernel(const GroupedArgs a, const 
     }
 }
 
-// y[t] = sum_j w[t, j] o[row(t, j)] in rank order, then + shared weight *
-// o[shared row].
-__global__ void __launch_bounds__(256) grouped_combine_kernel(const float *o, int64_t T, int d, int k,
+// y[t] = sum of the token's weighted rows o[row(t, j)] (already scaled by
+// w[t, j] in the down GEMM) in rank order, then the shared expert's row.
+__global__ void __launch_bounds__(256) grouped_combine_kernel(const uint16_t *o, int64_t T, int d, int k,
                                                               int has_shared, const int32_t *rows,
-                                                              int64_t nrows, const float *w,
-                                                              const float *sw, float *y)
+                                                              int64_t nrows, float *y)
 {
     const int64_t t = blockIdx.x;
-    for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
+    const int nslot = k + (has_shared ? 1 : 0);
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < nslot; ++j) {
             const int32_t r = __ldg(rows + t * (k + 1) + j);
             if (r < 0 || r >= nrows)
                 continue;
-            const float wj = __ldg(w + t * k + j);
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(o + (int64_t)r * d + c));
-            acc.x = fmaf(wj, v.x, acc.x);
-            acc.y = fmaf(wj, v.y, acc.y);
-            acc.z = fmaf(wj, v.z, acc.z);
-            acc.w = fmaf(wj, v.w, acc.w);
+            const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(o + (int64_t)r * d + c));
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                acc[2 * m] += bf16lo_to_f32(u[m]);
+                acc[2 * m + 1] += bf16hi_to_f32(u[m]);
+            }
         }
-        const int32_t rs = has_shared ? __ldg(rows + t * (k + 1) + k) : -1;
-        if (rs >= 0 && rs < nrows) {
-            const int32_t r = rs;
-            const float ws = __ldg(sw + t);
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(o + (int64_t)r * d + c));
-            acc.x = fmaf(ws, v.x, acc.x);
-            acc.y = fmaf(ws, v.y, acc.y);
-            acc.z = fmaf(ws, v.z, acc.z);
-            acc.w = fmaf(ws, v.w, acc.w);
-        }
-        *reinterpret_cast<float4 *>(y + t * d + c) = acc;
+        float4 *dst = reinterpret_cast<float4 *>(y + t * d + c);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
 }
 
@@ -1277,8 +1278,8 @@ int64_t grouped_max_rows(int64_t T, int E, int k, int has_shared)
     return (r + kGM - 1) / kGM * kGM;
 }
 
-cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, const float *w,
-                           const float *sw, float *y, int stage_mask, cudaStream_t s)
+cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, float *y, int stage_mask,
+                           cudaStream_t s)
 {
     if (a.T == 0)
         return cudaSuccess;
@@ -1324,7 +1325,7 @@ cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, cons
                               : launch_gemm_t<2, 1, false>(a, mh, s)) != cudaSuccess)
             return e;
         grouped_combine_kernel<<<nt, 256, 0, s>>>(a.o, a.T, a.d, a.k, a.has_shared, a.rows_of,
-                                                  a.rows, w, sw, y);
+                                                  a.rows, y);
         e = cudaGetLastError();
     }
     return e;

@@ -165,7 +165,9 @@ struct GroupedArgs {
     uint16_t *xs;                  // bf16 [rows][d]
     uint16_t *h;                   // bf16 [rows][hstride]
     int hstride;                   // max(f, fs)
-    float *o;                      // [rows][d]
+    uint16_t *o;                   // bf16 [rows][d]: row weight x (W_down h)
+    const float *w, *sw;           // routing weights [T][k], shared weights [T]
+    float *roww;                   // [rows] the weight of each sorted row
     int *status;
     // mixed bit depth per routed expert: bit e of q4mask set = expert e is
     // Q4, clear = Q2; the bank holds the experts back to back at their own
@@ -183,8 +185,8 @@ int64_t grouped_max_rows(int64_t T, int E, int k, int has_shared);
 cudaError_t launch_tc_logits(const uint16_t *x, const uint16_t *router_w, int64_t T, int d, int E,
                              int Epad, float *logits, int *status, cudaStream_t stream);
 // stage_mask: 1 sort + gather, 2 gate/up GEMM, 4 down GEMM + combine.
-cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, const float *w,
-                           const float *sw, float *y, int stage_mask, cudaStream_t stream);
+cudaError_t launch_grouped(const GroupedArgs &a, const void *x, int x_bf16, float *y, int stage_mask,
+                           cudaStream_t stream);
 
 int layer_grid_ctas_max();
 cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream);

@@ -326,7 +326,9 @@ smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, voi
  *              for small batches
  *   grouped    tokens sorted by expert, weights decoded to bf16 in shared
  *              memory, tensor-core GEMMs (tcgen05) with bf16 activations and
- *              bf16 h, fp32 accumulation; taken when T >= 16 and
+ *              bf16 h, fp32 accumulation, each expert's output scaled by its
+ *              routing weight and rounded to bf16 before the fp32 sum over
+ *              the token's experts; taken when T >= 16 and
  *              T * top_k >= 16 * num_experts (smoe_moe_path tells which)
  * Both are deterministic: the same inputs give the same bits on every call.
  *   x           device [T, d_model], fp32 or bf16 (x_dtype)

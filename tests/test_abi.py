@@ -156,7 +156,8 @@ def test_path_selection_and_path_argument(libs):
     w15 = L.smoe_moe_workspace_bytes(ctypes.byref(desc), 15)
     w16 = L.smoe_moe_workspace_bytes(ctypes.byref(desc), 16)
     rows16 = 16 * 2 + 8 * 127
-    assert w16 - w15 >= rows16 * (256 * 2 + 128 * 2 + 256 * 4)
+    # per sorted row: bf16 token (d), bf16 h (f), bf16 weighted output (d), its weight
+    assert w16 - w15 >= rows16 * (256 * 2 + 128 * 2 + 256 * 2 + 4)
 
 
 def test_router_options_are_validated_on_the_host(libs):
@@ -236,6 +237,6 @@ def test_mixed_depth_entry_points_validate_on_the_host(libs):
                                     P(1 << 20), 1 << 30, None, None, 5, None) == -1  # bad path
     w1 = L.smoe_moe_workspace_bytes_mixed(ctypes.byref(desc), 1)
     assert w1 > L.smoe_moe_workspace_bytes(ctypes.byref(desc), 1)
-    assert w1 >= 128 * (256 * 2 + 128 * 2 + 256 * 4)      # one padded 128-row tile per segment
+    assert w1 >= 128 * (256 * 2 + 128 * 2 + 256 * 2 + 4)  # one padded 128-row tile per segment
     assert L.smoe_moe_workspace_bytes_mixed(ctypes.byref(desc), 64) == \
         L.smoe_moe_workspace_bytes(ctypes.byref(desc), 64)
