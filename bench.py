@@ -462,6 +462,8 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
         "expert_bits": list(model.expert_bits), "shared_bits": model.shared_bits,
         "gemm1_flops": gateup_flops(model) if model.grouped else None,
         "gemm1_bytes": gateup_bytes(model) if model.grouped else None,
+        "y0": model.y[0].float().cpu().numpy(),
+        "routing": routing_summary([i.cpu().numpy() for i in model.ids], wl.E),
     }
     del model, graph, g2, g3
     torch.cuda.empty_cache()
@@ -502,15 +504,42 @@ def prepare_oracle(wl, bits, layer, T):
 
 
 def time_oracle(wl, bits, prep):
-    """Seconds for one oracle layer forward of the prepared tokens."""
+    """(seconds, y) of one oracle layer forward of the prepared tokens."""
     import oracle as O
     xf, router, blobs, sb, sg, bias = prep
     ebits, sbits = depths(wl, bits)
     t0 = time.perf_counter()
-    O.moe_forward(wl.d, wl.f, wl.E, wl.k, wl.norm, sbits, router, blobs, xf, expert_bias=bias,
-                  shared_blob=sb, fs=wl.shared_f, shared_gate=sg,
-                  expert_bits=ebits if bits == "mixed" else None)
-    return time.perf_counter() - t0
+    y, _, _, _ = O.moe_forward(wl.d, wl.f, wl.E, wl.k, wl.norm, sbits, router, blobs, xf,
+                               expert_bias=bias, shared_blob=sb, fs=wl.shared_f, shared_gate=sg,
+                               expert_bits=ebits if bits == "mixed" else None)
+    return time.perf_counter() - t0, y
+
+
+def parity_summary(y_gpu, y_ref, bar):
+    """Largest elementwise difference of the GPU layer output from the
+    oracle's, against the path's bar (a fraction of max |y_ref|)."""
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    err = float(np.abs(y_gpu - y_ref).max()) if y_ref.size else 0.0
+    ref = float(np.abs(y_ref).max()) if y_ref.size else 0.0
+    rel = err / ref if ref > 0 else 0.0
+    return {"max_abs_err": err, "ref_max_abs": ref, "rel": rel, "bar": bar, "ok": rel <= bar}
+
+
+def routing_summary(ids_list, E):
+    """Realised routing of a step: selections per expert summed over the
+    layers, the distinct experts per layer, the busiest expert's share."""
+    hist = np.zeros(E, dtype=np.int64)
+    distinct = []
+    for ids in ids_list:
+        v = np.asarray(ids).ravel()
+        v = v[(v >= 0) & (v < E)]
+        hist += np.bincount(v, minlength=E)
+        distinct.append(len(np.unique(v)))
+    total = int(hist.sum())
+    return {"distinct_experts_per_layer": float(np.mean(distinct)) if distinct else 0.0,
+            "max_expert_share": float(hist.max()) / total if total else 0.0,
+            "histogram": hist.tolist()}
 
 
 def run_reference(args, wl, T, n_layers, world, rank):
@@ -523,7 +552,7 @@ def run_reference(args, wl, T, n_layers, world, rank):
     prep = prepare_oracle(wl, bits, 0, T)
     for _ in range(args.warmup):
         time_oracle(wl, bits, prep)
-    per = [time_oracle(wl, bits, prep) for _ in range(args.steps)]
+    per = [time_oracle(wl, bits, prep)[0] for _ in range(args.steps)]
     layer_s = float(np.mean(per))
     step_s = layer_s * n_layers
     v = T / step_s
@@ -581,11 +610,15 @@ def main():
     r = results[main_bits]
     traffic = ncu_traffic(args.workload, main_bits)
     cpu = None
+    parity = None
     if rank == 0 and not args.no_cpu_baseline:
         prep = prepare_oracle(wl, main_bits, 0, T)
-        times, t_start = [], time.perf_counter()
+        times, t_start, y_ref = [], time.perf_counter(), None
         while time.perf_counter() - t_start < 10.0 or len(times) < 2:
-            times.append(time_oracle(wl, main_bits, prep))
+            sec, y_ref = time_oracle(wl, main_bits, prep)
+            times.append(sec)
+        parity = parity_summary(r["y0"], y_ref, 2e-2 if r["grouped"] else 1e-3)
+        parity.update({"layer": 0, "tokens": T})
         dt = float(np.mean(times))
         cpu = {"value": T / (dt * n_layers), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"oracle forward of {T} token(s) through layer 0 repeated "
@@ -649,6 +682,8 @@ def main():
         "cpu_baseline": cpu,
         "setup_s": round(r["setup_s"], 1),
         "device_status": r["device_status"],
+        "parity_vs_oracle": parity,
+        "routing": r["routing"],
     }
     for b in bits_list[1:]:
         q = results[b]

@@ -75,3 +75,24 @@ def test_launches_per_layer():
         FakeModel(ds, 4, [[[0] * 6]], 64, x_dtype=torch.float32, grouped=True)) == 6
     # two depths: one gate/up and one down GEMM per depth
     assert bench.launches_per_layer(FakeModel(ds, "mixed", [[[0] * 6]], 64, grouped=True)) == 9
+
+
+def test_parity_and_routing_summaries():
+    y_ref = np.array([[1.0, -2.0], [0.5, 4.0]])
+    p = bench.parity_summary(y_ref + np.array([[0.0, 0.002], [0.0, 0.0]]), y_ref, 1e-3)
+    assert p["max_abs_err"] == pytest.approx(0.002) and p["ref_max_abs"] == 4.0
+    assert p["rel"] == pytest.approx(5e-4) and p["ok"]
+    assert not bench.parity_summary(y_ref + 0.01, y_ref, 1e-3)["ok"]
+    r = bench.routing_summary([np.array([[0, 1], [1, 3]]), np.array([[1, 2], [3, 3]])], 4)
+    assert r["histogram"] == [1, 3, 1, 3]
+    assert r["distinct_experts_per_layer"] == 3.0
+    assert r["max_expert_share"] == 3 / 8
+
+
+def test_oracle_leg_returns_time_and_output():
+    """The CPU baseline leg times the oracle and keeps its output for the
+    parity field (tiny workload, 2 tokens)."""
+    wl = Y.WORKLOADS["tiny"]
+    prep = bench.prepare_oracle(wl, 4, 0, 2)
+    sec, y = bench.time_oracle(wl, 4, prep)
+    assert sec > 0 and y.shape == (2, wl.d) and np.isfinite(y).all()
