@@ -1,16 +1,18 @@
 // grouped.cu -- the expert-sorted batched path of one MoE layer: tokens
 // gathered per expert, a grouped GEMM on the fifth-generation tensor cores
 // (tcgen05.mma kind::f16, bf16 operands, fp32 accumulators in tensor memory)
-// for gate/up with SiLU(g)*u in the epilogue, the same for down, then the
-// routing-weighted combine.
+// for gate/up with SiLU(g)*u in the epilogue, the same for down with the
+// routing weight applied in its epilogue, then the sum over each token's
+// rows.
 //
 // The arithmetic is the one of "Model Agnosticism" / "Why Quantise"
 // (SMOE-Q4 w = (c - 7.5)/7.5 * s, SMOE-Q2 w = (c - 1.5)/1.5 * s, groups of
 // 64 along the input dim) and of "CMF v2 -- Format Specification", 2.2 MoE
 // (y = sum_j w_j * FFN_{e_j}(x) over the selected experts, plus the shared
 // expert weighted by sigmoid(gate . x)).  Here the weights are dequantised to
-// bf16 in shared memory (never written to global memory) and the
-// activations and h are rounded to bf16: the tensor-core operand type.
+// bf16 in shared memory (never written to global memory), the activations
+// and h are rounded to bf16 (the tensor-core operand type), and so is each
+// expert's weighted output row before the fp32 sum.
 //
 // Rows: every segment (a routed expert, then the shared expert) owns a run of
 // rows padded to a multiple of 128 in the sorted activation matrix; the
@@ -21,18 +23,22 @@
 // n-tile) are adjacent: CTAs working at the same time read the same weights.
 //
 // One persistent CTA per SM, 28 warps (warp w issues on sub-partition w % 4):
-//   warp 0        code producer: bulk copies of the 16 code tiles of every
-//                 K block (3-stage ring, freed once decoded)
+//   warp 0        code producer: the 16 code tiles of every K block, in
+//                 stages of 1 or 4 K blocks (one tensor copy per stage, or
+//                 one bulk copy per strip for mixed-depth banks), freed
+//                 once decoded
 //   warp 1        tensor memory allocation; lane 0 issues the MMAs, one
 //                 commit per K block frees that block's stage
-//   warp 2        activation producer: TMA of the item's one or two 128 x 64
-//                 bf16 activation tiles of every K block, 128-byte swizzle
-//   warps 3..6    epilogue: tensor memory -> registers -> h (bf16) or o (fp32)
+//   warp 2        activation producer: TMA of the item's one or two
+//                 activation tiles of every K block (boxes of 32, 64 or 128
+//                 rows x 64 bf16, 128-byte swizzle)
+//   warps 3..6    epilogue: tensor memory -> registers -> h (bf16) or the
+//                 row's routing weight x o (bf16)
 //   16 warps      decoders (warps 7..27 off sub-partition 1; the others
 //                 exit), one code tile each per K block: bf16 weights in the
 //                 128-byte-swizzled K-major layout the MMA reads
-// A stage holds a K block's activations and decoded weights: 3 stages when
-// items pair two m-tiles (two activation tiles each), 4 otherwise.
+// A stage holds a K block's activations and decoded weights: 3 stages (two
+// activation tiles each when items pair two m-tiles).
 // Two accumulators of 256 columns: an item of two m-tiles uses both, an item
 // of one m-tile alternates between them so that its epilogue overlaps the
 // next item's MMAs.  Every wait is bounded; a timeout records
