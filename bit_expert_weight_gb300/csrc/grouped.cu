@@ -95,7 +95,7 @@ constexpr uint32_t kBTileBytes = kGN * kGK * 2;   // 32 KB
 // shared memory holds beside the code ring (two activation tiles per stage
 // for items of two m-tiles, code stages of 4 K blocks for items of one).
 // 4 stages with code stages of 1 K block measured slower.
-__host__ __device__ constexpr int num_stages(bool pair) { return 3; }
+__host__ __device__ constexpr int num_stages(bool /* pair */) { return 3; }
 __host__ __device__ constexpr uint32_t a_stage_bytes(bool pair)
 {
     return pair ? 2 * kATileBytes : kATileBytes;
