@@ -240,3 +240,15 @@ def test_mixed_depth_entry_points_validate_on_the_host(libs):
     assert w1 >= 128 * (256 * 2 + 128 * 2 + 256 * 2 + 4)  # one padded 128-row tile per segment
     assert L.smoe_moe_workspace_bytes_mixed(ctypes.byref(desc), 64) == \
         L.smoe_moe_workspace_bytes(ctypes.byref(desc), 64)
+
+
+def test_binding_refuses_mixed_layers_where_the_abi_has_no_depths(libs):
+    """The built-in-workspace entry point takes single-depth layers only; the
+    binding says so before any call."""
+    S, _ = libs
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(256 * 8, dtype=torch.int16)  # never read: the binding refuses first
+    lay = S.MoELayer(256, 128, 8, 2, True, 4, t, t, expert_bits=[4, 2] * 4)
+    assert lay.expert_bits == [4, 2, 4, 2, 4, 2, 4, 2]
+    with pytest.raises(ValueError):
+        S.forward_noalloc(lay, t)
