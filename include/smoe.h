@@ -15,9 +15,15 @@
  *     shared_expert_ffn_dim, max_experts_per_layer (router rows),
  *     norm_topk_prob, moe_top_k; routing width capped at 16; SiLU only.
  *   "CMF v2 -- Format Specification", 2.2 MoE -- softmax over all router
- *     logits, top-k with ties to the lower index, selection-only
- *     expert_bias, optional renormalisation, y = sum_e w_e FFN_e(x), shared
- *     expert weighted by sigmoid(shared_expert_gate . x) (else 1).
+ *     logits (or per-expert sigmoid scores), top-k with ties to the lower
+ *     index, selection-only expert_bias, optional renormalisation, a routed
+ *     scaling factor, y = sum_e w_e FFN_e(x), shared expert weighted by
+ *     sigmoid(shared_expert_gate . x) (else 1); each expert entry with its
+ *     own dtype (per-expert depth: smoe_repack_mixed, smoe_moe_forward_mixed).
+ *   "CMF v2 -- Format Specification", 5 -- routing masks (expert bitfields,
+ *     LSB-first): smoe_router_opts.expert_mask.
+ *   ".smoe Binary Format", Expert Table Entry / Tensor Descriptor / Arch
+ *     Block "SARC" -- the vault reader (smoe_vault_*).
  *
  * Conventions (all entry points):
  *   - Every pointer argument is DEVICE memory owned by the caller unless the
