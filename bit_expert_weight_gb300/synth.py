@@ -114,10 +114,53 @@ def values_f32(key: int, n: int, sigma: float, p_out: float = 0.0, out_mult: flo
     return out
 
 
+def values_bf16_numpy(key: int, n: int, sigma: float, p_out: float = 0.0,
+                      out_mult: float = 10.0, p_zero: float = 0.0, start: int = 0) -> np.ndarray:
+    """bf16 bit patterns (uint16) of a stream: the definition, in numpy."""
+    return _f32_to_bf16_rne(values_f32(key, n, sigma, p_out, out_mult, p_zero, start))
+
+
+# The same stream computed by csrc/synth_host.c (plain C, built here with gcc
+# on first use): identical bits, about a hundred times faster, so that whole
+# full-size experts can be regenerated on the host.
+_HOST_SO = None
+
+
+def _host_lib():
+    global _HOST_SO
+    if _HOST_SO is None:
+        import ctypes
+        import os
+        import subprocess
+        here = os.path.dirname(os.path.abspath(__file__))
+        src = os.path.join(here, "csrc", "synth_host.c")
+        out_dir = os.path.join(here, "_build")
+        so = os.path.join(out_dir, "libsynth_host.so")
+        os.makedirs(out_dir, exist_ok=True)
+        if not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+            tmp = so + f".tmp{os.getpid()}"
+            subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                                   "-shared", "-o", tmp, src])
+            os.replace(tmp, so)
+        lib = ctypes.CDLL(so)
+        lib.synth_values_bf16.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_float,
+                                          ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64,
+                                          ctypes.c_int64, ctypes.c_void_p]
+        lib.synth_values_bf16.restype = ctypes.c_int
+        _HOST_SO = lib
+    return _HOST_SO
+
+
 def values_bf16(key: int, n: int, sigma: float, p_out: float = 0.0, out_mult: float = 10.0,
                 p_zero: float = 0.0, start: int = 0) -> np.ndarray:
-    """bf16 bit patterns (uint16) of a stream."""
-    return _f32_to_bf16_rne(values_f32(key, n, sigma, p_out, out_mult, p_zero, start))
+    """bf16 bit patterns (uint16) of a stream (the C twin of
+    values_bf16_numpy; tests/test_synth.py checks the two agree)."""
+    out = np.empty(n, np.uint16)
+    if n:
+        _host_lib().synth_values_bf16(key & MASK64, n, float(np.float32(sigma)),
+                                      float(np.float32(sigma * out_mult)), _thresh(p_out),
+                                      _thresh(p_zero), start, out.ctypes.data)
+    return out
 
 
 # ------------------------------------------------------------------ workloads
@@ -223,10 +266,11 @@ class Workload:
         Returns (x_f32, x_bits) where x_bits is the uint16 bf16 pattern for
         bf16 workloads and None for fp32 ones."""
         key = stream_key(self.seed, layer, 0, ROLE_X)
-        v = values_f32(key, T * self.d, 1.0, start=start_token * self.d).reshape(T, self.d)
         if self.x_dtype == "bf16":
-            bits = _f32_to_bf16_rne(v)
+            # the bf16 rounding of the fp32 stream, i.e. values_bf16 (C twin)
+            bits = values_bf16(key, T * self.d, 1.0, start=start_token * self.d).reshape(T, self.d)
             return bf16_to_f32(bits), bits
+        v = values_f32(key, T * self.d, 1.0, start=start_token * self.d).reshape(T, self.d)
         return v, None
 
 

@@ -62,3 +62,34 @@ def test_zipf_bias_construction():
     s_lo, s_mid, s_hi = (wl.zipf_share(0, t, 1024, lg) for t in (0.25, wl.zipf_tau, 0.5))
     assert s_lo < s_mid < s_hi
     assert abs(s_mid - target) <= 0.2 * target
+
+
+def test_c_twin_matches_the_numpy_definition():
+    """values_bf16 runs the plain-C twin of the generator; it must give the
+    numpy definition's bits for every parameter mix (outliers, zeros, an
+    offset start, the tiny layer's 20 % zeros, unit-sigma activations)."""
+    cases = [
+        (S.stream_key(1, 0, 3, S.ROLE_GATE), 50_000, 0.02, 0.01, 0.0, 0),
+        (S.stream_key(2, 93, 127, S.ROLE_DOWN), 20_000, 0.02, 0.01, 0.0, 123_457),
+        (S.stream_key(0, 0, 5, S.ROLE_UP), 30_000, 0.02, 0.01, 0.20, 0),
+        (S.stream_key(3, 0, 0, S.ROLE_X), 10_000, 1.0, 0.0, 0.0, 4096 * 7),
+        (S.stream_key(4, 1, S.SHARED_EXPERT, S.ROLE_SHARED_GATE), 2048, 0.02, 0.0, 0.0, 0),
+    ]
+    for key, n, sigma, p_out, p_zero, start in cases:
+        a = S.values_bf16(key, n, sigma, p_out=p_out, p_zero=p_zero, start=start)
+        b = S.values_bf16_numpy(key, n, sigma, p_out=p_out, p_zero=p_zero, start=start)
+        assert a.dtype == np.uint16 and a.shape == (n,)
+        assert np.array_equal(a, b), (key, start)
+
+
+def test_bf16_activations_are_the_rounded_fp32_stream():
+    """Workload.activations takes bf16 tokens from the C twin; they must be
+    the bf16 rounding of the fp32 stream (the definition), also at an
+    offset token."""
+    wl = S.WORKLOADS["deepseek16b"]
+    for start in (0, 7):
+        x, bits = wl.activations(3, 5, start_token=start)
+        key = S.stream_key(wl.seed, 3, 0, S.ROLE_X)
+        v = S.values_f32(key, 5 * wl.d, 1.0, start=start * wl.d).reshape(5, wl.d)
+        assert np.array_equal(bits, S._f32_to_bf16_rne(v))
+        assert np.array_equal(x, S.bf16_to_f32(bits))
