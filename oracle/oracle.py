@@ -19,7 +19,8 @@ import numpy as np
 __all__ = [
     "build_oracle", "lib", "quantize", "pack", "unpack", "dequantize", "encode", "decode",
     "grid", "f16_to_f32", "f32_to_f16", "stream_bytes", "scales_bytes", "blob_bytes",
-    "make_blob", "router_logits", "route", "expert_ffn", "moe_apply", "moe_forward",
+    "make_blob", "router_logits", "route", "expert_ffn", "moe_apply", "moe_apply_threads",
+    "moe_forward",
     "GROUP", "NCAND",
 ]
 
@@ -40,7 +41,7 @@ def build_oracle(force: bool = False) -> str:
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + f".tmp{os.getpid()}"
         subprocess.check_call([
-            "gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+            "gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread",
             "-o", tmp, _SRC, "-lm",
         ])
         os.replace(tmp, _SO)
@@ -97,6 +98,9 @@ def lib():
             L.oracle_route_ex2.argtypes = [P, I64, I32, I32, I32, P, I32, F, P, P, P]
             L.oracle_route_ex2.restype = ctypes.c_int
             L.oracle_moe_forward_ex.restype = ctypes.c_int
+            L.oracle_moe_apply_threads.argtypes = [I32, I32, I32, I32, ctypes.c_int, P, P, P, I32,
+                                                   P, P, I64, P, P, P, ctypes.c_int]
+            L.oracle_moe_apply_threads.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -286,6 +290,28 @@ def moe_apply(d, f, E, k, bits, blobs, x, ids, weights, shared_blob=None, fs=0,
                                       _p(sb), fs, _p(sg), _p(xx), T, _p(ii), _p(ww), _p(y))
     if rc:
         raise ValueError(f"oracle_moe_apply failed ({rc})")
+    del keep
+    return y
+
+
+def moe_apply_threads(d, f, E, k, bits, blobs, x, ids, weights, nthreads, shared_blob=None,
+                      fs=0, shared_gate=None, expert_bits=None):
+    """moe_apply with the (token, slot) expert FFNs spread over nthreads
+    threads; the same bits as moe_apply (the combine stays serial)."""
+    xx = _c(x, np.float32)
+    T = xx.shape[0]
+    table, keep = _blob_table(blobs, E)
+    sb = None if shared_blob is None else _c(shared_blob, np.uint8)
+    sg = None if shared_gate is None else _c(shared_gate, np.uint16)
+    ii = _c(ids, np.int32)
+    ww = _c(weights, np.float32)
+    y = np.zeros((T, d), np.float32)
+    eb_ = None if expert_bits is None else _c(expert_bits, np.int32)
+    rc = lib().oracle_moe_apply_threads(d, f, E, k, bits, _p(eb_),
+                                        ctypes.cast(table, ctypes.c_void_p), _p(sb), fs, _p(sg),
+                                        _p(xx), T, _p(ii), _p(ww), _p(y), int(nthreads))
+    if rc:
+        raise ValueError(f"oracle_moe_apply_threads failed ({rc})")
     del keep
     return y
 

@@ -6,7 +6,7 @@
  * baseline may call it; the product path never links or executes it.  It
  * shares no code, header, table or constant generator with the CUDA library.
  *
- * Build: gcc -O2 -ffp-contract=off -fno-fast-math -fPIC -shared
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -fPIC -shared -pthread
  * With contraction off every float operation below is rounded to fp32 on its
  * own, which is what makes the quantiser's codes reproducible bit for bit.
  *
@@ -37,6 +37,7 @@
  *   MSE is accumulated in double; the first (smallest) candidate wins ties.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -552,6 +553,148 @@ int oracle_moe_apply_mixed(int32_t d, int32_t f, int32_t E, int32_t k, int bits,
 done:
     free(o);
     free(acc);
+    return rc;
+}
+
+/* The same result as oracle_moe_apply_mixed, bit for bit, with the expert
+ * FFNs of all (token, slot) items spread over nthreads POSIX threads: each
+ * item runs the unchanged scalar oracle_expert_ffn on its own output row;
+ * the combine then runs on the calling thread in exactly the serial order
+ * (rank order in double, then the shared expert).  Only the benchmark's CPU
+ * baseline uses it, to time the oracle on every host core. */
+struct ffn_item {
+    const uint8_t *blob;
+    int32_t f, bits;
+    const float *x;
+    float *out;
+};
+struct ffn_pool {
+    const struct ffn_item *items;
+    int64_t n;
+    int32_t d;
+    int64_t next;
+    int failed;
+    pthread_mutex_t mu;
+};
+
+static void *ffn_worker(void *arg)
+{
+    struct ffn_pool *p = (struct ffn_pool *)arg;
+    for (;;) {
+        pthread_mutex_lock(&p->mu);
+        const int64_t i = p->next++;
+        pthread_mutex_unlock(&p->mu);
+        if (i >= p->n)
+            return NULL;
+        const struct ffn_item *it = &p->items[i];
+        if (oracle_expert_ffn(it->blob, p->d, it->f, it->bits, it->x, it->out, NULL)) {
+            pthread_mutex_lock(&p->mu);
+            p->failed = 1;
+            pthread_mutex_unlock(&p->mu);
+        }
+    }
+}
+
+int oracle_moe_apply_threads(int32_t d, int32_t f, int32_t E, int32_t k, int bits,
+                             const int32_t *expert_bits, const uint8_t *const *blobs,
+                             const uint8_t *shared_blob, int32_t fs, const uint16_t *shared_gate,
+                             const float *x, int64_t T, const int32_t *ids, const float *wts,
+                             float *y, int nthreads)
+{
+    if (d <= 0 || f <= 0 || E <= 0 || k < 1 || (bits != 2 && bits != 4) || nthreads < 1)
+        return -1;
+    if (expert_bits)
+        for (int32_t e = 0; e < E; ++e)
+            if (expert_bits[e] != 2 && expert_bits[e] != 4)
+                return -1;
+    const int has_sh = shared_blob && fs > 0;
+    const int64_t per_t = k + (has_sh ? 1 : 0);
+    struct ffn_item *items = (struct ffn_item *)malloc(sizeof(struct ffn_item) * (size_t)(T * per_t + 1));
+    float *o = (float *)malloc(sizeof(float) * (size_t)(T * per_t * d + 1));
+    double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int rc = 0, started = 0;
+    struct ffn_pool pool;
+    if (!items || !o || !acc || !th) {
+        rc = -1;
+        goto done;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < k; ++j) {
+            const int32_t e = ids[t * k + j];
+            if (e < 0 || e >= E) {
+                rc = -1;
+                goto done;
+            }
+            if (!blobs[e]) {
+                rc = -2;
+                goto done;
+            }
+            struct ffn_item *it = &items[t * per_t + j];
+            it->blob = blobs[e];
+            it->f = f;
+            it->bits = expert_bits ? expert_bits[e] : bits;
+            it->x = x + t * d;
+            it->out = o + (t * per_t + j) * d;
+        }
+        if (has_sh) {
+            struct ffn_item *it = &items[t * per_t + k];
+            it->blob = shared_blob;
+            it->f = fs;
+            it->bits = bits;
+            it->x = x + t * d;
+            it->out = o + (t * per_t + k) * d;
+        }
+    }
+    pool.items = items;
+    pool.n = T * per_t;
+    pool.d = d;
+    pool.next = 0;
+    pool.failed = 0;
+    pthread_mutex_init(&pool.mu, NULL);
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, ffn_worker, &pool) != 0)
+            break;
+        ++started;
+    }
+    if (started == 0)
+        ffn_worker(&pool);
+    for (int i = 0; i < started; ++i)
+        pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&pool.mu);
+    if (pool.failed) {
+        rc = -1;
+        goto done;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        const float *xt = x + t * d;
+        for (int32_t i = 0; i < d; ++i)
+            acc[i] = 0.0;
+        for (int32_t j = 0; j < k; ++j) {
+            const float *oj = o + (t * per_t + j) * d;
+            for (int32_t i = 0; i < d; ++i)
+                acc[i] += (double)wts[t * k + j] * (double)oj[i];
+        }
+        if (has_sh) {
+            double sw = 1.0;
+            if (shared_gate) {
+                double z = 0.0;
+                for (int32_t i = 0; i < d; ++i)
+                    z += (double)bf16_bits_to_f32(shared_gate[i]) * (double)xt[i];
+                sw = 1.0 / (1.0 + exp(-z));
+            }
+            const float *os = o + (t * per_t + k) * d;
+            for (int32_t i = 0; i < d; ++i)
+                acc[i] += sw * (double)os[i];
+        }
+        for (int32_t i = 0; i < d; ++i)
+            y[t * d + i] = (float)acc[i];
+    }
+done:
+    free(items);
+    free(o);
+    free(acc);
+    free(th);
     return rc;
 }
 

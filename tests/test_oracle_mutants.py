@@ -56,7 +56,7 @@ def test_pins_reject_mutant(name, old, new, tmp_path):
     mut.write_text(src.replace(old, new))
     so = tmp_path / "libmutant.so"
     subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-                           "-shared", "-o", str(so), str(mut), "-lm"])
+                           "-shared", "-pthread", "-o", str(so), str(mut), "-lm"])
     env = dict(os.environ, SMOE_ORACLE_SO=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_quant.py"),

@@ -230,3 +230,28 @@ def test_mixed_bit_depth_forward_matches_dense_brute_force():
     y4u, _, _, _ = O.moe_forward(d, f, E, k, True, 4, router,
                                  [layers[4][0][e]["blob"] for e in range(E)], x)
     assert np.array_equal(y4, y4u)
+
+
+def test_threaded_apply_gives_the_serial_bits():
+    """The benchmark's all-cores oracle leg (expert FFNs of the (token, slot)
+    items on several threads, the combine serial in rank order) must equal
+    the single-threaded oracle bit for bit; also checked against the dense
+    brute force so that a shared mistake would still show."""
+    d, f, E, k, fs, T = 128, 64, 5, 3, 64, 4
+    experts, router = make_layer(d, f, E, 4, seed=21, shared_f=fs)
+    blobs = [e["blob"] for e in experts[:E]]
+    gate = bf16((np.random.default_rng(5).standard_normal(d) * 0.3).astype(np.float32))
+    x = np.random.default_rng(6).standard_normal((T, d)).astype(np.float32)
+    _, ids, w, _ = O.moe_forward(d, f, E, k, True, 4, router, blobs, x)
+    ref = O.moe_apply(d, f, E, k, 4, blobs, x, ids, w, shared_blob=experts[E]["blob"], fs=fs,
+                      shared_gate=gate)
+    for nt in (1, 3, 16):
+        got = O.moe_apply_threads(d, f, E, k, 4, blobs, x, ids, w, nt,
+                                  shared_blob=experts[E]["blob"], fs=fs, shared_gate=gate)
+        assert np.array_equal(got, ref), nt
+    gv = S.bf16_to_f32(gate).astype(np.float64)
+    for t in range(T):
+        xt = x[t].astype(np.float64)
+        dense = sum(float(w[t, j]) * swiglu(experts[ids[t, j]], xt) for j in range(k))
+        dense = dense + expit(gv @ xt) * swiglu(experts[E], xt)
+        assert np.allclose(ref[t], dense, rtol=1e-4, atol=1e-5 * np.abs(dense).max())
