@@ -91,8 +91,32 @@ def test_parity_and_routing_summaries():
 
 def test_oracle_leg_returns_time_and_output():
     """The CPU baseline leg times the oracle and keeps its output for the
-    parity field (tiny workload, 2 tokens)."""
+    parity field (tiny workload, 2 tokens): one thread and several threads
+    give the same output."""
     wl = Y.WORKLOADS["tiny"]
-    prep = bench.prepare_oracle(wl, 4, 0, 2)
-    sec, y = bench.time_oracle(wl, 4, prep)
+    preps = bench.prepare_oracle(wl, 4, [0], 2)
+    sec, y = bench.time_oracle(wl, 4, preps[0])
     assert sec > 0 and y.shape == (2, wl.d) and np.isfinite(y).all()
+    sec4, y4 = bench.time_oracle(wl, 4, preps[0], nthreads=4)
+    assert sec4 > 0 and np.array_equal(y, y4)
+    mean_s, passes, ys = bench.time_oracle_layers(wl, 4, preps, 2, 0.0)
+    assert mean_s > 0 and passes == 1 and np.array_equal(ys[0], y)
+
+
+def test_check_layers_are_the_spot_check_layers():
+    """Qwen3-235B-like stack: the oracle spot-checks layers 0, 31, 62 and 93
+    of 94; short stacks are checked whole."""
+    assert bench.check_layers(94) == [0, 31, 62, 93]
+    assert bench.check_layers(27) == [0, 9, 17, 26]
+    assert bench.check_layers(2) == [0, 1]
+
+
+def test_both_arms_print_the_same_config():
+    """The reference arm's config dict is computed from the workload alone,
+    like the GPU arm's (resident bytes of the 94-layer Q4 stack: 128 x 94 x
+    10,027,008 B)."""
+    wl = Y.WORKLOADS["qwen235b"]
+    c = bench.config_dict(wl, 94, 1, 4, 1, True)
+    assert c == bench.config_dict(wl, 94, 1, 4, 1, True)
+    assert c["resident_GB"] == round(128 * 94 * 10_027_008 / 1e9, 3)
+    assert c["layers"] == 94 and c["tokens_per_step"] == 1 and c["bits"] == 4
