@@ -23,20 +23,46 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SMOE_NOALLOC_SC
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[kMaxDevices] = {nullptr};
+void *g_scratch_ctx[kMaxDevices] = {nullptr};
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// The driver's current context (cuCtxGetCurrent through the runtime's
+// driver entry point, so the library needs no link to libcuda), or null.
+void *current_context()
+{
+    using get_ctx_fn = int (*)(void **);
+    static get_ctx_fn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<get_ctx_fn>(p);
+    }();
+    void *ctx = nullptr;
+    if (!fn || fn(&ctx) != 0)
+        return nullptr;
+    return ctx;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up with
+// that device current and cached per device together with the context it
+// was looked up in: a new context (after a device reset) may have loaded the
+// module, and with it the array, at another address.
 smoe_status scratch_address(void **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return SMOE_ERR_CUDA;
+    // null before the runtime has made the device's context current: the
+    // lookup below then runs (and creates it), and the next call caches
+    void *ctx = current_context();
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || !ctx || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
             return SMOE_ERR_CUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return SMOE_OK;

@@ -467,8 +467,15 @@ smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
  *     them, or several host threads) race on it and give wrong results.
  *     Issue them on one stream, or order them with events.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it.  Make
- *     that first call before any stream capture begins.
+ *     (cudaGetSymbolAddress, with that device current) and caches it with
+ *     the device's current context; a later call made in another context of
+ *     that device (after cudaDeviceReset, say) looks the address up again.
+ *     Make the first call in each context before any stream capture begins.
+ *   - layer->expert_tiles must be a single-depth bank from smoe_repack: the
+ *     descriptor carries no per-expert depths, so a bank from
+ *     smoe_repack_mixed would be read as a uniform bank at layer->bits (past
+ *     the end of the caller's allocation).  Mixed-depth layers need
+ *     smoe_moe_forward_mixed with a workspace the caller allocates.
  *
  * Errors: those of smoe_moe_forward, and SMOE_ERR_WORKSPACE when
  * smoe_moe_workspace_bytes(layer, num_tokens) exceeds
@@ -477,6 +484,20 @@ smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,
 smoe_status smoe_moe_forward_noalloc(const smoe_layer_desc *layer, const void *x,
                                      smoe_dtype x_dtype, int64_t num_tokens, float *y,
                                      int32_t *ids_out, float *w_out, void *cuda_stream);
+
+/* Testing only: make the layer kernel's bounded waits short and, if
+ * stall_routing is nonzero, make its routing step wait for logits that no
+ * CTA ever writes.  The layer kernel (the streaming path) hands every value
+ * between CTAs over as a tagged word and each reader polls its words for the
+ * launch's tag; poll_cycles bounds each such poll in SM cycles (<= 0: the
+ * default, about two seconds).  With the stall, each CTA gives up after
+ * poll_cycles, records SMOE_ERR_TIMEOUT in the device status word, skips the
+ * rest of the layer (waits included) and returns; the next launch is not
+ * affected, so a test can check that a wait which runs out ends the launch
+ * with a status the host reads while the context stays usable.  Applies to
+ * forwards enqueued after the call, in this process; a test restores the
+ * defaults with smoe_debug_set_waits(0, 0).  No counterpart in the pages. */
+void smoe_debug_set_waits(long long poll_cycles, int stall_routing);
 
 /* Synchronise cuda_stream, then read and clear the device status word of the
  * current device.  Returns SMOE_OK, SMOE_ERR_DEVICE_FAULT, SMOE_ERR_TIMEOUT
