@@ -2,6 +2,7 @@
 // validation, workspace layout and the launch sequence of one MoE layer.
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "smoe.h"
@@ -80,6 +81,15 @@ using namespace smoe;
 
 namespace {
 
+// Bound of the layer kernel's tag polls (SM cycles; ~2 s at 2 GHz) and the
+// routing-poll stall that smoe_debug_set_waits sets for tests.
+std::atomic<long long> g_wait_cycles{kWaitCycles};
+std::atomic<unsigned> g_tag_stall{0u};
+
+}  // namespace
+
+namespace {
+
 inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -130,10 +140,10 @@ bool valid_layer(const smoe_layer_desc *L)
 
 struct Plan {
     int64_t T;
-    int ntiles, ksplit, Epad, max_pairs, fmax, ctas, max_strips;
-    size_t off_ctr_tile, off_ctr_done, off_ctr_sg, off_ctr_sd, off_ctr_comb, off_pair_done,
-        off_flags, off_ctaflags, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w, off_sw, off_pairs,
-        off_rmap, off_hhi, off_hlo, off_hspart, off_o, off_part, total;
+    int ntiles, ksplit, Epad, max_pairs, fmax, ctas;
+    size_t off_seq, off_ctr_tile, off_ctr_done, off_flags, off_started, off_logit_t, off_h_t, off_part_t,
+        off_o_t, off_meta, off_plog, off_logits, off_xsum, off_ids, off_w, off_sw, off_pairs, off_rmap,
+        off_o, total;
     // grouped path (T >= kGroupedMinT only)
     bool grouped;
     int64_t grows;
@@ -171,7 +181,6 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T, bool mixed = false)
         mp = 1;
     p.max_pairs = static_cast<int>(mp);
     p.fmax = L->ffn_dim > L->shared_ffn_dim ? L->ffn_dim : L->shared_ffn_dim;
-    p.max_strips = (p.fmax > d ? p.fmax : d) / 16;
     p.ctas = layer_grid_ctas_max();
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -179,15 +188,21 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T, bool mixed = false)
         o = align256(o + bytes);
         return at;
     };
-    // counters and flags first (zeroed once, kept at zero by the kernels)
+    // Zeroed prefix (smoe_moe_workspace_init): the launch sequence number
+    // first, at the same offset for every layer shape, so that it only ever
+    // grows and no tagged word left by an earlier launch (of any shape)
+    // carries a later launch's tag; then counters the kernels keep at zero,
+    // and the tagged exchange areas of the layer kernel.
+    const bool small = T <= kFusedCombineMaxT;
+    p.off_seq = take(sizeof(unsigned));
     p.off_ctr_tile = take(sizeof(unsigned) * p.ntiles);
     p.off_ctr_done = take(sizeof(unsigned));
-    p.off_ctr_sg = take(sizeof(unsigned) * (size_t)p.max_pairs * p.max_strips);
-    p.off_ctr_sd = take(sizeof(unsigned) * (size_t)p.max_pairs * p.max_strips);
-    p.off_ctr_comb = take(sizeof(unsigned) * (d / 16));
-    p.off_pair_done = take(sizeof(unsigned) * p.max_pairs);
     p.off_flags = take(sizeof(unsigned) * 4);
-    p.off_ctaflags = take(sizeof(unsigned) * 32 * (size_t)p.ctas);
+    p.off_started = take(8 * (size_t)p.ctas);
+    p.off_logit_t = take(small ? 8 * (size_t)T * p.Epad : 0);
+    p.off_h_t = take(8 * (size_t)p.max_pairs * kPairCols * p.fmax);
+    p.off_part_t = take(8 * (size_t)p.ctas * 2 * 32 * 8);
+    p.off_o_t = take(small ? 8 * (size_t)p.max_pairs * kPairCols * d : 0);
     p.off_meta = take(sizeof(int32_t) * 2);
     p.off_plog = take(sizeof(float) * p.ksplit * T * p.Epad);
     p.off_logits = take(sizeof(float) * T * p.Epad);
@@ -197,11 +212,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T, bool mixed = false)
     p.off_sw = take(sizeof(float) * T);
     p.off_pairs = take(sizeof(int32_t) * kPairInts * p.max_pairs);
     p.off_rmap = take(sizeof(int32_t) * T * (k + 1));
-    p.off_hhi = take(sizeof(uint16_t) * (size_t)p.max_pairs * kPairCols * p.fmax);
-    p.off_hlo = take(sizeof(uint16_t) * (size_t)p.max_pairs * kPairCols * p.fmax);
-    p.off_hspart = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * (p.fmax / 16) * 2);
-    p.off_o = take(sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
-    p.off_part = take(sizeof(float) * 4 * 2 * (size_t)p.ctas * 2 * 2 * 32);
+    p.off_o = take(small ? 0 : sizeof(float) * (size_t)p.max_pairs * kPairCols * d);
     p.grouped = T >= kGroupedMinT || mixed;
     p.grows = 0;
     p.off_grow = p.off_gseg = p.off_gtile = p.off_gxs = p.off_gh = p.off_go = p.off_grw = 0;
@@ -581,9 +592,6 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
     la.do_route = fused ? 1 : 0;
     la.fused_combine = num_tokens <= kFusedCombineMaxT ? 1 : 0;
     la.max_pairs = P.max_pairs;
-    la.max_strips = P.max_strips;
-    la.logits = at<float>(workspace, P.off_logits);
-    la.xsum = ra.xsum;
     la.ids = ra.ids;
     la.weights = ra.weights;
     la.shared_w = ra.shared_w;
@@ -592,19 +600,16 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
     la.pairs = ra.pairs;
     la.route_map = ra.route_map;
     la.meta = ra.meta;
-    la.h_hi = at<uint16_t>(workspace, P.off_hhi);
-    la.h_lo = at<uint16_t>(workspace, P.off_hlo);
-    la.hs_part = at<float>(workspace, P.off_hspart);
+    la.seq = at<unsigned>(workspace, P.off_seq);
+    la.started = at<unsigned long long>(workspace, P.off_started);
+    la.logit_t = at<unsigned long long>(workspace, P.off_logit_t);
+    la.h_t = at<unsigned long long>(workspace, P.off_h_t);
+    la.part_t = at<unsigned long long>(workspace, P.off_part_t);
+    la.o_t = at<unsigned long long>(workspace, P.off_o_t);
     la.o = at<float>(workspace, P.off_o);
-    la.partial = at<float>(workspace, P.off_part);
-    la.strip_ctr_g = at<unsigned>(workspace, P.off_ctr_sg);
-    la.strip_ctr_d = at<unsigned>(workspace, P.off_ctr_sd);
-    la.comb_ctr = at<unsigned>(workspace, P.off_ctr_comb);
-    la.pair_done = at<unsigned>(workspace, P.off_pair_done);
     unsigned *flags = at<unsigned>(workspace, P.off_flags);
-    la.route_ctr = flags + 0;
-    la.exit_ctr = flags + 1;
-    la.cta_flags = at<unsigned>(workspace, P.off_ctaflags);
+    la.wait_cycles = g_wait_cycles.load();
+    la.tag_stall = g_tag_stall.load();
     la.y = y;
     la.status = status;
     if (mixed) {
@@ -649,9 +654,11 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
         if (stage_mask & 1) {
             if (ra.x_bf16) {
                 if (launch_tc_logits(static_cast<const uint16_t *>(x), ra.router_w, num_tokens,
-                                     L.d_model, L.num_experts, P.Epad, la.logits, status,
+                                     L.d_model, L.num_experts, P.Epad,
+                                     at<float>(workspace, P.off_logits), status,
                                      s) != cudaSuccess ||
-                    launch_route_tiles(ra, la.logits, P.Epad, s) != cudaSuccess)
+                    launch_route_tiles(ra, at<float>(workspace, P.off_logits), P.Epad, s) !=
+                        cudaSuccess)
                     return SMOE_ERR_CUDA;
             } else if (launch_router(ra, s, false) != cudaSuccess) {
                 return SMOE_ERR_CUDA;
@@ -830,6 +837,12 @@ smoe_status smoe_moe_forward_stage_mixed(const smoe_layer_desc *layer, const uin
         return SMOE_ERR_INVALID_ARG;
     return forward_stages(layer, nullptr, x, x_dtype, num_tokens, y, workspace, workspace_bytes,
                           ids_out, w_out, 1 << stage, SMOE_PATH_AUTO, cuda_stream, expert_bits);
+}
+
+void smoe_debug_set_waits(long long poll_cycles, int stall_routing)
+{
+    g_wait_cycles.store(poll_cycles > 0 ? poll_cycles : kWaitCycles);
+    g_tag_stall.store(stall_routing ? 1u : 0u);
 }
 
 smoe_status smoe_get_device_status(void *cuda_stream)

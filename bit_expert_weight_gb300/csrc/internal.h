@@ -116,10 +116,9 @@ struct LayerArgs {
     ExpertMask mask;               // routable experts
     int do_route;                  // 1: phase R inside the kernel (T <= 8)
     int fused_combine;             // 1: combine inside the kernel (T <= 8)
-    int max_pairs, max_strips;     // counter strides
-    // workspace
-    float *logits;                 // [T][Epad]
-    float *xsum;                   // [T][d/64][2]
+    int max_pairs;
+    // workspace: routing tables (written by the router kernel when do_route
+    // is 0, by CTA 0 for the host otherwise)
     int32_t *ids;                  // [T][k]
     float *weights;                // [T][k]
     float *shared_w;               // [T]
@@ -128,17 +127,21 @@ struct LayerArgs {
     int32_t *pairs;                // [max_pairs][kPairInts]
     int32_t *route_map;            // [T][k+1]
     int32_t *meta;                 // [0] routed pairs, [1] all pairs
-    uint16_t *h_hi, *h_lo;         // bf16 [max_pairs][8][fmax]
-    float *hs_part;                // [max_pairs][8][fmax/16][2]
-    float *o;                      // [max_pairs][8][d]
-    float *partial;                // [phase][CTAs][2 slots][2][32] float4
-    unsigned *strip_ctr_g, *strip_ctr_d;  // [max_pairs][max_strips]
-    unsigned *comb_ctr;            // [d/16]
-    unsigned *pair_done;           // [max_pairs] finished gate/up strips
-    unsigned *route_ctr, *exit_ctr;
-    unsigned *cta_flags;           // [max CTAs][32]: word 0 route go
+    // Cross-CTA exchange by tagged words: a 64-bit word holds a 32-bit
+    // payload (low half) and the launch's tag (high half), written by one
+    // relaxed 64-bit store and polled with relaxed loads.  The tag of a
+    // launch is *seq + 1; the kernel leaves it in *seq for the next launch.
+    unsigned *seq;                 // [1], first word of the workspace
+    unsigned long long *started;   // [CTAs] each CTA's start mark
+    unsigned long long *logit_t;   // [T][Epad] logits (routing inside the kernel)
+    unsigned long long *h_t;       // [max_pairs][8][fmax] h: bf16 hi | bf16 lo << 16
+    unsigned long long *part_t;    // [CTAs][2 slots][32 lanes][8] split gate/up unit sums
+    unsigned long long *o_t;       // [max_pairs][8][d] down outputs (combine inside)
+    float *o;                      // [max_pairs][8][d] down outputs (combine kernel)
     float *y;                      // [T, d]
     int *status;
+    long long wait_cycles;         // bound of every tag poll
+    unsigned tag_stall;            // testing: the logits poll waits for tag + tag_stall
     // mixed bit depth per routed expert (as in GroupedArgs): the kernel
     // instance for mixed banks takes each pair's depth from q4mask and the
     // expert's place in the bank from the depths before it

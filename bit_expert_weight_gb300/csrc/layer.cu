@@ -9,33 +9,40 @@
 // renormalisation, y = sum_j w_j FFN_j(x) + the sigmoid-gated shared expert);
 // "Model Agnosticism", SmoeModelConfig (router rows = max_experts_per_layer).
 //
-// Phases (every warp runs them in order; cross-CTA dependencies are flags
-// polled with bounded acquire loads; the launch is cooperative so every CTA
-// is resident):
-//  R  (T <= 8 only) one warp per router row computes that expert's logits
-//     for all tokens over the full d (no K split, no partials); T more warps
-//     compute the per-group activation sums; each bumps an arrival counter.
-//     Every CTA then routes the tokens itself (one warp per token) and builds
-//     the pair table in its own shared memory -- the same deterministic code
-//     on the same logits gives the same table in every CTA, so nothing is
-//     written back and re-read.  For T > 8 a separate router kernel has
-//     built the tables in global memory before the launch.
+// Cross-CTA hand-offs are tagged words: every value one CTA passes to
+// another (a logit, an h value, a partial sum, a down output) is stored as
+// one 64-bit word {payload, tag} with a relaxed store, and the reader polls
+// its own words with relaxed loads until they carry this launch's tag.  A
+// reader that sees the tag sees the payload stored with it, so no fence,
+// counter or atomic sits between the producer and the consumer.  The tag is
+// the workspace's launch sequence number plus one; CTA 0 stores it back for
+// the next launch once every CTA has read it.
+//
+// Phases (the launch is cooperative, so every CTA is resident):
+//  R  (T <= 8 only) CTA c computes router rows c, c + grid, ... with all its
+//     threads (the rows' weights are loaded before the previous kernel has
+//     finished) and stores the tagged logits.  Every CTA then polls all the
+//     logits into shared memory, routes each token in one warp (k rounds of
+//     a warp arg-max in (key desc, index asc) order) and builds the pair
+//     table -- the same deterministic code on the same logits gives the same
+//     table in every CTA.  For T > 8 a separate router kernel has built the
+//     tables in global memory before the launch.
 //  G  gate/up: the tiles of all pairs (pair = one expert x <= 8 tokens) form
-//     one stream of 16-row strips; each warp takes an equal contiguous range
-//     (stream-K), streams it through a private ring of shared-memory stages
-//     filled by TMA bulk copies, decodes codes in registers and multiplies
-//     with mma.sync.  A strip (16 rows x all of d, gate and up interleaved)
-//     finished by one warp is finalised in registers; one shared by several
-//     warps is finalised by the last to arrive, summing the partials in warp
-//     order.  Finalising writes h = SiLU(g) * u as bf16 hi + lo and the
-//     strip's per-class sums of h, then bumps the pair's strip count.
-//  D  down: the same streaming over 16-row strips of W_down.  A warp issues
-//     its first weight copies before its CTA waits for the strip counts of
-//     the pairs it reads, so the weights are in flight while gate/up
-//     finishes.  The last pair to
-//     finish an output strip (T <= 8) sums sum_j w_j o_j (+ shared) in rank
-//     order into y.
-// Deterministic throughout: no float atomics.
+//     one stream of 16-row strips, cut into chunks of <= 32 groups; the
+//     chunks are split evenly over the CTAs (stream-K), streamed through a
+//     ring of shared-memory stages filled by TMA bulk copies, decoded in
+//     registers and multiplied with mma.sync by 16 warps.  Two epilogue
+//     warps sum the warps' partials, finalise h = SiLU(g) * u (bf16 hi + lo)
+//     and store it tagged; a strip split between CTAs is finished by its
+//     last contributor, which polls the others' tagged partial sums.
+//  D  down: steps of up to 4 whole output strips of one pair (one TMA copy
+//     each), so no unit is split; the copies are issued as soon as ring
+//     slots free up, while gate/up is still finishing.  Each warp polls the
+//     h values its two groups need (tagged) when it reaches a new pair.
+//  C  combine (T <= 8): every thread of the grid takes outputs (t, row) and
+//     sums sum_j w_j o_j (+ shared) in rank order from the tagged down
+//     outputs.  For T > 8 a separate combine kernel reads plain outputs.
+// Deterministic throughout: no float atomics, fixed summation orders.
 #include "common.cuh"
 #include "internal.h"
 
@@ -44,84 +51,82 @@ namespace smoe {
 namespace {
 
 // 16 streaming warps (decode, mma), 2 epilogue warps (unit sums, SiLU,
-// stores, cross-CTA fixups) and one producer warp (the TMA ring): global-
-// memory round trips and fences are slow while an SM streams, so the
-// streaming warps make none.
+// stores, split-strip joins) and one producer warp (the TMA ring): global-
+// memory round trips are slow while an SM streams, so the streaming warps
+// make none except their own B operand loads.
 constexpr int kStreamWarps = 16;
 constexpr int kEpiWarps = 2;
 constexpr int kProducerWarp = kStreamWarps + kEpiWarps;
 constexpr int kWarps = kStreamWarps + kEpiWarps + 1;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxStripsD = 4096 / 16;  // output strips (d <= 4096)
-constexpr long long kSpinCycles = 4000000000ll;  // ~2 s at 2 GHz
+constexpr int kMaxDownStrips = 4;  // output strips per down step
 
-__device__ __forceinline__ unsigned atom_add_acqrel(unsigned *p, unsigned v)
+// ------------------------------------------------------------ tagged words
+
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 tag_word(uint32_t payload, uint32_t tag)
 {
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
+    return (static_cast<u64>(tag) << 32) | payload;
 }
-// Release/acquire fence at GPU scope: orders this thread's (and, through the
-// preceding __syncwarp, its warp's) writes before a following signal, or a
-// signal observed before the following reads.
-__device__ __forceinline__ void fence_acq_rel()
+__device__ __forceinline__ uint32_t word_tag(u64 w) { return static_cast<uint32_t>(w >> 32); }
+__device__ __forceinline__ uint32_t word_payload(u64 w) { return static_cast<uint32_t>(w); }
+
+__device__ __forceinline__ void st_word(u64 *p, u64 v)
 {
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-// Relaxed fire-and-forget add / store: after one release fence these
-// pipeline, where a chain of acq_rel atomics would serialise.
-__device__ __forceinline__ void red_add_relaxed(unsigned *p, unsigned v)
+__device__ __forceinline__ void st_word2(u64 *p, u64 a, u64 b)
 {
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
-__device__ __forceinline__ void st_relaxed(unsigned *p, unsigned v)
+__device__ __forceinline__ u64 ld_word(const u64 *p)
+{
+    u64 v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+// Two words of one 16-byte aligned pair; each word is loaded atomically.
+__device__ __forceinline__ void ld_word2(const u64 *p, u64 &a, u64 &b)
+{
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(unsigned *p, unsigned v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 
-// Lane 0 polls until *p >= target (bounded); the result is broadcast.
-__device__ bool warp_wait_geq(const unsigned *p, unsigned target, int *status)
+// Poll one word until it carries `want` (bounded by `limit` SM cycles);
+// false if the bound ran out.
+__device__ __forceinline__ bool poll_word(const u64 *p, uint32_t want, long long limit, u64 &v)
 {
-    const int lane = threadIdx.x & 31;
-    int ok = 1;
-    if (lane == 0) {
-        const long long t0 = clock64();
-        unsigned ns = 20;
-        while (ld_acquire(p) < target) {
-            if (clock64() - t0 > kSpinCycles) {
-                ok = 0;
-                set_status(status, kStatusTimeout);
-                break;
-            }
-            __nanosleep(ns);
-            if (ns < 200)
-                ns *= 2;
-        }
+    v = ld_word(p);
+    if (word_tag(v) == want)
+        return true;
+    const long long t0 = clock64();
+    unsigned ns = 32;
+    for (;;) {
+        __nanosleep(ns);
+        if (ns < 256)
+            ns *= 2;
+        v = ld_word(p);
+        if (word_tag(v) == want)
+            return true;
+        if (clock64() - t0 > limit)
+            return false;
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
-// CTA-wide named barrier 1 (all kThreads threads); 2: the streaming warps;
-// 3: the epilogue warps.
+// CTA-wide named barrier 1 (all kThreads threads).
 __device__ __forceinline__ void cta_barrier()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
-}
-__device__ __forceinline__ void stream_barrier()
-{
-    asm volatile("bar.sync 2, %0;" ::"n"(kStreamWarps * 32) : "memory");
-}
-__device__ __forceinline__ void epi_barrier()
-{
-    asm volatile("bar.sync 3, %0;" ::"n"(kEpiWarps * 32) : "memory");
 }
 
 // Stream-K split of U units over W warps: warp w owns [start(w), start(w+1))
@@ -161,170 +166,140 @@ __device__ __forceinline__ float sigmoid_fast(float x)
     return __fdividef(1.0f, 1.0f + __expf(fminf(-x, 80.0f)));
 }
 
-// Routing from the logits of one CTA's copy in shared memory.  Every CTA
-// runs the same code on the same values, so every CTA derives the same
-// tables.  Task (token t, chunk c) on one warp: lane L takes expert
-// e = 32 c + L, whose rank is the number of experts before it in the order
-// (key descending, index ascending) -- ties go to the lower index; ranks
-// below k are the selection, stored at their rank with its score: the
-// softmax over all E logits, or (sigm) the expert's own sigmoid.  The
-// softmax maximum and sum run over all E logits in a fixed order
-// (lane-strided, then a shuffle tree), the same in every task; exp and divide
-// are the hardware approximations (a few ulp), well inside the weights'
-// tolerance.
-__device__ __noinline__ void route_chunk(const float *lg, const float *key, int E, int k, int c,
-                                         int sigm, int16_t *ids_s, float *p_s)
+// Router rows of one CTA (phase R): rows c, c + grid (E routed rows, then
+// the shared gate row), at most two.  Thread i holds columns 8i .. 8i+7 of
+// each row.
+struct RouterPre {
+    uint4 w0, w1;
+    int nrows;
+};
+
+__device__ __forceinline__ const uint16_t *router_row(const LayerArgs &a, int r)
 {
-    const int lane = threadIdx.x & 31;
-    float m = -INFINITY, z = 1.f;
-    if (!sigm) {
-        for (int i = lane; i < E; i += 32)
-            m = fmaxf(m, lg[i]);
-        for (int o = 16; o; o >>= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        z = 0.f;
-        for (int i = lane; i < E; i += 32)
-            z += __expf(lg[i] - m);
-        for (int o = 16; o; o >>= 1)
-            z += __shfl_xor_sync(0xffffffffu, z, o);
-    }
-    const int e = 32 * c + lane;
-    if (e >= E)
-        return;
-    const float ke = key[e];
-    int r = 0;
-    const float4 *k4 = reinterpret_cast<const float4 *>(key);
-#pragma unroll 2
-    for (int j = 0; j < E / 4; ++j) {
-        const float4 v = k4[j];
-        const int e0 = 4 * j;
-        r += (v.x > ke || (v.x == ke && e0 < e)) ? 1 : 0;
-        r += (v.y > ke || (v.y == ke && e0 + 1 < e)) ? 1 : 0;
-        r += (v.z > ke || (v.z == ke && e0 + 2 < e)) ? 1 : 0;
-        r += (v.w > ke || (v.w == ke && e0 + 3 < e)) ? 1 : 0;
-    }
-    for (int e2 = E & ~3; e2 < E; ++e2) {
-        const float v = key[e2];
-        r += (v > ke || (v == ke && e2 < e)) ? 1 : 0;
-    }
-    if (r < k) {
-        ids_s[r] = static_cast<int16_t>(e);
-        p_s[r] = sigm ? sigmoid_fast(lg[e]) : __fdividef(__expf(lg[e] - m), z);  // z in [1, E]
+    return r < a.E ? a.router_w + (int64_t)r * a.d : a.shared_gate;
+}
+
+__device__ __forceinline__ int router_rows_of_cta(const LayerArgs &a)
+{
+    const int rows = a.E + (a.shared_gate ? 1 : 0);
+    const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return c < rows ? (c + C < rows ? 2 : 1) : 0;
+}
+
+// Before the previous kernel on the stream has finished: pull the CTA's
+// router rows into L2 (one prefetch per 128-byte line).  Only a prefetch:
+// L2 is coherent, so a row that kernel still writes is read correctly after
+// the wait, where the rows are loaded.
+__device__ __forceinline__ void router_prefetch_l2(const LayerArgs &a)
+{
+    const int n = router_rows_of_cta(a), i = threadIdx.x;
+    const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    if (i < a.d / 64) {
+        for (int r = 0; r < n; ++r)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(router_row(a, c + r * C) + 64 * i));
     }
 }
 
-// Phase R work of one warp: unit < E (+1 shared gate row) -> logits of that
-// row for all tokens; unit >= rows -> group sums of token (unit - rows).
-template <bool XBF16>
-__device__ __forceinline__ void router_unit(const LayerArgs &a, int unit)
+__device__ __forceinline__ RouterPre router_load(const LayerArgs &a)
 {
-    const int lane = threadIdx.x & 31;
-    const int d = a.d, T = static_cast<int>(a.T);
-    const int rows = a.E + (a.shared_gate ? 1 : 0);
-    if (unit < rows) {
-        const uint16_t *wr = unit < a.E ? a.router_w + (int64_t)unit * d : a.shared_gate;
-        // per token: four 256-column slices per batch, all loads in flight
-#pragma unroll 1
-        for (int t = 0; t < T; ++t) {
-            float acc = 0.f;
-#pragma unroll 1
-            for (int c0 = lane * 8; c0 < d; c0 += 1024) {
-                uint4 wv[4], xv[4], xw[4];
+    RouterPre pre;
+    pre.nrows = router_rows_of_cta(a);
+    const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int i = threadIdx.x;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    pre.w0 = pre.w1 = z;
+    if (i < a.d / 8) {
+        if (pre.nrows > 0)
+            pre.w0 = __ldg(reinterpret_cast<const uint4 *>(router_row(a, c) + 8 * i));
+        if (pre.nrows > 1)
+            pre.w1 = __ldg(reinterpret_cast<const uint4 *>(router_row(a, c + C) + 8 * i));
+    }
+    return pre;
+}
+
+__device__ __forceinline__ float dot8_bf16(uint4 w, const float (&x)[8])
+{
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float acc = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = c0 + 256 * i;
-                    const bool in = c < d;
-                    wv[i] = in ? __ldg(reinterpret_cast<const uint4 *>(wr + c)) : make_uint4(0u, 0u, 0u, 0u);
-                    if (XBF16) {
-                        xv[i] = in ? __ldg(reinterpret_cast<const uint4 *>(
-                                         reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + c))
-                                   : make_uint4(0u, 0u, 0u, 0u);
-                    } else {
-                        const uint4 *xr = reinterpret_cast<const uint4 *>(
-                            reinterpret_cast<const float *>(a.x) + (int64_t)t * d + c);
-                        xv[i] = in ? __ldg(xr) : make_uint4(0u, 0u, 0u, 0u);
-                        xw[i] = in ? __ldg(xr + 1) : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
+    for (int q = 0; q < 4; ++q) {
+        acc = fmaf(bf16lo_to_f32(ww[q]), x[2 * q], acc);
+        acc = fmaf(bf16hi_to_f32(ww[q]), x[2 * q + 1], acc);
+    }
+    return acc;
+}
+
+// The CTA's router rows for all tokens: per-thread 8-column dot products,
+// a shuffle tree per warp, then the warps' sums in warp order; the logits
+// are stored tagged.  red: shared scratch of kWarps x 16 floats.  Every
+// thread of the CTA calls it.
+template <bool XBF16>
+__device__ __forceinline__ void router_rows(const LayerArgs &a, const RouterPre &pre, float *red,
+                                            uint32_t tag)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, i = threadIdx.x;
+    const int T = static_cast<int>(a.T), d = a.d;
+    const int nw = (d / 8 + 31) / 32;  // warps holding columns
+    if (pre.nrows > 0 && warp < nw) {
+        float acc[2][kPairCols];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-                    float xf[8];
-                    if (XBF16) {
-                        const uint32_t xx[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            xf[2 * q] = bf16lo_to_f32(xx[q]);
-                            xf[2 * q + 1] = bf16hi_to_f32(xx[q]);
-                        }
-                    } else {
-                        xf[0] = __uint_as_float(xv[i].x), xf[1] = __uint_as_float(xv[i].y);
-                        xf[2] = __uint_as_float(xv[i].z), xf[3] = __uint_as_float(xv[i].w);
-                        xf[4] = __uint_as_float(xw[i].x), xf[5] = __uint_as_float(xw[i].y);
-                        xf[6] = __uint_as_float(xw[i].z), xf[7] = __uint_as_float(xw[i].w);
-                    }
+        for (int t = 0; t < kPairCols; ++t) {
+            acc[0][t] = acc[1][t] = 0.f;
+            if (t < T && i < d / 8) {
+                float xf[8];
+                if (XBF16) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+                        reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + 8 * i));
+                    const uint32_t xx[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        acc = fmaf(bf16lo_to_f32(ww[q]), xf[2 * q], acc);
-                        acc = fmaf(bf16hi_to_f32(ww[q]), xf[2 * q + 1], acc);
+                        xf[2 * q] = bf16lo_to_f32(xx[q]);
+                        xf[2 * q + 1] = bf16hi_to_f32(xx[q]);
                     }
+                } else {
+                    const float4 *xr = reinterpret_cast<const float4 *>(
+                        reinterpret_cast<const float *>(a.x) + (int64_t)t * d + 8 * i);
+                    const float4 v0 = __ldg(xr), v1 = __ldg(xr + 1);
+                    xf[0] = v0.x, xf[1] = v0.y, xf[2] = v0.z, xf[3] = v0.w;
+                    xf[4] = v1.x, xf[5] = v1.y, xf[6] = v1.z, xf[7] = v1.w;
                 }
+                acc[0][t] = dot8_bf16(pre.w0, xf);
+                acc[1][t] = pre.nrows > 1 ? dot8_bf16(pre.w1, xf) : 0.f;
             }
-            for (int o = 16; o; o >>= 1)
-                acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0)
-                a.logits[(int64_t)t * a.Epad + unit] = acc;
         }
-    } else {
-        // group sums of token t: X0 over columns c % 4 in {0,1}, X1 over {2,3}
-        const int t = unit - rows;
-        for (int g = lane; g < d / kGroup; g += 32) {
-            float s0 = 0.f, s1 = 0.f;
-            if (XBF16) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const uint16_t *>(a.x) + (int64_t)t * d + g * kGroup);
-                uint4 v[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    v[i] = __ldg(src + i);
+        for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    s0 += bf16lo_to_f32(v[i].x) + bf16hi_to_f32(v[i].x);
-                    s1 += bf16lo_to_f32(v[i].y) + bf16hi_to_f32(v[i].y);
-                    s0 += bf16lo_to_f32(v[i].z) + bf16hi_to_f32(v[i].z);
-                    s1 += bf16lo_to_f32(v[i].w) + bf16hi_to_f32(v[i].w);
-                }
-            } else {
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    reinterpret_cast<const float *>(a.x) + (int64_t)t * d + g * kGroup);
-                float4 v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    v[i] = __ldg(src + i);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    s0 += v[i].x + v[i].y;
-                    s1 += v[i].z + v[i].w;
-                }
+            for (int t = 0; t < kPairCols; ++t) {
+                float v = acc[r][t];
+                for (int o = 16; o; o >>= 1)
+                    v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0)
+                    red[warp * 16 + r * kPairCols + t] = v;
             }
-            reinterpret_cast<float2 *>(a.xsum)[(int64_t)t * (d / kGroup) + g] = make_float2(s0, s1);
-        }
+    }
+    cta_barrier();
+    if (i < pre.nrows * T) {
+        const int r = i / T, t = i - r * T;
+        float v = 0.f;
+        for (int w = 0; w < nw; ++w)
+            v += red[w * 16 + r * kPairCols + t];
+        const int row = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
+        st_word(a.logit_t + (int64_t)t * a.Epad + row, tag_word(__float_as_uint(v), tag));
     }
 }
 
 // Routing tables of a CTA.  On the fused path (T <= 8) every CTA builds its
-// own copy in shared memory from the published logits (the same
-// deterministic code on the same logits gives the same tables everywhere);
-// otherwise they point to the tables the router kernel left in global memory.
+// own copy in shared memory from the tagged logits (the same deterministic
+// code on the same logits gives the same tables everywhere); otherwise they
+// point to the tables the router kernel left in global memory.
 constexpr int kFusedPairs = kPairCols * SMOE_MAX_TOPK_DEV + 1;
 // route_map, weights and ids are [T][k+1], [T][k], [T][k] with the runtime k
 // as the row stride, exactly like the global tables.
 struct __align__(16) RouteSmem {
     float lg[kPairCols * kMaxExperts];   // [T][E4] logits, row stride E4 = E rounded up to 4
-    float key[kPairCols * kMaxExperts];  // [T][E4] selection keys fl32(logit + bias)
-    float prob[kPairCols * SMOE_MAX_TOPK_DEV];  // [T][k] softmax of the rank-j expert
-    float warm_p[SMOE_MAX_TOPK_DEV];     // scratch of the instruction-cache warm-up
-    int16_t warm_id[SMOE_MAX_TOPK_DEV];
+    float key[kPairCols * kMaxExperts];  // [T][E4] selection keys
+    float red[kWarps * 16];              // router row partial sums
     int32_t pairs[kFusedPairs][kPairInts];
     int32_t route_map[kPairCols * (SMOE_MAX_TOPK_DEV + 1)];
     float weights[kPairCols * SMOE_MAX_TOPK_DEV];
@@ -339,6 +314,78 @@ struct RouteView {
     const float *weights;      // [T][k]
     const float *shared_w;     // [T]
 };
+
+// One token's routing in one warp, from its logits and selection keys in
+// shared memory: k rounds of a warp arg-max over the keys in the order
+// (key descending, index ascending) -- ties go to the lower index -- then
+// the scores of the selected experts (softmax over all E logits, or the
+// expert's own sigmoid) and the weights (renormalised over the selection if
+// norm, times the routed scaling factor), in rank order.  Lane L holds
+// experts L, L + 32, ... .  The softmax maximum and sum run over all E
+// logits in a fixed order (lane-strided, then a shuffle tree); exp and
+// divide are the hardware approximations (a few ulp), well inside the
+// weights' tolerance.
+__device__ __noinline__ void route_token(const float *lg, const float *key, int E, int k, int sigm,
+                                         int norm, float rsf, int16_t *ids, float *w)
+{
+    const int lane = threadIdx.x & 31;
+    float kv[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        kv[i] = e < E ? key[e] : -INFINITY;
+    }
+    unsigned taken = 0u;
+    int sel = 0;  // lane j < k: the rank-j expert
+    for (int r = 0; r < k; ++r) {
+        float bk = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (kv[i] > bk || (kv[i] == bk && e < bi))) {
+                bk = kv[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ok > bk || (ok == bk && oi < bi)) {
+                bk = ok;
+                bi = oi;
+            }
+        }
+        if (bi < E && lane == (bi & 31))
+            taken |= 1u << (bi >> 5);
+        if (lane == r)
+            sel = bi;
+    }
+    float m = -INFINITY, z = 1.f;
+    if (!sigm) {
+        for (int i = lane; i < E; i += 32)
+            m = fmaxf(m, lg[i]);
+        for (int o = 16; o; o >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        z = 0.f;
+        for (int i = lane; i < E; i += 32)
+            z += __expf(lg[i] - m);
+        for (int o = 16; o; o >>= 1)
+            z += __shfl_xor_sync(0xffffffffu, z, o);
+    }
+    float p = 0.f;
+    if (lane < k)
+        p = sigm ? sigmoid_fast(lg[sel]) : __fdividef(__expf(lg[sel] - m), z);  // z in [1, E]
+    // sum of the selected scores in rank order (the same order as the oracle)
+    float psel = 0.f;
+    for (int j = 0; j < k; ++j)
+        psel += __shfl_sync(0xffffffffu, p, j);
+    if (lane < k) {
+        ids[lane] = static_cast<int16_t>(sel);
+        w[lane] = (norm ? __fdividef(p, psel) : p) * rsf;
+    }
+}
 
 // One warp of the CTA: pair table from the routed ids (T <= 8).  Pair = one
 // selected expert with the ascending tokens that chose it, pairs in order of
@@ -393,10 +440,11 @@ __device__ __forceinline__ void cta_dispatch(const LayerArgs &a, RouteSmem &r)
 
 // ------------------------------------------------------------ streaming
 
-// A chunk is a run of up to kChunkGroups consecutive groups of one strip,
-// two per streaming warp (groups w and w + 16 of the chunk); one stage of
-// the CTA's ring holds one chunk.  Gate/up: a strip of d/64 groups in 1 or
-// 2 chunks (gate and up tile per group); down: the whole strip in one chunk.
+// Gate/up: a chunk is a run of up to kChunkGroups consecutive groups of one
+// strip, two per streaming warp (groups w and w + 16 of the chunk); one
+// stage of the CTA's ring holds one chunk (gate and up tile per group).
+// Down: a step is up to kMaxDownStrips whole output strips of one pair (all
+// f/64 groups each, f <= 2048), in one stage.
 constexpr int kChunkGroups = 2 * kStreamWarps;
 constexpr int kDownGroupsMax = kChunkGroups;  // ffn_dim <= 2048
 
@@ -407,35 +455,38 @@ __host__ __device__ constexpr int ring_bits(int bits) { return bits == 0 ? 4 : b
 // About 100 KB in flight per SM: the full HBM rate needs ~64 KB; deeper
 // rings delay every other memory access of the SM, which queues behind them.
 __host__ __device__ constexpr int num_stages(int bits) { return bits == 4 ? 3 : 5; }
-// kRedSlots slots of per-warp unit sums (gate and up float4 per lane)
+// kRedSlots slots of per-warp unit sums (two float4 per lane: gate and up,
+// or two down strips)
 constexpr int kRedSlots = 4;
 __host__ __device__ constexpr int red_bytes() { return kRedSlots * kStreamWarps * 2 * 32 * 16; }
 __host__ __device__ constexpr int smem_bytes(int bits)
 {
     return num_stages(bits) * stage_bytes(bits) + red_bytes() + (2 * num_stages(bits) + 2 * kRedSlots) * 8;
 }
-// Pairs whose finished gate/up strips a CTA counts in shared memory and
-// publishes once, at the end of its gate/up range.
-constexpr int kMaxSpan = 64;
 
-// Step geometry of one phase.  Units are (pair, strip) in pair order; a
-// unit's K groups are cut into ch chunks of gc groups (the last may be
-// shorter); the steps (chunks) of all units are split evenly over the CTAs.
+// Step geometry of one phase.  Gate/up: units are (pair, strip) in pair
+// order; a unit's K groups are cut into ch chunks of gc groups (the last may
+// be shorter); the steps (chunks) of all units are split evenly over the
+// CTAs, so a unit may be shared by neighbouring CTAs.  Down: a step is ms
+// consecutive strips of one pair (the last step of a pair may hold fewer);
+// nstr counts steps per pair and ch = 1, so no unit is ever split.
 // Index [0]: routed pairs, [1]: the shared expert's pair.
 // (Scalar fields with select accessors: a runtime-indexed array would live
 // in local memory.)
 struct Geo {
     int P_r, P_t;
-    int nstr0, gk0, ch0, gc0, spp0;  // routed: strips, groups per strip, chunks, groups per chunk, steps
-    int nstr1, gk1, ch1, gc1, spp1;  // shared
-    int SR, S;                       // steps of the routed pairs, of all pairs
-    Split sp;                        // steps over CTAs
-    int a0, a1;                      // this CTA's steps
-    int ts;                          // the CTA runs [ts, a1) first, then [a0, ts)
+    int nstr0, gk0, ch0, gc0, spp0, ms0;  // routed: strips (steps), groups per strip, chunks,
+                                          // groups per chunk, steps per pair, strips per step
+    int nstr1, gk1, ch1, gc1, spp1, ms1;  // shared
+    int rows;                             // down: output strips (d / 16)
+    int SR, S;                            // steps of the routed pairs, of all pairs
+    Split sp;                             // steps over CTAs
+    int a0, a1;                           // this CTA's steps
+    int ts;                               // the CTA runs [ts, a1) first, then [a0, ts)
 };
 
 struct UnitGeo {
-    int nstr, gk, ch, gc;
+    int nstr, gk, ch, gc, ms;
 };
 
 __device__ __forceinline__ UnitGeo unit_geo(const Geo &g, int p)
@@ -446,7 +497,18 @@ __device__ __forceinline__ UnitGeo unit_geo(const Geo &g, int p)
     u.gk = r ? g.gk0 : g.gk1;
     u.ch = r ? g.ch0 : g.ch1;
     u.gc = r ? g.gc0 : g.gc1;
+    u.ms = r ? g.ms0 : g.ms1;
     return u;
+}
+
+// Down strips per step: as many whole strips of gk tiles as a stage holds
+// (64 tiles at the ring's depth), at most kMaxDownStrips.
+__device__ __forceinline__ int down_strips_per_step(int gk)
+{
+    if (gk <= 0)
+        return 1;
+    const int m = (kChunkGroups * 2) / gk;
+    return m < 1 ? 1 : (m > kMaxDownStrips ? kMaxDownStrips : m);
 }
 
 __device__ __forceinline__ Geo make_geo(const LayerArgs &a, int phase, int P_r, int P_t)
@@ -454,34 +516,44 @@ __device__ __forceinline__ Geo make_geo(const LayerArgs &a, int phase, int P_r, 
     Geo g;
     g.P_r = P_r;
     g.P_t = P_t;
-    {
-        const int rows = phase == 0 ? a.f : a.d, K = phase == 0 ? a.d : a.f;
-        g.nstr0 = rows / kTileRows;
-        g.gk0 = K / kGroup;
-        g.ch0 = phase == 0 ? (g.gk0 + kChunkGroups - 1) / kChunkGroups : 1;
-        g.gc0 = g.ch0 > 0 ? (g.gk0 + g.ch0 - 1) / g.ch0 : 0;
-        g.spp0 = g.nstr0 * g.ch0;
+    g.rows = a.d / kTileRows;
+    if (phase == 0) {
+        g.gk0 = a.d / kGroup;
+        g.nstr0 = a.f / kTileRows;
+        g.ch0 = (g.gk0 + kChunkGroups - 1) / kChunkGroups;
+        g.gc0 = (g.gk0 + g.ch0 - 1) / g.ch0;
+        g.ms0 = 1;
+        g.gk1 = a.d / kGroup;
+        g.nstr1 = a.fs / kTileRows;
+        g.ch1 = g.ch0;
+        g.gc1 = g.gc0;
+        g.ms1 = 1;
+    } else {
+        g.gk0 = a.f / kGroup;
+        g.ms0 = down_strips_per_step(g.gk0);
+        g.nstr0 = (g.rows + g.ms0 - 1) / g.ms0;
+        g.ch0 = 1;
+        g.gc0 = g.gk0;
+        g.gk1 = a.fs / kGroup;
+        g.ms1 = down_strips_per_step(g.gk1);
+        g.nstr1 = g.gk1 > 0 ? (g.rows + g.ms1 - 1) / g.ms1 : 0;
+        g.ch1 = 1;
+        g.gc1 = g.gk1;
     }
-    {
-        const int rows = phase == 0 ? a.fs : a.d, K = phase == 0 ? a.d : a.fs;
-        g.nstr1 = rows / kTileRows;
-        g.gk1 = K / kGroup;
-        g.ch1 = phase == 0 ? (g.gk1 + kChunkGroups - 1) / kChunkGroups : (g.gk1 > 0 ? 1 : 0);
-        g.gc1 = g.ch1 > 0 ? (g.gk1 + g.ch1 - 1) / g.ch1 : 0;
-        g.spp1 = g.nstr1 * g.ch1;
-    }
+    g.spp0 = g.nstr0 * g.ch0;
+    g.spp1 = g.nstr1 * g.ch1;
     g.SR = P_r * g.spp0;
     g.S = g.SR + (P_t - P_r) * g.spp1;
     const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
     g.sp = make_split(g.S, C);
     g.a0 = split_start(g.sp, c);
     g.a1 = split_start(g.sp, c + 1);
-    // Whole units per CTA when every unit has the same chunk count and the
-    // extra unit a CTA may get costs under ~48 KB (about a microsecond of
-    // one SM's share of HBM): no unit is then shared between CTAs.
-    if (g.ch0 > 1 && (P_t == P_r || g.ch1 == g.ch0)) {
+    // Gate/up: whole units per CTA when every unit has the same chunk count
+    // and the extra unit a CTA may get costs under ~48 KB (about a
+    // microsecond of one SM's share of HBM): no unit is then shared.
+    if (phase == 0 && g.ch0 > 1 && (P_t == P_r || g.ch1 == g.ch0)) {
         const int U = g.S / g.ch0;
-        const int unit_bytes = g.gk0 * (phase == 0 ? 2 : 1) * (a.bits * 128 + 32);
+        const int unit_bytes = g.gk0 * 2 * (a.bits * 128 + 32);
         const int64_t extra = (int64_t)((U + C - 1) / C) * C - U;  // C x (max - mean) units
         if (extra * unit_bytes < (int64_t)C * 48 * 1024) {
             const Split su = make_split(U, C);
@@ -494,7 +566,7 @@ __device__ __forceinline__ Geo make_geo(const LayerArgs &a, int phase, int P_r, 
 }
 
 struct Pos {
-    int p, s, c;  // pair, strip, chunk
+    int p, s, c;  // pair, strip (gate/up) or step within the pair (down), chunk
 };
 
 __device__ __forceinline__ Pos decode(const Geo &g, int i)
@@ -527,12 +599,11 @@ __device__ __forceinline__ void advance(const UnitGeo &u, Pos &q)
     }
 }
 
-// The ring's producer (lane 0 of warp 0): the next stage to issue, as a
-// phase and a step of that phase.
-// Order of a CTA's steps: a unit cut by the end of the range is run first,
-// then the range from its start (whose first unit may be cut by the start).
-// Both contributors of a shared unit then reach it early, so the fixup that
-// joins their sums is off the critical path.
+// Order of a CTA's gate/up steps: a unit cut by the end of the range is run
+// first, then the range from its start (whose first unit may be cut by the
+// start).  The CTA then hands its part of the shared tail unit to the next
+// CTA early, and finishes its head unit (whose first part the previous CTA
+// ran first) last among its contributors.
 __device__ __forceinline__ void set_order(Geo &g)
 {
     g.ts = g.a1;
@@ -549,6 +620,14 @@ __device__ __forceinline__ int step_at(const Geo &g, int k)
 {
     const int nt = g.a1 - g.ts;
     return k < nt ? g.ts + k : g.a0 + (k - nt);
+}
+
+// Output strips of down step (pair, step s): [first, first + count).
+__device__ __forceinline__ int down_first(const UnitGeo &u, const Pos &q) { return q.s * u.ms; }
+__device__ __forceinline__ int down_count(const Geo &g, const UnitGeo &u, const Pos &q)
+{
+    const int s0 = q.s * u.ms;
+    return min(u.ms, g.rows - s0);
 }
 
 // Kept in shared memory, like the geometry of both phases (CTA-uniform).
@@ -604,9 +683,6 @@ __device__ __forceinline__ int produce(const LayerArgs &a, const RouteView &rv, 
     const UnitGeo u = unit_geo(g, pr.q.p);
     const int e = rv.pairs[pr.q.p * kPairInts];
     const int TB = tile_bytes(pair_bits<BITS>(a, e));
-    const int GB = pr.phase == 0 ? 2 * TB : TB;
-    const int g0 = pr.q.c * u.gc;
-    const int ng = min(u.gk - g0, u.gc);
     const uint8_t *base;
     if (e < 0)
         base = a.tiles_shared + (pr.phase ? a.down_off_shared : 0);
@@ -615,9 +691,19 @@ __device__ __forceinline__ int produce(const LayerArgs &a, const RouteView &rv, 
     else  // the expert's own place and down offset in a bank of mixed depths
         base = a.tiles_routed + mixed_expert_offset(a, e) +
                (pr.phase ? 2ll * a.d * a.f / 1024 * TB : 0);
-    const uint8_t *src = base + ((int64_t)pr.q.s * u.gk + g0) * GB;
-    mbar_arrive_expect_tx(&full[slot], static_cast<unsigned>(ng * GB));
-    bulk_g2s(ring + slot * SB, src, static_cast<unsigned>(ng * GB), &full[slot]);
+    const uint8_t *src;
+    unsigned bytes;
+    if (pr.phase == 0) {
+        const int g0 = pr.q.c * u.gc;
+        const int ng = min(u.gk - g0, u.gc);
+        src = base + ((int64_t)pr.q.s * u.gk + g0) * 2 * TB;
+        bytes = static_cast<unsigned>(ng * 2 * TB);
+    } else {
+        src = base + (int64_t)down_first(u, pr.q) * u.gk * TB;
+        bytes = static_cast<unsigned>(down_count(g, u, pr.q) * u.gk * TB);
+    }
+    mbar_arrive_expect_tx(&full[slot], bytes);
+    bulk_g2s(ring + slot * SB, src, bytes, &full[slot]);
     pr.next = j + 1;
     if (++pr.k == g.a1 - g.a0) {
         ++pr.phase;
@@ -630,21 +716,19 @@ __device__ __forceinline__ int produce(const LayerArgs &a, const RouteView &rv, 
     return 1;
 }
 
-// The lane's view of a pair record: column count, its token row (gq) and
-// the tokens of its two output columns.
+// The lane's view of a pair record: column count and the token of its row
+// of the B fragment (column gq).
 struct PairInfo {
-    int ncols, tok, t0, t1;
+    int ncols, tok;
 };
 
 __device__ __forceinline__ PairInfo read_pair(const RouteView &rv, int p)
 {
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const int lane = threadIdx.x & 31, gq = lane >> 2;
     const int32_t *pr = rv.pairs + p * kPairInts;
     PairInfo pi;
     pi.ncols = pr[1];
     pi.tok = gq < pi.ncols ? pr[2 + gq] : 0;
-    pi.t0 = 2 * tig < pi.ncols ? pr[2 + 2 * tig] : -1;
-    pi.t1 = 2 * tig + 1 < pi.ncols ? pr[2 + 2 * tig + 1] : -1;
     return pi;
 }
 
@@ -674,100 +758,128 @@ __device__ __forceinline__ void finish_bias(BFrag &f, float2 x0, float2 x1)
     }
 }
 
-// Raw B operand of one group as loaded: gate/up -- this lane's 16
-// activations (columns 64 gi + 16 tig .. +15 of its token; bf16 x: 2
-// vectors, fp32 x: 4) and the group sums of its two output columns; down --
-// h hi (v[0..1]) and lo (v[2..3]) and the lane's strip of the group sums.
-// All through L1: x is read-only, and h, the group sums and xsum were
-// published (release / acquire) before the first read of each.
-template <int NV>
-struct BRaw {
-    uint4 v[NV];
-    float2 xs0, xs1;
-};
-
-template <int PHASE, bool XBF16, int NV>
-__device__ __forceinline__ void load_raw(const LayerArgs &a, const PairInfo &pi, int p, int gi, int fmax,
-                                         BRaw<NV> &r)
+// Class sums of a group for the column biases: s0 over the lane's columns
+// 16 tig + i with i % 4 in {0, 1}, s1 over i % 4 in {2, 3} (the halves the
+// A fragment's registers 0-1 and 2-3 multiply).  Summed over the group's four
+// lanes of token row gq, then fetched for the two output columns this lane's
+// accumulators hold (2 tig and 2 tig + 1: lanes 8 tig and 8 tig + 4).
+template <int BITS>
+__device__ __forceinline__ void bias_from_sums(BFrag &f, float s0, float s1)
 {
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
-    const int d = a.d;
-    const bool valid = gq < pi.ncols;
-    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-    const float2 z2 = make_float2(0.f, 0.f);
-    if (PHASE == 0) {
-        if (XBF16) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const uint16_t *>(a.x) + (int64_t)pi.tok * d + gi * kGroup + 16 * tig);
-            r.v[0] = valid ? __ldg(row) : z4;
-            r.v[1] = valid ? __ldg(row + 1) : z4;
-        } else {
-            const uint4 *row = reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const float *>(a.x) + (int64_t)pi.tok * d + gi * kGroup + 16 * tig);
-#pragma unroll
-            for (int i = 0; i < NV; ++i)
-                r.v[i] = valid ? __ldg(row + i) : z4;
-        }
-        const float2 *xs = reinterpret_cast<const float2 *>(a.xsum);
-        r.xs0 = pi.t0 >= 0 ? __ldca(xs + (int64_t)pi.t0 * (d / kGroup) + gi) : z2;
-        r.xs1 = pi.t1 >= 0 ? __ldca(xs + (int64_t)pi.t1 * (d / kGroup) + gi) : z2;
-    } else {
-        const int64_t off = ((int64_t)p * kPairCols + gq) * fmax + gi * kGroup + 16 * tig;
-        const uint4 *hi = reinterpret_cast<const uint4 *>(a.h_hi + off);
-        const uint4 *lo = reinterpret_cast<const uint4 *>(a.h_lo + off);
-        r.v[0] = valid ? __ldca(hi) : z4;
-        r.v[1] = valid ? __ldca(hi + 1) : z4;
-        r.v[2] = valid ? __ldca(lo) : z4;
-        r.v[3] = valid ? __ldca(lo + 1) : z4;
-        // group sums of h: lane (gq, tig) loads strip 4 gi + (gq & 3) of its
-        // two columns; cook_b adds the four strips with shuffles
-        const int nstrip = fmax / kTileRows;
-        const int c0 = 2 * tig, c1 = c0 + 1;
-        const float2 *hp = reinterpret_cast<const float2 *>(a.hs_part);
-        const int st = 4 * gi + (gq & 3);
-        r.xs0 = c0 < pi.ncols ? __ldca(hp + ((int64_t)p * kPairCols + c0) * nstrip + st) : z2;
-        r.xs1 = c1 < pi.ncols ? __ldca(hp + ((int64_t)p * kPairCols + c1) * nstrip + st) : z2;
-    }
+    const int tig = threadIdx.x & 3;
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    float2 x0, x1;
+    x0.x = __shfl_sync(0xffffffffu, s0, 8 * tig);
+    x0.y = __shfl_sync(0xffffffffu, s1, 8 * tig);
+    x1.x = __shfl_sync(0xffffffffu, s0, 8 * tig + 4);
+    x1.y = __shfl_sync(0xffffffffu, s1, 8 * tig + 4);
+    finish_bias<BITS>(f, x0, x1);
 }
 
-// mma fragments and biases from a BRaw (every lane of the warp calls it).
-template <int BITS, int PHASE, bool XBF16, int NV>
-__device__ __forceinline__ void cook_b(const BRaw<NV> &r, BFrag &f)
+// Gate/up B operand of group gi: the lane's 16 activations of its token
+// (pair column gq) at columns 64 gi + 16 tig .. +15 (bf16 x: 2 vectors, fp32
+// x: 4, split into bf16 hi + lo), and the column biases.  on = the group
+// exists (warp-uniform); an absent group or column gives zeros.  Every lane
+// of the warp calls it.
+template <int BITS, bool XBF16>
+__device__ __forceinline__ void load_b_x(const LayerArgs &a, const PairInfo &pi, int gi, bool on,
+                                         BFrag &f)
 {
-    float2 x0 = r.xs0, x1 = r.xs1;
-    if (PHASE == 1) {
-        const uint32_t *hv = reinterpret_cast<const uint32_t *>(r.v);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f.b0[j] = hv[2 * j];
-            f.b1[j] = hv[2 * j + 1];
-            f.b0l[j] = hv[8 + 2 * j];
-            f.b1l[j] = hv[8 + 2 * j + 1];
-        }
-#pragma unroll
-        for (int o = 4; o <= 8; o <<= 1) {
-            x0.x += __shfl_xor_sync(0xffffffffu, x0.x, o);
-            x0.y += __shfl_xor_sync(0xffffffffu, x0.y, o);
-            x1.x += __shfl_xor_sync(0xffffffffu, x1.x, o);
-            x1.y += __shfl_xor_sync(0xffffffffu, x1.y, o);
-        }
-    } else if (!XBF16) {
-        const float *xv = reinterpret_cast<const float *>(r.v);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            split_bf16x2(xv[4 * j + 0], xv[4 * j + 1], f.b0[j], f.b0l[j]);
-            split_bf16x2(xv[4 * j + 2], xv[4 * j + 3], f.b1[j], f.b1l[j]);
-        }
-    } else {
-        const uint32_t *xv = reinterpret_cast<const uint32_t *>(r.v);
+    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const bool valid = on && gq < pi.ncols;
+    float s0 = 0.f, s1 = 0.f;
+    if (XBF16) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(
+            reinterpret_cast<const uint16_t *>(a.x) + (int64_t)pi.tok * a.d + gi * kGroup + 16 * tig);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 v0 = valid ? __ldg(row) : z, v1 = valid ? __ldg(row + 1) : z;
+        const uint32_t xv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             f.b0[j] = xv[2 * j];
             f.b1[j] = xv[2 * j + 1];
             f.b0l[j] = f.b1l[j] = 0u;
+            s0 += bf16lo_to_f32(xv[2 * j]) + bf16hi_to_f32(xv[2 * j]);
+            s1 += bf16lo_to_f32(xv[2 * j + 1]) + bf16hi_to_f32(xv[2 * j + 1]);
+        }
+    } else {
+        const float4 *row = reinterpret_cast<const float4 *>(
+            reinterpret_cast<const float *>(a.x) + (int64_t)pi.tok * a.d + gi * kGroup + 16 * tig);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 v = valid ? __ldg(row + j) : z;
+            split_bf16x2(v.x, v.y, f.b0[j], f.b0l[j]);
+            split_bf16x2(v.z, v.w, f.b1[j], f.b1l[j]);
+            s0 += v.x + v.y;
+            s1 += v.z + v.w;
         }
     }
-    finish_bias<BITS>(f, x0, x1);
+    bias_from_sums<BITS>(f, s0, s1);
+}
+
+// Down B operand of group gi of pair p: the lane's 16 h values of its
+// column (rows 64 gi + 16 tig .. +15), polled until every word carries the
+// launch's tag, split into the bf16 hi and lo fragments, and the column
+// biases.  False if the bounded poll ran out.  Every lane calls it.
+template <int BITS>
+__device__ __forceinline__ bool load_b_h(const LayerArgs &a, const PairInfo &pi, int p, int gi, bool on,
+                                         int fmax, uint32_t tag, BFrag &f)
+{
+    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const bool valid = on && gq < pi.ncols;
+    const u64 *src = a.h_t + ((int64_t)p * kPairCols + gq) * fmax + gi * kGroup + 16 * tig;
+    u64 w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        w[i] = 0ull;
+    bool ok = true;
+    if (__any_sync(0xffffffffu, valid)) {
+        const long long t0 = clock64();
+        unsigned ns = 64;
+        for (;;) {
+            bool mine = true;
+            if (valid) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 2)
+                    ld_word2(src + i, w[i], w[i + 1]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    mine = mine && word_tag(w[i]) == tag;
+            }
+            if (__all_sync(0xffffffffu, mine))
+                break;
+            if (clock64() - t0 > a.wait_cycles) {
+                ok = false;
+                break;
+            }
+            __nanosleep(ns);
+            if (ns < 512)
+                ns *= 2;
+        }
+    }
+    if (!valid || !ok) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = 0ull;
+    }
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t w0 = word_payload(w[4 * j]), w1 = word_payload(w[4 * j + 1]);
+        const uint32_t w2 = word_payload(w[4 * j + 2]), w3 = word_payload(w[4 * j + 3]);
+        f.b0[j] = __byte_perm(w0, w1, 0x5410);
+        f.b0l[j] = __byte_perm(w0, w1, 0x7632);
+        f.b1[j] = __byte_perm(w2, w3, 0x5410);
+        f.b1l[j] = __byte_perm(w2, w3, 0x7632);
+        s0 += (bf16lo_to_f32(w0) + bf16hi_to_f32(w0)) + (bf16lo_to_f32(w1) + bf16hi_to_f32(w1));
+        s1 += (bf16lo_to_f32(w2) + bf16hi_to_f32(w2)) + (bf16lo_to_f32(w3) + bf16hi_to_f32(w3));
+    }
+    bias_from_sums<BITS>(f, s0, s1);
+    return ok;
 }
 
 // Decode + multiply one tile from shared memory into acc: one mma chain
@@ -831,151 +943,128 @@ __device__ __forceinline__ void mac_tile(const uint8_t *tile, const BFrag &f, fl
     acc[3] = fmaf(s01.y, dv[3], acc[3]);
 }
 
-// Finalise unit (p, s) from its full-K sums, one warp (cold path).
-// Phase 0: h = SiLU(g) * u as bf16 hi + lo and the strip's per-class sums of
-// h.  Phase 1: o.  The caller counts the finished unit.
 // What the epilogue writes, passed by value (registers) to its cold helpers.
 struct EpiOut {
-    uint16_t *h_hi, *h_lo;
-    float *hs_part, *o, *partial;
-    unsigned *strip_ctr_g, *strip_ctr_d, *pair_done;
-    int d, fmax, max_strips;
+    u64 *h_t, *part_t, *o_t;
+    float *o;
+    int d, fmax, fused;
+    uint32_t tag;
+    long long wait_cycles;
+    int *status;
 };
 
-template <int BITS, int PHASE>
-__device__ __noinline__ void finalize_unit(const EpiOut a, int ncols, int p, int s, float4 ag, float4 au)
+// Finalise gate/up strip s of pair p from its full-K sums (one warp, cold
+// path): h = SiLU(g) * u as bf16 hi + lo, stored tagged.
+template <int BITS>
+__device__ __noinline__ void finalize_gateup(const EpiOut a, int ncols, int p, int s, float4 ag, float4 au)
 {
     constexpr float L = BITS == 4 ? 7.5f : 1.5f;
     const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
-    const int d = a.d;
-    const int fmax = a.fmax;
     const float invL = 1.0f / L;
-    const int c0 = 2 * tig;
     const float gv[4] = {ag.x, ag.y, ag.z, ag.w}, uv[4] = {au.x, au.y, au.z, au.w};
-    if (PHASE == 0) {
-        const int nstrip = fmax / kTileRows;
-        float hs[2] = {0.f, 0.f};  // per output column, this lane's rows
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 4; ++e) {
+        const int col = 2 * tig + (e & 1);
+        const int row = 16 * s + gq + 8 * (e >> 1);
+        if (col < ncols) {
             const float g = gv[e] * invL, u = uv[e] * invL;
             const float hv = __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;  // SiLU(g) * u
-            const int col = c0 + (e & 1);
-            const int row = 16 * s + gq + 8 * (e >> 1);
-            if (col < ncols) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
-                const int64_t off = ((int64_t)p * kPairCols + col) * fmax + row;
-                a.h_hi[off] = *reinterpret_cast<const uint16_t *>(&hi);
-                a.h_lo[off] = *reinterpret_cast<const uint16_t *>(&lo);
-            }
-            hs[e & 1] += hv;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
+            const uint32_t pay = static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&hi)) |
+                                 (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&lo)) << 16);
+            st_word(a.h_t + ((int64_t)p * kPairCols + col) * a.fmax + row, tag_word(pay, a.tag));
         }
-        // class of these rows within their 64-row group: (gq >> 1) & 1; sum
-        // over lanes with equal tig and class (lane bits 2 and 4)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            hs[c] += __shfl_xor_sync(0xffffffffu, hs[c], 4);
-            hs[c] += __shfl_xor_sync(0xffffffffu, hs[c], 16);
-        }
-        if ((gq & 5) == 0) {
-            const int cls = (gq >> 1) & 1;
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-                if (c0 + c < ncols)
-                    a.hs_part[(((int64_t)p * kPairCols + c0 + c) * nstrip + s) * 2 + cls] = hs[c];
-        }
-        __syncwarp();  // the caller counts the strip (see count_strip)
-    } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int col = c0 + (e & 1);
-            const int row = 16 * s + gq + 8 * (e >> 1);
-            if (col < ncols)
-                a.o[((int64_t)p * kPairCols + col) * d + row] = gv[e] * invL;
-        }
-        __syncwarp();  // the caller counts the output strip
     }
 }
 
-// One more finished gate/up strip of pair p: counted in shared memory and
-// published at the end of the CTA's gate/up range, or published at once
-// (release) when the CTA's range spans too many pairs.
-__device__ __forceinline__ void count_strip(const EpiOut &a, const int *pspan, unsigned *pcnt, int p)
+// Finalise down strip s of pair p: o rows, tagged for the in-kernel
+// combine or plain for the combine kernel.
+template <int BITS>
+__device__ __forceinline__ void finalize_down(const EpiOut &a, int ncols, int p, int s, float4 ag)
 {
-    if ((threadIdx.x & 31) != 0)
-        return;
-    const int j = p - pspan[0];
-    if (pspan[1] > 0 && j >= 0 && j < pspan[1]) {
-        atomicAdd(pcnt + j, 1u);
-    } else {
-        fence_acq_rel();
-        red_add_relaxed(a.pair_done + p, 1u);
+    constexpr float L = BITS == 4 ? 7.5f : 1.5f;
+    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const float invL = 1.0f / L;
+    const float gv[4] = {ag.x, ag.y, ag.z, ag.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int col = 2 * tig + (e & 1);
+        const int row = 16 * s + gq + 8 * (e >> 1);
+        if (col < ncols) {
+            const int64_t off = ((int64_t)p * kPairCols + col) * a.d + row;
+            const float ov = gv[e] * invL;
+            if (a.fused)
+                st_word(a.o_t + off, tag_word(__float_as_uint(ov), a.tag));
+            else
+                a.o[off] = ov;
+        }
     }
 }
 
-// A finished unit: a gate/up strip of pair p, or a down unit of output
-// strip s (counted per CTA, published after the down phase).
-template <int PHASE>
-__device__ __forceinline__ void count_unit(const EpiOut &a, const int *pspan, unsigned *pcnt,
-                                           unsigned *ccnt, int p, int s)
-{
-    if (PHASE == 0)
-        count_strip(a, pspan, pcnt, p);
-    else if ((threadIdx.x & 31) == 0)
-        atomicAdd(ccnt + s, 1u);
-}
-
-// Unit (p, s) shared with other CTAs (cold path): store this CTA's sums,
-// count the contributors; the last one adds all sums in CTA order and
-// finalises.  Slot 0 of a CTA holds the unit straddling its first step,
-// slot 1 the one straddling its last; each phase has its own slots.
-template <int BITS, int PHASE>
-__device__ __noinline__ void fixup_unit(const EpiOut a, int ncols, const Geo &g, int p, int s, int ustart,
-                                        int uend, float4 tg, float4 tu, unsigned *pcnt, const int *pspan,
-                                        unsigned *ccnt)
+// Gate/up strip (p, s) shared with other CTAs (cold path).  Slot 0 of a CTA
+// holds the unit straddling the start of its range, slot 1 the one
+// straddling its end.  A contributor that does not hold the unit's last
+// step stores its sums tagged and is done; the one that does (the last
+// contributor) polls the others' sums, adds them all in CTA order and
+// finalises.  False if a bounded poll ran out.
+template <int BITS>
+__device__ __noinline__ bool fixup_gateup(const EpiOut a, int ncols, const Geo &g, int p, int s, int ustart,
+                                          int uend, float4 tg, float4 tu)
 {
     const int lane = threadIdx.x & 31;
-    float4 *part = reinterpret_cast<float4 *>(a.partial) + (size_t)PHASE * gridDim.x * 2 * 64;
-    const int my = ustart < g.a0 ? 0 : 1;
-    float4 *mine = part + ((size_t)blockIdx.x * 2 + my) * 64;
-    mine[lane] = tg;
-    if (PHASE == 0)
-        mine[32 + lane] = tu;
-    __syncwarp();
+    const int c = static_cast<int>(blockIdx.x);
     const int cf = split_owner(g.sp, ustart), cl = split_owner(g.sp, uend - 1);
-    unsigned *ctr = (PHASE == 0 ? a.strip_ctr_g : a.strip_ctr_d) + (int64_t)p * a.max_strips + s;
-    unsigned old = 0;
-    if (lane == 0)
-        old = atom_add_acqrel(ctr, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != static_cast<unsigned>(cl - cf))
-        return;
-    __syncwarp();
-    float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg;
-    for (int c0 = cf; c0 <= cl; c0 += 4) {
-        float4 vg[4], vu[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int c = c0 + q;
-            vg[q] = vu[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c <= cl) {
-                const int sl = split_start(g.sp, c) > ustart ? 0 : 1;
-                const float4 *src = part + ((size_t)c * 2 + sl) * 64;
-                vg[q] = __ldcg(src + lane);
-                if (PHASE == 0)
-                    vu[q] = __ldcg(src + 32 + lane);
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            sg.x += vg[q].x, sg.y += vg[q].y, sg.z += vg[q].z, sg.w += vg[q].w;
-            su.x += vu[q].x, su.y += vu[q].y, su.z += vu[q].z, su.w += vu[q].w;
-        }
+    if (c != cl) {
+        const int my = ustart < g.a0 ? 0 : 1;
+        u64 *mine = a.part_t + (((int64_t)c * 2 + my) * 32 + lane) * 8;
+        st_word2(mine, tag_word(__float_as_uint(tg.x), a.tag), tag_word(__float_as_uint(tg.y), a.tag));
+        st_word2(mine + 2, tag_word(__float_as_uint(tg.z), a.tag), tag_word(__float_as_uint(tg.w), a.tag));
+        st_word2(mine + 4, tag_word(__float_as_uint(tu.x), a.tag), tag_word(__float_as_uint(tu.y), a.tag));
+        st_word2(mine + 6, tag_word(__float_as_uint(tu.z), a.tag), tag_word(__float_as_uint(tu.w), a.tag));
+        return true;
     }
-    if (lane == 0)
-        *ctr = 0u;
-    finalize_unit<BITS, PHASE>(a, ncols, p, s, sg, su);
-    count_unit<PHASE>(a, pspan, pcnt, ccnt, p, s);
+    float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg;
+    bool ok = true;
+    for (int c2 = cf; c2 <= cl; ++c2) {
+        float v[8];
+        if (c2 == c) {
+            v[0] = tg.x, v[1] = tg.y, v[2] = tg.z, v[3] = tg.w;
+            v[4] = tu.x, v[5] = tu.y, v[6] = tu.z, v[7] = tu.w;
+        } else {
+            const int sl = split_start(g.sp, c2) > ustart ? 0 : 1;
+            const u64 *src = a.part_t + (((int64_t)c2 * 2 + sl) * 32 + lane) * 8;
+            u64 w[8];
+            const long long t0 = clock64();
+            unsigned ns = 64;
+            for (;;) {
+                bool mine = true;
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    ld_word2(src + i, w[i], w[i + 1]);
+                    mine = mine && word_tag(w[i]) == a.tag && word_tag(w[i + 1]) == a.tag;
+                }
+                if (__all_sync(0xffffffffu, mine))
+                    break;
+                if (clock64() - t0 > a.wait_cycles) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(ns);
+                if (ns < 512)
+                    ns *= 2;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = __uint_as_float(word_payload(w[i]));
+        }
+        sg.x += v[0], sg.y += v[1], sg.z += v[2], sg.w += v[3];
+        su.x += v[4], su.y += v[5], su.z += v[6], su.w += v[7];
+    }
+    if (!ok)
+        return false;
+    finalize_gateup<BITS>(a, ncols, p, s, sg, su);
+    return true;
 }
 
 // Shared state of the streaming phases, one per CTA.
@@ -983,15 +1072,13 @@ struct Stream {
     uint8_t *ring;
     uint64_t *full, *empty;          // [NS]: 1 arrival + bytes / kStreamWarps arrivals
     uint64_t *red_full, *red_empty;  // [kRedSlots]: kStreamWarps arrivals / 1 arrival
-    unsigned *pcnt;                  // [kMaxSpan] finished gate/up strips per pair
-    const int *pspan;                // [0] first pair, [1] span (0: publish each at once)
-    unsigned *ccnt;                  // [d/16] finished down units per output strip
     float4 *red;                     // [kRedSlots][kStreamWarps][2][32]
     volatile int *fail;              // a bounded wait ran out somewhere in the CTA
-    Producer *pr;                    // shared; used by lane 0 of warp 0 only
+    Producer *pr;                    // shared; used by lane 0 of the producer warp only
     const Geo *geo;                  // shared, [2]
     uint32_t seq;                    // stages consumed by this (streaming) warp
-    int uc;                          // units ended so far
+    int uc;                          // reduction items so far
+    uint32_t tag;                    // this launch's tag
 };
 
 __device__ __forceinline__ bool unit_ends(const Geo &g, const UnitGeo &u, const Pos &q, int i)
@@ -999,57 +1086,66 @@ __device__ __forceinline__ bool unit_ends(const Geo &g, const UnitGeo &u, const 
     return q.c == u.ch - 1 || i == g.a1 - 1 || (g.ts < g.a1 && i == g.ts - 1);
 }
 
-// The warp's tiles of one stage (chunk c of the unit) at depth B:
-// branch-free over the warp's two groups (tiles of absent groups read
-// in-bounds stage bytes and are dropped), so the four (down: two) mma
-// chains of the step schedule together.
-template <int B, int PHASE, int KG, bool kSplit, int NB>
-__device__ __forceinline__ void step_tiles(const uint8_t *stage, const BFrag (&bf)[NB], int qc, bool g0,
-                                           bool g1, float (&accg)[4], float (&accu)[4],
-                                           float (&accg2)[4], float (&accu2)[4])
+// Wait for ring stage `st.seq` (bounded); false if the CTA has failed.
+template <int NS>
+__device__ __forceinline__ bool wait_stage(const LayerArgs &a, Stream &st, int slot)
 {
-    constexpr int TB = tile_bytes(B), GB = PHASE == 0 ? 2 * TB : TB;
-    const int warp = threadIdx.x >> 5;
-    if (PHASE == 0) {
-#pragma unroll
-        for (int c = 0; c < KG; ++c) {
-            if (c == qc) {
-                mac_tile<B, kSplit>(stage + warp * GB, bf[2 * c], accg, g0);
-                mac_tile<B, kSplit>(stage + warp * GB + TB, bf[2 * c], accu, g0);
-                mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * GB, bf[2 * c + 1], accg2, g1);
-                mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * GB + TB, bf[2 * c + 1], accu2, g1);
-            }
+    const int lane = threadIdx.x & 31;
+    if (*st.fail)
+        return false;
+    if (!mbar_wait_bounded(&st.full[slot], (st.seq / NS) & 1u)) {
+        if (lane == 0) {
+            set_status(a.status, kStatusTimeout);
+            *st.fail = 1;
         }
-    } else {
-        mac_tile<B, kSplit>(stage + warp * GB, bf[0], accg, g0);
-        mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * GB, bf[1], accu, g1);
+        return false;
     }
+    return true;
 }
 
-// One phase (0: gate/up, 1: down) of a streaming warp.  The warp holds the
-// B fragments of its groups of the current pair: groups c * gc + w and
-// c * gc + w + 16 of each chunk c (gate/up: at most KG chunks; down: one).
-// At a unit's end it leaves its sums in a slot for the epilogue warps.
-template <int BITS, bool XBF16, int KG, int PHASE>
-__device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView &rv, Stream &st)
+// Hand two float4 per lane to the epilogue warps through reduction slot
+// st.uc (waiting for the slot to be free).
+__device__ __forceinline__ void put_red(const LayerArgs &a, Stream &st, float4 v0, float4 v1)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rs = st.uc % kRedSlots;
+    const unsigned rph = static_cast<unsigned>(st.uc / kRedSlots);
+    if (st.uc >= kRedSlots && !*st.fail &&
+        !mbar_wait_bounded(&st.red_empty[rs], (rph - 1u) & 1u) && lane == 0) {
+        set_status(a.status, kStatusTimeout);
+        *st.fail = 1;
+    }
+    float4 *rw = st.red + ((rs * kStreamWarps + warp) * 2) * 32;
+    rw[lane] = v0;
+    rw[32 + lane] = v1;
+    __syncwarp();
+    if (lane == 0 && !*st.fail)
+        mbar_arrive(&st.red_full[rs]);
+    ++st.uc;
+}
+
+// The gate/up phase of a streaming warp.  The warp holds the B fragments
+// of its groups of the current pair: groups c * gc + w and c * gc + w + 16
+// of each chunk c (at most KG chunks).  At a unit's end it hands its sums to
+// the epilogue warps.
+template <int BITS, bool XBF16, int KG>
+__device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
     constexpr int NS = num_stages(ring_bits(BITS)), SB = stage_bytes(ring_bits(BITS));
-    constexpr int NV = (PHASE == 1 || !XBF16) ? 4 : 2;
-    constexpr bool kSplit = PHASE == 1 || !XBF16;
-    constexpr int NB = PHASE == 0 ? 2 * KG : 2;  // B fragments held
+    constexpr bool kSplit = !XBF16;
+    constexpr int NB = 2 * KG;  // B fragments held
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Geo &g = st.geo[PHASE];
+    const Geo &g = st.geo[0];
     const int a0 = g.a0, a1 = g.a1, n = a1 - a0, ts = g.ts, nt = a1 - ts;
     if (n <= 0)
         return;
-    const int fmax = a.f > a.fs ? a.f : a.fs;
     Pos q = decode(g, nt > 0 ? ts : a0);
     UnitGeo u = unit_geo(g, q.p);
     int loaded = -1;
     int pb = ring_bits(BITS);  // depth of the loaded pair
     BFrag bf[NB];
     float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
-    float accg2[4] = {0.f, 0.f, 0.f, 0.f}, accu2[4] = {0.f, 0.f, 0.f, 0.f};  // gate/up: second group
+    float accg2[4] = {0.f, 0.f, 0.f, 0.f}, accu2[4] = {0.f, 0.f, 0.f, 0.f};  // second group
 #pragma unroll 1
     for (int kk = 0; kk < n; ++kk) {
         const int i = kk < nt ? ts + kk : a0 + (kk - nt);
@@ -1057,95 +1153,152 @@ __device__ __forceinline__ void stream_phase(const LayerArgs &a, const RouteView
             q = decode(g, a0);
         if (q.p != loaded) {
             u = unit_geo(g, q.p);
-            if (PHASE == 1) {
-                // h of pair q.p is complete once all its gate/up strips are
-                // published; one warp polls, the others sleep at the barrier
-                stream_barrier();
-                if (warp == kStreamWarps - 1 && !*st.fail) {
-                    const int fp = q.p < g.P_r ? a.f : a.fs;
-                    if (!warp_wait_geq(a.pair_done + q.p, static_cast<unsigned>(fp / kTileRows), a.status) &&
-                        lane == 0)
-                        *st.fail = 1;
-                }
-                stream_barrier();
-            }
             const PairInfo pi = read_pair(rv, q.p);
             pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 const int c = b >> 1, lg = warp + (b & 1) * kStreamWarps;  // chunk, group in chunk
                 const int gi = c * u.gc + lg;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    bf[b].b0[j] = bf[b].b1[j] = bf[b].b0l[j] = bf[b].b1l[j] = 0u;
-                bf[b].bias0 = bf[b].bias1 = 0.f;
-                if (c < u.ch && lg < u.gc && gi < u.gk) {
-                    BRaw<NV> raw;
-                    load_raw<PHASE, XBF16, NV>(a, pi, q.p, gi, fmax, raw);
-                    if (BITS != 0 || pb == 4)
-                        cook_b<ring_bits(BITS), PHASE, XBF16, NV>(raw, bf[b]);
-                    else
-                        cook_b<2, PHASE, XBF16, NV>(raw, bf[b]);
-                }
+                const bool on = c < u.ch && lg < u.gc && gi < u.gk;
+                if (BITS != 0 || pb == 4)
+                    load_b_x<ring_bits(BITS), XBF16>(a, pi, gi, on, bf[b]);
+                else
+                    load_b_x<2, XBF16>(a, pi, gi, on, bf[b]);
             }
             loaded = q.p;
         }
         const int slot = static_cast<int>(st.seq % NS);
-        bool ok = !*st.fail;
-        if (ok && !mbar_wait_bounded(&st.full[slot], (st.seq / NS) & 1u)) {
-            ok = false;
-            if (lane == 0) {
-                set_status(a.status, kStatusTimeout);
-                *st.fail = 1;
-            }
-        }
+        const bool ok = wait_stage<NS>(a, st, slot);
         if (ok) {
             // branch-free over the warp's two groups (tiles of absent groups
-            // read in-bounds stage bytes and are dropped), so the four (down:
-            // two) mma chains of the step schedule together
+            // read in-bounds stage bytes and are dropped), so the four mma
+            // chains of the step schedule together
             const uint8_t *stage = st.ring + slot * SB;
             const int ng = min(u.gc, u.gk - q.c * u.gc);  // groups in this chunk
             const bool g0 = warp < ng, g1 = warp + kStreamWarps < ng;
-            if (BITS != 0 || pb == 4)
-                step_tiles<ring_bits(BITS), PHASE, KG, kSplit>(stage, bf, q.c, g0, g1, accg, accu, accg2,
-                                                               accu2);
-            else
-                step_tiles<2, PHASE, KG, kSplit>(stage, bf, q.c, g0, g1, accg, accu, accg2, accu2);
+#pragma unroll
+            for (int c = 0; c < KG; ++c) {
+                if (c == q.c) {
+                    if (BITS != 0 || pb == 4) {
+                        constexpr int B = ring_bits(BITS), TB = tile_bytes(B);
+                        mac_tile<B, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, g0);
+                        mac_tile<B, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, g0);
+                        mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2, g1);
+                        mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1], accu2,
+                                            g1);
+                    } else {
+                        constexpr int TB = tile_bytes(2);
+                        mac_tile<2, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, g0);
+                        mac_tile<2, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, g0);
+                        mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2, g1);
+                        mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1], accu2,
+                                            g1);
+                    }
+                }
+            }
         }
         __syncwarp();
         if (ok && lane == 0)
             mbar_arrive(&st.empty[slot]);
         ++st.seq;
-        if (q.c == u.ch - 1 || i == a1 - 1 || (nt > 0 && i == ts - 1)) {
-            const int rs = st.uc % kRedSlots;
-            const unsigned rph = static_cast<unsigned>(st.uc / kRedSlots);
-            if (st.uc >= kRedSlots && !*st.fail &&
-                !mbar_wait_bounded(&st.red_empty[rs], (rph - 1u) & 1u) && lane == 0) {
-                set_status(a.status, kStatusTimeout);
-                *st.fail = 1;
-            }
+        if (unit_ends(g, u, q, i)) {
             // the two groups' partial sums of the same output rows
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (PHASE == 1) {
-                    accg[e] += accu[e];
-                } else {
-                    accg[e] += accg2[e];
-                    accu[e] += accu2[e];
-                }
+                accg[e] += accg2[e];
+                accu[e] += accu2[e];
             }
-            float4 *rw = st.red + ((rs * kStreamWarps + warp) * 2) * 32;
-            rw[lane] = make_float4(accg[0], accg[1], accg[2], accg[3]);
-            if (PHASE == 0)
-                rw[32 + lane] = make_float4(accu[0], accu[1], accu[2], accu[3]);
+            put_red(a, st, make_float4(accg[0], accg[1], accg[2], accg[3]),
+                    make_float4(accu[0], accu[1], accu[2], accu[3]));
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 accg[e] = accu[e] = accg2[e] = accu2[e] = 0.f;
-            __syncwarp();
-            if (lane == 0 && !*st.fail)
-                mbar_arrive(&st.red_full[rs]);
-            ++st.uc;
         }
+        advance(u, q);
+    }
+}
+
+// The down phase of a streaming warp: a step is up to kMaxDownStrips whole
+// strips of one pair; the warp's groups w and w + 16 of each strip use the
+// same two B fragments (h of the pair, polled when the warp reaches the
+// pair).  Items of two strips go to the epilogue warps.
+template <int BITS>
+__device__ __forceinline__ void stream_down(const LayerArgs &a, const RouteView &rv, Stream &st)
+{
+    constexpr int NS = num_stages(ring_bits(BITS)), SB = stage_bytes(ring_bits(BITS));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = st.geo[1];
+    const int a0 = g.a0, n = g.a1 - g.a0;
+    if (n <= 0)
+        return;
+    const int fmax = a.f > a.fs ? a.f : a.fs;
+    Pos q = decode(g, a0);
+    UnitGeo u = unit_geo(g, q.p);
+    int loaded = -1;
+    int pb = ring_bits(BITS);
+    BFrag bf[2];
+    float acc[kMaxDownStrips][4];
+#pragma unroll
+    for (int j = 0; j < kMaxDownStrips; ++j)
+        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll 1
+    for (int kk = 0; kk < n; ++kk) {
+        if (q.p != loaded) {
+            u = unit_geo(g, q.p);
+            const PairInfo pi = read_pair(rv, q.p);
+            pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
+            bool okb = true;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int gi = warp + b * kStreamWarps;
+                const bool on = gi < u.gk && !*st.fail;
+                if (BITS != 0 || pb == 4)
+                    okb = load_b_h<ring_bits(BITS)>(a, pi, q.p, gi, on, fmax, st.tag, bf[b]) && okb;
+                else
+                    okb = load_b_h<2>(a, pi, q.p, gi, on, fmax, st.tag, bf[b]) && okb;
+            }
+            if (!okb && lane == 0) {
+                set_status(a.status, kStatusTimeout);
+                *st.fail = 1;
+            }
+            loaded = q.p;
+        }
+        const int slot = static_cast<int>(st.seq % NS);
+        const bool ok = wait_stage<NS>(a, st, slot);
+        const int ns = down_count(g, u, q);
+        if (ok) {
+            const uint8_t *stage = st.ring + slot * SB;
+            const bool g0 = warp < u.gk, g1 = warp + kStreamWarps < u.gk;
+#pragma unroll
+            for (int j = 0; j < kMaxDownStrips; ++j) {
+                const bool on0 = g0 && j < ns, on1 = g1 && j < ns;
+                // an absent tile reads tile 0 of the stage (in bounds) and is dropped
+                const int t0 = on0 ? j * u.gk + warp : 0, t1 = on1 ? j * u.gk + warp + kStreamWarps : 0;
+                if (BITS != 0 || pb == 4) {
+                    constexpr int B = ring_bits(BITS), TB = tile_bytes(B);
+                    mac_tile<B, true>(stage + t0 * TB, bf[0], acc[j], on0);
+                    mac_tile<B, true>(stage + t1 * TB, bf[1], acc[j], on1);
+                } else {
+                    constexpr int TB = tile_bytes(2);
+                    mac_tile<2, true>(stage + t0 * TB, bf[0], acc[j], on0);
+                    mac_tile<2, true>(stage + t1 * TB, bf[1], acc[j], on1);
+                }
+            }
+        }
+        __syncwarp();
+        if (ok && lane == 0)
+            mbar_arrive(&st.empty[slot]);
+        ++st.seq;
+#pragma unroll
+        for (int it = 0; it < kMaxDownStrips / 2; ++it) {
+            if (2 * it < ns)
+                put_red(a, st, make_float4(acc[2 * it][0], acc[2 * it][1], acc[2 * it][2], acc[2 * it][3]),
+                        make_float4(acc[2 * it + 1][0], acc[2 * it + 1][1], acc[2 * it + 1][2],
+                                    acc[2 * it + 1][3]));
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxDownStrips; ++j)
+            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
         advance(u, q);
     }
 }
@@ -1167,84 +1320,131 @@ __device__ __forceinline__ void produce_all(const LayerArgs &a, const RouteView 
     }
 }
 
-// One phase of an epilogue warp: the same walk over the CTA's steps; at
-// each unit end it owns (units alternate between the epilogue warps) it adds
-// the 16 streaming warps' sums in warp order, frees the slot, and finalises
-// the unit or, for a unit shared with another CTA, runs the fixup.
-template <int BITS, int PHASE>
-__device__ __forceinline__ void epi_phase(const LayerArgs &a, const RouteView &rv, Stream &st)
+// Sum reduction item st.uc over the 16 streaming warps (warp order) into
+// (v0, v1) and free its slot; false if the wait ran out or the CTA failed.
+__device__ __forceinline__ bool take_red(const LayerArgs &a, Stream &st, float4 &v0, float4 &v1)
 {
-    const int e = (threadIdx.x >> 5) - kStreamWarps, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
+    const int rs = st.uc % kRedSlots;
+    const unsigned rph = static_cast<unsigned>(st.uc / kRedSlots);
+    if (*st.fail)
+        return false;
+    if (!mbar_wait_bounded(&st.red_full[rs], rph & 1u)) {
+        if (lane == 0) {
+            set_status(a.status, kStatusTimeout);
+            *st.fail = 1;
+        }
+        return false;
+    }
+    v0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    v1 = v0;
+#pragma unroll 4
+    for (int w2 = 0; w2 < kStreamWarps; ++w2) {
+        const float4 *rr = st.red + ((rs * kStreamWarps + w2) * 2) * 32;
+        const float4 a0 = rr[lane], a1 = rr[32 + lane];
+        v0.x += a0.x, v0.y += a0.y, v0.z += a0.z, v0.w += a0.w;
+        v1.x += a1.x, v1.y += a1.y, v1.z += a1.z, v1.w += a1.w;
+    }
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(&st.red_empty[rs]);
+    return true;
+}
+
+__device__ __forceinline__ EpiOut epi_out(const LayerArgs &a, uint32_t tag)
+{
     EpiOut eo;
-    eo.h_hi = a.h_hi;
-    eo.h_lo = a.h_lo;
-    eo.hs_part = a.hs_part;
+    eo.h_t = a.h_t;
+    eo.part_t = a.part_t;
+    eo.o_t = a.o_t;
     eo.o = a.o;
-    eo.partial = a.partial;
-    eo.strip_ctr_g = a.strip_ctr_g;
-    eo.strip_ctr_d = a.strip_ctr_d;
-    eo.pair_done = a.pair_done;
     eo.d = a.d;
     eo.fmax = a.f > a.fs ? a.f : a.fs;
-    eo.max_strips = a.max_strips;
-    const Geo &g = st.geo[PHASE];
+    eo.fused = a.fused_combine;
+    eo.tag = tag;
+    eo.wait_cycles = a.wait_cycles;
+    eo.status = a.status;
+    return eo;
+}
+
+// The gate/up phase of an epilogue warp: the same walk over the CTA's
+// steps; at each unit end it owns (items alternate between the epilogue
+// warps) it sums the warps' partials and finalises the unit, or joins a
+// unit shared with other CTAs.
+template <int BITS>
+__device__ __forceinline__ void epi_gateup(const LayerArgs &a, const RouteView &rv, Stream &st)
+{
+    const int e = (threadIdx.x >> 5) - kStreamWarps, lane = threadIdx.x & 31;
+    const EpiOut eo = epi_out(a, st.tag);
+    const Geo &g = st.geo[0];
     const int a0 = g.a0, a1 = g.a1, nt = g.a1 - g.ts;
     if (a0 >= a1)
         return;
     Pos q = decode(g, step_at(g, 0));
     UnitGeo u = unit_geo(g, q.p);
-    int curp = q.p;
-    int pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
 #pragma unroll 1
     for (int kk = 0; kk < a1 - a0; ++kk) {
         const int i = step_at(g, kk);
         if (kk == nt && kk > 0)
             q = decode(g, a0);
-        if (q.p != curp) {
-            u = unit_geo(g, q.p);
-            curp = q.p;
-            pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
-        }
+        u = unit_geo(g, q.p);
         if (unit_ends(g, u, q, i)) {
-            if (st.uc % kEpiWarps == e && !*st.fail) {
-                const int rs = st.uc % kRedSlots;
-                const unsigned rph = static_cast<unsigned>(st.uc / kRedSlots);
-                if (!mbar_wait_bounded(&st.red_full[rs], rph & 1u)) {
-                    if (lane == 0) {
+            float4 tg, tu;
+            if (st.uc % kEpiWarps == e && take_red(a, st, tg, tu)) {
+                const int pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
+                const int ustart = i - q.c, uend = ustart + u.ch;
+                const int ncols = rv.pairs[q.p * kPairInts + 1];
+                constexpr int RB = ring_bits(BITS);
+                if (ustart >= a0 && uend <= a1) {
+                    if (BITS != 0 || pb == 4)
+                        finalize_gateup<RB>(eo, ncols, q.p, q.s, tg, tu);
+                    else
+                        finalize_gateup<2>(eo, ncols, q.p, q.s, tg, tu);
+                } else {
+                    const bool ok = (BITS != 0 || pb == 4)
+                                        ? fixup_gateup<RB>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu)
+                                        : fixup_gateup<2>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu);
+                    if (!ok && lane == 0) {
                         set_status(a.status, kStatusTimeout);
                         *st.fail = 1;
                     }
+                }
+            }
+            ++st.uc;
+        }
+        advance(u, q);
+    }
+}
+
+// The down phase of an epilogue warp: items of two strips of one step.
+template <int BITS>
+__device__ __forceinline__ void epi_down(const LayerArgs &a, const RouteView &rv, Stream &st)
+{
+    const int e = (threadIdx.x >> 5) - kStreamWarps;
+    const EpiOut eo = epi_out(a, st.tag);
+    const Geo &g = st.geo[1];
+    const int a0 = g.a0, n = g.a1 - g.a0;
+    if (n <= 0)
+        return;
+    Pos q = decode(g, a0);
+    UnitGeo u = unit_geo(g, q.p);
+#pragma unroll 1
+    for (int kk = 0; kk < n; ++kk) {
+        u = unit_geo(g, q.p);
+        const int ns = down_count(g, u, q), s0 = down_first(u, q);
+        for (int it = 0; 2 * it < ns; ++it) {
+            float4 v0, v1;
+            if (st.uc % kEpiWarps == e && take_red(a, st, v0, v1)) {
+                const int pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
+                const int ncols = rv.pairs[q.p * kPairInts + 1];
+                if (BITS != 0 || pb == 4) {
+                    finalize_down<ring_bits(BITS)>(eo, ncols, q.p, s0 + 2 * it, v0);
+                    if (2 * it + 1 < ns)
+                        finalize_down<ring_bits(BITS)>(eo, ncols, q.p, s0 + 2 * it + 1, v1);
                 } else {
-                    float4 tg = make_float4(0.f, 0.f, 0.f, 0.f), tu = tg;
-#pragma unroll 4
-                    for (int w2 = 0; w2 < kStreamWarps; ++w2) {
-                        const float4 *rr = st.red + ((rs * kStreamWarps + w2) * 2) * 32;
-                        const float4 vg = rr[lane];
-                        tg.x += vg.x, tg.y += vg.y, tg.z += vg.z, tg.w += vg.w;
-                        if (PHASE == 0) {
-                            const float4 vu = rr[32 + lane];
-                            tu.x += vu.x, tu.y += vu.y, tu.z += vu.z, tu.w += vu.w;
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&st.red_empty[rs]);
-                    const int ustart = i - q.c, uend = ustart + u.ch;
-                    const int ncols = rv.pairs[q.p * kPairInts + 1];
-                    constexpr int RB = ring_bits(BITS);
-                    if (ustart >= a0 && uend <= a1) {
-                        if (BITS != 0 || pb == 4)
-                            finalize_unit<RB, PHASE>(eo, ncols, q.p, q.s, tg, tu);
-                        else
-                            finalize_unit<2, PHASE>(eo, ncols, q.p, q.s, tg, tu);
-                        count_unit<PHASE>(eo, st.pspan, st.pcnt, st.ccnt, q.p, q.s);
-                    } else if (BITS != 0 || pb == 4) {
-                        fixup_unit<RB, PHASE>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
-                                              st.pspan, st.ccnt);
-                    } else {
-                        fixup_unit<2, PHASE>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu, st.pcnt,
-                                             st.pspan, st.ccnt);
-                    }
+                    finalize_down<2>(eo, ncols, q.p, s0 + 2 * it, v0);
+                    if (2 * it + 1 < ns)
+                        finalize_down<2>(eo, ncols, q.p, s0 + 2 * it + 1, v1);
                 }
             }
             ++st.uc;
@@ -1259,11 +1459,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     constexpr int NS = num_stages(ring_bits(BITS));
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ int s_ok;
     __shared__ int s_fail;
-    __shared__ unsigned s_pcnt[kMaxSpan];
-    __shared__ int s_pspan[2];
-    __shared__ unsigned s_ccnt[kMaxStripsD];
+    __shared__ uint32_t s_tag;
     Stream st;
     st.ring = smem;
     st.red = reinterpret_cast<float4 *>(smem + NS * stage_bytes(ring_bits(BITS)));
@@ -1271,9 +1468,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     st.empty = st.full + NS;
     st.red_full = st.empty + NS;
     st.red_empty = st.red_full + kRedSlots;
-    st.pcnt = s_pcnt;
-    st.pspan = s_pspan;
-    st.ccnt = s_ccnt;
     st.fail = &s_fail;
     st.seq = 0;
     st.uc = 0;
@@ -1289,118 +1483,92 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         fence_mbar_init();
         s_fail = 0;
     }
-    for (int j = threadIdx.x; j < kMaxStripsD; j += kThreads)
-        s_ccnt[j] = 0u;
     // Launched with programmatic stream serialization: the previous kernel on
-    // the stream may still be finishing.  Wait until it has completed and its
-    // writes are visible before any global access (the workspace, x), then
-    // let the next kernel's launch begin.
+    // the stream may still be finishing.  Only L2 prefetches of the router
+    // rows come before waiting for it; every load (the workspace, x, the
+    // rows) comes after it has completed and its writes are visible.  Then
+    // the next kernel's launch may begin.
+    if (a.do_route)
+        router_prefetch_l2(a);
     pdl_wait();
     pdl_launch_dependents();
+    RouterPre pre;
+    pre.nrows = 0;
+    if (a.do_route)
+        pre = router_load(a);
+    if (threadIdx.x == 0) {
+        const uint32_t tag = ld_relaxed_u32(a.seq) + 1u;
+        s_tag = tag;
+        st_word(a.started + blockIdx.x, tag_word(blockIdx.x, tag));
+    }
     cta_barrier();
-    bool ok = true;
+    const uint32_t tag = s_tag;
+    st.tag = tag;
 
     // ------------------------------------------------------------ phase R
     __shared__ RouteSmem rs;
     RouteView rv;
     int P_r = 0, P_t = 0;
     if (a.do_route) {
-        const int rows = a.E + (a.shared_gate ? 1 : 0);
-        const int units = rows + static_cast<int>(a.T);
-        // unit i runs on warp i / gridDim.x of CTA i % gridDim.x: one per SM first
-        const int64_t unit = (int64_t)warp * gridDim.x + blockIdx.x;
-        if (unit < units) {
-            router_unit<XBF16>(a, static_cast<int>(unit));
-            fence_acq_rel();
-            __syncwarp();
-            unsigned old = 0;
-            if (lane == 0)
-                old = atom_add_acqrel(a.route_ctr, 1u);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == static_cast<unsigned>(units - 1)) {
-                // the last router unit wakes every CTA through its own flag line
-                fence_acq_rel();
-                for (unsigned c = lane; c < gridDim.x; c += 32)
-                    st_relaxed(a.cta_flags + 32 * c, 1u);
-            }
-        }
-        // one poller per CTA, on the CTA's own flag; meanwhile other warps run
-        // the routing code once on scratch (in-bounds, results unused) so its
-        // instructions are fetched while the logits are still being made
-        cta_barrier();
-        if (warp == 0) {
-            const int good = warp_wait_geq(a.cta_flags + 32 * blockIdx.x, 1u, a.status) ? 1 : 0;
-            if (lane == 0) {
-                s_ok = good;
-                a.cta_flags[32 * blockIdx.x] = 0u;  // only this CTA reads it
-            }
-        } else if (warp <= (a.E + 31) / 32) {
-            route_chunk(rs.lg, rs.key, a.E, a.k, warp - 1, a.router_sigmoid, rs.warm_id, rs.warm_p);
-        }
-        cta_barrier();
-        ok = s_ok != 0;
-        // route: stage logits and keys, rank every expert, then warp t
-        // turns token t's selection into weights; the last warp builds the pairs
+        router_rows<XBF16>(a, pre, rs.red, tag);
+        // every CTA stages all logits (polled until tagged) and the keys
         const int T = static_cast<int>(a.T), E = a.E, kk = a.k, E4 = (a.E + 3) & ~3;
-        if (ok) {
-            for (int idx = threadIdx.x; idx < T * E; idx += kThreads) {
-                const int t = idx / E, e = idx - t * E;
-                float l = __ldcg(a.logits + (int64_t)t * a.Epad + e);
-                if (l != l) {
-                    set_status(a.status, kStatusBadArg);
-                    l = -INFINITY;
-                }
-                // selection key: the logit; with a bias, logit + bias
-                // (softmax) or fl32(sigmoid(logit)) + bias (sigmoid)
-                float key = a.expert_bias ? __fadd_rn(a.router_sigmoid ? sigmoid_fast(l) : l,
-                                                      __ldg(a.expert_bias + e))
-                                          : l;
-                if (key != key)
-                    key = -INFINITY;
-                // outside the routing mask: never selected, no softmax term
-                if (a.mask.on && !((a.mask.w[e >> 5] >> (e & 31)) & 1u)) {
-                    key = -INFINITY;
-                    l = -INFINITY;
-                }
-                rs.lg[t * E4 + e] = l;
-                rs.key[t * E4 + e] = key;
+        const int rows = E + (a.shared_gate ? 1 : 0);
+        const uint32_t want = tag + a.tag_stall;
+        for (int idx = threadIdx.x; idx < T * rows; idx += kThreads) {
+            const int t = idx / rows, e = idx - t * rows;
+            u64 v;
+            if (!poll_word(a.logit_t + (int64_t)t * a.Epad + e, want, a.wait_cycles, v)) {
+                set_status(a.status, kStatusTimeout);
+                s_fail = 1;
+                break;
             }
-        }
-        cta_barrier();
-        if (ok) {
-            const int nc = (E + 31) / 32;
-            for (int task = warp; task < T * nc; task += kWarps) {
-                const int t = task / nc, c = task - t * nc;
-                route_chunk(rs.lg + t * E4, rs.key + t * E4, E, kk, c, a.router_sigmoid,
-                            rs.ids + t * kk, rs.prob + t * kk);
+            float l = __uint_as_float(word_payload(v));
+            if (e == E) {  // the shared expert's gate
+                rs.shared_w[t] = sigmoid_fast(l);
+                continue;
             }
+            if (l != l) {
+                set_status(a.status, kStatusBadArg);
+                l = -INFINITY;
+            }
+            // selection key: the logit; with a bias, logit + bias (softmax)
+            // or fl32(sigmoid(logit)) + bias (sigmoid)
+            float key = a.expert_bias
+                            ? __fadd_rn(a.router_sigmoid ? sigmoid_fast(l) : l, __ldg(a.expert_bias + e))
+                            : l;
+            if (key != key)
+                key = -INFINITY;
+            // outside the routing mask: never selected, no softmax term
+            if (a.mask.on && !((a.mask.w[e >> 5] >> (e & 31)) & 1u)) {
+                key = -INFINITY;
+                l = -INFINITY;
+            }
+            rs.lg[t * E4 + e] = l;
+            rs.key[t * E4 + e] = key;
         }
+        if (!a.shared_gate && threadIdx.x < T)
+            rs.shared_w[threadIdx.x] = 1.0f;
         cta_barrier();
+        const bool ok = s_fail == 0;
         if (ok && warp < T) {
             const int t = warp;
-            float psel = 0.f;
-            for (int j = 0; j < kk; ++j)
-                psel += rs.prob[t * kk + j];
-            if (lane < kk) {
-                const float pj = rs.prob[t * kk + lane];
-                const float wv = (a.norm ? __fdividef(pj, psel) : pj) * a.rsf;
-                rs.weights[t * kk + lane] = wv;
-                if (blockIdx.x == 0) {
-                    const int id = rs.ids[t * kk + lane];
-                    a.ids[t * kk + lane] = id;
-                    a.weights[t * kk + lane] = wv;
-                    if (a.ids_out)
-                        a.ids_out[t * kk + lane] = id;
-                    if (a.w_out)
-                        a.w_out[t * kk + lane] = wv;
-                }
+            route_token(rs.lg + t * E4, rs.key + t * E4, E, kk, a.router_sigmoid, a.norm, a.rsf,
+                        rs.ids + t * kk, rs.weights + t * kk);
+            __syncwarp();
+            if (blockIdx.x == 0 && lane < kk) {
+                const int id = rs.ids[t * kk + lane];
+                const float wv = rs.weights[t * kk + lane];
+                a.ids[t * kk + lane] = id;
+                a.weights[t * kk + lane] = wv;
+                if (a.ids_out)
+                    a.ids_out[t * kk + lane] = id;
+                if (a.w_out)
+                    a.w_out[t * kk + lane] = wv;
             }
-            if (lane == 0)
-                rs.shared_w[t] =
-                    a.shared_gate ? sigmoid_fast(__ldcg(a.logits + (int64_t)t * a.Epad + a.E)) : 1.0f;
         }
-        // the pair table needs only the ids: built while the weights are
-        if (ok && warp == kWarps - 1)
+        cta_barrier();
+        if (ok && warp == 0)
             cta_dispatch(a, rs);
         cta_barrier();
         rv.pairs = &rs.pairs[0][0];
@@ -1419,15 +1587,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         P_r = __ldcg(a.meta + 0);
         P_t = __ldcg(a.meta + 1);
     }
-    if (!ok && threadIdx.x == 0)
-        s_fail = 1;
 
     // ------------------------------------------------------------ phases G, D
     __shared__ Geo s_geo[2];
     __shared__ Producer s_pr;
     if (lane == 0 && warp < 2) {
         Geo gg = make_geo(a, warp, P_r, P_t);
-        set_order(gg);
+        if (warp == 0)
+            set_order(gg);
         s_geo[warp] = gg;
     }
     cta_barrier();
@@ -1443,8 +1610,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     st.geo = s_geo;
     st.pr = &s_pr;
     if (warp < kStreamWarps) {
-        stream_phase<BITS, XBF16, KG, 0>(a, rv, st);
-        stream_phase<BITS, XBF16, KG, 1>(a, rv, st);
+        stream_gateup<BITS, XBF16, KG>(a, rv, st);
+        stream_down<BITS>(a, rv, st);
     } else if (warp == kProducerWarp) {
         if (lane == 0) {
             s_pr.phase = 0;
@@ -1455,117 +1622,83 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
         __syncwarp();
     } else {
-        if (warp == kStreamWarps) {
-            // the pairs of this CTA's gate/up range, for batched strip counts
-            if (lane == 0) {
-                s_pspan[0] = 0;
-                s_pspan[1] = 0;
-                if (s_geo[0].a0 < s_geo[0].a1) {
-                    const int pf = decode(s_geo[0], s_geo[0].a0).p, pl = decode(s_geo[0], s_geo[0].a1 - 1).p;
-                    if (pl - pf + 1 <= kMaxSpan) {
-                        s_pspan[0] = pf;
-                        s_pspan[1] = pl - pf + 1;
-                    }
-                }
-            }
-            for (int j = lane; j < kMaxSpan; j += 32)
-                s_pcnt[j] = 0u;
-        }
-        epi_barrier();
-        epi_phase<BITS, 0>(a, rv, st);
-        // publish this CTA's finished gate/up strips: the barrier orders the
-        // other epilogue warp's h stores before the release fence
-        epi_barrier();
-        if (warp == kStreamWarps && lane == 0 && !s_fail) {
-            bool any = false;
-            for (int j = 0; j < s_pspan[1]; ++j)
-                any |= s_pcnt[j] != 0u;
-            if (any) {
-                fence_acq_rel();
-                for (int j = 0; j < s_pspan[1]; ++j)
-                    if (s_pcnt[j])
-                        red_add_relaxed(a.pair_done + s_pspan[0] + j, s_pcnt[j]);
-            }
-        }
-        epi_phase<BITS, 1>(a, rv, st);
-        epi_barrier();
-        if (a.fused_combine && warp == kStreamWarps && lane == 0 && !s_fail) {
-            // publish the finished down units per output strip
-            const int ns = a.d / kTileRows;
-            bool any = false;
-            for (int j = 0; j < ns; ++j)
-                any |= s_ccnt[j] != 0u;
-            if (any) {
-                fence_acq_rel();
-                for (int j = 0; j < ns; ++j)
-                    if (s_ccnt[j])
-                        red_add_relaxed(a.comb_ctr + j, s_ccnt[j]);
-            }
-        }
+        epi_gateup<BITS>(a, rv, st);
+        epi_down<BITS>(a, rv, st);
     }
     cta_barrier();
 
     // ------------------------------------------------------------ combine
-    // (T <= 8) CTA c owns output strips c, c + grid, ...: once all P_t pairs
-    // have published their down unit of a strip, y rows = sum_j w_j o_j
-    // (+ shared) in rank order.
-    if (a.fused_combine) {
-        const int ns = a.d / kTileRows;
-        if (warp == 0 && !s_fail) {
-            for (int s = blockIdx.x; s < ns; s += gridDim.x)
-                if (!warp_wait_geq(a.comb_ctr + s, static_cast<unsigned>(P_t), a.status)) {
-                    if (lane == 0)
-                        s_fail = 1;
+    // (T <= 8) every thread of the grid takes outputs (t, row):
+    // y = sum_j w_j o_j (+ shared) in rank order, from the tagged outputs.
+    if (a.fused_combine && !s_fail) {
+        const int T = static_cast<int>(a.T), kk = a.k, d = a.d;
+        const bool has_sh = P_t > P_r;
+        const int nout = T * d;
+        for (int o = static_cast<int>(blockIdx.x) * kThreads + threadIdx.x; o < nout;
+             o += static_cast<int>(gridDim.x) * kThreads) {
+            const int t = o / d, row = o - t * d;
+            const int nj = kk + (has_sh ? 1 : 0);
+            u64 v[SMOE_MAX_TOPK_DEV + 1];
+            const long long t0 = clock64();
+            unsigned ns = 64;
+            bool good = true;
+            for (;;) {
+                bool all = true;
+#pragma unroll
+                for (int j = 0; j <= SMOE_MAX_TOPK_DEV; ++j) {
+                    if (j < nj) {
+                        const int rm = rv.route_map[t * (kk + 1) + j];
+                        v[j] = ld_word(a.o_t + (int64_t)rm * d + row);
+                        all = all && word_tag(v[j]) == tag;
+                    }
+                }
+                if (all)
+                    break;
+                if (clock64() - t0 > a.wait_cycles) {
+                    good = false;
                     break;
                 }
-        }
-        cta_barrier();
-        if (!s_fail) {
-            const int T = static_cast<int>(a.T), kk = a.k, d = a.d;
-            const bool has_sh = P_t > P_r;
-            for (int s = blockIdx.x; s < ns; s += gridDim.x) {
-                for (int i = threadIdx.x; i < kTileRows * T; i += kThreads) {
-                    const int t = i / kTileRows, row = 16 * s + i % kTileRows;
-                    float yv = 0.f;
-                    for (int j = 0; j < kk; ++j) {
-                        const int rm = rv.route_map[t * (kk + 1) + j];
-                        yv = fmaf(rv.weights[t * kk + j], __ldcg(a.o + (int64_t)rm * d + row), yv);
-                    }
-                    if (has_sh) {
-                        const int rm = rv.route_map[t * (kk + 1) + kk];
-                        yv = fmaf(rv.shared_w[t], __ldcg(a.o + (int64_t)rm * d + row), yv);
-                    }
-                    a.y[(int64_t)t * d + row] = yv;
-                }
-                if (threadIdx.x == 0)
-                    a.comb_ctr[s] = 0u;
+                __nanosleep(ns);
+                if (ns < 512)
+                    ns *= 2;
             }
+            if (!good) {
+                set_status(a.status, kStatusTimeout);
+                break;
+            }
+            float yv = 0.f;
+#pragma unroll
+            for (int j = 0; j < SMOE_MAX_TOPK_DEV; ++j)
+                if (j < kk)
+                    yv = fmaf(rv.weights[t * kk + j], __uint_as_float(word_payload(v[j])), yv);
+            if (has_sh)
+                yv = fmaf(rv.shared_w[t], __uint_as_float(word_payload(v[kk])), yv);
+            a.y[(int64_t)t * d + row] = yv;
         }
     }
 
     // ------------------------------------------------------------ exit
-    if (warp == 0) {
-        if (lane == 0) {
-            // every stage issued has been consumed unless a wait ran out;
-            // then wait (bounded) for the copies still in flight
-            const uint32_t n = s_pr.next;
-            for (uint32_t j = n > static_cast<uint32_t>(NS) ? n - NS : 0u; j < n; ++j)
-                (void)mbar_wait_bounded(&st.full[j % NS], (j / NS) & 1u);
+    if (warp == kProducerWarp && lane == 0) {
+        // every stage issued has been consumed unless a wait ran out; then
+        // wait (bounded) for the copies still in flight
+        const uint32_t n = s_pr.next;
+        for (uint32_t j = n > static_cast<uint32_t>(NS) ? n - NS : 0u; j < n; ++j)
+            (void)mbar_wait_bounded(&st.full[j % NS], (j / NS) & 1u);
+    }
+    if (blockIdx.x == 0 && warp == 0) {
+        // once every CTA has read the launch sequence number, leave this
+        // launch's tag for the next launch
+        bool all = true;
+        for (int c = lane; c < static_cast<int>(gridDim.x); c += 32) {
+            u64 v;
+            if (!poll_word(a.started + c, tag, a.wait_cycles, v))
+                all = false;
         }
-        // the last CTA out resets the per-launch counters
-        unsigned old = 0;
-        if (lane == 0)
-            old = atom_add_acqrel(a.exit_ctr, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == gridDim.x - 1) {
-            for (int p = lane; p < a.max_pairs; p += 32)
-                a.pair_done[p] = 0u;
-            if (lane == 0) {
-                *a.route_ctr = 0u;
-                fence_acq_rel();
-                *a.exit_ctr = 0u;
-            }
-        }
+        all = __all_sync(0xffffffffu, all);
+        if (all && lane == 0)
+            st_relaxed_u32(a.seq, tag);
+        if (!all && lane == 0)
+            set_status(a.status, kStatusTimeout);
     }
 }
 
@@ -1594,8 +1727,8 @@ cudaError_t launch_t(const LayerArgs &a, cudaStream_t stream)
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    // cooperative (every CTA resident: the phases hand off through global
-    // counters) and, where the runtime accepts it, programmatic stream
+    // cooperative (every CTA resident: the phases hand off through tagged
+    // words) and, where the runtime accepts it, programmatic stream
     // serialization so that the launch overlaps the previous kernel's tail
     static int pdl_refused[64] = {0};
     cudaLaunchAttribute attr[2];

@@ -36,6 +36,7 @@ EXPORTED = [
     "smoe_route_from_logits_ex", "smoe_moe_forward_ex",
     "smoe_repacked_bytes_mixed", "smoe_repack_mixed", "smoe_unpack_mixed",
     "smoe_moe_workspace_bytes_mixed", "smoe_moe_forward_mixed", "smoe_moe_forward_stage_mixed",
+    "smoe_debug_set_waits",
 ]
 
 # Execution paths (SMOE_PATH_* in include/smoe.h).
@@ -179,6 +180,8 @@ def load(path: str | None = None):
     L.smoe_moe_forward_stage_mixed.restype = I
     L.smoe_get_device_status.argtypes = [P]
     L.smoe_get_device_status.restype = I
+    L.smoe_debug_set_waits.argtypes = [ctypes.c_longlong, I]
+    L.smoe_debug_set_waits.restype = None
     _lib = L
     return L
 
@@ -497,6 +500,13 @@ def vault_repack_layer(meta: bytes, vault_dev: torch.Tensor, layer: int, num_exp
 
 def device_status(stream=None) -> int:
     return int(load().smoe_get_device_status(_stream(stream)))
+
+
+def debug_set_waits(poll_cycles: int = 0, stall_routing: bool = False):
+    """Testing only (smoe_debug_set_waits): short bounded waits in the layer
+    kernel and, with stall_routing, a routing step that waits for logits no
+    CTA writes; debug_set_waits() restores the defaults."""
+    load().smoe_debug_set_waits(int(poll_cycles), 1 if stall_routing else 0)
 
 
 def synth_bf16(out: torch.Tensor, key: int, sigma: float, p_out=0.0, out_mult=10.0, p_zero=0.0,
