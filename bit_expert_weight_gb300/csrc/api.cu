@@ -152,9 +152,11 @@ struct Plan {
 
 // Whether the forward takes the expert-sorted tensor-core path: a token
 // batch large enough that an average expert sees a dense block of rows.
-bool auto_grouped(const smoe_layer_desc *L, int64_t T)
+// bf16 tokens only: the tensor-core path rounds its operands to bf16, so
+// fp32 tokens always take the streaming path (fp32-accurate accumulation).
+bool auto_grouped(const smoe_layer_desc *L, int64_t T, smoe_dtype x_dtype)
 {
-    return T >= kGroupedMinT && T * L->top_k >= 16ll * L->num_experts;
+    return x_dtype == SMOE_BF16 && T >= kGroupedMinT && T * L->top_k >= 16ll * L->num_experts;
 }
 
 // mixed: a layer with per-expert depths, which always takes the grouped path.
@@ -199,7 +201,7 @@ Plan make_plan(const smoe_layer_desc *L, int64_t T, bool mixed = false)
     p.off_ctr_done = take(sizeof(unsigned));
     p.off_flags = take(sizeof(unsigned) * 4);
     p.off_started = take(8 * (size_t)p.ctas);
-    p.off_logit_t = take(small ? 8 * (size_t)T * p.Epad : 0);
+    p.off_logit_t = take(small ? 8 * (size_t)p.ctas * T * p.Epad : 0);
     p.off_h_t = take(8 * (size_t)p.max_pairs * kPairCols * p.fmax);
     p.off_part_t = take(8 * (size_t)p.ctas * 2 * 32 * 8);
     p.off_o_t = take(small ? 8 * (size_t)p.max_pairs * kPairCols * d : 0);
@@ -522,8 +524,11 @@ static smoe_status forward_stages(const smoe_layer_desc *layer, const smoe_route
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const smoe_layer_desc &L = *layer;
     int *status = device_status_word();
+    // the tensor-core path takes bf16 tokens only (it would round fp32 ones)
+    if (path == SMOE_PATH_GROUPED && x_dtype != SMOE_BF16)
+        return SMOE_ERR_UNSUPPORTED;
     const bool grouped = path == SMOE_PATH_GROUPED ||
-                         (path == SMOE_PATH_AUTO && auto_grouped(layer, num_tokens));
+                         (path == SMOE_PATH_AUTO && auto_grouped(layer, num_tokens, x_dtype));
     if (grouped && !P.grouped)
         return SMOE_ERR_UNSUPPORTED;
     // T <= 8 with all stages: one fused launch (routing inside the kernel)
@@ -713,9 +718,14 @@ smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, s
 
 int smoe_moe_path(const smoe_layer_desc *layer, int64_t num_tokens)
 {
-    if (!valid_layer(layer) || num_tokens < 0)
+    return smoe_moe_path_dtype(layer, num_tokens, SMOE_BF16);
+}
+
+int smoe_moe_path_dtype(const smoe_layer_desc *layer, int64_t num_tokens, smoe_dtype x_dtype)
+{
+    if (!valid_layer(layer) || num_tokens < 0 || (x_dtype != SMOE_F32 && x_dtype != SMOE_BF16))
         return -1;
-    return auto_grouped(layer, num_tokens) ? SMOE_PATH_GROUPED : SMOE_PATH_STREAM;
+    return auto_grouped(layer, num_tokens, x_dtype) ? SMOE_PATH_GROUPED : SMOE_PATH_STREAM;
 }
 
 smoe_status smoe_moe_forward_stage(const smoe_layer_desc *layer, const void *x,

@@ -133,7 +133,7 @@ struct LayerArgs {
     // launch is *seq + 1; the kernel leaves it in *seq for the next launch.
     unsigned *seq;                 // [1], first word of the workspace
     unsigned long long *started;   // [CTAs] each CTA's start mark
-    unsigned long long *logit_t;   // [T][Epad] logits (routing inside the kernel)
+    unsigned long long *logit_t;   // [CTAs][T][Epad] logits, one copy per CTA (routing inside)
     unsigned long long *h_t;       // [max_pairs][8][fmax] h: bf16 hi | bf16 lo << 16
     unsigned long long *part_t;    // [CTAs][2 slots][32 lanes][8] split gate/up unit sums
     unsigned long long *o_t;       // [max_pairs][8][d] down outputs (combine inside)

@@ -230,9 +230,10 @@ __device__ __forceinline__ float dot8_bf16(uint4 w, const float (&x)[8])
 }
 
 // The CTA's router rows for all tokens: per-thread 8-column dot products,
-// a shuffle tree per warp, then the warps' sums in warp order; the logits
-// are stored tagged.  red: shared scratch of kWarps x 16 floats.  Every
-// thread of the CTA calls it.
+// a shuffle tree per warp, then the warps' sums in warp order; each logit is
+// stored tagged into every CTA's own copy of the logits (so that each CTA
+// polls lines no other CTA polls).  red: shared scratch of kWarps x 16
+// floats plus 16 logits.  Every thread of the CTA calls it.
 template <bool XBF16>
 __device__ __forceinline__ void router_rows(const LayerArgs &a, const RouterPre &pre, float *red,
                                             uint32_t tag)
@@ -279,13 +280,20 @@ __device__ __forceinline__ void router_rows(const LayerArgs &a, const RouterPre 
             }
     }
     cta_barrier();
+    float *lg = red + kWarps * 16;
     if (i < pre.nrows * T) {
         const int r = i / T, t = i - r * T;
         float v = 0.f;
         for (int w = 0; w < nw; ++w)
             v += red[w * 16 + r * kPairCols + t];
-        const int row = static_cast<int>(blockIdx.x) + r * static_cast<int>(gridDim.x);
-        st_word(a.logit_t + (int64_t)t * a.Epad + row, tag_word(__float_as_uint(v), tag));
+        lg[i] = v;
+    }
+    cta_barrier();
+    const int C = static_cast<int>(gridDim.x), n = pre.nrows * T;
+    for (int j = i; j < n * C; j += kThreads) {
+        const int c = j / n, q = j - c * n, r = q / T, t = q - r * T;
+        const int row = static_cast<int>(blockIdx.x) + r * C;
+        st_word(a.logit_t + ((int64_t)c * T + t) * a.Epad + row, tag_word(__float_as_uint(lg[q]), tag));
     }
 }
 
@@ -299,9 +307,10 @@ constexpr int kFusedPairs = kPairCols * SMOE_MAX_TOPK_DEV + 1;
 struct __align__(16) RouteSmem {
     float lg[kPairCols * kMaxExperts];   // [T][E4] logits, row stride E4 = E rounded up to 4
     float key[kPairCols * kMaxExperts];  // [T][E4] selection keys
-    float red[kWarps * 16];              // router row partial sums
+    float red[kWarps * 16 + 16];         // router row partial sums, then the CTA's logits
     int32_t pairs[kFusedPairs][kPairInts];
     int32_t route_map[kPairCols * (SMOE_MAX_TOPK_DEV + 1)];
+    float score[kPairCols * SMOE_MAX_TOPK_DEV];  // [T][k] the rank-j expert's score
     float weights[kPairCols * SMOE_MAX_TOPK_DEV];
     float shared_w[kPairCols];
     int16_t ids[kPairCols * SMOE_MAX_TOPK_DEV];
@@ -315,53 +324,20 @@ struct RouteView {
     const float *shared_w;     // [T]
 };
 
-// One token's routing in one warp, from its logits and selection keys in
-// shared memory: k rounds of a warp arg-max over the keys in the order
-// (key descending, index ascending) -- ties go to the lower index -- then
-// the scores of the selected experts (softmax over all E logits, or the
-// expert's own sigmoid) and the weights (renormalised over the selection if
-// norm, times the routed scaling factor), in rank order.  Lane L holds
-// experts L, L + 32, ... .  The softmax maximum and sum run over all E
-// logits in a fixed order (lane-strided, then a shuffle tree); exp and
-// divide are the hardware approximations (a few ulp), well inside the
-// weights' tolerance.
-__device__ __noinline__ void route_token(const float *lg, const float *key, int E, int k, int sigm,
-                                         int norm, float rsf, int16_t *ids, float *w)
+// Routing of one token, experts 32 c .. 32 c + 31, in one warp (task (t, c)
+// of the CTA's T x ceil(E/32) routing tasks): lane L takes expert
+// e = 32 c + L, whose rank is the number of experts before it in the order
+// (key descending, index ascending) -- ties go to the lower index; ranks
+// below k are the selection, stored at their rank with the expert's score:
+// the softmax over all E logits, or (sigm) the expert's own sigmoid.  The
+// softmax maximum and sum run over all E logits in a fixed order
+// (lane-strided, then a shuffle tree), the same in every task of the token;
+// exp and divide are the hardware approximations (a few ulp), well inside
+// the weights' tolerance.  key rows are 16-byte aligned.
+__device__ __noinline__ void route_chunk(const float *lg, const float *key, int E, int k, int c, int sigm,
+                                         int16_t *ids, float *score)
 {
     const int lane = threadIdx.x & 31;
-    float kv[kMaxExperts / 32];
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = lane + 32 * i;
-        kv[i] = e < E ? key[e] : -INFINITY;
-    }
-    unsigned taken = 0u;
-    int sel = 0;  // lane j < k: the rank-j expert
-    for (int r = 0; r < k; ++r) {
-        float bk = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && (kv[i] > bk || (kv[i] == bk && e < bi))) {
-                bk = kv[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ok > bk || (ok == bk && oi < bi)) {
-                bk = ok;
-                bi = oi;
-            }
-        }
-        if (bi < E && lane == (bi & 31))
-            taken |= 1u << (bi >> 5);
-        if (lane == r)
-            sel = bi;
-    }
     float m = -INFINITY, z = 1.f;
     if (!sigm) {
         for (int i = lane; i < E; i += 32)
@@ -374,16 +350,28 @@ __device__ __noinline__ void route_token(const float *lg, const float *key, int 
         for (int o = 16; o; o >>= 1)
             z += __shfl_xor_sync(0xffffffffu, z, o);
     }
-    float p = 0.f;
-    if (lane < k)
-        p = sigm ? sigmoid_fast(lg[sel]) : __fdividef(__expf(lg[sel] - m), z);  // z in [1, E]
-    // sum of the selected scores in rank order (the same order as the oracle)
-    float psel = 0.f;
-    for (int j = 0; j < k; ++j)
-        psel += __shfl_sync(0xffffffffu, p, j);
-    if (lane < k) {
-        ids[lane] = static_cast<int16_t>(sel);
-        w[lane] = (norm ? __fdividef(p, psel) : p) * rsf;
+    const int e = 32 * c + lane;
+    if (e >= E)
+        return;
+    const float ke = key[e];
+    int r = 0;
+    const float4 *k4 = reinterpret_cast<const float4 *>(key);
+#pragma unroll 4
+    for (int j = 0; j < E / 4; ++j) {
+        const float4 v = k4[j];
+        const int e0 = 4 * j;
+        r += (v.x > ke || (v.x == ke && e0 < e)) ? 1 : 0;
+        r += (v.y > ke || (v.y == ke && e0 + 1 < e)) ? 1 : 0;
+        r += (v.z > ke || (v.z == ke && e0 + 2 < e)) ? 1 : 0;
+        r += (v.w > ke || (v.w == ke && e0 + 3 < e)) ? 1 : 0;
+    }
+    for (int e2 = E & ~3; e2 < E; ++e2) {
+        const float v = key[e2];
+        r += (v > ke || (v == ke && e2 < e)) ? 1 : 0;
+    }
+    if (r < k) {
+        ids[r] = static_cast<int16_t>(e);
+        score[r] = sigm ? sigmoid_fast(lg[e]) : __fdividef(__expf(lg[e] - m), z);  // z in [1, E]
     }
 }
 
@@ -716,19 +704,25 @@ __device__ __forceinline__ int produce(const LayerArgs &a, const RouteView &rv, 
     return 1;
 }
 
-// The lane's view of a pair record: column count and the token of its row
-// of the B fragment (column gq).
+// The lane's view of a pair record: column count, the pair column whose
+// activations this lane's row of the B fragment holds, and its token.  The
+// B fragment's column n is lane >> 2; with packed columns (pairs of at most
+// 4 tokens) columns 2c and 2c + 1 carry the bf16 hi and lo parts of pair
+// column c, so that one mma takes both parts and the two output columns are
+// added afterwards.
 struct PairInfo {
-    int ncols, tok;
+    int ncols, col, tok;
 };
 
+template <bool PACK>
 __device__ __forceinline__ PairInfo read_pair(const RouteView &rv, int p)
 {
-    const int lane = threadIdx.x & 31, gq = lane >> 2;
+    const int lane = threadIdx.x & 31;
     const int32_t *pr = rv.pairs + p * kPairInts;
     PairInfo pi;
     pi.ncols = pr[1];
-    pi.tok = gq < pi.ncols ? pr[2 + gq] : 0;
+    pi.col = PACK ? lane >> 3 : lane >> 2;
+    pi.tok = pi.col < pi.ncols ? pr[2 + pi.col] : 0;
     return pi;
 }
 
@@ -780,16 +774,18 @@ __device__ __forceinline__ void bias_from_sums(BFrag &f, float s0, float s1)
 }
 
 // Gate/up B operand of group gi: the lane's 16 activations of its token
-// (pair column gq) at columns 64 gi + 16 tig .. +15 (bf16 x: 2 vectors, fp32
-// x: 4, split into bf16 hi + lo), and the column biases.  on = the group
-// exists (warp-uniform); an absent group or column gives zeros.  Every lane
-// of the warp calls it.
-template <int BITS, bool XBF16>
+// (pair column pi.col) at columns 64 gi + 16 tig .. +15 (bf16 x: 2 vectors,
+// fp32 x: 4, split into bf16 hi + lo -- both parts in b*/b*l, or with PACK
+// the part of B column lane >> 2: hi for even, lo for odd), and the column
+// biases.  on = the group exists (warp-uniform); an absent group or column
+// gives zeros.  Every lane of the warp calls it.
+template <int BITS, bool XBF16, bool PACK>
 __device__ __forceinline__ void load_b_x(const LayerArgs &a, const PairInfo &pi, int gi, bool on,
                                          BFrag &f)
 {
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
-    const bool valid = on && gq < pi.ncols;
+    const int lane = threadIdx.x & 31, tig = lane & 3;
+    const bool valid = on && pi.col < pi.ncols;
+    const bool lo_part = ((lane >> 2) & 1) != 0;
     float s0 = 0.f, s1 = 0.f;
     if (XBF16) {
         const uint4 *row = reinterpret_cast<const uint4 *>(
@@ -814,24 +810,36 @@ __device__ __forceinline__ void load_b_x(const LayerArgs &a, const PairInfo &pi,
             const float4 v = valid ? __ldg(row + j) : z;
             split_bf16x2(v.x, v.y, f.b0[j], f.b0l[j]);
             split_bf16x2(v.z, v.w, f.b1[j], f.b1l[j]);
-            s0 += v.x + v.y;
-            s1 += v.z + v.w;
+            if (PACK) {
+                if (lo_part) {
+                    f.b0[j] = f.b0l[j];
+                    f.b1[j] = f.b1l[j];
+                }
+                f.b0l[j] = f.b1l[j] = 0u;
+                s0 += bf16lo_to_f32(f.b0[j]) + bf16hi_to_f32(f.b0[j]);
+                s1 += bf16lo_to_f32(f.b1[j]) + bf16hi_to_f32(f.b1[j]);
+            } else {
+                s0 += v.x + v.y;
+                s1 += v.z + v.w;
+            }
         }
     }
     bias_from_sums<BITS>(f, s0, s1);
 }
 
-// Down B operand of group gi of pair p: the lane's 16 h values of its
+// Down B operand of group gi of pair p: the lane's 16 h values of its pair
 // column (rows 64 gi + 16 tig .. +15), polled until every word carries the
-// launch's tag, split into the bf16 hi and lo fragments, and the column
-// biases.  False if the bounded poll ran out.  Every lane calls it.
-template <int BITS>
+// launch's tag, as the bf16 hi and lo fragments (or with PACK the part of B
+// column lane >> 2), and the column biases.  False if the bounded poll ran
+// out.  Every lane calls it.
+template <int BITS, bool PACK>
 __device__ __forceinline__ bool load_b_h(const LayerArgs &a, const PairInfo &pi, int p, int gi, bool on,
                                          int fmax, uint32_t tag, BFrag &f)
 {
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
-    const bool valid = on && gq < pi.ncols;
-    const u64 *src = a.h_t + ((int64_t)p * kPairCols + gq) * fmax + gi * kGroup + 16 * tig;
+    const int lane = threadIdx.x & 31, tig = lane & 3;
+    const bool valid = on && pi.col < pi.ncols;
+    const bool lo_part = ((lane >> 2) & 1) != 0;
+    const u64 *src = a.h_t + ((int64_t)p * kPairCols + pi.col) * fmax + gi * kGroup + 16 * tig;
     u64 w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
@@ -875,8 +883,18 @@ __device__ __forceinline__ bool load_b_h(const LayerArgs &a, const PairInfo &pi,
         f.b0l[j] = __byte_perm(w0, w1, 0x7632);
         f.b1[j] = __byte_perm(w2, w3, 0x5410);
         f.b1l[j] = __byte_perm(w2, w3, 0x7632);
-        s0 += (bf16lo_to_f32(w0) + bf16hi_to_f32(w0)) + (bf16lo_to_f32(w1) + bf16hi_to_f32(w1));
-        s1 += (bf16lo_to_f32(w2) + bf16hi_to_f32(w2)) + (bf16lo_to_f32(w3) + bf16hi_to_f32(w3));
+        if (PACK) {
+            if (lo_part) {
+                f.b0[j] = f.b0l[j];
+                f.b1[j] = f.b1l[j];
+            }
+            f.b0l[j] = f.b1l[j] = 0u;
+            s0 += bf16lo_to_f32(f.b0[j]) + bf16hi_to_f32(f.b0[j]);
+            s1 += bf16lo_to_f32(f.b1[j]) + bf16hi_to_f32(f.b1[j]);
+        } else {
+            s0 += (bf16lo_to_f32(w0) + bf16hi_to_f32(w0)) + (bf16lo_to_f32(w1) + bf16hi_to_f32(w1));
+            s1 += (bf16lo_to_f32(w2) + bf16hi_to_f32(w2)) + (bf16lo_to_f32(w3) + bf16hi_to_f32(w3));
+        }
     }
     bias_from_sums<BITS>(f, s0, s1);
     return ok;
@@ -953,21 +971,38 @@ struct EpiOut {
     int *status;
 };
 
+// Accumulator element e of the lane (rows gq, gq + 8; B columns 2 tig,
+// 2 tig + 1) as a value of pair column col: unpacked, element e itself;
+// packed, the hi + lo columns of pair column tig added (elements 0 + 1 for
+// row gq, 2 + 3 for row gq + 8; valid for e even).
+template <bool PACK>
+__device__ __forceinline__ float acc_col(const float (&v)[4], int e, int &col)
+{
+    const int tig = threadIdx.x & 3;
+    if (PACK) {
+        col = (e & 1) ? kPairCols : tig;  // odd elements are the lo parts: no output of their own
+        return v[e & 2] + v[(e & 2) + 1];
+    }
+    col = 2 * tig + (e & 1);
+    return v[e];
+}
+
 // Finalise gate/up strip s of pair p from its full-K sums (one warp, cold
 // path): h = SiLU(g) * u as bf16 hi + lo, stored tagged.
-template <int BITS>
+template <int BITS, bool PACK>
 __device__ __noinline__ void finalize_gateup(const EpiOut a, int ncols, int p, int s, float4 ag, float4 au)
 {
     constexpr float L = BITS == 4 ? 7.5f : 1.5f;
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const int lane = threadIdx.x & 31, gq = lane >> 2;
     const float invL = 1.0f / L;
     const float gv[4] = {ag.x, ag.y, ag.z, ag.w}, uv[4] = {au.x, au.y, au.z, au.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const int col = 2 * tig + (e & 1);
+        int col;
+        const float gsum = acc_col<PACK>(gv, e, col), usum = acc_col<PACK>(uv, e, col);
         const int row = 16 * s + gq + 8 * (e >> 1);
         if (col < ncols) {
-            const float g = gv[e] * invL, u = uv[e] * invL;
+            const float g = gsum * invL, u = usum * invL;
             const float hv = __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f))) * u;  // SiLU(g) * u
             const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
             const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
@@ -980,20 +1015,21 @@ __device__ __noinline__ void finalize_gateup(const EpiOut a, int ncols, int p, i
 
 // Finalise down strip s of pair p: o rows, tagged for the in-kernel
 // combine or plain for the combine kernel.
-template <int BITS>
+template <int BITS, bool PACK>
 __device__ __forceinline__ void finalize_down(const EpiOut &a, int ncols, int p, int s, float4 ag)
 {
     constexpr float L = BITS == 4 ? 7.5f : 1.5f;
-    const int lane = threadIdx.x & 31, gq = lane >> 2, tig = lane & 3;
+    const int lane = threadIdx.x & 31, gq = lane >> 2;
     const float invL = 1.0f / L;
     const float gv[4] = {ag.x, ag.y, ag.z, ag.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const int col = 2 * tig + (e & 1);
+        int col;
+        const float sum = acc_col<PACK>(gv, e, col);
         const int row = 16 * s + gq + 8 * (e >> 1);
         if (col < ncols) {
             const int64_t off = ((int64_t)p * kPairCols + col) * a.d + row;
-            const float ov = gv[e] * invL;
+            const float ov = sum * invL;
             if (a.fused)
                 st_word(a.o_t + off, tag_word(__float_as_uint(ov), a.tag));
             else
@@ -1008,7 +1044,7 @@ __device__ __forceinline__ void finalize_down(const EpiOut &a, int ncols, int p,
 // step stores its sums tagged and is done; the one that does (the last
 // contributor) polls the others' sums, adds them all in CTA order and
 // finalises.  False if a bounded poll ran out.
-template <int BITS>
+template <int BITS, bool PACK>
 __device__ __noinline__ bool fixup_gateup(const EpiOut a, int ncols, const Geo &g, int p, int s, int ustart,
                                           int uend, float4 tg, float4 tu)
 {
@@ -1063,7 +1099,7 @@ __device__ __noinline__ bool fixup_gateup(const EpiOut a, int ncols, const Geo &
     }
     if (!ok)
         return false;
-    finalize_gateup<BITS>(a, ncols, p, s, sg, su);
+    finalize_gateup<BITS, PACK>(a, ncols, p, s, sg, su);
     return true;
 }
 
@@ -1128,11 +1164,14 @@ __device__ __forceinline__ void put_red(const LayerArgs &a, Stream &st, float4 v
 // of its groups of the current pair: groups c * gc + w and c * gc + w + 16
 // of each chunk c (at most KG chunks).  At a unit's end it hands its sums to
 // the epilogue warps.
-template <int BITS, bool XBF16, int KG>
+template <int BITS, bool XBF16, int KG, bool PACK>
 __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
     constexpr int NS = num_stages(ring_bits(BITS)), SB = stage_bytes(ring_bits(BITS));
-    constexpr bool kSplit = !XBF16;
+    // fp32 tokens enter as bf16 hi + lo: two mmas per k-subtile, or with
+    // packed columns (<= 4 tokens) one mma whose column pairs are added later
+    constexpr bool PG = PACK && !XBF16;
+    constexpr bool kSplit = !XBF16 && !PG;
     constexpr int NB = 2 * KG;  // B fragments held
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geo &g = st.geo[0];
@@ -1143,6 +1182,7 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
     UnitGeo u = unit_geo(g, q.p);
     int loaded = -1;
     int pb = ring_bits(BITS);  // depth of the loaded pair
+    int ltok = -1, lncols = -1, lpb = -1;  // the token column and depth the fragments hold
     BFrag bf[NB];
     float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
     float accg2[4] = {0.f, 0.f, 0.f, 0.f}, accu2[4] = {0.f, 0.f, 0.f, 0.f};  // second group
@@ -1153,17 +1193,25 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
             q = decode(g, a0);
         if (q.p != loaded) {
             u = unit_geo(g, q.p);
-            const PairInfo pi = read_pair(rv, q.p);
+            const PairInfo pi = read_pair<PG>(rv, q.p);
             pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
+            // every pair's gate/up has K = d, so the fragments depend only on
+            // the tokens and the depth: reloaded only when those change
+            const bool same = __all_sync(0xffffffffu, pi.tok == ltok && pi.ncols == lncols && pb == lpb);
+            if (!same) {
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const int c = b >> 1, lg = warp + (b & 1) * kStreamWarps;  // chunk, group in chunk
-                const int gi = c * u.gc + lg;
-                const bool on = c < u.ch && lg < u.gc && gi < u.gk;
-                if (BITS != 0 || pb == 4)
-                    load_b_x<ring_bits(BITS), XBF16>(a, pi, gi, on, bf[b]);
-                else
-                    load_b_x<2, XBF16>(a, pi, gi, on, bf[b]);
+                for (int b = 0; b < NB; ++b) {
+                    const int c = b >> 1, lg = warp + (b & 1) * kStreamWarps;  // chunk, group in chunk
+                    const int gi = c * u.gc + lg;
+                    const bool on = c < u.ch && lg < u.gc && gi < u.gk;
+                    if (BITS != 0 || pb == 4)
+                        load_b_x<ring_bits(BITS), XBF16, PG>(a, pi, gi, on, bf[b]);
+                    else
+                        load_b_x<2, XBF16, PG>(a, pi, gi, on, bf[b]);
+                }
+                ltok = pi.tok;
+                lncols = pi.ncols;
+                lpb = pb;
             }
             loaded = q.p;
         }
@@ -1173,6 +1221,8 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
             // branch-free over the warp's two groups (tiles of absent groups
             // read in-bounds stage bytes and are dropped), so the four mma
             // chains of the step schedule together
+            // the warp's two groups of the chunk; a group past the chunk's
+            // end is skipped (the branch is uniform over the warp)
             const uint8_t *stage = st.ring + slot * SB;
             const int ng = min(u.gc, u.gk - q.c * u.gc);  // groups in this chunk
             const bool g0 = warp < ng, g1 = warp + kStreamWarps < ng;
@@ -1181,18 +1231,28 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
                 if (c == q.c) {
                     if (BITS != 0 || pb == 4) {
                         constexpr int B = ring_bits(BITS), TB = tile_bytes(B);
-                        mac_tile<B, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, g0);
-                        mac_tile<B, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, g0);
-                        mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2, g1);
-                        mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1], accu2,
-                                            g1);
+                        if (g0) {
+                            mac_tile<B, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, true);
+                            mac_tile<B, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, true);
+                        }
+                        if (g1) {
+                            mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2,
+                                                true);
+                            mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1],
+                                                accu2, true);
+                        }
                     } else {
                         constexpr int TB = tile_bytes(2);
-                        mac_tile<2, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, g0);
-                        mac_tile<2, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, g0);
-                        mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2, g1);
-                        mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1], accu2,
-                                            g1);
+                        if (g0) {
+                            mac_tile<2, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, true);
+                            mac_tile<2, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, true);
+                        }
+                        if (g1) {
+                            mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2,
+                                                true);
+                            mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1],
+                                                accu2, true);
+                        }
                     }
                 }
             }
@@ -1222,7 +1282,7 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
 // strips of one pair; the warp's groups w and w + 16 of each strip use the
 // same two B fragments (h of the pair, polled when the warp reaches the
 // pair).  Items of two strips go to the epilogue warps.
-template <int BITS>
+template <int BITS, bool PACK>
 __device__ __forceinline__ void stream_down(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
     constexpr int NS = num_stages(ring_bits(BITS)), SB = stage_bytes(ring_bits(BITS));
@@ -1245,7 +1305,7 @@ __device__ __forceinline__ void stream_down(const LayerArgs &a, const RouteView 
     for (int kk = 0; kk < n; ++kk) {
         if (q.p != loaded) {
             u = unit_geo(g, q.p);
-            const PairInfo pi = read_pair(rv, q.p);
+            const PairInfo pi = read_pair<PACK>(rv, q.p);
             pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
             bool okb = true;
 #pragma unroll
@@ -1253,9 +1313,9 @@ __device__ __forceinline__ void stream_down(const LayerArgs &a, const RouteView 
                 const int gi = warp + b * kStreamWarps;
                 const bool on = gi < u.gk && !*st.fail;
                 if (BITS != 0 || pb == 4)
-                    okb = load_b_h<ring_bits(BITS)>(a, pi, q.p, gi, on, fmax, st.tag, bf[b]) && okb;
+                    okb = load_b_h<ring_bits(BITS), PACK>(a, pi, q.p, gi, on, fmax, st.tag, bf[b]) && okb;
                 else
-                    okb = load_b_h<2>(a, pi, q.p, gi, on, fmax, st.tag, bf[b]) && okb;
+                    okb = load_b_h<2, PACK>(a, pi, q.p, gi, on, fmax, st.tag, bf[b]) && okb;
             }
             if (!okb && lane == 0) {
                 set_status(a.status, kStatusTimeout);
@@ -1267,21 +1327,28 @@ __device__ __forceinline__ void stream_down(const LayerArgs &a, const RouteView 
         const bool ok = wait_stage<NS>(a, st, slot);
         const int ns = down_count(g, u, q);
         if (ok) {
+            // the warp's groups w and w + 16 of each strip of the step; tiles
+            // past the strips' groups or the step's strips are skipped (the
+            // branches are uniform over the warp)
             const uint8_t *stage = st.ring + slot * SB;
             const bool g0 = warp < u.gk, g1 = warp + kStreamWarps < u.gk;
 #pragma unroll
             for (int j = 0; j < kMaxDownStrips; ++j) {
-                const bool on0 = g0 && j < ns, on1 = g1 && j < ns;
-                // an absent tile reads tile 0 of the stage (in bounds) and is dropped
-                const int t0 = on0 ? j * u.gk + warp : 0, t1 = on1 ? j * u.gk + warp + kStreamWarps : 0;
-                if (BITS != 0 || pb == 4) {
-                    constexpr int B = ring_bits(BITS), TB = tile_bytes(B);
-                    mac_tile<B, true>(stage + t0 * TB, bf[0], acc[j], on0);
-                    mac_tile<B, true>(stage + t1 * TB, bf[1], acc[j], on1);
-                } else {
-                    constexpr int TB = tile_bytes(2);
-                    mac_tile<2, true>(stage + t0 * TB, bf[0], acc[j], on0);
-                    mac_tile<2, true>(stage + t1 * TB, bf[1], acc[j], on1);
+                if (j < ns) {
+                    const int t0 = j * u.gk + warp, t1 = t0 + kStreamWarps;
+                    if (BITS != 0 || pb == 4) {
+                        constexpr int B = ring_bits(BITS), TB = tile_bytes(B);
+                        if (g0)
+                            mac_tile<B, !PACK>(stage + t0 * TB, bf[0], acc[j], true);
+                        if (g1)
+                            mac_tile<B, !PACK>(stage + t1 * TB, bf[1], acc[j], true);
+                    } else {
+                        constexpr int TB = tile_bytes(2);
+                        if (g0)
+                            mac_tile<2, !PACK>(stage + t0 * TB, bf[0], acc[j], true);
+                        if (g1)
+                            mac_tile<2, !PACK>(stage + t1 * TB, bf[1], acc[j], true);
+                    }
                 }
             }
         }
@@ -1371,7 +1438,7 @@ __device__ __forceinline__ EpiOut epi_out(const LayerArgs &a, uint32_t tag)
 // steps; at each unit end it owns (items alternate between the epilogue
 // warps) it sums the warps' partials and finalises the unit, or joins a
 // unit shared with other CTAs.
-template <int BITS>
+template <int BITS, bool PACK>
 __device__ __forceinline__ void epi_gateup(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
     const int e = (threadIdx.x >> 5) - kStreamWarps, lane = threadIdx.x & 31;
@@ -1397,13 +1464,13 @@ __device__ __forceinline__ void epi_gateup(const LayerArgs &a, const RouteView &
                 constexpr int RB = ring_bits(BITS);
                 if (ustart >= a0 && uend <= a1) {
                     if (BITS != 0 || pb == 4)
-                        finalize_gateup<RB>(eo, ncols, q.p, q.s, tg, tu);
+                        finalize_gateup<RB, PACK>(eo, ncols, q.p, q.s, tg, tu);
                     else
-                        finalize_gateup<2>(eo, ncols, q.p, q.s, tg, tu);
+                        finalize_gateup<2, PACK>(eo, ncols, q.p, q.s, tg, tu);
                 } else {
                     const bool ok = (BITS != 0 || pb == 4)
-                                        ? fixup_gateup<RB>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu)
-                                        : fixup_gateup<2>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu);
+                                        ? fixup_gateup<RB, PACK>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu)
+                                        : fixup_gateup<2, PACK>(eo, ncols, g, q.p, q.s, ustart, uend, tg, tu);
                     if (!ok && lane == 0) {
                         set_status(a.status, kStatusTimeout);
                         *st.fail = 1;
@@ -1417,7 +1484,7 @@ __device__ __forceinline__ void epi_gateup(const LayerArgs &a, const RouteView &
 }
 
 // The down phase of an epilogue warp: items of two strips of one step.
-template <int BITS>
+template <int BITS, bool PACK>
 __device__ __forceinline__ void epi_down(const LayerArgs &a, const RouteView &rv, Stream &st)
 {
     const int e = (threadIdx.x >> 5) - kStreamWarps;
@@ -1438,13 +1505,13 @@ __device__ __forceinline__ void epi_down(const LayerArgs &a, const RouteView &rv
                 const int pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
                 const int ncols = rv.pairs[q.p * kPairInts + 1];
                 if (BITS != 0 || pb == 4) {
-                    finalize_down<ring_bits(BITS)>(eo, ncols, q.p, s0 + 2 * it, v0);
+                    finalize_down<ring_bits(BITS), PACK>(eo, ncols, q.p, s0 + 2 * it, v0);
                     if (2 * it + 1 < ns)
-                        finalize_down<ring_bits(BITS)>(eo, ncols, q.p, s0 + 2 * it + 1, v1);
+                        finalize_down<ring_bits(BITS), PACK>(eo, ncols, q.p, s0 + 2 * it + 1, v1);
                 } else {
-                    finalize_down<2>(eo, ncols, q.p, s0 + 2 * it, v0);
+                    finalize_down<2, PACK>(eo, ncols, q.p, s0 + 2 * it, v0);
                     if (2 * it + 1 < ns)
-                        finalize_down<2>(eo, ncols, q.p, s0 + 2 * it + 1, v1);
+                        finalize_down<2, PACK>(eo, ncols, q.p, s0 + 2 * it + 1, v1);
                 }
             }
             ++st.uc;
@@ -1453,7 +1520,9 @@ __device__ __forceinline__ void epi_down(const LayerArgs &a, const RouteView &rv
     }
 }
 
-template <int BITS, bool XBF16, int KG>
+// PACK: every pair holds at most 4 tokens (T <= 4), so the bf16 hi and lo
+// parts of h (and of fp32 tokens) share one mma as column pairs.
+template <int BITS, bool XBF16, int KG, bool PACK>
 __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_constant__ LayerArgs a)
 {
     constexpr int NS = num_stages(ring_bits(BITS));
@@ -1518,7 +1587,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         for (int idx = threadIdx.x; idx < T * rows; idx += kThreads) {
             const int t = idx / rows, e = idx - t * rows;
             u64 v;
-            if (!poll_word(a.logit_t + (int64_t)t * a.Epad + e, want, a.wait_cycles, v)) {
+            if (!poll_word(a.logit_t + ((int64_t)blockIdx.x * T + t) * a.Epad + e, want, a.wait_cycles,
+                           v)) {
                 set_status(a.status, kStatusTimeout);
                 s_fail = 1;
                 break;
@@ -1551,24 +1621,40 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             rs.shared_w[threadIdx.x] = 1.0f;
         cta_barrier();
         const bool ok = s_fail == 0;
-        if (ok && warp < T) {
-            const int t = warp;
-            route_token(rs.lg + t * E4, rs.key + t * E4, E, kk, a.router_sigmoid, a.norm, a.rsf,
-                        rs.ids + t * kk, rs.weights + t * kk);
-            __syncwarp();
-            if (blockIdx.x == 0 && lane < kk) {
-                const int id = rs.ids[t * kk + lane];
-                const float wv = rs.weights[t * kk + lane];
-                a.ids[t * kk + lane] = id;
-                a.weights[t * kk + lane] = wv;
-                if (a.ids_out)
-                    a.ids_out[t * kk + lane] = id;
-                if (a.w_out)
-                    a.w_out[t * kk + lane] = wv;
+        if (ok) {
+            const int nc = (E + 31) / 32;
+            for (int task = warp; task < T * nc; task += kWarps) {
+                const int t = task / nc, c = task - t * nc;
+                route_chunk(rs.lg + t * E4, rs.key + t * E4, E, kk, c, a.router_sigmoid, rs.ids + t * kk,
+                            rs.score + t * kk);
             }
         }
         cta_barrier();
-        if (ok && warp == 0)
+        if (ok && warp < T) {
+            // the weights of token t in rank order: renormalised over the
+            // selection (summed in rank order, like the oracle) if norm,
+            // times the routed scaling factor
+            const int t = warp;
+            float psel = 0.f;
+            for (int j = 0; j < kk; ++j)
+                psel += rs.score[t * kk + j];
+            if (lane < kk) {
+                const float pj = rs.score[t * kk + lane];
+                const float wv = (a.norm ? __fdividef(pj, psel) : pj) * a.rsf;
+                rs.weights[t * kk + lane] = wv;
+                if (blockIdx.x == 0) {
+                    const int id = rs.ids[t * kk + lane];
+                    a.ids[t * kk + lane] = id;
+                    a.weights[t * kk + lane] = wv;
+                    if (a.ids_out)
+                        a.ids_out[t * kk + lane] = id;
+                    if (a.w_out)
+                        a.w_out[t * kk + lane] = wv;
+                }
+            }
+        }
+        // the pair table needs only the ids: built while the weights are
+        if (ok && warp == kWarps - 1)
             cta_dispatch(a, rs);
         cta_barrier();
         rv.pairs = &rs.pairs[0][0];
@@ -1596,12 +1682,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         if (warp == 0)
             set_order(gg);
         s_geo[warp] = gg;
-    }
-    cta_barrier();
-    if (threadIdx.x == 0) {
-        if (s_geo[0].ch0 > KG || (P_t > P_r && s_geo[0].ch1 > KG) || s_geo[1].gk0 > kDownGroupsMax ||
-            (P_t > P_r && s_geo[1].gk1 > kDownGroupsMax)) {
-            // the host checks both limits; never reached
+        // limits the host checks (never reached): gate/up chunks per strip
+        // (the B fragments a warp holds), down groups per strip (two per warp)
+        if (warp == 0 ? (gg.ch0 > KG || (P_t > P_r && gg.ch1 > KG))
+                      : (gg.gk0 > kDownGroupsMax || (P_t > P_r && gg.gk1 > kDownGroupsMax))) {
             set_status(a.status, kStatusBadArg);
             s_fail = 1;
         }
@@ -1610,8 +1694,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     st.geo = s_geo;
     st.pr = &s_pr;
     if (warp < kStreamWarps) {
-        stream_gateup<BITS, XBF16, KG>(a, rv, st);
-        stream_down<BITS>(a, rv, st);
+        stream_gateup<BITS, XBF16, KG, PACK>(a, rv, st);
+        stream_down<BITS, PACK>(a, rv, st);
     } else if (warp == kProducerWarp) {
         if (lane == 0) {
             s_pr.phase = 0;
@@ -1622,8 +1706,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
         __syncwarp();
     } else {
-        epi_gateup<BITS>(a, rv, st);
-        epi_down<BITS>(a, rv, st);
+        epi_gateup<BITS, PACK && !XBF16>(a, rv, st);
+        epi_down<BITS, PACK>(a, rv, st);
     }
     cta_barrier();
 
@@ -1702,10 +1786,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     }
 }
 
-template <int BITS, bool XBF16, int KG>
+template <int BITS, bool XBF16, int KG, bool PACK>
 cudaError_t launch_t(const LayerArgs &a, cudaStream_t stream)
 {
-    auto kern = moe_layer_kernel<BITS, XBF16, KG>;
+    auto kern = moe_layer_kernel<BITS, XBF16, KG, PACK>;
     const int smem = smem_bytes(ring_bits(BITS));
     static int attr_done[64] = {0};
     int dev = 0;
@@ -1787,6 +1871,14 @@ cudaError_t launch_combine(const LayerArgs &a, cudaStream_t stream)
 
 int layer_grid_ctas_max() { return device_sm_count() * kMaxLayerCtasPerSm; }
 
+template <int BITS, int KG>
+cudaError_t launch_depth(const LayerArgs &a, cudaStream_t stream)
+{
+    if (a.T <= 4)
+        return a.x_bf16 ? launch_t<BITS, true, KG, true>(a, stream) : launch_t<BITS, false, KG, true>(a, stream);
+    return a.x_bf16 ? launch_t<BITS, true, KG, false>(a, stream) : launch_t<BITS, false, KG, false>(a, stream);
+}
+
 cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream)
 {
     // gate/up chunks per strip (d / 2048, rounded up) decide how many B
@@ -1795,16 +1887,10 @@ cudaError_t launch_layer(const LayerArgs &a, cudaStream_t stream)
     if (kg > 2 || a.f / kGroup > kDownGroupsMax || a.fs / kGroup > kDownGroupsMax)
         return cudaErrorInvalidValue;
     if (a.mixed)
-        return kg <= 1 ? (a.x_bf16 ? launch_t<0, true, 1>(a, stream) : launch_t<0, false, 1>(a, stream))
-                       : (a.x_bf16 ? launch_t<0, true, 2>(a, stream) : launch_t<0, false, 2>(a, stream));
-    if (kg <= 1) {
-        if (a.bits == 4)
-            return a.x_bf16 ? launch_t<4, true, 1>(a, stream) : launch_t<4, false, 1>(a, stream);
-        return a.x_bf16 ? launch_t<2, true, 1>(a, stream) : launch_t<2, false, 1>(a, stream);
-    }
+        return kg <= 1 ? launch_depth<0, 1>(a, stream) : launch_depth<0, 2>(a, stream);
     if (a.bits == 4)
-        return a.x_bf16 ? launch_t<4, true, 2>(a, stream) : launch_t<4, false, 2>(a, stream);
-    return a.x_bf16 ? launch_t<2, true, 2>(a, stream) : launch_t<2, false, 2>(a, stream);
+        return kg <= 1 ? launch_depth<4, 1>(a, stream) : launch_depth<4, 2>(a, stream);
+    return kg <= 1 ? launch_depth<2, 1>(a, stream) : launch_depth<2, 2>(a, stream);
 }
 
 }  // namespace smoe

@@ -36,7 +36,7 @@ EXPORTED = [
     "smoe_route_from_logits_ex", "smoe_moe_forward_ex",
     "smoe_repacked_bytes_mixed", "smoe_repack_mixed", "smoe_unpack_mixed",
     "smoe_moe_workspace_bytes_mixed", "smoe_moe_forward_mixed", "smoe_moe_forward_stage_mixed",
-    "smoe_debug_set_waits",
+    "smoe_debug_set_waits", "smoe_moe_path_dtype",
 ]
 
 # Execution paths (SMOE_PATH_* in include/smoe.h).
@@ -148,6 +148,8 @@ def load(path: str | None = None):
     L.smoe_moe_forward_path.restype = I
     L.smoe_moe_path.argtypes = [ctypes.POINTER(LayerDesc), I64]
     L.smoe_moe_path.restype = I
+    L.smoe_moe_path_dtype.argtypes = [ctypes.POINTER(LayerDesc), I64, I]
+    L.smoe_moe_path_dtype.restype = I
     RP = ctypes.POINTER(RouterOpts)
     L.smoe_route_from_logits_ex.argtypes = [P, I64, I32, I32, I, P, RP, P, P, P]
     L.smoe_route_from_logits_ex.restype = I
@@ -428,10 +430,12 @@ def forward(layer: MoELayer, x: torch.Tensor, ws: torch.Tensor, y=None, ids=None
     return y
 
 
-def path_for(layer: MoELayer, T: int) -> int:
-    """smoe_moe_path: the execution path smoe_moe_forward (and, for a layer
-    with per-expert depths, smoe_moe_forward_mixed) takes at T tokens."""
-    return int(load().smoe_moe_path(ctypes.byref(layer.desc), T))
+def path_for(layer: MoELayer, T: int, x_dtype=None) -> int:
+    """smoe_moe_path_dtype: the execution path smoe_moe_forward (and, for a
+    layer with per-expert depths, smoe_moe_forward_mixed) takes at T tokens
+    of x_dtype (a torch dtype; default bf16 -- fp32 tokens always stream)."""
+    dt = SMOE_F32 if x_dtype == torch.float32 else SMOE_BF16
+    return int(load().smoe_moe_path_dtype(ctypes.byref(layer.desc), T, dt))
 
 
 def forward_noalloc(layer: MoELayer, x: torch.Tensor, y=None, ids=None, w=None, stream=None):

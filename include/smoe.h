@@ -334,8 +334,10 @@ smoe_status smoe_moe_workspace_init(void *workspace, size_t workspace_bytes, voi
  *              memory, tensor-core GEMMs (tcgen05) with bf16 activations and
  *              bf16 h, fp32 accumulation, each expert's output scaled by its
  *              routing weight and rounded to bf16 before the fp32 sum over
- *              the token's experts; taken when T >= 16 and
- *              T * top_k >= 16 * num_experts (smoe_moe_path tells which)
+ *              the token's experts; taken for bf16 tokens when T >= 16 and
+ *              T * top_k >= 16 * num_experts (smoe_moe_path_dtype tells
+ *              which).  fp32 tokens always take the streaming path, so that
+ *              their accuracy is never reduced to the bf16 operands'.
  * Both are deterministic: the same inputs give the same bits on every call.
  *   x           device [T, d_model], fp32 or bf16 (x_dtype)
  *   y           device out fp32 [T, d_model]
@@ -359,9 +361,10 @@ smoe_status smoe_moe_forward(const smoe_layer_desc *layer, const void *x, smoe_d
 
 /* smoe_moe_forward with the execution path chosen by the caller (path
  * SMOE_PATH_AUTO is smoe_moe_forward itself).  The grouped path needs
- * num_tokens >= 16 (the workspace of smaller batches has no room for it):
- * otherwise SMOE_ERR_UNSUPPORTED, nothing enqueued.  Same arguments and
- * errors as smoe_moe_forward, plus SMOE_ERR_INVALID_ARG for an unknown path. */
+ * num_tokens >= 16 (the workspace of smaller batches has no room for it) and
+ * bf16 tokens (it would round fp32 ones to bf16): otherwise
+ * SMOE_ERR_UNSUPPORTED, nothing enqueued.  Same arguments and errors as
+ * smoe_moe_forward, plus SMOE_ERR_INVALID_ARG for an unknown path. */
 smoe_status smoe_moe_forward_path(const smoe_layer_desc *layer, const void *x, smoe_dtype x_dtype,
                                   int64_t num_tokens, float *y, void *workspace,
                                   size_t workspace_bytes, int32_t *ids_out, float *w_out, int path,
@@ -408,9 +411,15 @@ smoe_status smoe_moe_forward_stage_mixed(const smoe_layer_desc *layer, const uin
                                          int32_t *ids_out, float *w_out, int stage,
                                          void *cuda_stream);
 
-/* The path smoe_moe_forward takes for this layer and token count
- * (SMOE_PATH_STREAM or SMOE_PATH_GROUPED), or -1 on invalid arguments. */
+/* The path smoe_moe_forward takes for this layer and token count with bf16
+ * tokens (SMOE_PATH_STREAM or SMOE_PATH_GROUPED), or -1 on invalid
+ * arguments; smoe_moe_path_dtype(layer, num_tokens, SMOE_BF16). */
 int smoe_moe_path(const smoe_layer_desc *layer, int64_t num_tokens);
+
+/* The path smoe_moe_forward takes for this layer, token count and token
+ * dtype (fp32 tokens: always SMOE_PATH_STREAM), or -1 on invalid
+ * arguments. */
+int smoe_moe_path_dtype(const smoe_layer_desc *layer, int64_t num_tokens, smoe_dtype x_dtype);
 
 /* The same forward as smoe_moe_forward, one launch stage at a time, so that
  * a caller can put its own work or timing events between the stages.  The

@@ -137,8 +137,9 @@ def test_other_entry_points_reject_bad_args(libs):
 
 def test_path_selection_and_path_argument(libs):
     """smoe_moe_path: the streaming path below 16 tokens or below 16 routed
-    rows per expert on average, the grouped path from there on; an unknown
-    path is refused before anything else."""
+    rows per expert on average, the grouped path from there on (bf16 tokens;
+    fp32 tokens always stream); an unknown path is refused before anything
+    else."""
     S, _ = libs
     L = S.load()
     P = ctypes.c_void_p
@@ -149,6 +150,12 @@ def test_path_selection_and_path_argument(libs):
     assert L.smoe_moe_path(ctypes.byref(desc), 64) == S.PATH_GROUPED    # 128 rows
     assert L.smoe_moe_path(ctypes.byref(desc), -1) == -1
     assert L.smoe_moe_path(ctypes.byref(_desc(S, bits=3)), 64) == -1
+    # fp32 tokens always stream (the tensor-core path would round them)
+    for T in (1, 64, 4096):
+        assert L.smoe_moe_path_dtype(ctypes.byref(desc), T, S.SMOE_F32) == S.PATH_STREAM
+        assert (L.smoe_moe_path_dtype(ctypes.byref(desc), T, S.SMOE_BF16) ==
+                L.smoe_moe_path(ctypes.byref(desc), T))
+    assert L.smoe_moe_path_dtype(ctypes.byref(desc), 64, 5) == -1
     for bad_path in (-1, 3, 7):
         assert L.smoe_moe_forward_path(ctypes.byref(desc), P(4096), 0, 64, P(8192), P(1 << 20),
                                        1 << 30, None, None, bad_path, None) == -1

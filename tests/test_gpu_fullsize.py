@@ -136,8 +136,9 @@ class FullLayer:
         Sampled tokens at or past T are skipped.  x_f32: the tokens as fp32
         values of the seeded stream (not rounded to bf16)."""
         wl = self.wl
+        xdt = torch.float32 if x_f32 else torch.bfloat16
         grouped = (path == S.PATH_GROUPED or
-                   (path in (None, S.PATH_AUTO) and S.path_for(self.lay, T) == S.PATH_GROUPED))
+                   (path in (None, S.PATH_AUTO) and S.path_for(self.lay, T, xdt) == S.PATH_GROUPED))
         if tol is None:
             tol = 2e-2 if grouped else 1e-3
         sample = [t for t in self.sample if t < T]
@@ -185,8 +186,11 @@ def test_deepseek16b_layer_full_size(S, pool, bits):
     fl.check(S, 1)
 
 
-def test_qwen235b_decode_layer_full_size(S, pool):
-    fl = FullLayer(S, pool, "qwen235b", 0, 4, sample=[0])
+@pytest.mark.parametrize("layer", [0, 31, 62, 93])
+def test_qwen235b_decode_layer_full_size(S, pool, layer):
+    """The 94-layer Qwen3-235B-like decode stack, spot-checked on four
+    evenly spaced layers (each its own seeded weights and token)."""
+    fl = FullLayer(S, pool, "qwen235b", layer, 4, sample=[0])
     fl.check(S, 1)
 
 
@@ -208,24 +212,78 @@ def test_a3b35b_grouped_path_full_size(S, pool, bits):
     fl.check(S, 256, path=S.PATH_GROUPED)
 
 
+def segment_picks(wl, layer, T, bias):
+    """Tokens whose grouped-path rows lie where the first tokens' rows never
+    do.  The sort is stable in token order, so the rank of a token among the
+    tokens that chose expert e is its row in e's segment: the hot expert's
+    rank-128 and rank-200 tokens (the second m-tile, at 4,096 tokens the
+    second accumulator of a paired item), its last token (the ragged last
+    m-tile), the last token of a segment of 33..64 rows (a 64-row activation
+    box) and of one of 1..32 rows (a 32-row box), and token T - 1.  Picked
+    from a host routing of all T tokens (fp64 logits plus the bias, top-k
+    with ties to the lower index); the oracle still routes the picked tokens
+    itself.  Returns (tokens, {what: token})."""
+    x, _ = wl.activations(layer, T)
+    r = Y.bf16_to_f32(wl.router_weight(layer)).astype(np.float64)
+    key = x.astype(np.float64) @ r.T
+    if bias is not None:
+        key = key + bias.astype(np.float64)
+    top = np.argsort(-key, axis=1, kind="stable")[:, :wl.k]
+    counts = np.bincount(top.ravel(), minlength=wl.E)
+    hot = int(np.argmax(counts))
+    rows_hot = np.nonzero((top == hot).any(axis=1))[0]
+    what = {"last token": T - 1, "hot last row": int(rows_hot[-1])}
+    if len(rows_hot) > 128:
+        what["hot row 128"] = int(rows_hot[128])
+    if len(rows_hot) > 200:
+        what["hot row 200"] = int(rows_hot[200])
+    for name, lo, hi in (("64-row box", 33, 64), ("32-row box", 1, 32)):
+        cand = [e for e in range(wl.E) if lo <= counts[e] <= hi]
+        if cand:
+            what[name] = int(np.nonzero((top == cand[0]).any(axis=1))[0][-1])
+    return sorted(set(what.values())), what
+
+
+def test_segment_picks_reach_the_second_m_tile():
+    """At 4,096 tokens (256 routed rows per expert on average: paired
+    m-tiles) the hot expert's segment spans several m-tiles, so the picks
+    include a second-m-tile row and a ragged last m-tile."""
+    wl = Y.WORKLOADS["qwen235b_batched"]
+    toks, what = segment_picks(wl, 0, 4096, wl.zipf_bias())
+    assert "hot row 128" in what and "hot row 200" in what
+    assert what["last token"] == 4095 and all(0 <= t < 4096 for t in toks)
+
+
 def test_qwen235b_batched_zipf_full_size(S, pool):
-    """Zipf(1.1)-skewed selection bias; T = 8, 64, 512, 4096 with the same
-    sampled tokens (token i is the same vector whatever T)."""
+    """Zipf(1.1)-skewed selection bias; T = 8 and 64 with tokens 0 and 5,
+    T = 512 and 4096 with tokens picked to reach the second m-tile of a
+    paired item, the ragged last m-tile, the 64- and 32-row activation boxes
+    and the last token (segment_picks)."""
     wl = Y.WORKLOADS["qwen235b_batched"]
     bias = wl.zipf_bias()
     fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=[0, 5], bias=bias)
-    for T in (8, 64, 512, 4096):
+    for T in (8, 64):
+        fl.check(S, T)
+    for T in (512, 4096):
+        toks, _ = segment_picks(wl, 0, T, bias)
+        fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=toks, bias=bias)
         fl.check(S, T)
 
 
 def test_qwen235b_batched_mixed_depth_full_size(S, pool):
     """Mixed depths at the batched geometry: the 32 most popular experts
     (Zipf rank) at Q4, the other 96 at Q2, with the Zipf selection bias;
-    T = 8, 64 and 4096 (the benchmark's batch), sampled."""
+    T = 8 and 64 with tokens 0 and 5, T = 512 and 4096 (the benchmark's
+    batch) with the segment_picks tokens."""
     wl = Y.WORKLOADS["qwen235b_batched"]
-    fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=[0, 5], bias=wl.zipf_bias(),
-                   expert_bits=wl.mixed_bits(0.25))
-    for T in (4096, 64, 8):
+    bias = wl.zipf_bias()
+    eb = wl.mixed_bits(0.25)
+    fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=[0, 5], bias=bias, expert_bits=eb)
+    for T in (64, 8):
+        fl.check(S, T)
+    for T in (512, 4096):
+        toks, _ = segment_picks(wl, 0, T, bias)
+        fl = FullLayer(S, pool, "qwen235b_batched", 0, 4, sample=toks, bias=bias, expert_bits=eb)
         fl.check(S, T)
 
 

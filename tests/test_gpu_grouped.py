@@ -1,12 +1,15 @@
 """GPU parity of the expert-sorted grouped (tensor-core) path against the
 oracle.
 
-The grouped path rounds the activations, the dequantised weights and h to
-bf16 (the tcgen05 kind::f16 operand type) and accumulates in fp32; its bar is
-max-abs-error <= 2e-2 * ||y_ref||_inf.  Shapes are chosen so that experts
-span several 128-row m-tiles with a ragged last one, gate/up n-tiles end
-half full (f % 128 == 64), down n-tiles end half full (d % 256 == 128), and
-the shared expert (all tokens) is a segment of its own.
+The grouped path takes bf16 tokens, rounds the dequantised weights and h to
+bf16 (the tcgen05 kind::f16 operand type) and accumulates in fp32; its bar
+for bf16 activations is max-abs-error <= 2e-2 * ||y_ref||_inf.  fp32 tokens
+never take it: the forward sends them to the streaming path, whose bar is
+1e-3 * ||y_ref||_inf, and a forced grouped forward of fp32 tokens is
+refused.  Shapes are chosen so that experts span several 128-row m-tiles
+with a ragged last one, gate/up n-tiles end half full (f % 128 == 64), down
+n-tiles end half full (d % 256 == 128), and the shared expert (all tokens)
+is a segment of its own.
 """
 import zlib
 
@@ -26,12 +29,16 @@ TOL = 2e-2
 
 CFG = {
     # name: (d, f, E, k, norm, x_dtype, shared_f, shared_gate, p_zero)
-    "tiny_f32": (256, 128, 8, 2, True, "f32", 0, False, 0.2),
+    "tiny_bf16": (256, 128, 8, 2, True, "bf16", 0, False, 0.2),
     "half_ntile_bf16": (256, 192, 16, 4, False, "bf16", 0, False, 0.0),
     "wide_bf16": (512, 128, 32, 6, True, "bf16", 0, False, 0.0),
     "shared_bf16": (256, 128, 24, 8, True, "bf16", 192, True, 0.0),
+    "shared_nogate_bf16": (384, 64, 12, 3, True, "bf16", 64, False, 0.0),
+    # fp32 tokens at grouped-path batch sizes (they stream)
+    "tiny_f32": (256, 128, 8, 2, True, "f32", 0, False, 0.2),
     "shared_nogate_f32": (384, 64, 12, 3, True, "f32", 64, False, 0.0),
 }
+TOL_F32 = 1e-3
 
 
 @pytest.fixture(scope="module")
@@ -74,19 +81,50 @@ def run(S, lay, wl, x_host, path):
 
 
 @pytest.mark.parametrize("bits", [4, 2])
-@pytest.mark.parametrize("name,T", [("tiny_f32", 16), ("tiny_f32", 200), ("tiny_f32", 700),
+@pytest.mark.parametrize("name,T", [("tiny_bf16", 16), ("tiny_bf16", 200), ("tiny_bf16", 700),
                                     ("half_ntile_bf16", 64), ("half_ntile_bf16", 333),
                                     ("wide_bf16", 257), ("shared_bf16", 40),
-                                    ("shared_bf16", 300), ("shared_nogate_f32", 150),
+                                    ("shared_bf16", 300), ("shared_nogate_bf16", 150),
                                     # >= 256 rows per expert on average: items pair two
                                     # m-tiles in the gate/up GEMM
-                                    ("tiny_f32", 1100), ("half_ntile_bf16", 1030)])
+                                    ("tiny_bf16", 1100), ("half_ntile_bf16", 1030)])
 def test_grouped_matches_oracle(S, name, T, bits):
     wl, hl = host_layer(name, bits)
     lay = hl.device_layer(DEV)
     x, _ = wl.activations(0, T)
     y, ids, w = run(S, lay, wl, x, S.PATH_GROUPED)
     check_forward(y, ids, w, hl, x, tol=TOL)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("name,T", [("tiny_f32", 200), ("tiny_f32", 1100),
+                                    ("shared_nogate_f32", 150)])
+def test_fp32_tokens_stream_at_grouped_batch_sizes(S, name, T, bits):
+    """Batches whose bf16 twin takes the grouped path: with fp32 tokens the
+    forward streams (fp32 accumulation) and holds the fp32 bar, 1e-3."""
+    wl, hl = host_layer(name, bits)
+    lay = hl.device_layer(DEV)
+    assert S.path_for(lay, T, torch.bfloat16) == S.PATH_GROUPED
+    assert S.path_for(lay, T, torch.float32) == S.PATH_STREAM
+    x, _ = wl.activations(0, T)
+    y, ids, w = run(S, lay, wl, x, None)
+    check_forward(y, ids, w, hl, x, tol=TOL_F32)
+
+
+def test_grouped_path_refuses_fp32_tokens(S):
+    """A forced grouped forward of fp32 tokens would round them to bf16: it
+    is refused (SMOE_ERR_UNSUPPORTED) and enqueues nothing."""
+    wl, hl = host_layer("tiny_f32", 4)
+    lay = hl.device_layer(DEV)
+    x, _ = wl.activations(0, 200)
+    xt = to_dev(x, DEV)
+    ws = S.workspace(lay, 200)
+    y = torch.full((200, wl.d), 7.0, dtype=torch.float32, device=DEV)
+    with pytest.raises(S.SmoeError) as ei:
+        S.forward(lay, xt, ws, y=y, path=S.PATH_GROUPED)
+    assert ei.value.status == -2
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
 
 
 def test_grouped_with_expert_bias_skew(S):
@@ -131,10 +169,10 @@ def test_grouped_is_deterministic(S):
 
 
 def test_grouped_refuses_small_batches(S):
-    wl, hl = host_layer("tiny_f32", 4)
+    wl, hl = host_layer("tiny_bf16", 4)
     lay = hl.device_layer(DEV)
     x, _ = wl.activations(0, 15)
-    xt = to_dev(x, DEV)
+    xt = to_dev(x, DEV).to(torch.bfloat16)
     ws = S.workspace(lay, 15)
     y = torch.full((15, wl.d), 7.0, dtype=torch.float32, device=DEV)
     with pytest.raises(S.SmoeError) as ei:

@@ -32,6 +32,9 @@ CFG = {
     "half_ntile_bf16": (256, 192, 16, 4, False, "bf16", 0, False, 4),
     "shared_bf16": (256, 128, 24, 8, True, "bf16", 192, True, 2),
     "shared_f32": (384, 64, 12, 3, True, "f32", 64, False, 4),
+    # bf16 twins of the fp32 shapes for the grouped path (bf16 tokens only)
+    "tiny_bf16": (256, 128, 8, 2, True, "bf16", 0, False, 4),
+    "shared_nogate_bf16": (384, 64, 12, 3, True, "bf16", 64, False, 4),
 }
 
 
@@ -90,27 +93,46 @@ STREAM, GROUPED = 1, 2
 
 
 @pytest.mark.parametrize("name,pat,T,path", [
-    # streaming: fused routing + combine (T <= 8), then the separate stages
+    # streaming: fused routing + combine (T <= 8), then the separate stages;
+    # fp32 tokens stream at every batch size
     ("tiny_f32", "alternate", 1, None), ("half_ntile_bf16", "alternate", 5, None),
     ("shared_bf16", "alternate", 3, None), ("shared_f32", "alternate", 9, None),
     ("shared_bf16", "one_q2", 40, STREAM), ("tiny_f32", "one_q4", 200, STREAM),
     ("half_ntile_bf16", "popular", 64, STREAM), ("shared_f32", "one_q4", 150, STREAM),
+    ("tiny_f32", "one_q2", 700, None),
     # grouped, small batches included
-    ("tiny_f32", "alternate", 1, GROUPED), ("shared_bf16", "popular", 7, GROUPED),
-    ("tiny_f32", "alternate", 16, GROUPED), ("tiny_f32", "one_q4", 200, GROUPED),
-    ("tiny_f32", "one_q2", 700, None), ("half_ntile_bf16", "one_q4", 333, None),
+    ("tiny_bf16", "alternate", 1, GROUPED), ("shared_bf16", "popular", 7, GROUPED),
+    ("tiny_bf16", "alternate", 16, GROUPED), ("tiny_bf16", "one_q4", 200, GROUPED),
+    ("tiny_bf16", "one_q2", 700, None), ("half_ntile_bf16", "one_q4", 333, None),
     ("shared_bf16", "popular", 300, None), ("shared_bf16", "one_q2", 40, GROUPED),
-    ("shared_f32", "one_q4", 150, GROUPED),
+    ("shared_nogate_bf16", "one_q4", 150, GROUPED),
     # >= 256 rows per expert on average: items pair two m-tiles
-    ("tiny_f32", "alternate", 1100, None), ("half_ntile_bf16", "popular", 1030, None),
+    ("tiny_bf16", "alternate", 1100, None), ("half_ntile_bf16", "popular", 1030, None),
 ])
 def test_mixed_matches_oracle(S, name, pat, T, path):
     wl, hl = host_layer(name, pat)
     lay = hl.device_layer(DEV)
-    grouped = path == GROUPED or (path is None and S.path_for(lay, T) == S.PATH_GROUPED)
+    xdt = torch.float32 if wl.x_dtype == "f32" else torch.bfloat16
+    grouped = path == GROUPED or (path is None and S.path_for(lay, T, xdt) == S.PATH_GROUPED)
     x, _ = wl.activations(0, T)
     y, ids, w = run(S, lay, wl, x, path=path)
     check_forward(y, ids, w, hl, x, tol=TOL if grouped else 1e-3)
+
+
+def test_mixed_grouped_path_refuses_fp32_tokens(S):
+    """The tensor-core path takes bf16 tokens only; a forced grouped forward
+    of fp32 tokens is refused with nothing enqueued."""
+    wl, hl = host_layer("tiny_f32", "alternate")
+    lay = hl.device_layer(DEV)
+    x, _ = wl.activations(0, 64)
+    xt = to_dev(x, DEV)
+    ws = S.workspace(lay, 64)
+    y = torch.full((64, wl.d), 7.0, dtype=torch.float32, device=DEV)
+    with pytest.raises(S.SmoeError) as ei:
+        S.forward(lay, xt, ws, y=y, path=GROUPED)
+    assert ei.value.status == -2
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
 
 
 def test_repack_mixed_is_the_per_expert_repacks_back_to_back(S):
@@ -179,7 +201,8 @@ def test_mixed_with_router_options(S, T):
         y_ref[mism] = hl.oracle_apply(x[mism], ids[mism], w[mism])
     ok = [t for t in range(T) if t not in mism]
     assert np.allclose(w[ok], w_ref[ok], rtol=1e-5, atol=1e-6)
-    tol = TOL if S.path_for(lay, T) == S.PATH_GROUPED else 1e-3
+    xdt = torch.float32 if wl.x_dtype == "f32" else torch.bfloat16
+    tol = TOL if S.path_for(lay, T, xdt) == S.PATH_GROUPED else 1e-3
     assert float(np.abs(y - y_ref).max()) <= tol * float(np.abs(y_ref).max())
 
 

@@ -73,6 +73,7 @@ def test_route_from_logits_variants(S, E, k, sigm, with_bias):
 CFG = {
     # name: (d, f, E, k, norm, x_dtype, shared_f, shared_gate)
     "tiny_f32": (256, 128, 8, 2, True, "f32", 0, False),
+    "tiny_bf16": (256, 128, 8, 2, True, "bf16", 0, False),
     "wide_bf16": (512, 128, 32, 6, True, "bf16", 0, False),
     "shared_bf16": (256, 128, 24, 8, False, "bf16", 192, True),
 }
@@ -92,7 +93,7 @@ def _host(name):
 @pytest.mark.parametrize("name,T,path", [("tiny_f32", 1, None), ("tiny_f32", 8, None),
                                          ("wide_bf16", 13, None), ("shared_bf16", 5, None),
                                          ("shared_bf16", 40, 2), ("wide_bf16", 96, 2),
-                                         ("tiny_f32", 64, 2)])
+                                         ("tiny_bf16", 64, 2), ("tiny_f32", 64, None)])
 @pytest.mark.parametrize("sigm,rsf,with_bias", [(True, 1.0, False), (True, 2.5, True),
                                                 (False, 2.5, True)])
 def test_forward_with_router_variants(S, name, T, path, sigm, rsf, with_bias):
@@ -126,7 +127,7 @@ def test_forward_with_router_variants(S, name, T, path, sigm, rsf, with_bias):
         y_ref[mism] = hl.oracle_apply(x[mism], ids[mism], w[mism])
     ok = [t for t in range(T) if t not in mism]
     assert np.allclose(w[ok], w_ref[ok], rtol=1e-5, atol=1e-6)
-    tol = 2e-2 if (path == 2 or S.path_for(lay, T) == S.PATH_GROUPED) else 1e-3
+    tol = 2e-2 if (path == 2 or S.path_for(lay, T, xt.dtype) == S.PATH_GROUPED) else 1e-3
     err = float(np.abs(y - y_ref).max())
     assert err <= tol * float(np.abs(y_ref).max()), (err, tol)
 
@@ -193,5 +194,5 @@ def test_forward_with_routing_mask(S, name, T, path):
         y_ref[mism] = hl.oracle_apply(x[mism], ids[mism], w[mism])
     ok = [t for t in range(T) if t not in mism]
     assert np.allclose(w[ok], w_ref[ok], rtol=1e-5, atol=1e-6)
-    tol = 2e-2 if (path == 2 or S.path_for(lay, T) == S.PATH_GROUPED) else 1e-3
+    tol = 2e-2 if (path == 2 or S.path_for(lay, T, xt.dtype) == S.PATH_GROUPED) else 1e-3
     assert float(np.abs(y - y_ref).max()) <= tol * float(np.abs(y_ref).max())
