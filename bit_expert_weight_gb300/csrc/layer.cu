@@ -1160,6 +1160,39 @@ __device__ __forceinline__ void put_red(const LayerArgs &a, Stream &st, float4 v
     ++st.uc;
 }
 
+// The warp's tiles of one gate/up stage at depth B: groups w (fragments
+// f0) and w + 16 (f1), each a gate and an up tile.
+template <int B, bool SPLIT>
+__device__ __forceinline__ void gateup_tiles(const uint8_t *stage, const BFrag &f0, const BFrag &f1, bool g0,
+                                             bool g1, float (&accg)[4], float (&accu)[4], float (&accg2)[4],
+                                             float (&accu2)[4])
+{
+    constexpr int TB = tile_bytes(B);
+    const int warp = threadIdx.x >> 5;
+    if (g0) {
+        mac_tile<B, SPLIT>(stage + warp * 2 * TB, f0, accg, true);
+        mac_tile<B, SPLIT>(stage + warp * 2 * TB + TB, f0, accu, true);
+    }
+    if (g1) {
+        mac_tile<B, SPLIT>(stage + (warp + kStreamWarps) * 2 * TB, f1, accg2, true);
+        mac_tile<B, SPLIT>(stage + (warp + kStreamWarps) * 2 * TB + TB, f1, accu2, true);
+    }
+}
+
+// The warp's two tiles of down strip j of a stage at depth B (groups w and
+// w + 16 of the strip's gk groups), added into acc.
+template <int B, bool SPLIT>
+__device__ __forceinline__ void down_tiles(const uint8_t *stage, int j, int gk, const BFrag (&bf)[2], bool g0,
+                                           bool g1, float (&acc)[4])
+{
+    constexpr int TB = tile_bytes(B);
+    const int t0 = j * gk + (threadIdx.x >> 5);
+    if (g0)
+        mac_tile<B, SPLIT>(stage + t0 * TB, bf[0], acc, true);
+    if (g1)
+        mac_tile<B, SPLIT>(stage + (t0 + kStreamWarps) * TB, bf[1], acc, true);
+}
+
 // The gate/up phase of a streaming warp.  The warp holds the B fragments
 // of its groups of the current pair: groups c * gc + w and c * gc + w + 16
 // of each chunk c (at most KG chunks).  At a unit's end it hands its sums to
@@ -1222,40 +1255,24 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
             // read in-bounds stage bytes and are dropped), so the four mma
             // chains of the step schedule together
             // the warp's two groups of the chunk; a group past the chunk's
-            // end is skipped (the branch is uniform over the warp)
+            // end is skipped (the branch is uniform over the warp).  The
+            // chunk's fragments are selected by value, so that the tile code
+            // exists once (a smaller loop for the instruction cache)
             const uint8_t *stage = st.ring + slot * SB;
             const int ng = min(u.gc, u.gk - q.c * u.gc);  // groups in this chunk
             const bool g0 = warp < ng, g1 = warp + kStreamWarps < ng;
+            BFrag f0 = bf[0], f1 = bf[1];
 #pragma unroll
-            for (int c = 0; c < KG; ++c) {
+            for (int c = 1; c < KG; ++c) {
                 if (c == q.c) {
-                    if (BITS != 0 || pb == 4) {
-                        constexpr int B = ring_bits(BITS), TB = tile_bytes(B);
-                        if (g0) {
-                            mac_tile<B, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, true);
-                            mac_tile<B, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, true);
-                        }
-                        if (g1) {
-                            mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2,
-                                                true);
-                            mac_tile<B, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1],
-                                                accu2, true);
-                        }
-                    } else {
-                        constexpr int TB = tile_bytes(2);
-                        if (g0) {
-                            mac_tile<2, kSplit>(stage + warp * 2 * TB, bf[2 * c], accg, true);
-                            mac_tile<2, kSplit>(stage + warp * 2 * TB + TB, bf[2 * c], accu, true);
-                        }
-                        if (g1) {
-                            mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB, bf[2 * c + 1], accg2,
-                                                true);
-                            mac_tile<2, kSplit>(stage + (warp + kStreamWarps) * 2 * TB + TB, bf[2 * c + 1],
-                                                accu2, true);
-                        }
-                    }
+                    f0 = bf[2 * c];
+                    f1 = bf[2 * c + 1];
                 }
             }
+            if (BITS != 0 || pb == 4)
+                gateup_tiles<ring_bits(BITS), kSplit>(stage, f0, f1, g0, g1, accg, accu, accg2, accu2);
+            else
+                gateup_tiles<2, kSplit>(stage, f0, f1, g0, g1, accg, accu, accg2, accu2);
         }
         __syncwarp();
         if (ok && lane == 0)
@@ -1297,10 +1314,6 @@ __device__ __forceinline__ void stream_down(const LayerArgs &a, const RouteView 
     int loaded = -1;
     int pb = ring_bits(BITS);
     BFrag bf[2];
-    float acc[kMaxDownStrips][4];
-#pragma unroll
-    for (int j = 0; j < kMaxDownStrips; ++j)
-        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll 1
     for (int kk = 0; kk < n; ++kk) {
         if (q.p != loaded) {
@@ -1326,46 +1339,39 @@ __device__ __forceinline__ void stream_down(const LayerArgs &a, const RouteView 
         const int slot = static_cast<int>(st.seq % NS);
         const bool ok = wait_stage<NS>(a, st, slot);
         const int ns = down_count(g, u, q);
-        if (ok) {
-            // the warp's groups w and w + 16 of each strip of the step; tiles
-            // past the strips' groups or the step's strips are skipped (the
-            // branches are uniform over the warp)
-            const uint8_t *stage = st.ring + slot * SB;
-            const bool g0 = warp < u.gk, g1 = warp + kStreamWarps < u.gk;
+        // the warp's groups w and w + 16 of each strip of the step (absent
+        // groups skipped by uniform branches), strips in pairs -- one
+        // reduction item each -- in a rolled loop, so that the tile code
+        // exists once (a smaller loop for the instruction cache)
+        const uint8_t *stage = st.ring + slot * SB;
+        const bool g0 = warp < u.gk, g1 = warp + kStreamWarps < u.gk;
+#pragma unroll 1
+        for (int j2 = 0; j2 < ns; j2 += 2) {
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            if (ok) {
+#pragma unroll 1
+                for (int jj = j2; jj < j2 + 2 && jj < ns; ++jj) {
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (BITS != 0 || pb == 4)
+                        down_tiles<ring_bits(BITS), !PACK>(stage, jj, u.gk, bf, g0, g1, c);
+                    else
+                        down_tiles<2, !PACK>(stage, jj, u.gk, bf, g0, g1, c);
+                    const bool first = jj == j2;
 #pragma unroll
-            for (int j = 0; j < kMaxDownStrips; ++j) {
-                if (j < ns) {
-                    const int t0 = j * u.gk + warp, t1 = t0 + kStreamWarps;
-                    if (BITS != 0 || pb == 4) {
-                        constexpr int B = ring_bits(BITS), TB = tile_bytes(B);
-                        if (g0)
-                            mac_tile<B, !PACK>(stage + t0 * TB, bf[0], acc[j], true);
-                        if (g1)
-                            mac_tile<B, !PACK>(stage + t1 * TB, bf[1], acc[j], true);
-                    } else {
-                        constexpr int TB = tile_bytes(2);
-                        if (g0)
-                            mac_tile<2, !PACK>(stage + t0 * TB, bf[0], acc[j], true);
-                        if (g1)
-                            mac_tile<2, !PACK>(stage + t1 * TB, bf[1], acc[j], true);
+                    for (int e = 0; e < 4; ++e) {
+                        a0[e] = first ? c[e] : a0[e];
+                        a1[e] = first ? a1[e] : c[e];
                     }
                 }
             }
+            if (j2 + 2 >= ns) {  // the stage's last tiles are read: release it
+                __syncwarp();
+                if (ok && lane == 0)
+                    mbar_arrive(&st.empty[slot]);
+            }
+            put_red(a, st, make_float4(a0[0], a0[1], a0[2], a0[3]), make_float4(a1[0], a1[1], a1[2], a1[3]));
         }
-        __syncwarp();
-        if (ok && lane == 0)
-            mbar_arrive(&st.empty[slot]);
         ++st.seq;
-#pragma unroll
-        for (int it = 0; it < kMaxDownStrips / 2; ++it) {
-            if (2 * it < ns)
-                put_red(a, st, make_float4(acc[2 * it][0], acc[2 * it][1], acc[2 * it][2], acc[2 * it][3]),
-                        make_float4(acc[2 * it + 1][0], acc[2 * it + 1][1], acc[2 * it + 1][2],
-                                    acc[2 * it + 1][3]));
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxDownStrips; ++j)
-            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
         advance(u, q);
     }
 }
