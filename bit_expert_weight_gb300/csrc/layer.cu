@@ -272,11 +272,13 @@ __device__ __forceinline__ void router_rows(const LayerArgs &a, const RouterPre 
         for (int r = 0; r < 2; ++r)
 #pragma unroll
             for (int t = 0; t < kPairCols; ++t) {
-                float v = acc[r][t];
-                for (int o = 16; o; o >>= 1)
-                    v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0)
-                    red[warp * 16 + r * kPairCols + t] = v;
+                if (r < pre.nrows && t < T) {  // uniform over the warp
+                    float v = acc[r][t];
+                    for (int o = 16; o; o >>= 1)
+                        v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0)
+                        red[warp * 16 + r * kPairCols + t] = v;
+                }
             }
     }
     cta_barrier();
@@ -324,18 +326,38 @@ struct RouteView {
     const float *shared_w;     // [T]
 };
 
-// Routing of one token, experts 32 c .. 32 c + 31, in one warp (task (t, c)
-// of the CTA's T x ceil(E/32) routing tasks): lane L takes expert
-// e = 32 c + L, whose rank is the number of experts before it in the order
-// (key descending, index ascending) -- ties go to the lower index; ranks
+// Rank of expert e (key ke) among the experts lo .. hi - 1 (lo a multiple of
+// 4; key rows 16-byte aligned): how many come before it in the order (key
+// descending, index ascending) -- ties go to the lower index.
+__device__ __forceinline__ int rank_range(const float *key, int e, float ke, int lo, int hi)
+{
+    int r = 0, j = lo;
+    const float4 *k4 = reinterpret_cast<const float4 *>(key);
+#pragma unroll 4
+    for (; j + 4 <= hi; j += 4) {
+        const float4 v = k4[j >> 2];
+        r += (v.x > ke || (v.x == ke && j < e)) ? 1 : 0;
+        r += (v.y > ke || (v.y == ke && j + 1 < e)) ? 1 : 0;
+        r += (v.z > ke || (v.z == ke && j + 2 < e)) ? 1 : 0;
+        r += (v.w > ke || (v.w == ke && j + 3 < e)) ? 1 : 0;
+    }
+    for (; j < hi; ++j) {
+        const float v = key[j];
+        r += (v > ke || (v == ke && j < e)) ? 1 : 0;
+    }
+    return r;
+}
+
+// Selection step of one token, experts 32 c .. 32 c + 31, in one warp: lane
+// L holds expert e = 32 c + L and its rank r over all E experts; ranks
 // below k are the selection, stored at their rank with the expert's score:
 // the softmax over all E logits, or (sigm) the expert's own sigmoid.  The
 // softmax maximum and sum run over all E logits in a fixed order
 // (lane-strided, then a shuffle tree), the same in every task of the token;
 // exp and divide are the hardware approximations (a few ulp), well inside
-// the weights' tolerance.  key rows are 16-byte aligned.
-__device__ __noinline__ void route_chunk(const float *lg, const float *key, int E, int k, int c, int sigm,
-                                         int16_t *ids, float *score)
+// the weights' tolerance.
+__device__ __forceinline__ void route_select(const float *lg, int E, int k, int c, int sigm, int r, int16_t *ids,
+                                          float *score)
 {
     const int lane = threadIdx.x & 31;
     float m = -INFINITY, z = 1.f;
@@ -351,25 +373,7 @@ __device__ __noinline__ void route_chunk(const float *lg, const float *key, int 
             z += __shfl_xor_sync(0xffffffffu, z, o);
     }
     const int e = 32 * c + lane;
-    if (e >= E)
-        return;
-    const float ke = key[e];
-    int r = 0;
-    const float4 *k4 = reinterpret_cast<const float4 *>(key);
-#pragma unroll 4
-    for (int j = 0; j < E / 4; ++j) {
-        const float4 v = k4[j];
-        const int e0 = 4 * j;
-        r += (v.x > ke || (v.x == ke && e0 < e)) ? 1 : 0;
-        r += (v.y > ke || (v.y == ke && e0 + 1 < e)) ? 1 : 0;
-        r += (v.z > ke || (v.z == ke && e0 + 2 < e)) ? 1 : 0;
-        r += (v.w > ke || (v.w == ke && e0 + 3 < e)) ? 1 : 0;
-    }
-    for (int e2 = E & ~3; e2 < E; ++e2) {
-        const float v = key[e2];
-        r += (v > ke || (v == ke && e2 < e)) ? 1 : 0;
-    }
-    if (r < k) {
+    if (e < E && r < k) {
         ids[r] = static_cast<int16_t>(e);
         score[r] = sigm ? sigmoid_fast(lg[e]) : __fdividef(__expf(lg[e] - m), z);  // z in [1, E]
     }
@@ -990,7 +994,7 @@ __device__ __forceinline__ float acc_col(const float (&v)[4], int e, int &col)
 // Finalise gate/up strip s of pair p from its full-K sums (one warp, cold
 // path): h = SiLU(g) * u as bf16 hi + lo, stored tagged.
 template <int BITS, bool PACK>
-__device__ __noinline__ void finalize_gateup(const EpiOut a, int ncols, int p, int s, float4 ag, float4 au)
+__device__ __forceinline__ void finalize_gateup(const EpiOut a, int ncols, int p, int s, float4 ag, float4 au)
 {
     constexpr float L = BITS == 4 ? 7.5f : 1.5f;
     const int lane = threadIdx.x & 31, gq = lane >> 2;
@@ -1045,7 +1049,7 @@ __device__ __forceinline__ void finalize_down(const EpiOut &a, int ncols, int p,
 // contributor) polls the others' sums, adds them all in CTA order and
 // finalises.  False if a bounded poll ran out.
 template <int BITS, bool PACK>
-__device__ __noinline__ bool fixup_gateup(const EpiOut a, int ncols, const Geo &g, int p, int s, int ustart,
+__device__ __forceinline__ bool fixup_gateup(const EpiOut a, int ncols, const Geo &g, int p, int s, int ustart,
                                           int uend, float4 tg, float4 tu)
 {
     const int lane = threadIdx.x & 31;
@@ -1627,12 +1631,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             rs.shared_w[threadIdx.x] = 1.0f;
         cta_barrier();
         const bool ok = s_fail == 0;
+        // Ranking: task (t, c) ranks experts 32 c .. 32 c + 31 of token t
+        // against all E keys, then stores the selected ones with their scores
+        const int nc = (E + 31) / 32;
         if (ok) {
-            const int nc = (E + 31) / 32;
             for (int task = warp; task < T * nc; task += kWarps) {
-                const int t = task / nc, c = task - t * nc;
-                route_chunk(rs.lg + t * E4, rs.key + t * E4, E, kk, c, a.router_sigmoid, rs.ids + t * kk,
-                            rs.score + t * kk);
+                const int t = task / nc, c = task - t * nc, e = 32 * c + lane;
+                const float *key = rs.key + t * E4;
+                const int r = e < E ? rank_range(key, e, key[e], 0, E) : kk;
+                route_select(rs.lg + t * E4, E, kk, c, a.router_sigmoid, r, rs.ids + t * kk, rs.score + t * kk);
             }
         }
         cta_barrier();
