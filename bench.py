@@ -480,7 +480,8 @@ def run_bits(args, wl, bits, n_layers, T, dev, world, rank):
         "gemm1_bytes": gateup_bytes(model) if model.grouped else None,
         "y_layers": {l: model.y[l].float().cpu().numpy() for l in check_layers(n_layers)},
         "timed_reps": len(rep_ms), "rep_ms": rep_ms,
-        "routing": routing_summary([i.cpu().numpy() for i in model.ids], wl.E),
+        "routing": routing_summary([i.cpu().numpy() for i in model.ids], wl, list(model.expert_bits),
+                                   model.shared_bits),
     }
     del model, graph, g2, g3
     torch.cuda.empty_cache()
@@ -587,19 +588,30 @@ def parity_summary(y_gpu, y_ref, bar):
     return {"max_abs_err": err, "ref_max_abs": ref, "rel": rel, "bar": bar, "ok": rel <= bar}
 
 
-def routing_summary(ids_list, E):
+def routing_summary(ids_list, wl, expert_bits, shared_bits):
     """Realised routing of a step: selections per expert summed over the
-    layers, the distinct experts per layer, the busiest expert's share."""
+    layers, the distinct experts per layer, the busiest expert's share, and
+    the expert weights the step streams (every distinct selected expert of
+    every layer at its depth, plus the shared expert): the footprint that
+    must exceed L2 for back-to-back steps to read HBM without a flush."""
+    E = wl.E
     hist = np.zeros(E, dtype=np.int64)
     distinct = []
+    step_bytes = 0
     for ids in ids_list:
         v = np.asarray(ids).ravel()
         v = v[(v >= 0) & (v < E)]
         hist += np.bincount(v, minlength=E)
-        distinct.append(len(np.unique(v)))
+        u = np.unique(v)
+        distinct.append(len(u))
+        step_bytes += sum(expert_bytes(wl, wl.f, expert_bits[e], 3) for e in u.tolist())
+        if wl.shared_f:
+            step_bytes += expert_bytes(wl, wl.shared_f, shared_bits, 3)
     total = int(hist.sum())
     return {"distinct_experts_per_layer": float(np.mean(distinct)) if distinct else 0.0,
             "max_expert_share": float(hist.max()) / total if total else 0.0,
+            "weight_MB_per_step": step_bytes / 1e6,
+            "l2_MB": 129,
             "histogram": hist.tolist()}
 
 
@@ -626,15 +638,12 @@ def config_dict(wl, n_layers, T, bits, world, graph):
     bank = sum(expert_bytes(wl, wl.f, b, 3) for b in ebits)
     if wl.shared_f:
         bank += expert_bytes(wl, wl.shared_f, sbits, 3)
-    # a token selects k distinct experts in every layer: a lower bound of a
-    # step's weight traffic
-    step_min = n_layers * min(wl.k * min(expert_bytes(wl, wl.f, b, 3) for b in ebits), bank)
     return {"workload": wl.name, "layers": n_layers, "tokens_per_step": T, "bits": bits,
             "d_model": wl.d, "ffn_dim": wl.f, "experts": wl.E, "top_k": wl.k,
             "norm_topk_prob": wl.norm, "shared_ffn_dim": wl.shared_f,
             "resident_GB": round(n_layers * bank / 1e9, 3),
-            "l2": f"inputs larger than L2 (per-step weight footprint >= {step_min / 1e6:.0f} MB "
-                  "> 129 MB); no flush",
+            "l2": "no flush: inputs larger than L2 (the realised per-step weight footprint is "
+                  "routing.weight_MB_per_step, against 129 MB of L2)",
             "graph": graph, "parallelism": f"replicas x{world}"}
 
 

@@ -83,10 +83,20 @@ def test_parity_and_routing_summaries():
     assert p["max_abs_err"] == pytest.approx(0.002) and p["ref_max_abs"] == 4.0
     assert p["rel"] == pytest.approx(5e-4) and p["ok"]
     assert not bench.parity_summary(y_ref + 0.01, y_ref, 1e-3)["ok"]
-    r = bench.routing_summary([np.array([[0, 1], [1, 3]]), np.array([[1, 2], [3, 3]])], 4)
-    assert r["histogram"] == [1, 3, 1, 3]
+    wl = Y.WORKLOADS["tiny"]
+    E = wl.E
+    bits = [4] * E
+    bits[3] = 2
+    r = bench.routing_summary([np.array([[0, 1], [1, 3]]), np.array([[1, 2], [3, 3]])], wl, bits, 4)
+    assert r["histogram"] == [1, 3, 1, 3] + [0] * (E - 4)
     assert r["distinct_experts_per_layer"] == 3.0
     assert r["max_expert_share"] == 3 / 8
+    # streamed weights: experts {0, 1, 3} and {1, 2, 3}, expert 3 at Q2, plus
+    # the shared expert in each layer
+    q4 = 3 * (wl.f * wl.d // 2 + wl.f * wl.d // 32)
+    q2 = 3 * (wl.f * wl.d // 4 + wl.f * wl.d // 32)
+    sh = 3 * (wl.shared_f * wl.d // 2 + wl.shared_f * wl.d // 32) if wl.shared_f else 0
+    assert r["weight_MB_per_step"] * 1e6 == pytest.approx(4 * q4 + 2 * q2 + 2 * sh)
 
 
 def test_oracle_leg_returns_time_and_output():
