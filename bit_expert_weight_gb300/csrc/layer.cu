@@ -1121,16 +1121,23 @@ struct Stream {
     uint32_t tag;                    // this launch's tag
 };
 
-__device__ __forceinline__ bool unit_ends(const Geo &g, const UnitGeo &u, const Pos &q, int i)
+// Step i (position q) ends its unit in the CTA's range [.., a1) run from
+// ts: the unit's last chunk, or the last step before a cut.  The range
+// bounds come in registers, not from the shared geometry.
+__device__ __forceinline__ bool unit_ends(int a1, int ts, const UnitGeo &u, const Pos &q, int i)
 {
-    return q.c == u.ch - 1 || i == g.a1 - 1 || (g.ts < g.a1 && i == g.ts - 1);
+    return q.c == u.ch - 1 || i == a1 - 1 || (ts < a1 && i == ts - 1);
 }
 
-// Wait for ring stage `st.seq` (bounded); false if the CTA has failed.
+// Wait for ring stage `st.seq` (bounded); false if the CTA has failed.  The
+// stage is tested first: the failure flag (a shared-memory read) is only
+// consulted when the stage is not there yet.
 template <int NS>
 __device__ __forceinline__ bool wait_stage(const LayerArgs &a, Stream &st, int slot)
 {
     const int lane = threadIdx.x & 31;
+    if (mbar_try_wait(&st.full[slot], (st.seq / NS) & 1u))
+        return true;
     if (*st.fail)
         return false;
     if (!mbar_wait_bounded(&st.full[slot], (st.seq / NS) & 1u)) {
@@ -1144,13 +1151,14 @@ __device__ __forceinline__ bool wait_stage(const LayerArgs &a, Stream &st, int s
 }
 
 // Hand two float4 per lane to the epilogue warps through reduction slot
-// st.uc (waiting for the slot to be free).
+// st.uc (waiting for the slot to be free; after a failure it is not waited
+// for, and the arrival completes a phase nobody takes).
 __device__ __forceinline__ void put_red(const LayerArgs &a, Stream &st, float4 v0, float4 v1)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rs = st.uc % kRedSlots;
     const unsigned rph = static_cast<unsigned>(st.uc / kRedSlots);
-    if (st.uc >= kRedSlots && !*st.fail &&
+    if (st.uc >= kRedSlots && !mbar_try_wait(&st.red_empty[rs], (rph - 1u) & 1u) && !*st.fail &&
         !mbar_wait_bounded(&st.red_empty[rs], (rph - 1u) & 1u) && lane == 0) {
         set_status(a.status, kStatusTimeout);
         *st.fail = 1;
@@ -1159,7 +1167,7 @@ __device__ __forceinline__ void put_red(const LayerArgs &a, Stream &st, float4 v
     rw[lane] = v0;
     rw[32 + lane] = v1;
     __syncwarp();
-    if (lane == 0 && !*st.fail)
+    if (lane == 0)
         mbar_arrive(&st.red_full[rs]);
     ++st.uc;
 }
@@ -1255,9 +1263,6 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
         const int slot = static_cast<int>(st.seq % NS);
         const bool ok = wait_stage<NS>(a, st, slot);
         if (ok) {
-            // branch-free over the warp's two groups (tiles of absent groups
-            // read in-bounds stage bytes and are dropped), so the four mma
-            // chains of the step schedule together
             // the warp's two groups of the chunk; a group past the chunk's
             // end is skipped (the branch is uniform over the warp).  The
             // chunk's fragments are selected by value, so that the tile code
@@ -1282,7 +1287,7 @@ __device__ __forceinline__ void stream_gateup(const LayerArgs &a, const RouteVie
         if (ok && lane == 0)
             mbar_arrive(&st.empty[slot]);
         ++st.seq;
-        if (unit_ends(g, u, q, i)) {
+        if (unit_ends(a1, ts, u, q, i)) {
             // the two groups' partial sums of the same output rows
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -1454,7 +1459,7 @@ __device__ __forceinline__ void epi_gateup(const LayerArgs &a, const RouteView &
     const int e = (threadIdx.x >> 5) - kStreamWarps, lane = threadIdx.x & 31;
     const EpiOut eo = epi_out(a, st.tag);
     const Geo &g = st.geo[0];
-    const int a0 = g.a0, a1 = g.a1, nt = g.a1 - g.ts;
+    const int a0 = g.a0, a1 = g.a1, ts = g.ts, nt = g.a1 - g.ts;
     if (a0 >= a1)
         return;
     Pos q = decode(g, step_at(g, 0));
@@ -1465,7 +1470,7 @@ __device__ __forceinline__ void epi_gateup(const LayerArgs &a, const RouteView &
         if (kk == nt && kk > 0)
             q = decode(g, a0);
         u = unit_geo(g, q.p);
-        if (unit_ends(g, u, q, i)) {
+        if (unit_ends(a1, ts, u, q, i)) {
             float4 tg, tu;
             if (st.uc % kEpiWarps == e && take_red(a, st, tg, tu)) {
                 const int pb = pair_bits<BITS>(a, rv.pairs[q.p * kPairInts]);
