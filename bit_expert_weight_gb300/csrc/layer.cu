@@ -312,7 +312,7 @@ struct __align__(16) RouteSmem {
     float red[kWarps * 16 + 16];         // router row partial sums, then the CTA's logits
     int32_t pairs[kFusedPairs][kPairInts];
     int32_t route_map[kPairCols * (SMOE_MAX_TOPK_DEV + 1)];
-    float score[kPairCols * SMOE_MAX_TOPK_DEV];  // [T][k] the rank-j expert's score
+    float smax[kPairCols], ssum[kPairCols];  // softmax statistics per token
     float weights[kPairCols * SMOE_MAX_TOPK_DEV];
     float shared_w[kPairCols];
     int16_t ids[kPairCols * SMOE_MAX_TOPK_DEV];
@@ -348,34 +348,26 @@ __device__ __forceinline__ int rank_range(const float *key, int e, float ke, int
     return r;
 }
 
-// Selection step of one token, experts 32 c .. 32 c + 31, in one warp: lane
-// L holds expert e = 32 c + L and its rank r over all E experts; ranks
-// below k are the selection, stored at their rank with the expert's score:
-// the softmax over all E logits, or (sigm) the expert's own sigmoid.  The
-// softmax maximum and sum run over all E logits in a fixed order
-// (lane-strided, then a shuffle tree), the same in every task of the token;
+// Softmax statistics of one token's E logits, in one warp: the maximum m and
+// the sum z of exp(l - m), lane-strided then a shuffle tree (a fixed order).
 // exp and divide are the hardware approximations (a few ulp), well inside
 // the weights' tolerance.
-__device__ __forceinline__ void route_select(const float *lg, int E, int k, int c, int sigm, int r, int16_t *ids,
-                                          float *score)
+__device__ __forceinline__ void softmax_stats(const float *lg, int E, float *m_out, float *z_out)
 {
     const int lane = threadIdx.x & 31;
-    float m = -INFINITY, z = 1.f;
-    if (!sigm) {
-        for (int i = lane; i < E; i += 32)
-            m = fmaxf(m, lg[i]);
-        for (int o = 16; o; o >>= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        z = 0.f;
-        for (int i = lane; i < E; i += 32)
-            z += __expf(lg[i] - m);
-        for (int o = 16; o; o >>= 1)
-            z += __shfl_xor_sync(0xffffffffu, z, o);
-    }
-    const int e = 32 * c + lane;
-    if (e < E && r < k) {
-        ids[r] = static_cast<int16_t>(e);
-        score[r] = sigm ? sigmoid_fast(lg[e]) : __fdividef(__expf(lg[e] - m), z);  // z in [1, E]
+    float m = -INFINITY;
+    for (int i = lane; i < E; i += 32)
+        m = fmaxf(m, lg[i]);
+    for (int o = 16; o; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+    for (int i = lane; i < E; i += 32)
+        z += __expf(lg[i] - m);
+    for (int o = 16; o; o >>= 1)
+        z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane == 0) {
+        *m_out = m;
+        *z_out = z;  // in [1, E]
     }
 }
 
@@ -1535,6 +1527,49 @@ __device__ __forceinline__ void epi_down(const LayerArgs &a, const RouteView &rv
     }
 }
 
+// Step geometry of one phase for P_r routed pairs of P_t; false if a limit
+// the host checks is exceeded (never reached): gate/up chunks per strip (the
+// B fragments a warp holds), down groups per strip (two per warp).
+template <int KG>
+__device__ __forceinline__ bool geo_phase(const LayerArgs &a, int phase, int P_r, int P_t, Geo *out)
+{
+    Geo gg = make_geo(a, phase, P_r, P_t);
+    if (phase == 0)
+        set_order(gg);
+    *out = gg;
+    return phase == 0 ? !(gg.ch0 > KG || (P_t > P_r && gg.ch1 > KG))
+                      : !(gg.gk0 > kDownGroupsMax || (P_t > P_r && gg.gk1 > kDownGroupsMax));
+}
+
+// Leave this launch's tag as the next launch's sequence number once every
+// CTA has marked its start (CTA 0, one warp, early in the launch: the next
+// launch reads the number only after this one has completed).  The marks are
+// loaded all at once, then any not yet tagged is polled (bounded); false if
+// a poll ran out.
+__device__ __forceinline__ bool publish_seq(const LayerArgs &a, uint32_t tag)
+{
+    const int lane = threadIdx.x & 31, C = static_cast<int>(gridDim.x);
+    bool all = true;
+    for (int c0 = 0; c0 < C; c0 += 8 * 32) {
+        u64 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = c0 + 32 * i + lane;
+            v[i] = c < C ? ld_word(a.started + c) : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = c0 + 32 * i + lane;
+            if (c < C && word_tag(v[i]) != tag && !poll_word(a.started + c, tag, a.wait_cycles, v[i]))
+                all = false;
+        }
+    }
+    all = __all_sync(0xffffffffu, all);
+    if (all && lane == 0)
+        st_relaxed_u32(a.seq, tag);
+    return all;
+}
+
 // PACK: every pair holds at most 4 tokens (T <= 4), so the bf16 hi and lo
 // parts of h (and of fp32 tokens) share one mma as column pairs.
 template <int BITS, bool XBF16, int KG, bool PACK>
@@ -1545,6 +1580,9 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int s_fail;
     __shared__ uint32_t s_tag;
+    __shared__ int s_spec;  // phases whose geometry was computed during routing
+    __shared__ Geo s_geo[2];
+    __shared__ Producer s_pr;
     Stream st;
     st.ring = smem;
     st.red = reinterpret_cast<float4 *>(smem + NS * stage_bytes(ring_bits(BITS)));
@@ -1566,6 +1604,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
         fence_mbar_init();
         s_fail = 0;
+        s_spec = 0;
     }
     // Launched with programmatic stream serialization: the previous kernel on
     // the stream may still be finishing.  Only L2 prefetches of the router
@@ -1636,29 +1675,59 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             rs.shared_w[threadIdx.x] = 1.0f;
         cta_barrier();
         const bool ok = s_fail == 0;
-        // Ranking: task (t, c) ranks experts 32 c .. 32 c + 31 of token t
-        // against all E keys, then stores the selected ones with their scores
-        const int nc = (E + 31) / 32;
-        if (ok) {
-            for (int task = warp; task < T * nc; task += kWarps) {
-                const int t = task / nc, c = task - t * nc, e = 32 * c + lane;
+        if (ok && warp < kStreamWarps) {
+            // Ranking: a quad of lanes per (token, expert), each lane counting
+            // the experts ahead of it in one quarter of the keys; an expert
+            // whose rank is below k is stored at its rank.
+            const int n = T * E, ql = ((E + 15) / 16) * 4;
+            const int qi = lane & 3, lo = qi * ql, hi = min(E, lo + ql);
+            for (int base = 8 * warp; base < n; base += 8 * kStreamWarps) {
+                const int item = base + (lane >> 2);
+                const bool on = item < n;
+                const int t = on ? item / E : 0, e = on ? item - t * E : 0;
                 const float *key = rs.key + t * E4;
-                const int r = e < E ? rank_range(key, e, key[e], 0, E) : kk;
-                route_select(rs.lg + t * E4, E, kk, c, a.router_sigmoid, r, rs.ids + t * kk, rs.score + t * kk);
+                int r = on && lo < hi ? rank_range(key, e, key[e], lo, hi) : 0;
+                r += __shfl_xor_sync(0xffffffffu, r, 1);
+                r += __shfl_xor_sync(0xffffffffu, r, 2);
+                if (on && qi == 0 && r < kk)
+                    rs.ids[t * kk + r] = static_cast<int16_t>(e);
+            }
+        } else if (ok) {
+            // the other three warps: softmax statistics of the tokens; with
+            // one token, which selects k distinct experts (k routed pairs and
+            // the shared one whatever the selection), the step geometry of
+            // the two phases on two of them while the ranking runs
+            const int w3 = warp - kStreamWarps;  // 0 .. 2
+            if (T == 1) {
+                if (w3 == 0 && !a.router_sigmoid)
+                    softmax_stats(rs.lg, E, rs.smax, rs.ssum);
+                if (w3 > 0 && lane == 0) {
+                    const bool good = geo_phase<KG>(a, w3 - 1, kk, kk + (a.has_shared ? 1 : 0), &s_geo[w3 - 1]);
+                    if (good)
+                        atomicAdd(&s_spec, 1);  // 2: both phases known
+                }
+            } else if (!a.router_sigmoid) {
+                for (int t = w3; t < T; t += 3)
+                    softmax_stats(rs.lg + t * E4, E, rs.smax + t, rs.ssum + t);
             }
         }
         cta_barrier();
         if (ok && warp < T) {
-            // the weights of token t in rank order: renormalised over the
+            // the weights of token t in rank order: the softmax over all E
+            // logits or the expert's own sigmoid, renormalised over the
             // selection (summed in rank order, like the oracle) if norm,
             // times the routed scaling factor
             const int t = warp;
+            float sc = 0.f;
+            if (lane < kk) {
+                const float l = rs.lg[t * E4 + rs.ids[t * kk + lane]];
+                sc = a.router_sigmoid ? sigmoid_fast(l) : __fdividef(__expf(l - rs.smax[t]), rs.ssum[t]);
+            }
             float psel = 0.f;
             for (int j = 0; j < kk; ++j)
-                psel += rs.score[t * kk + j];
+                psel += __shfl_sync(0xffffffffu, sc, j);
             if (lane < kk) {
-                const float pj = rs.score[t * kk + lane];
-                const float wv = (a.norm ? __fdividef(pj, psel) : pj) * a.rsf;
+                const float wv = (a.norm ? __fdividef(sc, psel) : sc) * a.rsf;
                 rs.weights[t * kk + lane] = wv;
                 if (blockIdx.x == 0) {
                     const int id = rs.ids[t * kk + lane];
@@ -1672,7 +1741,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             }
         }
         // the pair table needs only the ids: built while the weights are
-        if (ok && warp == kWarps - 1)
+        if (ok && warp == kProducerWarp)
             cta_dispatch(a, rs);
         cta_barrier();
         rv.pairs = &rs.pairs[0][0];
@@ -1693,22 +1762,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     }
 
     // ------------------------------------------------------------ phases G, D
-    __shared__ Geo s_geo[2];
-    __shared__ Producer s_pr;
-    if (lane == 0 && warp < 2) {
-        Geo gg = make_geo(a, warp, P_r, P_t);
-        if (warp == 0)
-            set_order(gg);
-        s_geo[warp] = gg;
-        // limits the host checks (never reached): gate/up chunks per strip
-        // (the B fragments a warp holds), down groups per strip (two per warp)
-        if (warp == 0 ? (gg.ch0 > KG || (P_t > P_r && gg.ch1 > KG))
-                      : (gg.gk0 > kDownGroupsMax || (P_t > P_r && gg.gk1 > kDownGroupsMax))) {
+    // (the geometry computed during routing holds exactly when the routing
+    // gave k routed pairs, which one token always does)
+    if (!(s_spec == 2 && P_r == a.k)) {
+        if (lane == 0 && warp < 2 && !geo_phase<KG>(a, warp, P_r, P_t, &s_geo[warp])) {
             set_status(a.status, kStatusBadArg);
             s_fail = 1;
         }
+        cta_barrier();
     }
-    cta_barrier();
     st.geo = s_geo;
     st.pr = &s_pr;
     if (warp < kStreamWarps) {
@@ -1724,25 +1786,30 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
         __syncwarp();
     } else {
+        // the epilogue's first item is at least one unit away
+        if (blockIdx.x == 0 && warp == kStreamWarps + 1 && !publish_seq(a, tag) && lane == 0)
+            set_status(a.status, kStatusTimeout);
         epi_gateup<BITS, PACK && !XBF16>(a, rv, st);
         epi_down<BITS, PACK>(a, rv, st);
     }
     cta_barrier();
 
     // ------------------------------------------------------------ combine
-    // (T <= 8) every thread of the grid takes outputs (t, row):
-    // y = sum_j w_j o_j (+ shared) in rank order, from the tagged outputs.
+    // (T <= 8) the outputs (t, row) dealt over the CTAs (output o to CTA
+    // o mod grid, so every CTA takes its share as soon as its own roles are
+    // done): y = sum_j w_j o_j (+ shared) in rank order, from the tagged
+    // outputs, polled with short back-off (the last ones land at the end).
     if (a.fused_combine && !s_fail) {
         const int T = static_cast<int>(a.T), kk = a.k, d = a.d;
         const bool has_sh = P_t > P_r;
         const int nout = T * d;
-        for (int o = static_cast<int>(blockIdx.x) * kThreads + threadIdx.x; o < nout;
-             o += static_cast<int>(gridDim.x) * kThreads) {
+        const int C = static_cast<int>(gridDim.x);
+        for (int o = static_cast<int>(threadIdx.x) * C + static_cast<int>(blockIdx.x); o < nout; o += C * kThreads) {
             const int t = o / d, row = o - t * d;
             const int nj = kk + (has_sh ? 1 : 0);
             u64 v[SMOE_MAX_TOPK_DEV + 1];
             const long long t0 = clock64();
-            unsigned ns = 64;
+            unsigned ns = 32;
             bool good = true;
             for (;;) {
                 bool all = true;
@@ -1761,7 +1828,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                     break;
                 }
                 __nanosleep(ns);
-                if (ns < 512)
+                if (ns < 128)
                     ns *= 2;
             }
             if (!good) {
@@ -1786,21 +1853,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         const uint32_t n = s_pr.next;
         for (uint32_t j = n > static_cast<uint32_t>(NS) ? n - NS : 0u; j < n; ++j)
             (void)mbar_wait_bounded(&st.full[j % NS], (j / NS) & 1u);
-    }
-    if (blockIdx.x == 0 && warp == 0) {
-        // once every CTA has read the launch sequence number, leave this
-        // launch's tag for the next launch
-        bool all = true;
-        for (int c = lane; c < static_cast<int>(gridDim.x); c += 32) {
-            u64 v;
-            if (!poll_word(a.started + c, tag, a.wait_cycles, v))
-                all = false;
-        }
-        all = __all_sync(0xffffffffu, all);
-        if (all && lane == 0)
-            st_relaxed_u32(a.seq, tag);
-        if (!all && lane == 0)
-            set_status(a.status, kStatusTimeout);
     }
 }
 
