@@ -229,12 +229,14 @@ __device__ __forceinline__ float dot8_bf16(uint4 w, const float (&x)[8])
     return acc;
 }
 
-// The CTA's router rows for all tokens: per-thread 8-column dot products,
+// The CTA's router rows for all tokens (at most TMAX: the token loops are
+// unrolled to the instance's bound, which keeps this once-per-launch code
+// small): per-thread 8-column dot products,
 // a shuffle tree per warp, then the warps' sums in warp order; each logit is
 // stored tagged into every CTA's own copy of the logits (so that each CTA
 // polls lines no other CTA polls).  red: shared scratch of kWarps x 16
 // floats plus 16 logits.  Every thread of the CTA calls it.
-template <bool XBF16>
+template <bool XBF16, int TMAX>
 __device__ __forceinline__ void router_rows(const LayerArgs &a, const RouterPre &pre, float *red,
                                             uint32_t tag)
 {
@@ -242,9 +244,9 @@ __device__ __forceinline__ void router_rows(const LayerArgs &a, const RouterPre 
     const int T = static_cast<int>(a.T), d = a.d;
     const int nw = (d / 8 + 31) / 32;  // warps holding columns
     if (pre.nrows > 0 && warp < nw) {
-        float acc[2][kPairCols];
+        float acc[2][TMAX];
 #pragma unroll
-        for (int t = 0; t < kPairCols; ++t) {
+        for (int t = 0; t < TMAX; ++t) {
             acc[0][t] = acc[1][t] = 0.f;
             if (t < T && i < d / 8) {
                 float xf[8];
@@ -271,7 +273,7 @@ __device__ __forceinline__ void router_rows(const LayerArgs &a, const RouterPre 
 #pragma unroll
         for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int t = 0; t < kPairCols; ++t) {
+            for (int t = 0; t < TMAX; ++t) {
                 if (r < pre.nrows && t < T) {  // uniform over the warp
                     float v = acc[r][t];
                     for (int o = 16; o; o >>= 1)
@@ -1633,7 +1635,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     RouteView rv;
     int P_r = 0, P_t = 0;
     if (a.do_route) {
-        router_rows<XBF16>(a, pre, rs.red, tag);
+        router_rows<XBF16, PACK ? 4 : kPairCols>(a, pre, rs.red, tag);
         // every CTA stages all logits (polled until tagged) and the keys
         const int T = static_cast<int>(a.T), E = a.E, kk = a.k, E4 = (a.E + 3) & ~3;
         const int rows = E + (a.shared_gate ? 1 : 0);
@@ -1799,6 +1801,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     // o mod grid, so every CTA takes its share as soon as its own roles are
     // done): y = sum_j w_j o_j (+ shared) in rank order, from the tagged
     // outputs, polled with short back-off (the last ones land at the end).
+    // The slots' words are indexed by constants only (the shared expert's
+    // apart), so they stay in registers.
     if (a.fused_combine && !s_fail) {
         const int T = static_cast<int>(a.T), kk = a.k, d = a.d;
         const bool has_sh = P_t > P_r;
@@ -1806,20 +1810,23 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         const int C = static_cast<int>(gridDim.x);
         for (int o = static_cast<int>(threadIdx.x) * C + static_cast<int>(blockIdx.x); o < nout; o += C * kThreads) {
             const int t = o / d, row = o - t * d;
-            const int nj = kk + (has_sh ? 1 : 0);
-            u64 v[SMOE_MAX_TOPK_DEV + 1];
+            u64 v[SMOE_MAX_TOPK_DEV], vs = 0;
             const long long t0 = clock64();
             unsigned ns = 32;
             bool good = true;
             for (;;) {
                 bool all = true;
 #pragma unroll
-                for (int j = 0; j <= SMOE_MAX_TOPK_DEV; ++j) {
-                    if (j < nj) {
+                for (int j = 0; j < SMOE_MAX_TOPK_DEV; ++j) {
+                    if (j < kk) {
                         const int rm = rv.route_map[t * (kk + 1) + j];
                         v[j] = ld_word(a.o_t + (int64_t)rm * d + row);
                         all = all && word_tag(v[j]) == tag;
                     }
+                }
+                if (has_sh) {
+                    vs = ld_word(a.o_t + (int64_t)rv.route_map[t * (kk + 1) + kk] * d + row);
+                    all = all && word_tag(vs) == tag;
                 }
                 if (all)
                     break;
@@ -1841,7 +1848,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                 if (j < kk)
                     yv = fmaf(rv.weights[t * kk + j], __uint_as_float(word_payload(v[j])), yv);
             if (has_sh)
-                yv = fmaf(rv.shared_w[t], __uint_as_float(word_payload(v[kk])), yv);
+                yv = fmaf(rv.shared_w[t], __uint_as_float(word_payload(vs)), yv);
             a.y[(int64_t)t * d + row] = yv;
         }
     }
