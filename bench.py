@@ -28,6 +28,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -93,11 +94,19 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def kernel_code(text):
+    """CUDA source with its comments and layout removed: what the compiler
+    sees, so that a comment edit does not retire a traffic measurement."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(files=("layer.cu", "common.cuh")):
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "bit_expert_weight_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bit_expert_weight_gb300", "csrc", f)) as fh:
+            h.update(kernel_code(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,10 +22,11 @@
 //  R  (T <= 8 only) CTA c computes router rows c, c + grid, ... with all its
 //     threads (the rows' weights are loaded before the previous kernel has
 //     finished) and stores the tagged logits.  Every CTA then polls all the
-//     logits into shared memory, routes each token in one warp (k rounds of
-//     a warp arg-max in (key desc, index asc) order) and builds the pair
-//     table -- the same deterministic code on the same logits gives the same
-//     table in every CTA.  For T > 8 a separate router kernel has built the
+//     logits into shared memory, ranks every (token, expert) against the
+//     keys in (key desc, index asc) order (a quad of lanes per expert over
+//     the streaming warps), turns the ranks below k into weights and builds
+//     the pair table -- the same deterministic code on the same logits gives
+//     the same table in every CTA.  For T > 8 a separate router kernel has built the
 //     tables in global memory before the launch.
 //  G  gate/up: the tiles of all pairs (pair = one expert x <= 8 tokens) form
 //     one stream of 16-row strips, cut into chunks of <= 32 groups; the
