@@ -130,3 +130,13 @@ def test_both_arms_print_the_same_config():
     assert c == bench.config_dict(wl, 94, 1, 4, 1, True)
     assert c["resident_GB"] == round(128 * 94 * 10_027_008 / 1e9, 3)
     assert c["layers"] == 94 and c["tokens_per_step"] == 1 and c["bits"] == 4
+
+
+def test_kernel_code_ignores_comments_and_layout():
+    """The traffic table is keyed on the kernel's code: a comment or layout
+    edit keeps the key, a code edit changes it."""
+    a = "int f(int x) {\n    return x + 1; // one\n}\n/* block\n comment */\n"
+    b = "int f(int x)\n{\n  return x + 1;\n}\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.kernel_code(a) == bench.kernel_code(b)
+    assert bench.kernel_code(a) != bench.kernel_code(c)
